@@ -1,0 +1,149 @@
+"""ORACLE -- test infrastructure only.
+
+ctypes wrapper over ``oracle/oracle.cpp``, the plain fp64 definitions of the
+losses.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg
+of ``bench.py`` may import this module; the library package never does.
+
+Every function takes host numpy arrays (bf16 tensors as uint16 bit patterns)
+and returns float64 results.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "oracle.cpp")
+LIB = os.path.join(HERE, "_build", "liboracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (g++, -O2, no fast-math: IEEE fp64 semantics kept)."""
+    os.makedirs(os.path.dirname(LIB), exist_ok=True)
+    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+        tmp = LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", "-std=c++17", "-O2", "-fno-fast-math", "-ffp-contract=off",
+                               "-fPIC", "-shared", "-pthread", SRC, "-o", tmp])
+        os.replace(tmp, LIB)
+    return LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(LIB)
+            vp, i64, dbl, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_int
+            lib.oracle_ce_f64.argtypes = [vp, vp, i64, i64, vp]
+            lib.oracle_ce_f64.restype = dbl
+            lib.oracle_ce_f32.argtypes = [vp, vp, i64, i64, vp]
+            lib.oracle_ce_f32.restype = dbl
+            lib.oracle_ce_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, vp]
+            lib.oracle_ce_sbv_bf16.restype = None
+            lib.oracle_flce_bf16.argtypes = [vp, vp, vp, i64, i64, i64, vp, ci]
+            lib.oracle_flce_bf16.restype = dbl
+            lib.oracle_jsd_f64.argtypes = [vp, vp, i64, i64, dbl, vp]
+            lib.oracle_jsd_f64.restype = dbl
+            lib.oracle_fljsd_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, vp, ci]
+            lib.oracle_fljsd_bf16.restype = dbl
+            lib.oracle_logits_bf16.argtypes = [vp, vp, i64, i64, i64, vp]
+            lib.oracle_logits_bf16.restype = None
+            _lib = lib
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data
+
+
+def _threads(threads):
+    return int(threads) if threads else (os.cpu_count() or 1)
+
+
+def ce_f64(z, target):
+    """Cross-entropy rows of fp64 logits [T, V]. Returns (mean, per-row losses)."""
+    z, pz = _c(z, np.float64)
+    T, V = z.shape
+    t, pt = _c(target, np.int64)
+    out = np.empty(T, np.float64)
+    m = _load().oracle_ce_f64(pz, pt, T, V, out.ctypes.data)
+    return m, out
+
+
+def ce_f32(z, target):
+    """Flat fp32 logits [T, V]. Returns (mean, per-row losses)."""
+    z, pz = _c(z, np.float32)
+    T, V = z.shape
+    t, pt = _c(target, np.int64)
+    out = np.empty(T, np.float64)
+    m = _load().oracle_ce_f32(pz, pt, T, V, out.ctypes.data)
+    return m, out
+
+
+def ce_sbv_bf16(z_bits, target):
+    """Megatron layout bf16 logits [S, B, V] (uint16 bits). Returns losses [S, B]."""
+    z, pz = _c(z_bits, np.uint16)
+    S, B, V = z.shape
+    t, pt = _c(target, np.int64)
+    out = np.empty((S, B), np.float64)
+    _load().oracle_ce_sbv_bf16(pz, pt, S, B, V, out.ctypes.data)
+    return out
+
+
+def flce_bf16(x_bits, W_bits, target, threads=None):
+    """Fused linear + CE. x [T, H], W [V, H] bf16 bits. Returns (mean, per-token)."""
+    x, px = _c(x_bits, np.uint16)
+    W, pw = _c(W_bits, np.uint16)
+    T, H = x.shape
+    V = W.shape[0]
+    assert W.shape[1] == H
+    t, pt = _c(target, np.int64)
+    out = np.empty(T, np.float64)
+    m = _load().oracle_flce_bf16(px, pw, pt, T, H, V, out.ctypes.data, _threads(threads))
+    return m, out
+
+
+def jsd_f64(zs, zt, beta=0.5):
+    """Generalized JSD between softmax(zs) and softmax(zt), rows of [T, V]."""
+    zs, ps = _c(zs, np.float64)
+    zt, pt = _c(zt, np.float64)
+    assert zs.shape == zt.shape
+    T, V = zs.shape
+    out = np.empty(T, np.float64)
+    m = _load().oracle_jsd_f64(ps, pt, T, V, float(beta), out.ctypes.data)
+    return m, out
+
+
+def fljsd_bf16(xs_bits, Ws_bits, xt_bits, Wt_bits, beta=0.5, threads=None):
+    """Fused linear + generalized JSD (batchmean). Returns (mean, per-token)."""
+    xs, p1 = _c(xs_bits, np.uint16)
+    Ws, p2 = _c(Ws_bits, np.uint16)
+    xt, p3 = _c(xt_bits, np.uint16)
+    Wt, p4 = _c(Wt_bits, np.uint16)
+    T, H = xs.shape
+    V = Ws.shape[0]
+    assert xt.shape == (T, H) and Ws.shape == (V, H) and Wt.shape == (V, H)
+    out = np.empty(T, np.float64)
+    m = _load().oracle_fljsd_bf16(p1, p2, p3, p4, T, H, V, float(beta), out.ctypes.data,
+                                  _threads(threads))
+    return m, out
+
+
+def logits_bf16(x_bits, W_bits):
+    """z = x W^T in fp64 from bf16 bits, x [T, H], W [V, H] -> [T, V]."""
+    x, px = _c(x_bits, np.uint16)
+    W, pw = _c(W_bits, np.uint16)
+    T, H = x.shape
+    V = W.shape[0]
+    z = np.empty((T, V), np.float64)
+    _load().oracle_logits_bf16(px, pw, T, H, V, z.ctypes.data)
+    return z

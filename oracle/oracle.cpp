@@ -1,0 +1,206 @@
+// ORACLE -- test infrastructure only.
+//
+// Plain, slow, obviously-correct fp64 definitions of the losses computed by the
+// GPU library.  Only the tests, the package smoke check and the bench's CPU
+// baseline leg may load this file's library; the product path never does.  It
+// shares no code, header, table or helper with the CUDA sources.
+//
+// Sources (KernelIndex operation pages; the pages name the losses and give
+// their tensor contracts but print no formula, so each definition below is the
+// textbook one the names denote):
+//   * "Cross-entropy loss", section Semantics: logits float [tokens, vocab],
+//     target int64 [tokens], loss float [1]  -> ce_mean_*.
+//   * "Vocab-parallel cross-entropy, Megatron layout", summary and Semantics:
+//     bf16 logits [seq, batch, vocab], target int64 [seq, batch], per-token fp32
+//     loss [seq, batch]; TP = 1 only                    -> ce_sbv_bf16.
+//   * "Fused linear + CPO loss", summary ("computed chunked without
+//     materializing logits") and Semantics: x [batch, seq, hidden], weight
+//     [vocab, hidden], target int64 [batch, seq], loss float [1].  Only the
+//     cross-entropy (NLL) core of that loss is defined here -> flce_bf16.
+//   * "Fused linear + JSD", summary ("generalized JSD (beta 0.5, batchmean)")
+//     and Semantics: student/teacher input [tokens, hidden], student/teacher
+//     weight [vocab, hidden], loss float [1]             -> fljsd_bf16.
+//
+// Definitions (natural log, fp64 throughout, inputs widened exactly):
+//   CE row:  loss_i = M_i + ln( sum_v exp(z_iv - M_i) ) - z_{i,t_i},
+//            M_i = max_v z_iv, computed as two plain passes over the row.
+//            A target outside [0, V) makes that row's loss NaN.
+//   mean:    (1/T) sum_i loss_i, summed in row order.
+//   fused:   z_iv = sum_k x_ik W_vk (sum in k order), then the CE row.
+//   JSD:     P_i = softmax(xs_i Ws^T), Q_i = softmax(xt_i Wt^T),
+//            M = beta P + (1-beta) Q,
+//            jsd_i = sum_v [ beta P ln(P/M) + (1-beta) Q ln(Q/M) ]
+//            (a term whose weight P or Q is 0 contributes 0), and the loss is
+//            (1/T) sum_i jsd_i ("batchmean").  P is the student.
+//
+// The thread-count argument of the fused functions only partitions tokens
+// across std::threads; each token's arithmetic is the single-threaded code.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+const double kNaN = std::numeric_limits<double>::quiet_NaN();
+
+double bf16_to_double(uint16_t b) {
+  uint32_t u = static_cast<uint32_t>(b) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return static_cast<double>(f);
+}
+
+// Cross-entropy of one row of V logits against target t (two passes).
+double ce_row(const double* z, int64_t V, int64_t t) {
+  if (t < 0 || t >= V) return kNaN;
+  double M = z[0];
+  for (int64_t v = 1; v < V; ++v)
+    if (z[v] > M || std::isnan(z[v])) M = z[v];
+  double sum = 0.0;
+  for (int64_t v = 0; v < V; ++v) sum += std::exp(z[v] - M);
+  return M + std::log(sum) - z[t];
+}
+
+// Log-softmax of one row into lp (lp_v = z_v - logsumexp(z)).
+void log_softmax_row(const double* z, int64_t V, double* lp) {
+  double M = z[0];
+  for (int64_t v = 1; v < V; ++v)
+    if (z[v] > M || std::isnan(z[v])) M = z[v];
+  double sum = 0.0;
+  for (int64_t v = 0; v < V; ++v) sum += std::exp(z[v] - M);
+  double lse = M + std::log(sum);
+  for (int64_t v = 0; v < V; ++v) lp[v] = z[v] - lse;
+}
+
+// Generalized JSD of one token from the two log-probability rows.
+double jsd_row(const double* lp, const double* lq, int64_t V, double beta) {
+  double acc = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    double P = std::exp(lp[v]);
+    double Q = std::exp(lq[v]);
+    double M = beta * P + (1.0 - beta) * Q;
+    double lm = std::log(M);
+    double term = 0.0;
+    if (P > 0.0) term += beta * P * (lp[v] - lm);
+    if (Q > 0.0) term += (1.0 - beta) * Q * (lq[v] - lm);
+    acc += term;
+  }
+  return acc;
+}
+
+// z_v = sum_k x_k W_vk for one token (bf16 inputs, exact products in fp64).
+void logits_row_bf16(const uint16_t* x, const uint16_t* W, int64_t H, int64_t V, double* z) {
+  std::vector<double> xd(H);
+  for (int64_t k = 0; k < H; ++k) xd[k] = bf16_to_double(x[k]);
+  for (int64_t v = 0; v < V; ++v) {
+    const uint16_t* w = W + v * H;
+    double acc = 0.0;
+    for (int64_t k = 0; k < H; ++k) acc += xd[k] * bf16_to_double(w[k]);
+    z[v] = acc;
+  }
+}
+
+template <class F>
+void over_tokens(int64_t T, int threads, F per_token) {
+  if (threads <= 1 || T <= 1) {
+    for (int64_t i = 0; i < T; ++i) per_token(i);
+    return;
+  }
+  std::vector<std::thread> pool;
+  int64_t n = threads < T ? threads : T;
+  for (int64_t w = 0; w < n; ++w)
+    pool.emplace_back([=] {
+      for (int64_t i = w; i < T; i += n) per_token(i);
+    });
+  for (auto& th : pool) th.join();
+}
+
+double mean_of(const double* a, int64_t T) {
+  double s = 0.0;
+  for (int64_t i = 0; i < T; ++i) s += a[i];
+  return s / static_cast<double>(T);
+}
+
+}  // namespace
+
+extern "C" {
+
+// Per-row CE over fp64 logits [T, V]; returns the mean, writes per-row losses.
+double oracle_ce_f64(const double* z, const int64_t* target, int64_t T, int64_t V,
+                     double* loss_rows) {
+  for (int64_t i = 0; i < T; ++i) loss_rows[i] = ce_row(z + i * V, V, target[i]);
+  return mean_of(loss_rows, T);
+}
+
+// Flat layout: fp32 logits [T, V] -> per-row losses and their mean.
+double oracle_ce_f32(const float* z32, const int64_t* target, int64_t T, int64_t V,
+                     double* loss_rows) {
+  std::vector<double> row(V);
+  for (int64_t i = 0; i < T; ++i) {
+    for (int64_t v = 0; v < V; ++v) row[v] = static_cast<double>(z32[i * V + v]);
+    loss_rows[i] = ce_row(row.data(), V, target[i]);
+  }
+  return mean_of(loss_rows, T);
+}
+
+// Megatron layout: bf16 logits [S, B, V] -> per-token losses [S, B] (row s*B+b).
+void oracle_ce_sbv_bf16(const uint16_t* z16, const int64_t* target, int64_t S, int64_t B,
+                        int64_t V, double* loss_sb) {
+  std::vector<double> row(V);
+  for (int64_t s = 0; s < S; ++s)
+    for (int64_t b = 0; b < B; ++b) {
+      int64_t r = s * B + b;
+      for (int64_t v = 0; v < V; ++v) row[v] = bf16_to_double(z16[r * V + v]);
+      loss_sb[r] = ce_row(row.data(), V, target[r]);
+    }
+}
+
+// Fused linear + CE: x [T, H], W [V, H] (bf16) -> per-token losses and their mean.
+double oracle_flce_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t T,
+                        int64_t H, int64_t V, double* loss_rows, int threads) {
+  over_tokens(T, threads, [&](int64_t i) {
+    std::vector<double> z(V);
+    logits_row_bf16(x + i * H, W, H, V, z.data());
+    loss_rows[i] = ce_row(z.data(), V, target[i]);
+  });
+  return mean_of(loss_rows, T);
+}
+
+// Generalized JSD over fp64 student/teacher logits [T, V]; returns batchmean.
+double oracle_jsd_f64(const double* zs, const double* zt, int64_t T, int64_t V, double beta,
+                      double* jsd_rows) {
+  std::vector<double> lp(V), lq(V);
+  for (int64_t i = 0; i < T; ++i) {
+    log_softmax_row(zs + i * V, V, lp.data());
+    log_softmax_row(zt + i * V, V, lq.data());
+    jsd_rows[i] = jsd_row(lp.data(), lq.data(), V, beta);
+  }
+  return mean_of(jsd_rows, T);
+}
+
+// Fused linear + generalized JSD (bf16 inputs) -> per-token JSD and batchmean.
+double oracle_fljsd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt,
+                         const uint16_t* Wt, int64_t T, int64_t H, int64_t V, double beta,
+                         double* jsd_rows, int threads) {
+  over_tokens(T, threads, [&](int64_t i) {
+    std::vector<double> zs(V), zt(V), lp(V), lq(V);
+    logits_row_bf16(xs + i * H, Ws, H, V, zs.data());
+    logits_row_bf16(xt + i * H, Wt, H, V, zt.data());
+    log_softmax_row(zs.data(), V, lp.data());
+    log_softmax_row(zt.data(), V, lq.data());
+    jsd_rows[i] = jsd_row(lp.data(), lq.data(), V, beta);
+  });
+  return mean_of(jsd_rows, T);
+}
+
+// Logits of the fused paths for a set of tokens (used by tests to pin the
+// fused functions against ce on explicit logits): z [T, V].
+void oracle_logits_bf16(const uint16_t* x, const uint16_t* W, int64_t T, int64_t H, int64_t V,
+                        double* z) {
+  for (int64_t i = 0; i < T; ++i) logits_row_bf16(x + i * H, W, H, V, z + i * V);
+}
+
+}  // extern "C"
