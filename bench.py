@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""Benchmark of the LM-head loss path on GB300.
+
+One step = one call of each entry point on its largest workload:
+  ce_fwd_f32       logits fp32 [16384, 131072] ~ N(0,1)           (8.6 GB)
+  ce_fwd_sbv_bf16  logits bf16 [2048, 4, 131072] ~ N(0, 2^2)       (2.1 GB)
+  flce_fwd_bf16    x bf16 [16*1024, 4096], W bf16 [128256, 4096]  (17.2 TFLOP)
+  fljsd_fwd_bf16   xs, xt bf16 [8192, 4096], Ws, Wt [128256, 4096] (34.4 TFLOP)
+Every input is larger than L2, and consecutive calls read different buffers,
+so no L2 flush is needed between timed steps.  Inputs come from the seeded
+generator (gen/), made on the host into pinned memory and copied to the GPU
+once; `value` times device-resident inputs, `e2e` re-copies every input from
+pinned host memory and reads the results back inside each timed step.
+
+Prints ONE JSON line.  `--impl reference` times the fp64 CPU oracle on
+bounded samples of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from lm_head_online_gb300 import roofline as rl  # noqa: E402
+
+METRIC = "CE µs & HBM GB/s vs roofline; fused-linear µs & TFLOP/s vs bf16 peak (1 GB300)"
+UNIT = "us/step"
+
+CE = dict(T=16384, V=131072)
+SBV = dict(S=2048, B=4, V=131072)
+FLCE = dict(T=16 * 1024, H=4096, V=128256)
+FLJSD = dict(T=8192, H=4096, V=128256)
+WORKLOAD = ("ce_fwd_f32 fp32[16384,131072] + ce_fwd_sbv_bf16 bf16[2048,4,131072] + "
+            "flce_fwd_bf16 x[16384,4096] W[128256,4096] + fljsd_fwd_bf16 T=8192 H=4096 V=128256 beta=0.5")
+KERNELS_PER_STEP = 1 + 1 + 2 + 4
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- peaks
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        p = json.load(open(path))
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p["bf16_tflops_sustained"]), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            c = [x.strip() for x in ln.split(",")]
+            if len(c) < 8:
+                continue
+            try:
+                sm.append(float(c[0]))
+                mx = max(mx, float(c[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, c[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- inputs
+def make_inputs(seed, torch, pinned=True):
+    import gen
+    thr = os.cpu_count() or 1
+
+    def host(shape, dtype):
+        t = torch.empty(shape, dtype=dtype)
+        return t.pin_memory() if pinned else t
+
+    h = {}
+    h["ce_z"] = host((CE["T"], CE["V"]), torch.float32)
+    gen.normal_f32(seed, gen.STREAM_LOGITS, h["ce_z"].shape, 1.0, out=h["ce_z"], threads=thr)
+    h["ce_t"] = host((CE["T"],), torch.int64)
+    gen.targets(seed, gen.STREAM_TARGET, h["ce_t"].shape, CE["V"], out=h["ce_t"], threads=thr)
+    h["sbv_z"] = host((SBV["S"], SBV["B"], SBV["V"]), torch.bfloat16)
+    gen.normal_bf16_bits(seed, gen.STREAM_LOGITS, h["sbv_z"].shape, 2.0, out=h["sbv_z"].view(torch.int16), threads=thr)
+    h["sbv_t"] = host((SBV["S"], SBV["B"]), torch.int64)
+    gen.targets(seed, gen.STREAM_TARGET, h["sbv_t"].shape, SBV["V"], out=h["sbv_t"], threads=thr)
+    h["fl_x"] = host((FLCE["T"], FLCE["H"]), torch.bfloat16)
+    gen.normal_bf16_bits(seed, gen.STREAM_X, h["fl_x"].shape, 1.0, out=h["fl_x"].view(torch.int16), threads=thr)
+    h["fl_w"] = host((FLCE["V"], FLCE["H"]), torch.bfloat16)
+    gen.normal_bf16_bits(seed, gen.STREAM_W, h["fl_w"].shape, 0.02, out=h["fl_w"].view(torch.int16), threads=thr)
+    h["fl_t"] = host((FLCE["T"],), torch.int64)
+    gen.targets(seed, gen.STREAM_TARGET, h["fl_t"].shape, FLCE["V"], out=h["fl_t"], threads=thr)
+    for k, stream, shape, sig in (("js_xs", gen.STREAM_X, (FLJSD["T"], FLJSD["H"]), 1.0),
+                                  ("js_ws", gen.STREAM_W, (FLJSD["V"], FLJSD["H"]), 0.02),
+                                  ("js_xt", gen.STREAM_XT, (FLJSD["T"], FLJSD["H"]), 1.0),
+                                  ("js_wt", gen.STREAM_WT, (FLJSD["V"], FLJSD["H"]), 0.02)):
+        h[k] = host(shape, torch.bfloat16)
+        gen.normal_bf16_bits(seed, stream, shape, sig, out=h[k].view(torch.int16), threads=thr)
+    return h
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import lm_head_online_gb300 as lmho
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lmho.load()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    t_gen = time.time()
+    h = make_inputs(args.seed + rank, torch)
+    t_gen = time.time() - t_gen
+    d = {k: v.to(dev, non_blocking=True) for k, v in h.items()}
+    torch.cuda.synchronize()
+
+    ws_ce = lmho.workspace(lmho.ce_workspace_bytes(CE["T"], CE["V"]), dev)
+    ws_fl = lmho.workspace(lmho.flce_workspace_bytes(FLCE["T"], FLCE["H"], FLCE["V"]), dev)
+    ws_js = lmho.workspace(lmho.fljsd_workspace_bytes(FLJSD["T"], FLJSD["H"], FLJSD["V"]), dev)
+    out = {"ce": torch.empty(1, device=dev), "sbv": torch.empty((SBV["S"], SBV["B"]), device=dev),
+           "fl": torch.empty(1, device=dev), "js": torch.empty(1, device=dev)}
+    stream = torch.cuda.current_stream()
+
+    # per-kernel events: ce 2, sbv 2, flce 3, fljsd 5
+    K = args.steps
+    ev = {op: [[torch.cuda.Event(enable_timing=True) for _ in range(n)] for _ in range(K)]
+          for op, n in (("ce", 2), ("sbv", 2), ("fl", 3), ("js", 5))}
+
+    for per_step in ev.values():       # create every event before the timed region
+        for evs in per_step:
+            for e in evs:
+                e.record(stream)
+    torch.cuda.synchronize()
+
+    def step(i=None):
+        def call(op, fn):
+            if i is not None:
+                lmho.set_launch_events(ev[op][i])
+            fn()
+            if i is not None:
+                lmho.set_launch_events(None)
+        call("ce", lambda: lmho.ce_fwd_f32(d["ce_z"], d["ce_t"], loss=out["ce"], ws=ws_ce))
+        call("sbv", lambda: lmho.ce_fwd_sbv_bf16(d["sbv_z"], d["sbv_t"], loss=out["sbv"]))
+        call("fl", lambda: lmho.flce_fwd_bf16(d["fl_x"], d["fl_w"], d["fl_t"], loss=out["fl"], ws=ws_fl))
+        call("js", lambda: lmho.fljsd_fwd_bf16(d["js_xs"], d["js_ws"], d["js_xt"], d["js_wt"], 0.5,
+                                               loss=out["js"], ws=ws_js))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for w in (ws_fl, ws_js):
+        st = lmho.ws_status(w)
+        if st:
+            raise RuntimeError(f"device status {st}: {lmho.strerror(st)}")
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if not dist:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # -------- device-resident timing
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        e0.record(stream)
+        for i in range(K):
+            step(i)
+        e1.record(stream)
+        barrier()
+    ms_total = e0.elapsed_time(e1)
+    ms_step = max_over_ranks(ms_total / K)
+    clock_dev = clocks.summary()
+
+    def kern_ms(op, j):
+        return float(np.mean([ev[op][i][j].elapsed_time(ev[op][i][j + 1]) for i in range(K)]))
+
+    kern = {
+        "ce_fwd_f32.row_kernel": ("ce", 0), "ce_fwd_sbv_bf16.row_kernel": ("sbv", 0),
+        "flce.tcgen05_gemm_ce": ("fl", 0), "flce.finalize": ("fl", 1),
+        "fljsd.tcgen05_gemm_lse": ("js", 0), "fljsd.lse_finalize": ("js", 1),
+        "fljsd.tcgen05_gemm_jsd": ("js", 2), "fljsd.jsd_finalize": ("js", 3),
+    }
+    kms = {k: kern_ms(*v) for k, v in kern.items()}
+    call_ms = {op: float(np.mean([ev[op][i][0].elapsed_time(ev[op][i][-1]) for i in range(K)]))
+               for op in ev}
+
+    pk = peaks()
+    ce_b = rl.ce_flat_bytes(CE["T"], CE["V"])
+    sbv_b = rl.ce_sbv_bytes(SBV["S"], SBV["B"], SBV["V"])
+    fl_f = rl.flce_flops(FLCE["T"], FLCE["H"], FLCE["V"])
+    js_pf = rl.fljsd_pass_flops(FLJSD["T"], FLJSD["H"], FLJSD["V"])
+    tf_peak = pk["bf16_sus"]
+
+    def hbm_roof(nbytes, ms, traffic=None):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                "frac": round(gbs / pk["hbm"], 4), "traffic": traffic}
+
+    def tc_roof(flops, ms, traffic=None):
+        tfs = flops / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(tfs, 1), "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": round(tfs / tf_peak, 4), "traffic": traffic}
+
+    roofs = {
+        "ce_fwd_f32.row_kernel": hbm_roof(ce_b, kms["ce_fwd_f32.row_kernel"]),
+        "ce_fwd_sbv_bf16.row_kernel": hbm_roof(sbv_b, kms["ce_fwd_sbv_bf16.row_kernel"]),
+        "flce.tcgen05_gemm_ce": tc_roof(fl_f, kms["flce.tcgen05_gemm_ce"]),
+        "fljsd.tcgen05_gemm_lse": tc_roof(js_pf, kms["fljsd.tcgen05_gemm_lse"]),
+        "fljsd.tcgen05_gemm_jsd": tc_roof(js_pf, kms["fljsd.tcgen05_gemm_jsd"]),
+    }
+    dominant = max(roofs, key=lambda k: kms[k])
+    ops = {
+        "ce_fwd_f32": {"us": round(call_ms["ce"] * 1e3, 2), "GB/s": round(ce_b / call_ms["ce"] / 1e6, 1),
+                       "bytes": ce_b, "loss": float(out["ce"].item())},
+        "ce_fwd_sbv_bf16": {"us": round(call_ms["sbv"] * 1e3, 2), "GB/s": round(sbv_b / call_ms["sbv"] / 1e6, 1),
+                            "bytes": sbv_b, "loss_mean": float(out["sbv"].double().mean().item())},
+        "flce_fwd_bf16": {"us": round(call_ms["fl"] * 1e3, 2), "TFLOP/s": round(fl_f / call_ms["fl"] / 1e9, 1),
+                          "flops": fl_f, "loss": float(out["fl"].item())},
+        "fljsd_fwd_bf16": {"us": round(call_ms["js"] * 1e3, 2),
+                           "TFLOP/s": round(2 * js_pf / call_ms["js"] / 1e9, 1), "flops": 2 * js_pf,
+                           "loss": float(out["js"].item())},
+    }
+
+    # -------- end to end through host buffers
+    e2e = None
+    clock_e2e = None
+    if not args.no_e2e:
+        host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+        h2d = sum(v.numel() * v.element_size() for v in h.values())
+        d2h = sum(v.numel() * v.element_size() for v in out.values())
+
+        def e2e_step():
+            for k, v in h.items():
+                d[k].copy_(v, non_blocking=True)
+            step()
+            for k, v in out.items():
+                host_out[k].copy_(v, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        Ke = max(3, min(K, 10))
+        with ClockSampler(local_rank) as ck:
+            barrier()
+            e0.record(stream)
+            for _ in range(Ke):
+                e2e_step()
+            e1.record(stream)
+            barrier()
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / Ke)
+        clock_e2e = ck.summary()
+        e2e = {"value": round(ms_e2e * 1e3, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": Ke}
+
+    result = {
+        "metric": METRIC, "value": round(ms_step * 1e3, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 tensor-core operands)",
+        "data": "synthetic (seeded Philox generator, host-made, pinned)",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "peaks": pk["src"]},
+        "ops": ops,
+        "kernels_ms": {k: round(v, 4) for k, v in kms.items()},
+        "roofline": dict(roofs[dominant], kernel=dominant),
+        "rooflines": roofs,
+        "e2e": e2e,
+        "gpu_launches": KERNELS_PER_STEP * K,
+        "clocks": clock_dev,
+        "clocks_e2e": clock_e2e,
+        "input_gen_s": round(t_gen, 1),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(h=h, budget_s=12.0, seed=args.seed)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+def oracle_samples(seed=0, h=None, budget_s=12.0):
+    """Bounded samples of every op's inputs (taken from the bench's own host
+    tensors when given, else regenerated by counter offset)."""
+    import gen
+    cores = os.cpu_count() or 1
+    f = budget_s / 12.0
+    n_ce = max(cores, int(1024 * f)) // cores * cores
+    n_sbv = max(cores, int(2048 * f)) // cores * cores
+    n_fl = max(1, int(cores * f))
+    n_js = max(1, int(cores * f / 2))
+
+    def np_bits(t):
+        import torch
+        return t.view(torch.int16).numpy().view(np.uint16)
+
+    s = {"n": dict(ce=n_ce, sbv=n_sbv, fl=n_fl, js=n_js), "cores": cores}
+    if h is not None:
+        s["ce"] = (h["ce_z"][:n_ce].numpy(), h["ce_t"][:n_ce].numpy())
+        s["sbv"] = (np_bits(h["sbv_z"]).reshape(-1, 1, SBV["V"])[:n_sbv], h["sbv_t"].numpy().reshape(-1, 1)[:n_sbv])
+        s["fl"] = (np_bits(h["fl_x"])[:n_fl], np_bits(h["fl_w"]), h["fl_t"][:n_fl].numpy())
+        s["js"] = (np_bits(h["js_xs"])[:n_js], np_bits(h["js_ws"]), np_bits(h["js_xt"])[:n_js], np_bits(h["js_wt"]))
+        return s
+    H, V = FLCE["H"], FLCE["V"]
+    s["ce"] = (gen.normal_f32(seed, gen.STREAM_LOGITS, (n_ce, CE["V"])),
+               gen.targets(seed, gen.STREAM_TARGET, (n_ce,), CE["V"]))
+    s["sbv"] = (gen.normal_bf16_bits(seed, gen.STREAM_LOGITS, (n_sbv, 1, SBV["V"]), 2.0),
+                gen.targets(seed, gen.STREAM_TARGET, (n_sbv, 1), SBV["V"]))
+    W = gen.normal_bf16_bits(seed, gen.STREAM_W, (V, H), 0.02)
+    s["fl"] = (gen.normal_bf16_bits(seed, gen.STREAM_X, (n_fl, H)), W,
+               gen.targets(seed, gen.STREAM_TARGET, (n_fl,), V))
+    s["js"] = (gen.normal_bf16_bits(seed, gen.STREAM_X, (n_js, H)), W,
+               gen.normal_bf16_bits(seed, gen.STREAM_XT, (n_js, H)),
+               gen.normal_bf16_bits(seed, gen.STREAM_WT, (V, H), 0.02))
+    return s
+
+
+def time_oracle(s):
+    """The oracle as it stands on the samples; CE rows are split over host
+    threads (each oracle call releases the GIL), fused tokens use the
+    oracle's own token partition.  Returns the extrapolated us per full step."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    cores, n = s["cores"], s["n"]
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    def rows_parallel(fn, z, t):
+        parts = np.array_split(np.arange(len(z)), cores)
+        with ThreadPoolExecutor(cores) as ex:
+            list(ex.map(lambda idx: fn(z[idx[0]:idx[-1] + 1], t[idx[0]:idx[-1] + 1]) if len(idx) else None, parts))
+
+    t_ce = timed(lambda: rows_parallel(oracle.ce_f32, *s["ce"]))
+    t_sbv = timed(lambda: rows_parallel(oracle.ce_sbv_bf16, *s["sbv"]))
+    t_fl = timed(lambda: oracle.flce_bf16(*s["fl"], threads=cores))
+    t_js = timed(lambda: oracle.fljsd_bf16(*s["js"], 0.5, threads=cores))
+    us = 1e6 * (t_ce * CE["T"] / n["ce"] + t_sbv * SBV["S"] * SBV["B"] / n["sbv"] +
+                t_fl * FLCE["T"] / n["fl"] + t_js * FLJSD["T"] / n["js"])
+    return {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"ce {n['ce']}/{CE['T']} rows, sbv {n['sbv']}/{SBV['S'] * SBV['B']} tokens, "
+                       f"flce {n['fl']}/{FLCE['T']} tokens, fljsd {n['js']}/{FLJSD['T']} tokens of the same "
+                       f"workload; scaled linearly to one full step"),
+            "seconds": {"ce": round(t_ce, 2), "sbv": round(t_sbv, 2), "flce": round(t_fl, 2),
+                        "fljsd": round(t_js, 2)}}
+
+
+def cpu_baseline(h=None, budget_s=12.0, seed=0):
+    return time_oracle(oracle_samples(seed, h, budget_s))
+
+
+def run_reference(args):
+    import oracle
+    oracle.build()
+    s = oracle_samples(args.seed, None, budget_s=3.0)
+    vals, r = [], None
+    for i in range(args.warmup + args.steps):
+        r = time_oracle(s)
+        if i >= args.warmup:
+            vals.append(r["value"])
+    v = float(np.median(vals))
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Philox generator)",
+            "config": {"workload": WORKLOAD, "l2": "n/a (host)", "parallelism": "host threads"},
+            "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                             "sample": r["sample"]},
+            "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * lmho.h -- C ABI of the GB300 (sm_103a) LM-head loss library.
+ *
+ * The operations are the four contracts of the KernelIndex operation pages
+ * "Cross-entropy loss", "Vocab-parallel cross-entropy, Megatron layout",
+ * "Fused linear + CPO loss" (its cross-entropy core) and "Fused linear + JSD".
+ * The pages give tensor names, dtypes and shapes (section "Semantics") and
+ * name the losses; the arithmetic is the textbook definition of each name:
+ *
+ *   cross-entropy of row i:  loss_i = ln(sum_v exp(z_iv)) - z_{i, t_i}
+ *   generalized JSD:         JSD_b(P||Q) = b KL(P||M) + (1-b) KL(Q||M),
+ *                            M = b P + (1-b) Q, natural log.
+ *
+ * Conventions shared by every entry point
+ *   - Tensor pointers are DEVICE pointers, owned by the caller, contiguous and
+ *     row-major.  bf16 tensors are passed as their 16-bit patterns
+ *     (const uint16_t*), so this header needs no CUDA include.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls only enqueue work on it: they never synchronise, never allocate and
+ *     keep no state between calls.  They are thread-safe.
+ *   - "No mutation or aliasing" (every page, section Semantics): inputs are
+ *     never written, and an output or workspace byte range that overlaps an
+ *     input (or each other) is rejected with LMHO_ERR_ALIAS.
+ *   - Host-checkable errors (NULL pointer, a size <= 0, aliasing, a short
+ *     workspace, a device that is not compute capability 10.3, an unsupported
+ *     hidden size) return a status and launch nothing.  Targets live on the
+ *     device and are not checked on the host: a target outside [0, V) makes
+ *     that token's loss NaN, and a mean over it NaN.
+ *   - NaN logits propagate (the token's loss is NaN); a +inf logit gives NaN.
+ *   - Results are bitwise reproducible run to run (fixed-order reductions).
+ *   - Workspaces are caller-owned device memory, 256-byte aligned, and must be
+ *     ZERO-FILLED before their first use; every call leaves the words that
+ *     must start at zero back at zero.  One workspace serves one call at a
+ *     time: calls in flight at once need distinct workspaces.
+ */
+#ifndef LMHO_H_
+#define LMHO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LMHO_OK = 0,
+  LMHO_ERR_INVALID_ARG = 1,  /* NULL pointer, size <= 0, bad option            */
+  LMHO_ERR_ALIAS = 2,        /* an output/workspace range overlaps another    */
+  LMHO_ERR_WORKSPACE = 3,    /* ws_bytes below the *_workspace_bytes() value  */
+  LMHO_ERR_UNSUPPORTED = 4,  /* not an sm_103 device, or H % 8 != 0           */
+  LMHO_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, attribute)*/
+  LMHO_ERR_TIMEOUT = 6       /* a bounded in-kernel wait gave up (device side)*/
+} lmho_status;
+
+/* Human-readable text of a status code (static storage, never NULL). */
+const char* lmho_strerror(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int lmho_version(void);
+
+/* ------------------------------------------------------------------------
+ * Flat cross-entropy, fp32 logits, mean-reduced.
+ * Page "Cross-entropy loss", section Semantics: logits float [tokens, vocab],
+ * target int64 [tokens], loss float [1].
+ *
+ *   logits  [T, V] fp32 device, row i at logits + i*V (any 4-byte alignment;
+ *           rows whose start is not 16-byte aligned are peeled in-kernel)
+ *   target  [T] int64 device
+ *   loss    [1] fp32 device output: (1/T) sum_i loss_i
+ *   ws      device workspace of ws_bytes >= ce_workspace_bytes(T, V), zeroed
+ *           before first use.  After the call completes, the first T floats
+ *           of ws hold the per-token losses loss_i.
+ * One kernel launch.
+ * ------------------------------------------------------------------------ */
+size_t ce_workspace_bytes(int64_t T, int64_t V);
+int ce_fwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
+               float* loss, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Megatron-layout cross-entropy, bf16 logits, per-token fp32 losses.
+ * Page "Vocab-parallel cross-entropy, Megatron layout", summary (bf16 logits,
+ * per-token fp32 losses, tensor parallel size 1) and section Semantics:
+ * logits [seq, batch, vocab], target int64 [seq, batch], loss fp32 [seq, batch].
+ *
+ *   logits  [S, B, V] bf16 device (row s*B+b at logits + (s*B+b)*V)
+ *   target  [S, B] int64 device
+ *   loss    [S, B] fp32 device output, loss[s*B+b] = loss of that token;
+ *           accumulation is fp32.
+ * No workspace.  One kernel launch.
+ * ------------------------------------------------------------------------ */
+int ce_fwd_sbv_bf16(const uint16_t* logits, const int64_t* target, int64_t S, int64_t B,
+                    int64_t V, float* loss, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Fused linear + cross-entropy (logits z = x W^T never written to memory).
+ * Page "Fused linear + CPO loss", summary ("computed chunked without
+ * materializing logits") and section Semantics: x [batch, seq, hidden],
+ * weight [vocab, hidden], target int64 [batch, seq], loss float [1]; bf16 per
+ * its workload table.  Only the cross-entropy core is computed: the page does
+ * not define the preference term.  Pass x flattened to [T = batch*seq, H].
+ *
+ *   x       [T, H] bf16 device, 16-byte aligned, H % 8 == 0
+ *   W       [V, H] bf16 device, 16-byte aligned
+ *   target  [T] int64 device
+ *   loss    [1] fp32 device output: (1/T) sum_i loss_i; logits are accumulated
+ *           in fp32 on the tensor cores and never rounded to bf16.
+ *   ws      ws_bytes >= flce_workspace_bytes(T, H, V), zeroed before first
+ *           use.  After completion the first T floats hold the per-token losses.
+ * Status: LMHO_ERR_TIMEOUT is reported through lmho_ws_status().
+ * ------------------------------------------------------------------------ */
+size_t flce_workspace_bytes(int64_t T, int64_t H, int64_t V);
+int flce_fwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t T,
+                  int64_t H, int64_t V, float* loss, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Fused linear + generalized Jensen-Shannon divergence, batchmean.
+ * Page "Fused linear + JSD", summary (separate vocab x hidden heads for student
+ * and teacher, generalized JSD with beta 0.5, batchmean) and section
+ * Semantics: student_input [tokens, hidden], student_weight [vocab, hidden],
+ * teacher_input, teacher_weight, loss float [1].
+ *
+ *   P = softmax(xs Ws^T) (student), Q = softmax(xt Wt^T) (teacher), per token;
+ *   loss = (1/T) sum_i JSD_beta(P_i || Q_i).
+ *
+ *   xs, xt  [T, H] bf16 device;  Ws, Wt  [V, H] bf16 device (16-byte aligned,
+ *           H % 8 == 0)
+ *   beta    in (0, 1)
+ *   loss    [1] fp32 device output
+ *   ws      ws_bytes >= fljsd_workspace_bytes(T, H, V), zeroed before first
+ *           use.  After completion the first T floats hold the per-token JSD.
+ * Two tensor-core passes (log-sum-exp of both heads, then a recompute pass
+ * that accumulates the divergence), since M couples both normalisers.
+ * ------------------------------------------------------------------------ */
+size_t fljsd_workspace_bytes(int64_t T, int64_t H, int64_t V);
+int fljsd_fwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt,
+                   const uint16_t* Wt, int64_t T, int64_t H, int64_t V, float beta,
+                   float* loss, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Device status of a workspace-carrying call (flce, fljsd).
+ * Synchronises `stream`, reads the status word of `ws`, clears it, and returns
+ * LMHO_OK or LMHO_ERR_TIMEOUT (a bounded wait inside a kernel gave up; that
+ * call's outputs are then undefined).  ws_bytes must be the size passed to
+ * the call.
+ * ------------------------------------------------------------------------ */
+int lmho_ws_status(void* ws, size_t ws_bytes, void* stream);
+
+/* Row decomposition of the two cross-entropy calls, process-wide:
+ *   0 = automatic (default: warp per row for rows <= 16 KB, a cluster of 8
+ *       CTAs per row when rows are few and >= 64 KB, else a CTA per row),
+ *   1 = warp per row, 2 = CTA (256 threads) per row, 3 = CTA (512) per row,
+ *   4 / 5 / 6 = cluster of 2 / 4 / 8 CTAs per row (DSMEM merge).
+ * Results agree to rounding whichever is chosen.  Returns LMHO_ERR_INVALID_ARG
+ * for other values.  The environment variable LMHO_CE_VARIANT (warp, cta,
+ * cta512, cluster2, cluster4, cluster8) sets the initial value. */
+int lmho_set_ce_variant(int variant);
+
+/* Measurement hook, process-wide and not thread-safe: while set, every call
+ * records events[0] (a caller-created cudaEvent_t) on its stream before its
+ * first kernel and events[i] after its i-th kernel, for i < n.  Kernels per
+ * call: ce_fwd_f32 1, ce_fwd_sbv_bf16 1, flce_fwd_bf16 2 (tensor-core pass,
+ * finaliser), fljsd_fwd_bf16 4 (log-sum-exp pass, finaliser, divergence
+ * pass, finaliser).  Pass (NULL, 0) to turn it off. */
+void lmho_set_launch_events(void* const* events, int n);
+
+/* Upper bound, in nanoseconds, of every in-kernel wait of later calls
+ * (default 2e9).  Process-wide. */
+void lmho_set_wait_timeout_ns(uint64_t ns);
+
+/* Self-test of the bounded-wait path: launches one block that waits on a
+ * barrier nothing completes, for at most timeout_ns, then records
+ * LMHO_ERR_TIMEOUT in the status word of ws (>= 256 bytes, zeroed).  Read it
+ * back with lmho_ws_status(). */
+int lmho_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* LMHO_H_ */

@@ -1,0 +1,260 @@
+"""GB300 (sm_103a) LM-head losses: softmax cross-entropy over a tokens x vocab
+logit matrix (flat fp32 mean and Megatron-layout bf16 per token), fused
+linear + cross-entropy and fused linear + generalized JSD.
+
+This module is a thin ctypes binding over the C ABI in ``include/lmho.h``
+(``liblmho.so``): it checks tensor dtypes/shapes/devices, passes raw device
+pointers and the current CUDA stream, and turns status codes into exceptions.
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback, and a missing library is an error.
+
+Build the library with ``python -m lm_head_online_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "liblmho.so")
+
+LMHO_OK = 0
+LMHO_ERR_INVALID_ARG = 1
+LMHO_ERR_ALIAS = 2
+LMHO_ERR_WORKSPACE = 3
+LMHO_ERR_UNSUPPORTED = 4
+LMHO_ERR_CUDA = 5
+LMHO_ERR_TIMEOUT = 6
+
+# Every symbol declared in include/lmho.h.
+EXPORTS = (
+    "lmho_strerror", "lmho_version", "ce_workspace_bytes", "ce_fwd_f32", "ce_fwd_sbv_bf16",
+    "flce_workspace_bytes", "flce_fwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16",
+    "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
+)
+
+CE_VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "cta512": 3, "cluster2": 4, "cluster4": 5, "cluster8": 6}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LmhoError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status}: {strerror(status)}")
+
+
+def load():
+    """Load liblmho.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m lm_head_online_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i64, sz, f32, u64, ci = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float,
+                                     ctypes.c_uint64, ctypes.c_int)
+        lib.lmho_strerror.argtypes = [ci]
+        lib.lmho_strerror.restype = ctypes.c_char_p
+        lib.lmho_version.restype = ci
+        lib.ce_workspace_bytes.argtypes = [i64, i64]
+        lib.ce_workspace_bytes.restype = sz
+        lib.ce_fwd_f32.argtypes = [vp, vp, i64, i64, vp, vp, sz, vp]
+        lib.ce_fwd_f32.restype = ci
+        lib.ce_fwd_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, vp, vp]
+        lib.ce_fwd_sbv_bf16.restype = ci
+        lib.flce_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.flce_workspace_bytes.restype = sz
+        lib.flce_fwd_bf16.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, sz, vp]
+        lib.flce_fwd_bf16.restype = ci
+        lib.fljsd_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.fljsd_workspace_bytes.restype = sz
+        lib.fljsd_fwd_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, sz, vp]
+        lib.fljsd_fwd_bf16.restype = ci
+        lib.lmho_ws_status.argtypes = [vp, sz, vp]
+        lib.lmho_ws_status.restype = ci
+        lib.lmho_set_ce_variant.argtypes = [ci]
+        lib.lmho_set_ce_variant.restype = ci
+        lib.lmho_set_launch_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ci]
+        lib.lmho_set_launch_events.restype = None
+        lib.lmho_set_wait_timeout_ns.argtypes = [u64]
+        lib.lmho_set_wait_timeout_ns.restype = None
+        lib.lmho_selftest_wait_timeout.argtypes = [vp, sz, u64, vp]
+        lib.lmho_selftest_wait_timeout.restype = ci
+        _lib = lib
+    return _lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return load().lmho_strerror(int(status)).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def _check(status: int, where: str):
+    if status != LMHO_OK:
+        raise LmhoError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """Zero-filled device workspace (torch allocations are 512-byte aligned)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# ---------------------------------------------------------------- sizes
+def ce_workspace_bytes(T: int, V: int) -> int:
+    return int(load().ce_workspace_bytes(T, V))
+
+
+def flce_workspace_bytes(T: int, H: int, V: int) -> int:
+    return int(load().flce_workspace_bytes(T, H, V))
+
+
+def fljsd_workspace_bytes(T: int, H: int, V: int) -> int:
+    return int(load().fljsd_workspace_bytes(T, H, V))
+
+
+# ---------------------------------------------------------------- ops
+def ce_fwd_f32(logits, target, loss=None, ws=None, stream=None):
+    """Mean cross-entropy of fp32 logits [T, V] against int64 targets [T] -> fp32 [1].
+
+    After the stream reaches this call's end, ``ws[:4*T]`` viewed as float32
+    holds the per-token losses.
+    """
+    lib = load()
+    pl = _dev(logits, "logits", torch.float32, 2)
+    T, V = logits.shape
+    pt = _dev(target, "target", torch.int64, 1)
+    if target.shape[0] != T:
+        raise ValueError("target must have T entries")
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=logits.device)
+    if ws is None:
+        ws = workspace(lib.ce_workspace_bytes(T, V), logits.device)
+    _check(lib.ce_fwd_f32(pl, pt, T, V, _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8),
+                          ws.numel(), _stream(stream)), "ce_fwd_f32")
+    return loss
+
+
+def ce_fwd_sbv_bf16(logits, target, loss=None, stream=None):
+    """Per-token cross-entropy of bf16 logits [S, B, V] -> fp32 [S, B]."""
+    lib = load()
+    pl = _dev(logits, "logits", torch.bfloat16, 3)
+    S, B, V = logits.shape
+    pt = _dev(target, "target", torch.int64, 2)
+    if tuple(target.shape) != (S, B):
+        raise ValueError("target must be [S, B]")
+    if loss is None:
+        loss = torch.empty((S, B), dtype=torch.float32, device=logits.device)
+    _check(lib.ce_fwd_sbv_bf16(pl, pt, S, B, V, _dev(loss, "loss", torch.float32), _stream(stream)),
+           "ce_fwd_sbv_bf16")
+    return loss
+
+
+def flce_fwd_bf16(x, W, target, loss=None, ws=None, stream=None):
+    """Mean cross-entropy of z = x W^T (never materialised) -> fp32 [1].
+
+    x is [T, H] or [batch, seq, H] bf16, W [V, H] bf16, target [T] or
+    [batch, seq] int64.  ``ws[:4*T]`` (float32) holds the per-token losses.
+    """
+    lib = load()
+    if x.dim() == 3:
+        x = x.reshape(-1, x.shape[-1])
+    if target.dim() == 2:
+        target = target.reshape(-1)
+    px = _dev(x, "x", torch.bfloat16, 2)
+    pw = _dev(W, "W", torch.bfloat16, 2)
+    pt = _dev(target, "target", torch.int64, 1)
+    T, H = x.shape
+    V = W.shape[0]
+    if W.shape[1] != H or target.shape[0] != T:
+        raise ValueError("shape mismatch: x [T,H], W [V,H], target [T]")
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(lib.flce_workspace_bytes(T, H, V), x.device)
+    _check(lib.flce_fwd_bf16(px, pw, pt, T, H, V, _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8),
+                             ws.numel(), _stream(stream)), "flce_fwd_bf16")
+    return loss
+
+
+def fljsd_fwd_bf16(xs, Ws, xt, Wt, beta=0.5, loss=None, ws=None, stream=None):
+    """Batchmean generalized JSD between softmax(xs Ws^T) (student, P) and
+    softmax(xt Wt^T) (teacher, Q) -> fp32 [1].  ``ws[:4*T]`` holds per-token JSD."""
+    lib = load()
+    p1 = _dev(xs, "xs", torch.bfloat16, 2)
+    p2 = _dev(Ws, "Ws", torch.bfloat16, 2)
+    p3 = _dev(xt, "xt", torch.bfloat16, 2)
+    p4 = _dev(Wt, "Wt", torch.bfloat16, 2)
+    T, H = xs.shape
+    V = Ws.shape[0]
+    if tuple(xt.shape) != (T, H) or tuple(Ws.shape) != (V, H) or tuple(Wt.shape) != (V, H):
+        raise ValueError("shape mismatch: xs, xt [T,H]; Ws, Wt [V,H]")
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=xs.device)
+    if ws is None:
+        ws = workspace(lib.fljsd_workspace_bytes(T, H, V), xs.device)
+    _check(lib.fljsd_fwd_bf16(p1, p2, p3, p4, T, H, V, float(beta), _dev(loss, "loss", torch.float32),
+                              _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "fljsd_fwd_bf16")
+    return loss
+
+
+def row_losses(ws: torch.Tensor, T: int) -> torch.Tensor:
+    """Per-token losses (or JSD) left in the first 4*T bytes of a workspace."""
+    return ws[: 4 * T].view(torch.float32)
+
+
+def ws_status(ws, stream=None) -> int:
+    """Synchronise the stream and return (and clear) the workspace status word."""
+    return int(load().lmho_ws_status(_dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)))
+
+
+def set_ce_variant(name: str):
+    """Row decomposition of the CE calls: auto, warp, cta, cta512, cluster2/4/8."""
+    _check(load().lmho_set_ce_variant(CE_VARIANTS[name]), "lmho_set_ce_variant")
+
+
+def set_launch_events(events):
+    """Measurement hook: a list of torch.cuda.Event (enable_timing=True) to be
+    recorded around the library's own kernel launches, or None to clear."""
+    if not events:
+        load().lmho_set_launch_events(None, 0)
+        return
+    for e in events:   # torch creates the CUDA event lazily, on its first record
+        if not e.cuda_event:
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    load().lmho_set_launch_events(arr, len(events))
+
+
+def set_wait_timeout_ns(ns: int):
+    load().lmho_set_wait_timeout_ns(int(ns))
+
+
+def selftest_wait_timeout(ws, timeout_ns: int, stream=None):
+    _check(load().lmho_selftest_wait_timeout(_dev(ws, "ws", torch.uint8), ws.numel(), int(timeout_ns),
+                                             _stream(stream)), "lmho_selftest_wait_timeout")

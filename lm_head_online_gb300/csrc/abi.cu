@@ -1,0 +1,363 @@
+// C ABI entry points (include/lmho.h): argument checks, workspace carve-up,
+// TMA tensor maps and kernel selection.  Nothing here allocates or
+// synchronises except lmho_ws_status, which is documented to.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/lmho.h"
+#include "lmho_internal.h"
+#include "ptx.cuh"
+
+namespace lmho {
+namespace {
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t n) { return (n + kAlign - 1) / kAlign * kAlign; }
+
+struct DeviceInfo {
+  bool checked = false;
+  bool ok = false;
+  int num_sms = 0;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+// Compute capability 10.3 (sm_103) is the only target the kernels are built for.
+int current_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return LMHO_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return LMHO_ERR_CUDA;
+    d.ok = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    d.checked = true;
+  }
+  if (!d.ok) return LMHO_ERR_UNSUPPORTED;
+  *num_sms = d.num_sms;
+  return LMHO_OK;
+}
+
+struct Range {
+  uintptr_t lo, hi;
+};
+inline Range rng(const void* p, size_t bytes) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + bytes};
+}
+inline bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Each `out` range must be disjoint from every input range and from the other outputs.
+int check_alias(const Range* in, int nin, const Range* out, int nout) {
+  for (int i = 0; i < nout; ++i) {
+    for (int j = 0; j < nin; ++j)
+      if (overlap(out[i], in[j])) return LMHO_ERR_ALIAS;
+    for (int j = i + 1; j < nout; ++j)
+      if (overlap(out[i], out[j])) return LMHO_ERR_ALIAS;
+  }
+  return LMHO_OK;
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? LMHO_OK : LMHO_ERR_CUDA; }
+
+inline Ctrl* ctrl_of(void* ws, size_t ws_bytes) {
+  return reinterpret_cast<Ctrl*>(static_cast<char*>(ws) + (ws_bytes / kAlign) * kAlign - kAlign);
+}
+
+// ---------------------------------------------------------------- CE selection
+// Process-wide decomposition override (lmho_set_ce_variant); initial value
+// from LMHO_CE_VARIANT = warp | cta | cta512 | cluster2 | cluster4 | cluster8.
+int env_ce_variant() {
+  const char* s = std::getenv("LMHO_CE_VARIANT");
+  if (!s) return 0;
+  const char* names[] = {"warp", "cta", "cta512", "cluster2", "cluster4", "cluster8"};
+  for (int i = 0; i < 6; ++i)
+    if (!std::strcmp(s, names[i])) return i + 1;
+  return 0;
+}
+std::atomic<int> g_ce_variant{env_ce_variant()};
+
+CeConfig choose_ce(int64_t rows, int64_t V, size_t elt, int num_sms) {
+  switch (g_ce_variant.load()) {
+    case 1: return CeConfig{kCeWarp, 256, 1};
+    case 2: return CeConfig{kCeCta, 256, 1};
+    case 3: return CeConfig{kCeCta, 512, 1};
+    case 4: return CeConfig{kCeCluster, 256, 2};
+    case 5: return CeConfig{kCeCluster, 256, 4};
+    case 6: return CeConfig{kCeCluster, 256, 8};
+    default: break;
+  }
+  const int64_t row_bytes = V * static_cast<int64_t>(elt);
+  if (row_bytes <= 16 * 1024) return CeConfig{kCeWarp, 256, 1};
+  // Few long rows: split each row over a cluster so every SM streams.
+  if (rows < 4 * static_cast<int64_t>(num_sms) && row_bytes >= 64 * 1024) return CeConfig{kCeCluster, 256, 8};
+  return CeConfig{kCeCta, 256, 1};
+}
+
+// ---------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? LMHO_OK : LMHO_ERR_CUDA;
+}
+
+// bf16 matrix [rows, H] (row-major, H contiguous), box = 64 (H) x box_rows, 128-byte swizzle.
+int tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t H, uint32_t box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LMHO_OK : LMHO_ERR_CUDA;
+}
+
+FusedGeometry geometry(int64_t T, int64_t H, int64_t V, int bn) {
+  FusedGeometry g{};
+  g.T = T;
+  g.H = H;
+  g.V = V;
+  g.num_m = (T + kBM - 1) / kBM;
+  g.num_n = (V + bn - 1) / bn;
+  g.group_m = static_cast<int>(g.num_m < 16 ? g.num_m : 16);
+  return g;
+}
+
+int check_fused_common(int64_t T, int64_t H, int64_t V) {
+  if (T <= 0 || H <= 0 || V <= 0) return LMHO_ERR_INVALID_ARG;
+  if (H % 8 != 0) return LMHO_ERR_UNSUPPORTED;  // TMA row stride must be a multiple of 16 bytes
+  if (T > (int64_t(1) << 31) || V > (int64_t(1) << 31)) return LMHO_ERR_INVALID_ARG;
+  return LMHO_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+std::mutex g_ev_mu;
+cudaEvent_t g_events[16];
+int g_nevents = 0;
+
+}  // namespace
+
+void launch_mark(int i, cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  if (i < g_nevents && g_events[i]) cudaEventRecord(g_events[i], st);
+}
+
+// ---------------------------------------------------------------- workspace layouts
+size_t flce_ws_bytes(int64_t T, int64_t H, int64_t V) {
+  (void)H;
+  const int64_t num_n = (V + kBN_CE - 1) / kBN_CE;
+  return align_up(4 * T) + 3 * align_up(4 * num_n * T) + kAlign;
+}
+FusedWs flce_ws_carve(void* ws, size_t ws_bytes, int64_t T, int64_t V) {
+  const int64_t num_n = (V + kBN_CE - 1) / kBN_CE;
+  char* p = static_cast<char*>(ws);
+  FusedWs w{};
+  w.row_out = reinterpret_cast<float*>(p);
+  p += align_up(4 * T);
+  w.part0 = reinterpret_cast<float*>(p);
+  p += align_up(4 * num_n * T);
+  w.part1 = reinterpret_cast<float*>(p);
+  p += align_up(4 * num_n * T);
+  w.part2 = reinterpret_cast<float*>(p);
+  w.ctrl = ctrl_of(ws, ws_bytes);
+  return w;
+}
+size_t fljsd_ws_bytes(int64_t T, int64_t H, int64_t V) {
+  (void)H;
+  const int64_t n256 = (V + kBN_CE - 1) / kBN_CE, n128 = (V + kBN_JSD - 1) / kBN_JSD;
+  const int64_t p0 = (2 * n256 > n128 ? 2 * n256 : n128) * T;
+  return align_up(4 * T) + align_up(4 * p0) + align_up(4 * 2 * n256 * T) + align_up(4 * 2 * T) + kAlign;
+}
+FusedWs fljsd_ws_carve(void* ws, size_t ws_bytes, int64_t T, int64_t V) {
+  const int64_t n256 = (V + kBN_CE - 1) / kBN_CE, n128 = (V + kBN_JSD - 1) / kBN_JSD;
+  const int64_t p0 = (2 * n256 > n128 ? 2 * n256 : n128) * T;
+  char* p = static_cast<char*>(ws);
+  FusedWs w{};
+  w.row_out = reinterpret_cast<float*>(p);
+  p += align_up(4 * T);
+  w.part0 = reinterpret_cast<float*>(p);
+  p += align_up(4 * p0);
+  w.part1 = reinterpret_cast<float*>(p);
+  p += align_up(4 * 2 * n256 * T);
+  w.lse = reinterpret_cast<float*>(p);
+  w.ctrl = ctrl_of(ws, ws_bytes);
+  return w;
+}
+
+}  // namespace lmho
+
+using namespace lmho;
+
+extern "C" {
+
+const char* lmho_strerror(int status) {
+  switch (status) {
+    case LMHO_OK: return "ok";
+    case LMHO_ERR_INVALID_ARG: return "invalid argument (null pointer, size <= 0 or out of range)";
+    case LMHO_ERR_ALIAS: return "an output or workspace range overlaps an input or another output";
+    case LMHO_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case LMHO_ERR_UNSUPPORTED: return "unsupported: device is not compute capability 10.3, or H % 8 != 0";
+    case LMHO_ERR_CUDA: return "a CUDA runtime call failed";
+    case LMHO_ERR_TIMEOUT: return "a bounded in-kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int lmho_version(void) { return 100; }
+
+void lmho_set_launch_events(void* const* events, int n) {
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  g_nevents = 0;
+  if (!events || n <= 0) return;
+  if (n > 16) n = 16;
+  for (int k = 0; k < n; ++k) g_events[k] = static_cast<cudaEvent_t>(events[k]);
+  g_nevents = n;
+}
+
+int lmho_set_ce_variant(int variant) {
+  if (variant < 0 || variant > 6) return LMHO_ERR_INVALID_ARG;
+  g_ce_variant.store(variant);
+  return LMHO_OK;
+}
+
+void lmho_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+size_t ce_workspace_bytes(int64_t T, int64_t V) {
+  (void)V;
+  if (T <= 0) return kAlign;
+  return align_up(4 * static_cast<size_t>(T)) + kAlign;
+}
+
+int ce_fwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V, float* loss, void* ws,
+               size_t ws_bytes, void* stream) {
+  if (!logits || !target || !loss || !ws) return LMHO_ERR_INVALID_ARG;
+  if (T <= 0 || V <= 0 || T > (int64_t(1) << 31) - 1) return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < ce_workspace_bytes(T, V) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const Range in[2] = {rng(logits, 4 * static_cast<size_t>(T) * V), rng(target, 8 * static_cast<size_t>(T))};
+  const Range out[2] = {rng(loss, 4), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 2, out, 2)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  const CeConfig cfg = choose_ce(T, V, 4, sms);
+  return cuda_status(launch_ce_f32(logits, target, T, V, loss, static_cast<float*>(ws), ctrl_of(ws, ws_bytes), cfg,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+int ce_fwd_sbv_bf16(const uint16_t* logits, const int64_t* target, int64_t S, int64_t B, int64_t V, float* loss,
+                    void* stream) {
+  if (!logits || !target || !loss) return LMHO_ERR_INVALID_ARG;
+  if (S <= 0 || B <= 0 || V <= 0) return LMHO_ERR_INVALID_ARG;
+  const int64_t rows = S * B;
+  if (rows > (int64_t(1) << 31) - 1) return LMHO_ERR_INVALID_ARG;
+  const Range in[2] = {rng(logits, 2 * static_cast<size_t>(rows) * V), rng(target, 8 * static_cast<size_t>(rows))};
+  const Range out[1] = {rng(loss, 4 * static_cast<size_t>(rows))};
+  if (int a = check_alias(in, 2, out, 1)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  const CeConfig cfg = choose_ce(rows, V, 2, sms);
+  return cuda_status(launch_ce_bf16_rows(logits, target, rows, V, loss, cfg, static_cast<cudaStream_t>(stream)));
+}
+
+size_t flce_workspace_bytes(int64_t T, int64_t H, int64_t V) {
+  if (T <= 0 || V <= 0) return kAlign;
+  return flce_ws_bytes(T, H, V);
+}
+
+int flce_fwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t T, int64_t H, int64_t V,
+                  float* loss, void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !W || !target || !loss || !ws) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_fused_common(T, H, V)) return c;
+  if (!aligned16(x) || !aligned16(W)) return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < flce_ws_bytes(T, H, V) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const Range in[3] = {rng(x, 2 * static_cast<size_t>(T) * H), rng(W, 2 * static_cast<size_t>(V) * H),
+                       rng(target, 8 * static_cast<size_t>(T))};
+  const Range out[2] = {rng(loss, 4), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 3, out, 2)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  CUtensorMap tx, tw;
+  if (tmap_bf16(&tx, x, T, H, kBM) || tmap_bf16(&tw, W, V, H, kBN_CE)) return LMHO_ERR_CUDA;
+  const FusedGeometry g = geometry(T, H, V, kBN_CE);
+  const FusedWs w = flce_ws_carve(ws, ws_bytes, T, V);
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_flce(tx, tw, target, g, loss, w, L));
+}
+
+size_t fljsd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
+  if (T <= 0 || V <= 0) return kAlign;
+  return fljsd_ws_bytes(T, H, V);
+}
+
+int fljsd_fwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, const uint16_t* Wt, int64_t T,
+                   int64_t H, int64_t V, float beta, float* loss, void* ws, size_t ws_bytes, void* stream) {
+  if (!xs || !Ws || !xt || !Wt || !loss || !ws) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_fused_common(T, H, V)) return c;
+  if (!(beta > 0.f && beta < 1.f)) return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(xs) || !aligned16(Ws) || !aligned16(xt) || !aligned16(Wt)) return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < fljsd_ws_bytes(T, H, V) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const size_t xb = 2 * static_cast<size_t>(T) * H, wb = 2 * static_cast<size_t>(V) * H;
+  const Range in[4] = {rng(xs, xb), rng(Ws, wb), rng(xt, xb), rng(Wt, wb)};
+  const Range out[2] = {rng(loss, 4), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 4, out, 2)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  CUtensorMap txs, txt, tws256, twt256, tws128, twt128;
+  if (tmap_bf16(&txs, xs, T, H, kBM) || tmap_bf16(&txt, xt, T, H, kBM) || tmap_bf16(&tws256, Ws, V, H, kBN_CE) ||
+      tmap_bf16(&twt256, Wt, V, H, kBN_CE) || tmap_bf16(&tws128, Ws, V, H, kBN_JSD) ||
+      tmap_bf16(&twt128, Wt, V, H, kBN_JSD))
+    return LMHO_ERR_CUDA;
+  const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD);
+  const FusedWs w = fljsd_ws_carve(ws, ws_bytes, T, V);
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_fljsd(txs, tws256, txt, twt256, tws128, twt128, g1, g2, beta, loss, w, L));
+}
+
+int lmho_ws_status(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kAlign || !aligned256(ws)) return LMHO_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LMHO_ERR_CUDA;
+  Ctrl* c = ctrl_of(ws, ws_bytes);
+  uint32_t st = 0;
+  if (cudaMemcpy(&st, &c->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return LMHO_ERR_CUDA;
+  if (st != 0) {
+    if (cudaMemset(&c->status, 0, 4) != cudaSuccess) return LMHO_ERR_CUDA;
+    return static_cast<int>(st);
+  }
+  return LMHO_OK;
+}
+
+int lmho_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, void* stream) {
+  if (!ws || ws_bytes < kAlign || !aligned256(ws)) return LMHO_ERR_INVALID_ARG;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  return cuda_status(launch_wait_selftest(ctrl_of(ws, ws_bytes), timeout_ns, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

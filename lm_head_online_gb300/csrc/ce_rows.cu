@@ -1,0 +1,260 @@
+// Row-wise softmax cross-entropy over a [rows, V] logit matrix, fp32 or bf16.
+//
+// Operation: pages "Cross-entropy loss" (fp32 [tokens, vocab], mean loss[1])
+// and "Vocab-parallel cross-entropy, Megatron layout" (bf16 [seq, batch,
+// vocab], per-token fp32 loss), section Semantics of each.  For row i:
+//   loss_i = m_i + ln(s_i) - z_{i,t_i},  m_i = max_v z_iv,
+//   s_i = sum_v exp(z_iv - m_i),
+// computed in ONE streaming pass with the online normaliser (Milakov &
+// Gimelshein 2018): each thread keeps a running (m, s) and rescales s by
+// exp(m_old - m_new) when a new block of values raises the maximum; partial
+// (m, s) pairs merge the same way, across lanes, warps and cluster CTAs.
+//
+// HBM-bound: every logit is read exactly once with 16-byte non-allocating
+// loads, several in flight per thread.  Three decompositions of a row:
+//   * warp per row   -- small rows; no shared memory, no block barrier;
+//   * CTA per row    -- mid/large rows; warp shuffles, then shared memory;
+//   * cluster per row -- C CTAs split the row, each merges its share, and CTA 0
+//     merges the C partials read from its peers' shared memory (DSMEM).
+// The flat variant's mean is a deterministic two-level sum: per-token losses
+// go to the workspace, and the last block to finish (atomic ticket, no spin)
+// sums them in a fixed order in fp64.
+#include <cmath>
+#include <cstdint>
+
+#include "lmho_internal.h"
+#include "ptx.cuh"
+#include "rowstats.cuh"
+
+namespace lmho {
+namespace {
+
+// ---------------------------------------------------------------- element types
+template <typename T> struct Elt;
+template <> struct Elt<float> {
+  static constexpr int kPerVec = 4;  // elements per 16-byte vector
+  __device__ static float load1(const float* p) { return __ldg(p); }
+  __device__ static void unpack(const uint4& r, float* v) {
+    v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
+    v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
+  }
+};
+template <> struct Elt<uint16_t> {  // bf16 bit patterns
+  static constexpr int kPerVec = 8;
+  __device__ static float load1(const uint16_t* p) {
+    return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
+  }
+  __device__ static void unpack(const uint4& r, float* v) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+};
+
+// Partial (m, s) of elements [lo, hi) of one row, shared by `nt` threads
+// (this one is `tid`).  Elements before the first 16-byte boundary and after
+// the last one are folded one at a time; the aligned body is read as 16-byte
+// vectors, U per thread per step, each load instruction coalesced across the
+// threads.
+template <typename T, int U>
+__device__ __forceinline__ MS row_partial(const T* row, int64_t lo, int64_t hi, int tid, int nt) {
+  constexpr int E = Elt<T>::kPerVec;
+  MS a = ms_empty();
+  if (hi <= lo) return a;
+  const uintptr_t base = reinterpret_cast<uintptr_t>(row + lo);
+  int64_t head = static_cast<int64_t>(((16u - (base & 15u)) & 15u) / sizeof(T));
+  if (head > hi - lo) head = hi - lo;
+  const int64_t nvec = (hi - lo - head) / E;
+  const int64_t body_end = lo + head + nvec * E;
+  // scalar head and tail
+  for (int64_t j = tid; j < head; j += nt) {
+    float v = Elt<T>::load1(row + lo + j);
+    ms_fold<1>(a, &v);
+  }
+  for (int64_t j = body_end + tid; j < hi; j += nt) {
+    float v = Elt<T>::load1(row + j);
+    ms_fold<1>(a, &v);
+  }
+  const uint4* vec = reinterpret_cast<const uint4*>(row + lo + head);
+  const int64_t step = static_cast<int64_t>(nt) * U;
+  int64_t q0 = 0;
+  // full steps: no bounds checks
+  for (; q0 + step <= nvec; q0 += step) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) r[u] = ldg_stream_v4(vec + q0 + u * nt + tid);
+    float v[U * E];
+#pragma unroll
+    for (int u = 0; u < U; ++u) Elt<T>::unpack(r[u], v + u * E);
+    ms_fold<U * E>(a, v);
+  }
+  // last partial step
+  if (q0 < nvec) {
+    uint4 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t q = q0 + u * nt + tid;
+      r[u] = q < nvec ? ldg_stream_v4(vec + q) : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+    }
+    float v[U * E];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      Elt<T>::unpack(r[u], v + u * E);
+      if (q0 + u * nt + tid >= nvec) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[u * E + e] = -INFINITY;
+      }
+    }
+    ms_fold<U * E>(a, v);
+  }
+  return a;
+}
+
+template <typename T>
+__device__ __forceinline__ float target_logit(const T* row, int64_t V, const int64_t* target, int64_t r) {
+  const int64_t t = __ldg(target + r);
+  return (t >= 0 && t < V) ? Elt<T>::load1(row + t) : __int_as_float(0x7FC00000);
+}
+
+__device__ __forceinline__ float finish_loss(MS a, float zt) {
+  return a.m + logf(a.s) - zt;
+}
+
+// ---------------------------------------------------------------- kernels
+// out_rows: per-row losses (per-token output, or the workspace of the flat mean)
+// mean_out: non-null for the flat variant.
+template <typename T, int U>
+__global__ void __launch_bounds__(256) ce_warp_rows(const T* __restrict__ logits,
+                                                    const int64_t* __restrict__ target, int64_t rows,
+                                                    int64_t V, float* __restrict__ out_rows,
+                                                    float* mean_out, Ctrl* ctrl) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r < rows) {
+    const T* row = logits + r * V;
+    float zt = 0.f;
+    if (lane == 0) zt = target_logit(row, V, target, r);
+    MS a = row_partial<T, U>(row, 0, V, lane, 32);
+    a = ms_warp_allreduce(a);
+    if (lane == 0) out_rows[r] = finish_loss(a, zt);
+  }
+  if (mean_out) mean_tail(out_rows, rows, mean_out, ctrl, gridDim.x);
+}
+
+template <int NT>
+__device__ __forceinline__ MS block_allreduce_to0(MS a, MS* s_part) {
+  a = ms_warp_allreduce(a);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) s_part[w] = a;
+  __syncthreads();
+  MS tot = s_part[0];
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 1; k < NT / 32; ++k) tot = ms_merge(tot, s_part[k]);
+  }
+  return tot;  // valid in thread 0
+}
+
+template <typename T, int U, int NT>
+__global__ void __launch_bounds__(NT) ce_cta_rows(const T* __restrict__ logits,
+                                                  const int64_t* __restrict__ target, int64_t rows,
+                                                  int64_t V, float* __restrict__ out_rows,
+                                                  float* mean_out, Ctrl* ctrl) {
+  __shared__ MS s_part[NT / 32];
+  const int64_t r = blockIdx.x;
+  const T* row = logits + r * V;
+  float zt = 0.f;
+  if (threadIdx.x == 0) zt = target_logit(row, V, target, r);
+  MS a = row_partial<T, U>(row, 0, V, threadIdx.x, NT);
+  a = block_allreduce_to0<NT>(a, s_part);
+  if (threadIdx.x == 0) out_rows[r] = finish_loss(a, zt);
+  if (mean_out) mean_tail(out_rows, rows, mean_out, ctrl, gridDim.x);
+}
+
+// Cluster of C CTAs per row; CTA k of the cluster takes the k-th contiguous
+// slice of the row (slices cut at 16-byte-vector granularity).
+template <typename T, int U, int NT, int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT)
+    ce_cluster_rows(const T* __restrict__ logits, const int64_t* __restrict__ target, int64_t rows,
+                    int64_t V, float* __restrict__ out_rows, float* mean_out, Ctrl* ctrl) {
+  __shared__ MS s_part[NT / 32];
+  __shared__ float s_ms[2];
+  const uint32_t rank = cluster_ctarank();
+  const int64_t r = blockIdx.x / C;
+  const T* row = logits + r * V;
+  // slice boundaries in elements, multiples of 64 elements
+  const int64_t chunk = ((V + C - 1) / C + 63) / 64 * 64;
+  const int64_t lo = (chunk * rank < V) ? chunk * rank : V;
+  const int64_t hi = (lo + chunk < V) ? lo + chunk : V;
+  float zt = 0.f;
+  if (rank == 0 && threadIdx.x == 0) zt = target_logit(row, V, target, r);
+  MS a = row_partial<T, U>(row, lo, hi, threadIdx.x, NT);
+  a = block_allreduce_to0<NT>(a, s_part);
+  if (threadIdx.x == 0) { s_ms[0] = a.m; s_ms[1] = a.s; }
+  cluster_sync();  // partials visible cluster-wide
+  if (rank == 0 && threadIdx.x == 0) {
+    MS tot{s_ms[0], s_ms[1]};
+    for (uint32_t k = 1; k < C; ++k) {
+      MS b{ld_dsmem_f32(mapa_shared(&s_ms[0], k)), ld_dsmem_f32(mapa_shared(&s_ms[1], k))};
+      tot = ms_merge(tot, b);
+    }
+    out_rows[r] = finish_loss(tot, zt);
+  }
+  cluster_sync();  // peers keep their shared memory until CTA 0 has read it
+  if (mean_out && rank == 0) mean_tail(out_rows, rows, mean_out, ctrl, gridDim.x / C);
+}
+
+template <typename T>
+cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, int64_t V,
+                        float* out_rows, float* mean_out, Ctrl* ctrl, const CeConfig& cfg,
+                        cudaStream_t st) {
+  launch_mark(0, st);
+  switch (cfg.variant) {
+    case kCeWarp: {
+      const int64_t blocks = (rows + 7) / 8;
+      ce_warp_rows<T, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(logits, target, rows, V,
+                                                                         out_rows, mean_out, ctrl);
+      break;
+    }
+    case kCeCta:
+      if (cfg.threads == 512)
+        ce_cta_rows<T, 4, 512><<<static_cast<unsigned>(rows), 512, 0, st>>>(logits, target, rows, V,
+                                                                             out_rows, mean_out, ctrl);
+      else
+        ce_cta_rows<T, 4, 256><<<static_cast<unsigned>(rows), 256, 0, st>>>(logits, target, rows, V,
+                                                                             out_rows, mean_out, ctrl);
+      break;
+    case kCeCluster: {
+      const unsigned grid = static_cast<unsigned>(rows * cfg.cluster);
+      if (cfg.cluster == 2)
+        ce_cluster_rows<T, 4, 256, 2><<<grid, 256, 0, st>>>(logits, target, rows, V, out_rows, mean_out, ctrl);
+      else if (cfg.cluster == 4)
+        ce_cluster_rows<T, 4, 256, 4><<<grid, 256, 0, st>>>(logits, target, rows, V, out_rows, mean_out, ctrl);
+      else
+        ce_cluster_rows<T, 4, 256, 8><<<grid, 256, 0, st>>>(logits, target, rows, V, out_rows, mean_out, ctrl);
+      break;
+    }
+    default:
+      return cudaErrorInvalidValue;
+  }
+  launch_mark(1, st);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ce_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
+                          float* loss, float* row_loss, Ctrl* ctrl, const CeConfig& cfg,
+                          cudaStream_t st) {
+  return launch_rows<float>(logits, target, T, V, row_loss, loss, ctrl, cfg, st);
+}
+
+cudaError_t launch_ce_bf16_rows(const uint16_t* logits, const int64_t* target, int64_t rows,
+                                int64_t V, float* loss_rows, const CeConfig& cfg, cudaStream_t st) {
+  return launch_rows<uint16_t>(logits, target, rows, V, loss_rows, nullptr, nullptr, cfg, st);
+}
+
+}  // namespace lmho

@@ -1,0 +1,523 @@
+// Fused linear + cross-entropy and fused linear + generalized JSD on the
+// 5th-generation tensor cores, logits never written to memory.
+//
+// Operations: page "Fused linear + CPO loss" (summary: activations projected
+// through a vocab x hidden LM head, "computed chunked without materializing
+// logits"; its cross-entropy core) and page "Fused linear + JSD" (summary:
+// student and teacher heads, generalized JSD with beta 0.5, batchmean).
+//
+// One persistent kernel per pass, one CTA per SM, warp-specialised:
+//   warp 0      TMA producer: bf16 tiles x[128 x 64] and W[BN x 64] (128-byte
+//               swizzle) into a ring of shared-memory stages (mbarrier
+//               complete_tx);
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
+//               (M=128, N=BN, K=16, bf16 x bf16 -> fp32) into one of two TMEM
+//               accumulators, frees stages with tcgen05.commit;
+//   warps 2..5  epilogue: each thread owns one token row (one TMEM lane),
+//               reads its accumulator row 32 columns at a time (tcgen05.ld) and
+//               folds it into per-row partials while the MMA fills the other
+//               accumulator.
+// Work unit = (token tile, vocab tile), rastered in groups of `group_m` token
+// tiles so a wave of CTAs shares the same W tiles in L2 and each W tile is
+// read from HBM about once per group.
+//
+// Epilogues (per row r of the tile, vocab columns n0 .. n0+BN-1):
+//   CE   running (max, sum exp) of the tile and the target logit if t_r falls
+//        in the tile  -> partials [num_n][T] x 3
+//   LSE  (max, sum exp) only, for the student and teacher heads (first JSD
+//        pass)        -> partials [2][num_n][T] x 2
+//   JSD  both heads' tiles in TMEM (BN = 128 each); with lp = z_s - lse_s,
+//        lq = z_t - lse_t, accumulates
+//          beta P (lp - lm) + (1-beta) Q (lq - lm),  lm = ln(beta P + (1-beta) Q)
+//        evaluated around the larger of lp, lq so no large terms cancel
+//                     -> partial sums [num_n][T]
+// Finalisers merge the vocab-tile partials of each row in a fixed order and
+// reduce the rows deterministically (see rowstats.cuh).
+#include <cmath>
+#include <cstdint>
+
+#include "lmho_internal.h"
+#include "ptx.cuh"
+#include "rowstats.cuh"
+
+namespace lmho {
+namespace {
+
+enum Mode { kModeCE = 0, kModeLSE = 1, kModeJSD = 2 };
+
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, 4 epilogue warps
+constexpr int kTmemCols = 512;                  // two accumulators of 256 columns
+constexpr int kAccCols = 256;
+constexpr int kSmemBudget = 192 * 1024;
+
+template <int MODE>
+struct ModeCfg {
+  static constexpr int BN = (MODE == kModeJSD) ? kBN_JSD : kBN_CE;
+  static constexpr int kHeadsPerUnit = (MODE == kModeJSD) ? 2 : 1;
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kSmemBudget / kStageBytes;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers*/;
+  static_assert(BN * kHeadsPerUnit == kAccCols, "accumulator holds 256 fp32 columns");
+  // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+  // (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
+  // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     (static_cast<uint32_t>(BN >> 3) << 17) |
+                                     (static_cast<uint32_t>(kBM >> 4) << 24);
+};
+
+struct Params {
+  int64_t T, V;
+  int32_t num_m, num_n, group_m, k_blocks;
+  int64_t units;
+  const int64_t* target;  // CE
+  float* part0;
+  float* part1;
+  float* part2;
+  const float* lse;  // JSD: [2][T]
+  float beta;
+  uint64_t timeout_ns;
+  uint32_t* status;
+};
+
+// Shared-memory descriptor of a K-major bf16 tile written by TMA with 128-byte
+// swizzle: rows of 128 bytes, 8-row core groups 1024 bytes apart (SBO), start
+// address >> 4 in bits 0-13, LBO field 1 (unused for this layout), bits 46-48
+// = 0b001, swizzle mode 2 (128-byte) in bits 61-63.  Tiles are 1024-byte
+// aligned, so the base-offset field is 0.  Moving 16 bf16 (32 bytes) along K
+// inside the swizzle row adds 2 to the start-address field.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+struct UnitCoord {
+  int head;  // LSE: which head; others 0
+  int mt, nt;
+};
+
+__device__ __forceinline__ UnitCoord decode_unit(const Params& p, int64_t u, int mode) {
+  UnitCoord c{0, 0, 0};
+  const int64_t per_head = static_cast<int64_t>(p.num_m) * p.num_n;
+  if (mode == kModeLSE) {
+    c.head = static_cast<int>(u / per_head);
+    u -= static_cast<int64_t>(c.head) * per_head;
+  }
+  const int64_t per_group = static_cast<int64_t>(p.group_m) * p.num_n;
+  const int64_t g = u / per_group;
+  const int64_t r = u - g * per_group;
+  const int64_t m_first = g * p.group_m;
+  const int64_t rem = p.num_m - m_first;
+  const int64_t gm = rem < p.group_m ? rem : p.group_m;
+  c.mt = static_cast<int>(m_first + r % gm);
+  c.nt = static_cast<int>(r / gm);
+  return c;
+}
+
+// Generalized-JSD term of one (token, vocab) pair from log-probabilities.
+// With hi = max(lp, lq), d = |lp - lq|, e = exp(-d) and weights (w_hi, w_lo)
+// the beta weights of the larger and smaller side:
+//   lm = hi + ln(w_hi + w_lo e),  hi - lm = -ln(w_hi + w_lo e),  lo - lm = (hi - lm) - d
+//   term = w_hi e^hi (hi - lm) + w_lo e^hi e (lo - lm).
+__device__ __forceinline__ float jsd_term(float lp, float lq, float beta, float omb) {
+  const float hi = fmaxf(lp, lq);
+  const float d = fabsf(lp - lq);
+  const bool p_is_hi = lp >= lq;
+  const float w_hi = p_is_hi ? beta : omb;
+  const float w_lo = p_is_hi ? omb : beta;
+  const float e = ex2_approx(-d * kLog2e);
+  const float a_hi = -kLn2 * lg2_approx(fmaf(w_lo, e, w_hi));
+  const float a_lo = a_hi - d;
+  const float p_hi = ex2_approx(hi * kLog2e);
+  return p_hi * (w_hi * a_hi + w_lo * e * a_lo);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_b0,
+                      const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b1,
+                      const Params p) {
+  using C = ModeCfg<MODE>;
+  constexpr int BN = C::BN;
+  constexpr int S = C::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+  uint64_t* full = bars;               // [S]
+  uint64_t* empty = bars + S;          // [S]
+  uint64_t* acc_full = bars + 2 * S;   // [2]
+  uint64_t* acc_empty = acc_full + 2;  // [2]
+  uint64_t* drain = acc_empty + 2;     // [1]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiWarps * 32);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_a0);
+    tma_prefetch_desc(&tm_b0);
+    if (MODE != kModeCE) {
+      tma_prefetch_desc(&tm_a1);
+      tma_prefetch_desc(&tm_b1);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled = 0, last_parity = 0;  // per-stage bit masks for the drain
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        const UnitCoord c = decode_unit(p, u, MODE);
+        for (int h = 0; h < C::kHeadsPerUnit && ok; ++h) {
+          const int head = (MODE == kModeLSE) ? c.head : h;
+          const CUtensorMap* ta = head ? &tm_a1 : &tm_a0;
+          const CUtensorMap* tb = head ? &tm_b1 : &tm_b0;
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, p.status)) { ok = false; break; }
+            uint8_t* sa = tiles + stage * C::kStageBytes;
+            uint8_t* sb = sa + C::kABytes;
+            mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+            tma_load_2d(sa, ta, kb * kBK, c.mt * kBM, &full[stage]);
+            tma_load_2d(sb, tb, kb * kBK, c.nt * BN, &full[stage]);
+            filled |= 1u << stage;
+            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+      // Never leave with copies in flight: wait for the last fill of each stage.
+      for (int s = 0; s < S; ++s)
+        if (filled & (1u << s)) mbar_wait(&full[s], (last_parity >> s) & 1u, p.timeout_ns, p.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const uint32_t a0 = smem_u32(tiles);
+      for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, p.status)) break;
+        tc_fence_after();
+        for (int h = 0; h < C::kHeadsPerUnit && ok; ++h) {
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols + h * BN);
+          for (int kb = 0; kb < p.k_blocks; ++kb) {
+            if (!mbar_wait(&full[stage], phase, p.timeout_ns, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = a0 + stage * C::kStageBytes;
+            const uint64_t da = smem_desc_sw128(sa);
+            const uint64_t db = smem_desc_sw128(sa + C::kABytes);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+              tc_mma_bf16(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
+            tc_commit(&empty[stage]);
+            if (++stage == S) { stage = 0; phase ^= 1u; }
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      // All MMAs issued by this thread complete before TMEM is released.
+      tc_commit(drain);
+      mbar_wait(drain, 0, p.timeout_ns, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;                // TMEM lane quadrant this warp may access
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const float beta = p.beta, omb = 1.f - p.beta;
+    for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
+      const UnitCoord c = decode_unit(p, u, MODE);
+      const int64_t row = static_cast<int64_t>(c.mt) * kBM + row_in_tile;
+      const bool row_ok = row < p.T;
+      const int64_t n0 = static_cast<int64_t>(c.nt) * BN;
+      int64_t tgt = -1;
+      float ls = 0.f, lt = 0.f;
+      if (MODE == kModeCE && row_ok) tgt = __ldg(p.target + row);
+      if (MODE == kModeJSD && row_ok) {
+        ls = __ldg(p.lse + row);
+        lt = __ldg(p.lse + p.T + row);
+      }
+      // tcgen05.ld is warp-collective: the whole warp proceeds or gives up together
+      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[acc], acc_phase, p.timeout_ns, p.status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + lane_addr + static_cast<uint32_t>(acc * kAccCols);
+      MS st = ms_empty();
+      float zt = 0.f;
+      bool has_t = false;
+      float jsd = 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        const int64_t col0 = n0 + cc * 32;
+        if (MODE == kModeJSD) {
+          float vs[32], vt[32];
+          tmem_ld32_sync(tbase + cc * 32, vs);
+          tmem_ld32_sync(tbase + BN + cc * 32, vt);
+          if (col0 + 32 <= p.V) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) jsd += jsd_term(vs[j] - ls, vt[j] - lt, beta, omb);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < p.V) jsd += jsd_term(vs[j] - ls, vt[j] - lt, beta, omb);
+          }
+        } else {
+          float v[32];
+          tmem_ld32_sync(tbase + cc * 32, v);
+          if (col0 + 32 > p.V) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j >= p.V) v[j] = -INFINITY;
+          }
+          if (MODE == kModeCE) {
+            const int64_t off = tgt - col0;
+            if (off >= 0 && off < 32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == off) zt = v[j];
+              has_t = true;
+            }
+          }
+          ms_fold<32>(st, v);
+        }
+      }
+      // accumulator fully read: hand it back to the MMA warp
+      tc_fence_before();
+      mbar_arrive(&acc_empty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (row_ok) {
+        if (MODE == kModeJSD) {
+          p.part0[static_cast<int64_t>(c.nt) * p.T + row] = jsd;
+        } else {
+          const int64_t idx = (static_cast<int64_t>(c.head) * p.num_n + c.nt) * p.T + row;
+          p.part0[idx] = st.m;
+          p.part1[idx] = st.s;
+          if (MODE == kModeCE && has_t) p.part2[static_cast<int64_t>(c.nt) * p.T + row] = zt;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- finalisers
+constexpr int kFinRows = 32;   // rows per block (one per lane)
+constexpr int kFinSplit = 8;   // warps per block, each merging a slice of the vocab tiles
+
+// Merge (m, s) partials [num_n][T] of each row, in vocab-tile order, into
+// its log-sum-exp.  Warp w handles tiles [w*cnt, (w+1)*cnt); the 8 results
+// merge in warp order.
+__device__ __forceinline__ float merge_lse_row(const float* pm, const float* ps, int64_t T, int num_n,
+                                               int64_t row, MS* s_tmp) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int cnt = (num_n + kFinSplit - 1) / kFinSplit;
+  const int n_lo = min(num_n, w * cnt), n_hi = min(num_n, n_lo + cnt);
+  MS a = ms_empty();
+  if (row < T) {
+#pragma unroll 4
+    for (int n = n_lo; n < n_hi; ++n) {
+      const int64_t i = static_cast<int64_t>(n) * T + row;
+      a = ms_merge(a, MS{__ldcg(pm + i), __ldcg(ps + i)});
+    }
+  }
+  s_tmp[w * 32 + l] = a;
+  __syncthreads();
+  MS tot = s_tmp[l];
+  for (int k = 1; k < kFinSplit; ++k) tot = ms_merge(tot, s_tmp[k * 32 + l]);
+  __syncthreads();
+  return tot.m + logf(tot.s);  // meaningful in warp 0
+}
+
+__global__ void __launch_bounds__(kFinRows * kFinSplit)
+    flce_finalize(const float* pm, const float* ps, const float* pz, const int64_t* target, int64_t T,
+                  int64_t V, int num_n, float* row_out, float* loss, Ctrl* ctrl) {
+  __shared__ MS s_tmp[kFinRows * kFinSplit];
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kFinRows + (threadIdx.x & 31);
+  const float lse = merge_lse_row(pm, ps, T, num_n, row, s_tmp);
+  if (threadIdx.x < 32 && row < T) {
+    const int64_t t = __ldg(target + row);
+    float zt = __int_as_float(0x7FC00000);
+    if (t >= 0 && t < V) zt = __ldcg(pz + (t / kBN_CE) * T + row);
+    row_out[row] = lse - zt;
+  }
+  mean_tail(row_out, T, loss, ctrl, gridDim.x);
+}
+
+__global__ void __launch_bounds__(kFinRows * kFinSplit)
+    lse_finalize(const float* pm, const float* ps, int64_t T, int num_n, float* lse_out) {
+  __shared__ MS s_tmp[kFinRows * kFinSplit];
+  const int head = blockIdx.y;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kFinRows + (threadIdx.x & 31);
+  const int64_t hoff = static_cast<int64_t>(head) * num_n * T;
+  const float lse = merge_lse_row(pm + hoff, ps + hoff, T, num_n, row, s_tmp);
+  if (threadIdx.x < 32 && row < T) lse_out[head * T + row] = lse;
+}
+
+__global__ void __launch_bounds__(kFinRows * kFinSplit)
+    jsd_finalize(const float* pj, int64_t T, int num_n, float* row_out, float* loss, Ctrl* ctrl) {
+  __shared__ double s_tmp[kFinRows * kFinSplit];
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kFinRows + l;
+  const int cnt = (num_n + kFinSplit - 1) / kFinSplit;
+  const int n_lo = min(num_n, w * cnt), n_hi = min(num_n, n_lo + cnt);
+  double a = 0.0;
+  if (row < T)
+    for (int n = n_lo; n < n_hi; ++n) a += static_cast<double>(__ldcg(pj + static_cast<int64_t>(n) * T + row));
+  s_tmp[w * 32 + l] = a;
+  __syncthreads();
+  if (w == 0 && row < T) {
+    double tot = 0.0;
+    for (int k = 0; k < kFinSplit; ++k) tot += s_tmp[k * 32 + l];
+    row_out[row] = static_cast<float>(tot);
+  }
+  mean_tail(row_out, T, loss, ctrl, gridDim.x);
+}
+
+__global__ void wait_selftest_kernel(Ctrl* ctrl, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    // Nothing ever arrives on `bar`: the bounded wait must give up and report.
+    mbar_wait(&bar, 0, timeout_ns, &ctrl->status);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
+                        const CUtensorMap& b1, const Params& p, const FusedLaunch& L) {
+  using C = ModeCfg<MODE>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fused_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int64_t grid = p.units < L.num_sms ? p.units : L.num_sms;
+  fused_gemm_kernel<MODE><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, L.stream>>>(a0, b0, a1, b1, p);
+  return cudaGetLastError();
+}
+
+Params base_params(const FusedGeometry& g, const FusedLaunch& L, Ctrl* ctrl) {
+  Params p{};
+  p.T = g.T;
+  p.V = g.V;
+  p.num_m = static_cast<int32_t>(g.num_m);
+  p.num_n = static_cast<int32_t>(g.num_n);
+  p.group_m = g.group_m;
+  p.k_blocks = static_cast<int32_t>((g.H + kBK - 1) / kBK);
+  p.timeout_ns = L.timeout_ns;
+  p.status = &ctrl->status;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_flce(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const int64_t* target,
+                        const FusedGeometry& g, float* loss, const FusedWs& ws, const FusedLaunch& L) {
+  Params p = base_params(g, L, ws.ctrl);
+  p.units = g.num_m * g.num_n;
+  p.target = target;
+  p.part0 = ws.part0;
+  p.part1 = ws.part1;
+  p.part2 = ws.part2;
+  launch_mark(0, L.stream);
+  cudaError_t e = launch_gemm<kModeCE>(tm_x, tm_w, tm_x, tm_w, p, L);
+  if (e != cudaSuccess) return e;
+  launch_mark(1, L.stream);
+  const unsigned blocks = static_cast<unsigned>((g.T + kFinRows - 1) / kFinRows);
+  flce_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, ws.part1, ws.part2, target, g.T, g.V,
+                                                               static_cast<int>(g.num_n), ws.row_out, loss, ws.ctrl);
+  launch_mark(2, L.stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, const CUtensorMap& tm_xt,
+                         const CUtensorMap& tm_wt256, const CUtensorMap& tm_ws128, const CUtensorMap& tm_wt128,
+                         const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta, float* loss,
+                         const FusedWs& ws, const FusedLaunch& L) {
+  // pass 1: log-sum-exp of both heads
+  Params p = base_params(g_lse, L, ws.ctrl);
+  p.units = 2 * g_lse.num_m * g_lse.num_n;
+  p.part0 = ws.part0;
+  p.part1 = ws.part1;
+  launch_mark(0, L.stream);
+  cudaError_t e = launch_gemm<kModeLSE>(tm_xs, tm_ws256, tm_xt, tm_wt256, p, L);
+  if (e != cudaSuccess) return e;
+  launch_mark(1, L.stream);
+  dim3 fb(static_cast<unsigned>((g_lse.T + kFinRows - 1) / kFinRows), 2);
+  lse_finalize<<<fb, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, ws.part1, g_lse.T, static_cast<int>(g_lse.num_n),
+                                                          ws.lse);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  launch_mark(2, L.stream);
+  // pass 2: recompute both heads' tiles, accumulate the divergence
+  Params q = base_params(g_jsd, L, ws.ctrl);
+  q.units = g_jsd.num_m * g_jsd.num_n;
+  q.part0 = ws.part0;
+  q.lse = ws.lse;
+  q.beta = beta;
+  e = launch_gemm<kModeJSD>(tm_xs, tm_ws128, tm_xt, tm_wt128, q, L);
+  if (e != cudaSuccess) return e;
+  launch_mark(3, L.stream);
+  const unsigned blocks = static_cast<unsigned>((g_jsd.T + kFinRows - 1) / kFinRows);
+  jsd_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, g_jsd.T, static_cast<int>(g_jsd.num_n),
+                                                              ws.row_out, loss, ws.ctrl);
+  launch_mark(4, L.stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(Ctrl* ctrl, uint64_t timeout_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(ctrl, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace lmho

@@ -1,0 +1,79 @@
+// Internal launch interface between the C ABI (abi.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace lmho {
+
+struct Ctrl;
+
+// ---------------------------------------------------------------- CE rows
+enum CeVariant { kCeWarp = 0, kCeCta = 1, kCeCluster = 2 };
+struct CeConfig {
+  int variant;   // CeVariant
+  int threads;   // CTA size of the CTA-per-row kernel (256 or 512)
+  int cluster;   // CTAs per row of the cluster kernel (2, 4 or 8)
+};
+
+cudaError_t launch_ce_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
+                          float* loss, float* row_loss, Ctrl* ctrl, const CeConfig& cfg,
+                          cudaStream_t st);
+cudaError_t launch_ce_bf16_rows(const uint16_t* logits, const int64_t* target, int64_t rows,
+                                int64_t V, float* loss_rows, const CeConfig& cfg, cudaStream_t st);
+
+// ---------------------------------------------------------------- fused linear
+// Tile geometry of the tensor-core kernels.
+constexpr int kBM = 128;        // token rows per tile (TMEM lanes)
+constexpr int kBK = 64;         // hidden elements per pipeline stage (one 128-byte swizzle row)
+constexpr int kBN_CE = 256;     // vocab columns per tile, single-head passes
+constexpr int kBN_JSD = 128;    // vocab columns per head per tile, two-head pass
+
+struct FusedGeometry {
+  int64_t T, H, V;
+  int64_t num_m, num_n;   // tiles along tokens and vocab
+  int group_m;            // m-tiles per raster group (L2 reuse of W)
+};
+
+// Workspace carve-up of the fused paths (all offsets 256-byte aligned).
+struct FusedWs {
+  float* row_out;     // [T] per-token loss / JSD (first bytes of ws, documented)
+  float* part0;       // [heads][num_n][T]  running max, or JSD partial sums
+  float* part1;       // [heads][num_n][T]  running sum of exp
+  float* part2;       // [num_n][T]         target logit (CE) / unused
+  float* lse;         // [2][T]             log-sum-exp of student, teacher (JSD)
+  Ctrl* ctrl;         // last 256 bytes
+};
+
+size_t flce_ws_bytes(int64_t T, int64_t H, int64_t V);
+size_t fljsd_ws_bytes(int64_t T, int64_t H, int64_t V);
+FusedWs flce_ws_carve(void* ws, size_t ws_bytes, int64_t T, int64_t V);
+FusedWs fljsd_ws_carve(void* ws, size_t ws_bytes, int64_t T, int64_t V);
+
+struct FusedLaunch {
+  int num_sms;
+  uint64_t timeout_ns;
+  cudaStream_t stream;
+};
+
+// x [T,H], W [V,H] -> loss[1]; tensor maps built by the caller.
+cudaError_t launch_flce(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const int64_t* target,
+                        const FusedGeometry& g, float* loss, const FusedWs& ws,
+                        const FusedLaunch& L);
+// Student/teacher head maps come twice: 256-row boxes for the log-sum-exp
+// pass and 128-row boxes for the two-head divergence pass.
+cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256,
+                         const CUtensorMap& tm_xt, const CUtensorMap& tm_wt256,
+                         const CUtensorMap& tm_ws128, const CUtensorMap& tm_wt128,
+                         const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta,
+                         float* loss, const FusedWs& ws, const FusedLaunch& L);
+
+// Records the caller's measurement event `i` on `st` if the hook is set
+// (lmho_set_launch_events); no-op otherwise.
+void launch_mark(int i, cudaStream_t st);
+
+cudaError_t launch_wait_selftest(Ctrl* ctrl, uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace lmho
