@@ -54,6 +54,12 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--case", choices=["ce", "sbv", "flce", "fljsd"],
+                    help="time one op alone at --T/--V/--H (profiling runs); prints one JSON line")
+    ap.add_argument("--T", type=int, default=None, help="tokens (ce: rows; sbv: seq, batch 4)")
+    ap.add_argument("--V", type=int, default=None)
+    ap.add_argument("--H", type=int, default=4096)
+    ap.add_argument("--ce-variant", default="auto")
     return ap.parse_args()
 
 
@@ -356,10 +362,12 @@ def oracle_samples(seed=0, h=None, budget_s=12.0):
     import gen
     cores = os.cpu_count() or 1
     f = budget_s / 12.0
-    n_ce = max(cores, int(1024 * f)) // cores * cores
-    n_sbv = max(cores, int(2048 * f)) // cores * cores
-    n_fl = max(1, int(cores * f))
-    n_js = max(1, int(cores * f / 2))
+    # sized for ~10 s of host time at budget_s = 12 on 16 cores (CE rows cost
+    # ~1.5 ms each per thread, fused tokens ~0.3 s (CE) / 0.6 s (JSD) per thread)
+    n_ce = min(CE["T"], max(cores, int(16384 * f)))
+    n_sbv = min(SBV["S"] * SBV["B"], max(cores, int(8192 * f)))
+    n_fl = max(1, int(8 * cores * f))
+    n_js = max(1, int(3 * cores * f))
 
     def np_bits(t):
         import torch
@@ -443,8 +451,73 @@ def run_reference(args):
             "gpu_launches": 0}
 
 
+def run_case(args):
+    """One op alone, `warmup` untimed + `steps` timed calls (CUDA events on
+    the launching stream).  Used for ncu captures on small cases."""
+    import torch
+    import gen
+    import lm_head_online_gb300 as lmho
+    torch.cuda.set_device(0)
+    lmho.load()
+    lmho.set_ce_variant(args.ce_variant)
+    thr = os.cpu_count() or 1
+
+    def bf16(seed, stream, shape, sigma):
+        t = torch.empty(shape, dtype=torch.bfloat16)
+        gen.normal_bf16_bits(seed, stream, shape, sigma, out=t.view(torch.int16), threads=thr)
+        return t.cuda()
+
+    def targets(shape, V):
+        return torch.from_numpy(gen.targets(args.seed, gen.STREAM_TARGET, shape, V, threads=thr)).cuda()
+
+    c, H = args.case, args.H
+    if c == "ce":
+        T, V = args.T or CE["T"], args.V or CE["V"]
+        z = torch.from_numpy(gen.normal_f32(args.seed, 0, (T, V), threads=thr)).cuda()
+        t = targets((T,), V)
+        ws = lmho.workspace(lmho.ce_workspace_bytes(T, V))
+        fn = lambda: lmho.ce_fwd_f32(z, t, ws=ws)  # noqa: E731
+        work, unit = rl.ce_flat_bytes(T, V), "GB/s"
+    elif c == "sbv":
+        S, V = args.T or SBV["S"], args.V or SBV["V"]
+        z = bf16(args.seed, 0, (S, 4, V), 2.0)
+        t = targets((S, 4), V)
+        fn = lambda: lmho.ce_fwd_sbv_bf16(z, t)  # noqa: E731
+        work, unit = rl.ce_sbv_bytes(S, 4, V), "GB/s"
+    elif c == "flce":
+        T, V = args.T or FLCE["T"], args.V or FLCE["V"]
+        x, W, t = bf16(args.seed, 0, (T, H), 1.0), bf16(args.seed, 2, (V, H), 0.02), targets((T,), V)
+        ws = lmho.workspace(lmho.flce_workspace_bytes(T, H, V))
+        fn = lambda: lmho.flce_fwd_bf16(x, W, t, ws=ws)  # noqa: E731
+        work, unit = rl.flce_flops(T, H, V), "TFLOP/s"
+    else:
+        T, V = args.T or FLJSD["T"], args.V or FLJSD["V"]
+        xs, Ws = bf16(args.seed, 0, (T, H), 1.0), bf16(args.seed, 2, (V, H), 0.02)
+        xt, Wt = bf16(args.seed, 3, (T, H), 1.0), bf16(args.seed, 4, (V, H), 0.02)
+        ws = lmho.workspace(lmho.fljsd_workspace_bytes(T, H, V))
+        fn = lambda: lmho.fljsd_fwd_bf16(xs, Ws, xt, Wt, 0.5, ws=ws)  # noqa: E731
+        work, unit = rl.fljsd_flops(T, H, V), "TFLOP/s"
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record()
+    for i in range(args.steps):
+        fn()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    med = float(np.median(ms))
+    rate = work / (med * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
+    return {"case": c, "T": args.T, "V": args.V, "H": H, "ce_variant": args.ce_variant, "us_median": round(med * 1e3, 2),
+            "us_all": [round(m * 1e3, 2) for m in ms], unit: round(rate, 1)}
+
+
 def main():
     args = parse()
+    if args.case:
+        print(json.dumps(run_case(args)), flush=True)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
