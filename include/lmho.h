@@ -78,6 +78,30 @@ int ce_fwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
                float* loss, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * ce_fwd_f32 without a caller workspace, for callers that cannot allocate
+ * device memory (e.g. while a CUDA graph is being captured, or under a fixed
+ * device-memory budget owned by someone else).  The operation pages have no
+ * counterpart of this entry point: it is a library convenience.
+ *
+ * Same operation, arguments, result and kernels as ce_fwd_f32, except that
+ * the per-token losses and the control words live in a scratch array inside
+ * the library: a file-scope __device__ array of 256 KB + 256 bytes that every
+ * GPU which loads the library holds until the process exits.
+ *   - T is limited to 65536 tokens; larger T returns LMHO_ERR_INVALID_ARG.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating routine.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture on that device.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents; each call first clears the control words it needs at
+ *     zero (one cudaMemsetAsync on `stream`, then one kernel).  Calls that
+ *     overlap on the GPU (other streams, other threads) race on the array and
+ *     give undefined results: serialise them.
+ * ------------------------------------------------------------------------ */
+int ce_fwd_f32_noalloc(const float* logits, const int64_t* target, int64_t T, int64_t V,
+                       float* loss, void* stream);
+
+/* ------------------------------------------------------------------------
  * Megatron-layout cross-entropy, bf16 logits, per-token fp32 losses.
  * Page "Vocab-parallel cross-entropy, Megatron layout", summary (bf16 logits,
  * per-token fp32 losses, tensor parallel size 1) and section Semantics:

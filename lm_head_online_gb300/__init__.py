@@ -31,7 +31,7 @@ LMHO_ERR_TIMEOUT = 6
 
 # Every symbol declared in include/lmho.h.
 EXPORTS = (
-    "lmho_strerror", "lmho_version", "ce_workspace_bytes", "ce_fwd_f32", "ce_fwd_sbv_bf16",
+    "lmho_strerror", "lmho_version", "ce_workspace_bytes", "ce_fwd_f32", "ce_fwd_f32_noalloc", "ce_fwd_sbv_bf16",
     "flce_workspace_bytes", "flce_fwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16",
     "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
@@ -66,6 +66,8 @@ def load():
         lib.ce_workspace_bytes.restype = sz
         lib.ce_fwd_f32.argtypes = [vp, vp, i64, i64, vp, vp, sz, vp]
         lib.ce_fwd_f32.restype = ci
+        lib.ce_fwd_f32_noalloc.argtypes = [vp, vp, i64, i64, vp, vp]
+        lib.ce_fwd_f32_noalloc.restype = ci
         lib.ce_fwd_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, vp, vp]
         lib.ce_fwd_sbv_bf16.restype = ci
         lib.flce_workspace_bytes.argtypes = [i64, i64, i64]
@@ -157,6 +159,23 @@ def ce_fwd_f32(logits, target, loss=None, ws=None, stream=None):
         ws = workspace(lib.ce_workspace_bytes(T, V), logits.device)
     _check(lib.ce_fwd_f32(pl, pt, T, V, _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8),
                           ws.numel(), _stream(stream)), "ce_fwd_f32")
+    return loss
+
+
+def ce_fwd_f32_noalloc(logits, target, loss, stream=None):
+    """ce_fwd_f32 for callers that cannot allocate device memory: no
+    workspace argument, the library's own scratch (at most 65536 tokens) is
+    used instead.  ``loss`` (fp32 [1], on the device) must be supplied by the
+    caller, since this call allocates nothing.  Calls that overlap on the GPU
+    share the scratch and race: serialise them."""
+    lib = load()
+    pl = _dev(logits, "logits", torch.float32, 2)
+    T, V = logits.shape
+    pt = _dev(target, "target", torch.int64, 1)
+    if target.shape[0] != T:
+        raise ValueError("target must have T entries")
+    _check(lib.ce_fwd_f32_noalloc(pl, pt, T, V, _dev(loss, "loss", torch.float32), _stream(stream)),
+           "ce_fwd_f32_noalloc")
     return loss
 
 
