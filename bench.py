@@ -500,16 +500,25 @@ def run_case(args):
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    evs[0].record()
+    # L2 is flushed before every timed call, outside the events, by READING a
+    # 512 MB buffer: small cases would otherwise find their inputs in the
+    # 129 MB L2, and a write-based flush would leave ~129 MB of dirty lines
+    # whose write-back the timed kernel would pay for.
+    flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
+    sink = torch.empty((), dtype=torch.float32, device="cuda")
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for i in range(args.steps):
+        torch.sum(flush, out=sink)
+        ev0[i].record()
         fn()
-        evs[i + 1].record()
+        ev1[i].record()
     torch.cuda.synchronize()
-    ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    ms = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
     med = float(np.median(ms))
     rate = work / (med * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
-    return {"case": c, "T": args.T, "V": args.V, "H": H, "ce_variant": args.ce_variant, "us_median": round(med * 1e3, 2),
+    return {"case": c, "T": args.T, "V": args.V, "H": H, "ce_variant": args.ce_variant, "l2": "flushed (512 MB read) before each call",
+            "us_median": round(med * 1e3, 2),
             "us_all": [round(m * 1e3, 2) for m in ms], unit: round(rate, 1)}
 
 

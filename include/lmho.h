@@ -171,13 +171,17 @@ int fljsd_fwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt,
 int lmho_ws_status(void* ws, size_t ws_bytes, void* stream);
 
 /* Row decomposition of the two cross-entropy calls, process-wide:
- *   0 = automatic (default: warp per row for rows <= 16 KB, a cluster of 8
- *       CTAs per row when rows are few and >= 64 KB, else a CTA per row),
+ *   0 = automatic (default): the bulk-copy ring for rows of at most 32 KB
+ *       whose start and length are multiples of 16 bytes; otherwise a warp
+ *       per row for rows <= 16 KB, a cluster of 8 CTAs per row when rows are
+ *       few and >= 64 KB, else a CTA per row;
  *   1 = warp per row, 2 = CTA (256 threads) per row, 3 = CTA (512) per row,
- *   4 / 5 / 6 = cluster of 2 / 4 / 8 CTAs per row (DSMEM merge).
+ *   4 / 5 / 6 = cluster of 2 / 4 / 8 CTAs per row (DSMEM merge),
+ *   7 = bulk-copy ring (rows up to 100 KB, 16-byte aligned; other rows fall
+ *       back to a CTA per row).
  * Results agree to rounding whichever is chosen.  Returns LMHO_ERR_INVALID_ARG
  * for other values.  The environment variable LMHO_CE_VARIANT (warp, cta,
- * cta512, cluster2, cluster4, cluster8) sets the initial value. */
+ * cta512, cluster2, cluster4, cluster8, bulk) sets the initial value. */
 int lmho_set_ce_variant(int variant);
 
 /* Measurement hook, process-wide and not thread-safe: while set, every call

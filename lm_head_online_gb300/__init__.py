@@ -19,7 +19,8 @@ import threading
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "_build", "liblmho.so")
+# LMHO_LIB overrides the library path (to compare builds of the same sources).
+LIB_PATH = os.environ.get("LMHO_LIB") or os.path.join(HERE, "_build", "liblmho.so")
 
 LMHO_OK = 0
 LMHO_ERR_INVALID_ARG = 1
@@ -36,7 +37,7 @@ EXPORTS = (
     "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
 
-CE_VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "cta512": 3, "cluster2": 4, "cluster4": 5, "cluster8": 6}
+CE_VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "cta512": 3, "cluster2": 4, "cluster4": 5, "cluster8": 6, "bulk": 7}
 
 _lock = threading.Lock()
 _lib = None
@@ -253,7 +254,7 @@ def ws_status(ws, stream=None) -> int:
 
 
 def set_ce_variant(name: str):
-    """Row decomposition of the CE calls: auto, warp, cta, cta512, cluster2/4/8."""
+    """Row decomposition of the CE calls: auto, warp, cta, cta512, cluster2/4/8, bulk."""
     _check(load().lmho_set_ce_variant(CE_VARIANTS[name]), "lmho_set_ce_variant")
 
 

@@ -84,28 +84,46 @@ inline Ctrl* ctrl_of(void* ws, size_t ws_bytes) {
 int env_ce_variant() {
   const char* s = std::getenv("LMHO_CE_VARIANT");
   if (!s) return 0;
-  const char* names[] = {"warp", "cta", "cta512", "cluster2", "cluster4", "cluster8"};
-  for (int i = 0; i < 6; ++i)
+  const char* names[] = {"warp", "cta", "cta512", "cluster2", "cluster4", "cluster8", "bulk"};
+  for (int i = 0; i < 7; ++i)
     if (!std::strcmp(s, names[i])) return i + 1;
   return 0;
 }
 std::atomic<int> g_ce_variant{env_ce_variant()};
 
-CeConfig choose_ce(int64_t rows, int64_t V, size_t elt, int num_sms) {
+// Rows the bulk-copy ring can take: whole 16-byte vectors, 16-byte aligned
+// start, two stages in the ring.
+bool bulk_ok(const void* base, int64_t V, size_t elt) {
+  const uint64_t row_bytes = static_cast<uint64_t>(V) * elt;
+  return (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && row_bytes % 16 == 0 && row_bytes <= kCeBulkMaxRow;
+}
+
+CeConfig choose_ce(const void* base, int64_t rows, int64_t V, size_t elt, int num_sms) {
+  CeConfig c{kCeCta, 256, 1};
+  c.num_sms = num_sms;
+  c.timeout_ns = g_timeout_ns.load();
+  const int64_t row_bytes = V * static_cast<int64_t>(elt);
   switch (g_ce_variant.load()) {
-    case 1: return CeConfig{kCeWarp, 256, 1};
-    case 2: return CeConfig{kCeCta, 256, 1};
-    case 3: return CeConfig{kCeCta, 512, 1};
-    case 4: return CeConfig{kCeCluster, 256, 2};
-    case 5: return CeConfig{kCeCluster, 256, 4};
-    case 6: return CeConfig{kCeCluster, 256, 8};
+    case 1: c.variant = kCeWarp; return c;
+    case 2: return c;
+    case 3: c.threads = 512; return c;
+    case 4: c.variant = kCeCluster; c.cluster = 2; return c;
+    case 5: c.variant = kCeCluster; c.cluster = 4; return c;
+    case 6: c.variant = kCeCluster; c.cluster = 8; return c;
+    case 7:
+      if (bulk_ok(base, V, elt)) c.variant = kCeBulk;   // else: CTA per row
+      return c;
     default: break;
   }
-  const int64_t row_bytes = V * static_cast<int64_t>(elt);
-  if (row_bytes <= 16 * 1024) return CeConfig{kCeWarp, 256, 1};
-  // Few long rows: split each row over a cluster so every SM streams.
-  if (rows < 4 * static_cast<int64_t>(num_sms) && row_bytes >= 64 * 1024) return CeConfig{kCeCluster, 256, 8};
-  return CeConfig{kCeCta, 256, 1};
+  if (bulk_ok(base, V, elt) && row_bytes <= 32 * 1024) {
+    c.variant = kCeBulk;
+  } else if (row_bytes <= 16 * 1024) {
+    c.variant = kCeWarp;
+  } else if (rows < 4 * static_cast<int64_t>(num_sms) && row_bytes >= 64 * 1024) {
+    c.variant = kCeCluster;   // few long rows: split each row over a cluster
+    c.cluster = 8;
+  }
+  return c;
 }
 
 // ---------------------------------------------------------------- TMA maps
@@ -188,15 +206,20 @@ FusedWs flce_ws_carve(void* ws, size_t ws_bytes, int64_t T, int64_t V) {
   w.ctrl = ctrl_of(ws, ws_bytes);
   return w;
 }
+// Partials: the log-sum-exp pass writes (max, sum) per (head, 256-wide vocab
+// tile); the divergence pass writes one sum per (kBN_JSD-wide vocab tile,
+// epilogue column slice).  part0 serves both passes.
 size_t fljsd_ws_bytes(int64_t T, int64_t H, int64_t V) {
   (void)H;
-  const int64_t n256 = (V + kBN_CE - 1) / kBN_CE, n128 = (V + kBN_JSD - 1) / kBN_JSD;
-  const int64_t p0 = (2 * n256 > n128 ? 2 * n256 : n128) * T;
+  const int64_t n256 = (V + kBN_CE - 1) / kBN_CE;
+  const int64_t njsd = (V + kBN_JSD - 1) / kBN_JSD * kJsdColSplit;
+  const int64_t p0 = (2 * n256 > njsd ? 2 * n256 : njsd) * T;
   return align_up(4 * T) + align_up(4 * p0) + align_up(4 * 2 * n256 * T) + align_up(4 * 2 * T) + kAlign;
 }
 FusedWs fljsd_ws_carve(void* ws, size_t ws_bytes, int64_t T, int64_t V) {
-  const int64_t n256 = (V + kBN_CE - 1) / kBN_CE, n128 = (V + kBN_JSD - 1) / kBN_JSD;
-  const int64_t p0 = (2 * n256 > n128 ? 2 * n256 : n128) * T;
+  const int64_t n256 = (V + kBN_CE - 1) / kBN_CE;
+  const int64_t njsd = (V + kBN_JSD - 1) / kBN_JSD * kJsdColSplit;
+  const int64_t p0 = (2 * n256 > njsd ? 2 * n256 : njsd) * T;
   char* p = static_cast<char*>(ws);
   FusedWs w{};
   w.row_out = reinterpret_cast<float*>(p);
@@ -241,7 +264,7 @@ void lmho_set_launch_events(void* const* events, int n) {
 }
 
 int lmho_set_ce_variant(int variant) {
-  if (variant < 0 || variant > 6) return LMHO_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 7) return LMHO_ERR_INVALID_ARG;
   g_ce_variant.store(variant);
   return LMHO_OK;
 }
@@ -264,7 +287,7 @@ int ce_fwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
   if (int a = check_alias(in, 2, out, 2)) return a;
   int sms = 0;
   if (int d = current_device(&sms)) return d;
-  const CeConfig cfg = choose_ce(T, V, 4, sms);
+  const CeConfig cfg = choose_ce(logits, T, V, 4, sms);
   return cuda_status(launch_ce_f32(logits, target, T, V, loss, static_cast<float*>(ws), ctrl_of(ws, ws_bytes), cfg,
                                    static_cast<cudaStream_t>(stream)));
 }
@@ -280,7 +303,7 @@ int ce_fwd_sbv_bf16(const uint16_t* logits, const int64_t* target, int64_t S, in
   if (int a = check_alias(in, 2, out, 1)) return a;
   int sms = 0;
   if (int d = current_device(&sms)) return d;
-  const CeConfig cfg = choose_ce(rows, V, 2, sms);
+  const CeConfig cfg = choose_ce(logits, rows, V, 2, sms);
   return cuda_status(launch_ce_bf16_rows(logits, target, rows, V, loss, cfg, static_cast<cudaStream_t>(stream)));
 }
 
@@ -329,15 +352,15 @@ int fljsd_fwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, c
   int sms = 0;
   if (int d = current_device(&sms)) return d;
   if (int e = get_encode()) return e;
-  CUtensorMap txs, txt, tws256, twt256, tws128, twt128;
+  CUtensorMap txs, txt, tws256, twt256, twsj, twtj;
   if (tmap_bf16(&txs, xs, T, H, kBM) || tmap_bf16(&txt, xt, T, H, kBM) || tmap_bf16(&tws256, Ws, V, H, kBN_CE) ||
-      tmap_bf16(&twt256, Wt, V, H, kBN_CE) || tmap_bf16(&tws128, Ws, V, H, kBN_JSD) ||
-      tmap_bf16(&twt128, Wt, V, H, kBN_JSD))
+      tmap_bf16(&twt256, Wt, V, H, kBN_CE) || tmap_bf16(&twsj, Ws, V, H, kBN_JSD) ||
+      tmap_bf16(&twtj, Wt, V, H, kBN_JSD))
     return LMHO_ERR_CUDA;
   const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD);
   const FusedWs w = fljsd_ws_carve(ws, ws_bytes, T, V);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
-  return cuda_status(launch_fljsd(txs, tws256, txt, twt256, tws128, twt128, g1, g2, beta, loss, w, L));
+  return cuda_status(launch_fljsd(txs, tws256, txt, twt256, twsj, twtj, g1, g2, beta, loss, w, L));
 }
 
 int lmho_ws_status(void* ws, size_t ws_bytes, void* stream) {

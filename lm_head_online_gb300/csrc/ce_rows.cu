@@ -15,7 +15,13 @@
 //   * warp per row   -- small rows; no shared memory, no block barrier;
 //   * CTA per row    -- mid/large rows; warp shuffles, then shared memory;
 //   * cluster per row -- C CTAs split the row, each merges its share, and CTA 0
-//     merges the C partials read from its peers' shared memory (DSMEM).
+//     merges the C partials read from its peers' shared memory (DSMEM);
+//   * bulk-copy ring -- rows up to 100 KB whose bytes are 16-byte aligned: one
+//     persistent CTA per SM, a producer thread copies whole rows with
+//     cp.async.bulk (1-D TMA) into a ring of shared-memory stages (mbarrier
+//     complete_tx), and 8 consumer warps each fold whole rows out of shared
+//     memory.  Memory-level parallelism is the ring (~200 KB per SM in
+//     flight), not registers, so short rows stream at full bandwidth.
 // The flat variant's mean is a deterministic two-level sum: per-token losses
 // go to the workspace, and the last block to finish (atomic ticket, no spin)
 // sums them in a fixed order in fp64.
@@ -34,6 +40,7 @@ template <typename T> struct Elt;
 template <> struct Elt<float> {
   static constexpr int kPerVec = 4;  // elements per 16-byte vector
   __device__ static float load1(const float* p) { return __ldg(p); }
+  __device__ static float load_any(const float* p) { return *p; }
   __device__ static void unpack(const uint4& r, float* v) {
     v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
     v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
@@ -44,6 +51,7 @@ template <> struct Elt<uint16_t> {  // bf16 bit patterns
   __device__ static float load1(const uint16_t* p) {
     return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
   }
+  __device__ static float load_any(const uint16_t* p) { return __uint_as_float(static_cast<uint32_t>(*p) << 16); }
   __device__ static void unpack(const uint4& r, float* v) {
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
@@ -207,6 +215,95 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT)
   if (mean_out && rank == 0) mean_tail(out_rows, rows, mean_out, ctrl, gridDim.x / C);
 }
 
+// Persistent bulk-copy ring: item i of this CTA is row blockIdx.x + i*gridDim.x,
+// held in stage i % stages and folded by consumer warp i % nwa, where nwa (the
+// active consumer warps) divides `stages`.  So each stage has ONE owner warp,
+// which waits on that stage's barrier fill after fill, in order: a parity wait
+// is only unambiguous when its waiter is never more than one phase ahead.
+// Every wait is bounded; a warp that gives up writes NaN for its remaining
+// rows and records the timeout when a status word exists.
+template <typename T, int NW>
+__global__ void __launch_bounds__(32 * (NW + 1), 1)
+    ce_bulk_rows(const T* __restrict__ logits, const int64_t* __restrict__ target, int64_t rows, int64_t V,
+                 float* __restrict__ out_rows, float* mean_out, Ctrl* ctrl, int stages, int nwa,
+                 uint32_t stage_bytes, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(stages) * stage_bytes);
+  uint64_t* empty = full + stages;
+  uint32_t* status = ctrl ? &ctrl->status : nullptr;
+  const uint32_t row_bytes = static_cast<uint32_t>(V * sizeof(T));
+  const int64_t n_items = (rows - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t filled = 0, last_parity = 0;  // stages <= 32
+      for (int64_t i = 0; i < n_items; ++i) {
+        const int s = static_cast<int>(i % stages);
+        const uint32_t k = static_cast<uint32_t>(i / stages);
+        if (!mbar_wait(&empty[s], (k & 1u) ^ 1u, timeout_ns, status)) break;
+        const int64_t r = blockIdx.x + i * gridDim.x;
+        mbar_arrive_expect_tx(&full[s], row_bytes);
+        bulk_load(ring + static_cast<size_t>(s) * stage_bytes, logits + r * V, row_bytes, &full[s]);
+        filled |= 1u << s;
+        last_parity = (last_parity & ~(1u << s)) | ((k & 1u) << s);
+      }
+      // never leave with copies in flight
+      for (int s = 0; s < stages; ++s)
+        if (filled & (1u << s)) mbar_wait(&full[s], (last_parity >> s) & 1u, timeout_ns, status);
+    }
+  } else {
+    constexpr int E = Elt<T>::kPerVec;
+    const int nvec = static_cast<int>(row_bytes / 16);
+    for (int64_t i = warp - 1; warp - 1 < nwa && i < n_items; i += nwa) {
+      const int s = static_cast<int>(i % stages);
+      const uint32_t k = static_cast<uint32_t>(i / stages);
+      const int64_t r = blockIdx.x + i * gridDim.x;
+      const int64_t t = __ldg(target + r);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], k & 1u, timeout_ns, status))) {
+        for (int64_t j = i; j < n_items; j += nwa)
+          if (lane == 0) out_rows[blockIdx.x + j * gridDim.x] = __int_as_float(0x7FC00000);
+        break;
+      }
+      const uint8_t* row = ring + static_cast<size_t>(s) * stage_bytes;
+      const uint4* vec = reinterpret_cast<const uint4*>(row);
+      MS a = ms_empty();
+      int q = lane;
+      for (; q + 96 < nvec; q += 128) {
+        uint4 rr[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) rr[u] = vec[q + 32 * u];
+        float v[4 * E];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) Elt<T>::unpack(rr[u], v + u * E);
+        ms_fold<4 * E>(a, v);
+      }
+      for (; q < nvec; q += 32) {
+        float v[E];
+        Elt<T>::unpack(vec[q], v);
+        ms_fold<E>(a, v);
+      }
+      a = ms_warp_allreduce(a);
+      if (lane == 0) {
+        const float zt = (t >= 0 && t < V) ? Elt<T>::load_any(reinterpret_cast<const T*>(row) + t)
+                                           : __int_as_float(0x7FC00000);
+        out_rows[r] = finish_loss(a, zt);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+  if (mean_out) mean_tail(out_rows, rows, mean_out, ctrl, gridDim.x);
+}
+
 template <typename T>
 cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, int64_t V,
                         float* out_rows, float* mean_out, Ctrl* ctrl, const CeConfig& cfg,
@@ -227,6 +324,28 @@ cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, in
         ce_cta_rows<T, 4, 256><<<static_cast<unsigned>(rows), 256, 0, st>>>(logits, target, rows, V,
                                                                              out_rows, mean_out, ctrl);
       break;
+    case kCeBulk: {
+      const uint32_t row_bytes = static_cast<uint32_t>(V * sizeof(T));
+      const uint32_t stage_bytes = (row_bytes + 127) / 128 * 128;
+      int stages = static_cast<int>(kCeBulkRingBytes / stage_bytes);
+      if (stages > 32) stages = 32;
+      const int nwa = stages < 8 ? stages : 8;   // active consumer warps
+      stages = stages / nwa * nwa;               // each stage owned by one warp
+      const size_t smem = static_cast<size_t>(stages) * stage_bytes + 128 + 16 * stages;
+      static bool attr[64] = {};
+      int dev = 0;
+      cudaGetDevice(&dev);
+      if (dev < 64 && !attr[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(ce_bulk_rows<T, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kCeBulkRingBytes + 128 + 16 * 32));
+        if (e != cudaSuccess) return e;
+        attr[dev] = true;
+      }
+      const int64_t grid = rows < cfg.num_sms ? rows : cfg.num_sms;
+      ce_bulk_rows<T, 8><<<static_cast<unsigned>(grid), 32 * 9, smem, st>>>(logits, target, rows, V, out_rows, mean_out,
+                                                                           ctrl, stages, nwa, stage_bytes, cfg.timeout_ns);
+      break;
+    }
     case kCeCluster: {
       const unsigned grid = static_cast<unsigned>(rows * cfg.cluster);
       if (cfg.cluster == 2)

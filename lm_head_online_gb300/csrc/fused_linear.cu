@@ -45,22 +45,27 @@ namespace {
 
 enum Mode { kModeCE = 0, kModeLSE = 1, kModeJSD = 2 };
 
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, 4 epilogue warps
-constexpr int kTmemCols = 512;                  // two accumulators of 256 columns
-constexpr int kAccCols = 256;
+constexpr int kTmemCols = 512;   // all of TMEM: accumulators of 256 or 512 fp32 columns
 constexpr int kSmemBudget = 192 * 1024;
 
 template <int MODE>
 struct ModeCfg {
   static constexpr int BN = (MODE == kModeJSD) ? kBN_JSD : kBN_CE;
   static constexpr int kHeadsPerUnit = (MODE == kModeJSD) ? 2 : 1;
+  static constexpr int kAccCols = BN * kHeadsPerUnit;      // TMEM columns of one accumulator
+  static constexpr int kNumAcc = kTmemCols / kAccCols;     // 2 = double-buffered, 1 = single
+  // Epilogue warps: 4 cover the 128 TMEM lanes; 8 = two per lane quadrant,
+  // each taking half of the columns (the two-head epilogue is the heavier one).
+  static constexpr int kEpiWarps = (MODE == kModeJSD) ? 4 * kJsdColSplit : 4;
+  static constexpr int kColSplit = kEpiWarps / 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;    // producer warp, MMA warp, epilogue
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = kSmemBudget / kStageBytes;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers*/;
-  static_assert(BN * kHeadsPerUnit == kAccCols, "accumulator holds 256 fp32 columns");
+  static_assert(kNumAcc >= 1 && kNumAcc * kAccCols == kTmemCols, "accumulators tile TMEM");
+  static_assert(BN % (32 * kColSplit) == 0, "epilogue column split");
   // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
   // (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
   // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -141,7 +146,7 @@ __device__ __forceinline__ float jsd_term(float lp, float lq, float beta, float 
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
     fused_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_b0,
                       const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b1,
                       const Params p) {
@@ -155,9 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
   uint64_t* full = bars;               // [S]
   uint64_t* empty = bars + S;          // [S]
-  uint64_t* acc_full = bars + 2 * S;   // [2]
-  uint64_t* acc_empty = acc_full + 2;  // [2]
-  uint64_t* drain = acc_empty + 2;     // [1]
+  uint64_t* acc_full = bars + 2 * S;                // [kNumAcc]
+  uint64_t* acc_empty = acc_full + C::kNumAcc;      // [kNumAcc]
+  uint64_t* drain = acc_empty + C::kNumAcc;         // [1]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -168,9 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kNumAcc; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], kEpiWarps * 32);
+      mbar_init(&acc_empty[b], C::kEpiWarps * 32);
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, p.status)) break;
         tc_fence_after();
         for (int h = 0; h < C::kHeadsPerUnit && ok; ++h) {
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols + h * BN);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols + h * BN);
           for (int kb = 0; kb < p.k_blocks; ++kb) {
             if (!mbar_wait(&full[stage], phase, p.timeout_ns, p.status)) { ok = false; break; }
             tc_fence_after();
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         tc_commit(&acc_full[acc]);
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (++acc == C::kNumAcc) { acc = 0; acc_phase ^= 1u; }
       }
       // All MMAs issued by this thread complete before TMEM is released.
       tc_commit(drain);
@@ -257,7 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;                // TMEM lane quadrant this warp may access
+    const int quad = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) / 4;            // which column slice (kColSplit slices)
+    constexpr int kCols = BN / C::kColSplit;    // columns of each head this warp reads
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     int acc = 0;
@@ -267,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitCoord c = decode_unit(p, u, MODE);
       const int64_t row = static_cast<int64_t>(c.mt) * kBM + row_in_tile;
       const bool row_ok = row < p.T;
-      const int64_t n0 = static_cast<int64_t>(c.nt) * BN;
+      const int64_t n0 = static_cast<int64_t>(c.nt) * BN + half * kCols;
       int64_t tgt = -1;
       float ls = 0.f, lt = 0.f;
       if (MODE == kModeCE && row_ok) tgt = __ldg(p.target + row);
@@ -279,13 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[acc], acc_phase, p.timeout_ns, p.status));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + lane_addr + static_cast<uint32_t>(acc * kAccCols);
+      const uint32_t tbase = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::kAccCols + half * kCols);
       MS st = ms_empty();
       float zt = 0.f;
       bool has_t = false;
       float jsd = 0.f;
 #pragma unroll 1
-      for (int cc = 0; cc < BN / 32; ++cc) {
+      for (int cc = 0; cc < kCols / 32; ++cc) {
         const int64_t col0 = n0 + cc * 32;
         if (MODE == kModeJSD) {
           float vs[32], vt[32];
@@ -322,15 +329,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulator fully read: hand it back to the MMA warp
       tc_fence_before();
       mbar_arrive(&acc_empty[acc]);
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == C::kNumAcc) { acc = 0; acc_phase ^= 1u; }
       if (row_ok) {
+        // partial slot of this (vocab tile, column slice)
+        const int64_t slot = static_cast<int64_t>(c.nt) * C::kColSplit + half;
         if (MODE == kModeJSD) {
-          p.part0[static_cast<int64_t>(c.nt) * p.T + row] = jsd;
+          p.part0[slot * p.T + row] = jsd;
         } else {
-          const int64_t idx = (static_cast<int64_t>(c.head) * p.num_n + c.nt) * p.T + row;
+          const int64_t idx = (static_cast<int64_t>(c.head) * p.num_n * C::kColSplit + slot) * p.T + row;
           p.part0[idx] = st.m;
           p.part1[idx] = st.s;
-          if (MODE == kModeCE && has_t) p.part2[static_cast<int64_t>(c.nt) * p.T + row] = zt;
+          if (MODE == kModeCE && has_t) p.part2[slot * p.T + row] = zt;
         }
       }
     }
@@ -400,20 +409,22 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
 
 __global__ void __launch_bounds__(kFinRows * kFinSplit)
     jsd_finalize(const float* pj, int64_t T, int num_n, float* row_out, float* loss, Ctrl* ctrl) {
-  __shared__ double s_tmp[kFinRows * kFinSplit];
+  __shared__ float s_tmp[kFinRows * kFinSplit];
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kFinRows + l;
   const int cnt = (num_n + kFinSplit - 1) / kFinSplit;
   const int n_lo = min(num_n, w * cnt), n_hi = min(num_n, n_lo + cnt);
-  double a = 0.0;
-  if (row < T)
-    for (int n = n_lo; n < n_hi; ++n) a += static_cast<double>(__ldcg(pj + static_cast<int64_t>(n) * T + row));
-  s_tmp[w * 32 + l] = a;
+  KSum a;   // compensated fp32: the partial sums are added in tile order
+  if (row < T) {
+#pragma unroll 4
+    for (int n = n_lo; n < n_hi; ++n) a.add(__ldcg(pj + static_cast<int64_t>(n) * T + row));
+  }
+  s_tmp[w * 32 + l] = a.s - a.c;
   __syncthreads();
   if (w == 0 && row < T) {
-    double tot = 0.0;
-    for (int k = 0; k < kFinSplit; ++k) tot += s_tmp[k * 32 + l];
-    row_out[row] = static_cast<float>(tot);
+    KSum tot;
+    for (int k = 0; k < kFinSplit; ++k) tot.add(s_tmp[k * 32 + l]);
+    row_out[row] = tot.s - tot.c;
   }
   mean_tail(row_out, T, loss, ctrl, gridDim.x);
 }
@@ -442,7 +453,7 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUte
     attr_set[dev] = true;
   }
   const int64_t grid = p.units < L.num_sms ? p.units : L.num_sms;
-  fused_gemm_kernel<MODE><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, L.stream>>>(a0, b0, a1, b1, p);
+  fused_gemm_kernel<MODE><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, L.stream>>>(a0, b0, a1, b1, p);
   return cudaGetLastError();
 }
 
@@ -481,7 +492,7 @@ cudaError_t launch_flce(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const 
 }
 
 cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, const CUtensorMap& tm_xt,
-                         const CUtensorMap& tm_wt256, const CUtensorMap& tm_ws128, const CUtensorMap& tm_wt128,
+                         const CUtensorMap& tm_wt256, const CUtensorMap& tm_wsj, const CUtensorMap& tm_wtj,
                          const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta, float* loss,
                          const FusedWs& ws, const FusedLaunch& L) {
   // pass 1: log-sum-exp of both heads
@@ -505,12 +516,12 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, 
   q.part0 = ws.part0;
   q.lse = ws.lse;
   q.beta = beta;
-  e = launch_gemm<kModeJSD>(tm_xs, tm_ws128, tm_xt, tm_wt128, q, L);
+  e = launch_gemm<kModeJSD>(tm_xs, tm_wsj, tm_xt, tm_wtj, q, L);
   if (e != cudaSuccess) return e;
   launch_mark(3, L.stream);
   const unsigned blocks = static_cast<unsigned>((g_jsd.T + kFinRows - 1) / kFinRows);
-  jsd_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, g_jsd.T, static_cast<int>(g_jsd.num_n),
-                                                              ws.row_out, loss, ws.ctrl);
+  jsd_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(
+      ws.part0, g_jsd.T, static_cast<int>(g_jsd.num_n * ModeCfg<kModeJSD>::kColSplit), ws.row_out, loss, ws.ctrl);
   launch_mark(4, L.stream);
   return cudaGetLastError();
 }

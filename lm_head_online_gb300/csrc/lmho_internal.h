@@ -11,12 +11,18 @@ namespace lmho {
 struct Ctrl;
 
 // ---------------------------------------------------------------- CE rows
-enum CeVariant { kCeWarp = 0, kCeCta = 1, kCeCluster = 2 };
+enum CeVariant { kCeWarp = 0, kCeCta = 1, kCeCluster = 2, kCeBulk = 3 };
 struct CeConfig {
-  int variant;   // CeVariant
-  int threads;   // CTA size of the CTA-per-row kernel (256 or 512)
-  int cluster;   // CTAs per row of the cluster kernel (2, 4 or 8)
+  int variant;          // CeVariant
+  int threads;          // CTA size of the CTA-per-row kernel (256 or 512)
+  int cluster;          // CTAs per row of the cluster kernel (2, 4 or 8)
+  int num_sms = 0;      // bulk kernel: one persistent CTA per SM
+  uint64_t timeout_ns = 2000000000ull;  // bulk kernel: bound of every mbarrier wait
 };
+
+// Largest row (bytes) the bulk-copy ring kernel takes: two stages must fit.
+constexpr uint32_t kCeBulkRingBytes = 200 * 1024;
+constexpr uint32_t kCeBulkMaxRow = kCeBulkRingBytes / 2;
 
 cudaError_t launch_ce_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
                           float* loss, float* row_loss, Ctrl* ctrl, const CeConfig& cfg,
@@ -29,7 +35,11 @@ cudaError_t launch_ce_bf16_rows(const uint16_t* logits, const int64_t* target, i
 constexpr int kBM = 128;        // token rows per tile (TMEM lanes)
 constexpr int kBK = 64;         // hidden elements per pipeline stage (one 128-byte swizzle row)
 constexpr int kBN_CE = 256;     // vocab columns per tile, single-head passes
-constexpr int kBN_JSD = 128;    // vocab columns per head per tile, two-head pass
+#ifndef LMHO_JSD_BN
+#define LMHO_JSD_BN 256
+#endif
+constexpr int kBN_JSD = LMHO_JSD_BN;  // vocab columns per head per tile, two-head pass
+constexpr int kJsdColSplit = 2;       // two-head pass: epilogue warps per TMEM lane quadrant
 
 struct FusedGeometry {
   int64_t T, H, V;
@@ -63,10 +73,10 @@ cudaError_t launch_flce(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const 
                         const FusedGeometry& g, float* loss, const FusedWs& ws,
                         const FusedLaunch& L);
 // Student/teacher head maps come twice: 256-row boxes for the log-sum-exp
-// pass and 128-row boxes for the two-head divergence pass.
+// pass and kBN_JSD-row boxes for the two-head divergence pass.
 cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256,
                          const CUtensorMap& tm_xt, const CUtensorMap& tm_wt256,
-                         const CUtensorMap& tm_ws128, const CUtensorMap& tm_wt128,
+                         const CUtensorMap& tm_wsj, const CUtensorMap& tm_wtj,
                          const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta,
                          float* loss, const FusedWs& ws, const FusedLaunch& L);
 

@@ -54,12 +54,29 @@ __device__ __forceinline__ MS ms_warp_allreduce(MS a) {
   return a;
 }
 
-// Deterministic mean of row_loss[0..T): called by every block that produced
-// losses once they are stored; the last of `nwriters` blocks sums them in a
-// fixed order in fp64 and writes *loss, then clears the ticket.
+// Compensated (Kahan) fp32 sum: ~1 ulp of the total regardless of the number
+// of terms, without fp64 arithmetic (whose rate on this part is a small
+// fraction of fp32).
+struct KSum {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float y = x - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+  }
+};
+
+// Deterministic mean of row_loss[0..T) (16-byte aligned): called by every
+// block that produced losses once they are stored; the last of `nwriters`
+// blocks sums them and writes *loss, then clears the ticket.  The summation
+// order is fixed and independent of the block size: 256 virtual lanes each
+// take every 256th float4 in index order (Kahan fp32, 8 loads in flight), and
+// the 256 lane sums are added in lane order in fp64.
 __device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, float* loss, Ctrl* ctrl, uint32_t nwriters) {
+  constexpr int kVL = 256;
   __shared__ uint32_t s_last;
-  __shared__ double s_red[32];
+  __shared__ float s_part[kVL];
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -69,18 +86,31 @@ __device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, floa
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const int nt = blockDim.x;
-  double acc = 0.0;
-  for (int64_t i = threadIdx.x; i < T; i += nt) acc += static_cast<double>(__ldcg(row_loss + i));
-  // fixed-order tree: lanes, then warps
+  const int64_t n4 = T / 4;
+  const float4* v4 = reinterpret_cast<const float4*>(row_loss);
+  for (int j = threadIdx.x; j < kVL; j += blockDim.x) {
+    KSum a;
+    int64_t i = j;
+    for (; i + 7 * kVL < n4; i += 8 * kVL) {
+      float4 q[8];
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) acc += __shfl_down_sync(0xFFFFFFFFu, acc, off);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) s_red[w] = acc;
+      for (int k = 0; k < 8; ++k) q[k] = __ldcg(v4 + i + k * kVL);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        a.add(q[k].x); a.add(q[k].y); a.add(q[k].z); a.add(q[k].w);
+      }
+    }
+    for (; i < n4; i += kVL) {
+      const float4 q = __ldcg(v4 + i);
+      a.add(q.x); a.add(q.y); a.add(q.z); a.add(q.w);
+    }
+    s_part[j] = a.s - a.c;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     double tot = 0.0;
-    for (int k = 0; k < (nt + 31) / 32; ++k) tot += s_red[k];
+    for (int j = 0; j < kVL; ++j) tot += static_cast<double>(s_part[j]);
+    for (int64_t i = n4 * 4; i < T; ++i) tot += static_cast<double>(__ldcg(row_loss + i));
     *loss = static_cast<float>(tot / static_cast<double>(T));
     ctrl->ticket = 0u;
     __threadfence();

@@ -91,6 +91,7 @@ def test_fused_argument_checks(lib):
 
 
 def test_ce_variant_override_validation(lib):
-    assert lib.lmho_set_ce_variant(7) == 1
+    assert lib.lmho_set_ce_variant(8) == 1
+    assert lib.lmho_set_ce_variant(7) == 0
     assert lib.lmho_set_ce_variant(-1) == 1
     assert lib.lmho_set_ce_variant(0) == 0

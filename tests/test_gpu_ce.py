@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 RTOL_F32, ATOL_F32 = 1e-5, 1e-6
 ATOL_BF16 = 2e-3
-VARIANTS = ["auto", "warp", "cta", "cta512", "cluster2", "cluster4", "cluster8"]
+VARIANTS = ["auto", "warp", "cta", "cta512", "cluster2", "cluster4", "cluster8", "bulk"]
 
 
 @pytest.fixture(autouse=True)
@@ -40,8 +40,10 @@ def run_flat(lmho, z, t, ws_extra=0):
 
 
 # ---------------------------------------------------------------- flat fp32
+# The last three put tens of rows on every persistent CTA, so ring stages and
+# barriers are reused many times over.
 FLAT_SHAPES = [(1, 1), (3, 1), (7, 2), (5, 3), (9, 5), (4, 8), (33, 4095), (17, 4097), (64, 4096),
-               (3, 131071), (130, 8192), (5, 65537), (300, 1000)]
+               (3, 131071), (130, 8192), (5, 65537), (300, 1000), (9000, 1024), (3000, 8192), (700, 24576)]
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
@@ -56,7 +58,7 @@ def test_flat_f32_matches_oracle(gpu_lib, variant, T, V):
     assert m == pytest.approx(m_ref, rel=RTOL_F32, abs=ATOL_F32)
 
 
-@pytest.mark.parametrize("variant", ["warp", "cta", "cluster4"])
+@pytest.mark.parametrize("variant", ["warp", "cta", "cluster4", "bulk"])
 def test_flat_unaligned_rows(gpu_lib, variant):
     # logits start 4 bytes past a 16-byte boundary and V*4 is not a multiple of 16:
     # every row has a scalar head and tail around its vector body
@@ -103,7 +105,7 @@ def test_flat_deterministic_and_reusable_workspace(gpu_lib):
     t = to_dev(gen.targets(5, 1, (T,), V))
     ws = gpu_lib.workspace(gpu_lib.ce_workspace_bytes(T, V))
     outs = []
-    for variant in ("warp", "cta", "cluster2"):
+    for variant in ("warp", "cta", "cluster2", "bulk"):
         gpu_lib.set_ce_variant(variant)
         for _ in range(5):
             outs.append(gpu_lib.ce_fwd_f32(z, t, ws=ws).clone())
@@ -148,7 +150,8 @@ def run_sbv(lmho, z_bits, t):
     return out.cpu().numpy().astype(np.float64)
 
 
-SBV_SHAPES = [(1, 1, 1), (3, 2, 5), (7, 3, 4095), (16, 4, 8193), (2, 4, 32768), (3, 1, 131072), (33, 4, 1000)]
+SBV_SHAPES = [(1, 1, 1), (3, 2, 5), (7, 3, 4095), (16, 4, 8193), (2, 4, 32768), (3, 1, 131072), (33, 4, 1000),
+              (2048, 4, 2048), (700, 4, 16384)]
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
