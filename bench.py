@@ -54,12 +54,15 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-clocks", action="store_true",
+                    help="also sample clocks during the e2e region (nvidia-smi polling slows host copies)")
     ap.add_argument("--case", choices=["ce", "sbv", "flce", "fljsd"],
                     help="time one op alone at --T/--V/--H (profiling runs); prints one JSON line")
     ap.add_argument("--T", type=int, default=None, help="tokens (ce: rows; sbv: seq, batch 4)")
     ap.add_argument("--V", type=int, default=None)
     ap.add_argument("--H", type=int, default=4096)
     ap.add_argument("--ce-variant", default="auto")
+    ap.add_argument("--raster-group", type=int, default=0, help="fused kernels: token tiles per raster group (0 = auto)")
     return ap.parse_args()
 
 
@@ -88,6 +91,8 @@ class ClockSampler:
         self.lines = []
 
     def __enter__(self):
+        if self.index < 0:
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
@@ -231,9 +236,8 @@ def run_ours(args, rank, world, local_rank):
     def max_over_ranks(x):
         if not dist:
             return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        from lm_head_online_gb300 import dist as lmdist
+        return lmdist.max_over_ranks(x)
 
     # -------- device-resident timing
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -306,28 +310,41 @@ def run_ours(args, rank, world, local_rank):
         h2d = sum(v.numel() * v.element_size() for v in h.values())
         d2h = sum(v.numel() * v.element_size() for v in out.values())
 
-        def e2e_step():
+        def e2e_step(marks=None):
+            if marks:
+                marks[0].record(stream)
             for k, v in h.items():
                 d[k].copy_(v, non_blocking=True)
+            if marks:
+                marks[1].record(stream)
             step()
+            if marks:
+                marks[2].record(stream)
             for k, v in out.items():
                 host_out[k].copy_(v, non_blocking=True)
+            if marks:
+                marks[3].record(stream)
 
         for _ in range(max(1, args.warmup)):
             e2e_step()
         torch.cuda.synchronize()
         Ke = max(3, min(K, 10))
-        with ClockSampler(local_rank) as ck:
+        marks = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Ke)]
+        with ClockSampler(local_rank if args.e2e_clocks else -1) as ck:
             barrier()
             e0.record(stream)
-            for _ in range(Ke):
-                e2e_step()
+            for j in range(Ke):
+                e2e_step(marks[j])
             e1.record(stream)
             barrier()
         ms_e2e = max_over_ranks(e0.elapsed_time(e1) / Ke)
         clock_e2e = ck.summary()
+        phase = [float(np.mean([m[a].elapsed_time(m[a + 1]) for m in marks])) for a in range(3)]
         e2e = {"value": round(ms_e2e * 1e3, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": Ke}
+               "d2h_bytes_per_step": int(d2h), "steps": Ke,
+               "phases_us": {"h2d": round(phase[0] * 1e3, 1), "compute": round(phase[1] * 1e3, 1),
+                             "d2h": round(phase[2] * 1e3, 1)},
+               "h2d_GBps": round(h2d / (phase[0] * 1e-3) / 1e9, 1)}
 
     result = {
         "metric": METRIC, "value": round(ms_step * 1e3, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -460,6 +477,7 @@ def run_case(args):
     torch.cuda.set_device(0)
     lmho.load()
     lmho.set_ce_variant(args.ce_variant)
+    lmho.set_raster_group(args.raster_group)
     thr = os.cpu_count() or 1
 
     def bf16(seed, stream, shape, sigma):
@@ -505,21 +523,29 @@ def run_case(args):
     # 129 MB L2, and a write-based flush would leave ~129 MB of dirty lines
     # whose write-back the timed kernel would pay for.
     flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
-    sink = torch.empty((), dtype=torch.float32, device="cuda")
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        torch.sum(flush, out=sink)
-        ev0[i].record()
-        fn()
-        ev1[i].record()
+    nk = {"ce": 1, "sbv": 1, "flce": 2, "fljsd": 4}[c]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    for row in evs:
+        for e in row:
+            e.record()
     torch.cuda.synchronize()
-    ms = [ev0[i].elapsed_time(ev1[i]) for i in range(args.steps)]
+    for i in range(args.steps):
+        flush.sum()
+        # events recorded by the library itself around its own launches: no
+        # host-side gap between the start event and the first kernel
+        lmho.set_launch_events(evs[i])
+        fn()
+        lmho.set_launch_events(None)
+    torch.cuda.synchronize()
+    ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(args.steps)]
+    kernel_ms = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(nk)] for i in range(args.steps)]
     med = float(np.median(ms))
     rate = work / (med * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
-    return {"case": c, "T": args.T, "V": args.V, "H": H, "ce_variant": args.ce_variant, "l2": "flushed (512 MB read) before each call",
+    return {"case": c, "T": args.T, "V": args.V, "H": H, "ce_variant": args.ce_variant, "raster_group": args.raster_group, "l2": "flushed (512 MB read) before each call",
             "us_median": round(med * 1e3, 2),
-            "us_all": [round(m * 1e3, 2) for m in ms], unit: round(rate, 1)}
+            "us_all": [round(m * 1e3, 2) for m in ms],
+            "kernels_us_median": [round(float(np.median([k[j] for k in kernel_ms])) * 1e3, 2) for j in range(nk)],
+            unit: round(rate, 1)}
 
 
 def main():

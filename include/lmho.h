@@ -184,6 +184,15 @@ int lmho_ws_status(void* ws, size_t ws_bytes, void* stream);
  * cta512, cluster2, cluster4, cluster8, bulk) sets the initial value. */
 int lmho_set_ce_variant(int variant);
 
+/* Raster of the fused-linear tensor-core passes, process-wide: work units
+ * (token tile x vocab tile) are ordered in groups of `group_m` token tiles,
+ * vocab tiles outer within a group, so the CTAs running at one time share W
+ * tiles in L2; W streams from HBM about ceil(T/128/group_m) times per head
+ * and pass.  0 = automatic (16); otherwise 1..1024.  Affects speed and DRAM
+ * traffic only, never results.  Returns LMHO_ERR_INVALID_ARG outside that
+ * range. */
+int lmho_set_raster_group(int group_m);
+
 /* Measurement hook, process-wide and not thread-safe: while set, every call
  * records events[0] (a caller-created cudaEvent_t) on its stream before its
  * first kernel and events[i] after its i-th kernel, for i < n.  Kernels per

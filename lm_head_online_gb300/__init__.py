@@ -34,7 +34,7 @@ LMHO_ERR_TIMEOUT = 6
 EXPORTS = (
     "lmho_strerror", "lmho_version", "ce_workspace_bytes", "ce_fwd_f32", "ce_fwd_f32_noalloc", "ce_fwd_sbv_bf16",
     "flce_workspace_bytes", "flce_fwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16",
-    "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
+    "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
 
 CE_VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "cta512": 3, "cluster2": 4, "cluster4": 5, "cluster8": 6, "bulk": 7}
@@ -83,6 +83,8 @@ def load():
         lib.lmho_ws_status.restype = ci
         lib.lmho_set_ce_variant.argtypes = [ci]
         lib.lmho_set_ce_variant.restype = ci
+        lib.lmho_set_raster_group.argtypes = [ci]
+        lib.lmho_set_raster_group.restype = ci
         lib.lmho_set_launch_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ci]
         lib.lmho_set_launch_events.restype = None
         lib.lmho_set_wait_timeout_ns.argtypes = [u64]
@@ -256,6 +258,11 @@ def ws_status(ws, stream=None) -> int:
 def set_ce_variant(name: str):
     """Row decomposition of the CE calls: auto, warp, cta, cta512, cluster2/4/8, bulk."""
     _check(load().lmho_set_ce_variant(CE_VARIANTS[name]), "lmho_set_ce_variant")
+
+
+def set_raster_group(group_m: int):
+    """Token tiles per raster group of the fused-linear passes (0 = automatic)."""
+    _check(load().lmho_set_raster_group(int(group_m)), "lmho_set_raster_group")
 
 
 def set_launch_events(events):

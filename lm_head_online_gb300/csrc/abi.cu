@@ -90,6 +90,16 @@ int env_ce_variant() {
   return 0;
 }
 std::atomic<int> g_ce_variant{env_ce_variant()};
+std::atomic<int> g_group_m{0};
+
+// Measurement knob: LMHO_CE_BULK_RING_KB (16..200) sets the bulk ring size.
+uint32_t env_bulk_ring() {
+  const char* s = std::getenv("LMHO_CE_BULK_RING_KB");
+  if (!s) return 0;
+  const long kb = std::strtol(s, nullptr, 10);
+  return (kb >= 16 && kb <= 200) ? static_cast<uint32_t>(kb) * 1024u : 0u;
+}
+const uint32_t g_bulk_ring = env_bulk_ring();
 
 // Rows the bulk-copy ring can take: whole 16-byte vectors, 16-byte aligned
 // start, two stages in the ring.
@@ -102,6 +112,7 @@ CeConfig choose_ce(const void* base, int64_t rows, int64_t V, size_t elt, int nu
   CeConfig c{kCeCta, 256, 1};
   c.num_sms = num_sms;
   c.timeout_ns = g_timeout_ns.load();
+  c.bulk_ring_bytes = g_bulk_ring;
   const int64_t row_bytes = V * static_cast<int64_t>(elt);
   switch (g_ce_variant.load()) {
     case 1: c.variant = kCeWarp; return c;
@@ -161,7 +172,8 @@ FusedGeometry geometry(int64_t T, int64_t H, int64_t V, int bn) {
   g.V = V;
   g.num_m = (T + kBM - 1) / kBM;
   g.num_n = (V + bn - 1) / bn;
-  g.group_m = static_cast<int>(g.num_m < 16 ? g.num_m : 16);
+  const int64_t want = g_group_m.load() > 0 ? g_group_m.load() : 16;
+  g.group_m = static_cast<int>(g.num_m < want ? g.num_m : want);
   return g;
 }
 
@@ -261,6 +273,12 @@ void lmho_set_launch_events(void* const* events, int n) {
   if (n > 16) n = 16;
   for (int k = 0; k < n; ++k) g_events[k] = static_cast<cudaEvent_t>(events[k]);
   g_nevents = n;
+}
+
+int lmho_set_raster_group(int group_m) {
+  if (group_m < 0 || group_m > 1024) return LMHO_ERR_INVALID_ARG;
+  g_group_m.store(group_m);
+  return LMHO_OK;
 }
 
 int lmho_set_ce_variant(int variant) {

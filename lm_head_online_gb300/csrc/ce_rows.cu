@@ -88,16 +88,20 @@ __device__ __forceinline__ MS row_partial(const T* row, int64_t lo, int64_t hi, 
   }
   const uint4* vec = reinterpret_cast<const uint4*>(row + lo + head);
   const int64_t step = static_cast<int64_t>(nt) * U;
+  constexpr int G = U < 4 ? U : 4;  // vectors per fold (bounds the unpacked registers)
   int64_t q0 = 0;
-  // full steps: no bounds checks
+  // full steps: all U loads in flight, no bounds checks
   for (; q0 + step <= nvec; q0 += step) {
     uint4 r[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) r[u] = ldg_stream_v4(vec + q0 + u * nt + tid);
-    float v[U * E];
 #pragma unroll
-    for (int u = 0; u < U; ++u) Elt<T>::unpack(r[u], v + u * E);
-    ms_fold<U * E>(a, v);
+    for (int g = 0; g < U; g += G) {
+      float v[G * E];
+#pragma unroll
+      for (int u = 0; u < G; ++u) Elt<T>::unpack(r[g + u], v + u * E);
+      ms_fold<G * E>(a, v);
+    }
   }
   // last partial step
   if (q0 < nvec) {
@@ -105,18 +109,21 @@ __device__ __forceinline__ MS row_partial(const T* row, int64_t lo, int64_t hi, 
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t q = q0 + u * nt + tid;
-      r[u] = q < nvec ? ldg_stream_v4(vec + q) : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+      r[u] = q < nvec ? ldg_stream_v4(vec + q) : make_uint4(0u, 0u, 0u, 0u);
     }
-    float v[U * E];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      Elt<T>::unpack(r[u], v + u * E);
-      if (q0 + u * nt + tid >= nvec) {
+    for (int g = 0; g < U; g += G) {
+      float v[G * E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) v[u * E + e] = -INFINITY;
+      for (int u = 0; u < G; ++u) {
+        Elt<T>::unpack(r[g + u], v + u * E);
+        if (q0 + (g + u) * nt + tid >= nvec) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) v[u * E + e] = -INFINITY;
+        }
       }
+      ms_fold<G * E>(a, v);
     }
-    ms_fold<U * E>(a, v);
   }
   return a;
 }
@@ -215,7 +222,9 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT)
   if (mean_out && rank == 0) mean_tail(out_rows, rows, mean_out, ctrl, gridDim.x / C);
 }
 
-// Persistent bulk-copy ring: item i of this CTA is row blockIdx.x + i*gridDim.x,
+// Persistent bulk-copy ring: CTA b takes the contiguous rows [b*per, b*per+n)
+// (per = ceil(rows / gridDim.x)), so each SM streams one contiguous range;
+// its item i is row b*per + i,
 // held in stage i % stages and folded by consumer warp i % nwa, where nwa (the
 // active consumer warps) divides `stages`.  So each stage has ONE owner warp,
 // which waits on that stage's barrier fill after fill, in order: a parity wait
@@ -233,7 +242,9 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
   uint64_t* empty = full + stages;
   uint32_t* status = ctrl ? &ctrl->status : nullptr;
   const uint32_t row_bytes = static_cast<uint32_t>(V * sizeof(T));
-  const int64_t n_items = (rows - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  const int64_t per = (rows + gridDim.x - 1) / gridDim.x;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * per;
+  const int64_t n_items = first < rows ? (rows - first < per ? rows - first : per) : 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -250,7 +261,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
         const int s = static_cast<int>(i % stages);
         const uint32_t k = static_cast<uint32_t>(i / stages);
         if (!mbar_wait(&empty[s], (k & 1u) ^ 1u, timeout_ns, status)) break;
-        const int64_t r = blockIdx.x + i * gridDim.x;
+        const int64_t r = first + i;
         mbar_arrive_expect_tx(&full[s], row_bytes);
         bulk_load(ring + static_cast<size_t>(s) * stage_bytes, logits + r * V, row_bytes, &full[s]);
         filled |= 1u << s;
@@ -266,11 +277,11 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
     for (int64_t i = warp - 1; warp - 1 < nwa && i < n_items; i += nwa) {
       const int s = static_cast<int>(i % stages);
       const uint32_t k = static_cast<uint32_t>(i / stages);
-      const int64_t r = blockIdx.x + i * gridDim.x;
+      const int64_t r = first + i;
       const int64_t t = __ldg(target + r);
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], k & 1u, timeout_ns, status))) {
         for (int64_t j = i; j < n_items; j += nwa)
-          if (lane == 0) out_rows[blockIdx.x + j * gridDim.x] = __int_as_float(0x7FC00000);
+          if (lane == 0) out_rows[first + j] = __int_as_float(0x7FC00000);
         break;
       }
       const uint8_t* row = ring + static_cast<size_t>(s) * stage_bytes;
@@ -311,9 +322,14 @@ cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, in
   launch_mark(0, st);
   switch (cfg.variant) {
     case kCeWarp: {
+      // short rows: 16 loads per lane in flight, so a row takes one or two memory round trips
       const int64_t blocks = (rows + 7) / 8;
-      ce_warp_rows<T, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(logits, target, rows, V,
-                                                                         out_rows, mean_out, ctrl);
+      if (V * static_cast<int64_t>(sizeof(T)) <= 16 * 1024)
+        ce_warp_rows<T, 16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(logits, target, rows, V, out_rows,
+                                                                            mean_out, ctrl);
+      else
+        ce_warp_rows<T, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(logits, target, rows, V, out_rows,
+                                                                           mean_out, ctrl);
       break;
     }
     case kCeCta:
@@ -327,9 +343,13 @@ cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, in
     case kCeBulk: {
       const uint32_t row_bytes = static_cast<uint32_t>(V * sizeof(T));
       const uint32_t stage_bytes = (row_bytes + 127) / 128 * 128;
-      int stages = static_cast<int>(kCeBulkRingBytes / stage_bytes);
+      const uint32_t ring = cfg.bulk_ring_bytes ? cfg.bulk_ring_bytes : kCeBulkRingBytes;
+      int stages = static_cast<int>(ring / stage_bytes);
       if (stages > 32) stages = 32;
-      const int nwa = stages < 8 ? stages : 8;   // active consumer warps
+      // active consumer warps: at least two stages each, so every warp has its
+      // next row in flight while it folds the current one
+      int nwa = stages / 2;
+      nwa = nwa < 1 ? 1 : (nwa > 8 ? 8 : nwa);
       stages = stages / nwa * nwa;               // each stage owned by one warp
       const size_t smem = static_cast<size_t>(stages) * stage_bytes + 128 + 16 * stages;
       static bool attr[64] = {};
@@ -341,7 +361,9 @@ cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, in
         if (e != cudaSuccess) return e;
         attr[dev] = true;
       }
-      const int64_t grid = rows < cfg.num_sms ? rows : cfg.num_sms;
+      int64_t grid = rows < cfg.num_sms ? rows : cfg.num_sms;
+      const int64_t per = (rows + grid - 1) / grid;
+      grid = (rows + per - 1) / per;   // no CTA without rows
       ce_bulk_rows<T, 8><<<static_cast<unsigned>(grid), 32 * 9, smem, st>>>(logits, target, rows, V, out_rows, mean_out,
                                                                            ctrl, stages, nwa, stage_bytes, cfg.timeout_ns);
       break;

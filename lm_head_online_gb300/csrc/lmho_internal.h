@@ -18,6 +18,7 @@ struct CeConfig {
   int cluster;          // CTAs per row of the cluster kernel (2, 4 or 8)
   int num_sms = 0;      // bulk kernel: one persistent CTA per SM
   uint64_t timeout_ns = 2000000000ull;  // bulk kernel: bound of every mbarrier wait
+  uint32_t bulk_ring_bytes = 0;         // bulk kernel: ring size (0 = kCeBulkRingBytes)
 };
 
 // Largest row (bytes) the bulk-copy ring kernel takes: two stages must fit.

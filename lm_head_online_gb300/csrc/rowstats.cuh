@@ -71,8 +71,11 @@ struct KSum {
 // block that produced losses once they are stored; the last of `nwriters`
 // blocks sums them and writes *loss, then clears the ticket.  The summation
 // order is fixed and independent of the block size: 256 virtual lanes each
-// take every 256th float4 in index order (Kahan fp32, 8 loads in flight), and
-// the 256 lane sums are added in lane order in fp64.
+// take every 256th float4 in index order (compensated fp32, 8 loads in
+// flight); warp 0 then folds 8 lane sums per lane (compensated) and finishes
+// with a butterfly whose partners add the same two values.  No fp64: its rate
+// on this part is a small fraction of fp32 and a serial fp64 tail costs tens
+// of microseconds.
 __device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, float* loss, Ctrl* ctrl, uint32_t nwriters) {
   constexpr int kVL = 256;
   __shared__ uint32_t s_last;
@@ -104,16 +107,23 @@ __device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, floa
       const float4 q = __ldcg(v4 + i);
       a.add(q.x); a.add(q.y); a.add(q.z); a.add(q.w);
     }
+    if (j == 0)
+      for (int64_t r = n4 * 4; r < T; ++r) a.add(__ldcg(row_loss + r));
     s_part[j] = a.s - a.c;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    double tot = 0.0;
-    for (int j = 0; j < kVL; ++j) tot += static_cast<double>(s_part[j]);
-    for (int64_t i = n4 * 4; i < T; ++i) tot += static_cast<double>(__ldcg(row_loss + i));
-    *loss = static_cast<float>(tot / static_cast<double>(T));
-    ctrl->ticket = 0u;
-    __threadfence();
+  if (threadIdx.x < 32) {
+    KSum a;
+#pragma unroll
+    for (int k = 0; k < kVL / 32; ++k) a.add(s_part[threadIdx.x * (kVL / 32) + k]);
+    float v = a.s - a.c;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+    if (threadIdx.x == 0) {
+      *loss = v / static_cast<float>(T);
+      ctrl->ticket = 0u;
+      __threadfence();
+    }
   }
 }
 

@@ -95,3 +95,10 @@ def test_ce_variant_override_validation(lib):
     assert lib.lmho_set_ce_variant(7) == 0
     assert lib.lmho_set_ce_variant(-1) == 1
     assert lib.lmho_set_ce_variant(0) == 0
+
+
+def test_raster_group_validation(lib):
+    assert lib.lmho_set_raster_group(-1) == 1
+    assert lib.lmho_set_raster_group(1025) == 1
+    assert lib.lmho_set_raster_group(32) == 0
+    assert lib.lmho_set_raster_group(0) == 0

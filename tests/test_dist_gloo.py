@@ -1,0 +1,125 @@
+"""Multi-process paths on CPU with the gloo backend, world size 2.
+
+* Token sharding (what `bench.py --gpus N` runs): each rank takes a
+  contiguous token slice; the per-rank means combine into the global mean.
+* Vocab-parallel cross-entropy (page "Vocab-parallel cross-entropy, Megatron
+  layout": vocab sharded over tensor-parallel ranks; only TP = 1 is built):
+  each rank reduces its vocab shard to per-token (max, sum of exp, target
+  logit or -inf) and one all-gather plus a fixed-order merge gives the
+  unsharded loss.  This checks the merge algebra the design relies on.
+"""
+import math
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import gen
+import oracle
+from lm_head_online_gb300 import dist as lmdist
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _run(rank, world, port, fn, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        q.put((rank, fn(rank, world)))
+    except Exception as e:  # report failures to the parent
+        q.put((rank, e))
+    finally:
+        dist.destroy_process_group()
+
+
+def spawn(fn, world=2):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_run, args=(r, world, port, fn, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = dict(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r, v in out.items():
+        if isinstance(v, Exception):
+            raise v
+    return out
+
+
+def test_shard_rows_cover_and_balance():
+    for T in (1, 2, 7, 16384):
+        for world in (1, 2, 3, 8):
+            spans = [lmdist.shard_rows(T, r, world) for r in range(world)]
+            assert spans[0][0] == 0 and spans[-1][1] == T
+            for (a, b), (c, d) in zip(spans, spans[1:]):
+                assert b == c
+            sizes = [b - a for a, b in spans]
+            assert max(sizes) - min(sizes) <= 1
+    with pytest.raises(ValueError):
+        lmdist.shard_rows(4, 2, 2)
+
+
+def _token_sharded(rank, world):
+    T, V = 37, 300
+    z = gen.normal_f32(3, 0, (T, V))
+    t = gen.targets(3, 1, (T,), V)
+    lo, hi = lmdist.shard_rows(T, rank, world)
+    local_mean, _ = oracle.ce_f32(z[lo:hi], t[lo:hi])
+    mean = lmdist.combine_mean(local_mean, hi - lo)
+    slowest = lmdist.max_over_ranks(float(rank + 1))
+    return mean, slowest
+
+
+def test_token_sharded_mean_over_gloo_ranks():
+    out = spawn(_token_sharded)
+    T, V = 37, 300
+    want, _ = oracle.ce_f32(gen.normal_f32(3, 0, (T, V)), gen.targets(3, 1, (T,), V))
+    for rank, (mean, slowest) in out.items():
+        assert mean == pytest.approx(want, rel=1e-13)
+        assert slowest == 2.0
+
+
+def _vocab_parallel(rank, world):
+    T, V = 9, 1001
+    z = gen.normal_f64(4, 0, (T, V), sigma=3.0)
+    t = gen.targets(4, 1, (T,), V)
+    lo, hi = lmdist.shard_rows(V, rank, world)
+    shard = z[:, lo:hi]
+    m = shard.max(axis=1)
+    s = np.exp(shard - m[:, None]).sum(axis=1)
+    own = (t >= lo) & (t < hi)
+    zt = np.where(own, z[np.arange(T), np.clip(t, lo, hi - 1)], -np.inf)
+    part = torch.from_numpy(np.stack([m, s, zt]))
+    gathered = [torch.empty_like(part) for _ in range(world)]
+    dist.all_gather(gathered, part)
+    # fixed-order merge of the per-rank (max, sum, target logit) triples
+    M = np.full(T, -np.inf)
+    S = np.zeros(T)
+    ZT = np.full(T, -np.inf)
+    for g in gathered:
+        gm, gs, gz = g.numpy()
+        new = np.maximum(M, gm)
+        S = S * np.exp(M - new) + gs * np.exp(gm - new)
+        M = new
+        ZT = np.maximum(ZT, gz)
+    return M + np.log(S) - ZT
+
+
+def test_vocab_parallel_merge_over_gloo_ranks():
+    out = spawn(_vocab_parallel)
+    T, V = 9, 1001
+    _, want = oracle.ce_f64(gen.normal_f64(4, 0, (T, V), sigma=3.0), gen.targets(4, 1, (T,), V))
+    for rank, loss in out.items():
+        np.testing.assert_allclose(loss, want, rtol=1e-12, atol=1e-12)

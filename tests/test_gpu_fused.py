@@ -69,6 +69,24 @@ def test_flce_zero_input_is_ln_V_and_deterministic(gpu_lib):
         assert torch.equal(gpu_lib.flce_fwd_bf16(xd, Wd, td, ws=ws), first)
 
 
+def test_raster_group_changes_order_not_results(gpu_lib):
+    """The unit order (raster group) must not change a single bit: each
+    (token tile, vocab tile) partial is computed the same way in any order."""
+    T, H, V = 1100, 256, 5000
+    x, W, t = flce_inputs(14, T, H, V, sw=0.1)
+    xs, Ws, xt, Wt = jsd_inputs(14, T, H, V, sw=0.1)
+    outs = []
+    try:
+        for g in (1, 3, 16, 64):
+            gpu_lib.set_raster_group(g)
+            outs.append((run_flce(gpu_lib, x, W, t), run_fljsd(gpu_lib, xs, Ws, xt, Wt)))
+    finally:
+        gpu_lib.set_raster_group(0)
+    for (fl, js) in outs[1:]:
+        assert fl[0] == outs[0][0][0] and np.array_equal(fl[1], outs[0][0][1])
+        assert js[0] == outs[0][1][0] and np.array_equal(js[1], outs[0][1][1])
+
+
 def test_flce_bad_target_gives_nan(gpu_lib):
     T, H, V = 10, 64, 300
     x, W, t = flce_inputs(9, T, H, V)
