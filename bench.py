@@ -44,6 +44,35 @@ WORKLOAD = ("ce_fwd_f32 fp32[16384,131072] + ce_fwd_sbv_bf16 bf16[2048,4,131072]
             "flce_fwd_bf16 x[16384,4096] W[128256,4096] + fljsd_fwd_bf16 T=8192 H=4096 V=128256 beta=0.5")
 KERNELS_PER_STEP = 1 + 1 + 2 + 4
 
+# DRAM bytes (read + write) per launch of each main kernel at the bench sizes,
+# from one ncu capture of a bench step (`ncu --metrics dram__bytes_read.sum,
+# dram__bytes_write.sum,gpu__time_duration.sum` over `bench.py --steps 1
+# --warmup 0 --no-e2e --no-cpu-baseline`; summary in
+# profiles/dram_traffic_bench_step.md).  They hold only for the kernel sources
+# they were taken from: a changed source makes the bench report null.
+KERNEL_SOURCES = ("fused_linear.cu", "ce_rows.cu", "rowstats.cuh", "ptx.cuh", "lmho_internal.h")
+TRAFFIC_SOURCE_DIGEST = "420857fce0827be2"
+TRAFFIC_BYTES = {
+    "ce_fwd_f32.row_kernel": 8590265600 + 2829824,
+    "ce_fwd_sbv_bf16.row_kernel": 2147623936 + 153600,
+    "flce.tcgen05_gemm_ce": 8541593344 + 66145792,
+    "fljsd.tcgen05_gemm_lse": 8540510976 + 65602816,
+    "fljsd.tcgen05_gemm_jsd": 10194999552 + 33913088,
+}
+
+
+def kernel_source_digest():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "lm_head_online_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(kernel):
+    return TRAFFIC_BYTES.get(kernel) if kernel_source_digest() == TRAFFIC_SOURCE_DIGEST else None
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -56,6 +85,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-clocks", action="store_true",
                     help="also sample clocks during the e2e region (nvidia-smi polling slows host copies)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every configuration of the workload table (one JSON line each)")
     ap.add_argument("--case", choices=["ce", "sbv", "flce", "fljsd"],
                     help="time one op alone at --T/--V/--H (profiling runs); prints one JSON line")
     ap.add_argument("--T", type=int, default=None, help="tokens (ce: rows; sbv: seq, batch 4)")
@@ -283,11 +314,12 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(tfs / tf_peak, 4), "traffic": traffic}
 
     roofs = {
-        "ce_fwd_f32.row_kernel": hbm_roof(ce_b, kms["ce_fwd_f32.row_kernel"]),
-        "ce_fwd_sbv_bf16.row_kernel": hbm_roof(sbv_b, kms["ce_fwd_sbv_bf16.row_kernel"]),
-        "flce.tcgen05_gemm_ce": tc_roof(fl_f, kms["flce.tcgen05_gemm_ce"]),
-        "fljsd.tcgen05_gemm_lse": tc_roof(js_pf, kms["fljsd.tcgen05_gemm_lse"]),
-        "fljsd.tcgen05_gemm_jsd": tc_roof(js_pf, kms["fljsd.tcgen05_gemm_jsd"]),
+        "ce_fwd_f32.row_kernel": hbm_roof(ce_b, kms["ce_fwd_f32.row_kernel"], traffic_of("ce_fwd_f32.row_kernel")),
+        "ce_fwd_sbv_bf16.row_kernel": hbm_roof(sbv_b, kms["ce_fwd_sbv_bf16.row_kernel"],
+                                               traffic_of("ce_fwd_sbv_bf16.row_kernel")),
+        "flce.tcgen05_gemm_ce": tc_roof(fl_f, kms["flce.tcgen05_gemm_ce"], traffic_of("flce.tcgen05_gemm_ce")),
+        "fljsd.tcgen05_gemm_lse": tc_roof(js_pf, kms["fljsd.tcgen05_gemm_lse"], traffic_of("fljsd.tcgen05_gemm_lse")),
+        "fljsd.tcgen05_gemm_jsd": tc_roof(js_pf, kms["fljsd.tcgen05_gemm_jsd"], traffic_of("fljsd.tcgen05_gemm_jsd")),
     }
     dominant = max(roofs, key=lambda k: kms[k])
     ops = {
@@ -548,8 +580,37 @@ def run_case(args):
             unit: round(rate, 1)}
 
 
+SWEEP = ([("ce", 16384, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
+         [("sbv", 2048, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
+         [("flce", 1024 * b, 128256) for b in (2, 4, 8, 16)] +
+         [("fljsd", T, 128256) for T in (1024, 2048, 4096, 8192)])
+
+
+def run_sweep(args):
+    """Every configuration of the workload table, one op alone each time
+    (L2 flushed by a read before each call), in this process."""
+    import torch
+    pk = peaks()
+    for case, T, V in SWEEP:
+        a = argparse.Namespace(**vars(args))
+        a.case, a.T, a.V = case, T, V
+        a.steps = max(args.steps, 3) if case in ("ce", "sbv") else 3
+        a.warmup = max(1, min(args.warmup, 2))
+        r = run_case(a)
+        if "GB/s" in r:
+            r["frac_of_measured_hbm"] = round(r["GB/s"] / pk["hbm"], 4)
+        else:
+            r["frac_of_measured_bf16_sustained"] = round(r["TFLOP/s"] / pk["bf16_sus"], 4)
+        r["peaks"] = pk["src"]
+        print(json.dumps(r), flush=True)
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.case:
         print(json.dumps(run_case(args)), flush=True)
         return

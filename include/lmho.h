@@ -162,6 +162,22 @@ int fljsd_fwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt,
                    float* loss, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * fljsd_fwd_bf16 with a temperature and a token mask (distillation variants;
+ * the page names only beta 0.5 and batchmean, so these options are this
+ * library's readings, and temperature 1 with no mask equals fljsd_fwd_bf16):
+ *   P = softmax(xs Ws^T / temperature), Q = softmax(xt Wt^T / temperature);
+ *   keep    [T] uint8 device, or NULL for all tokens: tokens with keep == 0
+ *           contribute 0 and the batchmean divides by the number of kept
+ *           tokens (a batch with no kept token has loss 0);
+ *   temperature > 0 (finite reciprocal).  Other arguments as fljsd_fwd_bf16;
+ *   the first T floats of ws hold the per-token JSD (0 for left-out tokens).
+ * ------------------------------------------------------------------------ */
+int fljsd_fwd_bf16_ex(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt,
+                      const uint16_t* Wt, int64_t T, int64_t H, int64_t V, float beta,
+                      float temperature, const uint8_t* keep, float* loss, void* ws,
+                      size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Device status of a workspace-carrying call (flce, fljsd).
  * Synchronises `stream`, reads the status word of `ws`, clears it, and returns
  * LMHO_OK or LMHO_ERR_TIMEOUT (a bounded wait inside a kernel gave up; that
@@ -171,10 +187,10 @@ int fljsd_fwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt,
 int lmho_ws_status(void* ws, size_t ws_bytes, void* stream);
 
 /* Row decomposition of the two cross-entropy calls, process-wide:
- *   0 = automatic (default): the bulk-copy ring for rows of at most 32 KB
- *       whose start and length are multiples of 16 bytes; otherwise a warp
- *       per row for rows <= 16 KB, a cluster of 8 CTAs per row when rows are
- *       few and >= 64 KB, else a CTA per row;
+ *   0 = automatic (default): fp32 rows of at most 32 KB whose start and
+ *       length are multiples of 16 bytes go through the bulk-copy ring;
+ *       other rows of at most 32 KB get a warp per row; longer rows a CTA per
+ *       row, or a cluster of 8 CTAs per row when rows are few (< 4 per SM);
  *   1 = warp per row, 2 = CTA (256 threads) per row, 3 = CTA (512) per row,
  *   4 / 5 / 6 = cluster of 2 / 4 / 8 CTAs per row (DSMEM merge),
  *   7 = bulk-copy ring (rows up to 100 KB, 16-byte aligned; other rows fall

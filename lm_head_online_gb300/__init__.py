@@ -33,7 +33,7 @@ LMHO_ERR_TIMEOUT = 6
 # Every symbol declared in include/lmho.h.
 EXPORTS = (
     "lmho_strerror", "lmho_version", "ce_workspace_bytes", "ce_fwd_f32", "ce_fwd_f32_noalloc", "ce_fwd_sbv_bf16",
-    "flce_workspace_bytes", "flce_fwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16",
+    "flce_workspace_bytes", "flce_fwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
 
@@ -79,6 +79,8 @@ def load():
         lib.fljsd_workspace_bytes.restype = sz
         lib.fljsd_fwd_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, sz, vp]
         lib.fljsd_fwd_bf16.restype = ci
+        lib.fljsd_fwd_bf16_ex.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, f32, vp, vp, vp, sz, vp]
+        lib.fljsd_fwd_bf16_ex.restype = ci
         lib.lmho_ws_status.argtypes = [vp, sz, vp]
         lib.lmho_ws_status.restype = ci
         lib.lmho_set_ce_variant.argtypes = [ci]
@@ -242,6 +244,36 @@ def fljsd_fwd_bf16(xs, Ws, xt, Wt, beta=0.5, loss=None, ws=None, stream=None):
         ws = workspace(lib.fljsd_workspace_bytes(T, H, V), xs.device)
     _check(lib.fljsd_fwd_bf16(p1, p2, p3, p4, T, H, V, float(beta), _dev(loss, "loss", torch.float32),
                               _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "fljsd_fwd_bf16")
+    return loss
+
+
+def fljsd_fwd_bf16_ex(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, loss=None, ws=None, stream=None):
+    """fljsd_fwd_bf16 with logits divided by `temperature` and an optional
+    per-token keep mask (CUDA bool/uint8 [T]); the batchmean divides by the
+    number of kept tokens."""
+    lib = load()
+    p1 = _dev(xs, "xs", torch.bfloat16, 2)
+    p2 = _dev(Ws, "Ws", torch.bfloat16, 2)
+    p3 = _dev(xt, "xt", torch.bfloat16, 2)
+    p4 = _dev(Wt, "Wt", torch.bfloat16, 2)
+    T, H = xs.shape
+    V = Ws.shape[0]
+    if tuple(xt.shape) != (T, H) or tuple(Ws.shape) != (V, H) or tuple(Wt.shape) != (V, H):
+        raise ValueError("shape mismatch: xs, xt [T,H]; Ws, Wt [V,H]")
+    pk = None
+    if keep is not None:
+        if keep.dtype == torch.bool:
+            keep = keep.view(torch.uint8)
+        pk = _dev(keep, "keep", torch.uint8, 1)
+        if keep.shape[0] != T:
+            raise ValueError("keep must have T entries")
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=xs.device)
+    if ws is None:
+        ws = workspace(lib.fljsd_workspace_bytes(T, H, V), xs.device)
+    _check(lib.fljsd_fwd_bf16_ex(p1, p2, p3, p4, T, H, V, float(beta), float(temperature), pk,
+                                 _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8), ws.numel(),
+                                 _stream(stream)), "fljsd_fwd_bf16_ex")
     return loss
 
 

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -126,9 +127,13 @@ CeConfig choose_ce(const void* base, int64_t rows, int64_t V, size_t elt, int nu
       return c;
     default: break;
   }
-  if (bulk_ok(base, V, elt) && row_bytes <= 32 * 1024) {
+  // Measured on GB300 (flat fp32 [16384, V], Megatron bf16 [2048, 4, V]):
+  // fp32 rows <= 32 KB stream fastest through the bulk-copy ring; bf16 rows
+  // (twice the exponentials per byte) of <= 32 KB through warp-per-row loads;
+  // longer rows through a CTA per row.
+  if (elt == 4 && bulk_ok(base, V, elt) && row_bytes <= 32 * 1024) {
     c.variant = kCeBulk;
-  } else if (row_bytes <= 16 * 1024) {
+  } else if (row_bytes <= 32 * 1024) {
     c.variant = kCeWarp;
   } else if (rows < 4 * static_cast<int64_t>(num_sms) && row_bytes >= 64 * 1024) {
     c.variant = kCeCluster;   // few long rows: split each row over a cluster
@@ -356,17 +361,20 @@ size_t fljsd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
   return fljsd_ws_bytes(T, H, V);
 }
 
-int fljsd_fwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, const uint16_t* Wt, int64_t T,
-                   int64_t H, int64_t V, float beta, float* loss, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+int fljsd_impl(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, const uint16_t* Wt, int64_t T, int64_t H,
+               int64_t V, float beta, float temperature, const uint8_t* keep, float* loss, void* ws, size_t ws_bytes,
+               void* stream) {
   if (!xs || !Ws || !xt || !Wt || !loss || !ws) return LMHO_ERR_INVALID_ARG;
   if (int c = check_fused_common(T, H, V)) return c;
   if (!(beta > 0.f && beta < 1.f)) return LMHO_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !(1.f / temperature < INFINITY)) return LMHO_ERR_INVALID_ARG;
   if (!aligned16(xs) || !aligned16(Ws) || !aligned16(xt) || !aligned16(Wt)) return LMHO_ERR_INVALID_ARG;
   if (ws_bytes < fljsd_ws_bytes(T, H, V) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
   const size_t xb = 2 * static_cast<size_t>(T) * H, wb = 2 * static_cast<size_t>(V) * H;
-  const Range in[4] = {rng(xs, xb), rng(Ws, wb), rng(xt, xb), rng(Wt, wb)};
+  const Range in[5] = {rng(xs, xb), rng(Ws, wb), rng(xt, xb), rng(Wt, wb), rng(keep, keep ? static_cast<size_t>(T) : 0)};
   const Range out[2] = {rng(loss, 4), rng(ws, ws_bytes)};
-  if (int a = check_alias(in, 4, out, 2)) return a;
+  if (int a = check_alias(in, 5, out, 2)) return a;
   int sms = 0;
   if (int d = current_device(&sms)) return d;
   if (int e = get_encode()) return e;
@@ -378,7 +386,20 @@ int fljsd_fwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, c
   const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD);
   const FusedWs w = fljsd_ws_carve(ws, ws_bytes, T, V);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
-  return cuda_status(launch_fljsd(txs, tws256, txt, twt256, twsj, twtj, g1, g2, beta, loss, w, L));
+  return cuda_status(
+      launch_fljsd(txs, tws256, txt, twt256, twsj, twtj, g1, g2, beta, 1.f / temperature, keep, loss, w, L));
+}
+}  // namespace
+
+int fljsd_fwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, const uint16_t* Wt, int64_t T,
+                   int64_t H, int64_t V, float beta, float* loss, void* ws, size_t ws_bytes, void* stream) {
+  return fljsd_impl(xs, Ws, xt, Wt, T, H, V, beta, 1.f, nullptr, loss, ws, ws_bytes, stream);
+}
+
+int fljsd_fwd_bf16_ex(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, const uint16_t* Wt, int64_t T,
+                      int64_t H, int64_t V, float beta, float temperature, const uint8_t* keep, float* loss, void* ws,
+                      size_t ws_bytes, void* stream) {
+  return fljsd_impl(xs, Ws, xt, Wt, T, H, V, beta, temperature, keep, loss, ws, ws_bytes, stream);
 }
 
 int lmho_ws_status(void* ws, size_t ws_bytes, void* stream) {

@@ -84,6 +84,7 @@ struct Params {
   float* part2;
   const float* lse;  // JSD: [2][T]
   float beta;
+  float inv_tau;     // LSE / JSD: logits are multiplied by 1 / temperature
   uint64_t timeout_ns;
   uint32_t* status;
 };
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
-    const float beta = p.beta, omb = 1.f - p.beta;
+    const float beta = p.beta, omb = 1.f - p.beta, it = p.inv_tau;
     for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
       const UnitCoord c = decode_unit(p, u, MODE);
       const int64_t row = static_cast<int64_t>(c.mt) * kBM + row_in_tile;
@@ -300,15 +301,19 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
           tmem_ld32_sync(tbase + BN + cc * 32, vt);
           if (col0 + 32 <= p.V) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) jsd += jsd_term(vs[j] - ls, vt[j] - lt, beta, omb);
+            for (int j = 0; j < 32; ++j) jsd += jsd_term(fmaf(vs[j], it, -ls), fmaf(vt[j], it, -lt), beta, omb);
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.V) jsd += jsd_term(vs[j] - ls, vt[j] - lt, beta, omb);
+              if (col0 + j < p.V) jsd += jsd_term(fmaf(vs[j], it, -ls), fmaf(vt[j], it, -lt), beta, omb);
           }
         } else {
           float v[32];
           tmem_ld32_sync(tbase + cc * 32, v);
+          if (MODE == kModeLSE) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= p.inv_tau;
+          }
           if (col0 + 32 > p.V) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -408,7 +413,7 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
 }
 
 __global__ void __launch_bounds__(kFinRows * kFinSplit)
-    jsd_finalize(const float* pj, int64_t T, int num_n, float* row_out, float* loss, Ctrl* ctrl) {
+    jsd_finalize(const float* pj, int64_t T, int num_n, const uint8_t* keep, float* row_out, float* loss, Ctrl* ctrl) {
   __shared__ float s_tmp[kFinRows * kFinSplit];
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kFinRows + l;
@@ -424,9 +429,9 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
   if (w == 0 && row < T) {
     KSum tot;
     for (int k = 0; k < kFinSplit; ++k) tot.add(s_tmp[k * 32 + l]);
-    row_out[row] = tot.s - tot.c;
+    row_out[row] = (keep && !__ldg(keep + row)) ? 0.f : tot.s - tot.c;
   }
-  mean_tail(row_out, T, loss, ctrl, gridDim.x);
+  mean_tail(row_out, T, loss, ctrl, gridDim.x, keep);
 }
 
 __global__ void wait_selftest_kernel(Ctrl* ctrl, uint64_t timeout_ns) {
@@ -467,6 +472,7 @@ Params base_params(const FusedGeometry& g, const FusedLaunch& L, Ctrl* ctrl) {
   p.k_blocks = static_cast<int32_t>((g.H + kBK - 1) / kBK);
   p.timeout_ns = L.timeout_ns;
   p.status = &ctrl->status;
+  p.inv_tau = 1.f;
   return p;
 }
 
@@ -493,13 +499,14 @@ cudaError_t launch_flce(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const 
 
 cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, const CUtensorMap& tm_xt,
                          const CUtensorMap& tm_wt256, const CUtensorMap& tm_wsj, const CUtensorMap& tm_wtj,
-                         const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta, float* loss,
-                         const FusedWs& ws, const FusedLaunch& L) {
+                         const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta, float inv_tau,
+                         const uint8_t* keep, float* loss, const FusedWs& ws, const FusedLaunch& L) {
   // pass 1: log-sum-exp of both heads
   Params p = base_params(g_lse, L, ws.ctrl);
   p.units = 2 * g_lse.num_m * g_lse.num_n;
   p.part0 = ws.part0;
   p.part1 = ws.part1;
+  p.inv_tau = inv_tau;
   launch_mark(0, L.stream);
   cudaError_t e = launch_gemm<kModeLSE>(tm_xs, tm_ws256, tm_xt, tm_wt256, p, L);
   if (e != cudaSuccess) return e;
@@ -516,12 +523,14 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, 
   q.part0 = ws.part0;
   q.lse = ws.lse;
   q.beta = beta;
+  q.inv_tau = inv_tau;
   e = launch_gemm<kModeJSD>(tm_xs, tm_wsj, tm_xt, tm_wtj, q, L);
   if (e != cudaSuccess) return e;
   launch_mark(3, L.stream);
   const unsigned blocks = static_cast<unsigned>((g_jsd.T + kFinRows - 1) / kFinRows);
   jsd_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(
-      ws.part0, g_jsd.T, static_cast<int>(g_jsd.num_n * ModeCfg<kModeJSD>::kColSplit), ws.row_out, loss, ws.ctrl);
+      ws.part0, g_jsd.T, static_cast<int>(g_jsd.num_n * ModeCfg<kModeJSD>::kColSplit), keep, ws.row_out, loss,
+      ws.ctrl);
   launch_mark(4, L.stream);
   return cudaGetLastError();
 }

@@ -79,7 +79,8 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256,
                          const CUtensorMap& tm_xt, const CUtensorMap& tm_wt256,
                          const CUtensorMap& tm_wsj, const CUtensorMap& tm_wtj,
                          const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta,
-                         float* loss, const FusedWs& ws, const FusedLaunch& L);
+                         float inv_tau, const uint8_t* keep, float* loss, const FusedWs& ws,
+                         const FusedLaunch& L);
 
 // Records the caller's measurement event `i` on `st` if the hook is set
 // (lmho_set_launch_events); no-op otherwise.

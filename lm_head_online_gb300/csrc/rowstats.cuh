@@ -75,11 +75,15 @@ struct KSum {
 // flight); warp 0 then folds 8 lane sums per lane (compensated) and finishes
 // with a butterfly whose partners add the same two values.  No fp64: its rate
 // on this part is a small fraction of fp32 and a serial fp64 tail costs tens
-// of microseconds.
-__device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, float* loss, Ctrl* ctrl, uint32_t nwriters) {
+// of microseconds.  With a keep mask (uint8 per row, may be null) the divisor
+// is the number of kept rows (a mean over no row is 0); left-out rows must
+// already hold 0 in row_loss.
+__device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, float* loss, Ctrl* ctrl, uint32_t nwriters,
+                                          const uint8_t* keep = nullptr) {
   constexpr int kVL = 256;
   __shared__ uint32_t s_last;
   __shared__ float s_part[kVL];
+  __shared__ int64_t s_cnt[kVL];
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -93,6 +97,10 @@ __device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, floa
   const float4* v4 = reinterpret_cast<const float4*>(row_loss);
   for (int j = threadIdx.x; j < kVL; j += blockDim.x) {
     KSum a;
+    int64_t cnt = 0;
+    if (keep)
+      for (int64_t r = j; r < T; r += kVL) cnt += __ldg(keep + r) != 0;
+    s_cnt[j] = cnt;
     int64_t i = j;
     for (; i + 7 * kVL < n4; i += 8 * kVL) {
       float4 q[8];
@@ -114,13 +122,21 @@ __device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, floa
   __syncthreads();
   if (threadIdx.x < 32) {
     KSum a;
+    int64_t n = 0;
 #pragma unroll
-    for (int k = 0; k < kVL / 32; ++k) a.add(s_part[threadIdx.x * (kVL / 32) + k]);
+    for (int k = 0; k < kVL / 32; ++k) {
+      a.add(s_part[threadIdx.x * (kVL / 32) + k]);
+      n += s_cnt[threadIdx.x * (kVL / 32) + k];
+    }
     float v = a.s - a.c;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+    for (int off = 16; off >= 1; off >>= 1) {
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+      n += __shfl_xor_sync(0xFFFFFFFFu, n, off);
+    }
     if (threadIdx.x == 0) {
-      *loss = v / static_cast<float>(T);
+      const int64_t count = keep ? n : T;
+      *loss = count > 0 ? v / static_cast<float>(count) : 0.f;
       ctrl->ticket = 0u;
       __threadfence();
     }

@@ -54,6 +54,8 @@ def _load():
             lib.oracle_jsd_f64.restype = dbl
             lib.oracle_fljsd_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, vp, ci]
             lib.oracle_fljsd_bf16.restype = dbl
+            lib.oracle_fljsd_ex_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, vp, ci]
+            lib.oracle_fljsd_ex_bf16.restype = dbl
             lib.oracle_logits_bf16.argtypes = [vp, vp, i64, i64, i64, vp]
             lib.oracle_logits_bf16.restype = None
             _lib = lib
@@ -135,6 +137,25 @@ def fljsd_bf16(xs_bits, Ws_bits, xt_bits, Wt_bits, beta=0.5, threads=None):
     out = np.empty(T, np.float64)
     m = _load().oracle_fljsd_bf16(p1, p2, p3, p4, T, H, V, float(beta), out.ctypes.data,
                                   _threads(threads))
+    return m, out
+
+
+def fljsd_ex_bf16(xs_bits, Ws_bits, xt_bits, Wt_bits, beta=0.5, temperature=1.0, keep=None, threads=None):
+    """JSD variant: logits / temperature, optional keep mask (uint8 [T]);
+    returns (mean over kept tokens, per-token JSD with 0 for left-out tokens)."""
+    xs, p1 = _c(xs_bits, np.uint16)
+    Ws, p2 = _c(Ws_bits, np.uint16)
+    xt, p3 = _c(xt_bits, np.uint16)
+    Wt, p4 = _c(Wt_bits, np.uint16)
+    T, H = xs.shape
+    V = Ws.shape[0]
+    pk = None
+    if keep is not None:
+        keep, pk = _c(keep, np.uint8)
+        assert keep.shape == (T,)
+    out = np.empty(T, np.float64)
+    m = _load().oracle_fljsd_ex_bf16(p1, p2, p3, p4, T, H, V, float(beta), float(temperature), pk,
+                                     out.ctypes.data, _threads(threads))
     return m, out
 
 

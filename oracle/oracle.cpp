@@ -33,6 +33,11 @@
 //            (a term whose weight P or Q is 0 contributes 0), and the loss is
 //            (1/T) sum_i jsd_i ("batchmean").  P is the student.
 //
+// Variant (JSD with temperature and a token mask): the logits of both heads
+// are divided by the temperature tau before the softmax; tokens whose keep
+// flag is 0 are left out, and the batchmean divides by the number of kept
+// tokens (0 when none is kept).
+//
 // The thread-count argument of the fused functions only partitions tokens
 // across std::threads; each token's arithmetic is the single-threaded code.
 #include <cmath>
@@ -194,6 +199,38 @@ double oracle_fljsd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t*
     jsd_rows[i] = jsd_row(lp.data(), lq.data(), V, beta);
   });
   return mean_of(jsd_rows, T);
+}
+
+// Fused linear + generalized JSD with temperature and an optional keep mask
+// (keep may be null = every token kept).  jsd_rows gets the per-token JSD
+// (0 for tokens left out); returns the mean over kept tokens.
+double oracle_fljsd_ex_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt,
+                            const uint16_t* Wt, int64_t T, int64_t H, int64_t V, double beta,
+                            double tau, const uint8_t* keep, double* jsd_rows, int threads) {
+  over_tokens(T, threads, [&](int64_t i) {
+    if (keep && !keep[i]) {
+      jsd_rows[i] = 0.0;
+      return;
+    }
+    std::vector<double> zs(V), zt(V), lp(V), lq(V);
+    logits_row_bf16(xs + i * H, Ws, H, V, zs.data());
+    logits_row_bf16(xt + i * H, Wt, H, V, zt.data());
+    for (int64_t v = 0; v < V; ++v) {
+      zs[v] /= tau;
+      zt[v] /= tau;
+    }
+    log_softmax_row(zs.data(), V, lp.data());
+    log_softmax_row(zt.data(), V, lq.data());
+    jsd_rows[i] = jsd_row(lp.data(), lq.data(), V, beta);
+  });
+  double sum = 0.0;
+  int64_t kept = 0;
+  for (int64_t i = 0; i < T; ++i)
+    if (!keep || keep[i]) {
+      sum += jsd_rows[i];
+      ++kept;
+    }
+  return kept ? sum / static_cast<double>(kept) : 0.0;
 }
 
 // Logits of the fused paths for a set of tokens (used by tests to pin the

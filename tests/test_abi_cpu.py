@@ -102,3 +102,15 @@ def test_raster_group_validation(lib):
     assert lib.lmho_set_raster_group(1025) == 1
     assert lib.lmho_set_raster_group(32) == 0
     assert lib.lmho_set_raster_group(0) == 0
+
+
+def test_fljsd_ex_argument_checks(lib):
+    ws = 1 << 30
+    f = ctypes.c_float
+    # temperature must be > 0 with a finite reciprocal
+    assert lib.fljsd_fwd_bf16_ex(A, B, C, D, 4, 16, 10, f(0.5), f(0.0), None, D + 8192, D + 16384, ws, None) == 1
+    assert lib.fljsd_fwd_bf16_ex(A, B, C, D, 4, 16, 10, f(0.5), f(-1.0), None, D + 8192, D + 16384, ws, None) == 1
+    assert lib.fljsd_fwd_bf16_ex(A, B, C, D, 4, 16, 10, f(0.5), f(1e-45), None, D + 8192, D + 16384, ws, None) == 1
+    # the mask is an input: the loss may not overlap it
+    assert lib.fljsd_fwd_bf16_ex(A, B, C, D, 4, 16, 10, f(0.5), f(1.0), 0x60000000, 0x60000001, D + 16384, ws,
+                                 None) == 2

@@ -188,3 +188,40 @@ def test_wait_timeout_reports_status(gpu_lib):
     x, W, t = flce_inputs(13, 8, 64, 100)
     m, rows = run_flce(gpu_lib, x, W, t)
     assert np.all(np.isfinite(rows))
+
+
+# ---------------------------------------------------------------- JSD variant: temperature, token mask
+def run_fljsd_ex(lmho, xs, Ws, xt, Wt, beta, tau, keep):
+    T, H = xs.shape
+    V = Ws.shape[0]
+    ws = lmho.workspace(lmho.fljsd_workspace_bytes(T, H, V))
+    kd = None if keep is None else to_dev(keep)
+    loss = lmho.fljsd_fwd_bf16_ex(to_dev_bf16(xs), to_dev_bf16(Ws), to_dev_bf16(xt), to_dev_bf16(Wt), beta, tau, kd,
+                                  ws=ws)
+    assert lmho.ws_status(ws) == 0
+    return float(loss.item()), lmho.row_losses(ws, T).cpu().numpy().astype(np.float64)
+
+
+def test_fljsd_ex_defaults_are_bitwise_base(gpu_lib):
+    xs, Ws, xt, Wt = jsd_inputs(16, 300, 128, 3000, sw=0.2)
+    a = run_fljsd(gpu_lib, xs, Ws, xt, Wt, 0.4)
+    b = run_fljsd_ex(gpu_lib, xs, Ws, xt, Wt, 0.4, 1.0, None)
+    assert a[0] == b[0] and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("tau,beta", [(2.0, 0.5), (0.7, 0.3), (4.0, 0.5)])
+@pytest.mark.parametrize("T,H,V", [(130, 128, 1000), (7, 4096, 2049)])
+def test_fljsd_ex_temperature_and_mask_match_oracle(gpu_lib, tau, beta, T, H, V):
+    xs, Ws, xt, Wt = jsd_inputs(17, T, H, V, sw=2.0 / math.sqrt(H))
+    keep = (gen.targets(17, 1, (T,), 3) != 0).astype(np.uint8)   # about two thirds kept
+    for k in (None, keep):
+        m, rows = run_fljsd_ex(gpu_lib, xs, Ws, xt, Wt, beta, tau, k)
+        m_ref, rows_ref = oracle.fljsd_ex_bf16(xs, Ws, xt, Wt, beta, tau, k)
+        np.testing.assert_allclose(rows, rows_ref, rtol=RTOL_JSD_TOKEN, atol=ATOL_JSD_TOKEN)
+        assert m == pytest.approx(m_ref, rel=RTOL_SCALAR)
+
+
+def test_fljsd_ex_nothing_kept_is_zero(gpu_lib):
+    xs, Ws, xt, Wt = jsd_inputs(18, 40, 64, 500, sw=0.3)
+    m, rows = run_fljsd_ex(gpu_lib, xs, Ws, xt, Wt, 0.5, 1.0, np.zeros(40, np.uint8))
+    assert m == 0.0 and np.all(rows == 0.0)

@@ -166,3 +166,48 @@ def test_fljsd_same_student_and_teacher_is_zero():
     W = gen.normal_bf16_bits(12, 2, (V, H))
     m, rows = oracle.fljsd_bf16(x, W, x, W, 0.5)
     assert abs(m) < 1e-14 and np.all(np.abs(rows) < 1e-14)
+
+
+# ---------------------------------------------------------------- JSD variant (temperature, mask)
+
+def _jsd_case(seed=15, T=6, H=32, V=57, sw=0.5):
+    return (gen.normal_bf16_bits(seed, 0, (T, H)), gen.normal_bf16_bits(seed, 2, (V, H), sigma=sw),
+            gen.normal_bf16_bits(seed, 3, (T, H)), gen.normal_bf16_bits(seed, 4, (V, H), sigma=sw))
+
+
+def test_jsd_ex_defaults_equal_base():
+    xs, Ws, xt, Wt = _jsd_case()
+    a = oracle.fljsd_bf16(xs, Ws, xt, Wt, 0.3)
+    b = oracle.fljsd_ex_bf16(xs, Ws, xt, Wt, 0.3, 1.0, None)
+    assert a[0] == b[0] and np.array_equal(a[1], b[1])
+
+
+def test_jsd_ex_temperature_two_equals_halved_inputs():
+    # tau = 2 divides every logit by 2; so does halving x (exact in bf16: an exponent step)
+    xs, Ws, xt, Wt = _jsd_case()
+    half = lambda b: bits(widen(b).astype(np.float32) / 2)  # noqa: E731
+    m2, r2 = oracle.fljsd_ex_bf16(xs, Ws, xt, Wt, 0.5, 2.0)
+    mh, rh = oracle.fljsd_bf16(half(xs), Ws, half(xt), Wt, 0.5)
+    np.testing.assert_allclose(r2, rh, rtol=1e-12, atol=1e-16)
+    assert m2 == pytest.approx(mh, rel=1e-12)
+
+
+def test_jsd_ex_high_temperature_goes_to_zero():
+    # tau -> infinity flattens both distributions to uniform: JSD -> 0 like 1/tau^2
+    xs, Ws, xt, Wt = _jsd_case()
+    m1, _ = oracle.fljsd_ex_bf16(xs, Ws, xt, Wt, 0.5, 1e3)
+    m2, _ = oracle.fljsd_ex_bf16(xs, Ws, xt, Wt, 0.5, 2e3)
+    assert 0 < m2 < m1 < 1e-5
+    assert m1 / m2 == pytest.approx(4.0, rel=1e-2)
+
+
+def test_jsd_ex_mask_means_over_kept_tokens():
+    xs, Ws, xt, Wt = _jsd_case()
+    keep = np.array([1, 0, 1, 1, 0, 1], np.uint8)
+    _, base = oracle.fljsd_bf16(xs, Ws, xt, Wt, 0.5)
+    m, rows = oracle.fljsd_ex_bf16(xs, Ws, xt, Wt, 0.5, 1.0, keep)
+    assert np.all(rows[keep == 0] == 0.0)
+    np.testing.assert_array_equal(rows[keep == 1], base[keep == 1])
+    assert m == pytest.approx(base[keep == 1].mean(), rel=1e-15)
+    m0, rows0 = oracle.fljsd_ex_bf16(xs, Ws, xt, Wt, 0.5, 1.0, np.zeros(6, np.uint8))
+    assert m0 == 0.0 and np.all(rows0 == 0.0)
