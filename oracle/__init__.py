@@ -56,6 +56,12 @@ def _load():
             lib.oracle_fljsd_bf16.restype = dbl
             lib.oracle_fljsd_ex_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, vp, ci]
             lib.oracle_fljsd_ex_bf16.restype = dbl
+            lib.oracle_ce_grad_f32.argtypes = [vp, vp, i64, i64, dbl, vp]
+            lib.oracle_ce_grad_f32.restype = None
+            lib.oracle_ce_grad_f64.argtypes = [vp, vp, i64, i64, vp, dbl, vp]
+            lib.oracle_ce_grad_f64.restype = None
+            lib.oracle_ce_grad_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, vp, dbl, vp]
+            lib.oracle_ce_grad_sbv_bf16.restype = None
             lib.oracle_logits_bf16.argtypes = [vp, vp, i64, i64, i64, vp]
             lib.oracle_logits_bf16.restype = None
             _lib = lib
@@ -157,6 +163,42 @@ def fljsd_ex_bf16(xs_bits, Ws_bits, xt_bits, Wt_bits, beta=0.5, temperature=1.0,
     m = _load().oracle_fljsd_ex_bf16(p1, p2, p3, p4, T, H, V, float(beta), float(temperature), pk,
                                      out.ctypes.data, _threads(threads))
     return m, out
+
+
+def ce_grad_f32(z, target, scale=1.0):
+    """d(scale * mean CE)/d logits for fp32 logits [T, V] -> fp64 [T, V]."""
+    z, pz = _c(z, np.float32)
+    T, V = z.shape
+    t, pt = _c(target, np.int64)
+    dz = np.empty((T, V), np.float64)
+    _load().oracle_ce_grad_f32(pz, pt, T, V, float(scale), dz.ctypes.data)
+    return dz
+
+
+def ce_grad_f64(z, target, dloss=None, scale=1.0):
+    """d(scale * sum_i dloss_i * loss_i)/d logits for fp64 logits [T, V]."""
+    z, pz = _c(z, np.float64)
+    T, V = z.shape
+    t, pt = _c(target, np.int64)
+    pd = None
+    if dloss is not None:
+        dloss, pd = _c(dloss, np.float64)
+    dz = np.empty((T, V), np.float64)
+    _load().oracle_ce_grad_f64(pz, pt, T, V, pd, float(scale), dz.ctypes.data)
+    return dz
+
+
+def ce_grad_sbv_bf16(z_bits, target, dloss=None, scale=1.0):
+    """Megatron layout: d(scale * sum dloss[s,b] * loss[s,b])/d logits -> fp64 [S, B, V]."""
+    z, pz = _c(z_bits, np.uint16)
+    S, B, V = z.shape
+    t, pt = _c(target, np.int64)
+    pd = None
+    if dloss is not None:
+        dloss, pd = _c(dloss, np.float64)
+    dz = np.empty((S, B, V), np.float64)
+    _load().oracle_ce_grad_sbv_bf16(pz, pt, S, B, V, pd, float(scale), dz.ctypes.data)
+    return dz
 
 
 def logits_bf16(x_bits, W_bits):

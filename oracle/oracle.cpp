@@ -33,6 +33,13 @@
 //            (a term whose weight P or Q is 0 contributes 0), and the loss is
 //            (1/T) sum_i jsd_i ("batchmean").  P is the student.
 //
+// Backward of the cross-entropy (gradient of the losses with respect to the
+// logits): for row i with upstream weight g_i,
+//   dz_iv = g_i * (softmax(z_i)_v - [v == t_i]),  softmax from the two-pass
+//   normaliser (exp(z - M) / sum exp(z - M)).
+// Flat mean: g_i = scale / T.  Megatron per token: g_i = scale * dloss_i
+// (dloss may be null = 1).  A target outside [0, V) makes the row NaN.
+//
 // Variant (JSD with temperature and a token mask): the logits of both heads
 // are divided by the temperature tau before the softmax; tokens whose keep
 // flag is 0 are left out, and the batchmean divides by the number of kept
@@ -231,6 +238,54 @@ double oracle_fljsd_ex_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16
       ++kept;
     }
   return kept ? sum / static_cast<double>(kept) : 0.0;
+}
+
+}  // extern "C"
+
+namespace {
+void ce_grad_row(const double* z, int64_t V, int64_t t, double g, double* dz) {
+  if (t < 0 || t >= V) {
+    for (int64_t v = 0; v < V; ++v) dz[v] = kNaN;
+    return;
+  }
+  double M = z[0];
+  for (int64_t v = 1; v < V; ++v)
+    if (z[v] > M || std::isnan(z[v])) M = z[v];
+  double sum = 0.0;
+  for (int64_t v = 0; v < V; ++v) sum += std::exp(z[v] - M);
+  for (int64_t v = 0; v < V; ++v) dz[v] = g * (std::exp(z[v] - M) / sum - (v == t ? 1.0 : 0.0));
+}
+}  // namespace
+
+extern "C" {
+
+// Gradient of the flat mean loss (times scale) w.r.t. fp32 logits [T, V] -> dz [T, V] fp64.
+void oracle_ce_grad_f32(const float* z32, const int64_t* target, int64_t T, int64_t V, double scale,
+                        double* dz) {
+  std::vector<double> row(V);
+  const double g = scale / static_cast<double>(T);
+  for (int64_t i = 0; i < T; ++i) {
+    for (int64_t v = 0; v < V; ++v) row[v] = static_cast<double>(z32[i * V + v]);
+    ce_grad_row(row.data(), V, target[i], g, dz + i * V);
+  }
+}
+
+// Gradient of sum_i dloss_i * loss_i (times scale) w.r.t. fp64 logits [T, V].
+void oracle_ce_grad_f64(const double* z, const int64_t* target, int64_t T, int64_t V,
+                        const double* dloss, double scale, double* dz) {
+  for (int64_t i = 0; i < T; ++i)
+    ce_grad_row(z + i * V, V, target[i], scale * (dloss ? dloss[i] : 1.0), dz + i * V);
+}
+
+// Megatron layout: bf16 logits [S, B, V], per-token upstream dloss [S, B] (may be
+// null) -> dz [S, B, V] fp64.
+void oracle_ce_grad_sbv_bf16(const uint16_t* z16, const int64_t* target, int64_t S, int64_t B,
+                             int64_t V, const double* dloss, double scale, double* dz) {
+  std::vector<double> row(V);
+  for (int64_t r = 0; r < S * B; ++r) {
+    for (int64_t v = 0; v < V; ++v) row[v] = bf16_to_double(z16[r * V + v]);
+    ce_grad_row(row.data(), V, target[r], scale * (dloss ? dloss[r] : 1.0), dz + r * V);
+  }
 }
 
 // Logits of the fused paths for a set of tokens (used by tests to pin the

@@ -1,0 +1,89 @@
+"""Pins of the cross-entropy backward oracle (gradient of the losses of the
+pages "Cross-entropy loss" and "Vocab-parallel cross-entropy, Megatron
+layout" with respect to the logits): central finite differences of the
+independently pinned forward oracle, zero row sums, closed forms."""
+import math
+
+import numpy as np
+import pytest
+
+import gen
+import oracle
+
+
+def test_matches_central_differences_of_the_forward():
+    T, V = 3, 7
+    z = gen.normal_f64(20, 0, (T, V), sigma=1.5)
+    t = gen.targets(20, 1, (T,), V)
+    dz = oracle.ce_grad_f64(z, t, None, scale=1.0 / T)   # gradient of the mean
+    h = 1e-5
+    for i in range(T):
+        for v in range(V):
+            zp, zm = z.copy(), z.copy()
+            zp[i, v] += h
+            zm[i, v] -= h
+            fd = (oracle.ce_f64(zp, t)[0] - oracle.ce_f64(zm, t)[0]) / (2 * h)
+            assert dz[i, v] == pytest.approx(fd, rel=1e-6, abs=1e-10)
+
+
+def test_weighted_rows_match_central_differences():
+    T, V = 4, 5
+    z = gen.normal_f64(21, 0, (T, V))
+    t = gen.targets(21, 1, (T,), V)
+    w = np.array([0.5, -2.0, 0.0, 3.0])
+    dz = oracle.ce_grad_f64(z, t, w, scale=2.0)
+    h = 1e-5
+    for i in range(T):
+        for v in range(V):
+            zp, zm = z.copy(), z.copy()
+            zp[i, v] += h
+            zm[i, v] -= h
+            lp = oracle.ce_f64(zp, t)[1]
+            lm = oracle.ce_f64(zm, t)[1]
+            fd = 2.0 * np.dot(w, lp - lm) / (2 * h)
+            assert dz[i, v] == pytest.approx(fd, rel=1e-6, abs=1e-10)
+
+
+def test_rows_sum_to_zero_and_target_column_is_negative():
+    z = gen.normal_f64(22, 0, (6, 300), sigma=3.0)
+    t = gen.targets(22, 1, (6,), 300)
+    dz = oracle.ce_grad_f64(z, t)
+    np.testing.assert_allclose(dz.sum(axis=1), 0.0, atol=1e-14)
+    assert np.all(dz[np.arange(6), t] < 0)
+    mask = np.ones_like(dz, bool)
+    mask[np.arange(6), t] = False
+    assert np.all(dz[mask] > 0)
+
+
+def test_closed_forms():
+    V = 9
+    dz = oracle.ce_grad_f64(np.full((2, V), 4.0), np.array([0, 8]))
+    want = np.full((2, V), 1.0 / V)
+    want[0, 0] -= 1
+    want[1, 8] -= 1
+    np.testing.assert_allclose(dz, want, rtol=1e-14, atol=1e-16)
+    assert np.all(oracle.ce_grad_f64(np.array([[2.5], [-1.0]]), np.array([0, 0])) == 0.0)
+
+
+def test_bad_target_row_is_nan_and_flat_scale():
+    z = gen.normal_f32(23, 0, (4, 50))
+    t = gen.targets(23, 1, (4,), 50)
+    t[2] = 50
+    dz = oracle.ce_grad_f32(z, t, scale=3.0)
+    assert np.all(np.isnan(dz[2])) and np.all(np.isfinite(np.delete(dz, 2, axis=0)))
+    ref = oracle.ce_grad_f64(z.astype(np.float64)[[0, 1, 3]], t[[0, 1, 3]], scale=3.0 / 4)
+    np.testing.assert_array_equal(np.delete(dz, 2, axis=0), ref)
+
+
+def test_sbv_layout_uses_row_s_times_B_plus_b():
+    S, B, V = 3, 2, 16
+    zb = gen.normal_bf16_bits(24, 0, (S, B, V), sigma=2.0)
+    t = gen.targets(24, 1, (S, B), V)
+    dl = np.arange(1, S * B + 1, dtype=np.float64).reshape(S, B)
+    dz = oracle.ce_grad_sbv_bf16(zb, t, dl, scale=0.5)
+    z = gen.bf16_bits_to_f32(zb).astype(np.float64).reshape(S * B, V)
+    ref = oracle.ce_grad_f64(z, t.reshape(-1), dl.reshape(-1), scale=0.5).reshape(S, B, V)
+    np.testing.assert_array_equal(dz, ref)
+    # weight k+1 on row k: row k's gradient is (k+1)/1 times row k's unit-weight gradient
+    unit = oracle.ce_grad_sbv_bf16(zb, t, None, scale=1.0)
+    np.testing.assert_allclose(dz, 0.5 * dl[:, :, None] * unit, rtol=1e-15)
