@@ -87,7 +87,7 @@ def parse():
                     help="also sample clocks during the e2e region (nvidia-smi polling slows host copies)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every configuration of the workload table (one JSON line each)")
-    ap.add_argument("--case", choices=["ce", "sbv", "flce", "fljsd"],
+    ap.add_argument("--case", choices=["ce", "sbv", "flce", "fljsd", "ce_fb", "sbv_fb"],
                     help="time one op alone at --T/--V/--H (profiling runs); prints one JSON line")
     ap.add_argument("--T", type=int, default=None, help="tokens (ce: rows; sbv: seq, batch 4)")
     ap.add_argument("--V", type=int, default=None)
@@ -534,6 +534,21 @@ def run_case(args):
         t = targets((S, 4), V)
         fn = lambda: lmho.ce_fwd_sbv_bf16(z, t)  # noqa: E731
         work, unit = rl.ce_sbv_bytes(S, 4, V), "GB/s"
+    elif c == "ce_fb":
+        T, V = args.T or CE["T"], args.V or CE["V"]
+        z = torch.from_numpy(gen.normal_f32(args.seed, 0, (T, V), threads=thr)).cuda()
+        t = targets((T,), V)
+        ws = lmho.workspace(lmho.ce_workspace_bytes(T, V))
+        dz = torch.empty_like(z)
+        fn = lambda: lmho.ce_fwd_bwd_f32(z, t, 1.0, ws=ws, dlogits=dz)  # noqa: E731
+        work, unit = rl.ce_flat_fwd_bwd_bytes(T, V), "GB/s"
+    elif c == "sbv_fb":
+        S, V = args.T or SBV["S"], args.V or SBV["V"]
+        z = bf16(args.seed, 0, (S, 4, V), 2.0)
+        t = targets((S, 4), V)
+        dz = torch.empty_like(z)
+        fn = lambda: lmho.ce_fwd_bwd_sbv_bf16(z, t, dlogits=dz)  # noqa: E731
+        work, unit = rl.ce_sbv_fwd_bwd_bytes(S, 4, V), "GB/s"
     elif c == "flce":
         T, V = args.T or FLCE["T"], args.V or FLCE["V"]
         x, W, t = bf16(args.seed, 0, (T, H), 1.0), bf16(args.seed, 2, (V, H), 0.02), targets((T,), V)
@@ -555,7 +570,7 @@ def run_case(args):
     # 129 MB L2, and a write-based flush would leave ~129 MB of dirty lines
     # whose write-back the timed kernel would pay for.
     flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
-    nk = {"ce": 1, "sbv": 1, "flce": 2, "fljsd": 4}[c]
+    nk = {"ce": 1, "sbv": 1, "flce": 2, "fljsd": 4, "ce_fb": 1, "sbv_fb": 1}[c]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     for row in evs:
         for e in row:
@@ -581,6 +596,8 @@ def run_case(args):
 
 
 SWEEP = ([("ce", 16384, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
+         [("ce_fb", 16384, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
+         [("sbv_fb", 2048, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
          [("sbv", 2048, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
          [("flce", 1024 * b, 128256) for b in (2, 4, 8, 16)] +
          [("fljsd", T, 128256) for T in (1024, 2048, 4096, 8192)])
@@ -594,7 +611,7 @@ def run_sweep(args):
     for case, T, V in SWEEP:
         a = argparse.Namespace(**vars(args))
         a.case, a.T, a.V = case, T, V
-        a.steps = max(args.steps, 3) if case in ("ce", "sbv") else 3
+        a.steps = max(args.steps, 3) if case in ("ce", "sbv", "ce_fb", "sbv_fb") else 3
         a.warmup = max(1, min(args.warmup, 2))
         r = run_case(a)
         if "GB/s" in r:

@@ -117,6 +117,34 @@ int ce_fwd_sbv_bf16(const uint16_t* logits, const int64_t* target, int64_t S, in
                     int64_t V, float* loss, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Cross-entropy forward + backward: the losses and their gradient with
+ * respect to the logits in one pass over HBM (logits read once, gradient
+ * written once).  Same operations as ce_fwd_f32 / ce_fwd_sbv_bf16 (pages
+ * "Cross-entropy loss" and "Vocab-parallel cross-entropy, Megatron layout",
+ * section Semantics); the pages do not say whether their timings include the
+ * backward, which is what training needs:
+ *   dlogits[i, v] = g_i * (softmax(z_i)_v - [v == t_i]).
+ * No mutation or aliasing: dlogits is a separate buffer the size of logits.
+ * A target outside [0, V) makes that token's loss and gradient row NaN.
+ *
+ * ce_fwd_bwd_f32: flat fp32 [T, V]; g_i = grad_scale / T, i.e. dlogits is the
+ *   gradient of grad_scale * loss with loss the mean.  loss [1] and the
+ *   per-token losses in ws exactly as ce_fwd_f32 (ws >= ce_workspace_bytes,
+ *   zeroed before first use).  dlogits fp32 [T, V] device output.
+ * ce_fwd_bwd_sbv_bf16: Megatron layout bf16 [S, B, V]; per-token upstream
+ *   gradients dloss fp32 [S, B] (device, or NULL for all ones) and
+ *   g = grad_scale * dloss[s, b]; loss fp32 [S, B] as ce_fwd_sbv_bf16; dlogits
+ *   bf16 [S, B, V] (round to nearest even).  No workspace.
+ * grad_scale must be finite.  One kernel launch each.
+ * ------------------------------------------------------------------------ */
+int ce_fwd_bwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
+                   float grad_scale, float* loss, float* dlogits, void* ws, size_t ws_bytes,
+                   void* stream);
+int ce_fwd_bwd_sbv_bf16(const uint16_t* logits, const int64_t* target, int64_t S, int64_t B,
+                        int64_t V, const float* dloss, float grad_scale, float* loss,
+                        uint16_t* dlogits, void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused linear + cross-entropy (logits z = x W^T never written to memory).
  * Page "Fused linear + CPO loss", summary ("computed chunked without
  * materializing logits") and section Semantics: x [batch, seq, hidden],

@@ -33,6 +33,7 @@ LMHO_ERR_TIMEOUT = 6
 # Every symbol declared in include/lmho.h.
 EXPORTS = (
     "lmho_strerror", "lmho_version", "ce_workspace_bytes", "ce_fwd_f32", "ce_fwd_f32_noalloc", "ce_fwd_sbv_bf16",
+    "ce_fwd_bwd_f32", "ce_fwd_bwd_sbv_bf16",
     "flce_workspace_bytes", "flce_fwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
@@ -71,6 +72,10 @@ def load():
         lib.ce_fwd_f32_noalloc.restype = ci
         lib.ce_fwd_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, vp, vp]
         lib.ce_fwd_sbv_bf16.restype = ci
+        lib.ce_fwd_bwd_f32.argtypes = [vp, vp, i64, i64, f32, vp, vp, vp, sz, vp]
+        lib.ce_fwd_bwd_f32.restype = ci
+        lib.ce_fwd_bwd_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, vp, f32, vp, vp, vp]
+        lib.ce_fwd_bwd_sbv_bf16.restype = ci
         lib.flce_workspace_bytes.argtypes = [i64, i64, i64]
         lib.flce_workspace_bytes.restype = sz
         lib.flce_fwd_bf16.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, sz, vp]
@@ -197,6 +202,54 @@ def ce_fwd_sbv_bf16(logits, target, loss=None, stream=None):
     _check(lib.ce_fwd_sbv_bf16(pl, pt, S, B, V, _dev(loss, "loss", torch.float32), _stream(stream)),
            "ce_fwd_sbv_bf16")
     return loss
+
+
+def ce_fwd_bwd_f32(logits, target, grad_scale=1.0, loss=None, dlogits=None, ws=None, stream=None):
+    """Mean cross-entropy of fp32 logits [T, V] and its gradient (times
+    grad_scale) with respect to the logits, in one pass.  Returns (loss, dlogits)."""
+    lib = load()
+    pl = _dev(logits, "logits", torch.float32, 2)
+    T, V = logits.shape
+    pt = _dev(target, "target", torch.int64, 1)
+    if target.shape[0] != T:
+        raise ValueError("target must have T entries")
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=logits.device)
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    if tuple(dlogits.shape) != (T, V):
+        raise ValueError("dlogits must be [T, V]")
+    if ws is None:
+        ws = workspace(lib.ce_workspace_bytes(T, V), logits.device)
+    _check(lib.ce_fwd_bwd_f32(pl, pt, T, V, float(grad_scale), _dev(loss, "loss", torch.float32),
+                              _dev(dlogits, "dlogits", torch.float32), _dev(ws, "ws", torch.uint8), ws.numel(),
+                              _stream(stream)), "ce_fwd_bwd_f32")
+    return loss, dlogits
+
+
+def ce_fwd_bwd_sbv_bf16(logits, target, dloss=None, grad_scale=1.0, loss=None, dlogits=None, stream=None):
+    """Per-token cross-entropy of bf16 logits [S, B, V] and the gradient of
+    grad_scale * sum(dloss * loss) with respect to the logits (bf16).
+    Returns (loss [S, B] fp32, dlogits [S, B, V] bf16)."""
+    lib = load()
+    pl = _dev(logits, "logits", torch.bfloat16, 3)
+    S, B, V = logits.shape
+    pt = _dev(target, "target", torch.int64, 2)
+    if tuple(target.shape) != (S, B):
+        raise ValueError("target must be [S, B]")
+    pd = None
+    if dloss is not None:
+        pd = _dev(dloss, "dloss", torch.float32, 2)
+        if tuple(dloss.shape) != (S, B):
+            raise ValueError("dloss must be [S, B]")
+    if loss is None:
+        loss = torch.empty((S, B), dtype=torch.float32, device=logits.device)
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    _check(lib.ce_fwd_bwd_sbv_bf16(pl, pt, S, B, V, pd, float(grad_scale), _dev(loss, "loss", torch.float32),
+                                   _dev(dlogits, "dlogits", torch.bfloat16, 3), _stream(stream)),
+           "ce_fwd_bwd_sbv_bf16")
+    return loss, dlogits
 
 
 def flce_fwd_bf16(x, W, target, loss=None, ws=None, stream=None):

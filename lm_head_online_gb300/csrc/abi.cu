@@ -330,6 +330,41 @@ int ce_fwd_sbv_bf16(const uint16_t* logits, const int64_t* target, int64_t S, in
   return cuda_status(launch_ce_bf16_rows(logits, target, rows, V, loss, cfg, static_cast<cudaStream_t>(stream)));
 }
 
+int ce_fwd_bwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V, float grad_scale, float* loss,
+                   float* dlogits, void* ws, size_t ws_bytes, void* stream) {
+  if (!logits || !target || !loss || !dlogits || !ws) return LMHO_ERR_INVALID_ARG;
+  if (T <= 0 || V <= 0 || T > (int64_t(1) << 31) / 8) return LMHO_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_scale)) return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < ce_workspace_bytes(T, V) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const size_t zb = 4 * static_cast<size_t>(T) * V;
+  const Range in[2] = {rng(logits, zb), rng(target, 8 * static_cast<size_t>(T))};
+  const Range out[3] = {rng(loss, 4), rng(dlogits, zb), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 2, out, 3)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  return cuda_status(launch_ce_fwd_bwd_f32(logits, target, T, V, grad_scale / static_cast<float>(T), loss,
+                                           static_cast<float*>(ws), dlogits, ctrl_of(ws, ws_bytes),
+                                           g_timeout_ns.load(), static_cast<cudaStream_t>(stream)));
+}
+
+int ce_fwd_bwd_sbv_bf16(const uint16_t* logits, const int64_t* target, int64_t S, int64_t B, int64_t V,
+                        const float* dloss, float grad_scale, float* loss, uint16_t* dlogits, void* stream) {
+  if (!logits || !target || !loss || !dlogits) return LMHO_ERR_INVALID_ARG;
+  if (S <= 0 || B <= 0 || V <= 0) return LMHO_ERR_INVALID_ARG;
+  const int64_t rows = S * B;
+  if (rows > (int64_t(1) << 31) / 8) return LMHO_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_scale)) return LMHO_ERR_INVALID_ARG;
+  const size_t zb = 2 * static_cast<size_t>(rows) * V;
+  const Range in[3] = {rng(logits, zb), rng(target, 8 * static_cast<size_t>(rows)),
+                       rng(dloss, dloss ? 4 * static_cast<size_t>(rows) : 0)};
+  const Range out[2] = {rng(loss, 4 * static_cast<size_t>(rows)), rng(dlogits, zb)};
+  if (int a = check_alias(in, 3, out, 2)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  return cuda_status(launch_ce_fwd_bwd_bf16_rows(logits, target, rows, V, dloss, grad_scale, loss, dlogits,
+                                                 g_timeout_ns.load(), static_cast<cudaStream_t>(stream)));
+}
+
 size_t flce_workspace_bytes(int64_t T, int64_t H, int64_t V) {
   if (T <= 0 || V <= 0) return kAlign;
   return flce_ws_bytes(T, H, V);

@@ -31,6 +31,16 @@ cudaError_t launch_ce_f32(const float* logits, const int64_t* target, int64_t T,
 cudaError_t launch_ce_bf16_rows(const uint16_t* logits, const int64_t* target, int64_t rows,
                                 int64_t V, float* loss_rows, const CeConfig& cfg, cudaStream_t st);
 
+// Forward + backward (loss and gradient w.r.t. the logits), one HBM pass.
+// gscale: gradient weight per row (flat: grad_scale / T; per-token rows also
+// multiplied by dloss[r] when dloss is non-null).
+cudaError_t launch_ce_fwd_bwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V, float gscale,
+                                  float* loss, float* row_loss, float* dlogits, Ctrl* ctrl, uint64_t timeout_ns,
+                                  cudaStream_t st);
+cudaError_t launch_ce_fwd_bwd_bf16_rows(const uint16_t* logits, const int64_t* target, int64_t rows, int64_t V,
+                                        const float* dloss, float gscale, float* loss_rows, uint16_t* dlogits,
+                                        uint64_t timeout_ns, cudaStream_t st);
+
 // ---------------------------------------------------------------- fused linear
 // Tile geometry of the tensor-core kernels.
 constexpr int kBM = 128;        // token rows per tile (TMEM lanes)

@@ -54,6 +54,47 @@ __device__ __forceinline__ MS ms_warp_allreduce(MS a) {
   return a;
 }
 
+// ---------------------------------------------------------------- element types
+template <typename T> struct Elt;
+template <> struct Elt<float> {
+  static constexpr int kPerVec = 4;  // elements per 16-byte vector
+  __device__ static float load1(const float* p) { return __ldg(p); }
+  __device__ static float load_any(const float* p) { return *p; }
+  __device__ static void unpack(const uint4& r, float* v) {
+    v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
+    v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
+  }
+};
+template <> struct Elt<uint16_t> {  // bf16 bit patterns
+  static constexpr int kPerVec = 8;
+  __device__ static float load1(const uint16_t* p) {
+    return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
+  }
+  __device__ static float load_any(const uint16_t* p) { return __uint_as_float(static_cast<uint32_t>(*p) << 16); }
+  __device__ static void unpack(const uint4& r, float* v) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+};
+
+template <int NT>
+__device__ __forceinline__ MS block_allreduce_to0(MS a, MS* s_part) {
+  a = ms_warp_allreduce(a);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) s_part[w] = a;
+  __syncthreads();
+  MS tot = s_part[0];
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 1; k < NT / 32; ++k) tot = ms_merge(tot, s_part[k]);
+  }
+  return tot;  // valid in thread 0
+}
+
 // Compensated (Kahan) fp32 sum: ~1 ulp of the total regardless of the number
 // of terms, without fp64 arithmetic (whose rate on this part is a small
 // fraction of fp32).

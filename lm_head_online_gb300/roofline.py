@@ -22,6 +22,16 @@ def ce_sbv_bytes(S: int, B: int, V: int, logit_bytes: int = 2) -> int:
     return logit_bytes * S * B * V + 8 * S * B + 4 * S * B
 
 
+def ce_flat_fwd_bwd_bytes(T: int, V: int) -> int:
+    """Forward + backward: logits read once and the fp32 gradient written once."""
+    return ce_flat_bytes(T, V) + 4 * T * V
+
+
+def ce_sbv_fwd_bwd_bytes(S: int, B: int, V: int, with_dloss: bool = False) -> int:
+    """Forward + backward, Megatron layout: bf16 logits read, bf16 gradient written."""
+    return ce_sbv_bytes(S, B, V) + 2 * S * B * V + (4 * S * B if with_dloss else 0)
+
+
 def flce_bytes(T: int, H: int, V: int) -> int:
     """bf16 x [T, H] + bf16 W [V, H] + int64 targets [T] + fp32 loss [1]."""
     return 2 * T * H + 2 * V * H + 8 * T + 4
