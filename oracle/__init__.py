@@ -62,6 +62,12 @@ def _load():
             lib.oracle_ce_grad_f64.restype = None
             lib.oracle_ce_grad_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, vp, dbl, vp]
             lib.oracle_ce_grad_sbv_bf16.restype = None
+            lib.oracle_flce_f64.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+            lib.oracle_flce_f64.restype = dbl
+            lib.oracle_flce_grad_f64.argtypes = [vp, vp, vp, i64, i64, i64, dbl, vp, vp]
+            lib.oracle_flce_grad_f64.restype = None
+            lib.oracle_flce_grad_bf16.argtypes = [vp, vp, vp, i64, i64, i64, dbl, vp, vp]
+            lib.oracle_flce_grad_bf16.restype = None
             lib.oracle_logits_bf16.argtypes = [vp, vp, i64, i64, i64, vp]
             lib.oracle_logits_bf16.restype = None
             _lib = lib
@@ -199,6 +205,44 @@ def ce_grad_sbv_bf16(z_bits, target, dloss=None, scale=1.0):
     dz = np.empty((S, B, V), np.float64)
     _load().oracle_ce_grad_sbv_bf16(pz, pt, S, B, V, pd, float(scale), dz.ctypes.data)
     return dz
+
+
+def flce_f64(x, W, target):
+    """Fused linear + CE on fp64 inputs. Returns (mean, per-token)."""
+    x, px = _c(x, np.float64)
+    W, pw = _c(W, np.float64)
+    T, H = x.shape
+    V = W.shape[0]
+    t, pt = _c(target, np.int64)
+    out = np.empty(T, np.float64)
+    m = _load().oracle_flce_f64(px, pw, pt, T, H, V, out.ctypes.data)
+    return m, out
+
+
+def flce_grad_f64(x, W, target, scale=1.0):
+    """(dx, dW) of scale * mean fused-linear CE, fp64 inputs."""
+    x, px = _c(x, np.float64)
+    W, pw = _c(W, np.float64)
+    T, H = x.shape
+    V = W.shape[0]
+    t, pt = _c(target, np.int64)
+    dx = np.empty((T, H), np.float64)
+    dW = np.empty((V, H), np.float64)
+    _load().oracle_flce_grad_f64(px, pw, pt, T, H, V, float(scale), dx.ctypes.data, dW.ctypes.data)
+    return dx, dW
+
+
+def flce_grad_bf16(x_bits, W_bits, target, scale=1.0):
+    """(dx, dW) of scale * mean fused-linear CE from bf16 inputs (uint16 bits)."""
+    x, px = _c(x_bits, np.uint16)
+    W, pw = _c(W_bits, np.uint16)
+    T, H = x.shape
+    V = W.shape[0]
+    t, pt = _c(target, np.int64)
+    dx = np.empty((T, H), np.float64)
+    dW = np.empty((V, H), np.float64)
+    _load().oracle_flce_grad_bf16(px, pw, pt, T, H, V, float(scale), dx.ctypes.data, dW.ctypes.data)
+    return dx, dW
 
 
 def logits_bf16(x_bits, W_bits):

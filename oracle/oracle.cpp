@@ -288,6 +288,60 @@ void oracle_ce_grad_sbv_bf16(const uint16_t* z16, const int64_t* target, int64_t
   }
 }
 
+// Fused linear + CE on fp64 inputs (for finite-difference pins): x [T, H],
+// W [V, H] -> per-token losses, returns the mean.
+double oracle_flce_f64(const double* x, const double* W, const int64_t* target, int64_t T, int64_t H,
+                       int64_t V, double* loss_rows) {
+  std::vector<double> z(V);
+  for (int64_t i = 0; i < T; ++i) {
+    for (int64_t v = 0; v < V; ++v) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < H; ++k) acc += x[i * H + k] * W[v * H + k];
+      z[v] = acc;
+    }
+    loss_rows[i] = ce_row(z.data(), V, target[i]);
+  }
+  return mean_of(loss_rows, T);
+}
+
+// Backward of the fused linear + CE mean (times scale) on fp64 inputs:
+//   dZ = (scale / T) (softmax(x W^T) - onehot(t)),  dx = dZ W [T, H],
+//   dW = dZ^T x [V, H]  (sums in index order).
+void oracle_flce_grad_f64(const double* x, const double* W, const int64_t* target, int64_t T, int64_t H,
+                          int64_t V, double scale, double* dx, double* dW) {
+  std::vector<double> z(V), dz(static_cast<size_t>(T) * V);
+  const double g = scale / static_cast<double>(T);
+  for (int64_t i = 0; i < T; ++i) {
+    for (int64_t v = 0; v < V; ++v) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < H; ++k) acc += x[i * H + k] * W[v * H + k];
+      z[v] = acc;
+    }
+    ce_grad_row(z.data(), V, target[i], g, dz.data() + i * V);
+  }
+  for (int64_t i = 0; i < T; ++i)
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t v = 0; v < V; ++v) acc += dz[i * V + v] * W[v * H + k];
+      dx[i * H + k] = acc;
+    }
+  for (int64_t v = 0; v < V; ++v)
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < T; ++i) acc += dz[i * V + v] * x[i * H + k];
+      dW[v * H + k] = acc;
+    }
+}
+
+// Same from bf16 inputs (widened exactly).
+void oracle_flce_grad_bf16(const uint16_t* x16, const uint16_t* W16, const int64_t* target, int64_t T,
+                           int64_t H, int64_t V, double scale, double* dx, double* dW) {
+  std::vector<double> x(static_cast<size_t>(T) * H), W(static_cast<size_t>(V) * H);
+  for (size_t i = 0; i < x.size(); ++i) x[i] = bf16_to_double(x16[i]);
+  for (size_t i = 0; i < W.size(); ++i) W[i] = bf16_to_double(W16[i]);
+  oracle_flce_grad_f64(x.data(), W.data(), target, T, H, V, scale, dx, dW);
+}
+
 // Logits of the fused paths for a set of tokens (used by tests to pin the
 // fused functions against ce on explicit logits): z [T, V].
 void oracle_logits_bf16(const uint16_t* x, const uint16_t* W, int64_t T, int64_t H, int64_t V,

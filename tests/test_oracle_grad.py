@@ -87,3 +87,54 @@ def test_sbv_layout_uses_row_s_times_B_plus_b():
     # weight k+1 on row k: row k's gradient is (k+1)/1 times row k's unit-weight gradient
     unit = oracle.ce_grad_sbv_bf16(zb, t, None, scale=1.0)
     np.testing.assert_allclose(dz, 0.5 * dl[:, :, None] * unit, rtol=1e-15)
+
+
+# ---------------------------------------------------------------- fused linear + CE backward
+def test_flce_f64_forward_matches_bf16_oracle():
+    x = gen.normal_bf16_bits(25, 0, (4, 24))
+    W = gen.normal_bf16_bits(25, 2, (31, 24), sigma=0.5)
+    t = gen.targets(25, 1, (4,), 31)
+    widen = lambda b: gen.bf16_bits_to_f32(b).astype(np.float64)  # noqa: E731
+    a = oracle.flce_bf16(x, W, t)
+    b = oracle.flce_f64(widen(x), widen(W), t)
+    assert a[0] == b[0] and np.array_equal(a[1], b[1])
+
+
+def test_flce_grads_match_central_differences():
+    T, H, V = 3, 5, 7
+    x = gen.normal_f64(26, 0, (T, H))
+    W = gen.normal_f64(26, 2, (V, H), sigma=0.7)
+    t = gen.targets(26, 1, (T,), V)
+    scale = 1.3
+    dx, dW = oracle.flce_grad_f64(x, W, t, scale)
+    h = 1e-5
+    for i in range(T):
+        for k in range(H):
+            xp, xm = x.copy(), x.copy()
+            xp[i, k] += h
+            xm[i, k] -= h
+            fd = scale * (oracle.flce_f64(xp, W, t)[0] - oracle.flce_f64(xm, W, t)[0]) / (2 * h)
+            assert dx[i, k] == pytest.approx(fd, rel=1e-6, abs=1e-10)
+    for v in range(V):
+        for k in range(H):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[v, k] += h
+            Wm[v, k] -= h
+            fd = scale * (oracle.flce_f64(x, Wp, t)[0] - oracle.flce_f64(x, Wm, t)[0]) / (2 * h)
+            assert dW[v, k] == pytest.approx(fd, rel=1e-6, abs=1e-10)
+
+
+def test_flce_grads_equal_chain_rule_through_explicit_logits():
+    # dx = dZ W, dW = dZ^T x with dZ the logits gradient of the (separately pinned) CE backward
+    T, H, V = 6, 16, 40
+    xb = gen.normal_bf16_bits(27, 0, (T, H))
+    Wb = gen.normal_bf16_bits(27, 2, (V, H), sigma=0.3)
+    t = gen.targets(27, 1, (T,), V)
+    widen = lambda b: gen.bf16_bits_to_f32(b).astype(np.float64)  # noqa: E731
+    x, W = widen(xb), widen(Wb)
+    dz = oracle.ce_grad_f64(x @ W.T, t, None, 1.0 / T)
+    dx, dW = oracle.flce_grad_bf16(xb, Wb, t, 1.0)
+    np.testing.assert_allclose(dx, dz @ W, rtol=1e-12, atol=1e-16)
+    np.testing.assert_allclose(dW, dz.T @ x, rtol=1e-12, atol=1e-16)
+    # rows of dZ sum to zero, so sum_v dW_v = sum_i (sum_v dZ_iv) x_i = 0
+    np.testing.assert_allclose(dW.sum(axis=0), 0.0, atol=1e-14)
