@@ -166,6 +166,27 @@ int flce_fwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, i
                   int64_t H, int64_t V, float* loss, void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Fused linear + cross-entropy, forward and backward.  Same loss as
+ * flce_fwd_bf16 ("Fused linear + CPO loss", its cross-entropy core); the
+ * gradients training needs, of grad_scale * loss (loss = the mean):
+ *   dZ = (grad_scale / T) (softmax(x W^T) - onehot(target))   [T, V]
+ *   dx = dZ W  [T, H] fp32 device output,  dW = dZ^T x  [V, H] fp32 device output
+ * dZ is recomputed on the tensor cores from a second pass over the logit
+ * tiles (after the forward pass gives each row's log-sum-exp), rounded to
+ * bf16 (as the GEMM operand of the two gradient products) and kept in the
+ * workspace with its transpose; the logits themselves are never stored.
+ * x, W, dx, dW 16-byte aligned; H % 8 == 0.  grad_scale finite.  A target
+ * outside [0, V) makes that token's loss, its dx row and all of dW NaN.
+ *   ws   ws_bytes >= flce_bwd_workspace_bytes(T, H, V) (about 4 T V + 2 (V + T) H
+ *        bytes beyond the forward's), zeroed before first use; the first T
+ *        floats hold the per-token losses afterwards.
+ * ------------------------------------------------------------------------ */
+size_t flce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V);
+int flce_fwd_bwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t T,
+                      int64_t H, int64_t V, float grad_scale, float* loss, float* dx, float* dW,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused linear + generalized Jensen-Shannon divergence, batchmean.
  * Page "Fused linear + JSD", summary (separate vocab x hidden heads for student
  * and teacher, generalized JSD with beta 0.5, batchmean) and section

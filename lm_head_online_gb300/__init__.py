@@ -34,7 +34,7 @@ LMHO_ERR_TIMEOUT = 6
 EXPORTS = (
     "lmho_strerror", "lmho_version", "ce_workspace_bytes", "ce_fwd_f32", "ce_fwd_f32_noalloc", "ce_fwd_sbv_bf16",
     "ce_fwd_bwd_f32", "ce_fwd_bwd_sbv_bf16",
-    "flce_workspace_bytes", "flce_fwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
+    "flce_workspace_bytes", "flce_fwd_bf16", "flce_bwd_workspace_bytes", "flce_fwd_bwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
 
@@ -80,6 +80,10 @@ def load():
         lib.flce_workspace_bytes.restype = sz
         lib.flce_fwd_bf16.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, sz, vp]
         lib.flce_fwd_bf16.restype = ci
+        lib.flce_bwd_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.flce_bwd_workspace_bytes.restype = sz
+        lib.flce_fwd_bwd_bf16.argtypes = [vp, vp, vp, i64, i64, i64, f32, vp, vp, vp, vp, sz, vp]
+        lib.flce_fwd_bwd_bf16.restype = ci
         lib.fljsd_workspace_bytes.argtypes = [i64, i64, i64]
         lib.fljsd_workspace_bytes.restype = sz
         lib.fljsd_fwd_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, sz, vp]
@@ -277,6 +281,39 @@ def flce_fwd_bf16(x, W, target, loss=None, ws=None, stream=None):
     _check(lib.flce_fwd_bf16(px, pw, pt, T, H, V, _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8),
                              ws.numel(), _stream(stream)), "flce_fwd_bf16")
     return loss
+
+
+def flce_bwd_workspace_bytes(T: int, H: int, V: int) -> int:
+    return int(load().flce_bwd_workspace_bytes(T, H, V))
+
+
+def flce_fwd_bwd_bf16(x, W, target, grad_scale=1.0, loss=None, dx=None, dW=None, ws=None, stream=None):
+    """Mean cross-entropy of z = x W^T and the gradients of grad_scale * loss:
+    returns (loss fp32 [1], dx fp32 [T, H], dW fp32 [V, H])."""
+    lib = load()
+    if x.dim() == 3:
+        x = x.reshape(-1, x.shape[-1])
+    if target.dim() == 2:
+        target = target.reshape(-1)
+    px = _dev(x, "x", torch.bfloat16, 2)
+    pw = _dev(W, "W", torch.bfloat16, 2)
+    pt = _dev(target, "target", torch.int64, 1)
+    T, H = x.shape
+    V = W.shape[0]
+    if W.shape[1] != H or target.shape[0] != T:
+        raise ValueError("shape mismatch: x [T,H], W [V,H], target [T]")
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=x.device)
+    if dx is None:
+        dx = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    if dW is None:
+        dW = torch.empty((V, H), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(lib.flce_bwd_workspace_bytes(T, H, V), x.device)
+    _check(lib.flce_fwd_bwd_bf16(px, pw, pt, T, H, V, float(grad_scale), _dev(loss, "loss", torch.float32),
+                                 _dev(dx, "dx", torch.float32, 2), _dev(dW, "dW", torch.float32, 2),
+                                 _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "flce_fwd_bwd_bf16")
+    return loss, dx, dW
 
 
 def fljsd_fwd_bf16(xs, Ws, xt, Wt, beta=0.5, loss=None, ws=None, stream=None):

@@ -158,16 +158,21 @@ int get_encode() {
   return g_encode ? LMHO_OK : LMHO_ERR_CUDA;
 }
 
-// bf16 matrix [rows, H] (row-major, H contiguous), box = 64 (H) x box_rows, 128-byte swizzle.
-int tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t H, uint32_t box_rows) {
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
+// bf16 matrix [rows, K] (row-major, K contiguous, row stride ld >= K elements,
+// ld * 2 a multiple of 16), box = 64 (K) x box_rows, 128-byte swizzle; reads
+// past K or past the last row are zero-filled.
+int tmap_bf16_ld(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int64_t ld, uint32_t box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? LMHO_OK : LMHO_ERR_CUDA;
+}
+int tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t H, uint32_t box_rows) {
+  return tmap_bf16_ld(m, base, rows, H, H, box_rows);
 }
 
 FusedGeometry geometry(int64_t T, int64_t H, int64_t V, int bn) {
@@ -223,6 +228,53 @@ FusedWs flce_ws_carve(void* ws, size_t ws_bytes, int64_t T, int64_t V) {
   w.ctrl = ctrl_of(ws, ws_bytes);
   return w;
 }
+// Fused linear + CE backward: the forward's workspace, then the log-sum-exp of
+// every row, dZ, dZ^T, W^T and x^T (bf16, padded row strides).
+namespace {
+struct BwdLayout {
+  int64_t ld_dz, ld_dzt, ld_wt, ld_xt;
+  size_t off_lse, off_dz, off_dzt, off_wt, off_xt, end;
+};
+BwdLayout bwd_layout(int64_t T, int64_t H, int64_t V) {
+  BwdLayout b{};
+  b.ld_dz = (V + kBN_CE - 1) / kBN_CE * kBN_CE;
+  b.ld_dzt = (T + 7) / 8 * 8;
+  b.ld_wt = (V + 7) / 8 * 8;
+  b.ld_xt = (T + 7) / 8 * 8;
+  size_t o = flce_ws_bytes(T, H, V);  // the forward's carve-up comes first
+  b.off_lse = o;
+  o += align_up(4 * static_cast<size_t>(T));
+  b.off_dz = o;
+  o += align_up(2 * static_cast<size_t>(T) * b.ld_dz);
+  b.off_dzt = o;
+  o += align_up(2 * static_cast<size_t>(V) * b.ld_dzt);
+  b.off_wt = o;
+  o += align_up(2 * static_cast<size_t>(H) * b.ld_wt);
+  b.off_xt = o;
+  o += align_up(2 * static_cast<size_t>(H) * b.ld_xt);
+  b.end = o + kAlign;  // the control block stays the last 256 bytes
+  return b;
+}
+}  // namespace
+
+size_t flce_bwd_ws_bytes(int64_t T, int64_t H, int64_t V) { return bwd_layout(T, H, V).end; }
+
+FlceBwdWs flce_bwd_ws_carve(void* ws, int64_t T, int64_t H, int64_t V) {
+  const BwdLayout b = bwd_layout(T, H, V);
+  char* p = static_cast<char*>(ws);
+  FlceBwdWs w{};
+  w.lse = reinterpret_cast<float*>(p + b.off_lse);
+  w.dz = reinterpret_cast<uint16_t*>(p + b.off_dz);
+  w.dzt = reinterpret_cast<uint16_t*>(p + b.off_dzt);
+  w.wt = reinterpret_cast<uint16_t*>(p + b.off_wt);
+  w.xt = reinterpret_cast<uint16_t*>(p + b.off_xt);
+  w.ld_dz = b.ld_dz;
+  w.ld_dzt = b.ld_dzt;
+  w.ld_wt = b.ld_wt;
+  w.ld_xt = b.ld_xt;
+  return w;
+}
+
 // Partials: the log-sum-exp pass writes (max, sum) per (head, 256-wide vocab
 // tile); the divergence pass writes one sum per (kBN_JSD-wide vocab tile,
 // epilogue column slice).  part0 serves both passes.
@@ -389,6 +441,38 @@ int flce_fwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, i
   const FusedWs w = flce_ws_carve(ws, ws_bytes, T, V);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_flce(tx, tw, target, g, loss, w, L));
+}
+
+size_t flce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
+  if (T <= 0 || V <= 0 || H <= 0) return kAlign;
+  return flce_bwd_ws_bytes(T, H, V);
+}
+
+int flce_fwd_bwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t T, int64_t H, int64_t V,
+                      float grad_scale, float* loss, float* dx, float* dW, void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !W || !target || !loss || !dx || !dW || !ws) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_fused_common(T, H, V)) return c;
+  if (!std::isfinite(grad_scale)) return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W) || !aligned16(dx) || !aligned16(dW)) return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < flce_bwd_ws_bytes(T, H, V) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const Range in[3] = {rng(x, 2 * static_cast<size_t>(T) * H), rng(W, 2 * static_cast<size_t>(V) * H),
+                       rng(target, 8 * static_cast<size_t>(T))};
+  const Range out[4] = {rng(loss, 4), rng(dx, 4 * static_cast<size_t>(T) * H), rng(dW, 4 * static_cast<size_t>(V) * H),
+                        rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 3, out, 4)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  const FusedWs w = flce_ws_carve(ws, ws_bytes, T, V);
+  const FlceBwdWs bw = flce_bwd_ws_carve(ws, T, H, V);
+  FlceBwdMaps m;
+  if (tmap_bf16(&m.x, x, T, H, kBM) || tmap_bf16(&m.w, W, V, H, kBN_CE) ||
+      tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) || tmap_bf16_ld(&m.wt, bw.wt, H, V, bw.ld_wt, kBN_CE) ||
+      tmap_bf16_ld(&m.dzt, bw.dzt, V, T, bw.ld_dzt, kBM) || tmap_bf16_ld(&m.xt, bw.xt, H, T, bw.ld_xt, kBN_CE))
+    return LMHO_ERR_CUDA;
+  const FusedGeometry g = geometry(T, H, V, kBN_CE);
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_flce_fwd_bwd(m, x, W, target, g, grad_scale, loss, dx, dW, w, bw, L));
 }
 
 size_t fljsd_workspace_bytes(int64_t T, int64_t H, int64_t V) {

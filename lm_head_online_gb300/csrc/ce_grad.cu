@@ -33,13 +33,6 @@ namespace {
 
 constexpr int64_t kSliceMaxBytes = 64 * 1024;
 
-// Two fp32 values -> packed bf16x2, round to nearest even (lo in the low half).
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  uint32_t d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-
 template <typename T> struct Out;
 template <> struct Out<float> {
   __device__ static void store1(float* p, float v) { *p = v; }

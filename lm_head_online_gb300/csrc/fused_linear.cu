@@ -43,7 +43,11 @@
 namespace lmho {
 namespace {
 
-enum Mode { kModeCE = 0, kModeLSE = 1, kModeJSD = 2 };
+// CE / LSE / JSD: loss epilogues.  DZ: gradient of the CE with respect to the
+// logits, written as bf16 dZ [T, ld_dz] and its transpose dZ^T [V, ld_dzt]
+// (inputs of the two backward GEMMs).  STORE: plain fp32 tile store (the
+// backward GEMMs dx = dZ W and dW = dZ^T x; rows = T, columns = V in Params).
+enum Mode { kModeCE = 0, kModeLSE = 1, kModeJSD = 2, kModeDZ = 3, kModeStore = 4 };
 
 constexpr int kTmemCols = 512;   // all of TMEM: accumulators of 256 or 512 fp32 columns
 constexpr int kSmemBudget = 192 * 1024;
@@ -85,6 +89,12 @@ struct Params {
   const float* lse;  // JSD: [2][T]
   float beta;
   float inv_tau;     // LSE / JSD: logits are multiplied by 1 / temperature
+  float gscale;      // DZ: gradient weight of every row (grad_scale / T)
+  uint16_t* dz;      // DZ: bf16 [T, ld_dz]
+  uint16_t* dzt;     // DZ: bf16 [V, ld_dzt]
+  int64_t ld_dz, ld_dzt;
+  float* out;        // STORE: fp32 [T, ld_out]
+  int64_t ld_out;
   uint64_t timeout_ns;
   uint32_t* status;
 };
@@ -278,7 +288,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       const int64_t n0 = static_cast<int64_t>(c.nt) * BN + half * kCols;
       int64_t tgt = -1;
       float ls = 0.f, lt = 0.f;
-      if (MODE == kModeCE && row_ok) tgt = __ldg(p.target + row);
+      if ((MODE == kModeCE || MODE == kModeDZ) && row_ok) tgt = __ldg(p.target + row);
+      if (MODE == kModeDZ && row_ok) ls = __ldg(p.lse + row);
       if (MODE == kModeJSD && row_ok) {
         ls = __ldg(p.lse + row);
         lt = __ldg(p.lse + p.T + row);
@@ -306,6 +317,46 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (col0 + j < p.V) jsd += jsd_term(fmaf(vs[j], it, -ls), fmaf(vt[j], it, -lt), beta, omb);
+          }
+        } else if (MODE == kModeDZ) {
+          float v[32];
+          tmem_ld32_sync(tbase + cc * 32, v);
+          if (row_ok) {
+            const bool bad = tgt < 0 || tgt >= p.V;
+            const float g = p.gscale, nl = -ls * kLog2e;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int64_t col = col0 + j;
+              float d = col < p.V ? g * ex2_approx(fmaf(v[j], kLog2e, nl)) : 0.f;
+              if (col == tgt) d -= g;
+              v[j] = bad ? __int_as_float(0x7FC00000) : d;
+            }
+            // dZ row segment: 32 bf16 = 64 contiguous bytes (ld_dz is a multiple of the tile width)
+            uint4* dst = reinterpret_cast<uint4*>(p.dz + row * p.ld_dz + col0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              dst[k] = make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                                  pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+            // dZ^T: for each column the 32 lanes (consecutive tokens) write 64 contiguous bytes
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < p.V)
+                p.dzt[(col0 + j) * p.ld_dzt + row] = static_cast<uint16_t>(pack_bf16x2(v[j], 0.f));
+          }
+        } else if (MODE == kModeStore) {
+          float v[32];
+          tmem_ld32_sync(tbase + cc * 32, v);
+          if (row_ok) {
+            float* dst = p.out + row * p.ld_out + col0;
+            if (col0 + 32 <= p.V) {
+              float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) d4[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j < p.V) dst[j] = v[j];
+            }
           }
         } else {
           float v[32];
@@ -335,7 +386,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(&acc_empty[acc]);
       if (++acc == C::kNumAcc) { acc = 0; acc_phase ^= 1u; }
-      if (row_ok) {
+      if (row_ok && (MODE == kModeCE || MODE == kModeLSE || MODE == kModeJSD)) {
         // partial slot of this (vocab tile, column slice)
         const int64_t slot = static_cast<int64_t>(c.nt) * C::kColSplit + half;
         if (MODE == kModeJSD) {
@@ -389,7 +440,7 @@ __device__ __forceinline__ float merge_lse_row(const float* pm, const float* ps,
 
 __global__ void __launch_bounds__(kFinRows * kFinSplit)
     flce_finalize(const float* pm, const float* ps, const float* pz, const int64_t* target, int64_t T,
-                  int64_t V, int num_n, float* row_out, float* loss, Ctrl* ctrl) {
+                  int64_t V, int num_n, float* row_out, float* loss, Ctrl* ctrl, float* lse_out) {
   __shared__ MS s_tmp[kFinRows * kFinSplit];
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kFinRows + (threadIdx.x & 31);
   const float lse = merge_lse_row(pm, ps, T, num_n, row, s_tmp);
@@ -398,6 +449,7 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
     float zt = __int_as_float(0x7FC00000);
     if (t >= 0 && t < V) zt = __ldcg(pz + (t / kBN_CE) * T + row);
     row_out[row] = lse - zt;
+    if (lse_out) lse_out[row] = lse;
   }
   mean_tail(row_out, T, loss, ctrl, gridDim.x);
 }
@@ -432,6 +484,48 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
     row_out[row] = (keep && !__ldg(keep + row)) ? 0.f : tot.s - tot.c;
   }
   mean_tail(row_out, T, loss, ctrl, gridDim.x, keep);
+}
+
+// out[c, r] = in[r, c] for a bf16 matrix in [rows, cols] (row-major) into
+// out [cols, ld_out]; 64 x 64 tiles through shared memory.  Global reads and
+// writes move 16 bytes (8 elements) per thread where the tile is whole and
+// both sides are 16-byte aligned, element by element otherwise.  Tile rows are
+// padded to 72 elements (144 bytes): 16-byte shared stores stay aligned and the
+// column reads of 8 consecutive rows fall on distinct banks.
+__global__ void __launch_bounds__(256)
+    transpose_bf16(const uint16_t* __restrict__ in, int64_t rows, int64_t cols, uint16_t* __restrict__ out,
+                   int64_t ld_out) {
+  __shared__ __align__(16) uint16_t tile[64][72];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
+  const bool whole = r0 + 64 <= rows && c0 + 64 <= cols && cols % 8 == 0 && ld_out % 8 == 0 &&
+                     (reinterpret_cast<uintptr_t>(in) & 15u) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+  if (whole) {
+    for (int k = threadIdx.x; k < 512; k += 256) {  // 64 rows x 8 vectors
+      const int i = k >> 3, v = k & 7;
+      *reinterpret_cast<uint4*>(&tile[i][v * 8]) =
+          *reinterpret_cast<const uint4*>(in + (r0 + i) * cols + c0 + v * 8);
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < 512; k += 256) {  // 64 output rows (input columns) x 8 vectors
+      const int c = k >> 3, v = k & 7;
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = static_cast<uint32_t>(tile[v * 8 + 2 * e][c]) | (static_cast<uint32_t>(tile[v * 8 + 2 * e + 1][c]) << 16);
+      *reinterpret_cast<uint4*>(out + (c0 + c) * ld_out + r0 + v * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return;
+  }
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4 threads
+  for (int i = ty; i < 64; i += 4) {
+    const int64_t r = r0 + i, c = c0 + tx;
+    if (r < rows && c < cols) tile[i][tx] = in[r * cols + c];
+  }
+  __syncthreads();
+  for (int i = ty; i < 64; i += 4) {
+    const int64_t c = c0 + i, r = r0 + tx;
+    if (c < cols && r < rows) out[c * ld_out + r] = tile[tx][i];
+  }
 }
 
 __global__ void wait_selftest_kernel(Ctrl* ctrl, uint64_t timeout_ns) {
@@ -492,7 +586,8 @@ cudaError_t launch_flce(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const 
   launch_mark(1, L.stream);
   const unsigned blocks = static_cast<unsigned>((g.T + kFinRows - 1) / kFinRows);
   flce_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, ws.part1, ws.part2, target, g.T, g.V,
-                                                               static_cast<int>(g.num_n), ws.row_out, loss, ws.ctrl);
+                                                               static_cast<int>(g.num_n), ws.row_out, loss, ws.ctrl,
+                                                               nullptr);
   launch_mark(2, L.stream);
   return cudaGetLastError();
 }
@@ -533,6 +628,78 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, 
       ws.ctrl);
   launch_mark(4, L.stream);
   return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t rows, int64_t cols, uint16_t* out, int64_t ld_out,
+                                  cudaStream_t st) {
+  dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
+  transpose_bf16<<<grid, 256, 0, st>>>(in, rows, cols, out, ld_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const uint16_t* x, const uint16_t* W, const int64_t* target,
+                                const FusedGeometry& g, float grad_scale, float* loss, float* dx, float* dW,
+                                const FusedWs& ws, const FlceBwdWs& bw, const FusedLaunch& L) {
+  cudaError_t e;
+  launch_mark(0, L.stream);
+  // transposed copies so both backward GEMMs read K-major operands
+  if ((e = launch_transpose_bf16(W, g.V, g.H, bw.wt, bw.ld_wt, L.stream)) != cudaSuccess) return e;
+  if ((e = launch_transpose_bf16(x, g.T, g.H, bw.xt, bw.ld_xt, L.stream)) != cudaSuccess) return e;
+  launch_mark(1, L.stream);
+  // forward: per-token loss, mean, and each row's log-sum-exp
+  Params p = base_params(g, L, ws.ctrl);
+  p.units = g.num_m * g.num_n;
+  p.target = target;
+  p.part0 = ws.part0;
+  p.part1 = ws.part1;
+  p.part2 = ws.part2;
+  if ((e = launch_gemm<kModeCE>(m.x, m.w, m.x, m.w, p, L)) != cudaSuccess) return e;
+  const unsigned fblocks = static_cast<unsigned>((g.T + kFinRows - 1) / kFinRows);
+  flce_finalize<<<fblocks, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, ws.part1, ws.part2, target, g.T, g.V,
+                                                                static_cast<int>(g.num_n), ws.row_out, loss, ws.ctrl,
+                                                                bw.lse);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  launch_mark(2, L.stream);
+  // recompute the logit tiles, write dZ and dZ^T
+  Params q = base_params(g, L, ws.ctrl);
+  q.units = g.num_m * g.num_n;
+  q.target = target;
+  q.lse = bw.lse;
+  q.gscale = grad_scale / static_cast<float>(g.T);
+  q.dz = bw.dz;
+  q.dzt = bw.dzt;
+  q.ld_dz = bw.ld_dz;
+  q.ld_dzt = bw.ld_dzt;
+  if ((e = launch_gemm<kModeDZ>(m.x, m.w, m.x, m.w, q, L)) != cudaSuccess) return e;
+  launch_mark(3, L.stream);
+  // dx [T, H] = dZ [T, V] * W [V, H]   (B operand W^T [H, V], K = V)
+  FusedGeometry gx = g;
+  gx.T = g.T;
+  gx.V = g.H;
+  gx.H = g.V;
+  gx.num_m = (g.T + kBM - 1) / kBM;
+  gx.num_n = (g.H + kBN_CE - 1) / kBN_CE;
+  Params a = base_params(gx, L, ws.ctrl);
+  a.units = gx.num_m * gx.num_n;
+  a.out = dx;
+  a.ld_out = g.H;
+  if ((e = launch_gemm<kModeStore>(m.dz, m.wt, m.dz, m.wt, a, L)) != cudaSuccess) return e;
+  launch_mark(4, L.stream);
+  // dW [V, H] = dZ^T [V, T] * x [T, H]   (B operand x^T [H, T], K = T)
+  FusedGeometry gw = g;
+  gw.T = g.V;
+  gw.V = g.H;
+  gw.H = g.T;
+  gw.num_m = (g.V + kBM - 1) / kBM;
+  gw.num_n = (g.H + kBN_CE - 1) / kBN_CE;
+  gw.group_m = g.group_m;
+  Params b = base_params(gw, L, ws.ctrl);
+  b.units = gw.num_m * gw.num_n;
+  b.out = dW;
+  b.ld_out = g.H;
+  if ((e = launch_gemm<kModeStore>(m.dzt, m.xt, m.dzt, m.xt, b, L)) != cudaSuccess) return e;
+  launch_mark(5, L.stream);
+  return cudaSuccess;
 }
 
 cudaError_t launch_wait_selftest(Ctrl* ctrl, uint64_t timeout_ns, cudaStream_t st) {

@@ -96,6 +96,28 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256,
 // (lmho_set_launch_events); no-op otherwise.
 void launch_mark(int i, cudaStream_t st);
 
+// Fused linear + CE forward and backward.  Workspace beyond the forward's:
+// each row's log-sum-exp, dZ (bf16 [T, ld_dz], ld_dz a multiple of 256),
+// dZ^T (bf16 [V, ld_dzt]), W^T (bf16 [H, ld_wt]), x^T (bf16 [H, ld_xt]).
+struct FlceBwdWs {
+  float* lse;
+  uint16_t* dz;
+  uint16_t* dzt;
+  uint16_t* wt;
+  uint16_t* xt;
+  int64_t ld_dz, ld_dzt, ld_wt, ld_xt;
+};
+struct FlceBwdMaps {
+  CUtensorMap x, w;      // forward and dZ passes: A = x [T, H], B = W [V, H]
+  CUtensorMap dz, wt;    // dx = dZ W:   A = dZ [T, V], B = W^T [H, V]
+  CUtensorMap dzt, xt;   // dW = dZ^T x: A = dZ^T [V, T], B = x^T [H, T]
+};
+size_t flce_bwd_ws_bytes(int64_t T, int64_t H, int64_t V);
+FlceBwdWs flce_bwd_ws_carve(void* ws, int64_t T, int64_t H, int64_t V);
+cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const uint16_t* x, const uint16_t* W, const int64_t* target,
+                                const FusedGeometry& g, float grad_scale, float* loss, float* dx, float* dW,
+                                const FusedWs& ws, const FlceBwdWs& bw, const FusedLaunch& L);
+
 cudaError_t launch_wait_selftest(Ctrl* ctrl, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace lmho

@@ -46,6 +46,12 @@ def flce_flops(T: int, H: int, V: int) -> int:
     return 2 * T * V * H
 
 
+def flce_fwd_bwd_flops(T: int, H: int, V: int) -> int:
+    """Forward (one GEMM), the recomputation of the logit tiles for dZ, and the
+    two gradient products dx = dZ W and dW = dZ^T x: four T x V x H GEMMs."""
+    return 8 * T * V * H
+
+
 def fljsd_flops(T: int, H: int, V: int) -> int:
     """Both passes, both heads."""
     return 8 * T * V * H
