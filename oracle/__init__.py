@@ -68,6 +68,12 @@ def _load():
             lib.oracle_flce_grad_f64.restype = None
             lib.oracle_flce_grad_bf16.argtypes = [vp, vp, vp, i64, i64, i64, dbl, vp, vp]
             lib.oracle_flce_grad_bf16.restype = None
+            lib.oracle_fljsd_ex_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, vp]
+            lib.oracle_fljsd_ex_f64.restype = dbl
+            lib.oracle_fljsd_grad_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, dbl, vp, vp]
+            lib.oracle_fljsd_grad_f64.restype = None
+            lib.oracle_fljsd_grad_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, dbl, vp, vp]
+            lib.oracle_fljsd_grad_bf16.restype = None
             lib.oracle_logits_bf16.argtypes = [vp, vp, i64, i64, i64, vp]
             lib.oracle_logits_bf16.restype = None
             _lib = lib
@@ -243,6 +249,44 @@ def flce_grad_bf16(x_bits, W_bits, target, scale=1.0):
     dW = np.empty((V, H), np.float64)
     _load().oracle_flce_grad_bf16(px, pw, pt, T, H, V, float(scale), dx.ctypes.data, dW.ctypes.data)
     return dx, dW
+
+
+def fljsd_ex_f64(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None):
+    """fp64-input fused JSD (mean over kept tokens, per-token JSD)."""
+    arrs = [_c(a, np.float64) for a in (xs, Ws, xt, Wt)]
+    T, H = arrs[0][0].shape
+    V = arrs[1][0].shape[0]
+    pk = None
+    if keep is not None:
+        keep, pk = _c(keep, np.uint8)
+    out = np.empty(T, np.float64)
+    m = _load().oracle_fljsd_ex_f64(*[a[1] for a in arrs], T, H, V, float(beta), float(temperature), pk,
+                                    out.ctypes.data)
+    return m, out
+
+
+def _fljsd_grad(fn, dtype, xs, Ws, xt, Wt, beta, temperature, keep, scale):
+    arrs = [_c(a, dtype) for a in (xs, Ws, xt, Wt)]
+    T, H = arrs[0][0].shape
+    V = arrs[1][0].shape[0]
+    pk = None
+    if keep is not None:
+        keep, pk = _c(keep, np.uint8)
+    dxs = np.empty((T, H), np.float64)
+    dWs = np.empty((V, H), np.float64)
+    fn(*[a[1] for a in arrs], T, H, V, float(beta), float(temperature), pk, float(scale), dxs.ctypes.data,
+       dWs.ctypes.data)
+    return dxs, dWs
+
+
+def fljsd_grad_f64(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, scale=1.0):
+    """Student gradients (dxs, dWs) of scale * fused JSD, fp64 inputs."""
+    return _fljsd_grad(_load().oracle_fljsd_grad_f64, np.float64, xs, Ws, xt, Wt, beta, temperature, keep, scale)
+
+
+def fljsd_grad_bf16(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, scale=1.0):
+    """Student gradients (dxs, dWs) of scale * fused JSD from bf16 bits."""
+    return _fljsd_grad(_load().oracle_fljsd_grad_bf16, np.uint16, xs, Ws, xt, Wt, beta, temperature, keep, scale)
 
 
 def logits_bf16(x_bits, W_bits):

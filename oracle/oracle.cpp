@@ -342,6 +342,98 @@ void oracle_flce_grad_bf16(const uint16_t* x16, const uint16_t* W16, const int64
   oracle_flce_grad_f64(x.data(), W.data(), target, T, H, V, scale, dx, dW);
 }
 
+// Fused linear + generalized JSD with temperature and keep mask on fp64
+// inputs: returns the mean over kept tokens (for finite-difference pins).
+double oracle_fljsd_ex_f64(const double* xs, const double* Ws, const double* xt, const double* Wt, int64_t T,
+                           int64_t H, int64_t V, double beta, double tau, const uint8_t* keep, double* jsd_rows) {
+  std::vector<double> zs(V), zt(V), lp(V), lq(V);
+  double sum = 0.0;
+  int64_t kept = 0;
+  for (int64_t i = 0; i < T; ++i) {
+    if (keep && !keep[i]) {
+      jsd_rows[i] = 0.0;
+      continue;
+    }
+    for (int64_t v = 0; v < V; ++v) {
+      double a = 0.0, b = 0.0;
+      for (int64_t k = 0; k < H; ++k) {
+        a += xs[i * H + k] * Ws[v * H + k];
+        b += xt[i * H + k] * Wt[v * H + k];
+      }
+      zs[v] = a / tau;
+      zt[v] = b / tau;
+    }
+    log_softmax_row(zs.data(), V, lp.data());
+    log_softmax_row(zt.data(), V, lq.data());
+    jsd_rows[i] = jsd_row(lp.data(), lq.data(), V, beta);
+    sum += jsd_rows[i];
+    ++kept;
+  }
+  return kept ? sum / static_cast<double>(kept) : 0.0;
+}
+
+// Student gradients of scale * (the loss above), teacher held fixed.  With
+// P = softmax(zs / tau), Q = softmax(zt / tau), M = beta P + (1 - beta) Q:
+//   dJSD/dP_v = beta ln(P_v / M_v), so through the softmax
+//   dzs_v = (scale / (n_kept tau)) beta P_v (ln P_v - ln M_v - KL(P || M)),
+//   dxs = dZs Ws [T, H],  dWs = dZs^T xs [V, H]; left-out tokens give 0 rows.
+void oracle_fljsd_grad_f64(const double* xs, const double* Ws, const double* xt, const double* Wt, int64_t T,
+                           int64_t H, int64_t V, double beta, double tau, const uint8_t* keep, double scale,
+                           double* dxs, double* dWs) {
+  int64_t kept = 0;
+  for (int64_t i = 0; i < T; ++i) kept += (!keep || keep[i]) ? 1 : 0;
+  const double g = kept ? scale / (static_cast<double>(kept) * tau) : 0.0;
+  std::vector<double> zs(V), zt(V), lp(V), lq(V), dz(static_cast<size_t>(T) * V, 0.0);
+  for (int64_t i = 0; i < T; ++i) {
+    if (keep && !keep[i]) continue;
+    for (int64_t v = 0; v < V; ++v) {
+      double a = 0.0, b = 0.0;
+      for (int64_t k = 0; k < H; ++k) {
+        a += xs[i * H + k] * Ws[v * H + k];
+        b += xt[i * H + k] * Wt[v * H + k];
+      }
+      zs[v] = a / tau;
+      zt[v] = b / tau;
+    }
+    log_softmax_row(zs.data(), V, lp.data());
+    log_softmax_row(zt.data(), V, lq.data());
+    double kl = 0.0;
+    std::vector<double> lm(V);
+    for (int64_t v = 0; v < V; ++v) {
+      lm[v] = std::log(beta * std::exp(lp[v]) + (1.0 - beta) * std::exp(lq[v]));
+      kl += std::exp(lp[v]) * (lp[v] - lm[v]);
+    }
+    for (int64_t v = 0; v < V; ++v) dz[i * V + v] = g * beta * std::exp(lp[v]) * (lp[v] - lm[v] - kl);
+  }
+  for (int64_t i = 0; i < T; ++i)
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t v = 0; v < V; ++v) acc += dz[i * V + v] * Ws[v * H + k];
+      dxs[i * H + k] = acc;
+    }
+  for (int64_t v = 0; v < V; ++v)
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < T; ++i) acc += dz[i * V + v] * xs[i * H + k];
+      dWs[v * H + k] = acc;
+    }
+}
+
+void oracle_fljsd_grad_bf16(const uint16_t* xs16, const uint16_t* Ws16, const uint16_t* xt16, const uint16_t* Wt16,
+                            int64_t T, int64_t H, int64_t V, double beta, double tau, const uint8_t* keep,
+                            double scale, double* dxs, double* dWs) {
+  std::vector<double> xs(static_cast<size_t>(T) * H), xt(xs.size()), Ws(static_cast<size_t>(V) * H), Wt(Ws.size());
+  for (size_t i = 0; i < xs.size(); ++i) {
+    xs[i] = bf16_to_double(xs16[i]);
+    xt[i] = bf16_to_double(xt16[i]);
+  }
+  for (size_t i = 0; i < Ws.size(); ++i) {
+    Ws[i] = bf16_to_double(Ws16[i]);
+    Wt[i] = bf16_to_double(Wt16[i]);
+  }
+  oracle_fljsd_grad_f64(xs.data(), Ws.data(), xt.data(), Wt.data(), T, H, V, beta, tau, keep, scale, dxs, dWs);
+}
+
 // Logits of the fused paths for a set of tokens (used by tests to pin the
 // fused functions against ce on explicit logits): z [T, V].
 void oracle_logits_bf16(const uint16_t* x, const uint16_t* W, int64_t T, int64_t H, int64_t V,

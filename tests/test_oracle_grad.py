@@ -138,3 +138,57 @@ def test_flce_grads_equal_chain_rule_through_explicit_logits():
     np.testing.assert_allclose(dW, dz.T @ x, rtol=1e-12, atol=1e-16)
     # rows of dZ sum to zero, so sum_v dW_v = sum_i (sum_v dZ_iv) x_i = 0
     np.testing.assert_allclose(dW.sum(axis=0), 0.0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- fused linear + JSD backward (student)
+@pytest.mark.parametrize("beta,tau,masked", [(0.5, 1.0, False), (0.3, 2.0, True)])
+def test_fljsd_student_grads_match_central_differences(beta, tau, masked):
+    T, H, V = 3, 4, 6
+    xs = gen.normal_f64(28, 0, (T, H))
+    Ws = gen.normal_f64(28, 2, (V, H), sigma=0.8)
+    xt = gen.normal_f64(28, 3, (T, H))
+    Wt = gen.normal_f64(28, 4, (V, H), sigma=0.8)
+    keep = np.array([1, 0, 1], np.uint8) if masked else None
+    scale = 1.7
+    dxs, dWs = oracle.fljsd_grad_f64(xs, Ws, xt, Wt, beta, tau, keep, scale)
+    f = lambda a, b: scale * oracle.fljsd_ex_f64(a, b, xt, Wt, beta, tau, keep)[0]  # noqa: E731
+    h = 1e-5
+    for i in range(T):
+        for k in range(H):
+            p, m = xs.copy(), xs.copy()
+            p[i, k] += h
+            m[i, k] -= h
+            assert dxs[i, k] == pytest.approx((f(p, Ws) - f(m, Ws)) / (2 * h), rel=1e-6, abs=1e-10)
+    for v in range(V):
+        for k in range(H):
+            p, m = Ws.copy(), Ws.copy()
+            p[v, k] += h
+            m[v, k] -= h
+            assert dWs[v, k] == pytest.approx((f(xs, p) - f(xs, m)) / (2 * h), rel=1e-6, abs=1e-10)
+    if masked:
+        assert np.all(dxs[1] == 0.0)
+
+
+def test_fljsd_grads_vanish_at_identical_heads_and_bf16_front_end():
+    T, H, V = 4, 8, 20
+    x = gen.normal_bf16_bits(29, 0, (T, H))
+    W = gen.normal_bf16_bits(29, 2, (V, H), sigma=0.5)
+    dxs, dWs = oracle.fljsd_grad_bf16(x, W, x, W)
+    assert np.all(np.abs(dxs) < 1e-15) and np.all(np.abs(dWs) < 1e-15)   # JSD minimum: P = Q
+    xt = gen.normal_bf16_bits(29, 3, (T, H))
+    Wt = gen.normal_bf16_bits(29, 4, (V, H), sigma=0.5)
+    widen = lambda b: gen.bf16_bits_to_f32(b).astype(np.float64)  # noqa: E731
+    a = oracle.fljsd_grad_bf16(x, W, xt, Wt, 0.4, 1.5, None, 2.0)
+    b = oracle.fljsd_grad_f64(widen(x), widen(W), widen(xt), widen(Wt), 0.4, 1.5, None, 2.0)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_fljsd_f64_forward_equals_bf16_oracle_on_widened_inputs():
+    T, H, V = 5, 16, 30
+    b = [gen.normal_bf16_bits(30, s, shp, sigma=sg) for s, shp, sg in
+         ((0, (T, H), 1.0), (2, (V, H), 0.4), (3, (T, H), 1.0), (4, (V, H), 0.4))]
+    widen = lambda a: gen.bf16_bits_to_f32(a).astype(np.float64)  # noqa: E731
+    keep = np.array([1, 1, 0, 1, 0], np.uint8)
+    a = oracle.fljsd_ex_bf16(*b, 0.3, 1.7, keep)
+    c = oracle.fljsd_ex_f64(*[widen(x) for x in b], 0.3, 1.7, keep)
+    assert a[0] == c[0] and np.array_equal(a[1], c[1])
