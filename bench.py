@@ -87,7 +87,7 @@ def parse():
                     help="also sample clocks during the e2e region (nvidia-smi polling slows host copies)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every configuration of the workload table (one JSON line each)")
-    ap.add_argument("--case", choices=["ce", "sbv", "flce", "fljsd", "ce_fb", "sbv_fb", "flce_fb"],
+    ap.add_argument("--case", choices=["ce", "sbv", "flce", "fljsd", "ce_fb", "sbv_fb", "flce_fb", "fljsd_fb"],
                     help="time one op alone at --T/--V/--H (profiling runs); prints one JSON line")
     ap.add_argument("--T", type=int, default=None, help="tokens (ce: rows; sbv: seq, batch 4)")
     ap.add_argument("--V", type=int, default=None)
@@ -563,6 +563,15 @@ def run_case(args):
         dW = torch.empty((V, H), dtype=torch.float32, device="cuda")
         fn = lambda: lmho.flce_fwd_bwd_bf16(x, W, t, 1.0, ws=ws, dx=dx, dW=dW)  # noqa: E731
         work, unit = rl.flce_fwd_bwd_flops(T, H, V), "TFLOP/s"
+    elif c == "fljsd_fb":
+        T, V = args.T or FLJSD["T"], args.V or FLJSD["V"]
+        xs, Ws = bf16(args.seed, 0, (T, H), 1.0), bf16(args.seed, 2, (V, H), 0.02)
+        xt, Wt = bf16(args.seed, 3, (T, H), 1.0), bf16(args.seed, 4, (V, H), 0.02)
+        ws = lmho.workspace(lmho.fljsd_bwd_workspace_bytes(T, H, V))
+        dxs = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        dWs = torch.empty((V, H), dtype=torch.float32, device="cuda")
+        fn = lambda: lmho.fljsd_fwd_bwd_bf16(xs, Ws, xt, Wt, 0.5, ws=ws, dxs=dxs, dWs=dWs)  # noqa: E731
+        work, unit = rl.fljsd_fwd_bwd_flops(T, H, V), "TFLOP/s"
     else:
         T, V = args.T or FLJSD["T"], args.V or FLJSD["V"]
         xs, Ws = bf16(args.seed, 0, (T, H), 1.0), bf16(args.seed, 2, (V, H), 0.02)
@@ -578,7 +587,7 @@ def run_case(args):
     # 129 MB L2, and a write-based flush would leave ~129 MB of dirty lines
     # whose write-back the timed kernel would pay for.
     flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
-    nk = {"ce": 1, "sbv": 1, "flce": 2, "fljsd": 4, "ce_fb": 1, "sbv_fb": 1, "flce_fb": 5}[c]
+    nk = {"ce": 1, "sbv": 1, "flce": 2, "fljsd": 4, "ce_fb": 1, "sbv_fb": 1, "flce_fb": 5, "fljsd_fb": 5}[c]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     for row in evs:
         for e in row:
@@ -609,6 +618,7 @@ SWEEP = ([("ce", 16384, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
          [("sbv", 2048, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
          [("flce", 1024 * b, 128256) for b in (2, 4, 8, 16)] +
          [("flce_fb", 1024 * b, 128256) for b in (2, 16)] +
+         [("fljsd_fb", T, 128256) for T in (1024, 8192)] +
          [("fljsd", T, 128256) for T in (1024, 2048, 4096, 8192)])
 
 
@@ -620,7 +630,7 @@ def run_sweep(args):
     for case, T, V in SWEEP:
         a = argparse.Namespace(**vars(args))
         a.case, a.T, a.V = case, T, V
-        a.steps = max(args.steps, 3) if case in ("ce", "sbv", "ce_fb", "sbv_fb") else (2 if case == "flce_fb" else 3)
+        a.steps = max(args.steps, 3) if case in ("ce", "sbv", "ce_fb", "sbv_fb") else (2 if case in ("flce_fb", "fljsd_fb") else 3)
         a.warmup = max(1, min(args.warmup, 2))
         r = run_case(a)
         if "GB/s" in r:

@@ -227,6 +227,24 @@ int fljsd_fwd_bf16_ex(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt
                       size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Fused linear + generalized JSD, forward and the student's backward (the
+ * teacher is held fixed, as in distillation).  Loss as fljsd_fwd_bf16_ex;
+ * gradients of grad_scale * loss with respect to the student input and head:
+ *   dzs = (grad_scale / (n_kept temperature)) beta P (ln P - ln M - KL(P || M)),
+ *   dxs = dZs Ws  [T, H] fp32,  dWs = dZs^T xs  [V, H] fp32,
+ * (dJSD/dP = beta ln(P / M) through the softmax); left-out tokens contribute
+ * nothing.  dZs is formed on the tensor cores from a third pass over both
+ * heads' logit tiles, rounded to bf16 and kept in the workspace with its
+ * transpose.  Arguments as fljsd_fwd_bf16_ex; dxs, dWs 16-byte aligned;
+ * ws_bytes >= fljsd_bwd_workspace_bytes(T, H, V), zeroed before first use.
+ * ------------------------------------------------------------------------ */
+size_t fljsd_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V);
+int fljsd_fwd_bwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt,
+                       const uint16_t* Wt, int64_t T, int64_t H, int64_t V, float beta,
+                       float temperature, const uint8_t* keep, float grad_scale, float* loss,
+                       float* dxs, float* dWs, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Device status of a workspace-carrying call (flce, fljsd).
  * Synchronises `stream`, reads the status word of `ws`, clears it, and returns
  * LMHO_OK or LMHO_ERR_TIMEOUT (a bounded wait inside a kernel gave up; that

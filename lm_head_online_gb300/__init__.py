@@ -35,6 +35,7 @@ EXPORTS = (
     "lmho_strerror", "lmho_version", "ce_workspace_bytes", "ce_fwd_f32", "ce_fwd_f32_noalloc", "ce_fwd_sbv_bf16",
     "ce_fwd_bwd_f32", "ce_fwd_bwd_sbv_bf16",
     "flce_workspace_bytes", "flce_fwd_bf16", "flce_bwd_workspace_bytes", "flce_fwd_bwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
+    "fljsd_bwd_workspace_bytes", "fljsd_fwd_bwd_bf16",
     "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
 
@@ -90,6 +91,10 @@ def load():
         lib.fljsd_fwd_bf16.restype = ci
         lib.fljsd_fwd_bf16_ex.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, f32, vp, vp, vp, sz, vp]
         lib.fljsd_fwd_bf16_ex.restype = ci
+        lib.fljsd_bwd_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.fljsd_bwd_workspace_bytes.restype = sz
+        lib.fljsd_fwd_bwd_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, f32, vp, f32, vp, vp, vp, vp, sz, vp]
+        lib.fljsd_fwd_bwd_bf16.restype = ci
         lib.lmho_ws_status.argtypes = [vp, sz, vp]
         lib.lmho_ws_status.restype = ci
         lib.lmho_set_ce_variant.argtypes = [ci]
@@ -365,6 +370,45 @@ def fljsd_fwd_bf16_ex(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, loss
                                  _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8), ws.numel(),
                                  _stream(stream)), "fljsd_fwd_bf16_ex")
     return loss
+
+
+def fljsd_bwd_workspace_bytes(T: int, H: int, V: int) -> int:
+    return int(load().fljsd_bwd_workspace_bytes(T, H, V))
+
+
+def fljsd_fwd_bwd_bf16(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, grad_scale=1.0, loss=None, dxs=None,
+                       dWs=None, ws=None, stream=None):
+    """Fused linear + JSD and the student gradients of grad_scale * loss:
+    returns (loss fp32 [1], dxs fp32 [T, H], dWs fp32 [V, H])."""
+    lib = load()
+    p1 = _dev(xs, "xs", torch.bfloat16, 2)
+    p2 = _dev(Ws, "Ws", torch.bfloat16, 2)
+    p3 = _dev(xt, "xt", torch.bfloat16, 2)
+    p4 = _dev(Wt, "Wt", torch.bfloat16, 2)
+    T, H = xs.shape
+    V = Ws.shape[0]
+    if tuple(xt.shape) != (T, H) or tuple(Ws.shape) != (V, H) or tuple(Wt.shape) != (V, H):
+        raise ValueError("shape mismatch: xs, xt [T,H]; Ws, Wt [V,H]")
+    pk = None
+    if keep is not None:
+        if keep.dtype == torch.bool:
+            keep = keep.view(torch.uint8)
+        pk = _dev(keep, "keep", torch.uint8, 1)
+        if keep.shape[0] != T:
+            raise ValueError("keep must have T entries")
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=xs.device)
+    if dxs is None:
+        dxs = torch.empty((T, H), dtype=torch.float32, device=xs.device)
+    if dWs is None:
+        dWs = torch.empty((V, H), dtype=torch.float32, device=xs.device)
+    if ws is None:
+        ws = workspace(lib.fljsd_bwd_workspace_bytes(T, H, V), xs.device)
+    _check(lib.fljsd_fwd_bwd_bf16(p1, p2, p3, p4, T, H, V, float(beta), float(temperature), pk, float(grad_scale),
+                                  _dev(loss, "loss", torch.float32), _dev(dxs, "dxs", torch.float32, 2),
+                                  _dev(dWs, "dWs", torch.float32, 2), _dev(ws, "ws", torch.uint8), ws.numel(),
+                                  _stream(stream)), "fljsd_fwd_bwd_bf16")
+    return loss, dxs, dWs
 
 
 def row_losses(ws: torch.Tensor, T: int) -> torch.Tensor:

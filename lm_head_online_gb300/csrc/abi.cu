@@ -235,13 +235,15 @@ struct BwdLayout {
   int64_t ld_dz, ld_dzt, ld_wt, ld_xt;
   size_t off_lse, off_dz, off_dzt, off_wt, off_xt, end;
 };
-BwdLayout bwd_layout(int64_t T, int64_t H, int64_t V) {
+// `base` = the forward's workspace bytes (its carve-up comes first, with its
+// control block moved to the very end).
+BwdLayout bwd_layout(int64_t T, int64_t H, int64_t V, size_t base) {
   BwdLayout b{};
   b.ld_dz = (V + kBN_CE - 1) / kBN_CE * kBN_CE;
   b.ld_dzt = (T + 7) / 8 * 8;
   b.ld_wt = (V + 7) / 8 * 8;
   b.ld_xt = (T + 7) / 8 * 8;
-  size_t o = flce_ws_bytes(T, H, V);  // the forward's carve-up comes first
+  size_t o = base;
   b.off_lse = o;
   o += align_up(4 * static_cast<size_t>(T));
   b.off_dz = o;
@@ -257,10 +259,12 @@ BwdLayout bwd_layout(int64_t T, int64_t H, int64_t V) {
 }
 }  // namespace
 
-size_t flce_bwd_ws_bytes(int64_t T, int64_t H, int64_t V) { return bwd_layout(T, H, V).end; }
+size_t flce_bwd_ws_bytes(int64_t T, int64_t H, int64_t V) {
+  return bwd_layout(T, H, V, flce_ws_bytes(T, H, V)).end;
+}
 
-FlceBwdWs flce_bwd_ws_carve(void* ws, int64_t T, int64_t H, int64_t V) {
-  const BwdLayout b = bwd_layout(T, H, V);
+namespace {
+FlceBwdWs bwd_carve(void* ws, const BwdLayout& b) {
   char* p = static_cast<char*>(ws);
   FlceBwdWs w{};
   w.lse = reinterpret_cast<float*>(p + b.off_lse);
@@ -273,6 +277,17 @@ FlceBwdWs flce_bwd_ws_carve(void* ws, int64_t T, int64_t H, int64_t V) {
   w.ld_wt = b.ld_wt;
   w.ld_xt = b.ld_xt;
   return w;
+}
+}  // namespace
+
+FlceBwdWs flce_bwd_ws_carve(void* ws, int64_t T, int64_t H, int64_t V) {
+  return bwd_carve(ws, bwd_layout(T, H, V, flce_ws_bytes(T, H, V)));
+}
+
+// JSD backward: the JSD forward's workspace, then the same backward buffers
+// (the per-row slot holds KL(P || M)), then one float for 1 / kept count.
+size_t fljsd_bwd_ws_bytes(int64_t T, int64_t H, int64_t V) {
+  return bwd_layout(T, H, V, fljsd_ws_bytes(T, H, V)).end + kAlign;
 }
 
 // Partials: the log-sum-exp pass writes (max, sum) per (head, 256-wide vocab
@@ -519,6 +534,46 @@ int fljsd_fwd_bf16_ex(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt
                       int64_t H, int64_t V, float beta, float temperature, const uint8_t* keep, float* loss, void* ws,
                       size_t ws_bytes, void* stream) {
   return fljsd_impl(xs, Ws, xt, Wt, T, H, V, beta, temperature, keep, loss, ws, ws_bytes, stream);
+}
+
+size_t fljsd_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
+  if (T <= 0 || V <= 0 || H <= 0) return kAlign;
+  return fljsd_bwd_ws_bytes(T, H, V);
+}
+
+int fljsd_fwd_bwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, const uint16_t* Wt, int64_t T,
+                       int64_t H, int64_t V, float beta, float temperature, const uint8_t* keep, float grad_scale,
+                       float* loss, float* dxs, float* dWs, void* ws, size_t ws_bytes, void* stream) {
+  if (!xs || !Ws || !xt || !Wt || !loss || !dxs || !dWs || !ws) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_fused_common(T, H, V)) return c;
+  if (!(beta > 0.f && beta < 1.f)) return LMHO_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !(1.f / temperature < INFINITY) || !std::isfinite(grad_scale)) return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(xs) || !aligned16(Ws) || !aligned16(xt) || !aligned16(Wt) || !aligned16(dxs) || !aligned16(dWs))
+    return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < fljsd_bwd_ws_bytes(T, H, V) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const size_t xb = 2 * static_cast<size_t>(T) * H, wb = 2 * static_cast<size_t>(V) * H;
+  const Range in[5] = {rng(xs, xb), rng(Ws, wb), rng(xt, xb), rng(Wt, wb), rng(keep, keep ? static_cast<size_t>(T) : 0)};
+  const Range out[4] = {rng(loss, 4), rng(dxs, 4 * static_cast<size_t>(T) * H), rng(dWs, 4 * static_cast<size_t>(V) * H),
+                        rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 5, out, 4)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  const BwdLayout lay = bwd_layout(T, H, V, fljsd_ws_bytes(T, H, V));
+  const FusedWs w = fljsd_ws_carve(ws, ws_bytes, T, V);
+  const FlceBwdWs bw = bwd_carve(ws, lay);
+  float* inv_count = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.end - kAlign);
+  FljsdBwdMaps m;
+  if (tmap_bf16(&m.xs, xs, T, H, kBM) || tmap_bf16(&m.xt, xt, T, H, kBM) || tmap_bf16(&m.ws256, Ws, V, H, kBN_CE) ||
+      tmap_bf16(&m.wt256, Wt, V, H, kBN_CE) || tmap_bf16(&m.wsj, Ws, V, H, kBN_JSD) ||
+      tmap_bf16(&m.wtj, Wt, V, H, kBN_JSD) || tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) ||
+      tmap_bf16_ld(&m.wst, bw.wt, H, V, bw.ld_wt, kBN_CE) || tmap_bf16_ld(&m.dzt, bw.dzt, V, T, bw.ld_dzt, kBM) ||
+      tmap_bf16_ld(&m.xst, bw.xt, H, T, bw.ld_xt, kBN_CE))
+    return LMHO_ERR_CUDA;
+  const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD);
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_fljsd_fwd_bwd(m, xs, Ws, g1, g2, beta, 1.f / temperature, keep, grad_scale, loss, dxs, dWs,
+                                          w, bw, bw.lse, inv_count, L));
 }
 
 int lmho_ws_status(void* ws, size_t ws_bytes, void* stream) {

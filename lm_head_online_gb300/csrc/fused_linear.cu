@@ -47,20 +47,25 @@ namespace {
 // logits, written as bf16 dZ [T, ld_dz] and its transpose dZ^T [V, ld_dzt]
 // (inputs of the two backward GEMMs).  STORE: plain fp32 tile store (the
 // backward GEMMs dx = dZ W and dW = dZ^T x; rows = T, columns = V in Params).
-enum Mode { kModeCE = 0, kModeLSE = 1, kModeJSD = 2, kModeDZ = 3, kModeStore = 4 };
+// JSDK: the divergence pass that also sums KL(P || M) per row (backward only).
+// DZJ: both heads recomputed, the student's gradient dZs written like DZ.
+enum Mode { kModeCE = 0, kModeLSE = 1, kModeJSD = 2, kModeDZ = 3, kModeStore = 4, kModeJSDK = 5, kModeDZJ = 6 };
+
+template <int MODE>
+constexpr bool two_head() { return MODE == kModeJSD || MODE == kModeJSDK || MODE == kModeDZJ; }
 
 constexpr int kTmemCols = 512;   // all of TMEM: accumulators of 256 or 512 fp32 columns
 constexpr int kSmemBudget = 192 * 1024;
 
 template <int MODE>
 struct ModeCfg {
-  static constexpr int BN = (MODE == kModeJSD) ? kBN_JSD : kBN_CE;
-  static constexpr int kHeadsPerUnit = (MODE == kModeJSD) ? 2 : 1;
+  static constexpr int BN = two_head<MODE>() ? kBN_JSD : kBN_CE;
+  static constexpr int kHeadsPerUnit = two_head<MODE>() ? 2 : 1;
   static constexpr int kAccCols = BN * kHeadsPerUnit;      // TMEM columns of one accumulator
   static constexpr int kNumAcc = kTmemCols / kAccCols;     // 2 = double-buffered, 1 = single
   // Epilogue warps: 4 cover the 128 TMEM lanes; 8 = two per lane quadrant,
   // each taking half of the columns (the two-head epilogue is the heavier one).
-  static constexpr int kEpiWarps = (MODE == kModeJSD) ? 4 * kJsdColSplit : 4;
+  static constexpr int kEpiWarps = two_head<MODE>() ? 4 * kJsdColSplit : 4;
   static constexpr int kColSplit = kEpiWarps / 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;    // producer warp, MMA warp, epilogue
   static constexpr int kABytes = kBM * kBK * 2;
@@ -95,6 +100,9 @@ struct Params {
   int64_t ld_dz, ld_dzt;
   float* out;        // STORE: fp32 [T, ld_out]
   int64_t ld_out;
+  const float* kl;         // DZJ: KL(P || M) of every row
+  const uint8_t* keep;     // DZJ: token mask (null = all kept)
+  const float* inv_count;  // DZJ: 1 / number of kept tokens (device scalar)
   uint64_t timeout_ns;
   uint32_t* status;
 };
@@ -154,6 +162,21 @@ __device__ __forceinline__ float jsd_term(float lp, float lq, float beta, float 
   const float a_lo = a_hi - d;
   const float p_hi = ex2_approx(hi * kLog2e);
   return p_hi * (w_hi * a_hi + w_lo * e * a_lo);
+}
+
+// The pieces of one generalized-JSD pair the backward needs: P = e^{lp} and
+// lp - lm (same larger-side evaluation as jsd_term).
+__device__ __forceinline__ void jsd_student(float lp, float lq, float beta, float omb, float* P, float* lp_lm) {
+  const float hi = fmaxf(lp, lq);
+  const float d = fabsf(lp - lq);
+  const bool p_is_hi = lp >= lq;
+  const float w_hi = p_is_hi ? beta : omb;
+  const float w_lo = p_is_hi ? omb : beta;
+  const float e = ex2_approx(-d * kLog2e);
+  const float a_hi = -kLn2 * lg2_approx(fmaf(w_lo, e, w_hi));
+  const float p_hi = ex2_approx(hi * kLog2e);
+  *P = p_is_hi ? p_hi : p_hi * e;
+  *lp_lm = p_is_hi ? a_hi : a_hi - d;
 }
 
 template <int MODE>
@@ -290,9 +313,15 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       float ls = 0.f, lt = 0.f;
       if ((MODE == kModeCE || MODE == kModeDZ) && row_ok) tgt = __ldg(p.target + row);
       if (MODE == kModeDZ && row_ok) ls = __ldg(p.lse + row);
-      if (MODE == kModeJSD && row_ok) {
+      if (two_head<MODE>() && row_ok) {
         ls = __ldg(p.lse + row);
         lt = __ldg(p.lse + p.T + row);
+      }
+      float krow = 0.f, gj = 0.f;
+      if (MODE == kModeDZJ && row_ok) {
+        krow = __ldg(p.kl + row);
+        const bool kept = !p.keep || __ldg(p.keep + row);
+        gj = kept ? p.gscale * __ldg(p.inv_count) * beta : 0.f;
       }
       // tcgen05.ld is warp-collective: the whole warp proceeds or gives up together
       const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[acc], acc_phase, p.timeout_ns, p.status));
@@ -302,11 +331,46 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       MS st = ms_empty();
       float zt = 0.f;
       bool has_t = false;
-      float jsd = 0.f;
+      float jsd = 0.f, kacc = 0.f;
 #pragma unroll 1
       for (int cc = 0; cc < kCols / 32; ++cc) {
         const int64_t col0 = n0 + cc * 32;
-        if (MODE == kModeJSD) {
+        if (MODE == kModeJSDK) {
+          float vs[32], vt[32];
+          tmem_ld32_sync(tbase + cc * 32, vs);
+          tmem_ld32_sync(tbase + BN + cc * 32, vt);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (col0 + j < p.V) {
+              const float lp = fmaf(vs[j], it, -ls), lq = fmaf(vt[j], it, -lt);
+              float P, lplm;
+              jsd_student(lp, lq, beta, omb, &P, &lplm);
+              jsd += jsd_term(lp, lq, beta, omb);
+              kacc = fmaf(P, lplm, kacc);
+            }
+          }
+        } else if (MODE == kModeDZJ) {
+          float vs[32], vt[32];
+          tmem_ld32_sync(tbase + cc * 32, vs);
+          tmem_ld32_sync(tbase + BN + cc * 32, vt);
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              float P, lplm;
+              jsd_student(fmaf(vs[j], it, -ls), fmaf(vt[j], it, -lt), beta, omb, &P, &lplm);
+              vs[j] = (col0 + j < p.V) ? gj * P * (lplm - krow) : 0.f;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.dz + row * p.ld_dz + col0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              dst[k] = make_uint4(pack_bf16x2(vs[8 * k], vs[8 * k + 1]), pack_bf16x2(vs[8 * k + 2], vs[8 * k + 3]),
+                                  pack_bf16x2(vs[8 * k + 4], vs[8 * k + 5]), pack_bf16x2(vs[8 * k + 6], vs[8 * k + 7]));
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < p.V)
+                p.dzt[(col0 + j) * p.ld_dzt + row] = static_cast<uint16_t>(pack_bf16x2(vs[j], 0.f));
+          }
+        } else if (MODE == kModeJSD) {
           float vs[32], vt[32];
           tmem_ld32_sync(tbase + cc * 32, vs);
           tmem_ld32_sync(tbase + BN + cc * 32, vt);
@@ -386,11 +450,12 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(&acc_empty[acc]);
       if (++acc == C::kNumAcc) { acc = 0; acc_phase ^= 1u; }
-      if (row_ok && (MODE == kModeCE || MODE == kModeLSE || MODE == kModeJSD)) {
+      if (row_ok && (MODE == kModeCE || MODE == kModeLSE || MODE == kModeJSD || MODE == kModeJSDK)) {
         // partial slot of this (vocab tile, column slice)
         const int64_t slot = static_cast<int64_t>(c.nt) * C::kColSplit + half;
-        if (MODE == kModeJSD) {
+        if (MODE == kModeJSD || MODE == kModeJSDK) {
           p.part0[slot * p.T + row] = jsd;
+          if (MODE == kModeJSDK) p.part1[slot * p.T + row] = kacc;
         } else {
           const int64_t idx = (static_cast<int64_t>(c.head) * p.num_n * C::kColSplit + slot) * p.T + row;
           p.part0[idx] = st.m;
@@ -465,7 +530,8 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
 }
 
 __global__ void __launch_bounds__(kFinRows * kFinSplit)
-    jsd_finalize(const float* pj, int64_t T, int num_n, const uint8_t* keep, float* row_out, float* loss, Ctrl* ctrl) {
+    jsd_finalize(const float* pj, int64_t T, int num_n, const uint8_t* keep, float* row_out, float* loss, Ctrl* ctrl,
+                 const float* pk = nullptr, float* kl_out = nullptr, float* inv_count_out = nullptr) {
   __shared__ float s_tmp[kFinRows * kFinSplit];
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kFinRows + l;
@@ -483,7 +549,22 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
     for (int k = 0; k < kFinSplit; ++k) tot.add(s_tmp[k * 32 + l]);
     row_out[row] = (keep && !__ldg(keep + row)) ? 0.f : tot.s - tot.c;
   }
-  mean_tail(row_out, T, loss, ctrl, gridDim.x, keep);
+  if (pk) {  // the same fixed-order sum of the KL(P || M) partials
+    __syncthreads();
+    KSum b;
+    if (row < T) {
+#pragma unroll 4
+      for (int n = n_lo; n < n_hi; ++n) b.add(__ldcg(pk + static_cast<int64_t>(n) * T + row));
+    }
+    s_tmp[w * 32 + l] = b.s - b.c;
+    __syncthreads();
+    if (w == 0 && row < T) {
+      KSum tot;
+      for (int k = 0; k < kFinSplit; ++k) tot.add(s_tmp[k * 32 + l]);
+      kl_out[row] = tot.s - tot.c;
+    }
+  }
+  mean_tail(row_out, T, loss, ctrl, gridDim.x, keep, inv_count_out);
 }
 
 // out[c, r] = in[r, c] for a bf16 matrix in [rows, cols] (row-major) into
@@ -698,6 +779,85 @@ cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const uint16_t* x, const u
   b.out = dW;
   b.ld_out = g.H;
   if ((e = launch_gemm<kModeStore>(m.dzt, m.xt, m.dzt, m.xt, b, L)) != cudaSuccess) return e;
+  launch_mark(5, L.stream);
+  return cudaSuccess;
+}
+
+cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const uint16_t* xs, const uint16_t* Ws,
+                                 const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta, float inv_tau,
+                                 const uint8_t* keep, float grad_scale, float* loss, float* dxs, float* dWs,
+                                 const FusedWs& ws, const FlceBwdWs& bw, float* kl, float* inv_count,
+                                 const FusedLaunch& L) {
+  cudaError_t e;
+  const int64_t T = g_lse.T, H = g_lse.H, V = g_lse.V;
+  launch_mark(0, L.stream);
+  if ((e = launch_transpose_bf16(Ws, V, H, bw.wt, bw.ld_wt, L.stream)) != cudaSuccess) return e;
+  if ((e = launch_transpose_bf16(xs, T, H, bw.xt, bw.ld_xt, L.stream)) != cudaSuccess) return e;
+  launch_mark(1, L.stream);
+  // pass 1: log-sum-exp of both heads
+  Params p = base_params(g_lse, L, ws.ctrl);
+  p.units = 2 * g_lse.num_m * g_lse.num_n;
+  p.part0 = ws.part0;
+  p.part1 = ws.part1;
+  p.inv_tau = inv_tau;
+  if ((e = launch_gemm<kModeLSE>(m.xs, m.ws256, m.xt, m.wt256, p, L)) != cudaSuccess) return e;
+  dim3 fb(static_cast<unsigned>((T + kFinRows - 1) / kFinRows), 2);
+  lse_finalize<<<fb, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, ws.part1, T, static_cast<int>(g_lse.num_n), ws.lse);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // pass 2: divergence and KL(P || M) of every row
+  Params q = base_params(g_jsd, L, ws.ctrl);
+  q.units = g_jsd.num_m * g_jsd.num_n;
+  q.part0 = ws.part0;
+  q.part1 = ws.part1;
+  q.lse = ws.lse;
+  q.beta = beta;
+  q.inv_tau = inv_tau;
+  if ((e = launch_gemm<kModeJSDK>(m.xs, m.wsj, m.xt, m.wtj, q, L)) != cudaSuccess) return e;
+  const unsigned blocks = static_cast<unsigned>((T + kFinRows - 1) / kFinRows);
+  const int nslots = static_cast<int>(g_jsd.num_n * ModeCfg<kModeJSDK>::kColSplit);
+  jsd_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, T, nslots, keep, ws.row_out, loss, ws.ctrl,
+                                                              ws.part1, kl, inv_count);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  launch_mark(2, L.stream);
+  // pass 3: both heads again, the student's dZ and dZ^T
+  Params r = base_params(g_jsd, L, ws.ctrl);
+  r.units = g_jsd.num_m * g_jsd.num_n;
+  r.lse = ws.lse;
+  r.beta = beta;
+  r.inv_tau = inv_tau;
+  r.gscale = grad_scale * inv_tau;
+  r.kl = kl;
+  r.keep = keep;
+  r.inv_count = inv_count;
+  r.dz = bw.dz;
+  r.dzt = bw.dzt;
+  r.ld_dz = bw.ld_dz;
+  r.ld_dzt = bw.ld_dzt;
+  if ((e = launch_gemm<kModeDZJ>(m.xs, m.wsj, m.xt, m.wtj, r, L)) != cudaSuccess) return e;
+  launch_mark(3, L.stream);
+  // dxs = dZs Ws, dWs = dZs^T xs
+  FusedGeometry gx = g_lse;
+  gx.V = H;
+  gx.H = V;
+  gx.num_m = (T + kBM - 1) / kBM;
+  gx.num_n = (H + kBN_CE - 1) / kBN_CE;
+  Params a = base_params(gx, L, ws.ctrl);
+  a.units = gx.num_m * gx.num_n;
+  a.out = dxs;
+  a.ld_out = H;
+  if ((e = launch_gemm<kModeStore>(m.dz, m.wst, m.dz, m.wst, a, L)) != cudaSuccess) return e;
+  launch_mark(4, L.stream);
+  FusedGeometry gw = g_lse;
+  gw.T = V;
+  gw.V = H;
+  gw.H = T;
+  gw.num_m = (V + kBM - 1) / kBM;
+  gw.num_n = (H + kBN_CE - 1) / kBN_CE;
+  Params b = base_params(gw, L, ws.ctrl);
+  b.units = gw.num_m * gw.num_n;
+  b.out = dWs;
+  b.ld_out = H;
+  if ((e = launch_gemm<kModeStore>(m.dzt, m.xst, m.dzt, m.xst, b, L)) != cudaSuccess) return e;
   launch_mark(5, L.stream);
   return cudaSuccess;
 }

@@ -118,6 +118,19 @@ cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const uint16_t* x, const u
                                 const FusedGeometry& g, float grad_scale, float* loss, float* dx, float* dW,
                                 const FusedWs& ws, const FlceBwdWs& bw, const FusedLaunch& L);
 
+// Fused linear + JSD forward and student backward.
+struct FljsdBwdMaps {
+  CUtensorMap xs, xt, ws256, wt256, wsj, wtj;  // the forward passes, and the dZ pass
+  CUtensorMap dz, wst;                          // dxs = dZs Ws:   A = dZs [T, V], B = Ws^T [H, V]
+  CUtensorMap dzt, xst;                         // dWs = dZs^T xs: A = dZs^T [V, T], B = xs^T [H, T]
+};
+size_t fljsd_bwd_ws_bytes(int64_t T, int64_t H, int64_t V);
+cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const uint16_t* xs, const uint16_t* Ws,
+                                 const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta, float inv_tau,
+                                 const uint8_t* keep, float grad_scale, float* loss, float* dxs, float* dWs,
+                                 const FusedWs& ws, const FlceBwdWs& bw, float* kl, float* inv_count,
+                                 const FusedLaunch& L);
+
 cudaError_t launch_wait_selftest(Ctrl* ctrl, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace lmho

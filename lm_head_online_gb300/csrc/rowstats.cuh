@@ -120,7 +120,7 @@ struct KSum {
 // is the number of kept rows (a mean over no row is 0); left-out rows must
 // already hold 0 in row_loss.
 __device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, float* loss, Ctrl* ctrl, uint32_t nwriters,
-                                          const uint8_t* keep = nullptr) {
+                                          const uint8_t* keep = nullptr, float* inv_count_out = nullptr) {
   constexpr int kVL = 256;
   __shared__ uint32_t s_last;
   __shared__ float s_part[kVL];
@@ -178,6 +178,7 @@ __device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, floa
     if (threadIdx.x == 0) {
       const int64_t count = keep ? n : T;
       *loss = count > 0 ? v / static_cast<float>(count) : 0.f;
+      if (inv_count_out) *inv_count_out = count > 0 ? 1.f / static_cast<float>(count) : 0.f;
       ctrl->ticket = 0u;
       __threadfence();
     }

@@ -57,6 +57,12 @@ def fljsd_flops(T: int, H: int, V: int) -> int:
     return 8 * T * V * H
 
 
+def fljsd_fwd_bwd_flops(T: int, H: int, V: int) -> int:
+    """Forward (two passes over both heads), a third pass over both heads for
+    the student's dZ, and the two student gradient products."""
+    return 16 * T * V * H
+
+
 def fljsd_pass_flops(T: int, H: int, V: int) -> int:
     """One pass over both heads (the log-sum-exp pass or the divergence pass)."""
     return 4 * T * V * H
