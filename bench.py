@@ -51,13 +51,13 @@ KERNELS_PER_STEP = 1 + 1 + 2 + 4
 # profiles/dram_traffic_bench_step.md).  They hold only for the kernel sources
 # they were taken from: a changed source makes the bench report null.
 KERNEL_SOURCES = ("fused_linear.cu", "ce_rows.cu", "rowstats.cuh", "ptx.cuh", "lmho_internal.h")
-TRAFFIC_SOURCE_DIGEST = "31f291a11039aea6"
+TRAFFIC_SOURCE_DIGEST = "7df7c427b4e448a6"
 TRAFFIC_BYTES = {
-    "ce_fwd_f32.row_kernel": 8590396672 + 2961408,
-    "ce_fwd_sbv_bf16.row_kernel": 2147622656 + 106496,
-    "flce.tcgen05_gemm_ce": 8542083584 + 65795072,
-    "fljsd.tcgen05_gemm_lse": 8541265920 + 65339648,
-    "fljsd.tcgen05_gemm_jsd": 10565027584 + 33126656,
+    "ce_fwd_f32.row_kernel": 8590294272 + 2893568,
+    "ce_fwd_sbv_bf16.row_kernel": 2147606784 + 165376,
+    "flce.tcgen05_gemm_ce": 8541684992 + 65786880,
+    "fljsd.tcgen05_gemm_lse": 8541654528 + 65471232,
+    "fljsd.tcgen05_gemm_jsd": 10554021632 + 32813568,
 }
 
 
