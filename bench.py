@@ -587,7 +587,7 @@ def run_case(args):
     # 129 MB L2, and a write-based flush would leave ~129 MB of dirty lines
     # whose write-back the timed kernel would pay for.
     flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
-    nk = {"ce": 1, "sbv": 1, "flce": 2, "fljsd": 4, "ce_fb": 1, "sbv_fb": 1, "flce_fb": 5, "fljsd_fb": 5}[c]
+    nk = {"ce": 1, "sbv": 1, "flce": 2, "fljsd": 4, "ce_fb": 1, "sbv_fb": 1, "flce_fb": 4, "fljsd_fb": 4}[c]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     for row in evs:
         for e in row:

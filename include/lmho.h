@@ -174,12 +174,16 @@ int flce_fwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, i
  * dZ is recomputed on the tensor cores from a second pass over the logit
  * tiles (after the forward pass gives each row's log-sum-exp), rounded to
  * bf16 (as the GEMM operand of the two gradient products) and kept in the
- * workspace with its transpose; the logits themselves are never stored.
+ * workspace; both products read it, W and x in place (no transposed copies);
+ * the logits themselves are never stored.  When dx has too few output tiles
+ * to fill the GPU (small T) its K range is split into fp32 slices summed in a
+ * fixed order, so results stay bitwise reproducible.
  * x, W, dx, dW 16-byte aligned; H % 8 == 0.  grad_scale finite.  A target
  * outside [0, V) makes that token's loss, its dx row and all of dW NaN.
- *   ws   ws_bytes >= flce_bwd_workspace_bytes(T, H, V) (about 4 T V + 2 (V + T) H
- *        bytes beyond the forward's), zeroed before first use; the first T
- *        floats hold the per-token losses afterwards.
+ *   ws   ws_bytes >= flce_bwd_workspace_bytes(T, H, V) (about 2 T V bytes beyond
+ *        the forward's, plus up to 32 T H for the split slices when T H is
+ *        small), zeroed before first use; the first T floats hold the per-token
+ *        losses afterwards.
  * ------------------------------------------------------------------------ */
 size_t flce_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V);
 int flce_fwd_bwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t T,
@@ -234,8 +238,9 @@ int fljsd_fwd_bf16_ex(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt
  *   dxs = dZs Ws  [T, H] fp32,  dWs = dZs^T xs  [V, H] fp32,
  * (dJSD/dP = beta ln(P / M) through the softmax); left-out tokens contribute
  * nothing.  dZs is formed on the tensor cores from a third pass over both
- * heads' logit tiles, rounded to bf16 and kept in the workspace with its
- * transpose.  Arguments as fljsd_fwd_bf16_ex; dxs, dWs 16-byte aligned;
+ * heads' logit tiles, rounded to bf16 and kept in the workspace; the gradient
+ * products read it as flce_fwd_bwd_bf16 does.  Arguments as
+ * fljsd_fwd_bf16_ex; dxs, dWs 16-byte aligned;
  * ws_bytes >= fljsd_bwd_workspace_bytes(T, H, V), zeroed before first use.
  * ------------------------------------------------------------------------ */
 size_t fljsd_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V);

@@ -175,6 +175,20 @@ int tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t H, uint32_
   return tmap_bf16_ld(m, base, rows, H, H, box_rows);
 }
 
+// bf16 matrix [k_rows, mn] (row-major, MN contiguous, row stride ld >= mn
+// elements, ld * 2 a multiple of 16) read MN-major: box = 64 (MN) x 64 (K),
+// 128-byte swizzle; reads past either edge are zero-filled.
+int tmap_bf16_mn(CUtensorMap* m, const void* base, int64_t k_rows, int64_t mn, int64_t ld) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(mn), static_cast<cuuint64_t>(k_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBK)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LMHO_OK : LMHO_ERR_CUDA;
+}
+
 FusedGeometry geometry(int64_t T, int64_t H, int64_t V, int bn) {
   FusedGeometry g{};
   g.T = T;
@@ -229,31 +243,28 @@ FusedWs flce_ws_carve(void* ws, size_t ws_bytes, int64_t T, int64_t V) {
   return w;
 }
 // Fused linear + CE backward: the forward's workspace, then the log-sum-exp of
-// every row, dZ, dZ^T, W^T and x^T (bf16, padded row strides).
+// every row, dZ (bf16, row stride padded to whole 256-column tiles) and the
+// fp32 K slices of a split gradient product (sized for the larger of dx and dW
+// where either can split).
 namespace {
 struct BwdLayout {
-  int64_t ld_dz, ld_dzt, ld_wt, ld_xt;
-  size_t off_lse, off_dz, off_dzt, off_wt, off_xt, end;
+  int64_t ld_dz;
+  size_t off_lse, off_dz, off_split, split_bytes, end;
 };
 // `base` = the forward's workspace bytes (its carve-up comes first, with its
 // control block moved to the very end).
 BwdLayout bwd_layout(int64_t T, int64_t H, int64_t V, size_t base) {
   BwdLayout b{};
   b.ld_dz = (V + kBN_CE - 1) / kBN_CE * kBN_CE;
-  b.ld_dzt = (T + 7) / 8 * 8;
-  b.ld_wt = (V + 7) / 8 * 8;
-  b.ld_xt = (T + 7) / 8 * 8;
   size_t o = base;
   b.off_lse = o;
   o += align_up(4 * static_cast<size_t>(T));
   b.off_dz = o;
   o += align_up(2 * static_cast<size_t>(T) * b.ld_dz);
-  b.off_dzt = o;
-  o += align_up(2 * static_cast<size_t>(V) * b.ld_dzt);
-  b.off_wt = o;
-  o += align_up(2 * static_cast<size_t>(H) * b.ld_wt);
-  b.off_xt = o;
-  o += align_up(2 * static_cast<size_t>(H) * b.ld_xt);
+  const size_t rx = k_split_reserve_bytes(T, H), rw = k_split_reserve_bytes(V, H);
+  b.split_bytes = rx > rw ? rx : rw;
+  b.off_split = o;
+  o += align_up(b.split_bytes);
   b.end = o + kAlign;  // the control block stays the last 256 bytes
   return b;
 }
@@ -269,13 +280,8 @@ FlceBwdWs bwd_carve(void* ws, const BwdLayout& b) {
   FlceBwdWs w{};
   w.lse = reinterpret_cast<float*>(p + b.off_lse);
   w.dz = reinterpret_cast<uint16_t*>(p + b.off_dz);
-  w.dzt = reinterpret_cast<uint16_t*>(p + b.off_dzt);
-  w.wt = reinterpret_cast<uint16_t*>(p + b.off_wt);
-  w.xt = reinterpret_cast<uint16_t*>(p + b.off_xt);
+  w.split = b.split_bytes ? reinterpret_cast<float*>(p + b.off_split) : nullptr;
   w.ld_dz = b.ld_dz;
-  w.ld_dzt = b.ld_dzt;
-  w.ld_wt = b.ld_wt;
-  w.ld_xt = b.ld_xt;
   return w;
 }
 }  // namespace
@@ -482,12 +488,12 @@ int flce_fwd_bwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* targe
   const FlceBwdWs bw = flce_bwd_ws_carve(ws, T, H, V);
   FlceBwdMaps m;
   if (tmap_bf16(&m.x, x, T, H, kBM) || tmap_bf16(&m.w, W, V, H, kBN_CE) ||
-      tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) || tmap_bf16_ld(&m.wt, bw.wt, H, V, bw.ld_wt, kBN_CE) ||
-      tmap_bf16_ld(&m.dzt, bw.dzt, V, T, bw.ld_dzt, kBM) || tmap_bf16_ld(&m.xt, bw.xt, H, T, bw.ld_xt, kBN_CE))
+      tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) || tmap_bf16_mn(&m.w_mn, W, V, H, H) ||
+      tmap_bf16_mn(&m.dz_mn, bw.dz, T, V, bw.ld_dz) || tmap_bf16_mn(&m.x_mn, x, T, H, H))
     return LMHO_ERR_CUDA;
   const FusedGeometry g = geometry(T, H, V, kBN_CE);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
-  return cuda_status(launch_flce_fwd_bwd(m, x, W, target, g, grad_scale, loss, dx, dW, w, bw, L));
+  return cuda_status(launch_flce_fwd_bwd(m, target, g, grad_scale, loss, dx, dW, w, bw, L));
 }
 
 size_t fljsd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
@@ -567,13 +573,13 @@ int fljsd_fwd_bwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* x
   if (tmap_bf16(&m.xs, xs, T, H, kBM) || tmap_bf16(&m.xt, xt, T, H, kBM) || tmap_bf16(&m.ws256, Ws, V, H, kBN_CE) ||
       tmap_bf16(&m.wt256, Wt, V, H, kBN_CE) || tmap_bf16(&m.wsj, Ws, V, H, kBN_JSD) ||
       tmap_bf16(&m.wtj, Wt, V, H, kBN_JSD) || tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) ||
-      tmap_bf16_ld(&m.wst, bw.wt, H, V, bw.ld_wt, kBN_CE) || tmap_bf16_ld(&m.dzt, bw.dzt, V, T, bw.ld_dzt, kBM) ||
-      tmap_bf16_ld(&m.xst, bw.xt, H, T, bw.ld_xt, kBN_CE))
+      tmap_bf16_mn(&m.ws_mn, Ws, V, H, H) || tmap_bf16_mn(&m.dz_mn, bw.dz, T, V, bw.ld_dz) ||
+      tmap_bf16_mn(&m.xs_mn, xs, T, H, H))
     return LMHO_ERR_CUDA;
   const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
-  return cuda_status(launch_fljsd_fwd_bwd(m, xs, Ws, g1, g2, beta, 1.f / temperature, keep, grad_scale, loss, dxs, dWs,
-                                          w, bw, bw.lse, inv_count, L));
+  return cuda_status(launch_fljsd_fwd_bwd(m, g1, g2, beta, 1.f / temperature, keep, grad_scale, loss, dxs, dWs, w, bw,
+                                          bw.lse, inv_count, L));
 }
 
 int lmho_ws_status(void* ws, size_t ws_bytes, void* stream) {

@@ -44,15 +44,28 @@ namespace lmho {
 namespace {
 
 // CE / LSE / JSD: loss epilogues.  DZ: gradient of the CE with respect to the
-// logits, written as bf16 dZ [T, ld_dz] and its transpose dZ^T [V, ld_dzt]
-// (inputs of the two backward GEMMs).  STORE: plain fp32 tile store (the
-// backward GEMMs dx = dZ W and dW = dZ^T x; rows = T, columns = V in Params).
-// JSDK: the divergence pass that also sums KL(P || M) per row (backward only).
-// DZJ: both heads recomputed, the student's gradient dZs written like DZ.
-enum Mode { kModeCE = 0, kModeLSE = 1, kModeJSD = 2, kModeDZ = 3, kModeStore = 4, kModeJSDK = 5, kModeDZJ = 6 };
+// logits, written as bf16 dZ [T, ld_dz] (the operand of both backward GEMMs).
+// STORE / STORET: plain fp32 tile store, rows = T and columns = V in Params, of
+// the backward GEMMs  dx = dZ W  (STORE: A = dZ K-major, B = W read MN-major)
+// and  dW = dZ^T x  (STORET: A = dZ and B = x, both read MN-major), optionally
+// split along K into fp32 slices.  JSDK: the divergence pass that also sums
+// KL(P || M) per row (backward only).  DZJ: both heads recomputed, the
+// student's gradient dZs written like DZ.
+enum Mode {
+  kModeCE = 0, kModeLSE = 1, kModeJSD = 2, kModeDZ = 3, kModeStore = 4, kModeJSDK = 5, kModeDZJ = 6, kModeStoreT = 7
+};
 
 template <int MODE>
 constexpr bool two_head() { return MODE == kModeJSD || MODE == kModeJSDK || MODE == kModeDZJ; }
+template <int MODE>
+constexpr bool store_mode() { return MODE == kModeStore || MODE == kModeStoreT; }
+// Operands stored MN-major in global memory ([K, M] / [K, N], M or N contiguous).
+template <int MODE>
+constexpr bool a_mn() { return MODE == kModeStoreT; }
+template <int MODE>
+constexpr bool b_mn() { return store_mode<MODE>(); }
+constexpr int kMnBox = 64;                      // MN extent of one 128-byte swizzle row of bf16
+constexpr int kMnBoxBytes = kMnBox * kBK * 2;   // one TMA box of an MN-major operand: 64 (MN) x 64 (K)
 
 constexpr int kTmemCols = 512;   // all of TMEM: accumulators of 256 or 512 fp32 columns
 constexpr int kSmemBudget = 192 * 1024;
@@ -76,11 +89,12 @@ struct ModeCfg {
   static_assert(kNumAcc >= 1 && kNumAcc * kAccCols == kTmemCols, "accumulators tile TMEM");
   static_assert(BN % (32 * kColSplit) == 0, "epilogue column split");
   // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
-  // (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
-  // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                                     (static_cast<uint32_t>(BN >> 3) << 17) |
+  // (bits 7-9 = 1, bits 10-12 = 1), operand majorness in bits 15 (A) and 16 (B),
+  // 0 = K-major, 1 = MN-major; N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (a_mn<MODE>() ? 1u << 15 : 0u) |
+                                     (b_mn<MODE>() ? 1u << 16 : 0u) | (static_cast<uint32_t>(BN >> 3) << 17) |
                                      (static_cast<uint32_t>(kBM >> 4) << 24);
+  static_assert(kBM % kMnBox == 0 && BN % kMnBox == 0, "MN-major tiles are whole 64-wide boxes");
 };
 
 struct Params {
@@ -96,10 +110,12 @@ struct Params {
   float inv_tau;     // LSE / JSD: logits are multiplied by 1 / temperature
   float gscale;      // DZ: gradient weight of every row (grad_scale / T)
   uint16_t* dz;      // DZ: bf16 [T, ld_dz]
-  uint16_t* dzt;     // DZ: bf16 [V, ld_dzt]
-  int64_t ld_dz, ld_dzt;
-  float* out;        // STORE: fp32 [T, ld_out]
+  int64_t ld_dz;
+  float* out;        // STORE: fp32 [T, ld_out], or [k_split][T, ld_out] slices
   int64_t ld_out;
+  int64_t split_stride;    // STORE: elements between K slices
+  int32_t k_split;         // STORE: K slices (units = tiles x k_split)
+  int32_t kb_per;          // STORE: k-blocks per slice (the last may be shorter, never empty)
   const float* kl;         // DZJ: KL(P || M) of every row
   const uint8_t* keep;     // DZJ: token mask (null = all kept)
   const float* inv_count;  // DZJ: 1 / number of kept tokens (device scalar)
@@ -123,15 +139,31 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// MN-major counterpart of smem_desc_sw128: TMA boxes of 64 (MN) x 64 (K)
+// bf16, each K index one 128-byte swizzled row of 64 MN-contiguous elements,
+// 8-row swizzle atoms of 1024 bytes.  Canonical MN-major 128-byte-swizzle
+// layout: the stride between 8-row groups along K (SBO) is 1024 bytes, the
+// stride between 64-element groups along MN (LBO) is one box, 8192 bytes.
+// Moving 16 along K advances the start address by 16 rows = 2048 bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(kMnBoxBytes >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 struct UnitCoord {
-  int head;  // LSE: which head; others 0
+  int head;  // LSE: which head; STORE: which K slice; others 0
   int mt, nt;
 };
 
 __device__ __forceinline__ UnitCoord decode_unit(const Params& p, int64_t u, int mode) {
   UnitCoord c{0, 0, 0};
   const int64_t per_head = static_cast<int64_t>(p.num_m) * p.num_n;
-  if (mode == kModeLSE) {
+  if (mode == kModeLSE || mode == kModeStore || mode == kModeStoreT) {
     c.head = static_cast<int>(u / per_head);
     u -= static_cast<int64_t>(c.head) * per_head;
   }
@@ -238,17 +270,33 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       bool ok = true;
       for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         const UnitCoord c = decode_unit(p, u, MODE);
+        const int kb_lo = store_mode<MODE>() ? c.head * p.kb_per : 0;
+        const int kb_hi = store_mode<MODE>() ? min(p.k_blocks, kb_lo + p.kb_per) : p.k_blocks;
         for (int h = 0; h < C::kHeadsPerUnit && ok; ++h) {
           const int head = (MODE == kModeLSE) ? c.head : h;
           const CUtensorMap* ta = head ? &tm_a1 : &tm_a0;
           const CUtensorMap* tb = head ? &tm_b1 : &tm_b0;
-          for (int kb = 0; kb < p.k_blocks; ++kb) {
+          for (int kb = kb_lo; kb < kb_hi; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, p.status)) { ok = false; break; }
             uint8_t* sa = tiles + stage * C::kStageBytes;
             uint8_t* sb = sa + C::kABytes;
             mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-            tma_load_2d(sa, ta, kb * kBK, c.mt * kBM, &full[stage]);
-            tma_load_2d(sb, tb, kb * kBK, c.nt * BN, &full[stage]);
+            // K-major operand: one box of 64 (K) x rows.  MN-major operand: boxes of
+            // 64 (MN) x 64 (K), one per 64 rows of the tile, kMnBoxBytes apart.
+            if (a_mn<MODE>()) {
+#pragma unroll
+              for (int j = 0; j < kBM / kMnBox; ++j)
+                tma_load_2d(sa + j * kMnBoxBytes, ta, c.mt * kBM + j * kMnBox, kb * kBK, &full[stage]);
+            } else {
+              tma_load_2d(sa, ta, kb * kBK, c.mt * kBM, &full[stage]);
+            }
+            if (b_mn<MODE>()) {
+#pragma unroll
+              for (int j = 0; j < BN / kMnBox; ++j)
+                tma_load_2d(sb + j * kMnBoxBytes, tb, c.nt * BN + j * kMnBox, kb * kBK, &full[stage]);
+            } else {
+              tma_load_2d(sb, tb, kb * kBK, c.nt * BN, &full[stage]);
+            }
             filled |= 1u << stage;
             last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -269,19 +317,24 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       bool ok = true;
       const uint32_t a0 = smem_u32(tiles);
       for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        const int kb_lo = store_mode<MODE>() ? decode_unit(p, u, MODE).head * p.kb_per : 0;
+        const int kb_hi = store_mode<MODE>() ? min(p.k_blocks, kb_lo + p.kb_per) : p.k_blocks;
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, p.status)) break;
         tc_fence_after();
         for (int h = 0; h < C::kHeadsPerUnit && ok; ++h) {
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols + h * BN);
-          for (int kb = 0; kb < p.k_blocks; ++kb) {
+          for (int kb = kb_lo; kb < kb_hi; ++kb) {
             if (!mbar_wait(&full[stage], phase, p.timeout_ns, p.status)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = a0 + stage * C::kStageBytes;
-            const uint64_t da = smem_desc_sw128(sa);
-            const uint64_t db = smem_desc_sw128(sa + C::kABytes);
+            // K step of 16: +32 bytes inside the swizzle row (K-major), +16 rows (MN-major)
+            const uint64_t da = a_mn<MODE>() ? smem_desc_sw128_mn(sa) : smem_desc_sw128(sa);
+            const uint64_t db = b_mn<MODE>() ? smem_desc_sw128_mn(sa + C::kABytes) : smem_desc_sw128(sa + C::kABytes);
+            constexpr uint64_t kStepA = a_mn<MODE>() ? (16 * 128) >> 4 : 32 >> 4;
+            constexpr uint64_t kStepB = b_mn<MODE>() ? (16 * 128) >> 4 : 32 >> 4;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-              tc_mma_bf16(d_tmem, da + 2 * k, db + 2 * k, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
+              tc_mma_bf16(d_tmem, da + kStepA * k, db + kStepB * k, C::kIdesc, (kb != kb_lo || k != 0) ? 1u : 0u);
             tc_commit(&empty[stage]);
             if (++stage == S) { stage = 0; phase ^= 1u; }
           }
@@ -365,10 +418,6 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
             for (int k = 0; k < 4; ++k)
               dst[k] = make_uint4(pack_bf16x2(vs[8 * k], vs[8 * k + 1]), pack_bf16x2(vs[8 * k + 2], vs[8 * k + 3]),
                                   pack_bf16x2(vs[8 * k + 4], vs[8 * k + 5]), pack_bf16x2(vs[8 * k + 6], vs[8 * k + 7]));
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.V)
-                p.dzt[(col0 + j) * p.ld_dzt + row] = static_cast<uint16_t>(pack_bf16x2(vs[j], 0.f));
           }
         } else if (MODE == kModeJSD) {
           float vs[32], vt[32];
@@ -401,17 +450,12 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
             for (int k = 0; k < 4; ++k)
               dst[k] = make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
                                   pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
-            // dZ^T: for each column the 32 lanes (consecutive tokens) write 64 contiguous bytes
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.V)
-                p.dzt[(col0 + j) * p.ld_dzt + row] = static_cast<uint16_t>(pack_bf16x2(v[j], 0.f));
           }
-        } else if (MODE == kModeStore) {
+        } else if (store_mode<MODE>()) {
           float v[32];
           tmem_ld32_sync(tbase + cc * 32, v);
           if (row_ok) {
-            float* dst = p.out + row * p.ld_out + col0;
+            float* dst = p.out + c.head * p.split_stride + row * p.ld_out + col0;
             if (col0 + 32 <= p.V) {
               float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
@@ -567,45 +611,25 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
   mean_tail(row_out, T, loss, ctrl, gridDim.x, keep, inv_count_out);
 }
 
-// out[c, r] = in[r, c] for a bf16 matrix in [rows, cols] (row-major) into
-// out [cols, ld_out]; 64 x 64 tiles through shared memory.  Global reads and
-// writes move 16 bytes (8 elements) per thread where the tile is whole and
-// both sides are 16-byte aligned, element by element otherwise.  Tile rows are
-// padded to 72 elements (144 bytes): 16-byte shared stores stay aligned and the
-// column reads of 8 consecutive rows fall on distinct banks.
+// out[i] = sum over s = 0 .. splits-1, in that order, of part[s * n + i]: the
+// K slices of a split gradient GEMM folded into the caller's buffer.  n % 4 == 0
+// and both buffers 16-byte aligned (checked by the caller).
 __global__ void __launch_bounds__(256)
-    transpose_bf16(const uint16_t* __restrict__ in, int64_t rows, int64_t cols, uint16_t* __restrict__ out,
-                   int64_t ld_out) {
-  __shared__ __align__(16) uint16_t tile[64][72];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
-  const bool whole = r0 + 64 <= rows && c0 + 64 <= cols && cols % 8 == 0 && ld_out % 8 == 0 &&
-                     (reinterpret_cast<uintptr_t>(in) & 15u) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
-  if (whole) {
-    for (int k = threadIdx.x; k < 512; k += 256) {  // 64 rows x 8 vectors
-      const int i = k >> 3, v = k & 7;
-      *reinterpret_cast<uint4*>(&tile[i][v * 8]) =
-          *reinterpret_cast<const uint4*>(in + (r0 + i) * cols + c0 + v * 8);
+    split_sum(const float* __restrict__ part, int splits, int64_t n, float* __restrict__ out) {
+  const int64_t n4 = n >> 2;
+  const float4* p4 = reinterpret_cast<const float4*>(part);
+  float4* o4 = reinterpret_cast<float4*>(out);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = __ldcs(p4 + i);
+    for (int k = 1; k < splits; ++k) {
+      const float4 b = __ldcs(p4 + k * n4 + i);
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
     }
-    __syncthreads();
-    for (int k = threadIdx.x; k < 512; k += 256) {  // 64 output rows (input columns) x 8 vectors
-      const int c = k >> 3, v = k & 7;
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        w[e] = static_cast<uint32_t>(tile[v * 8 + 2 * e][c]) | (static_cast<uint32_t>(tile[v * 8 + 2 * e + 1][c]) << 16);
-      *reinterpret_cast<uint4*>(out + (c0 + c) * ld_out + r0 + v * 8) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    return;
-  }
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4 threads
-  for (int i = ty; i < 64; i += 4) {
-    const int64_t r = r0 + i, c = c0 + tx;
-    if (r < rows && c < cols) tile[i][tx] = in[r * cols + c];
-  }
-  __syncthreads();
-  for (int i = ty; i < 64; i += 4) {
-    const int64_t c = c0 + i, r = r0 + tx;
-    if (c < cols && r < rows) out[c * ld_out + r] = tile[tx][i];
+    o4[i] = a;
   }
 }
 
@@ -711,22 +735,69 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t rows, int64_t cols, uint16_t* out, int64_t ld_out,
-                                  cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
-  transpose_bf16<<<grid, 256, 0, st>>>(in, rows, cols, out, ld_out);
-  return cudaGetLastError();
+int choose_k_split(int64_t tiles, int k_blocks, int num_sms) {
+  if (tiles >= kSplitTiles || num_sms <= 0) return 1;
+  auto fill = [&](int s) {  // share of the SM slots the last wave leaves busy
+    const int64_t units = tiles * s;
+    const int64_t waves = (units + num_sms - 1) / num_sms;
+    return static_cast<double>(units) / static_cast<double>(waves * num_sms);
+  };
+  int best = 1;
+  double best_fill = fill(1);
+  for (int s = 2; s <= kMaxKSplit && k_blocks / s >= kMinSplitKBlocks; ++s) {
+    const double f = fill(s);
+    if (f > best_fill + 0.02) {  // each slice costs a partial write and read
+      best = s;
+      best_fill = f;
+    }
+  }
+  return best;
 }
 
-cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const uint16_t* x, const uint16_t* W, const int64_t* target,
-                                const FusedGeometry& g, float grad_scale, float* loss, float* dx, float* dW,
-                                const FusedWs& ws, const FlceBwdWs& bw, const FusedLaunch& L) {
+size_t k_split_reserve_bytes(int64_t M, int64_t N) {
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN_CE - 1) / kBN_CE);
+  return tiles < kSplitTiles ? static_cast<size_t>(kMaxKSplit) * 4 * static_cast<size_t>(M) * N : 0;
+}
+
+namespace {
+// out [M, N] fp32 (row stride N) = A B with K = `K`, operands read through the
+// tensor maps the MODE expects.  With fewer output tiles than kSplitTiles the
+// K range is cut into slices written to `split_ws` and summed in slice order.
+template <int MODE>
+cudaError_t launch_store_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int64_t N, int64_t K, float* out,
+                              float* split_ws, int group_m, Ctrl* ctrl, const FusedLaunch& L) {
+  FusedGeometry g{};
+  g.T = M;
+  g.V = N;
+  g.H = K;
+  g.num_m = (M + kBM - 1) / kBM;
+  g.num_n = (N + kBN_CE - 1) / kBN_CE;
+  g.group_m = static_cast<int>(g.num_m < group_m ? g.num_m : group_m);
+  Params p = base_params(g, L, ctrl);
+  const int64_t tiles = g.num_m * g.num_n;
+  int splits = split_ws ? choose_k_split(tiles, p.k_blocks, L.num_sms) : 1;
+  p.kb_per = (p.k_blocks + splits - 1) / splits;
+  splits = (p.k_blocks + p.kb_per - 1) / p.kb_per;  // no empty slice
+  p.k_split = splits;
+  p.units = tiles * splits;
+  p.out = splits > 1 ? split_ws : out;
+  p.ld_out = N;
+  p.split_stride = M * N;
+  cudaError_t e = launch_gemm<MODE>(a, b, a, b, p, L);
+  if (e != cudaSuccess || splits == 1) return e;
+  const int64_t n4 = M * N / 4;
+  const int64_t cap = static_cast<int64_t>(L.num_sms) * 8;
+  const int64_t blocks = (n4 + 255) / 256 < cap ? (n4 + 255) / 256 : cap;
+  split_sum<<<static_cast<unsigned>(blocks), 256, 0, L.stream>>>(split_ws, splits, M * N, out);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const int64_t* target, const FusedGeometry& g, float grad_scale,
+                                float* loss, float* dx, float* dW, const FusedWs& ws, const FlceBwdWs& bw,
+                                const FusedLaunch& L) {
   cudaError_t e;
   launch_mark(0, L.stream);
-  // transposed copies so both backward GEMMs read K-major operands
-  if ((e = launch_transpose_bf16(W, g.V, g.H, bw.wt, bw.ld_wt, L.stream)) != cudaSuccess) return e;
-  if ((e = launch_transpose_bf16(x, g.T, g.H, bw.xt, bw.ld_xt, L.stream)) != cudaSuccess) return e;
-  launch_mark(1, L.stream);
   // forward: per-token loss, mean, and each row's log-sum-exp
   Params p = base_params(g, L, ws.ctrl);
   p.units = g.num_m * g.num_n;
@@ -740,60 +811,37 @@ cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const uint16_t* x, const u
                                                                 static_cast<int>(g.num_n), ws.row_out, loss, ws.ctrl,
                                                                 bw.lse);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  launch_mark(2, L.stream);
-  // recompute the logit tiles, write dZ and dZ^T
+  launch_mark(1, L.stream);
+  // recompute the logit tiles, write dZ
   Params q = base_params(g, L, ws.ctrl);
   q.units = g.num_m * g.num_n;
   q.target = target;
   q.lse = bw.lse;
   q.gscale = grad_scale / static_cast<float>(g.T);
   q.dz = bw.dz;
-  q.dzt = bw.dzt;
   q.ld_dz = bw.ld_dz;
-  q.ld_dzt = bw.ld_dzt;
   if ((e = launch_gemm<kModeDZ>(m.x, m.w, m.x, m.w, q, L)) != cudaSuccess) return e;
+  launch_mark(2, L.stream);
+  // dx [T, H] = dZ [T, V] W [V, H]  (K = V; W read MN-major)
+  if ((e = launch_store_gemm<kModeStore>(m.dz, m.w_mn, g.T, g.H, g.V, dx, bw.split, g.group_m, ws.ctrl, L)) !=
+      cudaSuccess)
+    return e;
   launch_mark(3, L.stream);
-  // dx [T, H] = dZ [T, V] * W [V, H]   (B operand W^T [H, V], K = V)
-  FusedGeometry gx = g;
-  gx.T = g.T;
-  gx.V = g.H;
-  gx.H = g.V;
-  gx.num_m = (g.T + kBM - 1) / kBM;
-  gx.num_n = (g.H + kBN_CE - 1) / kBN_CE;
-  Params a = base_params(gx, L, ws.ctrl);
-  a.units = gx.num_m * gx.num_n;
-  a.out = dx;
-  a.ld_out = g.H;
-  if ((e = launch_gemm<kModeStore>(m.dz, m.wt, m.dz, m.wt, a, L)) != cudaSuccess) return e;
+  // dW [V, H] = dZ^T [V, T] x [T, H]  (K = T; dZ and x read MN-major)
+  if ((e = launch_store_gemm<kModeStoreT>(m.dz_mn, m.x_mn, g.V, g.H, g.T, dW, bw.split, g.group_m, ws.ctrl, L)) !=
+      cudaSuccess)
+    return e;
   launch_mark(4, L.stream);
-  // dW [V, H] = dZ^T [V, T] * x [T, H]   (B operand x^T [H, T], K = T)
-  FusedGeometry gw = g;
-  gw.T = g.V;
-  gw.V = g.H;
-  gw.H = g.T;
-  gw.num_m = (g.V + kBM - 1) / kBM;
-  gw.num_n = (g.H + kBN_CE - 1) / kBN_CE;
-  gw.group_m = g.group_m;
-  Params b = base_params(gw, L, ws.ctrl);
-  b.units = gw.num_m * gw.num_n;
-  b.out = dW;
-  b.ld_out = g.H;
-  if ((e = launch_gemm<kModeStore>(m.dzt, m.xt, m.dzt, m.xt, b, L)) != cudaSuccess) return e;
-  launch_mark(5, L.stream);
   return cudaSuccess;
 }
 
-cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const uint16_t* xs, const uint16_t* Ws,
-                                 const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta, float inv_tau,
-                                 const uint8_t* keep, float grad_scale, float* loss, float* dxs, float* dWs,
-                                 const FusedWs& ws, const FlceBwdWs& bw, float* kl, float* inv_count,
-                                 const FusedLaunch& L) {
+cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const FusedGeometry& g_lse, const FusedGeometry& g_jsd,
+                                 float beta, float inv_tau, const uint8_t* keep, float grad_scale, float* loss,
+                                 float* dxs, float* dWs, const FusedWs& ws, const FlceBwdWs& bw, float* kl,
+                                 float* inv_count, const FusedLaunch& L) {
   cudaError_t e;
   const int64_t T = g_lse.T, H = g_lse.H, V = g_lse.V;
   launch_mark(0, L.stream);
-  if ((e = launch_transpose_bf16(Ws, V, H, bw.wt, bw.ld_wt, L.stream)) != cudaSuccess) return e;
-  if ((e = launch_transpose_bf16(xs, T, H, bw.xt, bw.ld_xt, L.stream)) != cudaSuccess) return e;
-  launch_mark(1, L.stream);
   // pass 1: log-sum-exp of both heads
   Params p = base_params(g_lse, L, ws.ctrl);
   p.units = 2 * g_lse.num_m * g_lse.num_n;
@@ -818,8 +866,8 @@ cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const uint16_t* xs, cons
   jsd_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, T, nslots, keep, ws.row_out, loss, ws.ctrl,
                                                               ws.part1, kl, inv_count);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  launch_mark(2, L.stream);
-  // pass 3: both heads again, the student's dZ and dZ^T
+  launch_mark(1, L.stream);
+  // pass 3: both heads again, the student's dZ
   Params r = base_params(g_jsd, L, ws.ctrl);
   r.units = g_jsd.num_m * g_jsd.num_n;
   r.lse = ws.lse;
@@ -830,35 +878,18 @@ cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const uint16_t* xs, cons
   r.keep = keep;
   r.inv_count = inv_count;
   r.dz = bw.dz;
-  r.dzt = bw.dzt;
   r.ld_dz = bw.ld_dz;
-  r.ld_dzt = bw.ld_dzt;
   if ((e = launch_gemm<kModeDZJ>(m.xs, m.wsj, m.xt, m.wtj, r, L)) != cudaSuccess) return e;
+  launch_mark(2, L.stream);
+  // dxs = dZs Ws (K = V), dWs = dZs^T xs (K = T)
+  if ((e = launch_store_gemm<kModeStore>(m.dz, m.ws_mn, T, H, V, dxs, bw.split, g_lse.group_m, ws.ctrl, L)) !=
+      cudaSuccess)
+    return e;
   launch_mark(3, L.stream);
-  // dxs = dZs Ws, dWs = dZs^T xs
-  FusedGeometry gx = g_lse;
-  gx.V = H;
-  gx.H = V;
-  gx.num_m = (T + kBM - 1) / kBM;
-  gx.num_n = (H + kBN_CE - 1) / kBN_CE;
-  Params a = base_params(gx, L, ws.ctrl);
-  a.units = gx.num_m * gx.num_n;
-  a.out = dxs;
-  a.ld_out = H;
-  if ((e = launch_gemm<kModeStore>(m.dz, m.wst, m.dz, m.wst, a, L)) != cudaSuccess) return e;
+  if ((e = launch_store_gemm<kModeStoreT>(m.dz_mn, m.xs_mn, V, H, T, dWs, bw.split, g_lse.group_m, ws.ctrl, L)) !=
+      cudaSuccess)
+    return e;
   launch_mark(4, L.stream);
-  FusedGeometry gw = g_lse;
-  gw.T = V;
-  gw.V = H;
-  gw.H = T;
-  gw.num_m = (V + kBM - 1) / kBM;
-  gw.num_n = (H + kBN_CE - 1) / kBN_CE;
-  Params b = base_params(gw, L, ws.ctrl);
-  b.units = gw.num_m * gw.num_n;
-  b.out = dWs;
-  b.ld_out = H;
-  if ((e = launch_gemm<kModeStore>(m.dzt, m.xst, m.dzt, m.xst, b, L)) != cudaSuccess) return e;
-  launch_mark(5, L.stream);
   return cudaSuccess;
 }
 

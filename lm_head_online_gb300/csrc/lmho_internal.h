@@ -97,39 +97,50 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256,
 void launch_mark(int i, cudaStream_t st);
 
 // Fused linear + CE forward and backward.  Workspace beyond the forward's:
-// each row's log-sum-exp, dZ (bf16 [T, ld_dz], ld_dz a multiple of 256),
-// dZ^T (bf16 [V, ld_dzt]), W^T (bf16 [H, ld_wt]), x^T (bf16 [H, ld_xt]).
+// each row's log-sum-exp, dZ (bf16 [T, ld_dz], ld_dz a multiple of 256) and,
+// when a gradient product has too few output tiles to fill the machine, fp32
+// K slices of it (kMaxKSplit x its size) for a split-K product.
 struct FlceBwdWs {
   float* lse;
   uint16_t* dz;
-  uint16_t* dzt;
-  uint16_t* wt;
-  uint16_t* xt;
-  int64_t ld_dz, ld_dzt, ld_wt, ld_xt;
+  float* split;   // null when neither product can split
+  int64_t ld_dz;
 };
+// Split-K of the gradient products dx = dZ W and dW = dZ^T x: only below
+// kSplitTiles output tiles of 128 x 256, into at most kMaxKSplit slices of at
+// least kMinSplitKBlocks k-blocks each.
+constexpr int64_t kSplitTiles = 4 * 152;
+constexpr int kMaxKSplit = 8;
+constexpr int kMinSplitKBlocks = 16;
+// Bytes of fp32 slices a product with an [M, N] output may need (0 = never splits).
+size_t k_split_reserve_bytes(int64_t M, int64_t N);
+// K slices for `tiles` output tiles and `k_blocks` k-blocks on `num_sms` SMs.
+int choose_k_split(int64_t tiles, int k_blocks, int num_sms);
+
+// Tensor maps of the backward.  K-major maps have boxes of 64 (K) x rows;
+// MN-major maps (_mn) cover a [K, MN] matrix with boxes of 64 (MN) x 64 (K).
 struct FlceBwdMaps {
   CUtensorMap x, w;      // forward and dZ passes: A = x [T, H], B = W [V, H]
-  CUtensorMap dz, wt;    // dx = dZ W:   A = dZ [T, V], B = W^T [H, V]
-  CUtensorMap dzt, xt;   // dW = dZ^T x: A = dZ^T [V, T], B = x^T [H, T]
+  CUtensorMap dz, w_mn;  // dx = dZ W:   A = dZ [T, V] (K = V), B = W [V, H] MN-major
+  CUtensorMap dz_mn, x_mn;  // dW = dZ^T x: A = dZ [T, V] MN-major (K = T), B = x [T, H] MN-major
 };
 size_t flce_bwd_ws_bytes(int64_t T, int64_t H, int64_t V);
 FlceBwdWs flce_bwd_ws_carve(void* ws, int64_t T, int64_t H, int64_t V);
-cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const uint16_t* x, const uint16_t* W, const int64_t* target,
-                                const FusedGeometry& g, float grad_scale, float* loss, float* dx, float* dW,
-                                const FusedWs& ws, const FlceBwdWs& bw, const FusedLaunch& L);
+cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const int64_t* target, const FusedGeometry& g, float grad_scale,
+                                float* loss, float* dx, float* dW, const FusedWs& ws, const FlceBwdWs& bw,
+                                const FusedLaunch& L);
 
 // Fused linear + JSD forward and student backward.
 struct FljsdBwdMaps {
   CUtensorMap xs, xt, ws256, wt256, wsj, wtj;  // the forward passes, and the dZ pass
-  CUtensorMap dz, wst;                          // dxs = dZs Ws:   A = dZs [T, V], B = Ws^T [H, V]
-  CUtensorMap dzt, xst;                         // dWs = dZs^T xs: A = dZs^T [V, T], B = xs^T [H, T]
+  CUtensorMap dz, ws_mn;                        // dxs = dZs Ws
+  CUtensorMap dz_mn, xs_mn;                     // dWs = dZs^T xs
 };
 size_t fljsd_bwd_ws_bytes(int64_t T, int64_t H, int64_t V);
-cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const uint16_t* xs, const uint16_t* Ws,
-                                 const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta, float inv_tau,
-                                 const uint8_t* keep, float grad_scale, float* loss, float* dxs, float* dWs,
-                                 const FusedWs& ws, const FlceBwdWs& bw, float* kl, float* inv_count,
-                                 const FusedLaunch& L);
+cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const FusedGeometry& g_lse, const FusedGeometry& g_jsd,
+                                 float beta, float inv_tau, const uint8_t* keep, float grad_scale, float* loss,
+                                 float* dxs, float* dWs, const FusedWs& ws, const FlceBwdWs& bw, float* kl,
+                                 float* inv_count, const FusedLaunch& L);
 
 cudaError_t launch_wait_selftest(Ctrl* ctrl, uint64_t timeout_ns, cudaStream_t st);
 
