@@ -74,6 +74,14 @@ def _load():
             lib.oracle_fljsd_grad_f64.restype = None
             lib.oracle_fljsd_grad_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, dbl, vp, vp]
             lib.oracle_fljsd_grad_bf16.restype = None
+            lib.oracle_cpo_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, dbl, vp, vp]
+            lib.oracle_cpo_f64.restype = dbl
+            lib.oracle_cpo_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, dbl, vp, vp, ci]
+            lib.oracle_cpo_bf16.restype = dbl
+            lib.oracle_cpo_grad_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, dbl, dbl, vp, vp]
+            lib.oracle_cpo_grad_f64.restype = None
+            lib.oracle_cpo_grad_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, dbl, dbl, vp, vp]
+            lib.oracle_cpo_grad_bf16.restype = None
             lib.oracle_logits_bf16.argtypes = [vp, vp, i64, i64, i64, vp]
             lib.oracle_logits_bf16.restype = None
             _lib = lib
@@ -298,3 +306,55 @@ def logits_bf16(x_bits, W_bits):
     z = np.empty((T, V), np.float64)
     _load().oracle_logits_bf16(px, pw, T, H, V, z.ctypes.data)
     return z
+
+
+def _cpo_args(x, W, target, dtype):
+    x, px = _c(x, dtype)
+    W, pw = _c(W, dtype)
+    B, S, H = x.shape
+    V = W.shape[0]
+    assert W.shape[1] == H and B % 2 == 0 and B >= 2
+    t, pt = _c(target, np.int64)
+    assert t.shape == (B, S)
+    return px, pw, pt, B, S, H, V
+
+
+def cpo_f64(x, W, target, beta=0.1, alpha=1.0):
+    """CPO on the fused linear + CE, fp64 inputs x [B, S, H] (chosen = first
+    B/2 sequences), W [V, H], target [B, S].  Returns (loss, per-token CE
+    losses [B, S], sequence log-likelihoods [B])."""
+    px, pw, pt, B, S, H, V = _cpo_args(x, W, target, np.float64)
+    rows = np.empty((B, S), np.float64)
+    lp = np.empty(B, np.float64)
+    m = _load().oracle_cpo_f64(px, pw, pt, B, S, H, V, float(beta), float(alpha), rows.ctypes.data, lp.ctypes.data)
+    return m, rows, lp
+
+
+def cpo_bf16(x_bits, W_bits, target, beta=0.1, alpha=1.0, threads=None):
+    """cpo_f64 from bf16 bits (uint16)."""
+    px, pw, pt, B, S, H, V = _cpo_args(x_bits, W_bits, target, np.uint16)
+    rows = np.empty((B, S), np.float64)
+    lp = np.empty(B, np.float64)
+    m = _load().oracle_cpo_bf16(px, pw, pt, B, S, H, V, float(beta), float(alpha), rows.ctypes.data, lp.ctypes.data,
+                                _threads(threads))
+    return m, rows, lp
+
+
+def cpo_grad_f64(x, W, target, beta=0.1, alpha=1.0, scale=1.0):
+    """(dx [B, S, H], dW [V, H]) of scale * CPO loss, fp64 inputs."""
+    px, pw, pt, B, S, H, V = _cpo_args(x, W, target, np.float64)
+    dx = np.empty((B, S, H), np.float64)
+    dW = np.empty((V, H), np.float64)
+    _load().oracle_cpo_grad_f64(px, pw, pt, B, S, H, V, float(beta), float(alpha), float(scale), dx.ctypes.data,
+                                dW.ctypes.data)
+    return dx, dW
+
+
+def cpo_grad_bf16(x_bits, W_bits, target, beta=0.1, alpha=1.0, scale=1.0):
+    """cpo_grad_f64 from bf16 bits (uint16)."""
+    px, pw, pt, B, S, H, V = _cpo_args(x_bits, W_bits, target, np.uint16)
+    dx = np.empty((B, S, H), np.float64)
+    dW = np.empty((V, H), np.float64)
+    _load().oracle_cpo_grad_bf16(px, pw, pt, B, S, H, V, float(beta), float(alpha), float(scale), dx.ctypes.data,
+                                 dW.ctypes.data)
+    return dx, dW

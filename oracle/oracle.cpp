@@ -15,8 +15,10 @@
 //     loss [seq, batch]; TP = 1 only                    -> ce_sbv_bf16.
 //   * "Fused linear + CPO loss", summary ("computed chunked without
 //     materializing logits") and Semantics: x [batch, seq, hidden], weight
-//     [vocab, hidden], target int64 [batch, seq], loss float [1].  Only the
-//     cross-entropy (NLL) core of that loss is defined here -> flce_bf16.
+//     [vocab, hidden], target int64 [batch, seq], loss float [1].  Its
+//     cross-entropy (NLL) core -> flce_bf16; the whole CPO objective -> cpo_*
+//     (the page names CPO without printing it: the definition below is the
+//     published one, Xu et al. 2024, "Contrastive Preference Optimization").
 //   * "Fused linear + JSD", summary ("generalized JSD (beta 0.5, batchmean)")
 //     and Semantics: student/teacher input [tokens, hidden], student/teacher
 //     weight [vocab, hidden], loss float [1]             -> fljsd_bf16.
@@ -40,6 +42,18 @@
 // Flat mean: g_i = scale / T.  Megatron per token: g_i = scale * dloss_i
 // (dloss may be null = 1).  A target outside [0, V) makes the row NaN.
 //
+// CPO: the batch holds 2 Bc sequences of S tokens; sequence b < Bc is the
+// chosen answer of pair b and sequence b + Bc its rejected answer.  With the
+// per-token CE losses l_{b,s} of the fused linear + CE:
+//   lp_b   = -sum_s l_{b,s}                  (sequence log-likelihood)
+//   d_k    = lp_k - lp_{k+Bc}
+//   pref   = (1/Bc) sum_k -ln sigmoid(beta d_k) = (1/Bc) sum_k softplus(-beta d_k)
+//   nll    = (1/(Bc S)) sum_{b < Bc, s} l_{b,s}  (token mean over the chosen half)
+//   loss   = alpha nll + pref.
+// Its gradient with respect to the per-token losses: alpha/(Bc S) +
+// (beta/Bc) sigmoid(-beta d_k) for a chosen token of pair k, and
+// -(beta/Bc) sigmoid(-beta d_k) for a rejected one; then the CE backward.
+
 // Variant (JSD with temperature and a token mask): the logits of both heads
 // are divided by the temperature tau before the softmax; tokens whose keep
 // flag is 0 are left out, and the batchmean divides by the number of kept
@@ -432,6 +446,95 @@ void oracle_fljsd_grad_bf16(const uint16_t* xs16, const uint16_t* Ws16, const ui
     Wt[i] = bf16_to_double(Wt16[i]);
   }
   oracle_fljsd_grad_f64(xs.data(), Ws.data(), xt.data(), Wt.data(), T, H, V, beta, tau, keep, scale, dxs, dWs);
+}
+
+// softplus(u) = ln(1 + e^u), and the logistic sigmoid, both without overflow.
+static double softplus(double u) { return (u > 0.0 ? u : 0.0) + std::log1p(std::exp(-std::fabs(u))); }
+static double sigmoid(double u) {
+  if (u >= 0.0) return 1.0 / (1.0 + std::exp(-u));
+  const double e = std::exp(u);
+  return e / (1.0 + e);
+}
+
+// The CPO combination of per-token losses rows [2 Bc * S] (see the header):
+// writes lp [2 Bc] (may be null) and sig [Bc] = sigmoid(-beta d_k) (may be
+// null), returns the loss.  Sums run in index order.
+static double cpo_combine(const double* rows, int64_t B, int64_t S, double beta, double alpha, double* lp, double* sig) {
+  const int64_t Bc = B / 2;
+  std::vector<double> seq(B);
+  for (int64_t b = 0; b < B; ++b) {
+    double acc = 0.0;
+    for (int64_t s = 0; s < S; ++s) acc += rows[b * S + s];
+    seq[b] = -acc;
+    if (lp) lp[b] = seq[b];
+  }
+  double pref = 0.0, nll = 0.0;
+  for (int64_t k = 0; k < Bc; ++k) {
+    const double d = seq[k] - seq[k + Bc];
+    pref += softplus(-beta * d);
+    if (sig) sig[k] = sigmoid(-beta * d);
+    nll -= seq[k];
+  }
+  return alpha * nll / (static_cast<double>(Bc) * S) + pref / static_cast<double>(Bc);
+}
+
+// CPO on the fused linear + CE, fp64 inputs x [B*S, H], W [V, H]: per-token
+// CE losses into loss_rows [B*S], sequence log-likelihoods into lp [B] (may
+// be null); returns the loss.
+double oracle_cpo_f64(const double* x, const double* W, const int64_t* target, int64_t B, int64_t S, int64_t H,
+                      int64_t V, double beta, double alpha, double* loss_rows, double* lp) {
+  oracle_flce_f64(x, W, target, B * S, H, V, loss_rows);
+  return cpo_combine(loss_rows, B, S, beta, alpha, lp, nullptr);
+}
+
+// Same from bf16 inputs; the per-token losses come from oracle_flce_bf16
+// (threads only partition tokens).
+double oracle_cpo_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t B, int64_t S,
+                       int64_t H, int64_t V, double beta, double alpha, double* loss_rows, double* lp,
+                       int threads) {
+  oracle_flce_bf16(x, W, target, B * S, H, V, loss_rows, threads);
+  return cpo_combine(loss_rows, B, S, beta, alpha, lp, nullptr);
+}
+
+// Gradient of scale * (CPO loss) on fp64 inputs:
+//   dz_i = scale w_i (softmax(z_i) - onehot(t_i)),  w_i as in the header,
+//   dx = dZ W [B*S, H],  dW = dZ^T x [V, H]  (sums in index order).
+void oracle_cpo_grad_f64(const double* x, const double* W, const int64_t* target, int64_t B, int64_t S, int64_t H,
+                         int64_t V, double beta, double alpha, double scale, double* dx, double* dW) {
+  const int64_t T = B * S, Bc = B / 2;
+  std::vector<double> rows(T), sig(Bc), z(V), dz(static_cast<size_t>(T) * V);
+  oracle_flce_f64(x, W, target, T, H, V, rows.data());
+  cpo_combine(rows.data(), B, S, beta, alpha, nullptr, sig.data());
+  for (int64_t i = 0; i < T; ++i) {
+    const int64_t b = i / S, k = b % Bc;
+    const double w = b < Bc ? alpha / (static_cast<double>(Bc) * S) + beta / Bc * sig[k] : -beta / Bc * sig[k];
+    for (int64_t v = 0; v < V; ++v) {
+      double acc = 0.0;
+      for (int64_t kk = 0; kk < H; ++kk) acc += x[i * H + kk] * W[v * H + kk];
+      z[v] = acc;
+    }
+    ce_grad_row(z.data(), V, target[i], scale * w, dz.data() + i * V);
+  }
+  for (int64_t i = 0; i < T; ++i)
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t v = 0; v < V; ++v) acc += dz[i * V + v] * W[v * H + k];
+      dx[i * H + k] = acc;
+    }
+  for (int64_t v = 0; v < V; ++v)
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < T; ++i) acc += dz[i * V + v] * x[i * H + k];
+      dW[v * H + k] = acc;
+    }
+}
+
+void oracle_cpo_grad_bf16(const uint16_t* x16, const uint16_t* W16, const int64_t* target, int64_t B, int64_t S,
+                          int64_t H, int64_t V, double beta, double alpha, double scale, double* dx, double* dW) {
+  std::vector<double> x(static_cast<size_t>(B * S) * H), W(static_cast<size_t>(V) * H);
+  for (size_t i = 0; i < x.size(); ++i) x[i] = bf16_to_double(x16[i]);
+  for (size_t i = 0; i < W.size(); ++i) W[i] = bf16_to_double(W16[i]);
+  oracle_cpo_grad_f64(x.data(), W.data(), target, B, S, H, V, beta, alpha, scale, dx, dW);
 }
 
 // Logits of the fused paths for a set of tokens (used by tests to pin the
