@@ -78,6 +78,8 @@ def _load():
             lib.oracle_cpo_f64.restype = dbl
             lib.oracle_cpo_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, dbl, vp, vp, ci]
             lib.oracle_cpo_bf16.restype = dbl
+            lib.oracle_cpo_combine.argtypes = [vp, i64, i64, dbl, dbl, vp, vp]
+            lib.oracle_cpo_combine.restype = dbl
             lib.oracle_cpo_grad_f64.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, dbl, dbl, vp, vp]
             lib.oracle_cpo_grad_f64.restype = None
             lib.oracle_cpo_grad_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, dbl, dbl, vp, vp]
@@ -358,3 +360,14 @@ def cpo_grad_bf16(x_bits, W_bits, target, beta=0.1, alpha=1.0, scale=1.0):
     _load().oracle_cpo_grad_bf16(px, pw, pt, B, S, H, V, float(beta), float(alpha), float(scale), dx.ctypes.data,
                                  dW.ctypes.data)
     return dx, dW
+
+
+def cpo_combine(rows, beta=0.1, alpha=1.0):
+    """The CPO combination of given per-token CE losses rows [B, S]: returns
+    (loss, lp [B], d loss / d l [B, S])."""
+    r, pr = _c(rows, np.float64)
+    B, S = r.shape
+    lp = np.empty(B, np.float64)
+    w = np.empty((B, S), np.float64)
+    m = _load().oracle_cpo_combine(pr, B, S, float(beta), float(alpha), lp.ctypes.data, w.ctypes.data)
+    return m, lp, w

@@ -478,6 +478,23 @@ static double cpo_combine(const double* rows, int64_t B, int64_t S, double beta,
   return alpha * nll / (static_cast<double>(Bc) * S) + pref / static_cast<double>(Bc);
 }
 
+// d loss / d l_i of a token of sequence b (see the header): sig = sigmoid(-beta d_k) of its pair.
+static double cpo_row_weight(int64_t b, int64_t S, int64_t Bc, double beta, double alpha, const double* sig) {
+  return b < Bc ? alpha / (static_cast<double>(Bc) * S) + beta / Bc * sig[b] : -beta / Bc * sig[b - Bc];
+}
+
+// The CPO combination alone, from given per-token losses rows [B*S]: writes
+// lp [B] and the per-token weights d loss / d l_i into row_w [B*S] (may be
+// null); returns the loss.  Lets tests check large cases from sampled rows.
+double oracle_cpo_combine(const double* rows, int64_t B, int64_t S, double beta, double alpha, double* lp,
+                          double* row_w) {
+  std::vector<double> sig(B / 2);
+  const double m = cpo_combine(rows, B, S, beta, alpha, lp, sig.data());
+  if (row_w)
+    for (int64_t i = 0; i < B * S; ++i) row_w[i] = cpo_row_weight(i / S, S, B / 2, beta, alpha, sig.data());
+  return m;
+}
+
 // CPO on the fused linear + CE, fp64 inputs x [B*S, H], W [V, H]: per-token
 // CE losses into loss_rows [B*S], sequence log-likelihoods into lp [B] (may
 // be null); returns the loss.
@@ -506,8 +523,7 @@ void oracle_cpo_grad_f64(const double* x, const double* W, const int64_t* target
   oracle_flce_f64(x, W, target, T, H, V, rows.data());
   cpo_combine(rows.data(), B, S, beta, alpha, nullptr, sig.data());
   for (int64_t i = 0; i < T; ++i) {
-    const int64_t b = i / S, k = b % Bc;
-    const double w = b < Bc ? alpha / (static_cast<double>(Bc) * S) + beta / Bc * sig[k] : -beta / Bc * sig[k];
+    const double w = cpo_row_weight(i / S, S, Bc, beta, alpha, sig.data());
     for (int64_t v = 0; v < V; ++v) {
       double acc = 0.0;
       for (int64_t kk = 0; kk < H; ++kk) acc += x[i * H + kk] * W[v * H + kk];

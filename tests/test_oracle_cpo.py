@@ -161,3 +161,26 @@ def test_bf16_front_end_and_bad_target():
     t[1, 2] = -1
     m, rows, lp = oracle.cpo_bf16(x, W, t)
     assert math.isnan(m) and np.isnan(rows[1, 2]) and np.isnan(lp[1]) and np.isfinite(lp[0])
+
+
+def test_combine_weights_are_the_derivative_of_the_combination():
+    # d loss / d l_i by central differences of the combination itself, and the
+    # combination of the oracle's own rows reproduces the full oracle
+    B, S = 6, 4
+    rng = np.random.default_rng(9)
+    rows = rng.uniform(0.5, 6.0, size=(B, S))
+    m, lp, w = oracle.cpo_combine(rows, beta=0.4, alpha=1.3)
+    np.testing.assert_allclose(lp, -rows.sum(axis=1), rtol=1e-15)
+    # loss ~ 4: fp64 round-off over 2h = 2e-5 is ~1e-10 and the h^2 term smaller
+    h = 1e-5
+    for i in range(B):
+        for s in range(S):
+            rp, rm = rows.copy(), rows.copy()
+            rp[i, s] += h
+            rm[i, s] -= h
+            fd = (oracle.cpo_combine(rp, 0.4, 1.3)[0] - oracle.cpo_combine(rm, 0.4, 1.3)[0]) / (2 * h)
+            assert w[i, s] == pytest.approx(fd, rel=1e-6, abs=1e-9)
+    x, W, t = rand_case(8, B, S, 6, 10)
+    mo, ro, lpo = oracle.cpo_f64(x, W, t, beta=0.4, alpha=1.3)
+    mc, lpc, _ = oracle.cpo_combine(ro, 0.4, 1.3)
+    assert mc == mo and np.array_equal(lpc, lpo)
