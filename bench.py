@@ -87,7 +87,8 @@ def parse():
                     help="also sample clocks during the e2e region (nvidia-smi polling slows host copies)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every configuration of the workload table (one JSON line each)")
-    ap.add_argument("--case", choices=["ce", "sbv", "flce", "fljsd", "ce_fb", "sbv_fb", "flce_fb", "fljsd_fb"],
+    ap.add_argument("--case", choices=["ce", "sbv", "flce", "fljsd", "ce_fb", "sbv_fb", "flce_fb", "fljsd_fb", "cpo",
+                                       "cpo_fb"],
                     help="time one op alone at --T/--V/--H (profiling runs); prints one JSON line")
     ap.add_argument("--T", type=int, default=None, help="tokens (ce: rows; sbv: seq, batch 4)")
     ap.add_argument("--V", type=int, default=None)
@@ -555,6 +556,24 @@ def run_case(args):
         ws = lmho.workspace(lmho.flce_workspace_bytes(T, H, V))
         fn = lambda: lmho.flce_fwd_bf16(x, W, t, ws=ws)  # noqa: E731
         work, unit = rl.flce_flops(T, H, V), "TFLOP/s"
+    elif c in ("cpo", "cpo_fb"):
+        # the CPO page's workload: seq 1024 x batch, chosen = first half of the batch
+        T, V = args.T or FLCE["T"], args.V or FLCE["V"]
+        Bq = max(2, T // 1024 // 2 * 2)
+        S = T // Bq
+        T = Bq * S
+        x, W, t = bf16(args.seed, 0, (Bq, S, H), 1.0), bf16(args.seed, 2, (V, H), 0.02), targets((Bq, S), V)
+        if c == "cpo":
+            ws = lmho.workspace(lmho.flce_cpo_workspace_bytes(Bq, S, H, V))
+            fn = lambda: lmho.flce_cpo_fwd_bf16(x, W, t, 0.1, 1.0, ws=ws)  # noqa: E731
+            work = rl.flce_flops(T, H, V)
+        else:
+            ws = lmho.workspace(lmho.flce_cpo_bwd_workspace_bytes(Bq, S, H, V))
+            dx = torch.empty((Bq, S, H), dtype=torch.float32, device="cuda")
+            dW = torch.empty((V, H), dtype=torch.float32, device="cuda")
+            fn = lambda: lmho.flce_cpo_fwd_bwd_bf16(x, W, t, 0.1, 1.0, ws=ws, dx=dx, dW=dW)  # noqa: E731
+            work = rl.flce_fwd_bwd_flops(T, H, V)
+        unit = "TFLOP/s"
     elif c == "flce_fb":
         T, V = args.T or FLCE["T"], args.V or FLCE["V"]
         x, W, t = bf16(args.seed, 0, (T, H), 1.0), bf16(args.seed, 2, (V, H), 0.02), targets((T,), V)
@@ -587,7 +606,8 @@ def run_case(args):
     # 129 MB L2, and a write-based flush would leave ~129 MB of dirty lines
     # whose write-back the timed kernel would pay for.
     flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
-    nk = {"ce": 1, "sbv": 1, "flce": 2, "fljsd": 4, "ce_fb": 1, "sbv_fb": 1, "flce_fb": 4, "fljsd_fb": 4}[c]
+    nk = {"ce": 1, "sbv": 1, "flce": 2, "fljsd": 4, "ce_fb": 1, "sbv_fb": 1, "flce_fb": 4, "fljsd_fb": 4, "cpo": 2,
+          "cpo_fb": 4}[c]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     for row in evs:
         for e in row:
@@ -618,6 +638,8 @@ SWEEP = ([("ce", 16384, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
          [("sbv", 2048, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
          [("flce", 1024 * b, 128256) for b in (2, 4, 8, 16)] +
          [("flce_fb", 1024 * b, 128256) for b in (2, 16)] +
+         [("cpo", 1024 * b, 128256) for b in (2, 4, 8, 16)] +
+         [("cpo_fb", 1024 * b, 128256) for b in (2, 16)] +
          [("fljsd_fb", T, 128256) for T in (1024, 8192)] +
          [("fljsd", T, 128256) for T in (1024, 2048, 4096, 8192)])
 

@@ -191,6 +191,48 @@ int flce_fwd_bwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* targe
                       void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Fused linear + CPO loss: the whole objective of page "Fused linear + CPO
+ * loss" (summary: CPO preference loss over batch x seq x hidden activations
+ * projected through a vocab x hidden LM head against integer targets, logits
+ * never materialised; Semantics: x [batch, seq, hidden], weight [vocab, hidden],
+ * target int64 [batch, seq], loss float [1]).  The page does not print the
+ * objective; this is the published CPO (Xu et al. 2024):
+ *   sequence b < B/2 is the chosen answer of pair b, b + B/2 its rejected one;
+ *   lp_b = sum_s ln softmax(x_{b,s} W^T)[t_{b,s}]   (all S tokens)
+ *   loss = alpha * (token mean of the CE over the chosen half)
+ *          + (2/B) sum_k -ln sigmoid(beta (lp_k - lp_{k+B/2})).
+ *   x       [B, S, H] bf16 device (B even, >= 2), W [V, H] bf16 device
+ *           (16-byte aligned, H % 8 == 0); target [B, S] int64 device
+ *   beta    > 0 (0.1 in the paper), alpha >= 0 (1 in the paper), finite
+ *   loss    [1] fp32 device output; logps [B] fp32 device output of lp, or NULL
+ *   ws      ws_bytes >= flce_cpo_workspace_bytes(B, S, H, V), zeroed before
+ *           first use; the first B*S floats hold the per-token CE losses.
+ * A target outside [0, V) makes its token's loss, its sequence's lp and the
+ * loss NaN.  One tensor-core pass (the fused CE) and two small finalisers.
+ * ------------------------------------------------------------------------ */
+size_t flce_cpo_workspace_bytes(int64_t B, int64_t S, int64_t H, int64_t V);
+int flce_cpo_fwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t B,
+                      int64_t S, int64_t H, int64_t V, float beta, float alpha, float* loss,
+                      float* logps, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * flce_cpo_fwd_bf16 and the gradients of grad_scale * loss:
+ *   dZ_i = grad_scale w_i (softmax(z_i) - onehot(t_i)),  w_i = d loss / d l_i
+ *        = alpha/(Bc S) + (beta/Bc) sigmoid(-beta d_k)  (chosen token, pair k)
+ *        = -(beta/Bc) sigmoid(-beta d_k)                (rejected token)
+ *   with Bc = B/2, d_k = lp_k - lp_{k+Bc};  dx = dZ W [B*S, H] fp32,
+ *   dW = dZ^T x [V, H] fp32 (as flce_fwd_bwd_bf16, dZ rounded to bf16).
+ * dx, dW 16-byte aligned; ws_bytes >= flce_cpo_bwd_workspace_bytes(B, S, H, V),
+ * zeroed before first use.  A bad target makes its pair's dx rows and all of
+ * dW NaN.
+ * ------------------------------------------------------------------------ */
+size_t flce_cpo_bwd_workspace_bytes(int64_t B, int64_t S, int64_t H, int64_t V);
+int flce_cpo_fwd_bwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t B,
+                          int64_t S, int64_t H, int64_t V, float beta, float alpha, float grad_scale,
+                          float* loss, float* logps, float* dx, float* dW, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused linear + generalized Jensen-Shannon divergence, batchmean.
  * Page "Fused linear + JSD", summary (separate vocab x hidden heads for student
  * and teacher, generalized JSD with beta 0.5, batchmean) and section

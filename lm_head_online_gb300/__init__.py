@@ -36,6 +36,7 @@ EXPORTS = (
     "ce_fwd_bwd_f32", "ce_fwd_bwd_sbv_bf16",
     "flce_workspace_bytes", "flce_fwd_bf16", "flce_bwd_workspace_bytes", "flce_fwd_bwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "fljsd_bwd_workspace_bytes", "fljsd_fwd_bwd_bf16",
+    "flce_cpo_workspace_bytes", "flce_cpo_fwd_bf16", "flce_cpo_bwd_workspace_bytes", "flce_cpo_fwd_bwd_bf16",
     "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
 
@@ -95,6 +96,15 @@ def load():
         lib.fljsd_bwd_workspace_bytes.restype = sz
         lib.fljsd_fwd_bwd_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, f32, vp, f32, vp, vp, vp, vp, sz, vp]
         lib.fljsd_fwd_bwd_bf16.restype = ci
+        lib.flce_cpo_workspace_bytes.argtypes = [i64, i64, i64, i64]
+        lib.flce_cpo_workspace_bytes.restype = sz
+        lib.flce_cpo_fwd_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, f32, f32, vp, vp, vp, sz, vp]
+        lib.flce_cpo_fwd_bf16.restype = ci
+        lib.flce_cpo_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
+        lib.flce_cpo_bwd_workspace_bytes.restype = sz
+        lib.flce_cpo_fwd_bwd_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, f32, f32, f32, vp, vp, vp, vp, vp, sz,
+                                              vp]
+        lib.flce_cpo_fwd_bwd_bf16.restype = ci
         lib.lmho_ws_status.argtypes = [vp, sz, vp]
         lib.lmho_ws_status.restype = ci
         lib.lmho_set_ce_variant.argtypes = [ci]
@@ -319,6 +329,75 @@ def flce_fwd_bwd_bf16(x, W, target, grad_scale=1.0, loss=None, dx=None, dW=None,
                                  _dev(dx, "dx", torch.float32, 2), _dev(dW, "dW", torch.float32, 2),
                                  _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "flce_fwd_bwd_bf16")
     return loss, dx, dW
+
+
+def flce_cpo_workspace_bytes(B: int, S: int, H: int, V: int) -> int:
+    return int(load().flce_cpo_workspace_bytes(B, S, H, V))
+
+
+def flce_cpo_bwd_workspace_bytes(B: int, S: int, H: int, V: int) -> int:
+    return int(load().flce_cpo_bwd_workspace_bytes(B, S, H, V))
+
+
+def _cpo_shapes(x, W, target):
+    if x.dim() != 3 or target.dim() != 2:
+        raise ValueError("x must be [B, S, H] and target [B, S] (chosen = first B/2 sequences)")
+    B, S, H = x.shape
+    V = W.shape[0]
+    if W.dim() != 2 or W.shape[1] != H or tuple(target.shape) != (B, S):
+        raise ValueError("shape mismatch: x [B,S,H], W [V,H], target [B,S]")
+    return B, S, H, V
+
+
+def flce_cpo_fwd_bf16(x, W, target, beta=0.1, alpha=1.0, loss=None, logps=None, ws=None, stream=None):
+    """CPO loss of the fused linear + CE (chosen = first half of the batch):
+    returns (loss fp32 [1], sequence log-likelihoods fp32 [B])."""
+    lib = load()
+    B, S, H, V = _cpo_shapes(x, W, target)
+    px = _dev(x, "x", torch.bfloat16, 3)
+    pw = _dev(W, "W", torch.bfloat16, 2)
+    pt = _dev(target, "target", torch.int64, 2)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=x.device)
+    if logps is None:
+        logps = torch.empty(B, dtype=torch.float32, device=x.device)
+    if logps.numel() != B or loss.numel() < 1:
+        raise ValueError("logps must hold B floats, loss at least one")
+    if ws is None:
+        ws = workspace(lib.flce_cpo_workspace_bytes(B, S, H, V), x.device)
+    _check(lib.flce_cpo_fwd_bf16(px, pw, pt, B, S, H, V, float(beta), float(alpha), _dev(loss, "loss", torch.float32),
+                                 _dev(logps, "logps", torch.float32, 1), _dev(ws, "ws", torch.uint8), ws.numel(),
+                                 _stream(stream)), "flce_cpo_fwd_bf16")
+    return loss, logps
+
+
+def flce_cpo_fwd_bwd_bf16(x, W, target, beta=0.1, alpha=1.0, grad_scale=1.0, loss=None, logps=None, dx=None, dW=None,
+                          ws=None, stream=None):
+    """CPO loss and the gradients of grad_scale * loss: returns (loss [1],
+    logps [B], dx fp32 [B, S, H], dW fp32 [V, H])."""
+    lib = load()
+    B, S, H, V = _cpo_shapes(x, W, target)
+    px = _dev(x, "x", torch.bfloat16, 3)
+    pw = _dev(W, "W", torch.bfloat16, 2)
+    pt = _dev(target, "target", torch.int64, 2)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=x.device)
+    if logps is None:
+        logps = torch.empty(B, dtype=torch.float32, device=x.device)
+    if dx is None:
+        dx = torch.empty((B, S, H), dtype=torch.float32, device=x.device)
+    if dW is None:
+        dW = torch.empty((V, H), dtype=torch.float32, device=x.device)
+    if logps.numel() != B or loss.numel() < 1 or tuple(dx.shape) != (B, S, H) or tuple(dW.shape) != (V, H):
+        raise ValueError("output shapes: loss [1], logps [B], dx [B, S, H], dW [V, H]")
+    if ws is None:
+        ws = workspace(lib.flce_cpo_bwd_workspace_bytes(B, S, H, V), x.device)
+    _check(lib.flce_cpo_fwd_bwd_bf16(px, pw, pt, B, S, H, V, float(beta), float(alpha), float(grad_scale),
+                                     _dev(loss, "loss", torch.float32), _dev(logps, "logps", torch.float32, 1),
+                                     _dev(dx, "dx", torch.float32, 3), _dev(dW, "dW", torch.float32, 2),
+                                     _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)),
+           "flce_cpo_fwd_bwd_bf16")
+    return loss, logps, dx, dW
 
 
 def fljsd_fwd_bf16(xs, Ws, xt, Wt, beta=0.5, loss=None, ws=None, stream=None):

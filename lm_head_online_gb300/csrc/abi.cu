@@ -290,6 +290,29 @@ FlceBwdWs flce_bwd_ws_carve(void* ws, int64_t T, int64_t H, int64_t V) {
   return bwd_carve(ws, bwd_layout(T, H, V, flce_ws_bytes(T, H, V)));
 }
 
+// CPO: the fused CE's workspace, then lp [B], sig [B/2] and one slot for the
+// token mean; the backward adds the flce backward buffers and row weights [T].
+namespace {
+struct CpoLayout {
+  size_t off_lp, off_sig, off_mean, end;  // end includes a control-block slot
+};
+CpoLayout cpo_layout(int64_t B, int64_t S, int64_t H, int64_t V) {
+  CpoLayout c{};
+  size_t o = flce_ws_bytes(B * S, H, V);
+  c.off_lp = o;
+  o += align_up(4 * static_cast<size_t>(B));
+  c.off_sig = o;
+  o += align_up(4 * static_cast<size_t>(B));
+  c.off_mean = o;
+  o += kAlign;
+  c.end = o + kAlign;
+  return c;
+}
+size_t cpo_bwd_ws_bytes(int64_t B, int64_t S, int64_t H, int64_t V) {
+  return bwd_layout(B * S, H, V, cpo_layout(B, S, H, V).end).end + align_up(4 * static_cast<size_t>(B * S));
+}
+}  // namespace
+
 // JSD backward: the JSD forward's workspace, then the same backward buffers
 // (the per-row slot holds KL(P || M)), then one float for 1 / kept count.
 size_t fljsd_bwd_ws_bytes(int64_t T, int64_t H, int64_t V) {
@@ -580,6 +603,88 @@ int fljsd_fwd_bwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* x
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_fljsd_fwd_bwd(m, g1, g2, beta, 1.f / temperature, keep, grad_scale, loss, dxs, dWs, w, bw,
                                           bw.lse, inv_count, L));
+}
+
+size_t flce_cpo_workspace_bytes(int64_t B, int64_t S, int64_t H, int64_t V) {
+  if (B <= 0 || S <= 0 || H <= 0 || V <= 0) return kAlign;
+  return cpo_layout(B, S, H, V).end;
+}
+
+size_t flce_cpo_bwd_workspace_bytes(int64_t B, int64_t S, int64_t H, int64_t V) {
+  if (B <= 0 || S <= 0 || H <= 0 || V <= 0) return kAlign;
+  return cpo_bwd_ws_bytes(B, S, H, V);
+}
+
+namespace {
+int check_cpo(int64_t B, int64_t S, int64_t H, int64_t V, float beta, float alpha) {
+  if (B < 2 || B % 2 != 0 || S <= 0) return LMHO_ERR_INVALID_ARG;
+  if (B > (int64_t(1) << 31) / S) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_fused_common(B * S, H, V)) return c;
+  if (!(beta > 0.f) || !std::isfinite(beta) || !(alpha >= 0.f) || !std::isfinite(alpha)) return LMHO_ERR_INVALID_ARG;
+  return LMHO_OK;
+}
+}  // namespace
+
+int flce_cpo_fwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t B, int64_t S, int64_t H,
+                      int64_t V, float beta, float alpha, float* loss, float* logps, void* ws, size_t ws_bytes,
+                      void* stream) {
+  if (!x || !W || !target || !loss || !ws) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_cpo(B, S, H, V, beta, alpha)) return c;
+  const int64_t T = B * S;
+  if (!aligned16(x) || !aligned16(W)) return LMHO_ERR_INVALID_ARG;
+  const CpoLayout lay = cpo_layout(B, S, H, V);
+  if (ws_bytes < lay.end || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const Range in[3] = {rng(x, 2 * static_cast<size_t>(T) * H), rng(W, 2 * static_cast<size_t>(V) * H),
+                       rng(target, 8 * static_cast<size_t>(T))};
+  const Range out[3] = {rng(loss, 4), rng(logps, logps ? 4 * static_cast<size_t>(B) : 0), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 3, out, 3)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  CUtensorMap tx, tw;
+  if (tmap_bf16(&tx, x, T, H, kBM) || tmap_bf16(&tw, W, V, H, kBN_CE)) return LMHO_ERR_CUDA;
+  const FusedGeometry g = geometry(T, H, V, kBN_CE);
+  const FusedWs w = flce_ws_carve(ws, ws_bytes, T, V);
+  char* base = static_cast<char*>(ws);
+  CpoArgs c{B, S, beta, alpha, reinterpret_cast<float*>(base + lay.off_lp), reinterpret_cast<float*>(base + lay.off_sig),
+            reinterpret_cast<float*>(base + lay.off_mean), logps, nullptr};
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_flce_cpo(tx, tw, target, g, loss, w, c, L));
+}
+
+int flce_cpo_fwd_bwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, int64_t B, int64_t S,
+                          int64_t H, int64_t V, float beta, float alpha, float grad_scale, float* loss, float* logps,
+                          float* dx, float* dW, void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !W || !target || !loss || !dx || !dW || !ws) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_cpo(B, S, H, V, beta, alpha)) return c;
+  if (!std::isfinite(grad_scale)) return LMHO_ERR_INVALID_ARG;
+  const int64_t T = B * S;
+  if (!aligned16(x) || !aligned16(W) || !aligned16(dx) || !aligned16(dW)) return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < cpo_bwd_ws_bytes(B, S, H, V) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const Range in[3] = {rng(x, 2 * static_cast<size_t>(T) * H), rng(W, 2 * static_cast<size_t>(V) * H),
+                       rng(target, 8 * static_cast<size_t>(T))};
+  const Range out[5] = {rng(loss, 4), rng(logps, logps ? 4 * static_cast<size_t>(B) : 0),
+                        rng(dx, 4 * static_cast<size_t>(T) * H), rng(dW, 4 * static_cast<size_t>(V) * H),
+                        rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 3, out, 5)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  const CpoLayout cl = cpo_layout(B, S, H, V);
+  const BwdLayout lay = bwd_layout(T, H, V, cl.end);
+  const FusedWs w = flce_ws_carve(ws, ws_bytes, T, V);
+  const FlceBwdWs bw = bwd_carve(ws, lay);
+  char* base = static_cast<char*>(ws);
+  CpoArgs c{B, S, beta, alpha, reinterpret_cast<float*>(base + cl.off_lp), reinterpret_cast<float*>(base + cl.off_sig),
+            reinterpret_cast<float*>(base + cl.off_mean), logps, reinterpret_cast<float*>(base + lay.end - kAlign)};
+  FlceBwdMaps m;
+  if (tmap_bf16(&m.x, x, T, H, kBM) || tmap_bf16(&m.w, W, V, H, kBN_CE) ||
+      tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) || tmap_bf16_mn(&m.w_mn, W, V, H, H) ||
+      tmap_bf16_mn(&m.dz_mn, bw.dz, T, V, bw.ld_dz) || tmap_bf16_mn(&m.x_mn, x, T, H, H))
+    return LMHO_ERR_CUDA;
+  const FusedGeometry g = geometry(T, H, V, kBN_CE);
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_flce_fwd_bwd(m, target, g, grad_scale, loss, dx, dW, w, bw, L, &c));
 }
 
 int lmho_ws_status(void* ws, size_t ws_bytes, void* stream) {

@@ -109,6 +109,7 @@ struct Params {
   float beta;
   float inv_tau;     // LSE / JSD: logits are multiplied by 1 / temperature
   float gscale;      // DZ: gradient weight of every row (grad_scale / T)
+  const float* row_w;  // DZ: per-row factor multiplying gscale (null = 1)
   uint16_t* dz;      // DZ: bf16 [T, ld_dz]
   int64_t ld_dz;
   float* out;        // STORE: fp32 [T, ld_out], or [k_split][T, ld_out] slices
@@ -365,7 +366,11 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       int64_t tgt = -1;
       float ls = 0.f, lt = 0.f;
       if ((MODE == kModeCE || MODE == kModeDZ) && row_ok) tgt = __ldg(p.target + row);
-      if (MODE == kModeDZ && row_ok) ls = __ldg(p.lse + row);
+      float gdz = 0.f;
+      if (MODE == kModeDZ && row_ok) {
+        ls = __ldg(p.lse + row);
+        gdz = p.row_w ? p.gscale * __ldg(p.row_w + row) : p.gscale;
+      }
       if (two_head<MODE>() && row_ok) {
         ls = __ldg(p.lse + row);
         lt = __ldg(p.lse + p.T + row);
@@ -436,7 +441,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
           tmem_ld32_sync(tbase + cc * 32, v);
           if (row_ok) {
             const bool bad = tgt < 0 || tgt >= p.V;
-            const float g = p.gscale, nl = -ls * kLog2e;
+            const float g = gdz, nl = -ls * kLog2e;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int64_t col = col0 + j;
@@ -611,6 +616,67 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
   mean_tail(row_out, T, loss, ctrl, gridDim.x, keep, inv_count_out);
 }
 
+// CPO from the per-token CE losses rows [B * S] (published objective, Xu et
+// al. 2024; page "Fused linear + CPO loss" names it): sequence b < B/2 is the
+// chosen answer of pair b, sequence b + B/2 its rejected answer.  One block of
+// 256 threads per sequence: thread j sums tokens j, j + 256, ... (compensated),
+// then a fixed butterfly and the 8 warp sums in order give lp_b = -sum.  The
+// last block to finish (atomic ticket) combines the pairs in order:
+//   d_k = lp_k - lp_{k+Bc},  loss = alpha (sum_{b<Bc} -lp_b) / (Bc S)
+//                                  + (1/Bc) sum_k softplus(-beta d_k),
+// keeping sig_k = sigmoid(-beta d_k); with row_w set it then writes
+// d loss / d l_i: alpha/(Bc S) + (beta/Bc) sig_k for a chosen token of pair k,
+// -(beta/Bc) sig_k for a rejected one; and leaves the ticket at 0.
+__global__ void __launch_bounds__(256)
+    cpo_finalize(const float* rows, int64_t B, int64_t S, float beta, float alpha, float* lp, float* sig, float* loss,
+                 float* logps, float* row_w, Ctrl* ctrl) {
+  __shared__ float s_warp[8];
+  __shared__ uint32_t s_last;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int64_t b = blockIdx.x;
+  KSum a;
+  for (int64_t s = threadIdx.x; s < S; s += 256) a.add(__ldcg(rows + b * S + s));
+  float v = a.s - a.c;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  if (l == 0) s_warp[w] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int k = 0; k < 8; ++k) t += s_warp[k];
+    lp[b] = -t;
+    if (logps) logps[b] = -t;
+    __threadfence();
+    s_last = atomicAdd(&ctrl->ticket, 1u) == gridDim.x - 1 ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int64_t Bc = B / 2;
+  if (threadIdx.x == 0) {
+    KSum pref, nll;
+    for (int64_t k = 0; k < Bc; ++k) {
+      const float lc = __ldcg(lp + k);
+      const float u = -beta * (lc - __ldcg(lp + k + Bc));
+      const float e = expf(-fabsf(u));
+      pref.add(fmaxf(u, 0.f) + log1pf(e));
+      sig[k] = u >= 0.f ? 1.f / (1.f + e) : e / (1.f + e);
+      nll.add(-lc);
+    }
+    *loss = alpha * (nll.s - nll.c) / (static_cast<float>(Bc) * static_cast<float>(S)) +
+            (pref.s - pref.c) / static_cast<float>(Bc);
+    ctrl->ticket = 0u;
+    __threadfence();
+  }
+  if (!row_w) return;
+  __syncthreads();
+  const float aw = alpha / (static_cast<float>(Bc) * static_cast<float>(S)), bw = beta / static_cast<float>(Bc);
+  for (int64_t i = threadIdx.x; i < B * S; i += blockDim.x) {
+    const int64_t q = i / S;
+    row_w[i] = q < Bc ? fmaf(bw, sig[q], aw) : -bw * sig[q - Bc];
+  }
+}
+
 // out[i] = sum over s = 0 .. splits-1, in that order, of part[s * n + i]: the
 // K slices of a split gradient GEMM folded into the caller's buffer.  n % 4 == 0
 // and both buffers 16-byte aligned (checked by the caller).
@@ -735,6 +801,30 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, 
   return cudaGetLastError();
 }
 
+cudaError_t launch_flce_cpo(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const int64_t* target,
+                            const FusedGeometry& g, float* loss, const FusedWs& ws, const CpoArgs& c,
+                            const FusedLaunch& L) {
+  Params p = base_params(g, L, ws.ctrl);
+  p.units = g.num_m * g.num_n;
+  p.target = target;
+  p.part0 = ws.part0;
+  p.part1 = ws.part1;
+  p.part2 = ws.part2;
+  launch_mark(0, L.stream);
+  cudaError_t e = launch_gemm<kModeCE>(tm_x, tm_w, tm_x, tm_w, p, L);
+  if (e != cudaSuccess) return e;
+  launch_mark(1, L.stream);
+  const unsigned blocks = static_cast<unsigned>((g.T + kFinRows - 1) / kFinRows);
+  flce_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, ws.part1, ws.part2, target, g.T, g.V,
+                                                               static_cast<int>(g.num_n), ws.row_out, c.mean, ws.ctrl,
+                                                               nullptr);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cpo_finalize<<<static_cast<unsigned>(c.B), 256, 0, L.stream>>>(ws.row_out, c.B, c.S, c.beta, c.alpha, c.lp, c.sig,
+                                                                 loss, c.logps, nullptr, ws.ctrl);
+  launch_mark(2, L.stream);
+  return cudaGetLastError();
+}
+
 int choose_k_split(int64_t tiles, int k_blocks, int num_sms) {
   if (tiles >= kSplitTiles || num_sms <= 0) return 1;
   auto fill = [&](int s) {  // share of the SM slots the last wave leaves busy
@@ -795,7 +885,7 @@ cudaError_t launch_store_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_
 
 cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const int64_t* target, const FusedGeometry& g, float grad_scale,
                                 float* loss, float* dx, float* dW, const FusedWs& ws, const FlceBwdWs& bw,
-                                const FusedLaunch& L) {
+                                const FusedLaunch& L, const CpoArgs* cpo) {
   cudaError_t e;
   launch_mark(0, L.stream);
   // forward: per-token loss, mean, and each row's log-sum-exp
@@ -808,16 +898,22 @@ cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const int64_t* target, con
   if ((e = launch_gemm<kModeCE>(m.x, m.w, m.x, m.w, p, L)) != cudaSuccess) return e;
   const unsigned fblocks = static_cast<unsigned>((g.T + kFinRows - 1) / kFinRows);
   flce_finalize<<<fblocks, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, ws.part1, ws.part2, target, g.T, g.V,
-                                                                static_cast<int>(g.num_n), ws.row_out, loss, ws.ctrl,
-                                                                bw.lse);
+                                                                static_cast<int>(g.num_n), ws.row_out,
+                                                                cpo ? cpo->mean : loss, ws.ctrl, bw.lse);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (cpo) {  // CPO: the loss and each token's weight d loss / d l_i
+    cpo_finalize<<<static_cast<unsigned>(cpo->B), 256, 0, L.stream>>>(
+        ws.row_out, cpo->B, cpo->S, cpo->beta, cpo->alpha, cpo->lp, cpo->sig, loss, cpo->logps, cpo->row_w, ws.ctrl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   launch_mark(1, L.stream);
   // recompute the logit tiles, write dZ
   Params q = base_params(g, L, ws.ctrl);
   q.units = g.num_m * g.num_n;
   q.target = target;
   q.lse = bw.lse;
-  q.gscale = grad_scale / static_cast<float>(g.T);
+  q.gscale = cpo ? grad_scale : grad_scale / static_cast<float>(g.T);
+  q.row_w = cpo ? cpo->row_w : nullptr;
   q.dz = bw.dz;
   q.ld_dz = bw.ld_dz;
   if ((e = launch_gemm<kModeDZ>(m.x, m.w, m.x, m.w, q, L)) != cudaSuccess) return e;

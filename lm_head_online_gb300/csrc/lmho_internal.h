@@ -126,9 +126,24 @@ struct FlceBwdMaps {
 };
 size_t flce_bwd_ws_bytes(int64_t T, int64_t H, int64_t V);
 FlceBwdWs flce_bwd_ws_carve(void* ws, int64_t T, int64_t H, int64_t V);
+// CPO on the fused linear + CE: pairs of sequences (chosen b, rejected b + B/2)
+// of S tokens.  Workspace pieces beyond the fused CE's.
+struct CpoArgs {
+  int64_t B, S;
+  float beta, alpha;
+  float* lp;      // [B]   sequence log-likelihoods
+  float* sig;     // [B/2] sigmoid(-beta d_k)
+  float* mean;    // [1]   the token mean the CE finaliser writes (not the CPO loss)
+  float* logps;   // [B]   caller copy of lp, or null
+  float* row_w;   // [T]   backward: d loss / d l_i, or null
+};
+cudaError_t launch_flce_cpo(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const int64_t* target,
+                            const FusedGeometry& g, float* loss, const FusedWs& ws, const CpoArgs& c,
+                            const FusedLaunch& L);
+// With `cpo` set the loss is the CPO objective and dZ carries its per-row weights.
 cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const int64_t* target, const FusedGeometry& g, float grad_scale,
                                 float* loss, float* dx, float* dW, const FusedWs& ws, const FlceBwdWs& bw,
-                                const FusedLaunch& L);
+                                const FusedLaunch& L, const CpoArgs* cpo = nullptr);
 
 // Fused linear + JSD forward and student backward.
 struct FljsdBwdMaps {
