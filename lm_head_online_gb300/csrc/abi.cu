@@ -327,7 +327,9 @@ size_t fljsd_ws_bytes(int64_t T, int64_t H, int64_t V) {
   const int64_t n256 = (V + kBN_CE - 1) / kBN_CE;
   const int64_t njsd = (V + kBN_JSD - 1) / kBN_JSD * kJsdColSplit;
   const int64_t p0 = (2 * n256 > njsd ? 2 * n256 : njsd) * T;
-  return align_up(4 * T) + align_up(4 * p0) + align_up(4 * 2 * n256 * T) + align_up(4 * 2 * T) + kAlign;
+  // part0 and part1 both hold either pass's partials: (max, sum) of the
+  // log-sum-exp pass, or the divergence and KL(P || M) sums of the JSD pass
+  return align_up(4 * T) + 2 * align_up(4 * p0) + align_up(4 * 2 * T) + kAlign;
 }
 FusedWs fljsd_ws_carve(void* ws, size_t ws_bytes, int64_t T, int64_t V) {
   const int64_t n256 = (V + kBN_CE - 1) / kBN_CE;
@@ -340,7 +342,7 @@ FusedWs fljsd_ws_carve(void* ws, size_t ws_bytes, int64_t T, int64_t V) {
   w.part0 = reinterpret_cast<float*>(p);
   p += align_up(4 * p0);
   w.part1 = reinterpret_cast<float*>(p);
-  p += align_up(4 * 2 * n256 * T);
+  p += align_up(4 * p0);
   w.lse = reinterpret_cast<float*>(p);
   w.ctrl = ctrl_of(ws, ws_bytes);
   return w;
