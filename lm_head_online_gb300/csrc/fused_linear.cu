@@ -179,26 +179,30 @@ __device__ __forceinline__ UnitCoord decode_unit(const Params& p, int64_t u, int
   return c;
 }
 
-// Generalized-JSD term of one (token, vocab) pair from log-probabilities.
-// With hi = max(lp, lq), d = |lp - lq|, e = exp(-d) and weights (w_hi, w_lo)
-// the beta weights of the larger and smaller side:
-//   lm = hi + ln(w_hi + w_lo e),  hi - lm = -ln(w_hi + w_lo e),  lo - lm = (hi - lm) - d
-//   term = w_hi e^hi (hi - lm) + w_lo e^hi e (lo - lm).
-__device__ __forceinline__ float jsd_term(float lp, float lq, float beta, float omb) {
-  const float hi = fmaxf(lp, lq);
-  const float d = fabsf(lp - lq);
-  const bool p_is_hi = lp >= lq;
+// Generalized-JSD term of one (token, vocab) pair,
+//   beta P (lp - lm) + (1-beta) Q (lq - lm),  lm = ln(beta P + (1-beta) Q),
+// from base-2 log-probabilities lp2 = lp log2 e, lq2 = lq log2 e, evaluated
+// around the larger side so no large terms cancel: with hi = max(lp2, lq2),
+// d = |lp2 - lq2|, (w_hi, w_lo) the beta weights of the larger and smaller
+// side, e = 2^-d, u = w_lo e and s = w_hi + u (the argument of the log),
+//   hi - lm = -ln2 lg2(s),  lo - lm = -ln2 (lg2(s) + d),
+//   term = -ln2 2^hi (s lg2(s) + u d).
+// Returns 2^hi (s lg2(s) + u d), the term divided by -ln2 (callers scale the
+// sum once): three MUFU operations and no ln2 / log2e multiplies per pair.
+__device__ __forceinline__ float jsd_term2(float lp2, float lq2, float beta, float omb) {
+  const float diff = lp2 - lq2;
+  const float hi = fmaxf(lp2, lq2);
+  const float d = fabsf(diff);
+  const bool p_is_hi = diff >= 0.f;
   const float w_hi = p_is_hi ? beta : omb;
   const float w_lo = p_is_hi ? omb : beta;
-  const float e = ex2_approx(-d * kLog2e);
-  const float a_hi = -kLn2 * lg2_approx(fmaf(w_lo, e, w_hi));
-  const float a_lo = a_hi - d;
-  const float p_hi = ex2_approx(hi * kLog2e);
-  return p_hi * (w_hi * a_hi + w_lo * e * a_lo);
+  const float u = w_lo * ex2_approx(-d);
+  const float sv = u + w_hi;
+  return ex2_approx(hi) * fmaf(sv, lg2_approx(sv), u * d);
 }
 
 // The pieces of one generalized-JSD pair the backward needs: P = e^{lp} and
-// lp - lm (same larger-side evaluation as jsd_term).
+// lp - lm (the larger-side evaluation of jsd_term2, in natural log).
 __device__ __forceinline__ void jsd_student(float lp, float lq, float beta, float omb, float* P, float* lp_lm) {
   const float hi = fmaxf(lp, lq);
   const float d = fabsf(lp - lq);
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
-    const float beta = p.beta, omb = 1.f - p.beta, it = p.inv_tau;
+    const float beta = p.beta, omb = 1.f - p.beta, it = p.inv_tau, it2 = p.inv_tau * kLog2e;
     for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
       const UnitCoord c = decode_unit(p, u, MODE);
       const int64_t row = static_cast<int64_t>(c.mt) * kBM + row_in_tile;
@@ -375,6 +379,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
         ls = __ldg(p.lse + row);
         lt = __ldg(p.lse + p.T + row);
       }
+      const float ls2 = ls * kLog2e, lt2 = lt * kLog2e;  // log-sum-exps in base 2
       float krow = 0.f, gj = 0.f;
       if (MODE == kModeDZJ && row_ok) {
         krow = __ldg(p.kl + row);
@@ -400,10 +405,9 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (col0 + j < p.V) {
-              const float lp = fmaf(vs[j], it, -ls), lq = fmaf(vt[j], it, -lt);
               float P, lplm;
-              jsd_student(lp, lq, beta, omb, &P, &lplm);
-              jsd += jsd_term(lp, lq, beta, omb);
+              jsd_student(fmaf(vs[j], it, -ls), fmaf(vt[j], it, -lt), beta, omb, &P, &lplm);
+              jsd += jsd_term2(fmaf(vs[j], it2, -ls2), fmaf(vt[j], it2, -lt2), beta, omb);
               kacc = fmaf(P, lplm, kacc);
             }
           }
@@ -430,11 +434,12 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
           tmem_ld32_sync(tbase + BN + cc * 32, vt);
           if (col0 + 32 <= p.V) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) jsd += jsd_term(fmaf(vs[j], it, -ls), fmaf(vt[j], it, -lt), beta, omb);
+            for (int j = 0; j < 32; ++j)
+              jsd += jsd_term2(fmaf(vs[j], it2, -ls2), fmaf(vt[j], it2, -lt2), beta, omb);
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.V) jsd += jsd_term(fmaf(vs[j], it, -ls), fmaf(vt[j], it, -lt), beta, omb);
+              if (col0 + j < p.V) jsd += jsd_term2(fmaf(vs[j], it2, -ls2), fmaf(vt[j], it2, -lt2), beta, omb);
           }
         } else if (MODE == kModeDZ) {
           float v[32];
@@ -503,7 +508,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
         // partial slot of this (vocab tile, column slice)
         const int64_t slot = static_cast<int64_t>(c.nt) * C::kColSplit + half;
         if (MODE == kModeJSD || MODE == kModeJSDK) {
-          p.part0[slot * p.T + row] = jsd;
+          p.part0[slot * p.T + row] = -kLn2 * jsd;
           if (MODE == kModeJSDK) p.part1[slot * p.T + row] = kacc;
         } else {
           const int64_t idx = (static_cast<int64_t>(c.head) * p.num_n * C::kColSplit + slot) * p.T + row;
@@ -526,10 +531,10 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
 
 // ---------------------------------------------------------------- finalisers
 constexpr int kFinRows = 32;   // rows per block (one per lane)
-constexpr int kFinSplit = 8;   // warps per block, each merging a slice of the vocab tiles
+constexpr int kFinSplit = 16;  // warps per block, each merging a slice of the vocab tiles
 
 // Merge (m, s) partials [num_n][T] of each row, in vocab-tile order, into
-// its log-sum-exp.  Warp w handles tiles [w*cnt, (w+1)*cnt); the 8 results
+// its log-sum-exp.  Warp w handles tiles [w*cnt, (w+1)*cnt); the kFinSplit results
 // merge in warp order.
 __device__ __forceinline__ float merge_lse_row(const float* pm, const float* ps, int64_t T, int num_n,
                                                int64_t row, MS* s_tmp) {
