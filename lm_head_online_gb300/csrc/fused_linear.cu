@@ -216,6 +216,32 @@ __device__ __forceinline__ void jsd_student(float lp, float lq, float beta, floa
   *lp_lm = p_is_hi ? a_hi : a_hi - d;
 }
 
+// Two-head epilogue walk over NCH 16-column chunks of this warp's slice: calls
+// f(chunk, student[16], teacher[16]) with the fp32 accumulator bits of the
+// warp's 32 rows, the next chunk's two TMEM loads in flight while the current
+// chunk is consumed.  No load is outstanding on return.
+template <int NCH, class F>
+__device__ __forceinline__ void two_head_chunks(uint32_t tbase, uint32_t head_off, F&& f) {
+  static_assert(NCH % 2 == 0, "chunks are consumed in pairs");
+  uint32_t as[16], at[16], bs[16], bt[16];
+  tmem_ld16(tbase, as);
+  tmem_ld16(tbase + head_off, at);
+  tmem_wait_ld(as, at);
+#pragma unroll
+  for (int cc = 0; cc < NCH; cc += 2) {
+    tmem_ld16(tbase + (cc + 1) * 16, bs);
+    tmem_ld16(tbase + head_off + (cc + 1) * 16, bt);
+    f(cc, as, at);
+    tmem_wait_ld(bs, bt);
+    if (cc + 2 < NCH) {
+      tmem_ld16(tbase + (cc + 2) * 16, as);
+      tmem_ld16(tbase + head_off + (cc + 2) * 16, at);
+    }
+    f(cc + 1, bs, bt);
+    if (cc + 2 < NCH) tmem_wait_ld(as, at);
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
     fused_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_b0,
@@ -395,109 +421,113 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       float zt = 0.f;
       bool has_t = false;
       float jsd = 0.f, kacc = 0.f;
-#pragma unroll 1
-      for (int cc = 0; cc < kCols / 32; ++cc) {
-        const int64_t col0 = n0 + cc * 32;
-        if (MODE == kModeJSDK) {
-          float vs[32], vt[32];
-          tmem_ld32_sync(tbase + cc * 32, vs);
-          tmem_ld32_sync(tbase + BN + cc * 32, vt);
+      if constexpr (two_head<MODE>()) {
+        two_head_chunks<kCols / 16>(tbase, BN, [&](int cc, const uint32_t(&rs)[16], const uint32_t(&rt)[16]) {
+          const int64_t col0 = n0 + cc * 16;
+          if constexpr (MODE == kModeJSD) {
+            if (col0 + 16 <= p.V) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (col0 + j < p.V) {
-              float P, lplm;
-              jsd_student(fmaf(vs[j], it, -ls), fmaf(vt[j], it, -lt), beta, omb, &P, &lplm);
-              jsd += jsd_term2(fmaf(vs[j], it2, -ls2), fmaf(vt[j], it2, -lt2), beta, omb);
-              kacc = fmaf(P, lplm, kacc);
-            }
-          }
-        } else if (MODE == kModeDZJ) {
-          float vs[32], vt[32];
-          tmem_ld32_sync(tbase + cc * 32, vs);
-          tmem_ld32_sync(tbase + BN + cc * 32, vt);
-          if (row_ok) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              float P, lplm;
-              jsd_student(fmaf(vs[j], it, -ls), fmaf(vt[j], it, -lt), beta, omb, &P, &lplm);
-              vs[j] = (col0 + j < p.V) ? gj * P * (lplm - krow) : 0.f;
-            }
-            uint4* dst = reinterpret_cast<uint4*>(p.dz + row * p.ld_dz + col0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              dst[k] = make_uint4(pack_bf16x2(vs[8 * k], vs[8 * k + 1]), pack_bf16x2(vs[8 * k + 2], vs[8 * k + 3]),
-                                  pack_bf16x2(vs[8 * k + 4], vs[8 * k + 5]), pack_bf16x2(vs[8 * k + 6], vs[8 * k + 7]));
-          }
-        } else if (MODE == kModeJSD) {
-          float vs[32], vt[32];
-          tmem_ld32_sync(tbase + cc * 32, vs);
-          tmem_ld32_sync(tbase + BN + cc * 32, vt);
-          if (col0 + 32 <= p.V) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              jsd += jsd_term2(fmaf(vs[j], it2, -ls2), fmaf(vt[j], it2, -lt2), beta, omb);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < p.V) jsd += jsd_term2(fmaf(vs[j], it2, -ls2), fmaf(vt[j], it2, -lt2), beta, omb);
-          }
-        } else if (MODE == kModeDZ) {
-          float v[32];
-          tmem_ld32_sync(tbase + cc * 32, v);
-          if (row_ok) {
-            const bool bad = tgt < 0 || tgt >= p.V;
-            const float g = gdz, nl = -ls * kLog2e;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int64_t col = col0 + j;
-              float d = col < p.V ? g * ex2_approx(fmaf(v[j], kLog2e, nl)) : 0.f;
-              if (col == tgt) d -= g;
-              v[j] = bad ? __int_as_float(0x7FC00000) : d;
-            }
-            // dZ row segment: 32 bf16 = 64 contiguous bytes (ld_dz is a multiple of the tile width)
-            uint4* dst = reinterpret_cast<uint4*>(p.dz + row * p.ld_dz + col0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              dst[k] = make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
-                                  pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
-          }
-        } else if (store_mode<MODE>()) {
-          float v[32];
-          tmem_ld32_sync(tbase + cc * 32, v);
-          if (row_ok) {
-            float* dst = p.out + c.head * p.split_stride + row * p.ld_out + col0;
-            if (col0 + 32 <= p.V) {
-              float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) d4[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+              for (int j = 0; j < 16; ++j)
+                jsd += jsd_term2(fmaf(__uint_as_float(rs[j]), it2, -ls2), fmaf(__uint_as_float(rt[j]), it2, -lt2),
+                                 beta, omb);
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (col0 + j < p.V) dst[j] = v[j];
+              for (int j = 0; j < 16; ++j)
+                if (col0 + j < p.V)
+                  jsd += jsd_term2(fmaf(__uint_as_float(rs[j]), it2, -ls2),
+                                   fmaf(__uint_as_float(rt[j]), it2, -lt2), beta, omb);
+            }
+          } else if constexpr (MODE == kModeJSDK) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (col0 + j < p.V) {
+                const float zs = __uint_as_float(rs[j]), zq = __uint_as_float(rt[j]);
+                float P, lplm;
+                jsd_student(fmaf(zs, it, -ls), fmaf(zq, it, -lt), beta, omb, &P, &lplm);
+                jsd += jsd_term2(fmaf(zs, it2, -ls2), fmaf(zq, it2, -lt2), beta, omb);
+                kacc = fmaf(P, lplm, kacc);
+              }
+            }
+          } else {  // kModeDZJ: the student's dZ for this row and 16 columns
+            if (row_ok) {
+              float g[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                float P, lplm;
+                jsd_student(fmaf(__uint_as_float(rs[j]), it, -ls), fmaf(__uint_as_float(rt[j]), it, -lt), beta,
+                            omb, &P, &lplm);
+                g[j] = (col0 + j < p.V) ? gj * P * (lplm - krow) : 0.f;
+              }
+              uint4* dst = reinterpret_cast<uint4*>(p.dz + row * p.ld_dz + col0);
+#pragma unroll
+              for (int k = 0; k < 2; ++k)
+                dst[k] = make_uint4(pack_bf16x2(g[8 * k], g[8 * k + 1]), pack_bf16x2(g[8 * k + 2], g[8 * k + 3]),
+                                    pack_bf16x2(g[8 * k + 4], g[8 * k + 5]), pack_bf16x2(g[8 * k + 6], g[8 * k + 7]));
             }
           }
-        } else {
-          float v[32];
-          tmem_ld32_sync(tbase + cc * 32, v);
-          if (MODE == kModeLSE) {
+        });
+      } else {
+#pragma unroll 1
+        for (int cc = 0; cc < kCols / 32; ++cc) {
+          const int64_t col0 = n0 + cc * 32;
+          if (MODE == kModeDZ) {
+            float v[32];
+            tmem_ld32_sync(tbase + cc * 32, v);
+            if (row_ok) {
+              const bool bad = tgt < 0 || tgt >= p.V;
+              const float g = gdz, nl = -ls * kLog2e;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] *= p.inv_tau;
-          }
-          if (col0 + 32 > p.V) {
+              for (int j = 0; j < 32; ++j) {
+                const int64_t col = col0 + j;
+                float d = col < p.V ? g * ex2_approx(fmaf(v[j], kLog2e, nl)) : 0.f;
+                if (col == tgt) d -= g;
+                v[j] = bad ? __int_as_float(0x7FC00000) : d;
+              }
+              // dZ row segment: 32 bf16 = 64 contiguous bytes (ld_dz is a multiple of the tile width)
+              uint4* dst = reinterpret_cast<uint4*>(p.dz + row * p.ld_dz + col0);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j >= p.V) v[j] = -INFINITY;
-          }
-          if (MODE == kModeCE) {
-            const int64_t off = tgt - col0;
-            if (off >= 0 && off < 32) {
+              for (int k = 0; k < 4; ++k)
+                dst[k] = make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                                    pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+            }
+          } else if (store_mode<MODE>()) {
+            float v[32];
+            tmem_ld32_sync(tbase + cc * 32, v);
+            if (row_ok) {
+              float* dst = p.out + c.head * p.split_stride + row * p.ld_out + col0;
+              if (col0 + 32 <= p.V) {
+                float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) d4[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (col0 + j < p.V) dst[j] = v[j];
+              }
+            }
+          } else {
+            float v[32];
+            tmem_ld32_sync(tbase + cc * 32, v);
+            if (MODE == kModeLSE) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] *= p.inv_tau;
+            }
+            if (col0 + 32 > p.V) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (j == off) zt = v[j];
-              has_t = true;
+                if (col0 + j >= p.V) v[j] = -INFINITY;
             }
+            if (MODE == kModeCE) {
+              const int64_t off = tgt - col0;
+              if (off >= 0 && off < 32) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j == off) zt = v[j];
+                has_t = true;
+              }
+            }
+            ms_fold<32>(st, v);
           }
-          ms_fold<32>(st, v);
         }
       }
       // accumulator fully read: hand it back to the MMA warp
