@@ -76,6 +76,9 @@ struct ModeCfg {
   static constexpr int kHeadsPerUnit = two_head<MODE>() ? 2 : 1;
   static constexpr int kAccCols = BN * kHeadsPerUnit;      // TMEM columns of one accumulator
   static constexpr int kNumAcc = kTmemCols / kAccCols;     // 2 = double-buffered, 1 = single
+  // Release barriers: one per accumulator, or one per head of the single
+  // two-head accumulator (its heads are freed separately).
+  static constexpr int kNumFree = two_head<MODE>() ? 2 : kNumAcc;
   // Epilogue warps: 4 cover the 128 TMEM lanes; 8 = two per lane quadrant,
   // each taking half of the columns (the two-head epilogue is the heavier one).
   static constexpr int kEpiWarps = two_head<MODE>() ? 4 * kJsdColSplit : 4;
@@ -216,30 +219,31 @@ __device__ __forceinline__ void jsd_student(float lp, float lq, float beta, floa
   *lp_lm = p_is_hi ? a_hi : a_hi - d;
 }
 
-// Two-head epilogue walk over NCH 16-column chunks of this warp's slice: calls
-// f(chunk, student[16], teacher[16]) with the fp32 accumulator bits of the
-// warp's 32 rows, the next chunk's two TMEM loads in flight while the current
-// chunk is consumed.  No load is outstanding on return.
+// Two-head epilogue walk over NCH 16-column chunks of this warp's slice of the
+// single two-head accumulator: calls f(chunk, student[16], teacher[16]) with
+// the fp32 accumulator bits of the warp's 32 rows.  The student head's chunks
+// are read into registers first and its TMEM columns released on free0, so the
+// MMA warp starts the next unit's student head while this walk reads the
+// teacher head chunk by chunk; free1 releases the teacher columns at the end.
 template <int NCH, class F>
-__device__ __forceinline__ void two_head_chunks(uint32_t tbase, uint32_t head_off, F&& f) {
-  static_assert(NCH % 2 == 0, "chunks are consumed in pairs");
-  uint32_t as[16], at[16], bs[16], bt[16];
-  tmem_ld16(tbase, as);
-  tmem_ld16(tbase + head_off, at);
-  tmem_wait_ld(as, at);
+__device__ __forceinline__ void two_head_walk(uint32_t tbase, uint32_t head_off, uint64_t* free0, uint64_t* free1,
+                                              F&& f) {
+  uint32_t st[NCH][16], te[16];
 #pragma unroll
-  for (int cc = 0; cc < NCH; cc += 2) {
-    tmem_ld16(tbase + (cc + 1) * 16, bs);
-    tmem_ld16(tbase + head_off + (cc + 1) * 16, bt);
-    f(cc, as, at);
-    tmem_wait_ld(bs, bt);
-    if (cc + 2 < NCH) {
-      tmem_ld16(tbase + (cc + 2) * 16, as);
-      tmem_ld16(tbase + head_off + (cc + 2) * 16, at);
-    }
-    f(cc + 1, bs, bt);
-    if (cc + 2 < NCH) tmem_wait_ld(as, at);
+  for (int c = 0; c < NCH; ++c) tmem_ld16(tbase + c * 16, st[c]);
+  tmem_wait_ld(st[0]);
+#pragma unroll
+  for (int c = 1; c < NCH; ++c) reg_after_wait(st[c]);
+  tc_fence_before();
+  mbar_arrive(free0);
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    tmem_ld16(tbase + head_off + c * 16, te);
+    tmem_wait_ld(te);
+    f(c, st[c], te);
   }
+  tc_fence_before();
+  mbar_arrive(free1);
 }
 
 template <int MODE>
@@ -258,8 +262,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
   uint64_t* full = bars;               // [S]
   uint64_t* empty = bars + S;          // [S]
   uint64_t* acc_full = bars + 2 * S;                // [kNumAcc]
-  uint64_t* acc_empty = acc_full + C::kNumAcc;      // [kNumAcc]
-  uint64_t* drain = acc_empty + C::kNumAcc;         // [1]
+  uint64_t* acc_empty = acc_full + C::kNumAcc;      // [kNumFree]
+  uint64_t* drain = acc_empty + C::kNumFree;        // [1]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -270,10 +274,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < C::kNumAcc; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], C::kEpiWarps * 32);
-    }
+    for (int b = 0; b < C::kNumAcc; ++b) mbar_init(&acc_full[b], 1);
+    for (int b = 0; b < C::kNumFree; ++b) mbar_init(&acc_empty[b], C::kEpiWarps * 32);
     mbar_init(drain, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_a0);
@@ -350,9 +352,15 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
         const int kb_lo = store_mode<MODE>() ? decode_unit(p, u, MODE).head * p.kb_per : 0;
         const int kb_hi = store_mode<MODE>() ? min(p.k_blocks, kb_lo + p.kb_per) : p.k_blocks;
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, p.status)) break;
-        tc_fence_after();
+        if constexpr (!two_head<MODE>()) {
+          if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, p.status)) break;
+          tc_fence_after();
+        }
         for (int h = 0; h < C::kHeadsPerUnit && ok; ++h) {
+          if constexpr (two_head<MODE>()) {  // this head's columns released by the previous unit's epilogue
+            if (!mbar_wait(&acc_empty[h], acc_phase ^ 1u, p.timeout_ns, p.status)) { ok = false; break; }
+            tc_fence_after();
+          }
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols + h * BN);
           for (int kb = kb_lo; kb < kb_hi; ++kb) {
             if (!mbar_wait(&full[stage], phase, p.timeout_ns, p.status)) { ok = false; break; }
@@ -422,7 +430,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       bool has_t = false;
       float jsd = 0.f, kacc = 0.f;
       if constexpr (two_head<MODE>()) {
-        two_head_chunks<kCols / 16>(tbase, BN, [&](int cc, const uint32_t(&rs)[16], const uint32_t(&rt)[16]) {
+        two_head_walk<kCols / 16>(tbase, BN, &acc_empty[0], &acc_empty[1],
+                                  [&](int cc, const uint32_t(&rs)[16], const uint32_t(&rt)[16]) {
           const int64_t col0 = n0 + cc * 16;
           if constexpr (MODE == kModeJSD) {
             if (col0 + 16 <= p.V) {
@@ -530,9 +539,11 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
           }
         }
       }
-      // accumulator fully read: hand it back to the MMA warp
-      tc_fence_before();
-      mbar_arrive(&acc_empty[acc]);
+      // accumulator fully read: hand it back to the MMA warp (two-head: done per head by the walk)
+      if constexpr (!two_head<MODE>()) {
+        tc_fence_before();
+        mbar_arrive(&acc_empty[acc]);
+      }
       if (++acc == C::kNumAcc) { acc = 0; acc_phase ^= 1u; }
       if (row_ok && (MODE == kModeCE || MODE == kModeLSE || MODE == kModeJSD || MODE == kModeJSDK)) {
         // partial slot of this (vocab tile, column slice)
