@@ -76,8 +76,8 @@ struct ModeCfg {
   static constexpr int kHeadsPerUnit = two_head<MODE>() ? 2 : 1;
   static constexpr int kAccCols = BN * kHeadsPerUnit;      // TMEM columns of one accumulator
   static constexpr int kNumAcc = kTmemCols / kAccCols;     // 2 = double-buffered, 1 = single
-  // Release barriers: one per accumulator, or one per head of the single
-  // two-head accumulator (its heads are freed separately).
+  // Full and release barriers: one per accumulator, or one per head of the
+  // single two-head accumulator (its heads complete and are freed separately).
   static constexpr int kNumFree = two_head<MODE>() ? 2 : kNumAcc;
   // Epilogue warps: 4 cover the 128 TMEM lanes; 8 = two per lane quadrant,
   // each taking half of the columns (the two-head epilogue is the heavier one).
@@ -221,13 +221,15 @@ __device__ __forceinline__ void jsd_student(float lp, float lq, float beta, floa
 
 // Two-head epilogue walk over NCH 16-column chunks of this warp's slice of the
 // single two-head accumulator: calls f(chunk, student[16], teacher[16]) with
-// the fp32 accumulator bits of the warp's 32 rows.  The student head's chunks
-// are read into registers first and its TMEM columns released on free0, so the
-// MMA warp starts the next unit's student head while this walk reads the
-// teacher head chunk by chunk; free1 releases the teacher columns at the end.
+// the fp32 accumulator bits of the warp's 32 rows.  The student head (complete
+// when the caller's wait on its full barrier returned) is read into registers
+// and its TMEM columns released on free0 while the MMA warp still computes the
+// teacher head; once full1 (the teacher head) completes its chunks are read one
+// by one, and free1 releases them.  Returns false if the wait on full1 gave up.
 template <int NCH, class F>
-__device__ __forceinline__ void two_head_walk(uint32_t tbase, uint32_t head_off, uint64_t* free0, uint64_t* free1,
-                                              F&& f) {
+__device__ __forceinline__ bool two_head_walk(uint32_t tbase, uint32_t head_off, uint64_t* full1, uint32_t parity,
+                                              uint64_t* free0, uint64_t* free1, uint64_t timeout_ns,
+                                              uint32_t* status, F&& f) {
   uint32_t st[NCH][16], te[16];
 #pragma unroll
   for (int c = 0; c < NCH; ++c) tmem_ld16(tbase + c * 16, st[c]);
@@ -236,6 +238,8 @@ __device__ __forceinline__ void two_head_walk(uint32_t tbase, uint32_t head_off,
   for (int c = 1; c < NCH; ++c) reg_after_wait(st[c]);
   tc_fence_before();
   mbar_arrive(free0);
+  if (!__all_sync(0xFFFFFFFFu, mbar_wait(full1, parity, timeout_ns, status))) return false;
+  tc_fence_after();
 #pragma unroll
   for (int c = 0; c < NCH; ++c) {
     tmem_ld16(tbase + head_off + c * 16, te);
@@ -244,6 +248,7 @@ __device__ __forceinline__ void two_head_walk(uint32_t tbase, uint32_t head_off,
   }
   tc_fence_before();
   mbar_arrive(free1);
+  return true;
 }
 
 template <int MODE>
@@ -261,8 +266,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
   uint64_t* full = bars;               // [S]
   uint64_t* empty = bars + S;          // [S]
-  uint64_t* acc_full = bars + 2 * S;                // [kNumAcc]
-  uint64_t* acc_empty = acc_full + C::kNumAcc;      // [kNumFree]
+  uint64_t* acc_full = bars + 2 * S;                // [kNumFree]
+  uint64_t* acc_empty = acc_full + C::kNumFree;     // [kNumFree]
   uint64_t* drain = acc_empty + C::kNumFree;        // [1]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
 
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < C::kNumAcc; ++b) mbar_init(&acc_full[b], 1);
+    for (int b = 0; b < C::kNumFree; ++b) mbar_init(&acc_full[b], 1);
     for (int b = 0; b < C::kNumFree; ++b) mbar_init(&acc_empty[b], C::kEpiWarps * 32);
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -377,9 +382,11 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
             tc_commit(&empty[stage]);
             if (++stage == S) { stage = 0; phase ^= 1u; }
           }
+          if constexpr (two_head<MODE>())
+            if (ok) tc_commit(&acc_full[h]);  // this head's accumulator is complete
         }
         if (!ok) break;
-        tc_commit(&acc_full[acc]);
+        if constexpr (!two_head<MODE>()) tc_commit(&acc_full[acc]);
         if (++acc == C::kNumAcc) { acc = 0; acc_phase ^= 1u; }
       }
       // All MMAs issued by this thread complete before TMEM is released.
@@ -430,8 +437,9 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       bool has_t = false;
       float jsd = 0.f, kacc = 0.f;
       if constexpr (two_head<MODE>()) {
-        two_head_walk<kCols / 16>(tbase, BN, &acc_empty[0], &acc_empty[1],
-                                  [&](int cc, const uint32_t(&rs)[16], const uint32_t(&rt)[16]) {
+        const bool walked = two_head_walk<kCols / 16>(
+            tbase, BN, &acc_full[1], acc_phase, &acc_empty[0], &acc_empty[1], p.timeout_ns, p.status,
+            [&](int cc, const uint32_t(&rs)[16], const uint32_t(&rt)[16]) {
           const int64_t col0 = n0 + cc * 16;
           if constexpr (MODE == kModeJSD) {
             if (col0 + 16 <= p.V) {
@@ -475,6 +483,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
             }
           }
         });
+        if (!walked) break;
       } else {
 #pragma unroll 1
         for (int cc = 0; cc < kCols / 32; ++cc) {
