@@ -88,7 +88,12 @@ struct ModeCfg {
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = kSmemBudget / kStageBytes;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers*/;
+  // STORE epilogues stage each warp's 32 x 32 fp32 block (rows padded to 36
+  // floats) to write it back as whole 128-byte rows.
+  static constexpr int kOutPitch = 36;
+  static constexpr int kOutStageBytes = store_mode<MODE>() ? kEpiWarps * 32 * kOutPitch * 4 : 0;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 512 /*barriers*/ + kOutStageBytes;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(kNumAcc >= 1 && kNumAcc * kAccCols == kTmemCols, "accumulators tile TMEM");
   static_assert(BN % (32 * kColSplit) == 0, "epilogue column split");
   // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
@@ -270,6 +275,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
   uint64_t* acc_empty = acc_full + C::kNumFree;     // [kNumFree]
   uint64_t* drain = acc_empty + C::kNumFree;        // [1]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  float* out_stage = reinterpret_cast<float*>(smem + S * C::kStageBytes + 512);  // STORE: [kEpiWarps][32][kOutPitch]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -509,20 +515,36 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
                                     pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
             }
           } else if (store_mode<MODE>()) {
+            // Lane = row: stage the warp's 32 rows x 32 columns in shared memory,
+            // then write them back 4 rows x 128 contiguous bytes per instruction
+            // (8 lanes per row) instead of 32 rows x 16 bytes.
             float v[32];
             tmem_ld32_sync(tbase + cc * 32, v);
-            if (row_ok) {
-              float* dst = p.out + c.head * p.split_stride + row * p.ld_out + col0;
-              if (col0 + 32 <= p.V) {
-                float4* d4 = reinterpret_cast<float4*>(dst);
+            float* sw = out_stage + (warp - 2) * 32 * C::kOutPitch;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) d4[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-              } else {
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(sw + lane * C::kOutPitch + 4 * k) =
+                  make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+            __syncwarp();
+            const int c4 = (lane & 7) * 4;
+            const int64_t row0 = static_cast<int64_t>(c.mt) * kBM + quad * 32;
+            float* obase = p.out + c.head * p.split_stride + col0 + c4;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (col0 + j < p.V) dst[j] = v[j];
+            for (int i = 0; i < 8; ++i) {
+              const int r = 4 * i + (lane >> 3);
+              const float4 val = *reinterpret_cast<const float4*>(sw + r * C::kOutPitch + c4);
+              if (row0 + r < p.T) {
+                float* dst = obase + (row0 + r) * p.ld_out;
+                if (col0 + c4 + 4 <= p.V) {
+                  *reinterpret_cast<float4*>(dst) = val;
+                } else {
+                  if (col0 + c4 < p.V) dst[0] = val.x;
+                  if (col0 + c4 + 1 < p.V) dst[1] = val.y;
+                  if (col0 + c4 + 2 < p.V) dst[2] = val.z;
+                }
               }
             }
+            __syncwarp();
           } else {
             float v[32];
             tmem_ld32_sync(tbase + cc * 32, v);
