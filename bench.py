@@ -239,18 +239,21 @@ def run_ours(args, rank, world, local_rank):
                 e.record(stream)
     torch.cuda.synchronize()
 
+    op_fns = {
+        "ce": lambda: lmho.ce_fwd_f32(d["ce_z"], d["ce_t"], loss=out["ce"], ws=ws_ce),
+        "sbv": lambda: lmho.ce_fwd_sbv_bf16(d["sbv_z"], d["sbv_t"], loss=out["sbv"]),
+        "fl": lambda: lmho.flce_fwd_bf16(d["fl_x"], d["fl_w"], d["fl_t"], loss=out["fl"], ws=ws_fl),
+        "js": lambda: lmho.fljsd_fwd_bf16(d["js_xs"], d["js_ws"], d["js_xt"], d["js_wt"], 0.5,
+                                          loss=out["js"], ws=ws_js),
+    }
+
     def step(i=None):
-        def call(op, fn):
+        for op in ("ce", "sbv", "fl", "js"):
             if i is not None:
                 lmho.set_launch_events(ev[op][i])
-            fn()
+            op_fns[op]()
             if i is not None:
                 lmho.set_launch_events(None)
-        call("ce", lambda: lmho.ce_fwd_f32(d["ce_z"], d["ce_t"], loss=out["ce"], ws=ws_ce))
-        call("sbv", lambda: lmho.ce_fwd_sbv_bf16(d["sbv_z"], d["sbv_t"], loss=out["sbv"]))
-        call("fl", lambda: lmho.flce_fwd_bf16(d["fl_x"], d["fl_w"], d["fl_t"], loss=out["fl"], ws=ws_fl))
-        call("js", lambda: lmho.fljsd_fwd_bf16(d["js_xs"], d["js_ws"], d["js_xt"], d["js_wt"], 0.5,
-                                               loss=out["js"], ws=ws_js))
 
     for _ in range(args.warmup):
         step()
@@ -343,16 +346,31 @@ def run_ours(args, rank, world, local_rank):
         h2d = sum(v.numel() * v.element_size() for v in h.values())
         d2h = sum(v.numel() * v.element_size() for v in out.values())
 
+        # Each op's inputs are copied on a second stream, in the order below (most
+        # compute per copied byte first), and each op waits only for its own
+        # inputs, so copies of later inputs overlap earlier ops' kernels.  A step's
+        # copies start after the previous step's kernels (buffers are reused).
+        copy_stream = torch.cuda.Stream(device=dev)
+        order = (("js", ("js_xs", "js_ws", "js_xt", "js_wt")), ("fl", ("fl_x", "fl_w", "fl_t")),
+                 ("sbv", ("sbv_z", "sbv_t")), ("ce", ("ce_z", "ce_t")))
+        assert sorted(k for _, ks in order for k in ks) == sorted(h)
+        landed = {op: torch.cuda.Event() for op, _ in order}
+
         def e2e_step(marks=None):
             if marks:
                 marks[0].record(stream)
-            for k, v in h.items():
-                d[k].copy_(v, non_blocking=True)
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                for op, keys in order:
+                    for k in keys:
+                        d[k].copy_(h[k], non_blocking=True)
+                    landed[op].record(copy_stream)
+            for op, _ in order:
+                stream.wait_event(landed[op])
+                op_fns[op]()
             if marks:
-                marks[1].record(stream)
-            step()
-            if marks:
-                marks[2].record(stream)
+                marks[1].record(copy_stream)   # last input landed
+                marks[2].record(stream)        # last kernel done
             for k, v in out.items():
                 host_out[k].copy_(v, non_blocking=True)
             if marks:
@@ -372,12 +390,15 @@ def run_ours(args, rank, world, local_rank):
             barrier()
         ms_e2e = max_over_ranks(e0.elapsed_time(e1) / Ke)
         clock_e2e = ck.summary()
-        phase = [float(np.mean([m[a].elapsed_time(m[a + 1]) for m in marks])) for a in range(3)]
+        copy_ms = float(np.mean([m[0].elapsed_time(m[1]) for m in marks]))
+        kern_ms = float(np.mean([m[0].elapsed_time(m[2]) for m in marks]))
+        d2h_ms = float(np.mean([m[2].elapsed_time(m[3]) for m in marks]))
         e2e = {"value": round(ms_e2e * 1e3, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": Ke,
-               "phases_us": {"h2d": round(phase[0] * 1e3, 1), "compute": round(phase[1] * 1e3, 1),
-                             "d2h": round(phase[2] * 1e3, 1)},
-               "h2d_GBps": round(h2d / (phase[0] * 1e-3) / 1e9, 1)}
+               "overlap": "each op's inputs copied on a second stream, ops start as their inputs land",
+               "phases_us": {"inputs_landed": round(copy_ms * 1e3, 1), "kernels_done": round(kern_ms * 1e3, 1),
+                             "d2h": round(d2h_ms * 1e3, 1)},
+               "h2d_GBps": round(h2d / (copy_ms * 1e-3) / 1e9, 1)}
 
     result = {
         "metric": METRIC, "value": round(ms_step * 1e3, 1), "unit": UNIT, "n_gpus": world, "steps": K,
