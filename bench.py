@@ -398,7 +398,9 @@ def run_ours(args, rank, world, local_rank):
                "overlap": "each op's inputs copied on a second stream, ops start as their inputs land",
                "phases_us": {"inputs_landed": round(copy_ms * 1e3, 1), "kernels_done": round(kern_ms * 1e3, 1),
                              "d2h": round(d2h_ms * 1e3, 1)},
-               "h2d_GBps": round(h2d / (copy_ms * 1e-3) / 1e9, 1)}
+               "h2d_GBps": round(h2d / (copy_ms * 1e-3) / 1e9, 1),
+               # per step: the host link is shared with other GPUs' jobs on the same CPU
+               "h2d_GBps_per_step": [round(h2d / (m[0].elapsed_time(m[1]) * 1e-3) / 1e9, 1) for m in marks]}
 
     result = {
         "metric": METRIC, "value": round(ms_step * 1e3, 1), "unit": UNIT, "n_gpus": world, "steps": K,
