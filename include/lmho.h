@@ -318,9 +318,10 @@ int lmho_set_ce_variant(int variant);
  * (token tile x vocab tile) are ordered in groups of `group_m` token tiles,
  * vocab tiles outer within a group, so the CTAs running at one time share W
  * tiles in L2; W streams from HBM about ceil(T/128/group_m) times per head
- * and pass.  0 = automatic (16); otherwise 1..1024.  Affects speed and DRAM
- * traffic only, never results.  Returns LMHO_ERR_INVALID_ARG outside that
- * range. */
+ * and pass.  0 = automatic: 32 for single-head passes, 16 for the two-head
+ * JSD passes (both heads' tiles share L2) and for the gradient products;
+ * otherwise 1..1024 for every pass.  Affects speed and DRAM traffic only,
+ * never results.  Returns LMHO_ERR_INVALID_ARG outside that range. */
 int lmho_set_raster_group(int group_m);
 
 /* Measurement hook, process-wide and not thread-safe: while set, every call

@@ -189,15 +189,18 @@ int tmap_bf16_mn(CUtensorMap* m, const void* base, int64_t k_rows, int64_t mn, i
   return r == CUDA_SUCCESS ? LMHO_OK : LMHO_ERR_CUDA;
 }
 
-FusedGeometry geometry(int64_t T, int64_t H, int64_t V, int bn) {
+// `group` = the default raster group of the pass (lmho_set_raster_group overrides it).
+FusedGeometry geometry(int64_t T, int64_t H, int64_t V, int bn, int group = kGroupSingle) {
   FusedGeometry g{};
   g.T = T;
   g.H = H;
   g.V = V;
   g.num_m = (T + kBM - 1) / kBM;
   g.num_n = (V + bn - 1) / bn;
-  const int64_t want = g_group_m.load() > 0 ? g_group_m.load() : 16;
+  const int over = g_group_m.load();
+  const int64_t want = over > 0 ? over : group;
   g.group_m = static_cast<int>(g.num_m < want ? g.num_m : want);
+  g.group_store = over > 0 ? over : kGroupStore;
   return g;
 }
 
@@ -548,7 +551,7 @@ int fljsd_impl(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, const
       tmap_bf16(&twt256, Wt, V, H, kBN_CE) || tmap_bf16(&twsj, Ws, V, H, kBN_JSD) ||
       tmap_bf16(&twtj, Wt, V, H, kBN_JSD))
     return LMHO_ERR_CUDA;
-  const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD);
+  const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD, kGroupTwoHead);
   const FusedWs w = fljsd_ws_carve(ws, ws_bytes, T, V);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
   return cuda_status(
@@ -601,7 +604,7 @@ int fljsd_fwd_bwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* x
       tmap_bf16_mn(&m.ws_mn, Ws, V, H, H) || tmap_bf16_mn(&m.dz_mn, bw.dz, T, V, bw.ld_dz) ||
       tmap_bf16_mn(&m.xs_mn, xs, T, H, H))
     return LMHO_ERR_CUDA;
-  const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD);
+  const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD, kGroupTwoHead);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_fljsd_fwd_bwd(m, g1, g2, beta, 1.f / temperature, keep, grad_scale, loss, dxs, dWs, w, bw,
                                           bw.lse, inv_count, L));

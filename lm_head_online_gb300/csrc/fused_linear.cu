@@ -1014,12 +1014,12 @@ cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const int64_t* target, con
   if ((e = launch_gemm<kModeDZ>(m.x, m.w, m.x, m.w, q, L)) != cudaSuccess) return e;
   launch_mark(2, L.stream);
   // dx [T, H] = dZ [T, V] W [V, H]  (K = V; W read MN-major)
-  if ((e = launch_store_gemm<kModeStore>(m.dz, m.w_mn, g.T, g.H, g.V, dx, bw.split, g.group_m, ws.ctrl, L)) !=
+  if ((e = launch_store_gemm<kModeStore>(m.dz, m.w_mn, g.T, g.H, g.V, dx, bw.split, g.group_store, ws.ctrl, L)) !=
       cudaSuccess)
     return e;
   launch_mark(3, L.stream);
   // dW [V, H] = dZ^T [V, T] x [T, H]  (K = T; dZ and x read MN-major)
-  if ((e = launch_store_gemm<kModeStoreT>(m.dz_mn, m.x_mn, g.V, g.H, g.T, dW, bw.split, g.group_m, ws.ctrl, L)) !=
+  if ((e = launch_store_gemm<kModeStoreT>(m.dz_mn, m.x_mn, g.V, g.H, g.T, dW, bw.split, g.group_store, ws.ctrl, L)) !=
       cudaSuccess)
     return e;
   launch_mark(4, L.stream);
@@ -1073,11 +1073,11 @@ cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const FusedGeometry& g_l
   if ((e = launch_gemm<kModeDZJ>(m.xs, m.wsj, m.xt, m.wtj, r, L)) != cudaSuccess) return e;
   launch_mark(2, L.stream);
   // dxs = dZs Ws (K = V), dWs = dZs^T xs (K = T)
-  if ((e = launch_store_gemm<kModeStore>(m.dz, m.ws_mn, T, H, V, dxs, bw.split, g_lse.group_m, ws.ctrl, L)) !=
+  if ((e = launch_store_gemm<kModeStore>(m.dz, m.ws_mn, T, H, V, dxs, bw.split, g_lse.group_store, ws.ctrl, L)) !=
       cudaSuccess)
     return e;
   launch_mark(3, L.stream);
-  if ((e = launch_store_gemm<kModeStoreT>(m.dz_mn, m.xs_mn, V, H, T, dWs, bw.split, g_lse.group_m, ws.ctrl, L)) !=
+  if ((e = launch_store_gemm<kModeStoreT>(m.dz_mn, m.xs_mn, V, H, T, dWs, bw.split, g_lse.group_store, ws.ctrl, L)) !=
       cudaSuccess)
     return e;
   launch_mark(4, L.stream);

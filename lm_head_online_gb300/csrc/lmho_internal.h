@@ -56,7 +56,16 @@ struct FusedGeometry {
   int64_t T, H, V;
   int64_t num_m, num_n;   // tiles along tokens and vocab
   int group_m;            // m-tiles per raster group (L2 reuse of W)
+  int group_store;        // raster group of the gradient products (dx, dW)
 };
+// Default raster groups (token tiles of 128): single-head passes keep 32 tiles'
+// x and the W tiles a wave shares in L2; a two-head pass holds both heads' tiles,
+// so half as many; the gradient products use 16.  Measured in the power-capped
+// bench step: 16 -> 32 took the flce and log-sum-exp passes 1-2 % faster and
+// the two-head pass 3 % slower; 64 and 128 thrash L2 (8-15 % slower).
+constexpr int kGroupSingle = 32;
+constexpr int kGroupTwoHead = 16;
+constexpr int kGroupStore = 16;
 
 // Workspace carve-up of the fused paths (all offsets 256-byte aligned).
 struct FusedWs {
