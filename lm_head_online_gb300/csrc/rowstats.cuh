@@ -112,8 +112,8 @@ struct KSum {
 // block that produced losses once they are stored; the last of `nwriters`
 // blocks sums them and writes *loss, then clears the ticket.  The summation
 // order is fixed and independent of the block size: 256 virtual lanes each
-// take every 256th float4 in index order (compensated fp32, 8 loads in
-// flight); warp 0 then folds 8 lane sums per lane (compensated) and finishes
+// take every 256th float4 in index order (compensated fp32, 16 or 8 loads
+// in flight); warp 0 then folds 8 lane sums per lane (compensated) and finishes
 // with a butterfly whose partners add the same two values.  No fp64: its rate
 // on this part is a small fraction of fp32 and a serial fp64 tail costs tens
 // of microseconds.  With a keep mask (uint8 per row, may be null) the divisor
@@ -143,6 +143,15 @@ __device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, floa
       for (int64_t r = j; r < T; r += kVL) cnt += __ldg(keep + r) != 0;
     s_cnt[j] = cnt;
     int64_t i = j;
+    for (; i + 15 * kVL < n4; i += 16 * kVL) {  // 16 loads in flight (T = 16384: one round trip)
+      float4 q[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) q[k] = __ldcg(v4 + i + k * kVL);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        a.add(q[k].x); a.add(q[k].y); a.add(q[k].z); a.add(q[k].w);
+      }
+    }
     for (; i + 7 * kVL < n4; i += 8 * kVL) {
       float4 q[8];
 #pragma unroll
