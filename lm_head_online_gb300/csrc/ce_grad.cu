@@ -7,8 +7,11 @@
 // log-sum-exp before any element can be written, so the logits would be read
 // twice; here each row is read once into shared memory and the gradient is
 // written from there:
-//   * a cluster of C CTAs per row (C = 1 for rows up to 48 KB), CTA k staging
-//     the k-th slice (at most 64 KB) while folding the online (max, sum exp);
+//   * a cluster of C CTAs per row (C = 1 for rows up to 64 KB), CTA k staging
+//     the k-th slice (at most 64 KB) while folding the online (max, sum exp).
+//     Measured on GB300: one CTA per 64 KB row moves 6.6 TB/s of read + write
+//     where a pair of CTAs moved 5.1-5.8; slices of 128 KB or more (one CTA per
+//     SM) are slower than clusters of 64 KB slices at every size;
 //   * the C slice partials are exchanged through distributed shared memory
 //     (every CTA merges them in rank order, so all agree bit for bit on the
 //     row's log-sum-exp);
@@ -23,6 +26,7 @@
 // in the status word when there is one).
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 
 #include "lmho_internal.h"
 #include "ptx.cuh"
@@ -31,7 +35,7 @@
 namespace lmho {
 namespace {
 
-constexpr int64_t kSliceMaxBytes = 64 * 1024;
+constexpr int64_t kSliceMaxBytes = 192 * 1024;   // largest slice a CTA can stage (shared memory)
 
 template <typename T> struct Out;
 template <> struct Out<float> {
@@ -239,21 +243,31 @@ cudaError_t launch_fb_rows(const T* logits, const int64_t* target, int64_t rows,
   auto slice_for = [&](int c) {  // elements per CTA, a multiple of 64
     return ((V + c - 1) / c + 63) / 64 * 64;
   };
+  // Largest slice a cluster CTA stages (default 64 KB) and longest row one CTA
+  // stages alone (default 64 KB); LMHO_FB_SLICE_KB / LMHO_FB_SINGLE_KB = 16..192
+  // override them for sweeps.
+  auto knob = [](const char* name, int64_t dflt) {
+    const char* v = std::getenv(name);
+    const long kb = v ? std::strtol(v, nullptr, 10) : 0;
+    return (kb >= 16 && kb * 1024 <= kSliceMaxBytes) ? static_cast<int64_t>(kb) * 1024 : dflt;
+  };
+  static const int64_t cap = knob("LMHO_FB_SLICE_KB", 64 * 1024);
+  static const int64_t single = knob("LMHO_FB_SINGLE_KB", 64 * 1024);
   launch_mark(0, st);
   cudaError_t e;
   if (row_bytes <= 16 * 1024)
     e = launch_fb<T, 1, 128, true>(logits, target, rows, V, slice_for(1), dloss, gscale, out_rows, dlogits, mean_out,
                                    ctrl, tmo, st);
-  else if (row_bytes <= 48 * 1024)
+  else if (row_bytes <= single)
     e = launch_fb<T, 1, 256, true>(logits, target, rows, V, slice_for(1), dloss, gscale, out_rows, dlogits, mean_out,
                                    ctrl, tmo, st);
-  else if (slice_for(2) * static_cast<int64_t>(sizeof(T)) <= kSliceMaxBytes)
+  else if (slice_for(2) * static_cast<int64_t>(sizeof(T)) <= cap)
     e = launch_fb<T, 2, 256, true>(logits, target, rows, V, slice_for(2), dloss, gscale, out_rows, dlogits, mean_out,
                                    ctrl, tmo, st);
-  else if (slice_for(4) * static_cast<int64_t>(sizeof(T)) <= kSliceMaxBytes)
+  else if (slice_for(4) * static_cast<int64_t>(sizeof(T)) <= cap)
     e = launch_fb<T, 4, 256, true>(logits, target, rows, V, slice_for(4), dloss, gscale, out_rows, dlogits, mean_out,
                                    ctrl, tmo, st);
-  else if (slice_for(8) * static_cast<int64_t>(sizeof(T)) <= kSliceMaxBytes)
+  else if (slice_for(8) * static_cast<int64_t>(sizeof(T)) <= cap)
     e = launch_fb<T, 8, 256, true>(logits, target, rows, V, slice_for(8), dloss, gscale, out_rows, dlogits, mean_out,
                                    ctrl, tmo, st);
   else
