@@ -1,36 +1,42 @@
-// Fused linear + cross-entropy and fused linear + generalized JSD on the
-// 5th-generation tensor cores, logits never written to memory.
+// Fused linear + cross-entropy, + CPO and + generalized JSD on the
+// 5th-generation tensor cores, forward and backward, logits never written to
+// memory.
 //
 // Operations: page "Fused linear + CPO loss" (summary: activations projected
 // through a vocab x hidden LM head, "computed chunked without materializing
-// logits"; its cross-entropy core) and page "Fused linear + JSD" (summary:
-// student and teacher heads, generalized JSD with beta 0.5, batchmean).
+// logits"; Semantics: x, weight, target, loss) and page "Fused linear + JSD"
+// (summary: student and teacher heads, generalized JSD with beta 0.5,
+// batchmean).
 //
 // One persistent kernel per pass, one CTA per SM, warp-specialised:
-//   warp 0      TMA producer: bf16 tiles x[128 x 64] and W[BN x 64] (128-byte
-//               swizzle) into a ring of shared-memory stages (mbarrier
-//               complete_tx);
+//   warp 0      TMA producer: bf16 tiles of A [128 x 64] and B [BN x 64]
+//               (128-byte swizzle; K-major, or MN-major boxes of 64 x 64 for
+//               the gradient products) into a ring of shared-memory stages
+//               (mbarrier complete_tx);
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
-//               (M=128, N=BN, K=16, bf16 x bf16 -> fp32) into one of two TMEM
-//               accumulators, frees stages with tcgen05.commit;
-//   warps 2..5  epilogue: each thread owns one token row (one TMEM lane),
-//               reads its accumulator row 32 columns at a time (tcgen05.ld) and
-//               folds it into per-row partials while the MMA fills the other
-//               accumulator.
+//               (M=128, N=BN, K=16, bf16 x bf16 -> fp32) and frees stages with
+//               tcgen05.commit;
+//   warps 2..   epilogue (4 warps, 8 for the two-head passes): each thread owns
+//               one token row (one TMEM lane) and reads its accumulator row with
+//               tcgen05.ld.
+// Single-head passes double-buffer two 256-column accumulators, so the epilogue
+// of one unit overlaps the MMAs of the next.  Two-head passes (BN = 256 per
+// head) fill TMEM with one unit; its heads complete and are released
+// separately, so the next unit's student MMAs overlap this unit's epilogue.
 // Work unit = (token tile, vocab tile), rastered in groups of `group_m` token
 // tiles so a wave of CTAs shares the same W tiles in L2 and each W tile is
 // read from HBM about once per group.
 //
 // Epilogues (per row r of the tile, vocab columns n0 .. n0+BN-1):
-//   CE   running (max, sum exp) of the tile and the target logit if t_r falls
-//        in the tile  -> partials [num_n][T] x 3
-//   LSE  (max, sum exp) only, for the student and teacher heads (first JSD
-//        pass)        -> partials [2][num_n][T] x 2
-//   JSD  both heads' tiles in TMEM (BN = 128 each); with lp = z_s - lse_s,
-//        lq = z_t - lse_t, accumulates
-//          beta P (lp - lm) + (1-beta) Q (lq - lm),  lm = ln(beta P + (1-beta) Q)
-//        evaluated around the larger of lp, lq so no large terms cancel
-//                     -> partial sums [num_n][T]
+//   CE     running (max, sum exp) of the tile and the target logit if t_r
+//          falls in the tile  -> partials [num_n][T] x 3
+//   LSE    (max, sum exp) only, for the student and teacher heads (first JSD
+//          pass)  -> partials [2][num_n][T] x 2
+//   JSD    both heads' tiles; the generalized-JSD term of every pair, evaluated
+//          around the larger log-probability so no large terms cancel
+//          -> partial sums [num_n][T] (JSDK: also KL(P || M) for the backward)
+//   DZ     the CE gradient of the tile, bf16 dZ rows (DZJ: the JSD student's)
+//   STORE  fp32 tile of a gradient product (dx = dZ W, dW = dZ^T x)
 // Finalisers merge the vocab-tile partials of each row in a fixed order and
 // reduce the rows deterministically (see rowstats.cuh).
 #include <cmath>
