@@ -12,9 +12,10 @@
 //     Measured on GB300: one CTA per 64 KB row moves 6.6 TB/s of read + write
 //     where a pair of CTAs moved 5.1-5.8; slices of 128 KB or more (one CTA per
 //     SM) are slower than clusters of 64 KB slices at every size;
-//   * the C slice partials are exchanged through distributed shared memory
-//     (every CTA merges them in rank order, so all agree bit for bit on the
-//     row's log-sum-exp);
+//   * the C slice partials are exchanged through distributed shared memory:
+//     each CTA pushes its partial into every peer, one cluster barrier, then
+//     every CTA merges them in rank order (all agree bit for bit on the row's
+//     log-sum-exp);
 //   * each CTA then writes its slice of the gradient, 16-byte stores where the
 //     gradient row has the logits' alignment, scalar stores otherwise.
 // When the slice's start and length are multiples of 16 bytes, one thread
@@ -64,10 +65,11 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT)
   constexpr int U = 4;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ MS s_part[NT / 32];
-  __shared__ float s_ms[2];
+  __shared__ float s_peer[C][2];   // (max, sum exp) of every CTA of the cluster, pushed by its owner
   __shared__ float s_lse;
   __shared__ uint64_t s_bar;
   const uint32_t rank = (C > 1) ? cluster_ctarank() : 0u;
+  if (C > 1) cluster_arrive_relaxed();   // barrier phase 0: this CTA is running
   const int tid = threadIdx.x;
   const int64_t r = blockIdx.x / C;
   const T* row = logits + r * V;
@@ -153,15 +155,22 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT)
   if (C == 1) {
     if (tid == 0) s_lse = a.m + logf(a.s);
   } else {
-    if (tid == 0) { s_ms[0] = a.m; s_ms[1] = a.s; }
+    // Phase 0 completes at once (every CTA arrived at its start), proving all
+    // peers run; each CTA then pushes its partial into every peer's s_peer.
+    // After phase 1 every CTA holds all C partials locally and touches no
+    // other CTA's shared memory again, so one full barrier suffices.
+    cluster_wait();
+    if (tid == 0)
+      for (uint32_t k = 0; k < C; ++k) {
+        st_dsmem_f32(mapa_shared(&s_peer[rank][0], k), a.m);
+        st_dsmem_f32(mapa_shared(&s_peer[rank][1], k), a.s);
+      }
     cluster_sync();
     if (tid == 0) {
       MS tot = ms_empty();
-      for (uint32_t k = 0; k < C; ++k)
-        tot = ms_merge(tot, MS{ld_dsmem_f32(mapa_shared(&s_ms[0], k)), ld_dsmem_f32(mapa_shared(&s_ms[1], k))});
+      for (uint32_t k = 0; k < C; ++k) tot = ms_merge(tot, MS{s_peer[k][0], s_peer[k][1]});
       s_lse = tot.m + logf(tot.s);
     }
-    cluster_sync();  // every CTA has read its peers' partials before any may exit
   }
   __syncthreads();
   const float lse = s_lse;
