@@ -140,3 +140,21 @@ def test_cpo_full_size_batch2(gpu_lib):
     xs = gen.bf16_bits_to_f32(xf).astype(np.float64)
     assert float(np.sum(dxn * xs)) == pytest.approx(float(np.sum(dWn * Ws)), rel=1e-3)
     assert np.abs(dWn.sum(axis=0)).max() <= 1e-3 * np.abs(dWn).sum(axis=0).max()
+
+
+def test_cpo_workspace_reuse_leaves_ticket_at_zero(gpu_lib):
+    """Both finalisers of a CPO call (the CE mean and the pair combination) use
+    the workspace's ticket word and must leave it at zero: repeated calls on one
+    workspace, forward and forward + backward, give identical bits."""
+    B, S, H, V = 4, 40, 128, 900
+    x, W, t = inputs(54, B, S, H, V, sw=0.2)
+    xd, Wd, td = to_dev_bf16(x), to_dev_bf16(W), to_dev(t)
+    ws = gpu_lib.workspace(gpu_lib.flce_cpo_bwd_workspace_bytes(B, S, H, V))
+    outs = [gpu_lib.flce_cpo_fwd_bwd_bf16(xd, Wd, td, 0.3, 1.0, ws=ws) for _ in range(3)]
+    outs = [[o.clone() for o in r] for r in outs]
+    assert int(ws[-256:].view(torch.int32)[1].item()) == 0
+    for r in outs[1:]:
+        assert all(torch.equal(p, q) for p, q in zip(r, outs[0]))
+    f = [gpu_lib.flce_cpo_fwd_bf16(xd, Wd, td, 0.3, 1.0, ws=ws)[0].clone() for _ in range(2)]
+    assert torch.equal(f[0], f[1]) and torch.equal(f[0], outs[0][0])
+    assert int(ws[-256:].view(torch.int32)[1].item()) == 0
