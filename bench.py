@@ -51,7 +51,7 @@ KERNELS_PER_STEP = 1 + 1 + 2 + 4
 # profiles/dram_traffic_bench_step.md).  They hold only for the kernel sources
 # they were taken from: a changed source makes the bench report null.
 KERNEL_SOURCES = ("fused_linear.cu", "ce_rows.cu", "rowstats.cuh", "ptx.cuh", "lmho_internal.h")
-TRAFFIC_SOURCE_DIGEST = "f3efd4d537a13e51"
+TRAFFIC_SOURCE_DIGEST = "cfd6a50431b8eca7"
 TRAFFIC_BYTES = {
     "ce_fwd_f32.row_kernel": 8590167040 + 3181568,
     "ce_fwd_sbv_bf16.row_kernel": 2147609856 + 90624,
