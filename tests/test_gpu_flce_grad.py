@@ -42,7 +42,8 @@ def close(got, ref):
     assert np.linalg.norm(got - ref) <= 5e-3 * np.linalg.norm(ref)
 
 
-SHAPES = [(1, 64, 1), (5, 64, 37), (130, 128, 1000), (257, 200, 4097), (64, 1024, 513), (256, 512, 4096)]
+SHAPES = [(1, 64, 1), (5, 64, 37), (130, 128, 1000), (257, 200, 4097), (64, 1024, 513), (256, 512, 4096),
+          (70, 8, 300), (129, 16, 2049)]   # H = 8, 16: MN-major boxes mostly past the edge (zero fill)
 
 
 @pytest.mark.parametrize("T,H,V", SHAPES)
