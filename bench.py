@@ -88,7 +88,7 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="time every configuration of the workload table (one JSON line each)")
     ap.add_argument("--case", choices=["ce", "sbv", "flce", "fljsd", "ce_fb", "sbv_fb", "flce_fb", "fljsd_fb", "cpo",
-                                       "cpo_fb"],
+                                       "cpo_fb", "cublas"],
                     help="time one op alone at --T/--V/--H (profiling runs); prints one JSON line")
     ap.add_argument("--T", type=int, default=None, help="tokens (ce: rows; sbv: seq, batch 4)")
     ap.add_argument("--V", type=int, default=None)
@@ -499,8 +499,30 @@ def time_oracle(s):
                         "fljsd": round(t_js, 2)}}
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(h=None, budget_s=12.0, seed=0):
-    return time_oracle(oracle_samples(seed, h, budget_s))
+    r = time_oracle(oracle_samples(seed, h, budget_s))
+    r["cpu_model"] = cpu_model()
+    return r
 
 
 def run_reference(args):
@@ -519,7 +541,7 @@ def run_reference(args):
             "data": "synthetic (seeded Philox generator)",
             "config": {"workload": WORKLOAD, "l2": "n/a (host)", "parallelism": "host threads"},
             "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": r["cores"], "kind": "oracle",
-                             "sample": r["sample"]},
+                             "sample": r["sample"], "cpu_model": cpu_model()},
             "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
@@ -573,6 +595,14 @@ def run_case(args):
         dz = torch.empty_like(z)
         fn = lambda: lmho.ce_fwd_bwd_sbv_bf16(z, t, dlogits=dz)  # noqa: E731
         work, unit = rl.ce_sbv_fwd_bwd_bytes(S, 4, V), "GB/s"
+    elif c == "cublas":
+        # practical ceiling of the fused configs: a library bf16 GEMM of the same
+        # shape, logits = x W^T written to memory (run only, timed like the rest)
+        T, V = args.T or FLCE["T"], args.V or FLCE["V"]
+        x, W = bf16(args.seed, 0, (T, H), 1.0), bf16(args.seed, 2, (V, H), 0.02)
+        logits = torch.empty((T, V), dtype=torch.bfloat16, device="cuda")
+        fn = lambda: torch.matmul(x, W.t(), out=logits)  # noqa: E731
+        work, unit = rl.flce_flops(T, H, V), "TFLOP/s"
     elif c == "flce":
         T, V = args.T or FLCE["T"], args.V or FLCE["V"]
         x, W, t = bf16(args.seed, 0, (T, H), 1.0), bf16(args.seed, 2, (V, H), 0.02), targets((T,), V)
@@ -630,7 +660,7 @@ def run_case(args):
     # whose write-back the timed kernel would pay for.
     flush = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
     nk = {"ce": 1, "sbv": 1, "flce": 2, "fljsd": 4, "ce_fb": 1, "sbv_fb": 1, "flce_fb": 4, "fljsd_fb": 4, "cpo": 2,
-          "cpo_fb": 4}[c]
+          "cpo_fb": 4, "cublas": 1}[c]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     for row in evs:
         for e in row:
@@ -640,6 +670,11 @@ def run_case(args):
         flush.sum()
         # events recorded by the library itself around its own launches: no
         # host-side gap between the start event and the first kernel
+        if c == "cublas":      # not a library call: bracket it here
+            evs[i][0].record()
+            fn()
+            evs[i][1].record()
+            continue
         lmho.set_launch_events(evs[i])
         fn()
         lmho.set_launch_events(None)
@@ -650,6 +685,8 @@ def run_case(args):
     rate = work / (med * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
     return {"case": c, "T": args.T, "V": args.V, "H": H, "ce_variant": args.ce_variant, "raster_group": args.raster_group, "l2": "flushed (512 MB read) before each call",
             "us_median": round(med * 1e3, 2),
+            "us_p10": round(float(np.percentile(ms, 10)) * 1e3, 2),
+            "us_p90": round(float(np.percentile(ms, 90)) * 1e3, 2),
             "us_all": [round(m * 1e3, 2) for m in ms],
             "kernels_us_median": [round(float(np.median([k[j] for k in kernel_ms])) * 1e3, 2) for j in range(nk)],
             unit: round(rate, 1)}
@@ -664,7 +701,8 @@ SWEEP = ([("ce", 16384, V) for V in (4096, 8192, 16384, 32768, 65536, 131072)] +
          [("cpo", 1024 * b, 128256) for b in (2, 4, 8, 16)] +
          [("cpo_fb", 1024 * b, 128256) for b in (2, 16)] +
          [("fljsd_fb", T, 128256) for T in (1024, 8192)] +
-         [("fljsd", T, 128256) for T in (1024, 2048, 4096, 8192)])
+         [("fljsd", T, 128256) for T in (1024, 2048, 4096, 8192)] +
+         [("cublas", 1024 * b, 128256) for b in (2, 16)])
 
 
 def run_sweep(args):
@@ -675,8 +713,9 @@ def run_sweep(args):
     for case, T, V in SWEEP:
         a = argparse.Namespace(**vars(args))
         a.case, a.T, a.V = case, T, V
-        a.steps = max(args.steps, 3) if case in ("ce", "sbv", "ce_fb", "sbv_fb") else (2 if case in ("flce_fb", "fljsd_fb") else 3)
-        a.warmup = max(1, min(args.warmup, 2))
+        # 5 warm-ups; 50 timed calls for the microsecond CE calls, 20 for the fused ones
+        a.steps = 50 if case in ("ce", "sbv", "ce_fb", "sbv_fb") else 20
+        a.warmup = 5
         r = run_case(a)
         if "GB/s" in r:
             r["frac_of_measured_hbm"] = round(r["GB/s"] / pk["hbm"], 4)
