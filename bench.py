@@ -46,18 +46,18 @@ KERNELS_PER_STEP = 1 + 1 + 2 + 4
 
 # DRAM bytes (read + write) per launch of each main kernel at the bench sizes,
 # from one ncu capture of a bench step (`ncu --metrics dram__bytes_read.sum,
-# dram__bytes_write.sum,gpu__time_duration.sum` over `bench.py --steps 1
-# --warmup 0 --no-e2e --no-cpu-baseline`; summary in
+# dram__bytes_write.sum,gpu__time_duration.sum` over `bench.py --steps 2
+# --warmup 1 --no-e2e --no-cpu-baseline`, mean of the 3 launches; summary in
 # profiles/dram_traffic_bench_step.md).  They hold only for the kernel sources
 # they were taken from: a changed source makes the bench report null.
 KERNEL_SOURCES = ("fused_linear.cu", "ce_rows.cu", "rowstats.cuh", "ptx.cuh", "lmho_internal.h")
-TRAFFIC_SOURCE_DIGEST = "cfd6a50431b8eca7"
+TRAFFIC_SOURCE_DIGEST = "1b1402b1b5ac24c3"
 TRAFFIC_BYTES = {
-    "ce_fwd_f32.row_kernel": 8590167040 + 3181568,
-    "ce_fwd_sbv_bf16.row_kernel": 2147609856 + 90624,
-    "flce.tcgen05_gemm_ce": 4339088128 + 65787136,
-    "fljsd.tcgen05_gemm_lse": 4338142464 + 65369600,
-    "fljsd.tcgen05_gemm_jsd": 10619322368 + 32736000,
+    "ce_fwd_f32.row_kernel": 8590346069 + 367189,
+    "ce_fwd_sbv_bf16.row_kernel": 2147636480 + 348928,
+    "flce.tcgen05_gemm_ce": 4341600427 + 66002005,
+    "fljsd.tcgen05_gemm_lse": 4339802368 + 65318400,
+    "fljsd.tcgen05_gemm_jsd": 10197501611 + 33213952,
 }
 
 

@@ -315,8 +315,9 @@ int lmho_ws_status(void* ws, size_t ws_bytes, void* stream);
 int lmho_set_ce_variant(int variant);
 
 /* Raster of the fused-linear tensor-core passes, process-wide: work units
- * (token tile x vocab tile) are ordered in groups of `group_m` token tiles,
- * vocab tiles outer within a group, so the CTAs running at one time share W
+ * (token tile x vocab tile) are ordered in groups of `group_m` token tiles
+ * of 128 (a paired pass's 256-row tiles count as two), vocab tiles outer
+ * within a group, so the CTAs running at one time share W
  * tiles in L2; W streams from HBM about ceil(T/128/group_m) times per head
  * and pass.  0 = automatic: 32 for single-head passes, 16 for the two-head
  * JSD passes (both heads' tiles share L2) and for the gradient products;

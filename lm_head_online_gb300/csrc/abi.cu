@@ -178,14 +178,31 @@ int tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t H, uint32_
 // bf16 matrix [k_rows, mn] (row-major, MN contiguous, row stride ld >= mn
 // elements, ld * 2 a multiple of 16) read MN-major: box = 64 (MN) x 64 (K),
 // 128-byte swizzle; reads past either edge are zero-filled.
-int tmap_bf16_mn(CUtensorMap* m, const void* base, int64_t k_rows, int64_t mn, int64_t ld) {
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(mn), static_cast<cuuint64_t>(k_rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBK)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+// `tile_mn` = the MN extent of the operand's tile (a multiple of kMnChunk).
+// With mn_chunked(mn) the map is 3-D: (64 contiguous elements, K rows at ld,
+// chunks 128 bytes apart), box (64, kBK, tile_mn / 64); the chunks land
+// kBK * 128 bytes apart in shared memory, as separate 2-D boxes would.  Every
+// chunk index below mn / 64 addresses only elements below mn.
+int tmap_bf16_mn(CUtensorMap* m, const void* base, int64_t k_rows, int64_t mn, int64_t ld, int tile_mn) {
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r;
+  if (mn_chunked(mn)) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kMnChunk), static_cast<cuuint64_t>(k_rows),
+                          static_cast<cuuint64_t>(mn / kMnChunk)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(kMnChunk) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kMnChunk), static_cast<cuuint32_t>(kBK),
+                         static_cast<cuuint32_t>(tile_mn / kMnChunk)};
+    r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(mn), static_cast<cuuint64_t>(k_rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kMnChunk), static_cast<cuuint32_t>(kBK)};
+    r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? LMHO_OK : LMHO_ERR_CUDA;
 }
 
@@ -485,7 +502,7 @@ int flce_fwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* target, i
   if (int d = current_device(&sms)) return d;
   if (int e = get_encode()) return e;
   CUtensorMap tx, tw;
-  if (tmap_bf16(&tx, x, T, H, kBM) || tmap_bf16(&tw, W, V, H, kBN_CE)) return LMHO_ERR_CUDA;
+  if (tmap_bf16(&tx, x, T, H, kBM) || tmap_bf16(&tw, W, V, H, kBoxBFwd)) return LMHO_ERR_CUDA;
   const FusedGeometry g = geometry(T, H, V, kBN_CE);
   const FusedWs w = flce_ws_carve(ws, ws_bytes, T, V);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
@@ -515,9 +532,9 @@ int flce_fwd_bwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* targe
   const FusedWs w = flce_ws_carve(ws, ws_bytes, T, V);
   const FlceBwdWs bw = flce_bwd_ws_carve(ws, T, H, V);
   FlceBwdMaps m;
-  if (tmap_bf16(&m.x, x, T, H, kBM) || tmap_bf16(&m.w, W, V, H, kBN_CE) ||
-      tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) || tmap_bf16_mn(&m.w_mn, W, V, H, H) ||
-      tmap_bf16_mn(&m.dz_mn, bw.dz, T, V, bw.ld_dz) || tmap_bf16_mn(&m.x_mn, x, T, H, H))
+  if (tmap_bf16(&m.x, x, T, H, kBM) || tmap_bf16(&m.w, W, V, H, kBoxBFwd) ||
+      tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) || tmap_bf16_mn(&m.w_mn, W, V, H, H, kBoxBGrad) ||
+      tmap_bf16_mn(&m.dz_mn, bw.dz, T, V, bw.ld_dz, kBM) || tmap_bf16_mn(&m.x_mn, x, T, H, H, kBoxBGrad))
     return LMHO_ERR_CUDA;
   const FusedGeometry g = geometry(T, H, V, kBN_CE);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
@@ -547,8 +564,8 @@ int fljsd_impl(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, const
   if (int d = current_device(&sms)) return d;
   if (int e = get_encode()) return e;
   CUtensorMap txs, txt, tws256, twt256, twsj, twtj;
-  if (tmap_bf16(&txs, xs, T, H, kBM) || tmap_bf16(&txt, xt, T, H, kBM) || tmap_bf16(&tws256, Ws, V, H, kBN_CE) ||
-      tmap_bf16(&twt256, Wt, V, H, kBN_CE) || tmap_bf16(&twsj, Ws, V, H, kBN_JSD) ||
+  if (tmap_bf16(&txs, xs, T, H, kBM) || tmap_bf16(&txt, xt, T, H, kBM) || tmap_bf16(&tws256, Ws, V, H, kBoxBFwd) ||
+      tmap_bf16(&twt256, Wt, V, H, kBoxBFwd) || tmap_bf16(&twsj, Ws, V, H, kBN_JSD) ||
       tmap_bf16(&twtj, Wt, V, H, kBN_JSD))
     return LMHO_ERR_CUDA;
   const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD, kGroupTwoHead);
@@ -598,11 +615,11 @@ int fljsd_fwd_bwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* x
   const FlceBwdWs bw = bwd_carve(ws, lay);
   float* inv_count = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.end - kAlign);
   FljsdBwdMaps m;
-  if (tmap_bf16(&m.xs, xs, T, H, kBM) || tmap_bf16(&m.xt, xt, T, H, kBM) || tmap_bf16(&m.ws256, Ws, V, H, kBN_CE) ||
-      tmap_bf16(&m.wt256, Wt, V, H, kBN_CE) || tmap_bf16(&m.wsj, Ws, V, H, kBN_JSD) ||
+  if (tmap_bf16(&m.xs, xs, T, H, kBM) || tmap_bf16(&m.xt, xt, T, H, kBM) || tmap_bf16(&m.ws256, Ws, V, H, kBoxBFwd) ||
+      tmap_bf16(&m.wt256, Wt, V, H, kBoxBFwd) || tmap_bf16(&m.wsj, Ws, V, H, kBN_JSD) ||
       tmap_bf16(&m.wtj, Wt, V, H, kBN_JSD) || tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) ||
-      tmap_bf16_mn(&m.ws_mn, Ws, V, H, H) || tmap_bf16_mn(&m.dz_mn, bw.dz, T, V, bw.ld_dz) ||
-      tmap_bf16_mn(&m.xs_mn, xs, T, H, H))
+      tmap_bf16_mn(&m.ws_mn, Ws, V, H, H, kBoxBGrad) || tmap_bf16_mn(&m.dz_mn, bw.dz, T, V, bw.ld_dz, kBM) ||
+      tmap_bf16_mn(&m.xs_mn, xs, T, H, H, kBoxBGrad))
     return LMHO_ERR_CUDA;
   const FusedGeometry g1 = geometry(T, H, V, kBN_CE), g2 = geometry(T, H, V, kBN_JSD, kGroupTwoHead);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
@@ -647,7 +664,7 @@ int flce_cpo_fwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* targe
   if (int d = current_device(&sms)) return d;
   if (int e = get_encode()) return e;
   CUtensorMap tx, tw;
-  if (tmap_bf16(&tx, x, T, H, kBM) || tmap_bf16(&tw, W, V, H, kBN_CE)) return LMHO_ERR_CUDA;
+  if (tmap_bf16(&tx, x, T, H, kBM) || tmap_bf16(&tw, W, V, H, kBoxBFwd)) return LMHO_ERR_CUDA;
   const FusedGeometry g = geometry(T, H, V, kBN_CE);
   const FusedWs w = flce_ws_carve(ws, ws_bytes, T, V);
   char* base = static_cast<char*>(ws);
@@ -683,9 +700,9 @@ int flce_cpo_fwd_bwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* t
   CpoArgs c{B, S, beta, alpha, reinterpret_cast<float*>(base + cl.off_lp), reinterpret_cast<float*>(base + cl.off_sig),
             reinterpret_cast<float*>(base + cl.off_mean), logps, reinterpret_cast<float*>(base + lay.end - kAlign)};
   FlceBwdMaps m;
-  if (tmap_bf16(&m.x, x, T, H, kBM) || tmap_bf16(&m.w, W, V, H, kBN_CE) ||
-      tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) || tmap_bf16_mn(&m.w_mn, W, V, H, H) ||
-      tmap_bf16_mn(&m.dz_mn, bw.dz, T, V, bw.ld_dz) || tmap_bf16_mn(&m.x_mn, x, T, H, H))
+  if (tmap_bf16(&m.x, x, T, H, kBM) || tmap_bf16(&m.w, W, V, H, kBoxBFwd) ||
+      tmap_bf16_ld(&m.dz, bw.dz, T, V, bw.ld_dz, kBM) || tmap_bf16_mn(&m.w_mn, W, V, H, H, kBoxBGrad) ||
+      tmap_bf16_mn(&m.dz_mn, bw.dz, T, V, bw.ld_dz, kBM) || tmap_bf16_mn(&m.x_mn, x, T, H, H, kBoxBGrad))
     return LMHO_ERR_CUDA;
   const FusedGeometry g = geometry(T, H, V, kBN_CE);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};

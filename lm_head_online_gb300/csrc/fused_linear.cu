@@ -9,20 +9,28 @@
 // batchmean).
 //
 // One persistent kernel per pass, one CTA per SM, warp-specialised:
-//   warp 0      TMA producer: bf16 tiles of A [128 x 64] and B [BN x 64]
-//               (128-byte swizzle; K-major, or MN-major boxes of 64 x 64 for
-//               the gradient products) into a ring of shared-memory stages
+//   warp 0      TMA producer: bf16 tiles of A [128 x 64] and B [rows x 64]
+//               (128-byte swizzle; K-major, or MN-major 64 x 64 boxes for the
+//               gradient products, one 3-D copy per tile where the MN extent is
+//               whole 64-element chunks) into a ring of shared-memory stages
 //               (mbarrier complete_tx);
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
-//               (M=128, N=BN, K=16, bf16 x bf16 -> fp32) and frees stages with
+//               (K=16, bf16 x bf16 -> fp32) and frees stages with
 //               tcgen05.commit;
 //   warps 2..   epilogue (4 warps, 8 for the two-head passes): each thread owns
 //               one token row (one TMEM lane) and reads its accumulator row with
 //               tcgen05.ld.
-// Single-head passes double-buffer two 256-column accumulators, so the epilogue
-// of one unit overlaps the MMAs of the next.  Two-head passes (BN = 256 per
-// head) fill TMEM with one unit; its heads complete and are released
-// separately, so the next unit's student MMAs overlap this unit's epilogue.
+// The gradient products (STORE) run on CTA pairs, clusters of 2 with tcgen05
+// cta_group::2: a unit is 256 rows x 256 columns, each CTA loads its 128 rows of
+// A and 128 of the 256 rows of B (a pair reads 2/3 of the operand bytes two lone
+// CTAs would), the even CTA issues M=256 N=256 MMAs for both, and each CTA's
+// TMEM holds its 128 rows of D.  The other single-head passes (CE, LSE, DZ) run
+// on lone CTAs, M=128 N=256 (which passes pair is a build-time choice).  Both
+// double-buffer two 256-column accumulators, so the epilogue of one unit
+// overlaps the MMAs of the next.  Two-head passes (JSD, JSDK, DZJ; BN = 256 per
+// head) run on lone CTAs: one unit fills TMEM, its heads complete and are
+// released separately, so the next unit's student MMAs overlap this unit's
+// epilogue.
 // Work unit = (token tile, vocab tile), rastered in groups of `group_m` token
 // tiles so a wave of CTAs shares the same W tiles in L2 and each W tile is
 // read from HBM about once per group.
@@ -70,7 +78,7 @@ template <int MODE>
 constexpr bool a_mn() { return MODE == kModeStoreT; }
 template <int MODE>
 constexpr bool b_mn() { return store_mode<MODE>(); }
-constexpr int kMnBox = 64;                      // MN extent of one 128-byte swizzle row of bf16
+constexpr int kMnBox = kMnChunk;                // MN extent of one 128-byte swizzle row of bf16
 constexpr int kMnBoxBytes = kMnBox * kBK * 2;   // one TMA box of an MN-major operand: 64 (MN) x 64 (K)
 
 constexpr int kTmemCols = 512;   // all of TMEM: accumulators of 256 or 512 fp32 columns
@@ -79,6 +87,11 @@ constexpr int kSmemBudget = 192 * 1024;
 template <int MODE>
 struct ModeCfg {
   static constexpr int BN = two_head<MODE>() ? kBN_JSD : kBN_CE;
+  // CTA pair (single-head passes): a unit is kRowsM = 2 kBM rows; this CTA loads
+  // kBM rows of A and kBRows = BN / 2 of B and holds kBM rows of the accumulator.
+  static constexpr bool kPair = two_head<MODE>() ? false : store_mode<MODE>() ? kPairGrad : kPairFwd;
+  static constexpr int kRowsM = kPair ? 2 * kBM : kBM;
+  static constexpr int kBRows = kPair ? BN / 2 : BN;
   static constexpr int kHeadsPerUnit = two_head<MODE>() ? 2 : 1;
   static constexpr int kAccCols = BN * kHeadsPerUnit;      // TMEM columns of one accumulator
   static constexpr int kNumAcc = kTmemCols / kAccCols;     // 2 = double-buffered, 1 = single
@@ -91,7 +104,7 @@ struct ModeCfg {
   static constexpr int kColSplit = kEpiWarps / 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;    // producer warp, MMA warp, epilogue
   static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = kSmemBudget / kStageBytes;
   // STORE epilogues stage each warp's 32 x 32 fp32 block (rows padded to 36
@@ -111,8 +124,10 @@ struct ModeCfg {
   // 0 = K-major, 1 = MN-major; N >> 3 in bits 17-22, M >> 4 in bits 24-28.
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (a_mn<MODE>() ? 1u << 15 : 0u) |
                                      (b_mn<MODE>() ? 1u << 16 : 0u) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                                     (static_cast<uint32_t>(kBM >> 4) << 24);
-  static_assert(kBM % kMnBox == 0 && BN % kMnBox == 0, "MN-major tiles are whole 64-wide boxes");
+                                     (static_cast<uint32_t>(kRowsM >> 4) << 24);
+  static_assert(kBM % kMnBox == 0 && kBRows % kMnBox == 0, "MN-major tiles are whole 64-wide boxes");
+  static_assert(two_head<MODE>() || kBRows == (store_mode<MODE>() ? kBoxBGrad : kBoxBFwd),
+                "B rows per CTA match the host's tensor-map boxes");
 };
 
 struct Params {
@@ -135,6 +150,7 @@ struct Params {
   int64_t split_stride;    // STORE: elements between K slices
   int32_t k_split;         // STORE: K slices (units = tiles x k_split)
   int32_t kb_per;          // STORE: k-blocks per slice (the last may be shorter, never empty)
+  uint32_t mn3d;           // STORE: bit 0 / bit 1 = the MN-major A / B map is 3-D (one copy per tile)
   const float* kl;         // DZJ: KL(P || M) of every row
   const uint8_t* keep;     // DZJ: token mask (null = all kept)
   const float* inv_count;  // DZJ: 1 / number of kept tokens (device scalar)
@@ -289,6 +305,13 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pair: rank 0 (the leader) issues the MMAs and owns the barriers both
+  // CTAs' copies complete on and both CTAs' epilogues release; the pair walks
+  // the units together (unit stride = number of pairs).
+  const uint32_t rank = C::kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int64_t first_unit = C::kPair ? (blockIdx.x >> 1) : blockIdx.x;
+  const int64_t unit_stride = C::kPair ? (gridDim.x >> 1) : gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -296,7 +319,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < C::kNumFree; ++b) mbar_init(&acc_full[b], 1);
-    for (int b = 0; b < C::kNumFree; ++b) mbar_init(&acc_empty[b], C::kEpiWarps * 32);
+    // pair: one arrival per epilogue warp of both CTAs; otherwise every epilogue thread
+    for (int b = 0; b < C::kNumFree; ++b) mbar_init(&acc_empty[b], C::kPair ? 2 * C::kEpiWarps : C::kEpiWarps * 32);
     mbar_init(drain, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_a0);
@@ -307,11 +331,19 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(s_tmem, kTmemCols);
-    tmem_relinquish();
+    if constexpr (C::kPair) {
+      tmem_alloc_pair(s_tmem, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(s_tmem, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (C::kPair)
+    cluster_sync();  // both CTAs' barriers initialised before any remote arrival or copy
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
 
@@ -322,7 +354,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       uint32_t phase = 0;
       uint32_t filled = 0, last_parity = 0;  // per-stage bit masks for the drain
       bool ok = true;
-      for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      for (int64_t u = first_unit; u < p.units && ok; u += unit_stride) {
         const UnitCoord c = decode_unit(p, u, MODE);
         const int kb_lo = store_mode<MODE>() ? c.head * p.kb_per : 0;
         const int kb_hi = store_mode<MODE>() ? min(p.k_blocks, kb_lo + p.kb_per) : p.k_blocks;
@@ -331,23 +363,68 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
           const CUtensorMap* ta = head ? &tm_a1 : &tm_a0;
           const CUtensorMap* tb = head ? &tm_b1 : &tm_b0;
           for (int kb = kb_lo; kb < kb_hi; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, p.status)) { ok = false; break; }
+            // pair: the leader's commits free the stage in both CTAs
+            const bool freed = C::kPair ? mbar_wait_cluster(&empty[stage], phase ^ 1u, p.timeout_ns, p.status)
+                                        : mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, p.status);
+            if (!freed) { ok = false; break; }
             uint8_t* sa = tiles + stage * C::kStageBytes;
             uint8_t* sb = sa + C::kABytes;
+            if constexpr (C::kPair) {
+              // both CTAs' copies complete on the leader's barrier, which expects them all
+              if (leader) mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+              const uint32_t fb = mapa_shared(&full[stage], 0);
+              const int32_t arow = c.mt * C::kRowsM + static_cast<int32_t>(rank) * kBM;   // this CTA's A rows
+              const int32_t brow = c.nt * BN + static_cast<int32_t>(rank) * C::kBRows;    // and B rows
+              if (a_mn<MODE>()) {
+                if (p.mn3d & 1u) {
+                  tma_load_3d_pair(sa, ta, 0, kb * kBK, arow / kMnBox, fb);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < kBM / kMnBox; ++j)
+                    tma_load_2d_pair(sa + j * kMnBoxBytes, ta, arow + j * kMnBox, kb * kBK, fb);
+                }
+              } else {
+                tma_load_2d_pair(sa, ta, kb * kBK, arow, fb);
+              }
+              if (b_mn<MODE>()) {
+                if (p.mn3d & 2u) {
+                  tma_load_3d_pair(sb, tb, 0, kb * kBK, brow / kMnBox, fb);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < C::kBRows / kMnBox; ++j)
+                    tma_load_2d_pair(sb + j * kMnBoxBytes, tb, brow + j * kMnBox, kb * kBK, fb);
+                }
+              } else {
+                tma_load_2d_pair(sb, tb, kb * kBK, brow, fb);
+              }
+              filled |= 1u << stage;
+              last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+              if (++stage == S) { stage = 0; phase ^= 1u; }
+              continue;
+            }
             mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
             // K-major operand: one box of 64 (K) x rows.  MN-major operand: boxes of
-            // 64 (MN) x 64 (K), one per 64 rows of the tile, kMnBoxBytes apart.
+            // 64 (MN) x 64 (K), one per 64 rows of the tile, kMnBoxBytes apart --
+            // as one 3-D copy when the map is 3-D, else one 2-D copy per box.
             if (a_mn<MODE>()) {
+              if (p.mn3d & 1u) {
+                tma_load_3d(sa, ta, 0, kb * kBK, c.mt * (kBM / kMnBox), &full[stage]);
+              } else {
 #pragma unroll
-              for (int j = 0; j < kBM / kMnBox; ++j)
-                tma_load_2d(sa + j * kMnBoxBytes, ta, c.mt * kBM + j * kMnBox, kb * kBK, &full[stage]);
+                for (int j = 0; j < kBM / kMnBox; ++j)
+                  tma_load_2d(sa + j * kMnBoxBytes, ta, c.mt * kBM + j * kMnBox, kb * kBK, &full[stage]);
+              }
             } else {
               tma_load_2d(sa, ta, kb * kBK, c.mt * kBM, &full[stage]);
             }
             if (b_mn<MODE>()) {
+              if (p.mn3d & 2u) {
+                tma_load_3d(sb, tb, 0, kb * kBK, c.nt * (BN / kMnBox), &full[stage]);
+              } else {
 #pragma unroll
-              for (int j = 0; j < BN / kMnBox; ++j)
-                tma_load_2d(sb + j * kMnBoxBytes, tb, c.nt * BN + j * kMnBox, kb * kBK, &full[stage]);
+                for (int j = 0; j < BN / kMnBox; ++j)
+                  tma_load_2d(sb + j * kMnBoxBytes, tb, c.nt * BN + j * kMnBox, kb * kBK, &full[stage]);
+              }
             } else {
               tma_load_2d(sb, tb, kb * kBK, c.nt * BN, &full[stage]);
             }
@@ -357,24 +434,34 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
           }
         }
       }
-      // Never leave with copies in flight: wait for the last fill of each stage.
+      // Never leave with copies in flight: wait for the last fill of each stage
+      // (pair: the leader's barriers count both CTAs' copies; the other CTA is
+      // held by the closing cluster barrier until the leader has waited).
       for (int s = 0; s < S; ++s)
-        if (filled & (1u << s)) mbar_wait(&full[s], (last_parity >> s) & 1u, p.timeout_ns, p.status);
+        if (filled & (1u << s)) {
+          if constexpr (C::kPair) {
+            if (leader) mbar_wait_cluster(&full[s], (last_parity >> s) & 1u, p.timeout_ns, p.status);
+          } else {
+            mbar_wait(&full[s], (last_parity >> s) & 1u, p.timeout_ns, p.status);
+          }
+        }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
       const uint32_t a0 = smem_u32(tiles);
-      for (int64_t u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      for (int64_t u = first_unit; u < p.units && ok; u += unit_stride) {
         const int kb_lo = store_mode<MODE>() ? decode_unit(p, u, MODE).head * p.kb_per : 0;
         const int kb_hi = store_mode<MODE>() ? min(p.k_blocks, kb_lo + p.kb_per) : p.k_blocks;
         if constexpr (!two_head<MODE>()) {
-          if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, p.status)) break;
+          const bool freed = C::kPair ? mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, p.status)
+                                      : mbar_wait(&acc_empty[acc], acc_phase ^ 1u, p.timeout_ns, p.status);
+          if (!freed) break;
           tc_fence_after();
         }
         for (int h = 0; h < C::kHeadsPerUnit && ok; ++h) {
@@ -384,7 +471,9 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
           }
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::kAccCols + h * BN);
           for (int kb = kb_lo; kb < kb_hi; ++kb) {
-            if (!mbar_wait(&full[stage], phase, p.timeout_ns, p.status)) { ok = false; break; }
+            const bool landed = C::kPair ? mbar_wait_cluster(&full[stage], phase, p.timeout_ns, p.status)
+                                         : mbar_wait(&full[stage], phase, p.timeout_ns, p.status);
+            if (!landed) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = a0 + stage * C::kStageBytes;
             // K step of 16: +32 bytes inside the swizzle row (K-major), +16 rows (MN-major)
@@ -392,21 +481,35 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
             const uint64_t db = b_mn<MODE>() ? smem_desc_sw128_mn(sa + C::kABytes) : smem_desc_sw128(sa + C::kABytes);
             constexpr uint64_t kStepA = a_mn<MODE>() ? (16 * 128) >> 4 : 32 >> 4;
             constexpr uint64_t kStepB = b_mn<MODE>() ? (16 * 128) >> 4 : 32 >> 4;
+            if constexpr (C::kPair) {
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              tc_mma_bf16(d_tmem, da + kStepA * k, db + kStepB * k, C::kIdesc, (kb != kb_lo || k != 0) ? 1u : 0u);
-            tc_commit(&empty[stage]);
+              for (int k = 0; k < kBK / 16; ++k)
+                tc_mma_bf16_pair(d_tmem, da + kStepA * k, db + kStepB * k, C::kIdesc,
+                                 (kb != kb_lo || k != 0) ? 1u : 0u);
+              tc_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
+            } else {
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k)
+                tc_mma_bf16(d_tmem, da + kStepA * k, db + kStepB * k, C::kIdesc, (kb != kb_lo || k != 0) ? 1u : 0u);
+              tc_commit(&empty[stage]);
+            }
             if (++stage == S) { stage = 0; phase ^= 1u; }
           }
           if constexpr (two_head<MODE>())
             if (ok) tc_commit(&acc_full[h]);  // this head's accumulator is complete
         }
         if (!ok) break;
-        if constexpr (!two_head<MODE>()) tc_commit(&acc_full[acc]);
+        if constexpr (C::kPair)
+          tc_commit_pair_mc(&acc_full[acc], 0x3);  // both CTAs' epilogues
+        else if constexpr (!two_head<MODE>())
+          tc_commit(&acc_full[acc]);
         if (++acc == C::kNumAcc) { acc = 0; acc_phase ^= 1u; }
       }
       // All MMAs issued by this thread complete before TMEM is released.
-      tc_commit(drain);
+      if constexpr (C::kPair)
+        tc_commit_pair_mc(drain, 0x1);
+      else
+        tc_commit(drain);
       mbar_wait(drain, 0, p.timeout_ns, p.status);
     }
   } else {
@@ -414,14 +517,14 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
     const int quad = warp & 3;                  // TMEM lane quadrant this warp may access
     const int half = (warp - 2) / 4;            // which column slice (kColSplit slices)
     constexpr int kCols = BN / C::kColSplit;    // columns of each head this warp reads
-    const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
     const float beta = p.beta, omb = 1.f - p.beta, it = p.inv_tau, it2 = p.inv_tau * kLog2e;
-    for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
+    for (int64_t u = first_unit; u < p.units; u += unit_stride) {
       const UnitCoord c = decode_unit(p, u, MODE);
-      const int64_t row = static_cast<int64_t>(c.mt) * kBM + row_in_tile;
+      const int64_t row0 = static_cast<int64_t>(c.mt) * C::kRowsM + rank * kBM + quad * 32;  // this warp's rows
+      const int64_t row = row0 + lane;
       const bool row_ok = row < p.T;
       const int64_t n0 = static_cast<int64_t>(c.nt) * BN + half * kCols;
       int64_t tgt = -1;
@@ -444,7 +547,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
         gj = kept ? p.gscale * __ldg(p.inv_count) * beta : 0.f;
       }
       // tcgen05.ld is warp-collective: the whole warp proceeds or gives up together
-      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[acc], acc_phase, p.timeout_ns, p.status));
+      const bool ok = __all_sync(0xFFFFFFFFu, C::kPair ? mbar_wait_cluster(&acc_full[acc], acc_phase, p.timeout_ns, p.status)
+                                                       : mbar_wait(&acc_full[acc], acc_phase, p.timeout_ns, p.status));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::kAccCols + half * kCols);
@@ -530,7 +634,6 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
                   make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
                              pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
             __syncwarp();
-            const int64_t row0 = static_cast<int64_t>(c.mt) * kBM + quad * 32;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int r = 8 * i + (lane >> 2), k = lane & 3;
@@ -551,7 +654,6 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
                   make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
             __syncwarp();
             const int c4 = (lane & 7) * 4;
-            const int64_t row0 = static_cast<int64_t>(c.mt) * kBM + quad * 32;
             float* obase = p.out + c.head * p.split_stride + col0 + c4;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -595,7 +697,11 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
         }
       }
       // accumulator fully read: hand it back to the MMA warp (two-head: done per head by the walk)
-      if constexpr (!two_head<MODE>()) {
+      if constexpr (C::kPair) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(&acc_empty[acc], 0));
+      } else if constexpr (!two_head<MODE>()) {
         tc_fence_before();
         mbar_arrive(&acc_empty[acc]);
       }
@@ -617,11 +723,17 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (C::kPair)
+    cluster_sync();  // neither CTA leaves while the pair's MMAs, copies or arrivals may touch it
+  else
+    __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (C::kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -823,18 +935,57 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUte
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int64_t grid = p.units < L.num_sms ? p.units : L.num_sms;
-  fused_gemm_kernel<MODE><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, L.stream>>>(a0, b0, a1, b1, p);
-  return cudaGetLastError();
+  if constexpr (C::kPair) {
+    // clusters of 2 CTAs (one per SM): as many pairs as can be resident at once
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = L.stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    static int pairs_max[64] = {};
+    int cap = L.num_sms / 2;
+    if (dev < 64) {
+      if (pairs_max[dev] == 0) {
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * (L.num_sms / 2)));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, fused_gemm_kernel<MODE>, &cfg) != cudaSuccess || n <= 0) {
+          (void)cudaGetLastError();
+          n = L.num_sms / 2;
+        }
+        pairs_max[dev] = n < L.num_sms / 2 ? n : L.num_sms / 2;
+      }
+      cap = pairs_max[dev];
+    }
+    const int64_t pairs = p.units < cap ? p.units : cap;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    return cudaLaunchKernelEx(&cfg, fused_gemm_kernel<MODE>, a0, b0, a1, b1, p);
+  } else {
+    const int64_t grid = p.units < L.num_sms ? p.units : L.num_sms;
+    fused_gemm_kernel<MODE><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, L.stream>>>(a0, b0, a1, b1,
+                                                                                                   p);
+    return cudaGetLastError();
+  }
 }
 
+// Tile grid of a MODE's units: token tiles of ModeCfg<MODE>::kRowsM rows (a
+// pair's tile is two of the geometry's kBM-row tiles), and a raster group
+// spanning the same tokens as the geometry's.
+template <int MODE>
 Params base_params(const FusedGeometry& g, const FusedLaunch& L, Ctrl* ctrl) {
+  constexpr int rows = ModeCfg<MODE>::kRowsM;
   Params p{};
   p.T = g.T;
   p.V = g.V;
-  p.num_m = static_cast<int32_t>(g.num_m);
+  p.num_m = static_cast<int32_t>((g.T + rows - 1) / rows);
   p.num_n = static_cast<int32_t>(g.num_n);
-  p.group_m = g.group_m;
+  const int gm = static_cast<int>(static_cast<int64_t>(g.group_m) * kBM / rows);
+  p.group_m = gm > 1 ? (gm < p.num_m ? gm : p.num_m) : 1;
   p.k_blocks = static_cast<int32_t>((g.H + kBK - 1) / kBK);
   p.timeout_ns = L.timeout_ns;
   p.status = &ctrl->status;
@@ -846,8 +997,8 @@ Params base_params(const FusedGeometry& g, const FusedLaunch& L, Ctrl* ctrl) {
 
 cudaError_t launch_flce(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const int64_t* target,
                         const FusedGeometry& g, float* loss, const FusedWs& ws, const FusedLaunch& L) {
-  Params p = base_params(g, L, ws.ctrl);
-  p.units = g.num_m * g.num_n;
+  Params p = base_params<kModeCE>(g, L, ws.ctrl);
+  p.units = static_cast<int64_t>(p.num_m) * p.num_n;
   p.target = target;
   p.part0 = ws.part0;
   p.part1 = ws.part1;
@@ -869,8 +1020,8 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, 
                          const FusedGeometry& g_lse, const FusedGeometry& g_jsd, float beta, float inv_tau,
                          const uint8_t* keep, float* loss, const FusedWs& ws, const FusedLaunch& L) {
   // pass 1: log-sum-exp of both heads
-  Params p = base_params(g_lse, L, ws.ctrl);
-  p.units = 2 * g_lse.num_m * g_lse.num_n;
+  Params p = base_params<kModeLSE>(g_lse, L, ws.ctrl);
+  p.units = 2 * static_cast<int64_t>(p.num_m) * p.num_n;
   p.part0 = ws.part0;
   p.part1 = ws.part1;
   p.inv_tau = inv_tau;
@@ -885,8 +1036,8 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, 
   if (e != cudaSuccess) return e;
   launch_mark(2, L.stream);
   // pass 2: recompute both heads' tiles, accumulate the divergence
-  Params q = base_params(g_jsd, L, ws.ctrl);
-  q.units = g_jsd.num_m * g_jsd.num_n;
+  Params q = base_params<kModeJSD>(g_jsd, L, ws.ctrl);
+  q.units = static_cast<int64_t>(q.num_m) * q.num_n;
   q.part0 = ws.part0;
   q.lse = ws.lse;
   q.beta = beta;
@@ -905,8 +1056,8 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, 
 cudaError_t launch_flce_cpo(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const int64_t* target,
                             const FusedGeometry& g, float* loss, const FusedWs& ws, const CpoArgs& c,
                             const FusedLaunch& L) {
-  Params p = base_params(g, L, ws.ctrl);
-  p.units = g.num_m * g.num_n;
+  Params p = base_params<kModeCE>(g, L, ws.ctrl);
+  p.units = static_cast<int64_t>(p.num_m) * p.num_n;
   p.target = target;
   p.part0 = ws.part0;
   p.part1 = ws.part1;
@@ -964,9 +1115,11 @@ cudaError_t launch_store_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_
   g.num_m = (M + kBM - 1) / kBM;
   g.num_n = (N + kBN_CE - 1) / kBN_CE;
   g.group_m = static_cast<int>(g.num_m < group_m ? g.num_m : group_m);
-  Params p = base_params(g, L, ctrl);
-  const int64_t tiles = g.num_m * g.num_n;
-  int splits = split_ws ? choose_k_split(tiles, p.k_blocks, L.num_sms) : 1;
+  Params p = base_params<MODE>(g, L, ctrl);
+  const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+  // a pair's tile occupies two SMs: plan the split in one-SM tile slots
+  const int64_t slots = ModeCfg<MODE>::kPair ? 2 * tiles : tiles;
+  int splits = split_ws ? choose_k_split(slots, p.k_blocks, L.num_sms) : 1;
   p.kb_per = (p.k_blocks + splits - 1) / splits;
   splits = (p.k_blocks + p.kb_per - 1) / p.kb_per;  // no empty slice
   p.k_split = splits;
@@ -974,6 +1127,8 @@ cudaError_t launch_store_gemm(const CUtensorMap& a, const CUtensorMap& b, int64_
   p.out = splits > 1 ? split_ws : out;
   p.ld_out = N;
   p.split_stride = M * N;
+  // the MN-major maps were made 3-D exactly when their MN extent is whole chunks
+  p.mn3d = (a_mn<MODE>() && mn_chunked(M) ? 1u : 0u) | (b_mn<MODE>() && mn_chunked(N) ? 2u : 0u);
   cudaError_t e = launch_gemm<MODE>(a, b, a, b, p, L);
   if (e != cudaSuccess || splits == 1) return e;
   const int64_t n4 = M * N / 4;
@@ -990,8 +1145,8 @@ cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const int64_t* target, con
   cudaError_t e;
   launch_mark(0, L.stream);
   // forward: per-token loss, mean, and each row's log-sum-exp
-  Params p = base_params(g, L, ws.ctrl);
-  p.units = g.num_m * g.num_n;
+  Params p = base_params<kModeCE>(g, L, ws.ctrl);
+  p.units = static_cast<int64_t>(p.num_m) * p.num_n;
   p.target = target;
   p.part0 = ws.part0;
   p.part1 = ws.part1;
@@ -1009,8 +1164,8 @@ cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const int64_t* target, con
   }
   launch_mark(1, L.stream);
   // recompute the logit tiles, write dZ
-  Params q = base_params(g, L, ws.ctrl);
-  q.units = g.num_m * g.num_n;
+  Params q = base_params<kModeDZ>(g, L, ws.ctrl);
+  q.units = static_cast<int64_t>(q.num_m) * q.num_n;
   q.target = target;
   q.lse = bw.lse;
   q.gscale = cpo ? grad_scale : grad_scale / static_cast<float>(g.T);
@@ -1040,8 +1195,8 @@ cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const FusedGeometry& g_l
   const int64_t T = g_lse.T, H = g_lse.H, V = g_lse.V;
   launch_mark(0, L.stream);
   // pass 1: log-sum-exp of both heads
-  Params p = base_params(g_lse, L, ws.ctrl);
-  p.units = 2 * g_lse.num_m * g_lse.num_n;
+  Params p = base_params<kModeLSE>(g_lse, L, ws.ctrl);
+  p.units = 2 * static_cast<int64_t>(p.num_m) * p.num_n;
   p.part0 = ws.part0;
   p.part1 = ws.part1;
   p.inv_tau = inv_tau;
@@ -1050,8 +1205,8 @@ cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const FusedGeometry& g_l
   lse_finalize<<<fb, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, ws.part1, T, static_cast<int>(g_lse.num_n), ws.lse);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // pass 2: divergence and KL(P || M) of every row
-  Params q = base_params(g_jsd, L, ws.ctrl);
-  q.units = g_jsd.num_m * g_jsd.num_n;
+  Params q = base_params<kModeJSDK>(g_jsd, L, ws.ctrl);
+  q.units = static_cast<int64_t>(q.num_m) * q.num_n;
   q.part0 = ws.part0;
   q.part1 = ws.part1;
   q.lse = ws.lse;
@@ -1065,8 +1220,8 @@ cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const FusedGeometry& g_l
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   launch_mark(1, L.stream);
   // pass 3: both heads again, the student's dZ
-  Params r = base_params(g_jsd, L, ws.ctrl);
-  r.units = g_jsd.num_m * g_jsd.num_n;
+  Params r = base_params<kModeDZJ>(g_jsd, L, ws.ctrl);
+  r.units = static_cast<int64_t>(r.num_m) * r.num_n;
   r.lse = ws.lse;
   r.beta = beta;
   r.inv_tau = inv_tau;

@@ -51,6 +51,33 @@ constexpr int kBN_CE = 256;     // vocab columns per tile, single-head passes
 #endif
 constexpr int kBN_JSD = LMHO_JSD_BN;  // vocab columns per head per tile, two-head pass
 constexpr int kJsdColSplit = 2;       // two-head pass: epilogue warps per TMEM lane quadrant
+// CTA pairs (tcgen05 cta_group::2): a unit is a tile of 2 x kBM rows by kBN_CE
+// columns, each CTA of the pair loading its kBM rows of A and half of B
+// (kBN_CE / 2 rows of the N extent) and holding its kBM rows of the
+// accumulator.  The gradient products (dx = dZ W, dW = dZ^T x) run on pairs:
+// their MN-major operands are feed-bound on a lone CTA, and the pair halves
+// each SM's operand bytes (dW 11 %, dx 7 % faster alone; 5-6 % in 40 ms
+// power-capped calls).  The CE, log-sum-exp and dZ passes run on lone CTAs
+// (M = 128): paired they are ~5 % faster in short calls but 3-5 % slower
+// under the power cap, where they spend most of their time.  LMHO_PAIR_FWD /
+// LMHO_PAIR_GRAD (0 or 1) choose at build time; kBoxBFwd / kBoxBGrad are the
+// B rows one CTA loads (the host's tensor-map boxes).
+#ifndef LMHO_PAIR_FWD
+#define LMHO_PAIR_FWD 0
+#endif
+#ifndef LMHO_PAIR_GRAD
+#define LMHO_PAIR_GRAD 1
+#endif
+constexpr bool kPairFwd = LMHO_PAIR_FWD != 0;    // CE, log-sum-exp, dZ passes
+constexpr bool kPairGrad = LMHO_PAIR_GRAD != 0;  // dx, dW
+constexpr int kBoxBFwd = kPairFwd ? kBN_CE / 2 : kBN_CE;
+constexpr int kBoxBGrad = kPairGrad ? kBN_CE / 2 : kBN_CE;
+// MN-major operands move in 128-byte rows of 64 bf16 ("chunks").  When the MN
+// extent is a whole number of chunks the tensor map is 3-D (64 elements, K rows,
+// chunks) and one TMA copy fills a whole tile's operand; otherwise it is 2-D and
+// a tile takes one copy per chunk, the map's edge zero-filling the ragged one.
+constexpr int kMnChunk = 64;
+inline bool mn_chunked(int64_t mn) { return mn % kMnChunk == 0; }
 
 struct FusedGeometry {
   int64_t T, H, V;
@@ -116,8 +143,8 @@ struct FlceBwdWs {
   int64_t ld_dz;
 };
 // Split-K of the gradient products dx = dZ W and dW = dZ^T x: only below
-// kSplitTiles output tiles of 128 x 256, into at most kMaxKSplit slices of at
-// least kMinSplitKBlocks k-blocks each.
+// kSplitTiles output tiles of 128 x 256 (a pair's 256-row tile counts as two),
+// into at most kMaxKSplit slices of at least kMinSplitKBlocks k-blocks each.
 constexpr int64_t kSplitTiles = 4 * 152;
 constexpr int kMaxKSplit = 8;
 constexpr int kMinSplitKBlocks = 16;
