@@ -74,6 +74,52 @@ def test_flat_unaligned_rows(gpu_lib, variant):
     assert float(loss.item()) == pytest.approx(m_ref, rel=RTOL_F32)
 
 
+EDGE_VARIANTS = ["warp", "cta", "cluster4", "bulk"]
+
+
+def edge_targets(V):
+    # first and last elements, the scalar head and tail of an unaligned row,
+    # both sides of 16-byte vector boundaries, the middle; then out of range
+    pos = [0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 15, 16, 17, V // 2, V - 17, V - 16, V - 9, V - 8, V - 7, V - 5, V - 4,
+           V - 3, V - 2, V - 1]
+    return np.array(pos + pos[::-1] + [-1, V], np.int64)
+
+
+@pytest.mark.parametrize("variant", EDGE_VARIANTS)
+def test_flat_targets_at_row_edges(gpu_lib, variant):
+    """The target logit is found wherever it sits in the row: in the scalar
+    head or tail around the 16-byte vector body, on a vector boundary, first
+    or last; an out-of-range target gives NaN for its row only."""
+    gpu_lib.set_ce_variant(variant)
+    V = 1001
+    t = edge_targets(V)
+    T = len(t)
+    z = gen.normal_f32(12, 0, (T * V + 1,), sigma=3.0)
+    zd = to_dev(z)[1:].view(T, V)      # 4 bytes past a 16-byte boundary
+    ws = gpu_lib.workspace(gpu_lib.ce_workspace_bytes(T, V))
+    gpu_lib.ce_fwd_f32(zd, to_dev(t), ws=ws)
+    rows = gpu_lib.row_losses(ws, T).cpu().numpy().astype(np.float64)
+    ok = (t >= 0) & (t < V)
+    _, rows_ref = oracle.ce_f32(z[1:].reshape(T, V)[ok], t[ok])
+    np.testing.assert_allclose(rows[ok], rows_ref, rtol=RTOL_F32, atol=ATOL_F32)
+    assert np.all(np.isnan(rows[~ok]))
+
+
+@pytest.mark.parametrize("variant", EDGE_VARIANTS)
+def test_sbv_targets_at_row_edges(gpu_lib, variant):
+    # odd V: consecutive bf16 rows start at every 2-byte offset of a 16-byte vector
+    gpu_lib.set_ce_variant(variant)
+    V = 1001
+    t = edge_targets(V)
+    S = len(t) // 2
+    z = gen.normal_bf16_bits(13, 0, (S, 2, V), sigma=3.0)
+    got = run_sbv(gpu_lib, z, t.reshape(S, 2)).reshape(-1)
+    ok = (t >= 0) & (t < V)
+    want = oracle.ce_sbv_bf16(z.reshape(1, S * 2, V)[:, ok], t[ok].reshape(1, -1)).reshape(-1)
+    np.testing.assert_allclose(got[ok], want, rtol=0, atol=ATOL_BF16)
+    assert np.all(np.isnan(got[~ok]))
+
+
 def test_flat_equal_logits_and_shift(gpu_lib):
     T, V = 8, 5000
     z = np.full((T, V), 3.0, np.float32)
