@@ -101,9 +101,10 @@ __device__ __forceinline__ MS row_partial(const T* row, int64_t lo, int64_t hi, 
   return a;
 }
 
-// z[t] of a row, or NaN for a target outside [0, V).  The kernels load t
-// before the row and call this after it: a load of z[t] that waits for t up
-// front would hold back the row's own loads.
+// z[t] of a row, or NaN for a target outside [0, V).  The warp-per-row kernel
+// loads t before the row and calls this after it (a load of z[t] that waits
+// for t up front would hold back the warp's own row loads); the CTA and
+// cluster kernels call it up front from one thread while the others stream.
 template <typename T>
 __device__ __forceinline__ float target_value(const T* row, int64_t t, int64_t V) {
   return (t >= 0 && t < V) ? Elt<T>::load1(row + t) : __int_as_float(0x7FC00000);
@@ -142,11 +143,14 @@ __global__ void __launch_bounds__(NT) ce_cta_rows(const T* __restrict__ logits,
   __shared__ MS s_part[NT / 32];
   const int64_t r = blockIdx.x;
   const T* row = logits + r * V;
-  const int64_t t = threadIdx.x == 0 ? __ldg(target + r) : 0;
+  // One thread reads z[t] up front: the CTA's other warps stream meanwhile,
+  // and a read at the end would hold the whole CTA (measured 5 % slower for
+  // 256 KB bf16 rows).
+  float zt = 0.f;
+  if (threadIdx.x == 0) zt = target_value(row, __ldg(target + r), V);
   MS a = row_partial<T, U>(row, 0, V, threadIdx.x, NT);
   a = block_allreduce_to0<NT>(a, s_part);
-  if (threadIdx.x == 0)
-    out_rows[r] = finish_loss(a, target_value(row, t, V));
+  if (threadIdx.x == 0) out_rows[r] = finish_loss(a, zt);
   if (mean_out) mean_tail(out_rows, rows, mean_out, ctrl, gridDim.x);
 }
 
@@ -165,13 +169,11 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT)
   const int64_t chunk = ((V + C - 1) / C + 63) / 64 * 64;
   const int64_t lo = (chunk * rank < V) ? chunk * rank : V;
   const int64_t hi = (lo + chunk < V) ? lo + chunk : V;
-  const int64_t t = (rank == 0 && threadIdx.x == 0) ? __ldg(target + r) : 0;
+  float zt = 0.f;  // as in ce_cta_rows
+  if (rank == 0 && threadIdx.x == 0) zt = target_value(row, __ldg(target + r), V);
   MS a = row_partial<T, U>(row, lo, hi, threadIdx.x, NT);
   a = block_allreduce_to0<NT>(a, s_part);
   if (threadIdx.x == 0) { s_ms[0] = a.m; s_ms[1] = a.s; }
-  float zt = 0.f;  // issued before the barrier, used after it
-  if (rank == 0 && threadIdx.x == 0)
-    zt = target_value(row, t, V);
   cluster_sync();  // partials visible cluster-wide
   if (rank == 0 && threadIdx.x == 0) {
     MS tot{s_ms[0], s_ms[1]};
