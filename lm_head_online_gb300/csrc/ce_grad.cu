@@ -229,15 +229,9 @@ cudaError_t launch_fb(const T* logits, const int64_t* target, int64_t rows, int6
   const size_t smem = STAGED ? static_cast<size_t>(slice) * sizeof(T) + 16 : 0;
   auto kern = ce_fb_rows<T, C, NT, STAGED>;
   if (smem > 48 * 1024) {
-    static bool attr[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kSliceMaxBytes + 16));
-      if (e != cudaSuccess) return e;
-      attr[dev] = true;
-    }
+    static std::atomic<bool> limit_set[kMaxDevices];
+    const cudaError_t e = ensure_smem_limit(kern, static_cast<int>(kSliceMaxBytes + 16), limit_set);
+    if (e != cudaSuccess) return e;
   }
   kern<<<static_cast<unsigned>(rows * C), NT, smem, st>>>(logits, target, rows, V, slice, dloss, gscale, out_rows,
                                                           dlogits, mean_out, ctrl, timeout_ns);

@@ -315,15 +315,10 @@ cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, in
       nwa = nwa < 1 ? 1 : (nwa > 8 ? 8 : nwa);
       stages = stages / nwa * nwa;               // each stage owned by one warp
       const size_t smem = static_cast<size_t>(stages) * stage_bytes + 128 + 16 * stages;
-      static bool attr[64] = {};
-      int dev = 0;
-      cudaGetDevice(&dev);
-      if (dev < 64 && !attr[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(ce_bulk_rows<T, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kCeBulkRingBytes + 128 + 16 * 32));
-        if (e != cudaSuccess) return e;
-        attr[dev] = true;
-      }
+      static std::atomic<bool> limit_set[kMaxDevices];
+      const cudaError_t e =
+          ensure_smem_limit(ce_bulk_rows<T, 8>, static_cast<int>(kCeBulkRingBytes + 128 + 16 * 32), limit_set);
+      if (e != cudaSuccess) return e;
       int64_t grid = rows < cfg.num_sms ? rows : cfg.num_sms;
       const int64_t per = (rows + grid - 1) / grid;
       grid = (rows + per - 1) / per;   // no CTA without rows

@@ -926,15 +926,9 @@ template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
                         const CUtensorMap& b1, const Params& p, const FusedLaunch& L) {
   using C = ModeCfg<MODE>;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fused_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  static std::atomic<bool> limit_set[kMaxDevices];
+  if (const cudaError_t e = ensure_smem_limit(fused_gemm_kernel<MODE>, C::kSmemBytes, limit_set); e != cudaSuccess)
+    return e;
   if constexpr (C::kPair) {
     // clusters of 2 CTAs (one per SM): as many pairs as can be resident at once
     cudaLaunchAttribute attr{};
@@ -948,19 +942,22 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUte
     cfg.stream = L.stream;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    static int pairs_max[64] = {};
-    int cap = L.num_sms / 2;
-    if (dev < 64) {
-      if (pairs_max[dev] == 0) {
-        cfg.gridDim = dim3(static_cast<unsigned>(2 * (L.num_sms / 2)));
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, fused_gemm_kernel<MODE>, &cfg) != cudaSuccess || n <= 0) {
-          (void)cudaGetLastError();
-          n = L.num_sms / 2;
-        }
-        pairs_max[dev] = n < L.num_sms / 2 ? n : L.num_sms / 2;
+    // resident pairs per device, queried once (0 = not yet; atomic: calls may
+    // come from several host threads, and racing first queries agree)
+    static std::atomic<int> pairs_max[kMaxDevices];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int cap = dev < kMaxDevices ? pairs_max[dev].load(std::memory_order_relaxed) : 0;
+    if (cap == 0) {
+      cfg.gridDim = dim3(static_cast<unsigned>(2 * (L.num_sms / 2)));
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, fused_gemm_kernel<MODE>, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        n = L.num_sms / 2;
       }
-      cap = pairs_max[dev];
+      cap = n < L.num_sms / 2 ? n : L.num_sms / 2;
+      if (cap < 1) cap = 1;
+      if (dev < kMaxDevices) pairs_max[dev].store(cap, std::memory_order_relaxed);
     }
     const int64_t pairs = p.units < cap ? p.units : cap;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));

@@ -1,12 +1,28 @@
 // Internal launch interface between the C ABI (abi.cu) and the kernels.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace lmho {
+
+// Raises `kern`'s dynamic shared-memory limit to `bytes` on the current device,
+// once per device per call site (`done`: the site's static per-device flags).
+// Safe to call from several host threads: the flags are atomic, and two first
+// calls that race both set the same attribute.
+constexpr int kMaxDevices = 64;
+template <class K>
+cudaError_t ensure_smem_limit(K kern, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < kMaxDevices && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev < kMaxDevices) done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 struct Ctrl;
 
