@@ -71,9 +71,10 @@ constexpr int kJsdColSplit = 2;       // two-head pass: epilogue warps per TMEM 
 // columns, each CTA of the pair loading its kBM rows of A and half of B
 // (kBN_CE / 2 rows of the N extent) and holding its kBM rows of the
 // accumulator.  The gradient products (dx = dZ W, dW = dZ^T x) run on pairs:
-// their MN-major operands are feed-bound on a lone CTA, and the pair halves
-// each SM's operand bytes (dW 11 %, dx 7 % faster alone; 5-6 % in 40 ms
-// power-capped calls).  The CE, log-sum-exp and dZ passes run on lone CTAs
+// their MN-major operands are feed-bound on a lone CTA, and a pair's SM loads
+// 2/3 of the operand bytes per k-block (dW 11 %, dx 9 % faster in short
+// calls, both 7 % in 40 ms power-capped ones).  The CE, log-sum-exp and dZ
+// passes run on lone CTAs
 // (M = 128): paired they are ~5 % faster in short calls but 3-5 % slower
 // under the power cap, where they spend most of their time.  LMHO_PAIR_FWD /
 // LMHO_PAIR_GRAD (0 or 1) choose at build time; kBoxBFwd / kBoxBGrad are the
