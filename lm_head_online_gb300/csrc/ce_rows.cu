@@ -118,7 +118,7 @@ __device__ __forceinline__ float finish_loss(MS a, float zt) {
 // out_rows: per-row losses (per-token output, or the workspace of the flat mean)
 // mean_out: non-null for the flat variant.
 template <typename T, int U>
-__global__ void __launch_bounds__(256) ce_warp_rows(const T* __restrict__ logits,
+__global__ void __launch_bounds__(64) ce_warp_rows(const T* __restrict__ logits,
                                                     const int64_t* __restrict__ target, int64_t rows,
                                                     int64_t V, float* __restrict__ out_rows,
                                                     float* mean_out, Ctrl* ctrl) {
@@ -289,10 +289,12 @@ cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, in
     case kCeWarp: {
       // 16 loads per lane in flight: a 16 KB row takes one or two memory round
       // trips, a 32 KB row four (with 4 in flight, 16; Megatron bf16 V = 16384
-      // measured 49.3-49.6 vs 50.1-50.2 us, 64 vs 54 registers)
-      const int64_t blocks = (rows + 7) / 8;
-      ce_warp_rows<T, 16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(logits, target, rows, V, out_rows, mean_out,
-                                                                          ctrl);
+      // measured 49.3-49.6 vs 50.1-50.2 us, 64 vs 54 registers).  Blocks of 2
+      // warps: Megatron V = 16384 47.6-47.9 us against 49.2 with 8 warps, the
+      // same at V = 4096 and 8192, one event tick slower with 16.
+      const int64_t blocks = (rows + 1) / 2;
+      ce_warp_rows<T, 16><<<static_cast<unsigned>(blocks), 64, 0, st>>>(logits, target, rows, V, out_rows, mean_out,
+                                                                         ctrl);
       break;
     }
     case kCeCta:
