@@ -43,7 +43,8 @@ def close(got, ref):
 
 
 SHAPES = [(1, 64, 1), (5, 64, 37), (130, 128, 1000), (257, 200, 4097), (64, 1024, 513), (256, 512, 4096),
-          (70, 8, 300), (129, 16, 2049)]   # H = 8, 16: MN-major boxes mostly past the edge (zero fill)
+          (70, 8, 300), (129, 16, 2049),   # H = 8, 16: MN-major boxes mostly past the edge (zero fill)
+          (300, 200, 1024), (33, 72, 640)]  # V whole 64-wide chunks, H not: 3-D map for dZ, 2-D for W and x
 
 
 @pytest.mark.parametrize("T,H,V", SHAPES)

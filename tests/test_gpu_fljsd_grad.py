@@ -40,7 +40,8 @@ def close(got, ref):
 
 
 CASES = [((5, 64, 37), 0.5, 1.0, False), ((130, 128, 1000), 0.3, 2.0, True), ((64, 256, 4097), 0.5, 1.0, True),
-         ((129, 4096, 300), 0.7, 0.8, False), ((256, 512, 2048), 0.5, 1.0, False)]
+         ((129, 4096, 300), 0.7, 0.8, False), ((256, 512, 2048), 0.5, 1.0, False),
+         ((100, 200, 1024), 0.5, 1.0, False)]
 
 
 @pytest.mark.parametrize("shape,beta,tau,masked", CASES)
