@@ -60,6 +60,8 @@ def test_workspace_sizes(lib):
 
 
 # Fake, non-dereferenced addresses: validation happens before any device use.
+# Every call below must be rejected by a host-side check: one that passed them
+# all would launch kernels on these addresses if a GPU were present.
 A = 0x10000000
 B = 0x20000000
 C = 0x30000000
@@ -114,3 +116,72 @@ def test_fljsd_ex_argument_checks(lib):
     # the mask is an input: the loss may not overlap it
     assert lib.fljsd_fwd_bf16_ex(A, B, C, D, 4, 16, 10, f(0.5), f(1.0), 0x60000000, 0x60000001, D + 16384, ws,
                                  None) == 2
+
+
+def test_ce_backward_argument_checks(lib):
+    nan, inf = float("nan"), float("inf")
+    E = 0x50000000
+    # flat: null dlogits, non-finite grad_scale, short workspace, dlogits over logits / over ws
+    assert lib.ce_fwd_bwd_f32(A, B, 4, 4, 1.0, C, None, D, 4096, None) == 1
+    assert lib.ce_fwd_bwd_f32(A, B, 4, 4, nan, C, E, D, 4096, None) == 1
+    assert lib.ce_fwd_bwd_f32(A, B, 4, 4, inf, C, E, D, 4096, None) == 1
+    assert lib.ce_fwd_bwd_f32(A, B, 4, 4, 1.0, C, E, D, 16, None) == 3
+    assert lib.ce_fwd_bwd_f32(A, B, 4, 4, 1.0, C, A + 16, D, 4096, None) == 2
+    assert lib.ce_fwd_bwd_f32(A, B, 4, 4, 1.0, C, D + 512, D, 4096, None) == 2
+    # Megatron: dlogits over the logits, loss over dloss, sizes
+    assert lib.ce_fwd_bwd_sbv_bf16(A, B, 2, 2, 8, None, 1.0, C, A + 2, None) == 2
+    assert lib.ce_fwd_bwd_sbv_bf16(A, B, 2, 2, 8, E, 1.0, E + 4, C, None) == 2
+    assert lib.ce_fwd_bwd_sbv_bf16(A, B, 2, 0, 8, None, 1.0, C, E, None) == 1
+    assert lib.ce_fwd_bwd_sbv_bf16(A, B, 2, 2, 8, None, nan, C, E, None) == 1
+
+
+def test_fused_backward_argument_checks(lib):
+    ws = 1 << 30
+    E, F = 0x50000000, 0x60000000
+    # flce: H % 8, dx misaligned, short workspace, dx over x, dW over W, dx over dW
+    assert lib.flce_fwd_bwd_bf16(A, B, C, 4, 12, 10, 1.0, D, E, F, D + 4096, ws, None) == 4
+    assert lib.flce_fwd_bwd_bf16(A, B, C, 4, 16, 10, 1.0, D, E + 4, F, D + 4096, ws, None) == 1
+    assert lib.flce_fwd_bwd_bf16(A, B, C, 4, 16, 10, float("inf"), D, E, F, D + 4096, ws, None) == 1
+    assert lib.flce_fwd_bwd_bf16(A, B, C, 4, 16, 10, 1.0, D, E, F, D + 4096, 256, None) == 3
+    assert lib.flce_fwd_bwd_bf16(A, B, C, 4, 16, 10, 1.0, D, A, F, D + 4096, ws, None) == 2
+    assert lib.flce_fwd_bwd_bf16(A, B, C, 4, 16, 10, 1.0, D, E, B, D + 4096, ws, None) == 2
+    assert lib.flce_fwd_bwd_bf16(A, B, C, 4, 16, 10, 1.0, D, E, E + 16, D + 4096, ws, None) == 2
+    # fljsd backward: beta outside (0, 1), temperature <= 0, dWs over Wt
+    args = lambda beta, tau, dws: (A, B, C, D, 4, 16, 10, beta, tau, None, 1.0, E, F, dws, 0x70000000, ws, None)  # noqa: E731
+    assert lib.fljsd_fwd_bwd_bf16(*args(1.0, 1.0, 0x68000000)) == 1
+    assert lib.fljsd_fwd_bwd_bf16(*args(0.5, 0.0, 0x68000000)) == 1
+    assert lib.fljsd_fwd_bwd_bf16(*args(0.5, 1.0, D)) == 2
+
+
+def test_cpo_argument_checks(lib):
+    ws = 1 << 30
+    E, F = 0x50000000, 0x60000000
+    fwd = lambda Bq, S, beta, alpha: lib.flce_cpo_fwd_bf16(A, B, C, Bq, S, 16, 10, beta, alpha, D, None,  # noqa: E731
+                                                           D + 4096, ws, None)
+    assert fwd(3, 4, 0.1, 1.0) == 1      # odd batch: no chosen/rejected halves
+    assert fwd(0, 4, 0.1, 1.0) == 1
+    assert fwd(2, 0, 0.1, 1.0) == 1
+    assert fwd(2, 4, 0.0, 1.0) == 1      # beta must be > 0
+    assert fwd(2, 4, float("nan"), 1.0) == 1
+    assert fwd(2, 4, 0.1, -1.0) == 1     # alpha must be >= 0
+    assert lib.flce_cpo_fwd_bf16(A, B, C, 2, 4, 12, 10, 0.1, 1.0, D, None, D + 4096, ws, None) == 4   # H % 8
+    assert lib.flce_cpo_fwd_bf16(A, B, C, 2, 4, 16, 10, 0.1, 1.0, D, A + 8, D + 4096, ws, None) == 2  # logps over x
+    assert lib.flce_cpo_fwd_bf16(A, B, C, 2, 4, 16, 10, 0.1, 1.0, D, None, D + 4096, 256, None) == 3
+    # backward: dW over W, non-finite grad_scale, misaligned dx
+    assert lib.flce_cpo_fwd_bwd_bf16(A, B, C, 2, 4, 16, 10, 0.1, 1.0, 1.0, D, None, E, B, D + 4096, ws, None) == 2
+    assert lib.flce_cpo_fwd_bwd_bf16(A, B, C, 2, 4, 16, 10, 0.1, 1.0, float("inf"), D, None, E, F, D + 4096, ws,
+                                     None) == 1
+    assert lib.flce_cpo_fwd_bwd_bf16(A, B, C, 2, 4, 16, 10, 0.1, 1.0, 1.0, D, None, E + 4, F, D + 4096, ws, None) == 1
+
+
+def test_backward_workspace_sizes(lib):
+    import lm_head_online_gb300 as lmho
+    T, H, V = 2048, 4096, 128256
+    fwd, bwd = lmho.flce_workspace_bytes(T, H, V), lmho.flce_bwd_workspace_bytes(T, H, V)
+    # the backward keeps bf16 dZ [T, V padded to whole 256-column tiles] beyond the forward's
+    assert bwd % 256 == 0 and bwd >= fwd + 2 * T * ((V + 255) // 256 * 256)
+    # small T x H: room for up to 8 fp32 K slices of the [T, H] product dx
+    assert lmho.flce_bwd_workspace_bytes(256, 512, 4096) >= 8 * 4 * 256 * 512
+    assert lmho.fljsd_bwd_workspace_bytes(1024, H, V) >= lmho.fljsd_workspace_bytes(1024, H, V) + 2 * 1024 * V
+    c, cb = lmho.flce_cpo_workspace_bytes(2, 1024, H, V), lmho.flce_cpo_bwd_workspace_bytes(2, 1024, H, V)
+    assert c >= lmho.flce_workspace_bytes(2048, H, V) and cb >= lmho.flce_bwd_workspace_bytes(2048, H, V)
