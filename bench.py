@@ -239,12 +239,23 @@ def run_ours(args, rank, world, local_rank):
                 e.record(stream)
     torch.cuda.synchronize()
 
+    def nvtx(name, fn):
+        # a named NVTX range around each call, for timeline profilers (no cost without one)
+        def call():
+            torch.cuda.nvtx.range_push(name)
+            try:
+                fn()
+            finally:
+                torch.cuda.nvtx.range_pop()
+        return call
+
     op_fns = {
-        "ce": lambda: lmho.ce_fwd_f32(d["ce_z"], d["ce_t"], loss=out["ce"], ws=ws_ce),
-        "sbv": lambda: lmho.ce_fwd_sbv_bf16(d["sbv_z"], d["sbv_t"], loss=out["sbv"]),
-        "fl": lambda: lmho.flce_fwd_bf16(d["fl_x"], d["fl_w"], d["fl_t"], loss=out["fl"], ws=ws_fl),
-        "js": lambda: lmho.fljsd_fwd_bf16(d["js_xs"], d["js_ws"], d["js_xt"], d["js_wt"], 0.5,
-                                          loss=out["js"], ws=ws_js),
+        "ce": nvtx("ce_fwd_f32", lambda: lmho.ce_fwd_f32(d["ce_z"], d["ce_t"], loss=out["ce"], ws=ws_ce)),
+        "sbv": nvtx("ce_fwd_sbv_bf16", lambda: lmho.ce_fwd_sbv_bf16(d["sbv_z"], d["sbv_t"], loss=out["sbv"])),
+        "fl": nvtx("flce_fwd_bf16",
+                   lambda: lmho.flce_fwd_bf16(d["fl_x"], d["fl_w"], d["fl_t"], loss=out["fl"], ws=ws_fl)),
+        "js": nvtx("fljsd_fwd_bf16", lambda: lmho.fljsd_fwd_bf16(d["js_xs"], d["js_ws"], d["js_xt"], d["js_wt"], 0.5,
+                                                                 loss=out["js"], ws=ws_js)),
     }
 
     def step(i=None):
