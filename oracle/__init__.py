@@ -84,6 +84,10 @@ def _load():
             lib.oracle_cpo_grad_f64.restype = None
             lib.oracle_cpo_grad_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, dbl, dbl, vp, vp]
             lib.oracle_cpo_grad_bf16.restype = None
+            lib.oracle_ce_partials_bf16.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp]
+            lib.oracle_ce_partials_bf16.restype = None
+            lib.oracle_ce_merge.argtypes = [vp, vp, vp, i64, vp, i64, i64, vp]
+            lib.oracle_ce_merge.restype = None
             lib.oracle_logits_bf16.argtypes = [vp, vp, i64, i64, i64, vp]
             lib.oracle_logits_bf16.restype = None
             _lib = lib
@@ -126,6 +130,35 @@ def ce_sbv_bf16(z_bits, target):
     t, pt = _c(target, np.int64)
     out = np.empty((S, B), np.float64)
     _load().oracle_ce_sbv_bf16(pz, pt, S, B, V, out.ctypes.data)
+    return out
+
+
+def ce_partials_bf16(z_bits, target, v0):
+    """Vocab-parallel CE, one shard: bf16 logits [..., Vl] (uint16 bits) holding
+    the global columns [v0, v0 + Vl), global targets [...].  Returns float64
+    (m, s, zt), each shaped like target: the shard's max, sum of exp(z - m),
+    and the target logit or -inf when the target is not in the shard."""
+    z, pz = _c(z_bits, np.uint16)
+    Vl = z.shape[-1]
+    t, pt = _c(target, np.int64)
+    assert z.shape[:-1] == t.shape
+    rows = t.size
+    m, s, zt = (np.empty(t.shape, np.float64) for _ in range(3))
+    _load().oracle_ce_partials_bf16(pz, pt, rows, Vl, int(v0), m.ctypes.data, s.ctypes.data, zt.ctypes.data)
+    return m, s, zt
+
+
+def ce_merge(m, s, zt, target, V):
+    """Per-row losses from k shards' partials m, s, zt (each [k, ...], shard
+    order), global targets [...] and the global vocabulary size V."""
+    m, pm = _c(m, np.float64)
+    s, ps = _c(s, np.float64)
+    zt, pz = _c(zt, np.float64)
+    t, pt = _c(target, np.int64)
+    k = m.shape[0]
+    assert m.shape == s.shape == zt.shape and m.shape[1:] == t.shape
+    out = np.empty(t.shape, np.float64)
+    _load().oracle_ce_merge(pm, ps, pz, k, pt, t.size, int(V), out.ctypes.data)
     return out
 
 

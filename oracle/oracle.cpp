@@ -54,6 +54,18 @@
 // (beta/Bc) sigmoid(-beta d_k) for a chosen token of pair k, and
 // -(beta/Bc) sigmoid(-beta d_k) for a rejected one; then the CE backward.
 
+// Vocab-parallel cross-entropy ("Vocab-parallel cross-entropy, Megatron
+// layout", summary: the vocabulary split over tensor-parallel ranks, each rank
+// holding the logits of its own vocab range, so the local logits are
+// [seq, batch, V_local]).  For the shard [v0, v0 + Vl) of row i, two plain
+// passes as in the CE row:
+//   m_i = max over the shard,  s_i = sum over the shard of exp(z - m_i),
+//   zt_i = z_{i, t_i} when v0 <= t_i < v0 + Vl, else -inf.
+// Rows of k shards that together cover [0, V) combine, shard by shard in the
+// given order, into the row's loss:
+//   M = max_j m_j,  loss = M + ln( sum_j s_j exp(m_j - M) ) - max_j zt_j,
+// NaN when t_i is outside [0, V).
+
 // Variant (JSD with temperature and a token mask): the logits of both heads
 // are divided by the temperature tau before the softmax; tokens whose keep
 // flag is 0 are left out, and the batchmean divides by the number of kept
@@ -182,6 +194,46 @@ void oracle_ce_sbv_bf16(const uint16_t* z16, const int64_t* target, int64_t S, i
       for (int64_t v = 0; v < V; ++v) row[v] = bf16_to_double(z16[r * V + v]);
       loss_sb[r] = ce_row(row.data(), V, target[r]);
     }
+}
+
+// Vocab-parallel CE, one shard: bf16 logits [rows, Vl] holding the global vocab
+// columns [v0, v0 + Vl); targets are global indices.  Writes m, s, zt per row.
+void oracle_ce_partials_bf16(const uint16_t* z16, const int64_t* target, int64_t rows, int64_t Vl, int64_t v0,
+                             double* m_out, double* s_out, double* zt_out) {
+  std::vector<double> row(Vl);
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t v = 0; v < Vl; ++v) row[v] = bf16_to_double(z16[r * Vl + v]);
+    double M = row[0];
+    for (int64_t v = 1; v < Vl; ++v)
+      if (row[v] > M || std::isnan(row[v])) M = row[v];
+    double sum = 0.0;
+    for (int64_t v = 0; v < Vl; ++v) sum += std::exp(row[v] - M);
+    const int64_t tl = target[r] - v0;
+    m_out[r] = M;
+    s_out[r] = sum;
+    zt_out[r] = (tl >= 0 && tl < Vl) ? row[tl] : -std::numeric_limits<double>::infinity();
+  }
+}
+
+// Vocab-parallel CE, the combination of k shards' partials (each [k][rows],
+// shard-major) into per-row losses; V = the global vocabulary size.
+void oracle_ce_merge(const double* m, const double* s, const double* zt, int64_t k, const int64_t* target,
+                     int64_t rows, int64_t V, double* loss) {
+  for (int64_t r = 0; r < rows; ++r) {
+    if (target[r] < 0 || target[r] >= V) {
+      loss[r] = kNaN;
+      continue;
+    }
+    double M = m[r];
+    double Z = zt[r];
+    for (int64_t j = 1; j < k; ++j) {
+      if (m[j * rows + r] > M || std::isnan(m[j * rows + r])) M = m[j * rows + r];
+      if (zt[j * rows + r] > Z || std::isnan(zt[j * rows + r])) Z = zt[j * rows + r];
+    }
+    double sum = 0.0;
+    for (int64_t j = 0; j < k; ++j) sum += s[j * rows + r] * std::exp(m[j * rows + r] - M);
+    loss[r] = M + std::log(sum) - Z;
+  }
 }
 
 // Fused linear + CE: x [T, H], W [V, H] (bf16) -> per-token losses and their mean.
