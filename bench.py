@@ -42,7 +42,13 @@ FLCE = dict(T=16 * 1024, H=4096, V=128256)
 FLJSD = dict(T=8192, H=4096, V=128256)
 WORKLOAD = ("ce_fwd_f32 fp32[16384,131072] + ce_fwd_sbv_bf16 bf16[2048,4,131072] + "
             "flce_fwd_bf16 x[16384,4096] W[128256,4096] + fljsd_fwd_bf16 T=8192 H=4096 V=128256 beta=0.5")
-KERNELS_PER_STEP = 1 + 1 + 2 + 4
+KERNELS_PER_STEP = 2 + 1 + 2 + 4   # ce_fwd_f32: row kernel + mean; sbv 1; flce 2; fljsd 4
+
+# The workload table's smallest CE configurations (the pages' own "Estimated
+# floor" workloads), timed after the step, each alone: fp32 [16384, 4096] and
+# Megatron bf16 [2048, 4, V] for V = 4096 and 8192.
+SMALL_CE = (("ce_fwd_f32", 16384, 4096), ("ce_fwd_sbv_bf16", 2048, 4096), ("ce_fwd_sbv_bf16", 2048, 8192))
+L2_BYTES = 129 * 2 ** 20
 
 # DRAM bytes (read + write) per launch of each main kernel at the bench sizes,
 # from one ncu capture of a bench step (`ncu --metrics dram__bytes_read.sum,
@@ -53,7 +59,7 @@ KERNELS_PER_STEP = 1 + 1 + 2 + 4
 KERNEL_SOURCES = ("fused_linear.cu", "ce_rows.cu", "rowstats.cuh", "ptx.cuh", "lmho_internal.h")
 TRAFFIC_SOURCE_DIGEST = "ae85cd14e6e6127e"
 TRAFFIC_BYTES = {
-    "ce_fwd_f32.row_kernel": 8590211243 + 243029,
+    "ce_fwd_f32.row_kernel_and_mean": 8590211243 + 243029,
     "ce_fwd_sbv_bf16.row_kernel": 2147706283 + 351744,
     "flce.tcgen05_gemm_ce": 4339754923 + 65928619,
     "fljsd.tcgen05_gemm_lse": 4338453333 + 65594624,
@@ -83,6 +89,10 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-small-ce", action="store_true", help="skip the small CE configurations after the step")
+    ap.add_argument("--tp", action="store_true",
+                    help="vocab-parallel Megatron CE: bf16 [2048, 4, 131072] with the vocab sharded over the N ranks "
+                         "(partials, one NCCL all-gather, merge); prints its own JSON line")
     ap.add_argument("--e2e-clocks", action="store_true",
                     help="also sample clocks during the e2e region (nvidia-smi polling slows host copies)")
     ap.add_argument("--sweep", action="store_true",
@@ -202,6 +212,92 @@ def make_inputs(seed, torch, pinned=True):
     return h
 
 
+# ---------------------------------------------------------------- small CE calls
+def rotating_copies(x, torch, min_total=3 * L2_BYTES):
+    """x and enough device copies of it that a call on copy i % R reads bytes
+    not touched during the previous ~3 L2 capacities of reads."""
+    nbytes = x.numel() * x.element_size()
+    R = max(2, -(-min_total // nbytes))
+    return [x] + [x.clone() for _ in range(R - 1)]
+
+
+def time_flushed(fns, torch, warmup, steps, flush):
+    """Per-call time: a 512 MB read (L2 flush) before each call, CUDA events
+    recorded around the call on its stream."""
+    for i in range(warmup):
+        fns[i % len(fns)]()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i, (e0, e1) in enumerate(evs):
+        flush.sum()
+        e0.record()
+        fns[i % len(fns)]()
+        e1.record()
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) * 1e3 for e0, e1 in evs]
+
+
+def time_back_to_back(fns, torch, warmup, steps):
+    """Per-call time of `steps` calls issued back to back on one stream, call i
+    reading copy i % R of the input (R copies > 3x L2), one event pair around
+    all of them: no per-call event cost, every call's logits come from HBM.
+    The calls are queued behind a sleeping kernel (~60 us of GPU time per
+    call), so the host, which takes tens of microseconds per call, is ahead
+    of the GPU and no call waits for its launch."""
+    for i in range(warmup):
+        fns[i % len(fns)]()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(2e6 + 1.2e5 * steps))
+    e0.record()
+    for i in range(steps):
+        fns[i % len(fns)]()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / steps
+
+
+def small_ce(lmho, torch, dev, seed, pk, steps=50):
+    """The smallest CE workloads, each timed alone two ways (see above).
+    The roofline uses the back-to-back time; the flushed per-call time, which
+    adds a fixed event and launch cost of about 3 us, is reported beside it."""
+    import gen
+    thr = os.cpu_count() or 1
+    flush = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+    ops, roofs = {}, {}
+    for name, T, V in SMALL_CE:
+        if name == "ce_fwd_f32":
+            z = torch.from_numpy(gen.normal_f32(seed, gen.STREAM_LOGITS, (T, V), 1.0, threads=thr)).to(dev)
+            t = torch.from_numpy(gen.targets(seed, gen.STREAM_TARGET, (T,), V, threads=thr)).to(dev)
+            ws = lmho.workspace(lmho.ce_workspace_bytes(T, V), dev)
+            loss = torch.empty(1, device=dev)
+            fns = [lambda zz=zz: lmho.ce_fwd_f32(zz, t, loss=loss, ws=ws) for zz in rotating_copies(z, torch)]
+            nbytes, key, shape = rl.ce_flat_bytes(T, V), f"ce_fwd_f32.T{T}_V{V}", f"fp32[{T},{V}]"
+        else:
+            z = torch.empty((T, 4, V), dtype=torch.bfloat16)
+            gen.normal_bf16_bits(seed, gen.STREAM_LOGITS, (T, 4, V), 2.0, out=z.view(torch.int16), threads=thr)
+            z = z.to(dev)
+            t = torch.from_numpy(gen.targets(seed, gen.STREAM_TARGET, (T, 4), V, threads=thr)).to(dev)
+            loss = torch.empty((T, 4), device=dev)
+            fns = [lambda zz=zz: lmho.ce_fwd_sbv_bf16(zz, t, loss=loss) for zz in rotating_copies(z, torch)]
+            nbytes, key, shape = rl.ce_sbv_bytes(T, 4, V), f"ce_fwd_sbv_bf16.S{T}_B4_V{V}", f"bf16[{T},4,{V}]"
+        b2b = time_back_to_back(fns, torch, 5, steps)
+        fl = time_flushed(fns, torch, 5, steps, flush)
+        med = float(np.median(fl))
+        gbs = nbytes / (b2b * 1e-6) / 1e9
+        ops[key] = {"shape": shape, "bytes": nbytes, "copies": len(fns),
+                    "us_back_to_back": round(b2b, 2), "GB/s_back_to_back": round(gbs, 1),
+                    "us_flushed_median": round(med, 2), "us_flushed_p10": round(float(np.percentile(fl, 10)), 2),
+                    "GB/s_flushed": round(nbytes / (med * 1e-6) / 1e9, 1),
+                    "frac_flushed": round(nbytes / (med * 1e-6) / 1e9 / pk["hbm"], 4)}
+        roofs[key] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                      "frac": round(gbs / pk["hbm"], 4), "traffic": None,
+                      "timing": f"back to back over {len(fns)} copies (> 3x L2), mean per call"}
+        del fns, z
+        torch.cuda.empty_cache()
+    return ops, roofs, 2 * steps * sum(2 if n == "ce_fwd_f32" else 1 for n, _, _ in SMALL_CE)
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -302,7 +398,7 @@ def run_ours(args, rank, world, local_rank):
         return float(np.mean([ev[op][i][j].elapsed_time(ev[op][i][j + 1]) for i in range(K)]))
 
     kern = {
-        "ce_fwd_f32.row_kernel": ("ce", 0), "ce_fwd_sbv_bf16.row_kernel": ("sbv", 0),
+        "ce_fwd_f32.row_kernel_and_mean": ("ce", 0), "ce_fwd_sbv_bf16.row_kernel": ("sbv", 0),
         "flce.tcgen05_gemm_ce": ("fl", 0), "flce.finalize": ("fl", 1),
         "fljsd.tcgen05_gemm_lse": ("js", 0), "fljsd.lse_finalize": ("js", 1),
         "fljsd.tcgen05_gemm_jsd": ("js", 2), "fljsd.jsd_finalize": ("js", 3),
@@ -329,7 +425,8 @@ def run_ours(args, rank, world, local_rank):
                 "frac": round(tfs / tf_peak, 4), "traffic": traffic}
 
     roofs = {
-        "ce_fwd_f32.row_kernel": hbm_roof(ce_b, kms["ce_fwd_f32.row_kernel"], traffic_of("ce_fwd_f32.row_kernel")),
+        "ce_fwd_f32.row_kernel_and_mean": hbm_roof(ce_b, kms["ce_fwd_f32.row_kernel_and_mean"],
+                                                   traffic_of("ce_fwd_f32.row_kernel_and_mean")),
         "ce_fwd_sbv_bf16.row_kernel": hbm_roof(sbv_b, kms["ce_fwd_sbv_bf16.row_kernel"],
                                                traffic_of("ce_fwd_sbv_bf16.row_kernel")),
         "flce.tcgen05_gemm_ce": tc_roof(fl_f, kms["flce.tcgen05_gemm_ce"], traffic_of("flce.tcgen05_gemm_ce")),
@@ -337,6 +434,9 @@ def run_ours(args, rank, world, local_rank):
         "fljsd.tcgen05_gemm_jsd": tc_roof(js_pf, kms["fljsd.tcgen05_gemm_jsd"], traffic_of("fljsd.tcgen05_gemm_jsd")),
     }
     dominant = max(roofs, key=lambda k: kms[k])
+    small_ops, small_roofs = {}, {}
+    if not args.no_small_ce:
+        small_ops, small_roofs, _ = small_ce(lmho, torch, dev, args.seed + rank, pk)
     ops = {
         "ce_fwd_f32": {"us": round(call_ms["ce"] * 1e3, 2), "GB/s": round(ce_b / call_ms["ce"] / 1e6, 1),
                        "bytes": ce_b, "loss": float(out["ce"].item())},
@@ -425,6 +525,8 @@ def run_ours(args, rank, world, local_rank):
         "kernels_ms": {k: round(v, 4) for k, v in kms.items()},
         "roofline": dict(roofs[dominant], kernel=dominant),
         "rooflines": roofs,
+        "small_ce": {"ops": small_ops, "rooflines": small_roofs,
+                     "note": "each configuration alone after the step; not part of value"},
         "e2e": e2e,
         "gpu_launches": KERNELS_PER_STEP * K,
         "clocks": clock_dev,
@@ -437,6 +539,93 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
         dist.destroy_process_group()
     return result
+
+
+# ---------------------------------------------------------------- vocab-parallel arm
+def run_tp(args, rank, world, local_rank):
+    """Tensor-parallel Megatron cross-entropy over `world` ranks (one GPU each):
+    rank r holds the vocab columns shard_vocab(V, r, world) of bf16 logits
+    [S, B, V] ~ N(0, 2^2); a step is the rank's partials kernel, one NCCL
+    all-gather of the partials (12 bytes per token per rank) and the merge
+    kernel.  Total work is fixed as N grows ("strong").  A one-rank NCCL group
+    is used at N = 1, so the collective path runs there too."""
+    import torch
+    import torch.distributed as tdist
+    import gen
+    import lm_head_online_gb300 as lmho
+    from lm_head_online_gb300 import dist as lmdist
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lmho.load()
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    os.environ.setdefault("MASTER_PORT", "29533")
+    tdist.init_process_group("nccl", rank=rank, world_size=world, device_id=dev)
+    S, B, V = SBV["S"], SBV["B"], SBV["V"]
+    v0, w = lmdist.shard_vocab(V, rank, world)
+    thr = os.cpu_count() or 1
+    full = torch.empty((S, B, V), dtype=torch.bfloat16)
+    gen.normal_bf16_bits(args.seed, gen.STREAM_LOGITS, (S, B, V), 2.0, out=full.view(torch.int16), threads=thr)
+    local = full[:, :, v0:v0 + w].contiguous().to(dev)
+    del full
+    t = torch.from_numpy(gen.targets(args.seed, gen.STREAM_TARGET, (S, B), V, threads=thr)).to(dev)
+    part = torch.empty((3, S, B), device=dev)
+    gathered = torch.empty((world, 3, S, B), device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        lmho.ce_partials_sbv_bf16(local, t, v0, partials=part)
+        if ev:
+            ev[1].record(stream)
+        tdist.all_gather_into_tensor(gathered.view(world * 3, S, B), part)
+        if ev:
+            ev[2].record(stream)
+        loss = lmho.ce_merge_partials(gathered, t, V)
+        if ev:
+            ev[3].record(stream)
+        return loss
+
+    for _ in range(args.warmup):
+        loss = step()
+    torch.cuda.synchronize()
+    single = lmho.ce_fwd_sbv_bf16(local, t) if world == 1 else None
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        tdist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(K):
+            loss = step(evs[i])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        tdist.barrier()
+    ms = lmdist.max_over_ranks(e0.elapsed_time(e1) / K)
+    ph = {name: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]))
+          for j, name in enumerate(("partials", "all_gather", "merge"))}
+    local_bytes = 2 * S * B * w + 8 * S * B + 12 * S * B
+    pk = peaks()
+    gbs = local_bytes / (ph["partials"] * 1e-3) / 1e9
+    res = {"metric": "vocab-parallel Megatron CE us/step (partials + all-gather + merge)", "impl": "ours",
+           "mode": "vocab-parallel", "value": round(ms * 1e3, 2), "unit": "us/step", "n_gpus": world, "steps": K,
+           "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": False, "scaling": "strong",
+           "vs_baseline": None, "dtype": "bf16 in, f32 accumulate", "data": "synthetic (seeded Philox generator)",
+           "config": {"workload": f"ce_partials_sbv_bf16 + all-gather + ce_merge_partials, bf16[{S},{B},{V}] "
+                                  f"vocab-sharded over {world} rank(s)", "parallelism": f"tp{world}",
+                      "l2": "local logits larger than L2 (no flush)" if 2 * S * B * w > L2_BYTES else
+                            "local logits smaller than L2 (consecutive steps may hit L2)"},
+           "phases_us": {k: round(v * 1e3, 2) for k, v in ph.items()},
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                        "frac": round(gbs / pk["hbm"], 4), "traffic": None, "kernel": "ce_partials_sbv_bf16"},
+           "gpu_launches": 2 * K, "clocks": clocks.summary(),
+           "loss_mean": float(loss.double().mean().item())}
+    if single is not None:
+        res["max_abs_diff_vs_ce_fwd_sbv_bf16"] = float((loss - single).abs().max().item())
+    tdist.destroy_process_group()
+    return res
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm
@@ -662,6 +851,16 @@ def run_case(args):
         ws = lmho.workspace(lmho.fljsd_workspace_bytes(T, H, V))
         fn = lambda: lmho.fljsd_fwd_bf16(xs, Ws, xt, Wt, 0.5, ws=ws)  # noqa: E731
         work, unit = rl.fljsd_flops(T, H, V), "TFLOP/s"
+    b2b = None
+    if c in ("ce", "sbv"):
+        # the same call back to back over rotating copies of the logits (> 3x L2)
+        if c == "ce":
+            fns = [lambda zz=zz: lmho.ce_fwd_f32(zz, t, ws=ws) for zz in rotating_copies(z, torch)]
+        else:
+            fns = [lambda zz=zz: lmho.ce_fwd_sbv_bf16(zz, t) for zz in rotating_copies(z, torch)]
+        b2b = time_back_to_back(fns, torch, max(args.warmup, 3), max(args.steps, 20))
+        del fns
+        torch.cuda.empty_cache()
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
@@ -694,7 +893,10 @@ def run_case(args):
     kernel_ms = [[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(nk)] for i in range(args.steps)]
     med = float(np.median(ms))
     rate = work / (med * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
-    return {"case": c, "T": args.T, "V": args.V, "H": H, "ce_variant": args.ce_variant, "raster_group": args.raster_group, "l2": "flushed (512 MB read) before each call",
+    extra = {}
+    if b2b is not None:
+        extra = {"us_back_to_back": round(b2b, 2), "GB/s_back_to_back": round(work / (b2b * 1e-6) / 1e9, 1)}
+    return {**extra, "case": c, "T": args.T, "V": args.V, "H": H, "ce_variant": args.ce_variant, "raster_group": args.raster_group, "l2": "flushed (512 MB read) before each call",
             "us_median": round(med * 1e3, 2),
             "us_p10": round(float(np.percentile(ms, 10)) * 1e3, 2),
             "us_p90": round(float(np.percentile(ms, 90)) * 1e3, 2),
@@ -751,6 +953,11 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.tp:
+        res = run_tp(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
         return
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:

@@ -17,7 +17,12 @@
  *     (const uint16_t*), so this header needs no CUDA include.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Calls only enqueue work on it: they never synchronise, never allocate and
- *     keep no state between calls.  They are thread-safe.
+ *     keep no state between calls.  They are thread-safe.  The exceptions are
+ *     the process-wide tuning settings at the end of this header
+ *     (lmho_set_ce_variant, lmho_set_raster_group, lmho_set_wait_timeout_ns):
+ *     a change made by one thread applies to later calls of every thread.
+ *     They choose kernels and limits, never results beyond rounding.  The
+ *     measurement hook lmho_set_launch_events is per host thread.
  *   - "No mutation or aliasing" (every page, section Semantics): inputs are
  *     never written, and an output or workspace byte range that overlaps an
  *     input (or each other) is rejected with LMHO_ERR_ALIAS.
@@ -71,7 +76,9 @@ int lmho_version(void);
  *   ws      device workspace of ws_bytes >= ce_workspace_bytes(T, V), zeroed
  *           before first use.  After the call completes, the first T floats
  *           of ws hold the per-token losses loss_i.
- * One kernel launch.
+ * Two kernel launches: the row kernel, then a one-block mean kernel launched
+ * as its programmatic dependent (it starts while the rows drain and waits
+ * in-kernel for their completion); the mean's summation order is fixed.
  * ------------------------------------------------------------------------ */
 size_t ce_workspace_bytes(int64_t T, int64_t V);
 int ce_fwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
@@ -115,6 +122,40 @@ int ce_fwd_f32_noalloc(const float* logits, const int64_t* target, int64_t T, in
  * ------------------------------------------------------------------------ */
 int ce_fwd_sbv_bf16(const uint16_t* logits, const int64_t* target, int64_t S, int64_t B,
                     int64_t V, float* loss, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Vocab-parallel (tensor-parallel) Megatron-layout cross-entropy.
+ * Page "Vocab-parallel cross-entropy, Megatron layout", summary: with the
+ * vocabulary sharded over tensor-parallel ranks each rank holds only its own
+ * vocab range, so the local logits are [seq, batch, V_local].  A rank reduces
+ * each token to its shard's partial; the ranks exchange the partials (one
+ * all-gather of 12 bytes per token per rank, done by the caller, e.g. NCCL);
+ * every rank then merges all shards into the per-token losses.
+ *
+ * ce_partials_sbv_bf16: one shard.
+ *   logits_local [S, B, V_local] bf16 device: global vocab columns
+ *                [vocab_start, vocab_start + V_local) of every token
+ *   target       [S, B] int64 device, GLOBAL vocab indices
+ *   partials     [3][S*B] fp32 device output: m[i] = max of the shard's
+ *                logits of token i, s[i] = sum of exp(z - m[i]) over the
+ *                shard, z[i] = the target logit when the target lies in this
+ *                shard, else -inf.  (Token i = s*B + b.)
+ *   vocab_start >= 0.  One kernel launch (the Megatron CE row decompositions).
+ *
+ * ce_merge_partials: `shards` blocks of partials, contiguous in shard order
+ * ([shards][3][S*B] fp32 device, as an all-gather of the per-rank blocks in
+ * rank order leaves them), merged per token in that order:
+ *   M = max m_j,  loss = M + ln(sum_j s_j exp(m_j - M)) - max_j z_j;
+ *   target [S, B] int64 device (global), V = the global vocabulary size; the
+ *   shards must cover [0, V) exactly once (not checked).  A target outside
+ *   [0, V) gives NaN.  loss [S, B] fp32 device output.  One kernel launch.
+ * Both: no workspace; accumulation in fp32; outputs must not overlap inputs.
+ * ------------------------------------------------------------------------ */
+int ce_partials_sbv_bf16(const uint16_t* logits_local, const int64_t* target, int64_t S,
+                         int64_t B, int64_t V_local, int64_t vocab_start, float* partials,
+                         void* stream);
+int ce_merge_partials(const float* partials, int64_t shards, const int64_t* target, int64_t S,
+                      int64_t B, int64_t V, float* loss, void* stream);
 
 /* ------------------------------------------------------------------------
  * Cross-entropy forward + backward: the losses and their gradient with
@@ -300,11 +341,11 @@ int fljsd_fwd_bwd_bf16(const uint16_t* xs, const uint16_t* Ws, const uint16_t* x
  * ------------------------------------------------------------------------ */
 int lmho_ws_status(void* ws, size_t ws_bytes, void* stream);
 
-/* Row decomposition of the two cross-entropy calls, process-wide:
- *   0 = automatic (default): fp32 rows of at most 32 KB whose start and
- *       length are multiples of 16 bytes go through the bulk-copy ring;
- *       other rows of at most 32 KB get a warp per row; longer rows a CTA per
- *       row, or a cluster of 8 CTAs per row when rows are few (< 4 per SM);
+/* Row decomposition of the cross-entropy forward calls (ce_fwd_f32,
+ * ce_fwd_f32_noalloc, ce_fwd_sbv_bf16, ce_partials_sbv_bf16), process-wide:
+ *   0 = automatic (default): rows of at most 32 KB get a warp per row; longer
+ *       rows a CTA per row, or a cluster of 8 CTAs per row when rows are few
+ *       (< 4 per SM);
  *   1 = warp per row, 2 = CTA (256 threads) per row, 3 = CTA (512) per row,
  *   4 / 5 / 6 = cluster of 2 / 4 / 8 CTAs per row (DSMEM merge),
  *   7 = bulk-copy ring (rows up to 100 KB, 16-byte aligned; other rows fall
@@ -325,12 +366,15 @@ int lmho_set_ce_variant(int variant);
  * never results.  Returns LMHO_ERR_INVALID_ARG outside that range. */
 int lmho_set_raster_group(int group_m);
 
-/* Measurement hook, process-wide and not thread-safe: while set, every call
- * records events[0] (a caller-created cudaEvent_t) on its stream before its
- * first kernel and events[i] after its i-th kernel, for i < n.  Kernels per
- * call: ce_fwd_f32 1, ce_fwd_sbv_bf16 1, flce_fwd_bf16 2 (tensor-core pass,
- * finaliser), fljsd_fwd_bf16 4 (log-sum-exp pass, finaliser, divergence
- * pass, finaliser).  Pass (NULL, 0) to turn it off. */
+/* Measurement hook of the calling host thread: while set, every call that
+ * thread makes records events[0] (a caller-created cudaEvent_t) on its stream
+ * before its first kernel and events[i] after its i-th timed segment, for
+ * i < n.  Segments per call: ce_fwd_f32 1 (the row kernel and its dependent
+ * mean kernel together: an event between them would break their overlap),
+ * ce_fwd_sbv_bf16 1, ce_partials_sbv_bf16 1, ce_merge_partials 1,
+ * flce_fwd_bf16 2 (tensor-core pass, finaliser), fljsd_fwd_bf16 4
+ * (log-sum-exp pass, finaliser, divergence pass, finaliser).  Calls made by
+ * other threads are not affected.  Pass (NULL, 0) to turn it off. */
 void lmho_set_launch_events(void* const* events, int n);
 
 /* Upper bound, in nanoseconds, of every in-kernel wait of later calls

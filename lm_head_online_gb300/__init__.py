@@ -33,6 +33,7 @@ LMHO_ERR_TIMEOUT = 6
 # Every symbol declared in include/lmho.h.
 EXPORTS = (
     "lmho_strerror", "lmho_version", "ce_workspace_bytes", "ce_fwd_f32", "ce_fwd_f32_noalloc", "ce_fwd_sbv_bf16",
+    "ce_partials_sbv_bf16", "ce_merge_partials",
     "ce_fwd_bwd_f32", "ce_fwd_bwd_sbv_bf16",
     "flce_workspace_bytes", "flce_fwd_bf16", "flce_bwd_workspace_bytes", "flce_fwd_bwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "fljsd_bwd_workspace_bytes", "fljsd_fwd_bwd_bf16",
@@ -74,6 +75,10 @@ def load():
         lib.ce_fwd_f32_noalloc.restype = ci
         lib.ce_fwd_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, vp, vp]
         lib.ce_fwd_sbv_bf16.restype = ci
+        lib.ce_partials_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, i64, vp, vp]
+        lib.ce_partials_sbv_bf16.restype = ci
+        lib.ce_merge_partials.argtypes = [vp, i64, vp, i64, i64, i64, vp, vp]
+        lib.ce_merge_partials.restype = ci
         lib.ce_fwd_bwd_f32.argtypes = [vp, vp, i64, i64, f32, vp, vp, vp, sz, vp]
         lib.ce_fwd_bwd_f32.restype = ci
         lib.ce_fwd_bwd_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, vp, f32, vp, vp, vp]
@@ -220,6 +225,46 @@ def ce_fwd_sbv_bf16(logits, target, loss=None, stream=None):
         loss = torch.empty((S, B), dtype=torch.float32, device=logits.device)
     _check(lib.ce_fwd_sbv_bf16(pl, pt, S, B, V, _dev(loss, "loss", torch.float32), _stream(stream)),
            "ce_fwd_sbv_bf16")
+    return loss
+
+
+def ce_partials_sbv_bf16(logits_local, target, vocab_start, partials=None, stream=None):
+    """One vocabulary shard of the vocab-parallel Megatron cross-entropy.
+
+    logits_local: bf16 [S, B, V_local], the global vocab columns
+    [vocab_start, vocab_start + V_local); target: int64 [S, B] global indices.
+    Returns fp32 [3, S, B]: the shard's max, sum of exp(z - max), and the
+    target logit (-inf where the target is not in this shard)."""
+    lib = load()
+    pl = _dev(logits_local, "logits_local", torch.bfloat16, 3)
+    S, B, Vl = logits_local.shape
+    pt = _dev(target, "target", torch.int64, 2)
+    if tuple(target.shape) != (S, B):
+        raise ValueError("target must be [S, B]")
+    if partials is None:
+        partials = torch.empty((3, S, B), dtype=torch.float32, device=logits_local.device)
+    if tuple(partials.shape) != (3, S, B):
+        raise ValueError("partials must be [3, S, B]")
+    _check(lib.ce_partials_sbv_bf16(pl, pt, S, B, Vl, int(vocab_start), _dev(partials, "partials", torch.float32, 3),
+                                    _stream(stream)), "ce_partials_sbv_bf16")
+    return partials
+
+
+def ce_merge_partials(partials, target, V, loss=None, stream=None):
+    """Per-token losses fp32 [S, B] from the partials of every vocabulary
+    shard, fp32 [shards, 3, S, B] in shard order; V = global vocabulary size."""
+    lib = load()
+    pp = _dev(partials, "partials", torch.float32, 4)
+    k, three, S, B = partials.shape
+    if three != 3:
+        raise ValueError("partials must be [shards, 3, S, B]")
+    pt = _dev(target, "target", torch.int64, 2)
+    if tuple(target.shape) != (S, B):
+        raise ValueError("target must be [S, B]")
+    if loss is None:
+        loss = torch.empty((S, B), dtype=torch.float32, device=partials.device)
+    _check(lib.ce_merge_partials(pp, k, pt, S, B, int(V), _dev(loss, "loss", torch.float32, 2), _stream(stream)),
+           "ce_merge_partials")
     return loss
 
 

@@ -102,6 +102,7 @@ uint32_t env_bulk_ring() {
 }
 const uint32_t g_bulk_ring = env_bulk_ring();
 
+
 // Rows the bulk-copy ring can take: whole 16-byte vectors, 16-byte aligned
 // start, two stages in the ring.
 bool bulk_ok(const void* base, int64_t V, size_t elt) {
@@ -127,13 +128,12 @@ CeConfig choose_ce(const void* base, int64_t rows, int64_t V, size_t elt, int nu
       return c;
     default: break;
   }
-  // Measured on GB300 (flat fp32 [16384, V], Megatron bf16 [2048, 4, V]):
-  // fp32 rows <= 32 KB stream fastest through the bulk-copy ring; bf16 rows
-  // (twice the exponentials per byte) of <= 32 KB through warp-per-row loads;
-  // longer rows through a CTA per row.
-  if (elt == 4 && bulk_ok(base, V, elt) && row_bytes <= 32 * 1024) {
-    c.variant = kCeBulk;
-  } else if (row_bytes <= 32 * 1024) {
+  // Measured on GB300 (flat fp32 [16384, V], Megatron bf16 [2048, 4, V],
+  // calls back to back over inputs larger than L2): rows of at most 32 KB
+  // stream fastest through warp-per-row loads (fp32 V = 4096: 43.3 us against
+  // 46.9 for the bulk-copy ring; V = 8192: 82.5 against 83.3); longer rows
+  // through a CTA per row (fp32 V = 16384: 149 us, warp per row 155, ring 352).
+  if (row_bytes <= 32 * 1024) {
     c.variant = kCeWarp;
   } else if (rows < 4 * static_cast<int64_t>(num_sms) && row_bytes >= 64 * 1024) {
     c.variant = kCeCluster;   // few long rows: split each row over a cluster
@@ -231,15 +231,14 @@ int check_fused_common(int64_t T, int64_t H, int64_t V) {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 
-std::mutex g_ev_mu;
-cudaEvent_t g_events[16];
-int g_nevents = 0;
+// The measurement hook is per host thread (each thread's own events).
+thread_local cudaEvent_t t_events[16];
+thread_local int t_nevents = 0;
 
 }  // namespace
 
 void launch_mark(int i, cudaStream_t st) {
-  std::lock_guard<std::mutex> lk(g_ev_mu);
-  if (i < g_nevents && g_events[i]) cudaEventRecord(g_events[i], st);
+  if (i < t_nevents && t_events[i]) cudaEventRecord(t_events[i], st);
 }
 
 // ---------------------------------------------------------------- workspace layouts
@@ -390,12 +389,11 @@ const char* lmho_strerror(int status) {
 int lmho_version(void) { return 100; }
 
 void lmho_set_launch_events(void* const* events, int n) {
-  std::lock_guard<std::mutex> lk(g_ev_mu);
-  g_nevents = 0;
+  t_nevents = 0;
   if (!events || n <= 0) return;
   if (n > 16) n = 16;
-  for (int k = 0; k < n; ++k) g_events[k] = static_cast<cudaEvent_t>(events[k]);
-  g_nevents = n;
+  for (int k = 0; k < n; ++k) t_events[k] = static_cast<cudaEvent_t>(events[k]);
+  t_nevents = n;
 }
 
 int lmho_set_raster_group(int group_m) {
@@ -446,6 +444,38 @@ int ce_fwd_sbv_bf16(const uint16_t* logits, const int64_t* target, int64_t S, in
   if (int d = current_device(&sms)) return d;
   const CeConfig cfg = choose_ce(logits, rows, V, 2, sms);
   return cuda_status(launch_ce_bf16_rows(logits, target, rows, V, loss, cfg, static_cast<cudaStream_t>(stream)));
+}
+
+int ce_partials_sbv_bf16(const uint16_t* logits_local, const int64_t* target, int64_t S, int64_t B,
+                         int64_t V_local, int64_t vocab_start, float* partials, void* stream) {
+  if (!logits_local || !target || !partials) return LMHO_ERR_INVALID_ARG;
+  if (S <= 0 || B <= 0 || V_local <= 0 || vocab_start < 0) return LMHO_ERR_INVALID_ARG;
+  const int64_t rows = S * B;
+  if (rows > (int64_t(1) << 31) - 1 || vocab_start > (int64_t(1) << 62)) return LMHO_ERR_INVALID_ARG;
+  const Range in[2] = {rng(logits_local, 2 * static_cast<size_t>(rows) * V_local),
+                       rng(target, 8 * static_cast<size_t>(rows))};
+  const Range out[1] = {rng(partials, 12 * static_cast<size_t>(rows))};
+  if (int a = check_alias(in, 2, out, 1)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  CeConfig cfg = choose_ce(logits_local, rows, V_local, 2, sms);
+  return cuda_status(launch_ce_partials_bf16(logits_local, target, rows, V_local, vocab_start, partials, cfg,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int ce_merge_partials(const float* partials, int64_t shards, const int64_t* target, int64_t S, int64_t B, int64_t V,
+                      float* loss, void* stream) {
+  if (!partials || !target || !loss) return LMHO_ERR_INVALID_ARG;
+  if (shards <= 0 || S <= 0 || B <= 0 || V <= 0) return LMHO_ERR_INVALID_ARG;
+  const int64_t rows = S * B;
+  if (rows > (int64_t(1) << 31) - 1 || shards > (int64_t(1) << 20)) return LMHO_ERR_INVALID_ARG;
+  const Range in[2] = {rng(partials, 12 * static_cast<size_t>(rows) * static_cast<size_t>(shards)),
+                       rng(target, 8 * static_cast<size_t>(rows))};
+  const Range out[1] = {rng(loss, 4 * static_cast<size_t>(rows))};
+  if (int a = check_alias(in, 2, out, 1)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  return cuda_status(launch_ce_merge(partials, shards, target, rows, V, loss, sms, static_cast<cudaStream_t>(stream)));
 }
 
 int ce_fwd_bwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V, float grad_scale, float* loss,

@@ -47,6 +47,15 @@ cudaError_t launch_ce_f32(const float* logits, const int64_t* target, int64_t T,
 cudaError_t launch_ce_bf16_rows(const uint16_t* logits, const int64_t* target, int64_t rows,
                                 int64_t V, float* loss_rows, const CeConfig& cfg, cudaStream_t st);
 
+// Vocab-parallel cross-entropy: one shard's partials (max, sum of exp,
+// target logit or -inf) of bf16 rows [rows, V_local] holding the global
+// columns [v0, v0 + V_local), written as [3][rows] floats; and the merge of
+// `shards` such blocks ([shards][3][rows]) into per-row losses.
+cudaError_t launch_ce_partials_bf16(const uint16_t* logits, const int64_t* target, int64_t rows, int64_t V_local,
+                                    int64_t v0, float* partials, const CeConfig& cfg, cudaStream_t st);
+cudaError_t launch_ce_merge(const float* partials, int64_t shards, const int64_t* target, int64_t rows, int64_t V,
+                            float* loss, int num_sms, cudaStream_t st);
+
 // Forward + backward (loss and gradient w.r.t. the logits), one HBM pass.
 // gscale: gradient weight per row (flat: grad_scale / T; per-token rows also
 // multiplied by dloss[r] when dloss is non-null).

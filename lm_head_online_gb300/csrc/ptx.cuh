@@ -52,6 +52,19 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
   return r;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: a kernel launched after this one with the
+// programmatic-stream-serialization attribute may be scheduled once every CTA
+// of this grid has executed launch_dependents (or exited); that kernel's
+// griddep_wait() returns only when this whole grid has completed and its
+// memory writes are visible.  Both are no-ops when no such launch exists.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

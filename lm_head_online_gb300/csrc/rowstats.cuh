@@ -81,6 +81,120 @@ template <> struct Elt<uint16_t> {  // bf16 bit patterns
   }
 };
 
+// ---------------------------------------------------------------- packed folds
+// Packed fp32 pairs (sm_100+): one instruction does two fp32 FMAs or adds.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t p, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// max of three fp32 values in one instruction (sm_100+)
+__device__ __forceinline__ float max3_f32(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// A 16-byte vector of -inf in the element type (the fill of masked lanes).
+template <typename T> __device__ __forceinline__ uint4 neg_inf_vec();
+template <> __device__ __forceinline__ uint4 neg_inf_vec<float>() {
+  return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+}
+template <> __device__ __forceinline__ uint4 neg_inf_vec<uint16_t>() {
+  return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+}
+
+// Maximum of the elements of N raw 16-byte vectors (NaNs are dropped here;
+// they still reach the sum below and make it NaN).
+template <typename T, int N> __device__ __forceinline__ float vec_max(const uint4* r);
+template <int N> struct VecMaxF32 {
+  static __device__ __forceinline__ float run(const uint4* r) {
+    float m = max3_f32(__uint_as_float(r[0].x), __uint_as_float(r[0].y), __uint_as_float(r[0].z));
+    m = fmaxf(m, __uint_as_float(r[0].w));
+#pragma unroll
+    for (int i = 1; i < N; ++i) {
+      m = max3_f32(m, __uint_as_float(r[i].x), __uint_as_float(r[i].y));
+      m = max3_f32(m, __uint_as_float(r[i].z), __uint_as_float(r[i].w));
+    }
+    return m;
+  }
+};
+template <> __device__ __forceinline__ float vec_max<float, 1>(const uint4* r) { return VecMaxF32<1>::run(r); }
+template <> __device__ __forceinline__ float vec_max<float, 2>(const uint4* r) { return VecMaxF32<2>::run(r); }
+template <> __device__ __forceinline__ float vec_max<float, 4>(const uint4* r) { return VecMaxF32<4>::run(r); }
+template <> __device__ __forceinline__ float vec_max<float, 16>(const uint4* r) { return VecMaxF32<16>::run(r); }
+template <int N> struct VecMaxBf16 {
+  // on the packed words: max.bf16x2 compares two elements per instruction
+  static __device__ __forceinline__ float run(const uint4* r) {
+    uint32_t w = max_bf16x2(max_bf16x2(r[0].x, r[0].y), max_bf16x2(r[0].z, r[0].w));
+#pragma unroll
+    for (int i = 1; i < N; ++i) w = max_bf16x2(w, max_bf16x2(max_bf16x2(r[i].x, r[i].y), max_bf16x2(r[i].z, r[i].w)));
+    return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  }
+};
+template <> __device__ __forceinline__ float vec_max<uint16_t, 1>(const uint4* r) { return VecMaxBf16<1>::run(r); }
+template <> __device__ __forceinline__ float vec_max<uint16_t, 2>(const uint4* r) { return VecMaxBf16<2>::run(r); }
+template <> __device__ __forceinline__ float vec_max<uint16_t, 4>(const uint4* r) { return VecMaxBf16<4>::run(r); }
+template <> __device__ __forceinline__ float vec_max<uint16_t, 16>(const uint4* r) { return VecMaxBf16<16>::run(r); }
+
+// Fold N raw 16-byte vectors into (m, s): the max first (one rescale of s
+// when it rises), then exp(z - m) of every element with the exponent
+// argument z log2e - m log2e formed two elements per FMA and the terms summed
+// two per add.  Same arithmetic as ms_fold (fp32 FMA, ex2.approx, fp32 sums);
+// about half the instructions per element.
+template <typename T, int N>
+__device__ __forceinline__ void ms_fold_vecs(MS& a, const uint4* r) {
+  const float vm = vec_max<T, N>(r);
+  if (vm > a.m) {
+    a.s *= ex2_approx((a.m - vm) * kLog2e);
+    a.m = vm;
+  }
+  const float nml = (a.m == -INFINITY) ? 0.f : -a.m * kLog2e;  // all -inf so far: terms are 0
+  const uint64_t l2e = f32x2(kLog2e, kLog2e), off = f32x2(nml, nml);
+  uint64_t acc = f32x2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+      for (int k = 0; k < 4; k += 2) {
+        float e0, e1;
+        f32x2_split(fma_f32x2(f32x2(__uint_as_float(w[k]), __uint_as_float(w[k + 1])), l2e, off), e0, e1);
+        acc = add_f32x2(acc, f32x2(ex2_approx(e0), ex2_approx(e1)));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float e0, e1;
+        f32x2_split(fma_f32x2(f32x2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u)), l2e, off),
+                    e0, e1);
+        acc = add_f32x2(acc, f32x2(ex2_approx(e0), ex2_approx(e1)));
+      }
+    }
+  }
+  float s0, s1;
+  f32x2_split(acc, s0, s1);
+  a.s += s0 + s1;
+}
+
 template <int NT>
 __device__ __forceinline__ MS block_allreduce_to0(MS a, MS* s_part) {
   a = ms_warp_allreduce(a);
@@ -108,32 +222,22 @@ struct KSum {
   }
 };
 
-// Deterministic mean of row_loss[0..T) (16-byte aligned): called by every
-// block that produced losses once they are stored; the last of `nwriters`
-// blocks sums them and writes *loss, then clears the ticket.  The summation
-// order is fixed and independent of the block size: 256 virtual lanes each
-// take every 256th float4 in index order (compensated fp32, 16 or 8 loads
-// in flight); warp 0 then folds 8 lane sums per lane (compensated) and finishes
+// Deterministic mean of row_loss[0..T) (16-byte aligned), computed by the
+// whole calling block and written to *loss by thread 0.  The summation order
+// is fixed and independent of the block size: 256 virtual lanes each take
+// every 256th float4 in index order (compensated fp32, 16 or 8 loads in
+// flight); warp 0 then folds 8 lane sums per lane (compensated) and finishes
 // with a butterfly whose partners add the same two values.  No fp64: its rate
 // on this part is a small fraction of fp32 and a serial fp64 tail costs tens
 // of microseconds.  With a keep mask (uint8 per row, may be null) the divisor
 // is the number of kept rows (a mean over no row is 0); left-out rows must
-// already hold 0 in row_loss.
-__device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, float* loss, Ctrl* ctrl, uint32_t nwriters,
-                                          const uint8_t* keep = nullptr, float* inv_count_out = nullptr) {
+// already hold 0 in row_loss.  Loads bypass L1 (the rows were written by
+// other blocks or another grid).
+__device__ __forceinline__ void mean_sum(const float* row_loss, int64_t T, float* loss, const uint8_t* keep = nullptr,
+                                         float* inv_count_out = nullptr) {
   constexpr int kVL = 256;
-  __shared__ uint32_t s_last;
   __shared__ float s_part[kVL];
   __shared__ int64_t s_cnt[kVL];
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const uint32_t prev = atomicAdd(&ctrl->ticket, 1u);
-    s_last = (prev == nwriters - 1) ? 1u : 0u;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
   const int64_t n4 = T / 4;
   const float4* v4 = reinterpret_cast<const float4*>(row_loss);
   for (int j = threadIdx.x; j < kVL; j += blockDim.x) {
@@ -188,9 +292,30 @@ __device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, floa
       const int64_t count = keep ? n : T;
       *loss = count > 0 ? v / static_cast<float>(count) : 0.f;
       if (inv_count_out) *inv_count_out = count > 0 ? 1.f / static_cast<float>(count) : 0.f;
-      ctrl->ticket = 0u;
-      __threadfence();
     }
+  }
+}
+
+// The same mean, taken inside a grid whose `nwriters` blocks each produced
+// some of the rows: called by every such block once its rows are stored; the
+// last block to arrive (atomic ticket, no spin) computes the mean and clears
+// the ticket.
+__device__ __forceinline__ void mean_tail(const float* row_loss, int64_t T, float* loss, Ctrl* ctrl, uint32_t nwriters,
+                                          const uint8_t* keep = nullptr, float* inv_count_out = nullptr) {
+  __shared__ uint32_t s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t prev = atomicAdd(&ctrl->ticket, 1u);
+    s_last = (prev == nwriters - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  mean_sum(row_loss, T, loss, keep, inv_count_out);
+  if (threadIdx.x == 0) {
+    ctrl->ticket = 0u;
+    __threadfence();
   }
 }
 

@@ -1,10 +1,18 @@
 """Host-side helpers of the multi-process (one process per GPU) mode.
 
-The losses shard by tokens with no data exchange: every row's loss depends on
-that row alone, so N processes each run the kernels on their own token slice.
-What crosses processes is scalar bookkeeping only:
+Token sharding: every row's loss depends on that row alone, so N processes
+each run the kernels on their own token slice, and what crosses processes is
+scalar bookkeeping only:
   * the global mean of a token-sharded batch, from each rank's (sum, count);
   * timing (max over ranks) and barriers for the benchmark.
+
+Vocab sharding (tensor parallelism, page "Vocab-parallel cross-entropy,
+Megatron layout": each rank holds the logits of its own vocab range): each
+rank reduces its shard to per-token partials (ce_partials_sbv_bf16), one
+all-gather puts every rank's partials on every rank in rank order, and each
+rank merges them into the per-token losses (ce_merge_partials).  12 bytes
+per token per rank cross the link; the logits never do.
+
 These run over any torch.distributed backend (NCCL between GPUs, gloo on CPU).
 """
 from __future__ import annotations
@@ -41,3 +49,39 @@ def max_over_ranks(x: float, group=None) -> float:
     t = torch.tensor([float(x)], dtype=torch.float64, device=_device_of(group))
     dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
     return float(t.item())
+
+
+def shard_vocab(V: int, rank: int, world: int) -> tuple[int, int]:
+    """(vocab_start, width) of `rank`'s contiguous vocab shard: the shards
+    cover [0, V) in rank order, widths differ by at most one."""
+    lo, hi = shard_rows(V, rank, world)
+    return lo, hi - lo
+
+
+def gather_partials(part_local: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather of every rank's shard partials [3, ...] into [world, 3, ...]
+    in rank order: the layout ce_merge_partials reads.  One collective."""
+    world = dist.get_world_size(group)
+    part_local = part_local.contiguous()
+    shape = tuple(part_local.shape)
+    # concatenated along the first dimension (the form every backend takes), viewed per rank
+    out = torch.empty((world * shape[0],) + shape[1:], dtype=part_local.dtype, device=part_local.device)
+    dist.all_gather_into_tensor(out, part_local, group=group)
+    return out.view((world,) + shape)
+
+
+def vocab_parallel_ce(logits_local, target, vocab_start: int, V: int, group=None, partials=None, gathered=None):
+    """Per-token Megatron-layout cross-entropy [S, B] of logits whose vocab is
+    sharded over the ranks of `group`: this rank holds the columns
+    [vocab_start, vocab_start + V_local) of the global vocab V, as bf16
+    [S, B, V_local]; target [S, B] holds global indices (the same on every
+    rank).  Every rank returns the same losses."""
+    from lm_head_online_gb300 import ce_merge_partials, ce_partials_sbv_bf16
+
+    part = ce_partials_sbv_bf16(logits_local, target, vocab_start, partials=partials)
+    if gathered is None:
+        allp = gather_partials(part, group)
+    else:   # caller-owned [world, 3, S, B] buffer
+        dist.all_gather_into_tensor(gathered.view((-1,) + tuple(part.shape[1:])), part, group=group)
+        allp = gathered
+    return ce_merge_partials(allp, target, V)

@@ -185,3 +185,19 @@ def test_backward_workspace_sizes(lib):
     assert lmho.fljsd_bwd_workspace_bytes(1024, H, V) >= lmho.fljsd_workspace_bytes(1024, H, V) + 2 * 1024 * V
     c, cb = lmho.flce_cpo_workspace_bytes(2, 1024, H, V), lmho.flce_cpo_bwd_workspace_bytes(2, 1024, H, V)
     assert c >= lmho.flce_workspace_bytes(2048, H, V) and cb >= lmho.flce_bwd_workspace_bytes(2048, H, V)
+
+
+def test_vocab_parallel_argument_checks(lib):
+    # ce_partials_sbv_bf16(logits_local, target, S, B, V_local, vocab_start, partials, stream)
+    assert lib.ce_partials_sbv_bf16(None, B, 2, 2, 8, 0, C, None) == 1          # null logits
+    assert lib.ce_partials_sbv_bf16(A, B, 0, 2, 8, 0, C, None) == 1             # S = 0
+    assert lib.ce_partials_sbv_bf16(A, B, 2, 2, 0, 0, C, None) == 1             # V_local = 0
+    assert lib.ce_partials_sbv_bf16(A, B, 2, 2, 8, -1, C, None) == 1            # negative vocab start
+    assert lib.ce_partials_sbv_bf16(A, B, 2, 2, 8, 16, A + 8, None) == 2        # partials over logits
+    assert lib.ce_partials_sbv_bf16(A, B, 2, 2, 8, 16, B + 24, None) == 2       # partials over target
+    # ce_merge_partials(partials, shards, target, S, B, V, loss, stream)
+    assert lib.ce_merge_partials(None, 2, B, 2, 2, 16, C, None) == 1
+    assert lib.ce_merge_partials(A, 0, B, 2, 2, 16, C, None) == 1               # no shard
+    assert lib.ce_merge_partials(A, 2, B, 2, 2, 0, C, None) == 1                # V = 0
+    assert lib.ce_merge_partials(A, 2, B, 2, 2, 16, A + 80, None) == 2          # loss inside partials
+    assert lib.ce_merge_partials(A, 2, B, 2, 2, 16, B, None) == 2               # loss over target

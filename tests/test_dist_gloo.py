@@ -3,10 +3,12 @@
 * Token sharding (what `bench.py --gpus N` runs): each rank takes a
   contiguous token slice; the per-rank means combine into the global mean.
 * Vocab-parallel cross-entropy (page "Vocab-parallel cross-entropy, Megatron
-  layout": vocab sharded over tensor-parallel ranks; only TP = 1 is built):
-  each rank reduces its vocab shard to per-token (max, sum of exp, target
-  logit or -inf) and one all-gather plus a fixed-order merge gives the
-  unsharded loss.  This checks the merge algebra the design relies on.
+  layout": vocab sharded over tensor-parallel ranks): each rank reduces its
+  vocab shard to per-token (max, sum of exp, target logit or -inf),
+  dist.gather_partials all-gathers them in rank order, and the merge gives
+  the unsharded loss.  The ranks' reductions and the merge here are the
+  oracle's (no GPU); the GPU kernels of the same steps are checked against
+  the oracle in test_gpu_vp.py.
 """
 import math
 import os
@@ -92,34 +94,37 @@ def test_token_sharded_mean_over_gloo_ranks():
 
 
 def _vocab_parallel(rank, world):
-    T, V = 9, 1001
-    z = gen.normal_f64(4, 0, (T, V), sigma=3.0)
-    t = gen.targets(4, 1, (T,), V)
-    lo, hi = lmdist.shard_rows(V, rank, world)
-    shard = z[:, lo:hi]
-    m = shard.max(axis=1)
-    s = np.exp(shard - m[:, None]).sum(axis=1)
-    own = (t >= lo) & (t < hi)
-    zt = np.where(own, z[np.arange(T), np.clip(t, lo, hi - 1)], -np.inf)
+    """Each rank: the oracle's partials of its own vocab shard (the rank's
+    local logits only), the exchange through dist.gather_partials, and the
+    oracle's merge of the gathered block."""
+    S, B, V = 5, 3, 1001
+    z = gen.normal_bf16_bits(4, 0, (S, B, V), sigma=3.0)
+    t = gen.targets(4, 1, (S, B), V)
+    v0, w = lmdist.shard_vocab(V, rank, world)
+    local = np.ascontiguousarray(z[..., v0:v0 + w])
+    m, s, zt = oracle.ce_partials_bf16(local, t, v0)
     part = torch.from_numpy(np.stack([m, s, zt]))
-    gathered = [torch.empty_like(part) for _ in range(world)]
-    dist.all_gather(gathered, part)
-    # fixed-order merge of the per-rank (max, sum, target logit) triples
-    M = np.full(T, -np.inf)
-    S = np.zeros(T)
-    ZT = np.full(T, -np.inf)
-    for g in gathered:
-        gm, gs, gz = g.numpy()
-        new = np.maximum(M, gm)
-        S = S * np.exp(M - new) + gs * np.exp(gm - new)
-        M = new
-        ZT = np.maximum(ZT, gz)
-    return M + np.log(S) - ZT
+    gathered = lmdist.gather_partials(part).numpy()
+    assert gathered.shape == (world, 3, S, B)
+    np.testing.assert_array_equal(gathered[rank], part.numpy())   # rank order
+    return oracle.ce_merge(gathered[:, 0], gathered[:, 1], gathered[:, 2], t, V)
 
 
-def test_vocab_parallel_merge_over_gloo_ranks():
-    out = spawn(_vocab_parallel)
-    T, V = 9, 1001
-    _, want = oracle.ce_f64(gen.normal_f64(4, 0, (T, V), sigma=3.0), gen.targets(4, 1, (T,), V))
+@pytest.mark.parametrize("world", [2, 3])
+def test_vocab_parallel_exchange_over_gloo_ranks(world):
+    out = spawn(_vocab_parallel, world=world)
+    S, B, V = 5, 3, 1001
+    want = oracle.ce_sbv_bf16(gen.normal_bf16_bits(4, 0, (S, B, V), sigma=3.0), gen.targets(4, 1, (S, B), V))
     for rank, loss in out.items():
         np.testing.assert_allclose(loss, want, rtol=1e-12, atol=1e-12)
+
+
+def test_shard_vocab_covers_in_rank_order():
+    for V in (1, 7, 128256):
+        for world in (1, 2, 3, 8):
+            if V < world:
+                continue
+            shards = [lmdist.shard_vocab(V, r, world) for r in range(world)]
+            assert shards[0][0] == 0 and sum(w for _, w in shards) == V
+            for (a, wa), (b, _) in zip(shards, shards[1:]):
+                assert a + wa == b
