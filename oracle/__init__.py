@@ -88,6 +88,8 @@ def _load():
             lib.oracle_ce_partials_bf16.restype = None
             lib.oracle_ce_merge.argtypes = [vp, vp, vp, i64, vp, i64, i64, vp]
             lib.oracle_ce_merge.restype = None
+            lib.oracle_fljsd_dz_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, dbl, vp, vp]
+            lib.oracle_fljsd_dz_bf16.restype = None
             lib.oracle_logits_bf16.argtypes = [vp, vp, i64, i64, i64, vp]
             lib.oracle_logits_bf16.restype = None
             _lib = lib
@@ -330,6 +332,27 @@ def fljsd_grad_f64(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, scale=1
 def fljsd_grad_bf16(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, scale=1.0):
     """Student gradients (dxs, dWs) of scale * fused JSD from bf16 bits."""
     return _fljsd_grad(_load().oracle_fljsd_grad_bf16, np.uint16, xs, Ws, xt, Wt, beta, temperature, keep, scale)
+
+
+def fljsd_dz_bf16(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, scale=1.0):
+    """The student's dZs [T, V] (fp64, unrounded) of scale * fused linear + JSD
+    (bf16 bit inputs): the operand of its gradient products.  Returns
+    (dZs, g beta P), the second being the factor of dZs besides
+    ln P - ln M - KL(P || M) (g = scale / (n_kept temperature))."""
+    xs, p1 = _c(xs, np.uint16)
+    Ws, p2 = _c(Ws, np.uint16)
+    xt, p3 = _c(xt, np.uint16)
+    Wt, p4 = _c(Wt, np.uint16)
+    T, H = xs.shape
+    V = Ws.shape[0]
+    pk = None
+    if keep is not None:
+        keep, pk = _c(keep, np.uint8)
+    dz = np.empty((T, V), np.float64)
+    gbp = np.empty((T, V), np.float64)
+    _load().oracle_fljsd_dz_bf16(p1, p2, p3, p4, T, H, V, float(beta), float(temperature), pk, float(scale),
+                                 dz.ctypes.data, gbp.ctypes.data)
+    return dz, gbp
 
 
 def logits_bf16(x_bits, W_bits):

@@ -443,15 +443,27 @@ double oracle_fljsd_ex_f64(const double* xs, const double* Ws, const double* xt,
 //   dJSD/dP_v = beta ln(P_v / M_v), so through the softmax
 //   dzs_v = (scale / (n_kept tau)) beta P_v (ln P_v - ln M_v - KL(P || M)),
 //   dxs = dZs Ws [T, H],  dWs = dZs^T xs [V, H]; left-out tokens give 0 rows.
-void oracle_fljsd_grad_f64(const double* xs, const double* Ws, const double* xt, const double* Wt, int64_t T,
-                           int64_t H, int64_t V, double beta, double tau, const uint8_t* keep, double scale,
-                           double* dxs, double* dWs) {
+}  // extern "C"
+
+namespace {
+// The student's dZs [T, V] of scale * (fused linear + JSD mean over kept
+// tokens) on fp64 inputs (the definition in the comment above); when gbp is
+// not null it also receives g beta P [T, V], the factor dZs carries besides
+// (ln P - ln M - KL(P || M)).
+void fljsd_dz_f64(const double* xs, const double* Ws, const double* xt, const double* Wt, int64_t T, int64_t H,
+                  int64_t V, double beta, double tau, const uint8_t* keep, double scale, double* dz,
+                  double* gbp = nullptr) {
   int64_t kept = 0;
   for (int64_t i = 0; i < T; ++i) kept += (!keep || keep[i]) ? 1 : 0;
   const double g = kept ? scale / (static_cast<double>(kept) * tau) : 0.0;
-  std::vector<double> zs(V), zt(V), lp(V), lq(V), dz(static_cast<size_t>(T) * V, 0.0);
+  std::vector<double> zs(V), zt(V), lp(V), lq(V), lm(V);
   for (int64_t i = 0; i < T; ++i) {
-    if (keep && !keep[i]) continue;
+    if (keep && !keep[i]) {
+      for (int64_t v = 0; v < V; ++v) dz[i * V + v] = 0.0;
+      if (gbp)
+        for (int64_t v = 0; v < V; ++v) gbp[i * V + v] = 0.0;
+      continue;
+    }
     for (int64_t v = 0; v < V; ++v) {
       double a = 0.0, b = 0.0;
       for (int64_t k = 0; k < H; ++k) {
@@ -464,13 +476,24 @@ void oracle_fljsd_grad_f64(const double* xs, const double* Ws, const double* xt,
     log_softmax_row(zs.data(), V, lp.data());
     log_softmax_row(zt.data(), V, lq.data());
     double kl = 0.0;
-    std::vector<double> lm(V);
     for (int64_t v = 0; v < V; ++v) {
       lm[v] = std::log(beta * std::exp(lp[v]) + (1.0 - beta) * std::exp(lq[v]));
       kl += std::exp(lp[v]) * (lp[v] - lm[v]);
     }
     for (int64_t v = 0; v < V; ++v) dz[i * V + v] = g * beta * std::exp(lp[v]) * (lp[v] - lm[v] - kl);
+    if (gbp)
+      for (int64_t v = 0; v < V; ++v) gbp[i * V + v] = g * beta * std::exp(lp[v]);
   }
+}
+}  // namespace
+
+extern "C" {
+
+void oracle_fljsd_grad_f64(const double* xs, const double* Ws, const double* xt, const double* Wt, int64_t T,
+                           int64_t H, int64_t V, double beta, double tau, const uint8_t* keep, double scale,
+                           double* dxs, double* dWs) {
+  std::vector<double> dz(static_cast<size_t>(T) * V, 0.0);
+  fljsd_dz_f64(xs, Ws, xt, Wt, T, H, V, beta, tau, keep, scale, dz.data());
   for (int64_t i = 0; i < T; ++i)
     for (int64_t k = 0; k < H; ++k) {
       double acc = 0.0;
@@ -498,6 +521,23 @@ void oracle_fljsd_grad_bf16(const uint16_t* xs16, const uint16_t* Ws16, const ui
     Wt[i] = bf16_to_double(Wt16[i]);
   }
   oracle_fljsd_grad_f64(xs.data(), Ws.data(), xt.data(), Wt.data(), T, H, V, beta, tau, keep, scale, dxs, dWs);
+}
+
+// The student's dZs [T, V] (fp64) from bf16 inputs (widened exactly): the
+// operand the gradient products multiply, before any rounding; and g beta P.
+void oracle_fljsd_dz_bf16(const uint16_t* xs16, const uint16_t* Ws16, const uint16_t* xt16, const uint16_t* Wt16,
+                          int64_t T, int64_t H, int64_t V, double beta, double tau, const uint8_t* keep,
+                          double scale, double* dz, double* gbp) {
+  std::vector<double> xs(static_cast<size_t>(T) * H), xt(xs.size()), Ws(static_cast<size_t>(V) * H), Wt(Ws.size());
+  for (size_t i = 0; i < xs.size(); ++i) {
+    xs[i] = bf16_to_double(xs16[i]);
+    xt[i] = bf16_to_double(xt16[i]);
+  }
+  for (size_t i = 0; i < Ws.size(); ++i) {
+    Ws[i] = bf16_to_double(Ws16[i]);
+    Wt[i] = bf16_to_double(Wt16[i]);
+  }
+  fljsd_dz_f64(xs.data(), Ws.data(), xt.data(), Wt.data(), T, H, V, beta, tau, keep, scale, dz, gbp);
 }
 
 // softplus(u) = ln(1 + e^u), and the logistic sigmoid, both without overflow.
