@@ -260,7 +260,9 @@ def time_back_to_back(fns, torch, warmup, steps):
 def small_ce(lmho, torch, dev, seed, pk, steps=50):
     """The smallest CE workloads, each timed alone two ways (see above).
     The roofline uses the back-to-back time; the flushed per-call time, which
-    adds a fixed event and launch cost of about 3 us, is reported beside it."""
+    adds a fixed event and launch cost of about 3 us, is reported beside it,
+    and so is the back-to-back time of a bare read of the same bytes with the
+    same loads (lmho_probe_read): the floor at that size."""
     import gen
     thr = os.cpu_count() or 1
     flush = torch.ones(128 << 20, dtype=torch.float32, device=dev)
@@ -271,7 +273,8 @@ def small_ce(lmho, torch, dev, seed, pk, steps=50):
             t = torch.from_numpy(gen.targets(seed, gen.STREAM_TARGET, (T,), V, threads=thr)).to(dev)
             ws = lmho.workspace(lmho.ce_workspace_bytes(T, V), dev)
             loss = torch.empty(1, device=dev)
-            fns = [lambda zz=zz: lmho.ce_fwd_f32(zz, t, loss=loss, ws=ws) for zz in rotating_copies(z, torch)]
+            copies = rotating_copies(z, torch)
+            fns = [lambda zz=zz: lmho.ce_fwd_f32(zz, t, loss=loss, ws=ws) for zz in copies]
             nbytes, key, shape = rl.ce_flat_bytes(T, V), f"ce_fwd_f32.T{T}_V{V}", f"fp32[{T},{V}]"
         else:
             z = torch.empty((T, 4, V), dtype=torch.bfloat16)
@@ -279,21 +282,29 @@ def small_ce(lmho, torch, dev, seed, pk, steps=50):
             z = z.to(dev)
             t = torch.from_numpy(gen.targets(seed, gen.STREAM_TARGET, (T, 4), V, threads=thr)).to(dev)
             loss = torch.empty((T, 4), device=dev)
-            fns = [lambda zz=zz: lmho.ce_fwd_sbv_bf16(zz, t, loss=loss) for zz in rotating_copies(z, torch)]
+            copies = rotating_copies(z, torch)
+            fns = [lambda zz=zz: lmho.ce_fwd_sbv_bf16(zz, t, loss=loss) for zz in copies]
             nbytes, key, shape = rl.ce_sbv_bytes(T, 4, V), f"ce_fwd_sbv_bf16.S{T}_B4_V{V}", f"bf16[{T},4,{V}]"
         b2b = time_back_to_back(fns, torch, 5, steps)
         fl = time_flushed(fns, torch, 5, steps, flush)
+        # the bare read of the same bytes with the same loads (nothing computed)
+        seg = z.shape[-1] * z.element_size()
+        probe_out = torch.empty(z.numel() * z.element_size() // seg, dtype=torch.int32, device=dev)
+        reads = [lambda c=c: lmho.probe_read(c, seg, out=probe_out) for c in copies]
+        floor = time_back_to_back(reads, torch, 5, steps)
         med = float(np.median(fl))
         gbs = nbytes / (b2b * 1e-6) / 1e9
         ops[key] = {"shape": shape, "bytes": nbytes, "copies": len(fns),
                     "us_back_to_back": round(b2b, 2), "GB/s_back_to_back": round(gbs, 1),
+                    "us_bare_read_back_to_back": round(floor, 2),
+                    "frac_of_bare_read": round(floor / b2b, 4),
                     "us_flushed_median": round(med, 2), "us_flushed_p10": round(float(np.percentile(fl, 10)), 2),
                     "GB/s_flushed": round(nbytes / (med * 1e-6) / 1e9, 1),
                     "frac_flushed": round(nbytes / (med * 1e-6) / 1e9 / pk["hbm"], 4)}
         roofs[key] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                       "frac": round(gbs / pk["hbm"], 4), "traffic": None,
                       "timing": f"back to back over {len(fns)} copies (> 3x L2), mean per call"}
-        del fns, z
+        del fns, reads, copies, z
         torch.cuda.empty_cache()
     return ops, roofs, 2 * steps * sum(2 if n == "ce_fwd_f32" else 1 for n, _, _ in SMALL_CE)
 

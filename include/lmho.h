@@ -86,9 +86,10 @@ int ce_fwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
 
 /* ------------------------------------------------------------------------
  * ce_fwd_f32 without a caller workspace, for callers that cannot allocate
- * device memory (e.g. while a CUDA graph is being captured, or under a fixed
- * device-memory budget owned by someone else).  The operation pages have no
- * counterpart of this entry point: it is a library convenience.
+ * device memory: a process that reserved its device-memory pool up front and
+ * must not grow its footprint, a plug-in running inside another framework's
+ * allocator, a binding with no device allocator to hand.  The operation pages
+ * have no counterpart of this entry point: it is a library convenience.
  *
  * Same operation, arguments, result and kernels as ce_fwd_f32, except that
  * the per-token losses and the control words live in a scratch array inside
@@ -96,12 +97,13 @@ int ce_fwd_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
  * GPU which loads the library holds until the process exits.
  *   - T is limited to 65536 tokens; larger T returns LMHO_ERR_INVALID_ARG.
  *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating routine.
- *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture on that device.
+ *   - The first call on a device (and the first after that device's context
+ *     has been replaced, e.g. by cudaDeviceReset) looks up the array's device
+ *     address with that device current and caches it; make that first call
+ *     before any stream capture on that device.
  *   - Every call on a device shares the one array, which keeps the previous
  *     call's contents; each call first clears the control words it needs at
- *     zero (one cudaMemsetAsync on `stream`, then one kernel).  Calls that
+ *     zero (one cudaMemsetAsync on `stream`, then the kernels).  Calls that
  *     overlap on the GPU (other streams, other threads) race on the array and
  *     give undefined results: serialise them.
  * ------------------------------------------------------------------------ */
@@ -376,6 +378,17 @@ int lmho_set_raster_group(int group_m);
  * (log-sum-exp pass, finaliser, divergence pass, finaliser).  Calls made by
  * other threads are not affected.  Pass (NULL, 0) to turn it off. */
 void lmho_set_launch_events(void* const* events, int n);
+
+/* Bandwidth probe (a measurement aid; the operation pages have no such
+ * operation): reads `segments` consecutive segments of segment_bytes (a
+ * multiple of 16; data 16-byte aligned) with exactly the memory access of the
+ * warp-per-row cross-entropy kernel (two-warp blocks, a warp per segment,
+ * 16-byte streaming loads, 16 per lane in flight) and writes the XOR of each
+ * segment's 32-bit words to out[segments] (uint32, device).  It computes
+ * nothing else, so its time is the read-once floor that a cross-entropy call
+ * over rows of that size can approach on this device.  One kernel launch. */
+int lmho_probe_read(const void* data, int64_t segments, int64_t segment_bytes, uint32_t* out,
+                    void* stream);
 
 /* Upper bound, in nanoseconds, of every in-kernel wait of later calls
  * (default 2e9).  Process-wide. */

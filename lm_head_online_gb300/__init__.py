@@ -38,7 +38,7 @@ EXPORTS = (
     "flce_workspace_bytes", "flce_fwd_bf16", "flce_bwd_workspace_bytes", "flce_fwd_bwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "fljsd_bwd_workspace_bytes", "fljsd_fwd_bwd_bf16",
     "flce_cpo_workspace_bytes", "flce_cpo_fwd_bf16", "flce_cpo_bwd_workspace_bytes", "flce_cpo_fwd_bwd_bf16",
-    "lmho_ws_status", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
+    "lmho_ws_status", "lmho_probe_read", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
 
 CE_VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "cta512": 3, "cluster2": 4, "cluster4": 5, "cluster8": 6, "bulk": 7}
@@ -110,6 +110,8 @@ def load():
         lib.flce_cpo_fwd_bwd_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, f32, f32, f32, vp, vp, vp, vp, vp, sz,
                                               vp]
         lib.flce_cpo_fwd_bwd_bf16.restype = ci
+        lib.lmho_probe_read.argtypes = [vp, i64, i64, vp, vp]
+        lib.lmho_probe_read.restype = ci
         lib.lmho_ws_status.argtypes = [vp, sz, vp]
         lib.lmho_ws_status.restype = ci
         lib.lmho_set_ce_variant.argtypes = [ci]
@@ -156,6 +158,17 @@ def _dev(t: torch.Tensor, name: str, dtype, ndim=None):
     return t.data_ptr()
 
 
+def _on(*tensors):
+    """Context in which a call runs: the device of its tensors, which must all
+    be on one device (the kernels are launched on the current device, with the
+    current stream of that device)."""
+    dev = tensors[0].device
+    for t in tensors[1:]:
+        if t is not None and t.device != dev:
+            raise ValueError(f"tensors on different devices: {dev} and {t.device}")
+    return torch.cuda.device(dev)
+
+
 def workspace(nbytes: int, device=None) -> torch.Tensor:
     """Zero-filled device workspace (torch allocations are 512-byte aligned)."""
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
@@ -191,25 +204,28 @@ def ce_fwd_f32(logits, target, loss=None, ws=None, stream=None):
         loss = torch.empty(1, dtype=torch.float32, device=logits.device)
     if ws is None:
         ws = workspace(lib.ce_workspace_bytes(T, V), logits.device)
-    _check(lib.ce_fwd_f32(pl, pt, T, V, _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8),
-                          ws.numel(), _stream(stream)), "ce_fwd_f32")
+    with _on(logits, target, loss, ws):
+        _check(lib.ce_fwd_f32(pl, pt, T, V, _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8),
+                              ws.numel(), _stream(stream)), "ce_fwd_f32")
     return loss
 
 
 def ce_fwd_f32_noalloc(logits, target, loss, stream=None):
-    """ce_fwd_f32 for callers that cannot allocate device memory: no
-    workspace argument, the library's own scratch (at most 65536 tokens) is
-    used instead.  ``loss`` (fp32 [1], on the device) must be supplied by the
-    caller, since this call allocates nothing.  Calls that overlap on the GPU
-    share the scratch and race: serialise them."""
+    """ce_fwd_f32 for callers that cannot allocate device memory (a fixed
+    device-memory budget owned by someone else): no workspace argument, the
+    library's own scratch (at most 65536 tokens) is used instead.  ``loss``
+    (fp32 [1], on the device) must be supplied by the caller, since this call
+    allocates nothing.  Calls that overlap on the GPU share the scratch and
+    race: serialise them."""
     lib = load()
     pl = _dev(logits, "logits", torch.float32, 2)
     T, V = logits.shape
     pt = _dev(target, "target", torch.int64, 1)
     if target.shape[0] != T:
         raise ValueError("target must have T entries")
-    _check(lib.ce_fwd_f32_noalloc(pl, pt, T, V, _dev(loss, "loss", torch.float32), _stream(stream)),
-           "ce_fwd_f32_noalloc")
+    pd = _dev(loss, "loss", torch.float32)
+    with _on(logits, target, loss):
+        _check(lib.ce_fwd_f32_noalloc(pl, pt, T, V, pd, _stream(stream)), "ce_fwd_f32_noalloc")
     return loss
 
 
@@ -223,8 +239,9 @@ def ce_fwd_sbv_bf16(logits, target, loss=None, stream=None):
         raise ValueError("target must be [S, B]")
     if loss is None:
         loss = torch.empty((S, B), dtype=torch.float32, device=logits.device)
-    _check(lib.ce_fwd_sbv_bf16(pl, pt, S, B, V, _dev(loss, "loss", torch.float32), _stream(stream)),
-           "ce_fwd_sbv_bf16")
+    with _on(logits, target, loss):
+        _check(lib.ce_fwd_sbv_bf16(pl, pt, S, B, V, _dev(loss, "loss", torch.float32), _stream(stream)),
+               "ce_fwd_sbv_bf16")
     return loss
 
 
@@ -245,8 +262,9 @@ def ce_partials_sbv_bf16(logits_local, target, vocab_start, partials=None, strea
         partials = torch.empty((3, S, B), dtype=torch.float32, device=logits_local.device)
     if tuple(partials.shape) != (3, S, B):
         raise ValueError("partials must be [3, S, B]")
-    _check(lib.ce_partials_sbv_bf16(pl, pt, S, B, Vl, int(vocab_start), _dev(partials, "partials", torch.float32, 3),
-                                    _stream(stream)), "ce_partials_sbv_bf16")
+    with _on(logits_local, target, partials):
+        _check(lib.ce_partials_sbv_bf16(pl, pt, S, B, Vl, int(vocab_start), _dev(partials, "partials", torch.float32, 3),
+                                        _stream(stream)), "ce_partials_sbv_bf16")
     return partials
 
 
@@ -263,8 +281,9 @@ def ce_merge_partials(partials, target, V, loss=None, stream=None):
         raise ValueError("target must be [S, B]")
     if loss is None:
         loss = torch.empty((S, B), dtype=torch.float32, device=partials.device)
-    _check(lib.ce_merge_partials(pp, k, pt, S, B, int(V), _dev(loss, "loss", torch.float32, 2), _stream(stream)),
-           "ce_merge_partials")
+    with _on(partials, target, loss):
+        _check(lib.ce_merge_partials(pp, k, pt, S, B, int(V), _dev(loss, "loss", torch.float32, 2), _stream(stream)),
+               "ce_merge_partials")
     return loss
 
 
@@ -285,9 +304,10 @@ def ce_fwd_bwd_f32(logits, target, grad_scale=1.0, loss=None, dlogits=None, ws=N
         raise ValueError("dlogits must be [T, V]")
     if ws is None:
         ws = workspace(lib.ce_workspace_bytes(T, V), logits.device)
-    _check(lib.ce_fwd_bwd_f32(pl, pt, T, V, float(grad_scale), _dev(loss, "loss", torch.float32),
-                              _dev(dlogits, "dlogits", torch.float32), _dev(ws, "ws", torch.uint8), ws.numel(),
-                              _stream(stream)), "ce_fwd_bwd_f32")
+    with _on(logits, target, loss, dlogits, ws):
+        _check(lib.ce_fwd_bwd_f32(pl, pt, T, V, float(grad_scale), _dev(loss, "loss", torch.float32),
+                                  _dev(dlogits, "dlogits", torch.float32), _dev(ws, "ws", torch.uint8), ws.numel(),
+                                  _stream(stream)), "ce_fwd_bwd_f32")
     return loss, dlogits
 
 
@@ -310,9 +330,10 @@ def ce_fwd_bwd_sbv_bf16(logits, target, dloss=None, grad_scale=1.0, loss=None, d
         loss = torch.empty((S, B), dtype=torch.float32, device=logits.device)
     if dlogits is None:
         dlogits = torch.empty_like(logits)
-    _check(lib.ce_fwd_bwd_sbv_bf16(pl, pt, S, B, V, pd, float(grad_scale), _dev(loss, "loss", torch.float32),
-                                   _dev(dlogits, "dlogits", torch.bfloat16, 3), _stream(stream)),
-           "ce_fwd_bwd_sbv_bf16")
+    with _on(logits, target, loss, dlogits, dloss):
+        _check(lib.ce_fwd_bwd_sbv_bf16(pl, pt, S, B, V, pd, float(grad_scale), _dev(loss, "loss", torch.float32),
+                                       _dev(dlogits, "dlogits", torch.bfloat16, 3), _stream(stream)),
+               "ce_fwd_bwd_sbv_bf16")
     return loss, dlogits
 
 
@@ -338,8 +359,9 @@ def flce_fwd_bf16(x, W, target, loss=None, ws=None, stream=None):
         loss = torch.empty(1, dtype=torch.float32, device=x.device)
     if ws is None:
         ws = workspace(lib.flce_workspace_bytes(T, H, V), x.device)
-    _check(lib.flce_fwd_bf16(px, pw, pt, T, H, V, _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8),
-                             ws.numel(), _stream(stream)), "flce_fwd_bf16")
+    with _on(x, W, target, loss, ws):
+        _check(lib.flce_fwd_bf16(px, pw, pt, T, H, V, _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8),
+                                 ws.numel(), _stream(stream)), "flce_fwd_bf16")
     return loss
 
 
@@ -370,9 +392,10 @@ def flce_fwd_bwd_bf16(x, W, target, grad_scale=1.0, loss=None, dx=None, dW=None,
         dW = torch.empty((V, H), dtype=torch.float32, device=x.device)
     if ws is None:
         ws = workspace(lib.flce_bwd_workspace_bytes(T, H, V), x.device)
-    _check(lib.flce_fwd_bwd_bf16(px, pw, pt, T, H, V, float(grad_scale), _dev(loss, "loss", torch.float32),
-                                 _dev(dx, "dx", torch.float32, 2), _dev(dW, "dW", torch.float32, 2),
-                                 _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "flce_fwd_bwd_bf16")
+    with _on(x, W, target, loss, dx, dW, ws):
+        _check(lib.flce_fwd_bwd_bf16(px, pw, pt, T, H, V, float(grad_scale), _dev(loss, "loss", torch.float32),
+                                     _dev(dx, "dx", torch.float32, 2), _dev(dW, "dW", torch.float32, 2),
+                                     _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "flce_fwd_bwd_bf16")
     return loss, dx, dW
 
 
@@ -410,9 +433,10 @@ def flce_cpo_fwd_bf16(x, W, target, beta=0.1, alpha=1.0, loss=None, logps=None, 
         raise ValueError("logps must hold B floats, loss at least one")
     if ws is None:
         ws = workspace(lib.flce_cpo_workspace_bytes(B, S, H, V), x.device)
-    _check(lib.flce_cpo_fwd_bf16(px, pw, pt, B, S, H, V, float(beta), float(alpha), _dev(loss, "loss", torch.float32),
-                                 _dev(logps, "logps", torch.float32, 1), _dev(ws, "ws", torch.uint8), ws.numel(),
-                                 _stream(stream)), "flce_cpo_fwd_bf16")
+    with _on(x, W, target, loss, logps, ws):
+        _check(lib.flce_cpo_fwd_bf16(px, pw, pt, B, S, H, V, float(beta), float(alpha), _dev(loss, "loss", torch.float32),
+                                     _dev(logps, "logps", torch.float32, 1), _dev(ws, "ws", torch.uint8), ws.numel(),
+                                     _stream(stream)), "flce_cpo_fwd_bf16")
     return loss, logps
 
 
@@ -437,11 +461,12 @@ def flce_cpo_fwd_bwd_bf16(x, W, target, beta=0.1, alpha=1.0, grad_scale=1.0, los
         raise ValueError("output shapes: loss [1], logps [B], dx [B, S, H], dW [V, H]")
     if ws is None:
         ws = workspace(lib.flce_cpo_bwd_workspace_bytes(B, S, H, V), x.device)
-    _check(lib.flce_cpo_fwd_bwd_bf16(px, pw, pt, B, S, H, V, float(beta), float(alpha), float(grad_scale),
-                                     _dev(loss, "loss", torch.float32), _dev(logps, "logps", torch.float32, 1),
-                                     _dev(dx, "dx", torch.float32, 3), _dev(dW, "dW", torch.float32, 2),
-                                     _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)),
-           "flce_cpo_fwd_bwd_bf16")
+    with _on(x, W, target, loss, logps, dx, dW, ws):
+        _check(lib.flce_cpo_fwd_bwd_bf16(px, pw, pt, B, S, H, V, float(beta), float(alpha), float(grad_scale),
+                                         _dev(loss, "loss", torch.float32), _dev(logps, "logps", torch.float32, 1),
+                                         _dev(dx, "dx", torch.float32, 3), _dev(dW, "dW", torch.float32, 2),
+                                         _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)),
+               "flce_cpo_fwd_bwd_bf16")
     return loss, logps, dx, dW
 
 
@@ -461,8 +486,9 @@ def fljsd_fwd_bf16(xs, Ws, xt, Wt, beta=0.5, loss=None, ws=None, stream=None):
         loss = torch.empty(1, dtype=torch.float32, device=xs.device)
     if ws is None:
         ws = workspace(lib.fljsd_workspace_bytes(T, H, V), xs.device)
-    _check(lib.fljsd_fwd_bf16(p1, p2, p3, p4, T, H, V, float(beta), _dev(loss, "loss", torch.float32),
-                              _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "fljsd_fwd_bf16")
+    with _on(xs, Ws, xt, Wt, loss, ws):
+        _check(lib.fljsd_fwd_bf16(p1, p2, p3, p4, T, H, V, float(beta), _dev(loss, "loss", torch.float32),
+                                  _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "fljsd_fwd_bf16")
     return loss
 
 
@@ -490,9 +516,10 @@ def fljsd_fwd_bf16_ex(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, loss
         loss = torch.empty(1, dtype=torch.float32, device=xs.device)
     if ws is None:
         ws = workspace(lib.fljsd_workspace_bytes(T, H, V), xs.device)
-    _check(lib.fljsd_fwd_bf16_ex(p1, p2, p3, p4, T, H, V, float(beta), float(temperature), pk,
-                                 _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8), ws.numel(),
-                                 _stream(stream)), "fljsd_fwd_bf16_ex")
+    with _on(xs, Ws, xt, Wt, keep, loss, ws):
+        _check(lib.fljsd_fwd_bf16_ex(p1, p2, p3, p4, T, H, V, float(beta), float(temperature), pk,
+                                     _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8), ws.numel(),
+                                     _stream(stream)), "fljsd_fwd_bf16_ex")
     return loss
 
 
@@ -528,16 +555,34 @@ def fljsd_fwd_bwd_bf16(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, gra
         dWs = torch.empty((V, H), dtype=torch.float32, device=xs.device)
     if ws is None:
         ws = workspace(lib.fljsd_bwd_workspace_bytes(T, H, V), xs.device)
-    _check(lib.fljsd_fwd_bwd_bf16(p1, p2, p3, p4, T, H, V, float(beta), float(temperature), pk, float(grad_scale),
-                                  _dev(loss, "loss", torch.float32), _dev(dxs, "dxs", torch.float32, 2),
-                                  _dev(dWs, "dWs", torch.float32, 2), _dev(ws, "ws", torch.uint8), ws.numel(),
-                                  _stream(stream)), "fljsd_fwd_bwd_bf16")
+    with _on(xs, Ws, xt, Wt, keep, loss, dxs, dWs, ws):
+        _check(lib.fljsd_fwd_bwd_bf16(p1, p2, p3, p4, T, H, V, float(beta), float(temperature), pk, float(grad_scale),
+                                      _dev(loss, "loss", torch.float32), _dev(dxs, "dxs", torch.float32, 2),
+                                      _dev(dWs, "dWs", torch.float32, 2), _dev(ws, "ws", torch.uint8), ws.numel(),
+                                      _stream(stream)), "fljsd_fwd_bwd_bf16")
     return loss, dxs, dWs
 
 
 def row_losses(ws: torch.Tensor, T: int) -> torch.Tensor:
     """Per-token losses (or JSD) left in the first 4*T bytes of a workspace."""
     return ws[: 4 * T].view(torch.float32)
+
+
+def probe_read(data: torch.Tensor, segment_bytes: int, out=None, stream=None) -> torch.Tensor:
+    """Bandwidth probe: read `data` (contiguous, CUDA) in segments of
+    segment_bytes with the warp-per-row CE kernel's loads; returns the XOR of
+    each segment's words (uint32 as int32 [segments])."""
+    if not isinstance(data, torch.Tensor) or data.device.type != "cuda" or not data.is_contiguous():
+        raise TypeError("data must be a contiguous CUDA tensor")
+    nbytes = data.numel() * data.element_size()
+    if segment_bytes <= 0 or nbytes % segment_bytes:
+        raise ValueError("data must be a whole number of segments")
+    n = nbytes // segment_bytes
+    if out is None:
+        out = torch.empty(n, dtype=torch.int32, device=data.device)
+    _check(load().lmho_probe_read(data.data_ptr(), n, int(segment_bytes), _dev(out, "out", torch.int32, 1),
+                                  _stream(stream)), "lmho_probe_read")
+    return out
 
 
 def ws_status(ws, stream=None) -> int:

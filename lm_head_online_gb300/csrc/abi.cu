@@ -110,6 +110,8 @@ bool bulk_ok(const void* base, int64_t V, size_t elt) {
   return (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && row_bytes % 16 == 0 && row_bytes <= kCeBulkMaxRow;
 }
 
+}  // namespace
+
 CeConfig choose_ce(const void* base, int64_t rows, int64_t V, size_t elt, int num_sms) {
   CeConfig c{kCeCta, 256, 1};
   c.num_sms = num_sms;
@@ -141,6 +143,8 @@ CeConfig choose_ce(const void* base, int64_t rows, int64_t V, size_t elt, int nu
   }
   return c;
 }
+
+namespace {
 
 // ---------------------------------------------------------------- TMA maps
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -737,6 +741,17 @@ int flce_cpo_fwd_bwd_bf16(const uint16_t* x, const uint16_t* W, const int64_t* t
   const FusedGeometry g = geometry(T, H, V, kBN_CE);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_flce_fwd_bwd(m, target, g, grad_scale, loss, dx, dW, w, bw, L, &c));
+}
+
+int lmho_probe_read(const void* data, int64_t segments, int64_t segment_bytes, uint32_t* out, void* stream) {
+  if (!data || !out || segments <= 0 || segment_bytes <= 0 || segment_bytes % 16 != 0) return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(data) || segments > (int64_t(1) << 31) - 2) return LMHO_ERR_INVALID_ARG;
+  const Range in[1] = {rng(data, static_cast<size_t>(segments) * static_cast<size_t>(segment_bytes))};
+  const Range out_r[1] = {rng(out, 4 * static_cast<size_t>(segments))};
+  if (int a = check_alias(in, 1, out_r, 1)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  return cuda_status(launch_probe_read(data, segments, segment_bytes, out, static_cast<cudaStream_t>(stream)));
 }
 
 int lmho_ws_status(void* ws, size_t ws_bytes, void* stream) {

@@ -441,6 +441,32 @@ cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, in
   return cudaGetLastError();
 }
 
+// Bare read of `nseg` segments of `seg_vec` 16-byte vectors with the access of
+// the warp-per-row kernel (two-warp blocks, a warp per segment, 16 loads per
+// lane in flight, coalesced), folding nothing but an XOR per segment: the
+// read-once floor a cross-entropy call over rows of that size can approach.
+__global__ void __launch_bounds__(64, 16) probe_read_rows(const uint4* __restrict__ data, int64_t nseg,
+                                                          int64_t seg_vec, uint32_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 2 + (threadIdx.x >> 5);
+  if (r >= nseg) return;
+  const uint4* row = data + r * seg_vec;
+  uint32_t acc = 0;
+  for (int64_t q0 = 0; q0 < seg_vec; q0 += 32 * 16) {
+    uint4 v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int64_t q = q0 + u * 32 + lane;
+      v[u] = q < seg_vec ? ldg_stream_v4(row + q) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) acc ^= __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (lane == 0) out[r] = acc;
+}
+
 }  // namespace
 
 cudaError_t launch_ce_f32(const float* logits, const int64_t* target, int64_t T, int64_t V,
@@ -458,6 +484,14 @@ cudaError_t launch_ce_partials_bf16(const uint16_t* logits, const int64_t* targe
                                     int64_t v0, float* partials, const CeConfig& cfg, cudaStream_t st) {
   const PartialSink sink{partials, partials + rows, partials + 2 * rows, v0};
   return launch_rows<uint16_t>(logits, target, rows, V_local, sink, nullptr, nullptr, nullptr, cfg, st);
+}
+
+cudaError_t launch_probe_read(const void* data, int64_t nseg, int64_t seg_bytes, uint32_t* out, cudaStream_t st) {
+  launch_mark(0, st);
+  const unsigned nb = static_cast<unsigned>((nseg + 1) / 2);
+  probe_read_rows<<<nb, 64, 0, st>>>(static_cast<const uint4*>(data), nseg, seg_bytes / 16, out);
+  launch_mark(1, st);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_ce_merge(const float* partials, int64_t shards, const int64_t* target, int64_t rows, int64_t V,

@@ -37,6 +37,11 @@ struct CeConfig {
   uint32_t bulk_ring_bytes = 0;         // bulk kernel: ring size (0 = kCeBulkRingBytes)
 };
 
+// Row decomposition of a cross-entropy call over `rows` rows of V elements of
+// `elt` bytes starting at `base` (the automatic rule, or the process-wide
+// override of lmho_set_ce_variant).
+CeConfig choose_ce(const void* base, int64_t rows, int64_t V, size_t elt, int num_sms);
+
 // Largest row (bytes) the bulk-copy ring kernel takes: two stages must fit.
 constexpr uint32_t kCeBulkRingBytes = 200 * 1024;
 constexpr uint32_t kCeBulkMaxRow = kCeBulkRingBytes / 2;
@@ -55,6 +60,10 @@ cudaError_t launch_ce_partials_bf16(const uint16_t* logits, const int64_t* targe
                                     int64_t v0, float* partials, const CeConfig& cfg, cudaStream_t st);
 cudaError_t launch_ce_merge(const float* partials, int64_t shards, const int64_t* target, int64_t rows, int64_t V,
                             float* loss, int num_sms, cudaStream_t st);
+
+// Bandwidth probe: `nseg` segments of seg_bytes (a multiple of 16) read with
+// the warp-per-row kernel's loads; one XOR word per segment to out.
+cudaError_t launch_probe_read(const void* data, int64_t nseg, int64_t seg_bytes, uint32_t* out, cudaStream_t st);
 
 // Forward + backward (loss and gradient w.r.t. the logits), one HBM pass.
 // gscale: gradient weight per row (flat: grad_scale / T; per-token rows also

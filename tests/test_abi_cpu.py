@@ -201,3 +201,12 @@ def test_vocab_parallel_argument_checks(lib):
     assert lib.ce_merge_partials(A, 2, B, 2, 2, 0, C, None) == 1                # V = 0
     assert lib.ce_merge_partials(A, 2, B, 2, 2, 16, A + 80, None) == 2          # loss inside partials
     assert lib.ce_merge_partials(A, 2, B, 2, 2, 16, B, None) == 2               # loss over target
+
+
+def test_probe_read_argument_checks(lib):
+    # lmho_probe_read(data, segments, segment_bytes, out, stream)
+    assert lib.lmho_probe_read(None, 4, 64, C, None) == 1
+    assert lib.lmho_probe_read(A, 0, 64, C, None) == 1
+    assert lib.lmho_probe_read(A, 4, 24, C, None) == 1            # segment not whole 16-byte vectors
+    assert lib.lmho_probe_read(A + 8, 4, 64, C, None) == 1        # data not 16-byte aligned
+    assert lib.lmho_probe_read(A, 4, 64, A + 16, None) == 2       # out inside data

@@ -16,7 +16,7 @@ import torch
 
 import gen
 import oracle
-from tests.helpers import sample_rows, to_dev, to_dev_bf16
+from tests.helpers import tile_samples, sample_rows, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -100,12 +100,14 @@ def test_flce_bad_target_gives_nan(gpu_lib):
 @pytest.mark.parametrize("batch", [2, 16])
 def test_flce_full_size_sampled(gpu_lib, batch):
     """x bf16 [batch*1024, 4096] ~ N(0,1), W bf16 [128256, 4096] ~ N(0, 0.02^2):
-    24 sampled tokens against the oracle; mean against the kernel's own
-    per-token losses and the closed-form expectation ln V + H sigma_w^2 / 2."""
+    one token of every 128-token tile, the last token and both sides of every
+    raster-group boundary (groups of 32 tiles) against the oracle; mean
+    against the kernel's own per-token losses and the closed-form expectation
+    ln V + H sigma_w^2 / 2."""
     T, H, V = batch * 1024, 4096, 128256
     x, W, t = flce_inputs(0, T, H, V)
     m, rows = run_flce(gpu_lib, x, W, t)
-    idx = sample_rows(T, 22)
+    idx = tile_samples(T, groups=(32,), seed=batch)
     _, ref = oracle.flce_bf16(x[idx], W, t[idx])
     np.testing.assert_allclose(rows[idx], ref, rtol=RTOL_CE_TOKEN, atol=1e-5)
     assert m == pytest.approx(rows.mean(), rel=1e-6)
@@ -166,11 +168,13 @@ def test_fljsd_bounds_and_symmetry(gpu_lib):
 @pytest.mark.parametrize("T", [1024, 8192])
 def test_fljsd_full_size_sampled(gpu_lib, T):
     """Student/teacher bf16 [T, 4096] ~ N(0,1), heads [128256, 4096] ~ N(0, 0.02^2),
-    beta 0.5: 12 sampled tokens against the oracle."""
+    beta 0.5: one token of every 128-token tile, the last token and both sides
+    of every raster-group boundary of both passes (16 and 32 tiles) against
+    the oracle."""
     H, V = 4096, 128256
     xs, Ws, xt, Wt = jsd_inputs(0, T, H, V)
     m, rows = run_fljsd(gpu_lib, xs, Ws, xt, Wt)
-    idx = sample_rows(T, 10)
+    idx = tile_samples(T, groups=(16, 32), seed=T)
     _, ref = oracle.fljsd_bf16(xs[idx], Ws, xt[idx], Wt, 0.5)
     np.testing.assert_allclose(rows[idx], ref, rtol=RTOL_JSD_TOKEN, atol=ATOL_JSD_TOKEN)
     assert m == pytest.approx(rows.mean(), rel=1e-6)
