@@ -54,6 +54,10 @@
 #include "ptx.cuh"
 #include "rowstats.cuh"
 
+#ifndef LMHO_JSD_PACKED
+#define LMHO_JSD_PACKED 1
+#endif
+
 namespace lmho {
 namespace {
 
@@ -233,6 +237,33 @@ __device__ __forceinline__ float jsd_term2(float lp2, float lq2, float beta, flo
   const float u = w_lo * ex2_approx(-d);
   const float sv = u + w_hi;
   return ex2_approx(hi) * fmaf(sv, lg2_approx(sv), u * d);
+}
+
+// jsd_term2 for two pairs at once (columns j and j + 1 of a row): the FMA,
+// subtract, multiply and add steps on packed fp32 pairs (one instruction for
+// both), the max / selects and the three MUFU operations per pair unpacked.
+// Same arithmetic as jsd_term2; returns the sum of the two terms.
+__device__ __forceinline__ float jsd_term2_x2(uint64_t zs2, uint64_t zq2, uint64_t it2x2, uint64_t nls2,
+                                              uint64_t nlt2, float beta, float omb) {
+  float lp0, lp1, lq0, lq1;
+  f32x2_split(fma_f32x2(zs2, it2x2, nls2), lp0, lp1);
+  f32x2_split(fma_f32x2(zq2, it2x2, nlt2), lq0, lq1);
+  float df0, df1;
+  f32x2_split(sub_f32x2(f32x2(lp0, lp1), f32x2(lq0, lq1)), df0, df1);
+  const float d0 = fabsf(df0), d1 = fabsf(df1);
+  const float hi0 = fmaxf(lp0, lq0), hi1 = fmaxf(lp1, lq1);
+  const float wh0 = df0 >= 0.f ? beta : omb, wh1 = df1 >= 0.f ? beta : omb;
+  const float wl0 = df0 >= 0.f ? omb : beta, wl1 = df1 >= 0.f ? omb : beta;
+  float u0, u1;
+  f32x2_split(mul_f32x2(f32x2(wl0, wl1), f32x2(ex2_approx(-d0), ex2_approx(-d1))), u0, u1);
+  const uint64_t u = f32x2(u0, u1);
+  const uint64_t sv = add_f32x2(u, f32x2(wh0, wh1));
+  float s0, s1;
+  f32x2_split(sv, s0, s1);
+  const uint64_t inner = fma_f32x2(sv, f32x2(lg2_approx(s0), lg2_approx(s1)), mul_f32x2(u, f32x2(d0, d1)));
+  float t0, t1;
+  f32x2_split(mul_f32x2(f32x2(ex2_approx(hi0), ex2_approx(hi1)), inner), t0, t1);
+  return t0 + t1;
 }
 
 // The pieces of one generalized-JSD pair the backward needs: P = e^{lp} and
@@ -563,10 +594,18 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
           const int64_t col0 = n0 + cc * 16;
           if constexpr (MODE == kModeJSD) {
             if (col0 + 16 <= p.V) {
+#if LMHO_JSD_PACKED
+              const uint64_t i2 = f32x2(it2, it2), ns = f32x2(-ls2, -ls2), nt = f32x2(-lt2, -lt2);
+#pragma unroll
+              for (int j = 0; j < 16; j += 2)
+                jsd += jsd_term2_x2(f32x2(__uint_as_float(rs[j]), __uint_as_float(rs[j + 1])),
+                                    f32x2(__uint_as_float(rt[j]), __uint_as_float(rt[j + 1])), i2, ns, nt, beta, omb);
+#else
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 jsd += jsd_term2(fmaf(__uint_as_float(rs[j]), it2, -ls2), fmaf(__uint_as_float(rt[j]), it2, -lt2),
                                  beta, omb);
+#endif
             } else {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
