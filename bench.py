@@ -49,21 +49,28 @@ KERNELS_PER_STEP = 2 + 1 + 2 + 4   # ce_fwd_f32: row kernel + mean; sbv 1; flce 
 # Megatron bf16 [2048, 4, V] for V = 4096 and 8192.
 SMALL_CE = (("ce_fwd_f32", 16384, 4096), ("ce_fwd_sbv_bf16", 2048, 4096), ("ce_fwd_sbv_bf16", 2048, 8192))
 L2_BYTES = 129 * 2 ** 20
+# Host seconds of one timed oracle step, the same for the bench's cpu_baseline
+# leg and every step of the reference arm (so the two time the same sample).
+ORACLE_BUDGET_S = 6.0
 
 # DRAM bytes (read + write) per launch of each main kernel at the bench sizes,
-# from one ncu capture of a bench step (`ncu --metrics dram__bytes_read.sum,
-# dram__bytes_write.sum,gpu__time_duration.sum` over `bench.py --steps 2
-# --warmup 1 --no-e2e --no-cpu-baseline`, mean of the 3 launches; summary in
-# profiles/dram_traffic_bench_step.md).  They hold only for the kernel sources
-# they were taken from: a changed source makes the bench report null.
+# scaled from small-case ncu captures of the same kernel sources (their summaries
+# are under profiles/, named for the kernels and workloads):
+# the tensor-core passes were captured at T = 4096 and their traffic follows T
+# (W is re-read once per raster group of fixed token span): flce x 4 (T 16384),
+# the log-sum-exp and divergence passes x 2 (T 8192).  The row kernels read the
+# logits once (read / algorithmic = 1.0003 at V = 4096), so theirs is that ratio
+# times the full-size logits and targets, plus the per-token losses written.
+# The figures hold only for the sources they were taken from: a changed source
+# makes the bench report null.
 KERNEL_SOURCES = ("fused_linear.cu", "ce_rows.cu", "rowstats.cuh", "ptx.cuh", "lmho_internal.h")
-TRAFFIC_SOURCE_DIGEST = "ae85cd14e6e6127e"
+TRAFFIC_SOURCE_DIGEST = "de71b69dd76a6864"
 TRAFFIC_BYTES = {
-    "ce_fwd_f32.row_kernel_and_mean": 8590211243 + 243029,
-    "ce_fwd_sbv_bf16.row_kernel": 2147706283 + 351744,
-    "flce.tcgen05_gemm_ce": 4339754923 + 65928619,
-    "fljsd.tcgen05_gemm_lse": 4338453333 + 65594624,
-    "fljsd.tcgen05_gemm_jsd": 10289461675 + 32997035,
+    "ce_fwd_f32.row_kernel_and_mean": int((16384 * 131072 * 4 + 16384 * 8) * 1.0003) + 16384 * 4 + 4,
+    "ce_fwd_sbv_bf16.row_kernel": int((8192 * 131072 * 2 + 8192 * 8) * 1.0003) + 8192 * 4,
+    "flce.tcgen05_gemm_ce": 4 * (1084502400 + 19199232),
+    "fljsd.tcgen05_gemm_lse": 2 * (2169526528 + 35907456),
+    "fljsd.tcgen05_gemm_jsd": 2 * (4788695296 + 19929472),
 }
 
 
@@ -90,6 +97,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-small-ce", action="store_true", help="skip the small CE configurations after the step")
+    ap.add_argument("--small-ce-only", action="store_true",
+                    help="only the small CE configurations (timed back to back and flushed, with the bare read of "
+                         "the same bytes); prints their JSON line (used for launch lists of the small calls)")
     ap.add_argument("--tp", action="store_true",
                     help="vocab-parallel Megatron CE: bf16 [2048, 4, 131072] with the vocab sharded over the N ranks "
                          "(partials, one NCCL all-gather, merge); prints its own JSON line")
@@ -255,6 +265,17 @@ def time_back_to_back(fns, torch, warmup, steps):
     e1.record()
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) * 1e3 / steps
+
+
+def run_small_ce_only(args):
+    import torch
+    import lm_head_online_gb300 as lmho
+    torch.cuda.set_device(0)
+    lmho.load()
+    pk = peaks()
+    ops, roofs, _ = small_ce(lmho, torch, torch.device("cuda", 0), args.seed, pk, steps=args.steps)
+    return {"metric": "small CE calls, us per call", "peaks": pk["src"], "ops": ops, "rooflines": roofs,
+            "steps": args.steps}
 
 
 def small_ce(lmho, torch, dev, seed, pk, steps=50):
@@ -545,7 +566,7 @@ def run_ours(args, rank, world, local_rank):
         "input_gen_s": round(t_gen, 1),
     }
     if world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(h=h, budget_s=12.0, seed=args.seed)
+        result["cpu_baseline"] = cpu_baseline(h=h, seed=args.seed)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -640,7 +661,7 @@ def run_tp(args, rank, world, local_rank):
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm
-def oracle_samples(seed=0, h=None, budget_s=12.0):
+def oracle_samples(seed=0, h=None, budget_s=ORACLE_BUDGET_S):
     """Bounded samples of every op's inputs (taken from the bench's own host
     tensors when given, else regenerated by counter offset)."""
     import gen
@@ -678,7 +699,7 @@ def oracle_samples(seed=0, h=None, budget_s=12.0):
     return s
 
 
-def time_oracle(s):
+def time_oracle(s, single_thread=False):
     """The oracle as it stands on the samples; CE rows are split over host
     threads (each oracle call releases the GIL), fused tokens use the
     oracle's own token partition.  Returns the extrapolated us per full step."""
@@ -702,12 +723,28 @@ def time_oracle(s):
     t_js = timed(lambda: oracle.fljsd_bf16(*s["js"], 0.5, threads=cores))
     us = 1e6 * (t_ce * CE["T"] / n["ce"] + t_sbv * SBV["S"] * SBV["B"] / n["sbv"] +
                 t_fl * FLCE["T"] / n["fl"] + t_js * FLJSD["T"] / n["js"])
-    return {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": (f"ce {n['ce']}/{CE['T']} rows, sbv {n['sbv']}/{SBV['S'] * SBV['B']} tokens, "
-                       f"flce {n['fl']}/{FLCE['T']} tokens, fljsd {n['js']}/{FLJSD['T']} tokens of the same "
-                       f"workload; scaled linearly to one full step"),
-            "seconds": {"ce": round(t_ce, 2), "sbv": round(t_sbv, 2), "flce": round(t_fl, 2),
-                        "fljsd": round(t_js, 2)}}
+    out = {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": (f"ce {n['ce']}/{CE['T']} rows, sbv {n['sbv']}/{SBV['S'] * SBV['B']} tokens, "
+                      f"flce {n['fl']}/{FLCE['T']} tokens, fljsd {n['js']}/{FLJSD['T']} tokens of the same "
+                      f"workload on {cores} threads; scaled linearly to one full step"),
+           "seconds": {"ce": round(t_ce, 2), "sbv": round(t_sbv, 2), "flce": round(t_fl, 2),
+                       "fljsd": round(t_js, 2)}}
+    if single_thread:
+        # one thread on a fixed small subset of the same sample (16 CE rows of each
+        # layout, 2 flce tokens, 1 fljsd token), extrapolated to one step
+        k_ce, k_sbv = min(16, n["ce"]), min(16, n["sbv"])
+        t1_ce = timed(lambda: oracle.ce_f32(s["ce"][0][:k_ce], s["ce"][1][:k_ce]))
+        t1_sbv = timed(lambda: oracle.ce_sbv_bf16(s["sbv"][0][:k_sbv], s["sbv"][1][:k_sbv]))
+        x, W, t = s["fl"]
+        t1_fl = timed(lambda: oracle.flce_bf16(x[:2], W, t[:2], threads=1))
+        xs, Ws, xt, Wt = s["js"]
+        t1_js = timed(lambda: oracle.fljsd_bf16(xs[:1], Ws, xt[:1], Wt, 0.5, threads=1))
+        us1 = 1e6 * (t1_ce * CE["T"] / k_ce + t1_sbv * SBV["S"] * SBV["B"] / k_sbv +
+                     t1_fl * FLCE["T"] / 2 + t1_js * FLJSD["T"])
+        out["single_thread"] = {"value": round(us1, 1), "unit": UNIT, "cores": 1, "extrapolated": True,
+                                "sample": f"ce {k_ce} rows, sbv {k_sbv} tokens, flce 2 tokens, fljsd 1 token "
+                                          f"on one thread, scaled linearly to one full step"}
+    return out
 
 
 def cpu_model():
@@ -730,8 +767,8 @@ def cpu_model():
     return platform.processor() or platform.machine()
 
 
-def cpu_baseline(h=None, budget_s=12.0, seed=0):
-    r = time_oracle(oracle_samples(seed, h, budget_s))
+def cpu_baseline(h=None, budget_s=ORACLE_BUDGET_S, seed=0):
+    r = time_oracle(oracle_samples(seed, h, budget_s), single_thread=True)
     r["cpu_model"] = cpu_model()
     return r
 
@@ -739,7 +776,7 @@ def cpu_baseline(h=None, budget_s=12.0, seed=0):
 def run_reference(args):
     import oracle
     oracle.build()
-    s = oracle_samples(args.seed, None, budget_s=3.0)
+    s = oracle_samples(args.seed, None, budget_s=ORACLE_BUDGET_S)
     vals, r = [], None
     for i in range(args.warmup + args.steps):
         r = time_oracle(s)
@@ -957,6 +994,9 @@ def main():
         return
     if args.case:
         print(json.dumps(run_case(args)), flush=True)
+        return
+    if args.small_ce_only:
+        print(json.dumps(run_small_ce_only(args)), flush=True)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
