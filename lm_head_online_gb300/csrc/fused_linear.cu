@@ -57,6 +57,9 @@
 #ifndef LMHO_JSD_PACKED
 #define LMHO_JSD_PACKED 1
 #endif
+#ifndef LMHO_FOLD_PACKED
+#define LMHO_FOLD_PACKED 1
+#endif
 
 namespace lmho {
 namespace {
@@ -731,7 +734,11 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
                 has_t = true;
               }
             }
+#if LMHO_FOLD_PACKED
+            ms_fold_packed<32>(st, v);
+#else
             ms_fold<32>(st, v);
+#endif
           }
         }
       }

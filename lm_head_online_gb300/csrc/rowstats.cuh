@@ -205,6 +205,34 @@ __device__ __forceinline__ void ms_fold_vecs(MS& a, const uint4* r) {
   a.s += s0 + s1;
 }
 
+// ms_fold over N fp32 values (N a multiple of 4) with the same steps as
+// ms_fold_vecs: a 3-input max, one rescale of s when it rises, and the
+// exponent arguments and the sum two values per fp32x2 instruction.
+template <int N>
+__device__ __forceinline__ void ms_fold_packed(MS& a, const float* v) {
+  static_assert(N % 4 == 0, "pairs of pairs");
+  float vm = max3_f32(v[0], v[1], v[2]);
+#pragma unroll
+  for (int i = 3; i + 1 < N; i += 2) vm = max3_f32(vm, v[i], v[i + 1]);
+  vm = fmaxf(vm, v[N - 1]);
+  if (vm > a.m) {
+    a.s *= ex2_approx((a.m - vm) * kLog2e);
+    a.m = vm;
+  }
+  const float nml = (a.m == -INFINITY) ? 0.f : -a.m * kLog2e;
+  const uint64_t l2e = f32x2(kLog2e, kLog2e), off = f32x2(nml, nml);
+  uint64_t acc = f32x2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    float e0, e1;
+    f32x2_split(fma_f32x2(f32x2(v[i], v[i + 1]), l2e, off), e0, e1);
+    acc = add_f32x2(acc, f32x2(ex2_approx(e0), ex2_approx(e1)));
+  }
+  float s0, s1;
+  f32x2_split(acc, s0, s1);
+  a.s += s0 + s1;
+}
+
 template <int NT>
 __device__ __forceinline__ MS block_allreduce_to0(MS a, MS* s_part) {
   a = ms_warp_allreduce(a);

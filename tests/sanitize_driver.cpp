@@ -63,6 +63,13 @@ void oracle_cpo_grad_f64(const double* x, const double* W, const int64_t* target
 void oracle_cpo_grad_bf16(const uint16_t* x16, const uint16_t* W16, const int64_t* target, int64_t B, int64_t S,
                           int64_t H, int64_t V, double beta, double alpha, double scale, double* dx, double* dW);
 void oracle_logits_bf16(const uint16_t* x, const uint16_t* W, int64_t T, int64_t H, int64_t V, double* z);
+void oracle_ce_partials_bf16(const uint16_t* z16, const int64_t* target, int64_t rows, int64_t Vl, int64_t v0,
+                             double* m_out, double* s_out, double* zt_out);
+void oracle_ce_merge(const double* m, const double* s, const double* zt, int64_t k, const int64_t* target,
+                     int64_t rows, int64_t V, double* loss);
+void oracle_fljsd_dz_bf16(const uint16_t* xs16, const uint16_t* Ws16, const uint16_t* xt16, const uint16_t* Wt16,
+                          int64_t T, int64_t H, int64_t V, double beta, double tau, const uint8_t* keep,
+                          double scale, double* dz, double* gbp);
 }
 
 namespace {
@@ -116,6 +123,22 @@ void run_shape(int64_t T, int64_t H, int64_t V, int threads) {
   oracle_fljsd_grad_bf16(xb.data(), Wb.data(), xb2.data(), Wb2.data(), T, H, V, 0.5, 1.0, nullptr, 2.0, dx.data(),
                          dW.data());
   oracle_logits_bf16(xb.data(), Wb.data(), T, H, V, zl.data());
+  oracle_fljsd_dz_bf16(xb.data(), Wb.data(), xb2.data(), Wb2.data(), T, H, V, 0.3, 2.0, keep.data(), 1.0, dz.data(),
+                       zl.data());
+  // vocab-parallel: split V into up to three shards (each its own [T, w] buffer), merge
+  {
+    const int64_t k = V >= 3 ? 3 : V;
+    std::vector<double> m(k * T), sm(k * T), zt(k * T);
+    for (int64_t j = 0; j < k; ++j) {
+      const int64_t v0 = V * j / k, w1 = V * (j + 1) / k - v0;
+      std::vector<uint16_t> local(T * w1);
+      for (int64_t i = 0; i < T; ++i)
+        for (int64_t v = 0; v < w1; ++v) local[i * w1 + v] = zb[i * V + v0 + v];
+      oracle_ce_partials_bf16(local.data(), t.data(), T, w1, v0, m.data() + j * T, sm.data() + j * T,
+                              zt.data() + j * T);
+    }
+    oracle_ce_merge(m.data(), sm.data(), zt.data(), k, t.data(), T, V, rows.data());
+  }
   if (T % 2 == 0) {
     const int64_t B = 2, S = T / 2;
     oracle_cpo_combine(rows2.data(), B, S, 0.1, 1.0, lp.data(), w.data());

@@ -274,3 +274,35 @@ def test_api_errors_raise(gpu_lib):
     assert e.value.status == gpu_lib.LMHO_ERR_WORKSPACE
     with pytest.raises(TypeError):
         gpu_lib.ce_fwd_f32(z.double(), t)
+
+
+def test_launch_events_are_per_host_thread(gpu_lib):
+    """lmho_set_launch_events applies to the calls of the thread that set it:
+    another thread's call, queued behind a sleeping kernel on its own stream,
+    leaves this thread's events alone (were they recorded there, they would
+    still be pending); this thread's next call records them."""
+    import threading
+    z = to_dev_bf16(gen.normal_bf16_bits(5, 0, (16, 4, 512), sigma=2.0))
+    t = to_dev(gen.targets(5, 1, (16, 4), 512))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    gpu_lib.set_launch_events(evs)
+    side = torch.cuda.Stream()
+
+    def other():
+        with torch.cuda.stream(side):
+            torch.cuda._sleep(100_000_000)          # tens of milliseconds of GPU time
+            gpu_lib.ce_fwd_sbv_bf16(z, t, stream=side)
+
+    th = threading.Thread(target=other)
+    th.start()
+    th.join()
+    try:
+        assert all(e.query() for e in evs), "another thread's call recorded this thread's events"
+        gpu_lib.ce_fwd_sbv_bf16(z, t)
+    finally:
+        gpu_lib.set_launch_events(None)
+    torch.cuda.synchronize()
+    assert evs[0].elapsed_time(evs[1]) > 0.0

@@ -184,3 +184,44 @@ def test_cpo_guards(gpu_lib, B, S, H, V):
     assert gpu_lib.ws_status(ws2) == 0
     written(loss2, lp2, dx, dW)
     unchanged(before, [x, W, t])
+
+
+@pytest.mark.parametrize("S,B,V,shards", [(7, 3, 1001, 3), (64, 4, 4096, 2), (3, 2, 70000, 8)])
+def test_vocab_parallel_guards(gpu_lib, S, B, V, shards):
+    """Each shard's partials and the merged losses inside guard regions; the
+    shards are separate buffers as on separate ranks (odd widths included)."""
+    g = Guarded()
+    z = gen.normal_bf16_bits(24, 0, (S, B, V), sigma=2.0)
+    t = to_dev(gen.targets(24, 1, (S, B), V))
+    cuts = [round(V * j / shards) + (j % 2) for j in range(shards)] + [V]
+    cuts[0] = 0
+    parts = g.view(shards * 3 * S * B * 4, torch.float32, (shards, 3, S, B))
+    locals_ = []
+    for j in range(shards):
+        v0, w = cuts[j], cuts[j + 1] - cuts[j]
+        local = to_dev_bf16(np.ascontiguousarray(z[..., v0:v0 + w]))
+        locals_.append(local)
+        before = snapshot(local, t)
+        gpu_lib.ce_partials_sbv_bf16(local, t, v0, partials=parts[j])
+        unchanged(before, [local, t])
+    loss = g.view(S * B * 4, torch.float32, (S, B))
+    before = snapshot(parts, t)
+    gpu_lib.ce_merge_partials(parts, t, V, loss=loss)
+    g.check()
+    unchanged(before, [parts, t])
+    torch.cuda.synchronize()
+    assert not bool(torch.isnan(parts).any()), "a partial was never written"   # -inf is a valid target logit
+    written(loss)
+
+
+def test_probe_read_guards(gpu_lib):
+    g = Guarded()
+    words = gen.targets(25, 0, (5 * 4096,), 2 ** 32).astype(np.uint32)
+    data = torch.from_numpy(words.view(np.int32)).cuda()
+    out = g.view(5 * 4, torch.int32, (5,), fill=0)
+    before = snapshot(data)
+    gpu_lib.probe_read(data, 16384, out=out)
+    g.check()
+    unchanged(before, [data])
+    want = np.bitwise_xor.reduce(words.reshape(5, -1), axis=1)
+    np.testing.assert_array_equal(out.cpu().numpy().view(np.uint32), want)
