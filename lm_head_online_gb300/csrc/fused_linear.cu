@@ -230,24 +230,27 @@ __device__ __forceinline__ UnitCoord decode_unit(const Params& p, int64_t u, int
 //   term = -ln2 2^hi (s lg2(s) + u d).
 // Returns 2^hi (s lg2(s) + u d), the term divided by -ln2 (callers scale the
 // sum once): three MUFU operations and no ln2 / log2e multiplies per pair.
+// Every step is an explicitly rounded operation (no multiply-add contraction
+// left to the compiler), so this and the packed form below give the same bits.
 __device__ __forceinline__ float jsd_term2(float lp2, float lq2, float beta, float omb) {
-  const float diff = lp2 - lq2;
+  const float diff = __fsub_rn(lp2, lq2);
   const float hi = fmaxf(lp2, lq2);
   const float d = fabsf(diff);
   const bool p_is_hi = diff >= 0.f;
   const float w_hi = p_is_hi ? beta : omb;
   const float w_lo = p_is_hi ? omb : beta;
-  const float u = w_lo * ex2_approx(-d);
-  const float sv = u + w_hi;
-  return ex2_approx(hi) * fmaf(sv, lg2_approx(sv), u * d);
+  const float u = __fmul_rn(w_lo, ex2_approx(-d));
+  const float sv = __fadd_rn(u, w_hi);
+  return __fmul_rn(ex2_approx(hi), fmaf(sv, lg2_approx(sv), __fmul_rn(u, d)));
 }
 
 // jsd_term2 for two pairs at once (columns j and j + 1 of a row): the FMA,
 // subtract, multiply and add steps on packed fp32 pairs (one instruction for
 // both), the max / selects and the three MUFU operations per pair unpacked.
-// Same arithmetic as jsd_term2; returns the sum of the two terms.
-__device__ __forceinline__ float jsd_term2_x2(uint64_t zs2, uint64_t zq2, uint64_t it2x2, uint64_t nls2,
-                                              uint64_t nlt2, float beta, float omb) {
+// Same arithmetic as jsd_term2; adds the two terms to acc in column order, so
+// the row sum is bitwise the one the one-column loops give.
+__device__ __forceinline__ void jsd_term2_x2(float& acc, uint64_t zs2, uint64_t zq2, uint64_t it2x2,
+                                             uint64_t nls2, uint64_t nlt2, float beta, float omb) {
   float lp0, lp1, lq0, lq1;
   f32x2_split(fma_f32x2(zs2, it2x2, nls2), lp0, lp1);
   f32x2_split(fma_f32x2(zq2, it2x2, nlt2), lq0, lq1);
@@ -266,7 +269,8 @@ __device__ __forceinline__ float jsd_term2_x2(uint64_t zs2, uint64_t zq2, uint64
   const uint64_t inner = fma_f32x2(sv, f32x2(lg2_approx(s0), lg2_approx(s1)), mul_f32x2(u, f32x2(d0, d1)));
   float t0, t1;
   f32x2_split(mul_f32x2(f32x2(ex2_approx(hi0), ex2_approx(hi1)), inner), t0, t1);
-  return t0 + t1;
+  acc += t0;
+  acc += t1;
 }
 
 // The pieces of one generalized-JSD pair the backward needs: P = e^{lp} and
@@ -601,8 +605,8 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
               const uint64_t i2 = f32x2(it2, it2), ns = f32x2(-ls2, -ls2), nt = f32x2(-lt2, -lt2);
 #pragma unroll
               for (int j = 0; j < 16; j += 2)
-                jsd += jsd_term2_x2(f32x2(__uint_as_float(rs[j]), __uint_as_float(rs[j + 1])),
-                                    f32x2(__uint_as_float(rt[j]), __uint_as_float(rt[j + 1])), i2, ns, nt, beta, omb);
+                jsd_term2_x2(jsd, f32x2(__uint_as_float(rs[j]), __uint_as_float(rs[j + 1])),
+                             f32x2(__uint_as_float(rt[j]), __uint_as_float(rt[j + 1])), i2, ns, nt, beta, omb);
 #else
 #pragma unroll
               for (int j = 0; j < 16; ++j)
