@@ -92,6 +92,16 @@ def _load():
             lib.oracle_fljsd_dz_bf16.restype = None
             lib.oracle_logits_bf16.argtypes = [vp, vp, i64, i64, i64, vp]
             lib.oracle_logits_bf16.restype = None
+            lib.oracle_flce_partials_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, vp, ci]
+            lib.oracle_flce_partials_bf16.restype = None
+            lib.oracle_fljsd_lse_shard_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, vp, ci]
+            lib.oracle_fljsd_lse_shard_bf16.restype = None
+            lib.oracle_lse_merge.argtypes = [vp, i64, i64, vp]
+            lib.oracle_lse_merge.restype = None
+            lib.oracle_fljsd_terms_shard_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, vp, ci]
+            lib.oracle_fljsd_terms_shard_bf16.restype = None
+            lib.oracle_jsd_merge.argtypes = [vp, i64, i64, vp, vp]
+            lib.oracle_jsd_merge.restype = dbl
             _lib = lib
     return _lib
 
@@ -427,3 +437,77 @@ def cpo_combine(rows, beta=0.1, alpha=1.0):
     w = np.empty((B, S), np.float64)
     m = _load().oracle_cpo_combine(pr, B, S, float(beta), float(alpha), lp.ctypes.data, w.ctypes.data)
     return m, lp, w
+
+
+def flce_partials_bf16(x_bits, Wl_bits, target, v0, threads=None):
+    """Vocab-parallel fused linear + CE, one shard: x [T, H], Wl [Vl, H] (bf16
+    bits) = the global vocab rows [v0, v0 + Vl), global targets [T].  Returns
+    float64 (m, s, zt) [T] of the shard's logits x Wl^T."""
+    x, px = _c(x_bits, np.uint16)
+    Wl, pw = _c(Wl_bits, np.uint16)
+    t, pt = _c(target, np.int64)
+    T, H = x.shape
+    Vl = Wl.shape[0]
+    assert Wl.shape[1] == H and t.shape == (T,)
+    m, s, zt = (np.empty(T, np.float64) for _ in range(3))
+    _load().oracle_flce_partials_bf16(px, pw, pt, T, H, Vl, int(v0), m.ctypes.data, s.ctypes.data, zt.ctypes.data,
+                                      _threads(threads))
+    return m, s, zt
+
+
+def _two_heads(xs_bits, Wsl_bits, xt_bits, Wtl_bits):
+    xs, p1 = _c(xs_bits, np.uint16)
+    Ws, p2 = _c(Wsl_bits, np.uint16)
+    xt, p3 = _c(xt_bits, np.uint16)
+    Wt, p4 = _c(Wtl_bits, np.uint16)
+    T, H = xs.shape
+    Vl = Ws.shape[0]
+    assert xt.shape == (T, H) and Ws.shape == (Vl, H) and Wt.shape == (Vl, H)
+    return (xs, Ws, xt, Wt), (p1, p2, p3, p4), T, H, Vl
+
+
+def fljsd_lse_shard_bf16(xs_bits, Wsl_bits, xt_bits, Wtl_bits, temperature=1.0, threads=None):
+    """Vocab-parallel fused linear + JSD, one shard: each head's log-sum-exp
+    over the shard's columns of logits / temperature -> float64 [2, T]
+    (0 = student, 1 = teacher)."""
+    keep_alive, ptrs, T, H, Vl = _two_heads(xs_bits, Wsl_bits, xt_bits, Wtl_bits)
+    lse = np.empty((2, T), np.float64)
+    _load().oracle_fljsd_lse_shard_bf16(*ptrs, T, H, Vl, float(temperature), lse.ctypes.data, _threads(threads))
+    return lse
+
+
+def lse_merge(parts):
+    """Global log-sum-exps [2, T] from k shards' [k, 2, T], in shard order."""
+    p, pp = _c(parts, np.float64)
+    k, two, T = p.shape
+    assert two == 2
+    out = np.empty((2, T), np.float64)
+    _load().oracle_lse_merge(pp, k, T, out.ctypes.data)
+    return out
+
+
+def fljsd_terms_shard_bf16(xs_bits, Wsl_bits, xt_bits, Wtl_bits, lse, beta=0.5, temperature=1.0, threads=None):
+    """Vocab-parallel fused linear + JSD, one shard: with the global
+    log-sum-exps lse [2, T], each token's sum of the JSD terms over the
+    shard's columns -> float64 [T]."""
+    keep_alive, ptrs, T, H, Vl = _two_heads(xs_bits, Wsl_bits, xt_bits, Wtl_bits)
+    lse, pl = _c(lse, np.float64)
+    assert lse.shape == (2, T)
+    out = np.empty(T, np.float64)
+    _load().oracle_fljsd_terms_shard_bf16(*ptrs, T, H, Vl, float(beta), float(temperature), pl, out.ctypes.data,
+                                          _threads(threads))
+    return out
+
+
+def jsd_merge(terms, keep=None):
+    """Per-token JSD [T] from k shards' term sums [k, T] (0 where keep is 0)
+    and their batchmean over kept tokens: returns (mean, rows)."""
+    tm, pt = _c(terms, np.float64)
+    k, T = tm.shape
+    pk = None
+    if keep is not None:
+        keep, pk = _c(keep, np.uint8)
+        assert keep.shape == (T,)
+    rows = np.empty(T, np.float64)
+    m = _load().oracle_jsd_merge(pt, k, T, pk, rows.ctypes.data)
+    return m, rows

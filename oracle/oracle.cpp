@@ -66,6 +66,18 @@
 //   M = max_j m_j,  loss = M + ln( sum_j s_j exp(m_j - M) ) - max_j zt_j,
 // NaN when t_i is outside [0, V).
 
+// Vocab-parallel fused losses (the same vocab split applied to the output
+// layer: each rank holds the rows [v0, v0 + Vl) of W, so its logits are
+// x W_local^T, [tokens, Vl]):
+//   fused CE:  the shard's (m, s, zt) of those logits, combined as above;
+//   fused JSD: two combinations.  First each head's log-sum-exp over the
+//     shard, l_h = ln sum_{v in shard} exp(z_hv / tau), and the global one
+//     lse_h = L + ln( sum_j exp(l_hj - L) ), L = max_j l_hj, in shard order;
+//     then, with the global lse, the shard's sum of the JSD terms
+//     beta P (lp - ln M) + (1 - beta) Q (lq - ln M), lp = zs/tau - lse_0,
+//     lq = zt/tau - lse_1, and the token's JSD is the sum of its shards' sums
+//     in shard order (so the split changes only the order of one sum).
+//
 // Variant (JSD with temperature and a token mask): the logits of both heads
 // are divided by the temperature tau before the softmax; tokens whose keep
 // flag is 0 are left out, and the batchmean divides by the number of kept
@@ -650,6 +662,101 @@ void oracle_cpo_grad_bf16(const uint16_t* x16, const uint16_t* W16, const int64_
 void oracle_logits_bf16(const uint16_t* x, const uint16_t* W, int64_t T, int64_t H, int64_t V,
                         double* z) {
   for (int64_t i = 0; i < T; ++i) logits_row_bf16(x + i * H, W, H, V, z + i * V);
+}
+
+// Vocab-parallel fused linear + CE, one shard: x [T, H], Wl [Vl, H] (bf16) =
+// the global vocab rows [v0, v0 + Vl); targets are global.  The shard's max m,
+// sum of exp(z - m) s and target logit zt (-inf when the target is not in the
+// shard) of each token's logits x_i Wl^T, two plain passes as in ce_row.
+void oracle_flce_partials_bf16(const uint16_t* x, const uint16_t* Wl, const int64_t* target, int64_t T, int64_t H,
+                               int64_t Vl, int64_t v0, double* m_out, double* s_out, double* zt_out, int threads) {
+  over_tokens(T, threads, [&](int64_t i) {
+    std::vector<double> z(Vl);
+    logits_row_bf16(x + i * H, Wl, H, Vl, z.data());
+    double M = z[0];
+    for (int64_t v = 1; v < Vl; ++v)
+      if (z[v] > M || std::isnan(z[v])) M = z[v];
+    double sum = 0.0;
+    for (int64_t v = 0; v < Vl; ++v) sum += std::exp(z[v] - M);
+    const int64_t tl = target[i] - v0;
+    m_out[i] = M;
+    s_out[i] = sum;
+    zt_out[i] = (tl >= 0 && tl < Vl) ? z[tl] : -std::numeric_limits<double>::infinity();
+  });
+}
+
+// Vocab-parallel fused linear + JSD, first combination, one shard: each head's
+// log-sum-exp over the shard's columns of the logits divided by tau; lse [2][T]
+// (head 0 = student xs Wsl^T, head 1 = teacher xt Wtl^T).
+void oracle_fljsd_lse_shard_bf16(const uint16_t* xs, const uint16_t* Wsl, const uint16_t* xt, const uint16_t* Wtl,
+                                 int64_t T, int64_t H, int64_t Vl, double tau, double* lse, int threads) {
+  over_tokens(T, threads, [&](int64_t i) {
+    std::vector<double> z(Vl);
+    for (int h = 0; h < 2; ++h) {
+      logits_row_bf16((h ? xt : xs) + i * H, h ? Wtl : Wsl, H, Vl, z.data());
+      for (int64_t v = 0; v < Vl; ++v) z[v] /= tau;
+      double M = z[0];
+      for (int64_t v = 1; v < Vl; ++v)
+        if (z[v] > M || std::isnan(z[v])) M = z[v];
+      double sum = 0.0;
+      for (int64_t v = 0; v < Vl; ++v) sum += std::exp(z[v] - M);
+      lse[h * T + i] = M + std::log(sum);
+    }
+  });
+}
+
+// The global log-sum-exps [2][T] from k shards' [k][2][T] (shard-major), in
+// shard order: L = max_j l_j, lse = L + ln sum_j exp(l_j - L).
+void oracle_lse_merge(const double* parts, int64_t k, int64_t T, double* lse) {
+  for (int64_t h = 0; h < 2; ++h)
+    for (int64_t i = 0; i < T; ++i) {
+      double L = parts[h * T + i];
+      for (int64_t j = 1; j < k; ++j) {
+        const double l = parts[(j * 2 + h) * T + i];
+        if (l > L || std::isnan(l)) L = l;
+      }
+      double sum = 0.0;
+      for (int64_t j = 0; j < k; ++j) sum += std::exp(parts[(j * 2 + h) * T + i] - L);
+      lse[h * T + i] = L + std::log(sum);
+    }
+}
+
+// Vocab-parallel fused linear + JSD, second combination, one shard: with the
+// global log-sum-exps lse [2][T], each token's sum over the shard's columns of
+// the generalized JSD terms (jsd_row on the shard's log-probabilities).
+void oracle_fljsd_terms_shard_bf16(const uint16_t* xs, const uint16_t* Wsl, const uint16_t* xt, const uint16_t* Wtl,
+                                   int64_t T, int64_t H, int64_t Vl, double beta, double tau, const double* lse,
+                                   double* terms, int threads) {
+  over_tokens(T, threads, [&](int64_t i) {
+    std::vector<double> lp(Vl), lq(Vl);
+    logits_row_bf16(xs + i * H, Wsl, H, Vl, lp.data());
+    logits_row_bf16(xt + i * H, Wtl, H, Vl, lq.data());
+    for (int64_t v = 0; v < Vl; ++v) {
+      lp[v] = lp[v] / tau - lse[i];
+      lq[v] = lq[v] / tau - lse[T + i];
+    }
+    terms[i] = jsd_row(lp.data(), lq.data(), Vl, beta);
+  });
+}
+
+// The per-token JSD from k shards' term sums [k][T] (summed in shard order; 0
+// for tokens whose keep flag is 0, keep may be null) and their batchmean over
+// the kept tokens (0 when none is kept).
+double oracle_jsd_merge(const double* terms, int64_t k, int64_t T, const uint8_t* keep, double* rows) {
+  double total = 0.0;
+  int64_t kept = 0;
+  for (int64_t i = 0; i < T; ++i) {
+    if (keep && !keep[i]) {
+      rows[i] = 0.0;
+      continue;
+    }
+    double acc = 0.0;
+    for (int64_t j = 0; j < k; ++j) acc += terms[j * T + i];
+    rows[i] = acc;
+    total += acc;
+    ++kept;
+  }
+  return kept ? total / static_cast<double>(kept) : 0.0;
 }
 
 }  // extern "C"

@@ -70,6 +70,15 @@ void oracle_ce_merge(const double* m, const double* s, const double* zt, int64_t
 void oracle_fljsd_dz_bf16(const uint16_t* xs16, const uint16_t* Ws16, const uint16_t* xt16, const uint16_t* Wt16,
                           int64_t T, int64_t H, int64_t V, double beta, double tau, const uint8_t* keep,
                           double scale, double* dz, double* gbp);
+void oracle_flce_partials_bf16(const uint16_t* x, const uint16_t* Wl, const int64_t* target, int64_t T, int64_t H,
+                               int64_t Vl, int64_t v0, double* m_out, double* s_out, double* zt_out, int threads);
+void oracle_fljsd_lse_shard_bf16(const uint16_t* xs, const uint16_t* Wsl, const uint16_t* xt, const uint16_t* Wtl,
+                                 int64_t T, int64_t H, int64_t Vl, double tau, double* lse, int threads);
+void oracle_lse_merge(const double* parts, int64_t k, int64_t T, double* lse);
+void oracle_fljsd_terms_shard_bf16(const uint16_t* xs, const uint16_t* Wsl, const uint16_t* xt, const uint16_t* Wtl,
+                                   int64_t T, int64_t H, int64_t Vl, double beta, double tau, const double* lse,
+                                   double* terms, int threads);
+double oracle_jsd_merge(const double* terms, int64_t k, int64_t T, const uint8_t* keep, double* rows);
 }
 
 namespace {
@@ -138,6 +147,24 @@ void run_shape(int64_t T, int64_t H, int64_t V, int threads) {
                               zt.data() + j * T);
     }
     oracle_ce_merge(m.data(), sm.data(), zt.data(), k, t.data(), T, V, rows.data());
+    // the fused forms: shards of W's rows, each its own [w, H] slice of the same buffer
+    std::vector<double> lparts(k * 2 * T), lse(2 * T), terms(k * T);
+    for (int64_t j = 0; j < k; ++j) {
+      const int64_t v0 = V * j / k, w1 = V * (j + 1) / k - v0;
+      oracle_flce_partials_bf16(xb.data(), Wb.data() + v0 * H, t.data(), T, H, w1, v0, m.data() + j * T,
+                                sm.data() + j * T, zt.data() + j * T, threads);
+      oracle_fljsd_lse_shard_bf16(xb.data(), Wb.data() + v0 * H, xb2.data(), Wb2.data() + v0 * H, T, H, w1, 1.5,
+                                  lparts.data() + j * 2 * T, threads);
+    }
+    oracle_ce_merge(m.data(), sm.data(), zt.data(), k, t.data(), T, V, rows.data());
+    oracle_lse_merge(lparts.data(), k, T, lse.data());
+    for (int64_t j = 0; j < k; ++j) {
+      const int64_t v0 = V * j / k, w1 = V * (j + 1) / k - v0;
+      oracle_fljsd_terms_shard_bf16(xb.data(), Wb.data() + v0 * H, xb2.data(), Wb2.data() + v0 * H, T, H, w1, 0.3,
+                                    1.5, lse.data(), terms.data() + j * T, threads);
+    }
+    oracle_jsd_merge(terms.data(), k, T, keep.data(), rows.data());
+    oracle_jsd_merge(terms.data(), k, T, nullptr, rows.data());
   }
   if (T % 2 == 0) {
     const int64_t B = 2, S = T / 2;
