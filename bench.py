@@ -64,13 +64,13 @@ ORACLE_BUDGET_S = 6.0
 # The figures hold only for the sources they were taken from: a changed source
 # makes the bench report null.
 KERNEL_SOURCES = ("fused_linear.cu", "ce_rows.cu", "rowstats.cuh", "ptx.cuh", "lmho_internal.h")
-TRAFFIC_SOURCE_DIGEST = "de71b69dd76a6864"
+TRAFFIC_SOURCE_DIGEST = "175b7b3fd505fdf5"
 TRAFFIC_BYTES = {
     "ce_fwd_f32.row_kernel_and_mean": int((16384 * 131072 * 4 + 16384 * 8) * 1.0003) + 16384 * 4 + 4,
     "ce_fwd_sbv_bf16.row_kernel": int((8192 * 131072 * 2 + 8192 * 8) * 1.0003) + 8192 * 4,
-    "flce.tcgen05_gemm_ce": 4 * (1084502400 + 19199232),
-    "fljsd.tcgen05_gemm_lse": 2 * (2169526528 + 35907456),
-    "fljsd.tcgen05_gemm_jsd": 2 * (4788695296 + 19929472),
+    "flce.tcgen05_gemm_ce": 4 * (1084840192 + 19158656),
+    "fljsd.tcgen05_gemm_lse": 2 * (2169591936 + 36189824),
+    "fljsd.tcgen05_gemm_jsd": 2 * (4477051904 + 19567744),
 }
 
 
@@ -103,6 +103,9 @@ def parse():
     ap.add_argument("--tp", action="store_true",
                     help="vocab-parallel Megatron CE: bf16 [2048, 4, 131072] with the vocab sharded over the N ranks "
                          "(partials, one NCCL all-gather, merge); prints its own JSON line")
+    ap.add_argument("--tp-fused", action="store_true",
+                    help="vocab-parallel fused linear + CE (x [16384, 4096]) and + JSD (xs, xt [8192, 4096]) with the "
+                         "rows of W [128256, 4096] (both heads) sharded over the N ranks; prints its own JSON line")
     ap.add_argument("--e2e-clocks", action="store_true",
                     help="also sample clocks during the e2e region (nvidia-smi polling slows host copies)")
     ap.add_argument("--sweep", action="store_true",
@@ -489,6 +492,23 @@ def run_ours(args, rank, world, local_rank):
         h2d = sum(v.numel() * v.element_size() for v in h.values())
         d2h = sum(v.numel() * v.element_size() for v in out.values())
 
+        # The host link's own rate here: a 1 GiB pinned copy, median of 3 after one
+        # untimed.  h2d / link_GBps is the floor of an end-to-end step (the copies
+        # alone); splitting copies over streams or reading pinned memory from SMs
+        # reached the same rate on this machine.
+        probe_h = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+        probe_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+        link = []
+        for _ in range(4):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            probe_d.copy_(probe_h, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            link.append((1 << 30) / (a.elapsed_time(b) * 1e-3) / 1e9)
+        link_gbps = float(np.median(link[1:]))
+        del probe_h, probe_d
+
         # Each op's inputs are copied on a second stream, in the order below (most
         # compute per copied byte first), and each op waits only for its own
         # inputs, so copies of later inputs overlap earlier ops' kernels.  A step's
@@ -542,6 +562,8 @@ def run_ours(args, rank, world, local_rank):
                "phases_us": {"inputs_landed": round(copy_ms * 1e3, 1), "kernels_done": round(kern_ms * 1e3, 1),
                              "d2h": round(d2h_ms * 1e3, 1)},
                "h2d_GBps": round(h2d / (copy_ms * 1e-3) / 1e9, 1),
+               "link_GBps": round(link_gbps, 1),
+               "copy_floor_us": round(h2d / (link_gbps * 1e9) * 1e6, 1),
                # per step: the host link is shared with other GPUs' jobs on the same CPU
                "h2d_GBps_per_step": [round(h2d / (m[0].elapsed_time(m[1]) * 1e-3) / 1e9, 1) for m in marks]}
 
@@ -656,6 +678,147 @@ def run_tp(args, rank, world, local_rank):
            "loss_mean": float(loss.double().mean().item())}
     if single is not None:
         res["max_abs_diff_vs_ce_fwd_sbv_bf16"] = float((loss - single).abs().max().item())
+    tdist.destroy_process_group()
+    return res
+
+
+def run_tp_fused(args, rank, world, local_rank):
+    """Vocab-parallel fused losses over `world` ranks (one GPU each): rank r
+    holds the rows shard_vocab(V, r, world) of W (of both heads for the JSD);
+    the inputs x / xs, xt and the targets are on every rank.  One step:
+      flce:  flce_partials_bf16, one NCCL all-gather of [3, T], ce_merge_partials,
+             rows_mean;
+      fljsd: fljsd_lse_partials_bf16, all-gather of [2, T], lse_merge_partials,
+             fljsd_terms_bf16, all-gather of [1, T], jsd_merge_terms.
+    Total work is fixed as N grows ("strong").  A one-rank NCCL group is used at
+    N = 1 (the collectives run there too), where the unsharded calls are timed
+    beside it and their results compared."""
+    import torch
+    import torch.distributed as tdist
+    import gen
+    import lm_head_online_gb300 as lmho
+    from lm_head_online_gb300 import dist as lmdist
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lmho.load()
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    os.environ.setdefault("MASTER_PORT", "29534")
+    tdist.init_process_group("nccl", rank=rank, world_size=world, device_id=dev)
+    thr = os.cpu_count() or 1
+    H, V = FLCE["H"], FLCE["V"]
+    Tc, Tj = FLCE["T"], FLJSD["T"]
+    v0, w = lmdist.shard_vocab(V, rank, world)
+
+    def rows_of(stream_id, sigma):
+        full = torch.empty((V, H), dtype=torch.bfloat16)
+        gen.normal_bf16_bits(args.seed, stream_id, (V, H), sigma, out=full.view(torch.int16), threads=thr)
+        return full[v0:v0 + w].contiguous().to(dev)
+
+    def host_bf16(stream_id, T):
+        t = torch.empty((T, H), dtype=torch.bfloat16)
+        gen.normal_bf16_bits(args.seed, stream_id, (T, H), 1.0, out=t.view(torch.int16), threads=thr)
+        return t.to(dev)
+
+    x = host_bf16(gen.STREAM_X, Tc)
+    W = rows_of(gen.STREAM_W, 0.02)
+    tgt = torch.from_numpy(gen.targets(args.seed, gen.STREAM_TARGET, (Tc,), V, threads=thr)).to(dev)
+    xs, xt = host_bf16(gen.STREAM_X, Tj), host_bf16(gen.STREAM_XT, Tj)
+    Ws, Wt = rows_of(gen.STREAM_W, 0.02), rows_of(gen.STREAM_WT, 0.02)
+    ws_c = lmho.workspace(lmho.flce_workspace_bytes(Tc, H, w), dev)
+    ws_j = lmho.workspace(lmho.fljsd_workspace_bytes(Tj, H, w), dev)
+    part = torch.empty((3, Tc), device=dev)
+    g_part = torch.empty((world, 3, Tc), device=dev)
+    lse_l = torch.empty((2, Tj), device=dev)
+    g_lse = torch.empty((world, 2, Tj), device=dev)
+    terms = torch.empty((Tj,), device=dev)
+    g_terms = torch.empty((world, Tj), device=dev)
+    stream = torch.cuda.current_stream()
+    names = ("flce_pass", "flce_gather", "flce_merge", "lse_pass", "lse_gather", "lse_merge", "jsd_pass",
+             "jsd_gather", "jsd_merge")
+
+    def step(ev=None):
+        def mark(i):
+            if ev:
+                ev[i].record(stream)
+        mark(0)
+        lmho.flce_partials_bf16(x, W, tgt, v0, partials=part, ws=ws_c)
+        mark(1)
+        tdist.all_gather_into_tensor(g_part.view(world * 3, Tc), part)
+        mark(2)
+        rows = lmho.ce_merge_partials(g_part.view(world, 3, Tc, 1), tgt.view(Tc, 1), V).view(Tc)
+        ce_mean = lmho.rows_mean(rows)
+        mark(3)
+        lmho.fljsd_lse_partials_bf16(xs, Ws, xt, Wt, 1.0, out=lse_l, ws=ws_j)
+        mark(4)
+        tdist.all_gather_into_tensor(g_lse.view(world * 2, Tj), lse_l)
+        mark(5)
+        lse = lmho.lse_merge_partials(g_lse)
+        mark(6)
+        lmho.fljsd_terms_bf16(xs, Ws, xt, Wt, lse, 0.5, 1.0, out=terms, ws=ws_j)
+        mark(7)
+        tdist.all_gather_into_tensor(g_terms, terms)
+        mark(8)
+        jsd, _ = lmho.jsd_merge_terms(g_terms)
+        mark(9)
+        return ce_mean, jsd
+
+    for _ in range(max(1, args.warmup)):
+        ce_mean, jsd = step()
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        tdist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(K):
+            ce_mean, jsd = step(evs[i])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        tdist.barrier()
+    ms = lmdist.max_over_ranks(e0.elapsed_time(e1) / K)
+    ph = {name: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]))
+          for j, name in enumerate(names)}
+    pk = peaks()
+    fl_flops = 2 * Tc * H * w
+    js_flops = 4 * Tj * H * w
+    tf = js_flops / (ph["jsd_pass"] * 1e-3) / 1e12
+    res = {"metric": "vocab-parallel fused linear + CE and + JSD, us/step", "impl": "ours",
+           "mode": "vocab-parallel fused", "value": round(ms * 1e3, 1), "unit": "us/step", "n_gpus": world,
+           "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False,
+           "scaling": "strong", "vs_baseline": None, "dtype": "bf16 in, f32 accumulate",
+           "data": "synthetic (seeded Philox generator)",
+           "config": {"workload": f"flce x[{Tc},{H}] + fljsd xs,xt[{Tj},{H}], W rows [{V},{H}] sharded over "
+                                  f"{world} rank(s) ({w} rows here)", "parallelism": f"tp{world}",
+                      "l2": "inputs larger than L2 (no flush)"},
+           "phases_us": {k: round(v * 1e3, 1) for k, v in ph.items()},
+           "TFLOP/s": {"flce_pass": round(fl_flops / (ph["flce_pass"] * 1e-3) / 1e12, 1),
+                       "lse_pass": round(js_flops / 2 / (ph["lse_pass"] * 1e-3) / 1e12, 1),
+                       "jsd_pass": round(tf, 1)},
+           "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_sus"],
+                        "unit": "TFLOP/s", "frac": round(tf / pk["bf16_sus"], 4), "traffic": None,
+                        "kernel": "fljsd_terms_bf16 tensor-core pass"},
+           "gpu_launches": 11 * K, "clocks": clocks.summary(),
+           "flce_loss": float(ce_mean.item()), "fljsd_loss": float(jsd.item())}
+    if world == 1:
+        # the unsharded calls on the same inputs, timed the same way
+        ws1 = lmho.workspace(lmho.flce_workspace_bytes(Tc, H, V), dev)
+        ws2 = lmho.workspace(lmho.fljsd_workspace_bytes(Tj, H, V), dev)
+        for _ in range(2):
+            a = lmho.flce_fwd_bf16(x, W, tgt, ws=ws1)
+            b = lmho.fljsd_fwd_bf16(xs, Ws, xt, Wt, 0.5, ws=ws2)
+        torch.cuda.synchronize()
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        for _ in range(K):
+            a = lmho.flce_fwd_bf16(x, W, tgt, ws=ws1)
+            b = lmho.fljsd_fwd_bf16(xs, Ws, xt, Wt, 0.5, ws=ws2)
+        u1.record(stream)
+        torch.cuda.synchronize()
+        res["unsharded_us_per_step"] = round(u0.elapsed_time(u1) / K * 1e3, 1)
+        res["bitwise_equal_to_unsharded"] = bool(torch.equal(a, ce_mean) and torch.equal(b, jsd))
     tdist.destroy_process_group()
     return res
 
@@ -1004,6 +1167,11 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.tp_fused:
+        res = run_tp_fused(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
         return
     if args.tp:
         res = run_tp(args, rank, world, local_rank)

@@ -316,6 +316,73 @@ int fljsd_fwd_bf16_ex(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt
                       size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Vocab-parallel fused losses: the vocabulary split of the page "Vocab-
+ * parallel cross-entropy, Megatron layout" (summary: each tensor-parallel
+ * rank holds its own vocab range) applied to the output layer.  A rank holds
+ * the rows [vocab_start, vocab_start + V_local) of W (W_local [V_local, H]
+ * bf16 device, 16-byte aligned), so its logits are x W_local^T; the full
+ * inputs x / xs / xt [T, H] are on every rank.  Ranks exchange small per-token
+ * results (all-gathers done by the caller, e.g. NCCL, in rank order); the
+ * logits never leave the tensor cores.
+ *
+ * Fused linear + CE (pages "Fused linear + CPO loss", its cross-entropy core):
+ * flce_partials_bf16: one shard.
+ *   target    [T] int64 device, GLOBAL vocab indices
+ *   partials  [3][T] fp32 device output, as ce_partials_sbv_bf16 writes them
+ *             (m, s over the shard's logits; z = target logit or -inf)
+ *   ws        ws_bytes >= flce_workspace_bytes(T, H, V_local), zeroed before
+ *             first use.  Two launches (tensor-core pass, finaliser).
+ * Then: all-gather the partials into [shards][3][T]; ce_merge_partials(...,
+ * S = T, B = 1, V = global vocab, ...) gives the per-token losses, and
+ * rows_mean_f32 their mean (the loss of flce_fwd_bf16 over the whole W, up to
+ * rounding).
+ *
+ * Fused linear + generalized JSD (page "Fused linear + JSD"); beta,
+ * temperature and the keep mask as fljsd_fwd_bf16_ex.  The divergence couples
+ * both heads' normalisers, so there are two exchanges:
+ * fljsd_lse_partials_bf16: shard pass 1.  lse_local [2][T] fp32 device
+ *   output: each head's log-sum-exp of logits / temperature over the shard's
+ *   columns (row 0 = student xs Ws_local^T, row 1 = teacher xt Wt_local^T).
+ *   ws_bytes >= fljsd_workspace_bytes(T, H, V_local).  Two launches.
+ * lse_merge_partials: [shards][2][T] fp32 device (the all-gather of the
+ *   lse_local blocks, in rank order) -> lse [2][T] fp32 device, the global
+ *   log-sum-exps: L = max_j l_j, lse = L + ln(sum_j exp(l_j - L)), in shard
+ *   order.  One launch, no workspace.
+ * fljsd_terms_bf16: shard pass 2.  lse [2][T] fp32 device = the global
+ *   log-sum-exps; terms [T] fp32 device output: each token's sum over the
+ *   shard's columns of beta P ln(P/M) + (1 - beta) Q ln(Q/M), with P, Q from
+ *   the global normalisers.  ws as pass 1 (the same workspace may serve both,
+ *   one after the other).  Two launches.
+ * jsd_merge_terms: [shards][T] fp32 device (the all-gather of the terms) ->
+ *   rows [T] fp32 device (16-byte aligned): each token's JSD, the shards'
+ *   sums added in shard order (0 where keep[i] == 0; keep [T] uint8 device or
+ *   NULL); loss [1] fp32 device: their batchmean over the kept tokens (0 when
+ *   none is kept).  Two launches, no workspace.
+ * The shards must cover [0, V) exactly once (not checked); every shard uses
+ * the same beta, temperature and inputs x.  Accumulation in fp32.
+ * ------------------------------------------------------------------------ */
+int flce_partials_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t* target, int64_t T,
+                       int64_t H, int64_t V_local, int64_t vocab_start, float* partials, void* ws,
+                       size_t ws_bytes, void* stream);
+int fljsd_lse_partials_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_t* xt,
+                            const uint16_t* Wt_local, int64_t T, int64_t H, int64_t V_local,
+                            float temperature, float* lse_local, void* ws, size_t ws_bytes,
+                            void* stream);
+int lse_merge_partials(const float* parts, int64_t shards, int64_t T, float* lse, void* stream);
+int fljsd_terms_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_t* xt,
+                     const uint16_t* Wt_local, const float* lse, int64_t T, int64_t H,
+                     int64_t V_local, float beta, float temperature, float* terms, void* ws,
+                     size_t ws_bytes, void* stream);
+int jsd_merge_terms(const float* terms, int64_t shards, int64_t T, const uint8_t* keep,
+                    float* rows, float* loss, void* stream);
+
+/* Deterministic mean of n fp32 values (rows 16-byte aligned, device) over
+ * those with keep[i] != 0 (keep [n] uint8 device, or NULL = all; 0 when none
+ * is kept) -> mean [1] fp32 device: compensated fp32 in a fixed order,
+ * bitwise reproducible.  One launch, no workspace. */
+int rows_mean_f32(const float* rows, int64_t n, const uint8_t* keep, float* mean, void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused linear + generalized JSD, forward and the student's backward (the
  * teacher is held fixed, as in distillation).  Loss as fljsd_fwd_bf16_ex;
  * gradients of grad_scale * loss with respect to the student input and head:
@@ -375,7 +442,10 @@ int lmho_set_raster_group(int group_m);
  * mean kernel together: an event between them would break their overlap),
  * ce_fwd_sbv_bf16 1, ce_partials_sbv_bf16 1, ce_merge_partials 1,
  * flce_fwd_bf16 2 (tensor-core pass, finaliser), fljsd_fwd_bf16 4
- * (log-sum-exp pass, finaliser, divergence pass, finaliser).  Calls made by
+ * (log-sum-exp pass, finaliser, divergence pass, finaliser),
+ * flce_partials_bf16, fljsd_lse_partials_bf16 and fljsd_terms_bf16 2 each
+ * (tensor-core pass, finaliser), lse_merge_partials 1, jsd_merge_terms 1
+ * (the merge and its dependent mean together), rows_mean_f32 1.  Calls made by
  * other threads are not affected.  Pass (NULL, 0) to turn it off. */
 void lmho_set_launch_events(void* const* events, int n);
 

@@ -38,6 +38,8 @@ EXPORTS = (
     "flce_workspace_bytes", "flce_fwd_bf16", "flce_bwd_workspace_bytes", "flce_fwd_bwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "fljsd_bwd_workspace_bytes", "fljsd_fwd_bwd_bf16",
     "flce_cpo_workspace_bytes", "flce_cpo_fwd_bf16", "flce_cpo_bwd_workspace_bytes", "flce_cpo_fwd_bwd_bf16",
+    "flce_partials_bf16", "fljsd_lse_partials_bf16", "lse_merge_partials", "fljsd_terms_bf16", "jsd_merge_terms",
+    "rows_mean_f32",
     "lmho_ws_status", "lmho_probe_read", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
 
@@ -110,6 +112,18 @@ def load():
         lib.flce_cpo_fwd_bwd_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, f32, f32, f32, vp, vp, vp, vp, vp, sz,
                                               vp]
         lib.flce_cpo_fwd_bwd_bf16.restype = ci
+        lib.flce_partials_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, sz, vp]
+        lib.flce_partials_bf16.restype = ci
+        lib.fljsd_lse_partials_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, sz, vp]
+        lib.fljsd_lse_partials_bf16.restype = ci
+        lib.lse_merge_partials.argtypes = [vp, i64, i64, vp, vp]
+        lib.lse_merge_partials.restype = ci
+        lib.fljsd_terms_bf16.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, f32, f32, vp, vp, sz, vp]
+        lib.fljsd_terms_bf16.restype = ci
+        lib.jsd_merge_terms.argtypes = [vp, i64, i64, vp, vp, vp, vp]
+        lib.jsd_merge_terms.restype = ci
+        lib.rows_mean_f32.argtypes = [vp, i64, vp, vp, vp]
+        lib.rows_mean_f32.restype = ci
         lib.lmho_probe_read.argtypes = [vp, i64, i64, vp, vp]
         lib.lmho_probe_read.restype = ci
         lib.lmho_ws_status.argtypes = [vp, sz, vp]
@@ -561,6 +575,149 @@ def fljsd_fwd_bwd_bf16(xs, Ws, xt, Wt, beta=0.5, temperature=1.0, keep=None, gra
                                       _dev(dWs, "dWs", torch.float32, 2), _dev(ws, "ws", torch.uint8), ws.numel(),
                                       _stream(stream)), "fljsd_fwd_bwd_bf16")
     return loss, dxs, dWs
+
+
+# ---------------------------------------------------------------- vocab-parallel fused losses
+def _shard_pair(xs, Ws_local, xt, Wt_local):
+    pxs = _dev(xs, "xs", torch.bfloat16, 2)
+    pws = _dev(Ws_local, "Ws_local", torch.bfloat16, 2)
+    pxt = _dev(xt, "xt", torch.bfloat16, 2)
+    pwt = _dev(Wt_local, "Wt_local", torch.bfloat16, 2)
+    T, H = xs.shape
+    Vl = Ws_local.shape[0]
+    if tuple(xt.shape) != (T, H) or tuple(Ws_local.shape) != (Vl, H) or tuple(Wt_local.shape) != (Vl, H):
+        raise ValueError("shape mismatch: xs, xt [T,H], Ws_local, Wt_local [V_local,H]")
+    return (pxs, pws, pxt, pwt), T, H, Vl
+
+
+def _keep_ptr(keep, T):
+    """Device pointer of a token mask (CUDA uint8 or bool [T]; None = all kept)."""
+    if keep is None:
+        return None
+    if keep.dtype == torch.bool:
+        keep = keep.view(torch.uint8)
+    pk = _dev(keep, "keep", torch.uint8, 1)
+    if keep.shape[0] != T:
+        raise ValueError("keep must be [T]")
+    return pk
+
+
+def flce_partials_bf16(x, W_local, target, vocab_start, partials=None, ws=None, stream=None):
+    """One vocabulary shard of the fused linear + CE: W_local [V_local, H] bf16
+    holds the global vocab rows [vocab_start, vocab_start + V_local); x [T, H]
+    bf16; target [T] int64 global indices.  Returns fp32 [3, T]: the shard's
+    max and sum of exp of x W_local^T per token, and the target logit (-inf
+    where the target is not in this shard).  Merge the shards' blocks with
+    ce_merge_partials(all.view(k, 3, T, 1), target.view(T, 1), V)."""
+    lib = load()
+    px = _dev(x, "x", torch.bfloat16, 2)
+    pw = _dev(W_local, "W_local", torch.bfloat16, 2)
+    pt = _dev(target, "target", torch.int64, 1)
+    T, H = x.shape
+    Vl = W_local.shape[0]
+    if W_local.shape[1] != H or target.shape[0] != T:
+        raise ValueError("shape mismatch: x [T,H], W_local [V_local,H], target [T]")
+    if partials is None:
+        partials = torch.empty((3, T), dtype=torch.float32, device=x.device)
+    if tuple(partials.shape) != (3, T):
+        raise ValueError("partials must be [3, T]")
+    if ws is None:
+        ws = workspace(lib.flce_workspace_bytes(T, H, Vl), x.device)
+    with _on(x, W_local, target, partials, ws):
+        _check(lib.flce_partials_bf16(px, pw, pt, T, H, Vl, int(vocab_start), _dev(partials, "partials", torch.float32, 2),
+                                      _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "flce_partials_bf16")
+    return partials
+
+
+def fljsd_lse_partials_bf16(xs, Ws_local, xt, Wt_local, temperature=1.0, out=None, ws=None, stream=None):
+    """Vocab-parallel fused linear + JSD, shard pass 1: fp32 [2, T], each
+    head's log-sum-exp of logits / temperature over the shard's columns
+    (0 = student xs Ws_local^T, 1 = teacher xt Wt_local^T)."""
+    lib = load()
+    ptrs, T, H, Vl = _shard_pair(xs, Ws_local, xt, Wt_local)
+    if out is None:
+        out = torch.empty((2, T), dtype=torch.float32, device=xs.device)
+    if tuple(out.shape) != (2, T):
+        raise ValueError("out must be [2, T]")
+    if ws is None:
+        ws = workspace(lib.fljsd_workspace_bytes(T, H, Vl), xs.device)
+    with _on(xs, Ws_local, xt, Wt_local, out, ws):
+        _check(lib.fljsd_lse_partials_bf16(*ptrs, T, H, Vl, float(temperature), _dev(out, "out", torch.float32, 2),
+                                           _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)),
+               "fljsd_lse_partials_bf16")
+    return out
+
+
+def lse_merge_partials(parts, out=None, stream=None):
+    """Global log-sum-exps fp32 [2, T] from every shard's [shards, 2, T] (shard order)."""
+    lib = load()
+    pp = _dev(parts, "parts", torch.float32, 3)
+    k, two, T = parts.shape
+    if two != 2:
+        raise ValueError("parts must be [shards, 2, T]")
+    if out is None:
+        out = torch.empty((2, T), dtype=torch.float32, device=parts.device)
+    if tuple(out.shape) != (2, T):
+        raise ValueError("out must be [2, T]")
+    with _on(parts, out):
+        _check(lib.lse_merge_partials(pp, k, T, _dev(out, "out", torch.float32, 2), _stream(stream)),
+               "lse_merge_partials")
+    return out
+
+
+def fljsd_terms_bf16(xs, Ws_local, xt, Wt_local, lse, beta=0.5, temperature=1.0, out=None, ws=None, stream=None):
+    """Vocab-parallel fused linear + JSD, shard pass 2: with the global
+    log-sum-exps lse fp32 [2, T], each token's sum of the JSD terms over the
+    shard's columns, fp32 [T]."""
+    lib = load()
+    ptrs, T, H, Vl = _shard_pair(xs, Ws_local, xt, Wt_local)
+    pl = _dev(lse, "lse", torch.float32, 2)
+    if tuple(lse.shape) != (2, T):
+        raise ValueError("lse must be [2, T]")
+    if out is None:
+        out = torch.empty(T, dtype=torch.float32, device=xs.device)
+    if tuple(out.shape) != (T,):
+        raise ValueError("out must be [T]")
+    if ws is None:
+        ws = workspace(lib.fljsd_workspace_bytes(T, H, Vl), xs.device)
+    with _on(xs, Ws_local, xt, Wt_local, lse, out, ws):
+        _check(lib.fljsd_terms_bf16(*ptrs, pl, T, H, Vl, float(beta), float(temperature),
+                                    _dev(out, "out", torch.float32, 1), _dev(ws, "ws", torch.uint8), ws.numel(),
+                                    _stream(stream)), "fljsd_terms_bf16")
+    return out
+
+
+def jsd_merge_terms(terms, keep=None, rows=None, loss=None, stream=None):
+    """Per-token JSD fp32 [T] from every shard's term sums [shards, T] (shard
+    order; 0 where keep == 0) and its batchmean over the kept tokens: returns
+    (loss [1], rows [T])."""
+    lib = load()
+    pt = _dev(terms, "terms", torch.float32, 2)
+    k, T = terms.shape
+    pk = _keep_ptr(keep, T)
+    if rows is None:
+        rows = torch.empty(T, dtype=torch.float32, device=terms.device)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=terms.device)
+    if tuple(rows.shape) != (T,):
+        raise ValueError("rows must be [T]")
+    with _on(terms, rows, loss, keep):
+        _check(lib.jsd_merge_terms(pt, k, T, pk, _dev(rows, "rows", torch.float32, 1), _dev(loss, "loss", torch.float32),
+                                   _stream(stream)), "jsd_merge_terms")
+    return loss, rows
+
+
+def rows_mean(rows, keep=None, out=None, stream=None):
+    """Deterministic mean fp32 [1] of rows fp32 [n] (over keep != 0 when given)."""
+    lib = load()
+    pr = _dev(rows, "rows", torch.float32, 1)
+    n = rows.shape[0]
+    pk = _keep_ptr(keep, n)
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=rows.device)
+    with _on(rows, out, keep):
+        _check(lib.rows_mean_f32(pr, n, pk, _dev(out, "out", torch.float32), _stream(stream)), "rows_mean_f32")
+    return out
 
 
 def row_losses(ws: torch.Tensor, T: int) -> torch.Tensor:

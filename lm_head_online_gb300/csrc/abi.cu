@@ -621,6 +621,128 @@ int fljsd_fwd_bf16_ex(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt
   return fljsd_impl(xs, Ws, xt, Wt, T, H, V, beta, temperature, keep, loss, ws, ws_bytes, stream);
 }
 
+// ---------------------------------------------------------------- vocab-parallel fused losses
+int flce_partials_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t* target, int64_t T, int64_t H,
+                       int64_t V_local, int64_t vocab_start, float* partials, void* ws, size_t ws_bytes,
+                       void* stream) {
+  if (!x || !W_local || !target || !partials || !ws) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_fused_common(T, H, V_local)) return c;
+  if (vocab_start < 0 || vocab_start > (int64_t(1) << 62)) return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_local)) return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < flce_ws_bytes(T, H, V_local) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const Range in[3] = {rng(x, 2 * static_cast<size_t>(T) * H), rng(W_local, 2 * static_cast<size_t>(V_local) * H),
+                       rng(target, 8 * static_cast<size_t>(T))};
+  const Range out[2] = {rng(partials, 12 * static_cast<size_t>(T)), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 3, out, 2)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  CUtensorMap tx, tw;
+  if (tmap_bf16(&tx, x, T, H, kBM) || tmap_bf16(&tw, W_local, V_local, H, kBoxBFwd)) return LMHO_ERR_CUDA;
+  const FusedGeometry g = geometry(T, H, V_local, kBN_CE);
+  const FusedWs w = flce_ws_carve(ws, ws_bytes, T, V_local);
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_flce_partials(tx, tw, target, vocab_start, g, partials, w, L));
+}
+
+namespace {
+// Arguments shared by the two shard passes of the vocab-parallel fused JSD.
+int check_jsd_shard(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, const uint16_t* Wt, int64_t T,
+                    int64_t H, int64_t V_local, float temperature, void* ws, size_t ws_bytes) {
+  if (!xs || !Ws || !xt || !Wt || !ws) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_fused_common(T, H, V_local)) return c;
+  if (!(temperature > 0.f) || !(1.f / temperature < INFINITY)) return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(xs) || !aligned16(Ws) || !aligned16(xt) || !aligned16(Wt)) return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < fljsd_ws_bytes(T, H, V_local) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  return LMHO_OK;
+}
+}  // namespace
+
+int fljsd_lse_partials_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_t* xt, const uint16_t* Wt_local,
+                            int64_t T, int64_t H, int64_t V_local, float temperature, float* lse_local, void* ws,
+                            size_t ws_bytes, void* stream) {
+  if (!lse_local) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_jsd_shard(xs, Ws_local, xt, Wt_local, T, H, V_local, temperature, ws, ws_bytes)) return c;
+  const size_t xb = 2 * static_cast<size_t>(T) * H, wb = 2 * static_cast<size_t>(V_local) * H;
+  const Range in[4] = {rng(xs, xb), rng(Ws_local, wb), rng(xt, xb), rng(Wt_local, wb)};
+  const Range out[2] = {rng(lse_local, 8 * static_cast<size_t>(T)), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 4, out, 2)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  CUtensorMap txs, txt, tws, twt;
+  if (tmap_bf16(&txs, xs, T, H, kBM) || tmap_bf16(&txt, xt, T, H, kBM) ||
+      tmap_bf16(&tws, Ws_local, V_local, H, kBoxBFwd) || tmap_bf16(&twt, Wt_local, V_local, H, kBoxBFwd))
+    return LMHO_ERR_CUDA;
+  const FusedGeometry g = geometry(T, H, V_local, kBN_CE);
+  const FusedWs w = fljsd_ws_carve(ws, ws_bytes, T, V_local);
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_fljsd_lse_shard(txs, tws, txt, twt, g, 1.f / temperature, lse_local, w, L));
+}
+
+int lse_merge_partials(const float* parts, int64_t shards, int64_t T, float* lse, void* stream) {
+  if (!parts || !lse) return LMHO_ERR_INVALID_ARG;
+  if (shards <= 0 || shards > (int64_t(1) << 20) || T <= 0 || T > (int64_t(1) << 31) - 1)
+    return LMHO_ERR_INVALID_ARG;
+  const Range in[1] = {rng(parts, 8 * static_cast<size_t>(T) * static_cast<size_t>(shards))};
+  const Range out[1] = {rng(lse, 8 * static_cast<size_t>(T))};
+  if (int a = check_alias(in, 1, out, 1)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  return cuda_status(launch_lse_merge(parts, shards, T, lse, sms, static_cast<cudaStream_t>(stream)));
+}
+
+int fljsd_terms_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_t* xt, const uint16_t* Wt_local,
+                     const float* lse, int64_t T, int64_t H, int64_t V_local, float beta, float temperature,
+                     float* terms, void* ws, size_t ws_bytes, void* stream) {
+  if (!lse || !terms) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_jsd_shard(xs, Ws_local, xt, Wt_local, T, H, V_local, temperature, ws, ws_bytes)) return c;
+  if (!(beta > 0.f && beta < 1.f)) return LMHO_ERR_INVALID_ARG;
+  const size_t xb = 2 * static_cast<size_t>(T) * H, wb = 2 * static_cast<size_t>(V_local) * H;
+  const Range in[5] = {rng(xs, xb), rng(Ws_local, wb), rng(xt, xb), rng(Wt_local, wb),
+                       rng(lse, 8 * static_cast<size_t>(T))};
+  const Range out[2] = {rng(terms, 4 * static_cast<size_t>(T)), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 5, out, 2)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  CUtensorMap txs, txt, tws, twt;
+  if (tmap_bf16(&txs, xs, T, H, kBM) || tmap_bf16(&txt, xt, T, H, kBM) ||
+      tmap_bf16(&tws, Ws_local, V_local, H, kBN_JSD) || tmap_bf16(&twt, Wt_local, V_local, H, kBN_JSD))
+    return LMHO_ERR_CUDA;
+  const FusedGeometry g = geometry(T, H, V_local, kBN_JSD, kGroupTwoHead);
+  const FusedWs w = fljsd_ws_carve(ws, ws_bytes, T, V_local);
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_fljsd_terms_shard(txs, tws, txt, twt, g, lse, beta, 1.f / temperature, terms, w, L));
+}
+
+int jsd_merge_terms(const float* terms, int64_t shards, int64_t T, const uint8_t* keep, float* rows, float* loss,
+                    void* stream) {
+  if (!terms || !rows || !loss) return LMHO_ERR_INVALID_ARG;
+  if (shards <= 0 || shards > (int64_t(1) << 20) || T <= 0 || T > (int64_t(1) << 31) - 1)
+    return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(rows)) return LMHO_ERR_INVALID_ARG;  // the mean reads 16-byte vectors
+  const Range in[2] = {rng(terms, 4 * static_cast<size_t>(T) * static_cast<size_t>(shards)),
+                       rng(keep, keep ? static_cast<size_t>(T) : 0)};
+  const Range out[2] = {rng(rows, 4 * static_cast<size_t>(T)), rng(loss, 4)};
+  if (int a = check_alias(in, 2, out, 2)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  return cuda_status(launch_jsd_merge(terms, shards, T, keep, rows, loss, sms, static_cast<cudaStream_t>(stream)));
+}
+
+int rows_mean_f32(const float* rows, int64_t n, const uint8_t* keep, float* mean, void* stream) {
+  if (!rows || !mean) return LMHO_ERR_INVALID_ARG;
+  if (n <= 0 || n > (int64_t(1) << 31) - 1) return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(rows)) return LMHO_ERR_INVALID_ARG;
+  const Range in[2] = {rng(rows, 4 * static_cast<size_t>(n)), rng(keep, keep ? static_cast<size_t>(n) : 0)};
+  const Range out[1] = {rng(mean, 4)};
+  if (int a = check_alias(in, 2, out, 1)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  return cuda_status(launch_rows_mean(rows, n, keep, mean, static_cast<cudaStream_t>(stream)));
+}
+
 size_t fljsd_bwd_workspace_bytes(int64_t T, int64_t H, int64_t V) {
   if (T <= 0 || V <= 0 || H <= 0) return kAlign;
   return fljsd_bwd_ws_bytes(T, H, V);

@@ -142,6 +142,7 @@ struct Params {
   int32_t num_m, num_n, group_m, k_blocks;
   int64_t units;
   const int64_t* target;  // CE
+  int64_t v0;             // CE: first global vocab column of W (a vocabulary shard; 0 = the whole vocabulary)
   float* part0;
   float* part1;
   float* part2;
@@ -567,7 +568,10 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
       const int64_t n0 = static_cast<int64_t>(c.nt) * BN + half * kCols;
       int64_t tgt = -1;
       float ls = 0.f, lt = 0.f;
-      if ((MODE == kModeCE || MODE == kModeDZ) && row_ok) tgt = __ldg(p.target + row);
+      if ((MODE == kModeCE || MODE == kModeDZ) && row_ok) {
+        tgt = __ldg(p.target + row);
+        if (MODE == kModeCE) tgt = tgt >= p.v0 ? tgt - p.v0 : -1;  // column within this W (shard)
+      }
       float gdz = 0.f;
       if (MODE == kModeDZ && row_ok) {
         ls = __ldg(p.lse + row);
@@ -794,8 +798,8 @@ constexpr int kFinSplit = 16;  // warps per block, each merging a slice of the v
 // Merge (m, s) partials [num_n][T] of each row, in vocab-tile order, into
 // its log-sum-exp.  Warp w handles tiles [w*cnt, (w+1)*cnt); the kFinSplit results
 // merge in warp order.
-__device__ __forceinline__ float merge_lse_row(const float* pm, const float* ps, int64_t T, int num_n,
-                                               int64_t row, MS* s_tmp) {
+__device__ __forceinline__ MS merge_ms_row(const float* pm, const float* ps, int64_t T, int num_n, int64_t row,
+                                           MS* s_tmp) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   const int cnt = (num_n + kFinSplit - 1) / kFinSplit;
   const int n_lo = min(num_n, w * cnt), n_hi = min(num_n, n_lo + cnt);
@@ -812,7 +816,12 @@ __device__ __forceinline__ float merge_lse_row(const float* pm, const float* ps,
   MS tot = s_tmp[l];
   for (int k = 1; k < kFinSplit; ++k) tot = ms_merge(tot, s_tmp[k * 32 + l]);
   __syncthreads();
-  return tot.m + logf(tot.s);  // meaningful in warp 0
+  return tot;  // meaningful in warp 0
+}
+__device__ __forceinline__ float merge_lse_row(const float* pm, const float* ps, int64_t T, int num_n,
+                                               int64_t row, MS* s_tmp) {
+  const MS tot = merge_ms_row(pm, ps, T, num_n, row, s_tmp);
+  return tot.m + logf(tot.s);
 }
 
 __global__ void __launch_bounds__(kFinRows * kFinSplit)
@@ -829,6 +838,26 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
     if (lse_out) lse_out[row] = lse;
   }
   mean_tail(row_out, T, loss, ctrl, gridDim.x);
+}
+
+// One vocabulary shard of the fused linear + CE (W = the global rows [v0, v0 + V)):
+// each token's (max, sum of exp) over the shard, merged over its vocab tiles
+// as in flce_finalize, and its target logit when the (global) target is in
+// the shard, else -inf; written as part [3][T] (m, s, z).
+__global__ void __launch_bounds__(kFinRows * kFinSplit)
+    flce_partials_finalize(const float* pm, const float* ps, const float* pz, const int64_t* target, int64_t T,
+                           int64_t V, int64_t v0, int num_n, float* part) {
+  __shared__ MS s_tmp[kFinRows * kFinSplit];
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kFinRows + (threadIdx.x & 31);
+  const MS tot = merge_ms_row(pm, ps, T, num_n, row, s_tmp);
+  if (threadIdx.x < 32 && row < T) {
+    const int64_t t = __ldg(target + row);
+    float zt = -INFINITY;
+    if (t >= v0 && t - v0 < V) zt = __ldcg(pz + ((t - v0) / kBN_CE) * T + row);
+    part[row] = tot.m;
+    part[T + row] = tot.s;
+    part[2 * T + row] = zt;
+  }
 }
 
 __global__ void __launch_bounds__(kFinRows * kFinSplit)
@@ -876,7 +905,7 @@ __global__ void __launch_bounds__(kFinRows * kFinSplit)
       kl_out[row] = tot.s - tot.c;
     }
   }
-  mean_tail(row_out, T, loss, ctrl, gridDim.x, keep, inv_count_out);
+  if (loss) mean_tail(row_out, T, loss, ctrl, gridDim.x, keep, inv_count_out);  // null: per-row sums only
 }
 
 // CPO from the per-token CE losses rows [B * S] (published objective, Xu et
@@ -1097,6 +1126,67 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, 
       ws.part0, g_jsd.T, static_cast<int>(g_jsd.num_n * ModeCfg<kModeJSD>::kColSplit), keep, ws.row_out, loss,
       ws.ctrl);
   launch_mark(4, L.stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flce_partials(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const int64_t* target, int64_t v0,
+                                 const FusedGeometry& g, float* partials, const FusedWs& ws, const FusedLaunch& L) {
+  Params p = base_params<kModeCE>(g, L, ws.ctrl);
+  p.units = static_cast<int64_t>(p.num_m) * p.num_n;
+  p.target = target;
+  p.v0 = v0;
+  p.part0 = ws.part0;
+  p.part1 = ws.part1;
+  p.part2 = ws.part2;
+  launch_mark(0, L.stream);
+  cudaError_t e = launch_gemm<kModeCE>(tm_x, tm_w, tm_x, tm_w, p, L);
+  if (e != cudaSuccess) return e;
+  launch_mark(1, L.stream);
+  const unsigned blocks = static_cast<unsigned>((g.T + kFinRows - 1) / kFinRows);
+  flce_partials_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(
+      ws.part0, ws.part1, ws.part2, target, g.T, g.V, v0, static_cast<int>(g.num_n), partials);
+  launch_mark(2, L.stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fljsd_lse_shard(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, const CUtensorMap& tm_xt,
+                                   const CUtensorMap& tm_wt256, const FusedGeometry& g_lse, float inv_tau,
+                                   float* lse_local, const FusedWs& ws, const FusedLaunch& L) {
+  Params p = base_params<kModeLSE>(g_lse, L, ws.ctrl);
+  p.units = 2 * static_cast<int64_t>(p.num_m) * p.num_n;
+  p.part0 = ws.part0;
+  p.part1 = ws.part1;
+  p.inv_tau = inv_tau;
+  launch_mark(0, L.stream);
+  cudaError_t e = launch_gemm<kModeLSE>(tm_xs, tm_ws256, tm_xt, tm_wt256, p, L);
+  if (e != cudaSuccess) return e;
+  launch_mark(1, L.stream);
+  dim3 fb(static_cast<unsigned>((g_lse.T + kFinRows - 1) / kFinRows), 2);
+  lse_finalize<<<fb, kFinRows * kFinSplit, 0, L.stream>>>(ws.part0, ws.part1, g_lse.T, static_cast<int>(g_lse.num_n),
+                                                          lse_local);
+  launch_mark(2, L.stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fljsd_terms_shard(const CUtensorMap& tm_xs, const CUtensorMap& tm_wsj, const CUtensorMap& tm_xt,
+                                     const CUtensorMap& tm_wtj, const FusedGeometry& g_jsd, const float* lse,
+                                     float beta, float inv_tau, float* terms, const FusedWs& ws,
+                                     const FusedLaunch& L) {
+  Params q = base_params<kModeJSD>(g_jsd, L, ws.ctrl);
+  q.units = static_cast<int64_t>(q.num_m) * q.num_n;
+  q.part0 = ws.part0;
+  q.lse = lse;
+  q.beta = beta;
+  q.inv_tau = inv_tau;
+  launch_mark(0, L.stream);
+  cudaError_t e = launch_gemm<kModeJSD>(tm_xs, tm_wsj, tm_xt, tm_wtj, q, L);
+  if (e != cudaSuccess) return e;
+  launch_mark(1, L.stream);
+  const unsigned blocks = static_cast<unsigned>((g_jsd.T + kFinRows - 1) / kFinRows);
+  jsd_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(
+      ws.part0, g_jsd.T, static_cast<int>(g_jsd.num_n * ModeCfg<kModeJSD>::kColSplit), nullptr, terms, nullptr,
+      ws.ctrl);
+  launch_mark(2, L.stream);
   return cudaGetLastError();
 }
 

@@ -163,6 +163,33 @@ cudaError_t launch_fljsd(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256,
                          float inv_tau, const uint8_t* keep, float* loss, const FusedWs& ws,
                          const FusedLaunch& L);
 
+// Vocab-parallel fused losses, one shard of W's rows (the global vocab
+// columns [v0, v0 + g.V)):
+//  * fused linear + CE: each token's (max, sum of exp, target logit or -inf)
+//    over the shard -> partials [3][T] (m, s, z);
+cudaError_t launch_flce_partials(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const int64_t* target, int64_t v0,
+                                 const FusedGeometry& g, float* partials, const FusedWs& ws, const FusedLaunch& L);
+//  * fused linear + JSD, first pass: each head's log-sum-exp of logits / tau
+//    over the shard -> lse_local [2][T];
+cudaError_t launch_fljsd_lse_shard(const CUtensorMap& tm_xs, const CUtensorMap& tm_ws256, const CUtensorMap& tm_xt,
+                                   const CUtensorMap& tm_wt256, const FusedGeometry& g_lse, float inv_tau,
+                                   float* lse_local, const FusedWs& ws, const FusedLaunch& L);
+//  * fused linear + JSD, second pass: with the global log-sum-exps lse [2][T],
+//    each token's sum of the JSD terms over the shard's columns -> terms [T].
+cudaError_t launch_fljsd_terms_shard(const CUtensorMap& tm_xs, const CUtensorMap& tm_wsj, const CUtensorMap& tm_xt,
+                                     const CUtensorMap& tm_wtj, const FusedGeometry& g_jsd, const float* lse,
+                                     float beta, float inv_tau, float* terms, const FusedWs& ws,
+                                     const FusedLaunch& L);
+// Their combinations (vp_merge.cu): global log-sum-exps [2][T] from k shards'
+// [k][2][T]; per-token JSD rows [T] and their batchmean from k shards' term
+// sums [k][T] (keep may be null); and the deterministic mean of n values
+// (16-byte aligned) over the kept ones.
+cudaError_t launch_lse_merge(const float* parts, int64_t shards, int64_t T, float* lse, int num_sms,
+                             cudaStream_t st);
+cudaError_t launch_jsd_merge(const float* terms, int64_t shards, int64_t T, const uint8_t* keep, float* rows,
+                             float* loss, int num_sms, cudaStream_t st);
+cudaError_t launch_rows_mean(const float* rows, int64_t n, const uint8_t* keep, float* mean, cudaStream_t st);
+
 // Records the caller's measurement event `i` on `st` if the hook is set
 // (lmho_set_launch_events); no-op otherwise.
 void launch_mark(int i, cudaStream_t st);

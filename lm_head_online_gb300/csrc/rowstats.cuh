@@ -267,10 +267,17 @@ struct KSum {
 // flight); warp 0 then folds 8 lane sums per lane (compensated) and finishes
 // with a butterfly whose partners add the same two values.  No fp64: its rate
 // on this part is a small fraction of fp32 and a serial fp64 tail costs tens
-// of microseconds.  With a keep mask (uint8 per row, may be null) the divisor
-// is the number of kept rows (a mean over no row is 0); left-out rows must
-// already hold 0 in row_loss.  Loads bypass L1 (the rows were written by
-// other blocks or another grid).
+// of microseconds.  With a keep mask (uint8 per row, may be null) left-out
+// rows count as 0 whatever row_loss holds there, and the divisor is the number
+// of kept rows (a mean over no row is 0).  Loads bypass L1 (the rows were
+// written by other blocks or another grid).
+__device__ __forceinline__ float4 keep_only(float4 q, const uint8_t* keep, int64_t r0) {
+  if (!__ldg(keep + r0)) q.x = 0.f;
+  if (!__ldg(keep + r0 + 1)) q.y = 0.f;
+  if (!__ldg(keep + r0 + 2)) q.z = 0.f;
+  if (!__ldg(keep + r0 + 3)) q.w = 0.f;
+  return q;
+}
 __device__ __forceinline__ void mean_sum(const float* row_loss, int64_t T, float* loss, const uint8_t* keep = nullptr,
                                          float* inv_count_out = nullptr) {
   constexpr int kVL = 256;
@@ -289,6 +296,10 @@ __device__ __forceinline__ void mean_sum(const float* row_loss, int64_t T, float
       float4 q[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) q[k] = __ldcg(v4 + i + k * kVL);
+      if (keep) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) q[k] = keep_only(q[k], keep, 4 * (i + k * kVL));
+      }
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         a.add(q[k].x); a.add(q[k].y); a.add(q[k].z); a.add(q[k].w);
@@ -298,17 +309,22 @@ __device__ __forceinline__ void mean_sum(const float* row_loss, int64_t T, float
       float4 q[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) q[k] = __ldcg(v4 + i + k * kVL);
+      if (keep) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = keep_only(q[k], keep, 4 * (i + k * kVL));
+      }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         a.add(q[k].x); a.add(q[k].y); a.add(q[k].z); a.add(q[k].w);
       }
     }
     for (; i < n4; i += kVL) {
-      const float4 q = __ldcg(v4 + i);
+      float4 q = __ldcg(v4 + i);
+      if (keep) q = keep_only(q, keep, 4 * i);
       a.add(q.x); a.add(q.y); a.add(q.z); a.add(q.w);
     }
     if (j == 0)
-      for (int64_t r = n4 * 4; r < T; ++r) a.add(__ldcg(row_loss + r));
+      for (int64_t r = n4 * 4; r < T; ++r) a.add((keep && !__ldg(keep + r)) ? 0.f : __ldcg(row_loss + r));
     s_part[j] = a.s - a.c;
   }
   __syncthreads();

@@ -13,6 +13,13 @@ all-gather puts every rank's partials on every rank in rank order, and each
 rank merges them into the per-token losses (ce_merge_partials).  12 bytes
 per token per rank cross the link; the logits never do.
 
+The same split of the output layer's rows for the fused losses: the fused CE
+exchanges the same 12 bytes per token (flce_partials_bf16); the fused JSD
+exchanges twice, each head's log-sum-exp over the shard (8 bytes per token,
+then lse_merge_partials) and then the shard's sum of JSD terms (4 bytes per
+token, then jsd_merge_terms), since the divergence needs both heads' global
+normalisers.
+
 These run over any torch.distributed backend (NCCL between GPUs, gloo on CPU).
 """
 from __future__ import annotations
@@ -85,3 +92,33 @@ def vocab_parallel_ce(logits_local, target, vocab_start: int, V: int, group=None
         dist.all_gather_into_tensor(gathered.view((-1,) + tuple(part.shape[1:])), part, group=group)
         allp = gathered
     return ce_merge_partials(allp, target, V)
+
+
+def vocab_parallel_flce(x, W_local, target, vocab_start: int, V: int, group=None, ws=None):
+    """Fused linear + CE with the output layer's rows sharded over the ranks
+    of `group`: this rank holds W_local = the global rows [vocab_start,
+    vocab_start + V_local) of W, bf16 [V_local, H]; x [T, H] bf16 and target
+    [T] int64 (global indices) are the same on every rank.  Returns (mean loss
+    [1], per-token losses [T]), the same on every rank."""
+    from lm_head_online_gb300 import ce_merge_partials, flce_partials_bf16, rows_mean
+
+    T = target.shape[0]
+    part = flce_partials_bf16(x, W_local, target, vocab_start, ws=ws)     # [3, T]
+    allp = gather_partials(part, group)                                    # [world, 3, T]
+    rows = ce_merge_partials(allp.view(allp.shape[0], 3, T, 1), target.view(T, 1), V).view(T)
+    return rows_mean(rows), rows
+
+
+def vocab_parallel_fljsd(xs, Ws_local, xt, Wt_local, beta=0.5, temperature=1.0, keep=None, group=None, ws=None):
+    """Fused linear + generalized JSD with both heads' rows sharded over the
+    ranks of `group` (Ws_local, Wt_local: this rank's rows [V_local, H] of the
+    student and teacher heads, the same vocab range); xs, xt [T, H] and keep
+    are the same on every rank.  Returns (batchmean [1], per-token JSD [T])."""
+    from lm_head_online_gb300 import fljsd_lse_partials_bf16, fljsd_terms_bf16, jsd_merge_terms, lse_merge_partials
+
+    T = xs.shape[0]
+    lse_local = fljsd_lse_partials_bf16(xs, Ws_local, xt, Wt_local, temperature, ws=ws)       # [2, T]
+    lse = lse_merge_partials(gather_partials(lse_local, group))                              # [2, T]
+    terms = fljsd_terms_bf16(xs, Ws_local, xt, Wt_local, lse, beta, temperature, ws=ws)       # [T]
+    all_terms = gather_partials(terms.view(1, T), group).view(-1, T)                         # [world, T]
+    return jsd_merge_terms(all_terms, keep)

@@ -203,6 +203,47 @@ def test_vocab_parallel_argument_checks(lib):
     assert lib.ce_merge_partials(A, 2, B, 2, 2, 16, B, None) == 2               # loss over target
 
 
+def test_vocab_parallel_fused_argument_checks(lib):
+    ws = 1 << 30
+    f = ctypes.c_float
+    E = 0x50000000
+    # flce_partials_bf16(x, W_local, target, T, H, V_local, vocab_start, partials, ws, ws_bytes, stream)
+    assert lib.flce_partials_bf16(None, B, C, 4, 16, 10, 0, D, E, ws, None) == 1         # null x
+    assert lib.flce_partials_bf16(A, B, C, 4, 16, 0, 0, D, E, ws, None) == 1             # V_local = 0
+    assert lib.flce_partials_bf16(A, B, C, 4, 16, 10, -1, D, E, ws, None) == 1           # negative vocab start
+    assert lib.flce_partials_bf16(A, B, C, 4, 12, 10, 0, D, E, ws, None) == 4            # H % 8
+    assert lib.flce_partials_bf16(A, B + 2, C, 4, 16, 10, 0, D, E, ws, None) == 1        # W_local unaligned
+    assert lib.flce_partials_bf16(A, B, C, 4, 16, 10, 0, D, E, 256, None) == 3           # short workspace
+    assert lib.flce_partials_bf16(A, B, C, 4, 16, 10, 0, C + 16, E, ws, None) == 2       # partials over target
+    # fljsd_lse_partials_bf16(xs, Ws, xt, Wt, T, H, V_local, temperature, lse_local, ws, ws_bytes, stream)
+    assert lib.fljsd_lse_partials_bf16(A, B, C, D, 4, 16, 10, f(1.0), None, E, ws, None) == 1
+    assert lib.fljsd_lse_partials_bf16(A, B, C, D, 4, 16, 10, f(0.0), E + (1 << 31), E, ws, None) == 1
+    assert lib.fljsd_lse_partials_bf16(A, B, C, D, 4, 16, 10, f(1.0), E + (1 << 31), E, 256, None) == 3
+    assert lib.fljsd_lse_partials_bf16(A, B, C, D, 4, 16, 10, f(1.0), B + 8, E, ws, None) == 2   # over Ws
+    # lse_merge_partials(parts, shards, T, lse, stream)
+    assert lib.lse_merge_partials(None, 2, 4, C, None) == 1
+    assert lib.lse_merge_partials(A, 0, 4, C, None) == 1
+    assert lib.lse_merge_partials(A, 2, 0, C, None) == 1
+    assert lib.lse_merge_partials(A, 2, 4, A + 32, None) == 2                  # lse inside parts [2][2][4]
+    # fljsd_terms_bf16(xs, Ws, xt, Wt, lse, T, H, V_local, beta, temperature, terms, ws, ws_bytes, stream)
+    assert lib.fljsd_terms_bf16(A, B, C, D, None, 4, 16, 10, f(0.5), f(1.0), E + (1 << 31), E, ws, None) == 1
+    assert lib.fljsd_terms_bf16(A, B, C, D, 0x60000000, 4, 16, 10, f(1.0), f(1.0), E + (1 << 31), E, ws,
+                                None) == 1                                     # beta not in (0, 1)
+    assert lib.fljsd_terms_bf16(A, B, C, D, 0x60000000, 4, 16, 10, f(0.5), f(1.0), 0x60000010, E, ws,
+                                None) == 2                                     # terms over lse
+    # jsd_merge_terms(terms, shards, T, keep, rows, loss, stream)
+    assert lib.jsd_merge_terms(A, 2, 4, None, None, C, None) == 1
+    assert lib.jsd_merge_terms(A, 0, 4, None, B, C, None) == 1
+    assert lib.jsd_merge_terms(A, 2, 4, None, B + 4, C, None) == 1            # rows not 16-byte aligned
+    assert lib.jsd_merge_terms(A, 2, 4, None, A + 16, C, None) == 2           # rows inside terms
+    assert lib.jsd_merge_terms(A, 2, 4, D, B, D + 2, None) == 2               # loss over keep
+    # rows_mean_f32(rows, n, keep, mean, stream)
+    assert lib.rows_mean_f32(None, 4, None, C, None) == 1
+    assert lib.rows_mean_f32(A, 0, None, C, None) == 1
+    assert lib.rows_mean_f32(A + 4, 4, None, C, None) == 1                    # rows not 16-byte aligned
+    assert lib.rows_mean_f32(A, 4, None, A + 8, None) == 2                    # mean inside rows
+
+
 def test_probe_read_argument_checks(lib):
     # lmho_probe_read(data, segments, segment_bytes, out, stream)
     assert lib.lmho_probe_read(None, 4, 64, C, None) == 1

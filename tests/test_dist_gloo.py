@@ -128,3 +128,55 @@ def test_shard_vocab_covers_in_rank_order():
             assert shards[0][0] == 0 and sum(w for _, w in shards) == V
             for (a, wa), (b, _) in zip(shards, shards[1:]):
                 assert a + wa == b
+
+
+def _vp_flce(rank, world):
+    """Each rank: the oracle's shard partials of the fused CE from its rows
+    of W, the exchange through dist.gather_partials, the oracle's merge."""
+    T, H, V = 6, 16, 101
+    x = gen.normal_bf16_bits(5, 0, (T, H), sigma=1.0)
+    W = gen.normal_bf16_bits(5, 1, (V, H), sigma=0.3)
+    t = gen.targets(5, 2, (T,), V)
+    v0, w = lmdist.shard_vocab(V, rank, world)
+    m, s, zt = oracle.flce_partials_bf16(x, np.ascontiguousarray(W[v0:v0 + w]), t, v0)
+    g = lmdist.gather_partials(torch.from_numpy(np.stack([m, s, zt]))).numpy()
+    assert g.shape == (world, 3, T)
+    return oracle.ce_merge(g[:, 0], g[:, 1], g[:, 2], t, V)
+
+
+def _vp_fljsd(rank, world):
+    """Each rank: its heads' rows, the two exchanges of dist.vocab_parallel_fljsd
+    (log-sum-exps [2, T], then term sums [1, T]) with the oracle's shard steps."""
+    T, H, V = 7, 16, 89
+    xs = gen.normal_bf16_bits(6, 0, (T, H), sigma=1.0)
+    Ws = gen.normal_bf16_bits(6, 1, (V, H), sigma=0.3)
+    xt = gen.normal_bf16_bits(6, 2, (T, H), sigma=1.0)
+    Wt = gen.normal_bf16_bits(6, 3, (V, H), sigma=0.3)
+    keep = (np.arange(T) % 3 != 2).astype(np.uint8)
+    v0, w = lmdist.shard_vocab(V, rank, world)
+    a, b = np.ascontiguousarray(Ws[v0:v0 + w]), np.ascontiguousarray(Wt[v0:v0 + w])
+    lse_local = oracle.fljsd_lse_shard_bf16(xs, a, xt, b, 1.5)
+    lse = oracle.lse_merge(lmdist.gather_partials(torch.from_numpy(lse_local)).numpy())
+    terms = oracle.fljsd_terms_shard_bf16(xs, a, xt, b, lse, 0.3, 1.5)
+    allt = lmdist.gather_partials(torch.from_numpy(terms).view(1, T)).view(-1, T).numpy()
+    assert allt.shape == (world, T)
+    return oracle.jsd_merge(allt, keep)
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_vocab_parallel_fused_exchanges_over_gloo_ranks(world):
+    out = spawn(_vp_flce, world=world)
+    T, H, V = 6, 16, 101
+    _, want = oracle.flce_bf16(gen.normal_bf16_bits(5, 0, (T, H), sigma=1.0),
+                               gen.normal_bf16_bits(5, 1, (V, H), sigma=0.3), gen.targets(5, 2, (T,), V))
+    for loss in out.values():
+        np.testing.assert_allclose(loss, want, rtol=1e-12, atol=1e-12)
+    out = spawn(_vp_fljsd, world=world)
+    T, H, V = 7, 16, 89
+    want_mean, want_rows = oracle.fljsd_ex_bf16(
+        gen.normal_bf16_bits(6, 0, (T, H), sigma=1.0), gen.normal_bf16_bits(6, 1, (V, H), sigma=0.3),
+        gen.normal_bf16_bits(6, 2, (T, H), sigma=1.0), gen.normal_bf16_bits(6, 3, (V, H), sigma=0.3), 0.3, 1.5,
+        (np.arange(T) % 3 != 2).astype(np.uint8))
+    for mean, rows in out.values():
+        np.testing.assert_allclose(rows, want_rows, rtol=1e-11, atol=1e-15)
+        assert mean == pytest.approx(want_mean, rel=1e-11)

@@ -214,6 +214,50 @@ def test_vocab_parallel_guards(gpu_lib, S, B, V, shards):
     written(loss)
 
 
+@pytest.mark.parametrize("T,H,V", FUSED)
+def test_vocab_parallel_fused_guards(gpu_lib, T, H, V):
+    """The shard calls of the vocab-parallel fused losses on an uneven 2-way
+    split of W's rows, and their merges, each into guarded outputs."""
+    g = Guarded()
+    x = to_dev_bf16(gen.normal_bf16_bits(26, 0, (T, H)))
+    xt = to_dev_bf16(gen.normal_bf16_bits(26, 3, (T, H)))
+    W = to_dev_bf16(gen.normal_bf16_bits(26, 2, (V, H), sigma=1.0 / math.sqrt(H)))
+    Wt = to_dev_bf16(gen.normal_bf16_bits(26, 4, (V, H), sigma=1.0 / math.sqrt(H)))
+    t = to_dev(gen.targets(26, 1, (T,), V))
+    keep = to_dev((gen.targets(26, 5, (T,), 3) != 0).astype(np.uint8))
+    cut = V // 3 if V > 1 else 1
+    shards = [(0, cut), (cut, V - cut)] if V > 1 else [(0, 1)]
+    before = snapshot(x, xt, W, Wt, t, keep)
+    k = len(shards)
+    parts = g.view(k * 3 * T * 4, torch.float32, (k, 3, T))
+    lparts = g.view(k * 2 * T * 4, torch.float32, (k, 2, T))
+    terms = g.view(k * T * 4, torch.float32, (k, T))
+    for j, (v0, w) in enumerate(shards):
+        ws = g.ws(max(gpu_lib.flce_workspace_bytes(T, H, w), gpu_lib.fljsd_workspace_bytes(T, H, w)))
+        gpu_lib.flce_partials_bf16(x, W[v0:v0 + w], t, v0, partials=parts[j], ws=ws)
+        gpu_lib.fljsd_lse_partials_bf16(x, W[v0:v0 + w], xt, Wt[v0:v0 + w], 1.5, out=lparts[j], ws=ws)
+        g.check()
+        assert gpu_lib.ws_status(ws) == 0
+    lse = g.view(2 * T * 4, torch.float32, (2, T))
+    gpu_lib.lse_merge_partials(lparts, out=lse)
+    for j, (v0, w) in enumerate(shards):
+        ws = g.ws(gpu_lib.fljsd_workspace_bytes(T, H, w))
+        gpu_lib.fljsd_terms_bf16(x, W[v0:v0 + w], xt, Wt[v0:v0 + w], lse, 0.3, 1.5, out=terms[j], ws=ws)
+        g.check()
+        assert gpu_lib.ws_status(ws) == 0
+    rows = g.view(T * 4, torch.float32, (T,))
+    loss = g.view(4, torch.float32, (1,))
+    gpu_lib.jsd_merge_terms(terms, keep, rows=rows, loss=loss)
+    ce_rows = g.view(T * 4, torch.float32, (T, 1))
+    gpu_lib.ce_merge_partials(parts.view(k, 3, T, 1), t.view(T, 1), V, loss=ce_rows)
+    mean = g.view(4, torch.float32, (1,))
+    gpu_lib.rows_mean(ce_rows.view(T), out=mean)
+    g.check()
+    assert not bool(torch.isnan(parts).any()), "a partial was never written"   # -inf is a valid target logit
+    written(lparts, lse, terms, rows, loss, ce_rows, mean)
+    unchanged(before, [x, xt, W, Wt, t, keep])
+
+
 def test_probe_read_guards(gpu_lib):
     g = Guarded()
     words = gen.targets(25, 0, (5 * 4096,), 2 ** 32).astype(np.uint32)

@@ -1,0 +1,310 @@
+"""GPU parity of the vocab-parallel fused losses against the fp64 oracle.
+
+The vocabulary split of the page "Vocab-parallel cross-entropy, Megatron
+layout" (summary: each tensor-parallel rank holds its own vocab range) applied
+to the output layer of the fused losses (pages "Fused linear + CPO loss", its
+cross-entropy core, and "Fused linear + JSD"): a rank holds the rows
+[v0, v0 + V_local) of W.  The ranks are emulated on one GPU: W is cut into k
+uneven row blocks, each copied to its own buffer (a rank's local head); the
+per-shard results are stacked as an all-gather in rank order leaves them and
+merged by the library's merge calls.
+
+Bars: as the unsharded fused tests (per-token CE losses 1e-4 relative;
+per-token JSD 1e-3 relative + 1e-5 absolute; scalars 2e-3 relative).  Shard
+log-sum-exps 1e-5 relative.  With one shard (the whole W) every result must
+equal the unsharded call's bit for bit: the merges of a single block are
+exact and every other step is the same kernel.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from tests.helpers import to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+RTOL_SCALAR = 2e-3
+RTOL_CE_TOKEN = 1e-4
+RTOL_JSD_TOKEN, ATOL_JSD_TOKEN = 1e-3, 1e-5
+RTOL_LSE = 1e-5
+
+
+def uneven_shards(V, k, seed):
+    if k == 1:
+        return [(0, V)]
+    rng = np.random.default_rng(seed)
+    cuts = np.sort(rng.choice(np.arange(1, V), size=k - 1, replace=False))
+    edges = np.concatenate([[0], cuts, [V]])
+    return [(int(a), int(b - a)) for a, b in zip(edges[:-1], edges[1:])]
+
+
+def flce_inputs(seed, T, H, V):
+    x = gen.normal_bf16_bits(seed, gen.STREAM_X, (T, H))
+    W = gen.normal_bf16_bits(seed, gen.STREAM_W, (V, H), sigma=2.0 / math.sqrt(H))
+    t = gen.targets(seed, gen.STREAM_TARGET, (T,), V)
+    return x, W, t
+
+
+def jsd_inputs(seed, T, H, V, sw):
+    xs = gen.normal_bf16_bits(seed, gen.STREAM_X, (T, H))
+    Ws = gen.normal_bf16_bits(seed, gen.STREAM_W, (V, H), sigma=sw)
+    xt = gen.normal_bf16_bits(seed, gen.STREAM_XT, (T, H))
+    Wt = gen.normal_bf16_bits(seed, gen.STREAM_WT, (V, H), sigma=sw)
+    return xs, Ws, xt, Wt
+
+
+def run_flce_vp(lmho, xd, Wd, td, shards, V):
+    """Returns (partials [k, 3, T], per-token losses [T], mean [1])."""
+    T = xd.shape[0]
+    parts = torch.full((len(shards), 3, T), float("nan"), device="cuda")
+    for j, (v0, w) in enumerate(shards):
+        lmho.flce_partials_bf16(xd, Wd[v0:v0 + w].clone(), td, v0, partials=parts[j])
+    rows = lmho.ce_merge_partials(parts.view(len(shards), 3, T, 1), td.view(T, 1), V).view(T)
+    mean = lmho.rows_mean(rows)
+    torch.cuda.synchronize()
+    return parts, rows, mean
+
+
+def run_fljsd_vp(lmho, xsd, Wsd, xtd, Wtd, shards, beta, tau, keep=None):
+    """Returns (lse parts [k, 2, T], lse [2, T], terms [k, T], rows [T], loss [1])."""
+    T = xsd.shape[0]
+    k = len(shards)
+    local = [(Wsd[v0:v0 + w].clone(), Wtd[v0:v0 + w].clone()) for v0, w in shards]
+    lparts = torch.full((k, 2, T), float("nan"), device="cuda")
+    for j, (a, b) in enumerate(local):
+        lmho.fljsd_lse_partials_bf16(xsd, a, xtd, b, tau, out=lparts[j])
+    lse = lmho.lse_merge_partials(lparts)
+    terms = torch.full((k, T), float("nan"), device="cuda")
+    for j, (a, b) in enumerate(local):
+        lmho.fljsd_terms_bf16(xsd, a, xtd, b, lse, beta, tau, out=terms[j])
+    loss, rows = lmho.jsd_merge_terms(terms, keep)
+    torch.cuda.synchronize()
+    return lparts, lse, terms, rows, loss
+
+
+def np64(t):
+    return t.cpu().numpy().astype(np.float64)
+
+
+# ---------------------------------------------------------------- fused linear + CE
+FLCE_VP_CASES = [(64, 64, 300, 2), (200, 128, 1500, 3), (129, 256, 777, 4), (5, 64, 37, 5), (96, 4096, 2000, 3)]
+
+
+@pytest.mark.parametrize("T,H,V,k", FLCE_VP_CASES)
+def test_flce_vp_matches_oracle(gpu_lib, T, H, V, k):
+    x, W, t = flce_inputs(20 + k, T, H, V)
+    shards = uneven_shards(V, k, 3 + k)
+    # targets on every shard's first and last column, then one out of range each way
+    edge = [c for v0, w in shards for c in (v0, v0 + w - 1)]
+    n = min(len(edge), T - 2) if T > 2 else 0
+    t[:n] = edge[:n]
+    if T > 2:
+        t[-2], t[-1] = -1, V
+    parts, rows, mean = run_flce_vp(gpu_lib, to_dev_bf16(x), to_dev_bf16(W), to_dev(t), shards, V)
+    # per shard: the shard log-sum-exp m + ln s, and the target logit or -inf
+    for j, (v0, w) in enumerate(shards):
+        m, s, zt = oracle.flce_partials_bf16(x, np.ascontiguousarray(W[v0:v0 + w]), t, v0)
+        p = np64(parts[j])
+        np.testing.assert_allclose(p[0] + np.log(p[1]), m + np.log(s), rtol=RTOL_LSE, atol=1e-5)
+        own = (t >= v0) & (t < v0 + w)
+        assert np.all(p[2][~own] == -np.inf)
+        np.testing.assert_allclose(p[2][own], zt[own], rtol=1e-5, atol=1e-5)
+    _, want = oracle.flce_bf16(x, W, t)
+    got = np64(rows)
+    bad = (t < 0) | (t >= V)
+    assert np.all(np.isnan(got[bad])) and np.all(np.isnan(want[bad]))
+    np.testing.assert_allclose(got[~bad], want[~bad], rtol=RTOL_CE_TOKEN, atol=1e-5)
+    if not bad.any():
+        assert float(mean.item()) == pytest.approx(want.mean(), rel=RTOL_SCALAR)
+
+
+def test_flce_vp_mean_and_single_shard_bitwise(gpu_lib):
+    """One shard holding all of W gives flce_fwd_bf16's per-token losses and
+    mean bit for bit; three shards give the same within rounding."""
+    T, H, V = 300, 256, 3000
+    x, W, t = flce_inputs(31, T, H, V)
+    xd, Wd, td = to_dev_bf16(x), to_dev_bf16(W), to_dev(t)
+    ws = gpu_lib.workspace(gpu_lib.flce_workspace_bytes(T, H, V))
+    ref = gpu_lib.flce_fwd_bf16(xd, Wd, td, ws=ws)
+    ref_rows = gpu_lib.row_losses(ws, T).clone()
+    _, rows1, mean1 = run_flce_vp(gpu_lib, xd, Wd, td, [(0, V)], V)
+    assert torch.equal(rows1, ref_rows) and torch.equal(mean1, ref)
+    _, rows3, mean3 = run_flce_vp(gpu_lib, xd, Wd, td, uneven_shards(V, 3, 1), V)
+    torch.testing.assert_close(rows3, ref_rows, rtol=1e-5, atol=1e-5)
+    assert float(mean3.item()) == pytest.approx(float(ref.item()), rel=1e-5)
+
+
+def test_flce_vp_deterministic(gpu_lib):
+    T, H, V = 257, 128, 1000
+    x, W, t = flce_inputs(33, T, H, V)
+    xd, Wd, td = to_dev_bf16(x), to_dev_bf16(W), to_dev(t)
+    shards = uneven_shards(V, 3, 7)
+    a = run_flce_vp(gpu_lib, xd, Wd, td, shards, V)
+    b = run_flce_vp(gpu_lib, xd, Wd, td, shards, V)
+    assert all(torch.equal(p, q) for p, q in zip(a, b))
+
+
+def test_flce_vp_full_size_sampled(gpu_lib):
+    """x [2048, 4096], W [128256, 4096] ~ N(0, 0.02^2) split over 8 ranks
+    (16032 rows each, as tensor parallelism 8 would): the merged losses within
+    1e-5 of the unsharded call and sampled tokens against the oracle."""
+    T, H, V, k = 2048, 4096, 128256, 8
+    x = gen.normal_bf16_bits(0, gen.STREAM_X, (T, H))
+    W = gen.normal_bf16_bits(0, gen.STREAM_W, (V, H), sigma=0.02)
+    t = gen.targets(0, gen.STREAM_TARGET, (T,), V)
+    xd, Wd, td = to_dev_bf16(x), to_dev_bf16(W), to_dev(t)
+    shards = [(j * V // k, (j + 1) * V // k - j * V // k) for j in range(k)]
+    _, rows, mean = run_flce_vp(gpu_lib, xd, Wd, td, shards, V)
+    ws = gpu_lib.workspace(gpu_lib.flce_workspace_bytes(T, H, V))
+    ref = gpu_lib.flce_fwd_bf16(xd, Wd, td, ws=ws)
+    torch.testing.assert_close(rows, gpu_lib.row_losses(ws, T), rtol=1e-5, atol=1e-5)
+    assert float(mean.item()) == pytest.approx(float(ref.item()), rel=1e-5)
+    idx = np.array([0, 1, 127, 128, 1023, 1024, 2046, 2047])
+    _, want = oracle.flce_bf16(x[idx], W, t[idx])
+    np.testing.assert_allclose(np64(rows)[idx], want, rtol=RTOL_CE_TOKEN, atol=1e-5)
+
+
+# ---------------------------------------------------------------- fused linear + JSD
+FLJSD_VP_CASES = [(64, 64, 300, 2, 0.5, 1.0, False), (200, 128, 1500, 3, 0.3, 2.0, True),
+                  (129, 256, 777, 4, 0.5, 0.7, False), (5, 64, 37, 5, 0.8, 1.0, True),
+                  (64, 4096, 2000, 3, 0.5, 1.0, False)]
+
+
+@pytest.mark.parametrize("T,H,V,k,beta,tau,masked", FLJSD_VP_CASES)
+def test_fljsd_vp_matches_oracle(gpu_lib, T, H, V, k, beta, tau, masked):
+    xs, Ws, xt, Wt = jsd_inputs(40 + k, T, H, V, sw=2.0 / math.sqrt(H))
+    keep = (np.arange(T) % 4 != 2).astype(np.uint8) if masked else None
+    shards = uneven_shards(V, k, 9 + k)
+    lparts, lse, terms, rows, loss = run_fljsd_vp(gpu_lib, to_dev_bf16(xs), to_dev_bf16(Ws), to_dev_bf16(xt),
+                                                  to_dev_bf16(Wt), shards, beta, tau,
+                                                  None if keep is None else to_dev(keep))
+    sl = [(np.ascontiguousarray(Ws[v0:v0 + w]), np.ascontiguousarray(Wt[v0:v0 + w])) for v0, w in shards]
+    want_parts = np.stack([oracle.fljsd_lse_shard_bf16(xs, a, xt, b, tau) for a, b in sl])
+    np.testing.assert_allclose(np64(lparts), want_parts, rtol=RTOL_LSE, atol=1e-5)
+    want_lse = oracle.lse_merge(want_parts)
+    np.testing.assert_allclose(np64(lse), want_lse, rtol=RTOL_LSE, atol=1e-5)
+    want_terms = np.stack([oracle.fljsd_terms_shard_bf16(xs, a, xt, b, want_lse, beta, tau) for a, b in sl])
+    np.testing.assert_allclose(np64(terms), want_terms, rtol=RTOL_JSD_TOKEN, atol=ATOL_JSD_TOKEN)
+    want_mean, want_rows = oracle.fljsd_ex_bf16(xs, Ws, xt, Wt, beta, tau, keep)
+    np.testing.assert_allclose(np64(rows), want_rows, rtol=RTOL_JSD_TOKEN, atol=ATOL_JSD_TOKEN)
+    if keep is not None:
+        assert np.all(np64(rows)[keep == 0] == 0.0)
+    assert float(loss.item()) == pytest.approx(want_mean, rel=RTOL_SCALAR)
+
+
+@pytest.mark.parametrize("beta,tau,masked", [(0.5, 1.0, False), (0.3, 2.0, True)])
+def test_fljsd_vp_single_shard_is_bitwise_unsharded(gpu_lib, beta, tau, masked):
+    T, H, V = 300, 128, 3000
+    xs, Ws, xt, Wt = jsd_inputs(51, T, H, V, sw=0.2)
+    d = [to_dev_bf16(a) for a in (xs, Ws, xt, Wt)]
+    keep = to_dev((np.arange(T) % 3 != 0).astype(np.uint8)) if masked else None
+    ws = gpu_lib.workspace(gpu_lib.fljsd_workspace_bytes(T, H, V))
+    ref = gpu_lib.fljsd_fwd_bf16_ex(*d, beta, tau, keep, ws=ws)
+    ref_rows = gpu_lib.row_losses(ws, T).clone()
+    _, _, _, rows, loss = run_fljsd_vp(gpu_lib, *d, [(0, V)], beta, tau, keep)
+    assert torch.equal(rows, ref_rows) and torch.equal(loss, ref)
+    _, _, _, rows3, loss3 = run_fljsd_vp(gpu_lib, *d, uneven_shards(V, 3, 2), beta, tau, keep)
+    torch.testing.assert_close(rows3, ref_rows, rtol=1e-4, atol=1e-6)
+    assert float(loss3.item()) == pytest.approx(float(ref.item()), rel=1e-4)
+
+
+def test_fljsd_vp_identical_heads_is_zero(gpu_lib):
+    T, H, V = 70, 128, 2000
+    xs, Ws, _, _ = jsd_inputs(52, T, H, V, sw=0.2)
+    xsd, Wsd = to_dev_bf16(xs), to_dev_bf16(Ws)
+    _, _, terms, rows, loss = run_fljsd_vp(gpu_lib, xsd, Wsd, xsd, Wsd, uneven_shards(V, 3, 4), 0.5, 1.0)
+    assert abs(float(loss.item())) <= 1e-6 and float(terms.abs().max()) <= 1e-6
+
+
+def test_fljsd_vp_full_size_sampled(gpu_lib):
+    """Student/teacher [1024, 4096], heads [128256, 4096] ~ N(0, 0.02^2) split
+    over 4 ranks: the merged per-token JSD within 1e-4 of the unsharded call,
+    sampled tokens against the oracle."""
+    T, H, V, k = 1024, 4096, 128256, 4
+    xs, Ws, xt, Wt = jsd_inputs(0, T, H, V, sw=0.02)
+    d = [to_dev_bf16(a) for a in (xs, Ws, xt, Wt)]
+    shards = [(j * V // k, (j + 1) * V // k - j * V // k) for j in range(k)]
+    _, _, _, rows, loss = run_fljsd_vp(gpu_lib, *d, shards, 0.5, 1.0)
+    ws = gpu_lib.workspace(gpu_lib.fljsd_workspace_bytes(T, H, V))
+    ref = gpu_lib.fljsd_fwd_bf16(*d, 0.5, ws=ws)
+    torch.testing.assert_close(rows, gpu_lib.row_losses(ws, T), rtol=1e-4, atol=1e-6)
+    assert float(loss.item()) == pytest.approx(float(ref.item()), rel=1e-4)
+    idx = np.array([0, 127, 128, 511, 512, 1023])
+    _, want = oracle.fljsd_bf16(xs[idx], Ws, xt[idx], Wt, 0.5)
+    np.testing.assert_allclose(np64(rows)[idx], want, rtol=RTOL_JSD_TOKEN, atol=ATOL_JSD_TOKEN)
+
+
+# ---------------------------------------------------------------- merges alone
+def test_lse_merge_and_rows_mean(gpu_lib):
+    rng = np.random.default_rng(3)
+    parts = rng.normal(0.0, 4.0, (3, 2, 1001)).astype(np.float32)
+    got = np64(gpu_lib.lse_merge_partials(torch.from_numpy(parts).cuda()))
+    want = np.logaddexp(np.logaddexp(parts[0].astype(np.float64), parts[1]), parts[2])
+    np.testing.assert_allclose(got, want, rtol=1e-6, atol=1e-6)
+    rows = torch.from_numpy(rng.normal(1.0, 1.0, 1003).astype(np.float32)).cuda()
+    keep = torch.from_numpy((np.arange(1003) % 5 != 0).astype(np.uint8)).cuda()
+    r = rows.double().cpu().numpy()
+    assert float(gpu_lib.rows_mean(rows).item()) == pytest.approx(r.mean(), rel=1e-6)
+    kk = keep.cpu().numpy() != 0
+    assert float(gpu_lib.rows_mean(rows, keep).item()) == pytest.approx(r[kk].mean(), rel=1e-6)
+    assert float(gpu_lib.rows_mean(rows, torch.zeros_like(keep)).item()) == 0.0
+
+
+# ---------------------------------------------------------------- through dist.py and NCCL
+def _nccl_one_rank(port, q):
+    """Child process: a one-rank NCCL group runs the product helpers; with one
+    rank the shard is the whole head, so they must give the unsharded calls'
+    bits (the all-gathers and merges of one block are exact)."""
+    import os
+
+    import torch.distributed as dist
+
+    import lm_head_online_gb300 as lmho
+    from lm_head_online_gb300 import dist as lmdist
+
+    try:
+        os.environ["MASTER_ADDR"] = "127.0.0.1"
+        os.environ["MASTER_PORT"] = str(port)
+        torch.cuda.set_device(0)
+        dist.init_process_group("nccl", rank=0, world_size=1)
+        T, H, V = 256, 128, 2500
+        x, W, t = flce_inputs(61, T, H, V)
+        xd, Wd, td = to_dev_bf16(x), to_dev_bf16(W), to_dev(t)
+        mean, rows = lmdist.vocab_parallel_flce(xd, Wd, td, 0, V)
+        ws = lmho.workspace(lmho.flce_workspace_bytes(T, H, V))
+        ref = lmho.flce_fwd_bf16(xd, Wd, td, ws=ws)
+        ok_ce = torch.equal(rows, lmho.row_losses(ws, T)) and torch.equal(mean, ref)
+        xs, Ws, xt, Wt = jsd_inputs(62, T, H, V, sw=0.2)
+        d = [to_dev_bf16(a) for a in (xs, Ws, xt, Wt)]
+        keep = to_dev((np.arange(T) % 5 != 3).astype(np.uint8))
+        loss, jrows = lmdist.vocab_parallel_fljsd(*d, 0.4, 1.5, keep)
+        ws2 = lmho.workspace(lmho.fljsd_workspace_bytes(T, H, V))
+        ref2 = lmho.fljsd_fwd_bf16_ex(*d, 0.4, 1.5, keep, ws=ws2)
+        ok_jsd = torch.equal(jrows, lmho.row_losses(ws2, T)) and torch.equal(loss, ref2)
+        dist.destroy_process_group()
+        q.put((ok_ce, ok_jsd, None))
+    except Exception as e:  # report to the parent
+        q.put((False, False, repr(e)))
+
+
+def test_vocab_parallel_helpers_over_nccl_one_rank(gpu_lib):
+    import socket
+
+    import torch.multiprocessing as mp
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_nccl_one_rank, args=(port, q))
+    p.start()
+    ok_ce, ok_jsd, err = q.get(timeout=300)
+    p.join(timeout=60)
+    assert err is None, err
+    assert ok_ce and ok_jsd
+    assert p.exitcode == 0
