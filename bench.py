@@ -795,7 +795,7 @@ def run_tp_fused(args, rank, world, local_rank):
                       "l2": "inputs larger than L2 (no flush)"},
            "phases_us": {k: round(v * 1e3, 1) for k, v in ph.items()},
            "TFLOP/s": {"flce_pass": round(fl_flops / (ph["flce_pass"] * 1e-3) / 1e12, 1),
-                       "lse_pass": round(js_flops / 2 / (ph["lse_pass"] * 1e-3) / 1e12, 1),
+                       "lse_pass": round(js_flops / (ph["lse_pass"] * 1e-3) / 1e12, 1),
                        "jsd_pass": round(tf, 1)},
            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_sus"],
                         "unit": "TFLOP/s", "frac": round(tf / pk["bf16_sus"], 4), "traffic": None,
