@@ -100,6 +100,10 @@ def _load():
             lib.oracle_lse_merge.restype = None
             lib.oracle_fljsd_terms_shard_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, vp, ci]
             lib.oracle_fljsd_terms_shard_bf16.restype = None
+            lib.oracle_ce_partials_lse.argtypes = [vp, vp, i64, i64, vp]
+            lib.oracle_ce_partials_lse.restype = None
+            lib.oracle_flce_grad_shard_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, vp, dbl, vp, vp]
+            lib.oracle_flce_grad_shard_bf16.restype = None
             lib.oracle_jsd_merge.argtypes = [vp, i64, i64, vp, vp]
             lib.oracle_jsd_merge.restype = dbl
             _lib = lib
@@ -511,3 +515,33 @@ def jsd_merge(terms, keep=None):
     rows = np.empty(T, np.float64)
     m = _load().oracle_jsd_merge(pt, k, T, pk, rows.ctypes.data)
     return m, rows
+
+
+def ce_partials_lse(m, s):
+    """Each row's global log-sum-exp [...] from k shards' CE partials m, s
+    (each [k, ...], shard order)."""
+    m, pm = _c(m, np.float64)
+    s, ps = _c(s, np.float64)
+    assert m.shape == s.shape
+    k = m.shape[0]
+    out = np.empty(m.shape[1:], np.float64)
+    _load().oracle_ce_partials_lse(pm, ps, k, out.size, out.ctypes.data)
+    return out
+
+
+def flce_grad_shard_bf16(x_bits, Wl_bits, target, v0, V, lse, scale=1.0):
+    """Backward of one shard of the vocab-parallel fused linear + CE: with the
+    tokens' global log-sum-exps lse [T], returns float64 (dx_partial [T, H],
+    dWl [Vl, H]) of scale * mean loss (the shards' dx_partial sum to dx)."""
+    x, px = _c(x_bits, np.uint16)
+    Wl, pw = _c(Wl_bits, np.uint16)
+    t, pt = _c(target, np.int64)
+    lse, pl = _c(lse, np.float64)
+    T, H = x.shape
+    Vl = Wl.shape[0]
+    assert Wl.shape[1] == H and t.shape == (T,) and lse.shape == (T,)
+    dx = np.empty((T, H), np.float64)
+    dW = np.empty((Vl, H), np.float64)
+    _load().oracle_flce_grad_shard_bf16(px, pw, pt, T, H, Vl, int(v0), int(V), pl, float(scale), dx.ctypes.data,
+                                        dW.ctypes.data)
+    return dx, dW

@@ -77,6 +77,10 @@
 //     beta P (lp - ln M) + (1 - beta) Q (lq - ln M), lp = zs/tau - lse_0,
 //     lq = zt/tau - lse_1, and the token's JSD is the sum of its shards' sums
 //     in shard order (so the split changes only the order of one sum).
+//   fused CE backward: with each token's global log-sum-exp (from the
+//     gathered partials), the shard's columns of dz = (scale/T)(softmax -
+//     onehot); its share dz Wl of dx (the shares sum to dx) and its rows
+//     dz^T x of dW.
 //
 // Variant (JSD with temperature and a token mask): the logits of both heads
 // are divided by the temperature tau before the softmax; tokens whose keep
@@ -737,6 +741,54 @@ void oracle_fljsd_terms_shard_bf16(const uint16_t* xs, const uint16_t* Wsl, cons
     }
     terms[i] = jsd_row(lp.data(), lq.data(), Vl, beta);
   });
+}
+
+// Each row's global log-sum-exp from k shards' CE partials (each [k][rows],
+// shard-major): M = max_j m_j, lse = M + ln sum_j s_j exp(m_j - M).
+void oracle_ce_partials_lse(const double* m, const double* s, int64_t k, int64_t rows, double* lse) {
+  for (int64_t r = 0; r < rows; ++r) {
+    double M = m[r];
+    for (int64_t j = 1; j < k; ++j)
+      if (m[j * rows + r] > M || std::isnan(m[j * rows + r])) M = m[j * rows + r];
+    double sum = 0.0;
+    for (int64_t j = 0; j < k; ++j) sum += s[j * rows + r] * std::exp(m[j * rows + r] - M);
+    lse[r] = M + std::log(sum);
+  }
+}
+
+// Backward of one shard of the vocab-parallel fused linear + CE (W rows
+// [v0, v0 + Vl) in Wl), gradient of scale * mean loss over the T tokens:
+//   dz_iv = (scale / T) (exp(z_iv - lse_i) - [v0 + v == t_i]) for the shard's
+//   columns v, lse_i the token's global log-sum-exp; a target outside [0, V)
+//   makes the row NaN;
+//   dx_partial = dz Wl [T, H] (the shards' shares sum to dx), dWl = dz^T x [Vl, H].
+void oracle_flce_grad_shard_bf16(const uint16_t* x16, const uint16_t* Wl16, const int64_t* target, int64_t T,
+                                 int64_t H, int64_t Vl, int64_t v0, int64_t V, const double* lse, double scale,
+                                 double* dx, double* dWl) {
+  std::vector<double> x(static_cast<size_t>(T) * H), W(static_cast<size_t>(Vl) * H), dz(static_cast<size_t>(T) * Vl);
+  for (size_t i = 0; i < x.size(); ++i) x[i] = bf16_to_double(x16[i]);
+  for (size_t i = 0; i < W.size(); ++i) W[i] = bf16_to_double(Wl16[i]);
+  const double g = scale / static_cast<double>(T);
+  for (int64_t i = 0; i < T; ++i) {
+    const bool bad = target[i] < 0 || target[i] >= V;
+    for (int64_t v = 0; v < Vl; ++v) {
+      double z = 0.0;
+      for (int64_t k = 0; k < H; ++k) z += x[i * H + k] * W[v * H + k];
+      dz[i * Vl + v] = bad ? kNaN : g * (std::exp(z - lse[i]) - (v0 + v == target[i] ? 1.0 : 0.0));
+    }
+  }
+  for (int64_t i = 0; i < T; ++i)
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t v = 0; v < Vl; ++v) acc += dz[i * Vl + v] * W[v * H + k];
+      dx[i * H + k] = acc;
+    }
+  for (int64_t v = 0; v < Vl; ++v)
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < T; ++i) acc += dz[i * Vl + v] * x[i * H + k];
+      dWl[v * H + k] = acc;
+    }
 }
 
 // The per-token JSD from k shards' term sums [k][T] (summed in shard order; 0

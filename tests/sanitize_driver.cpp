@@ -79,6 +79,10 @@ void oracle_fljsd_terms_shard_bf16(const uint16_t* xs, const uint16_t* Wsl, cons
                                    int64_t T, int64_t H, int64_t Vl, double beta, double tau, const double* lse,
                                    double* terms, int threads);
 double oracle_jsd_merge(const double* terms, int64_t k, int64_t T, const uint8_t* keep, double* rows);
+void oracle_ce_partials_lse(const double* m, const double* s, int64_t k, int64_t rows, double* lse);
+void oracle_flce_grad_shard_bf16(const uint16_t* x16, const uint16_t* Wl16, const int64_t* target, int64_t T,
+                                 int64_t H, int64_t Vl, int64_t v0, int64_t V, const double* lse, double scale,
+                                 double* dx, double* dWl);
 }
 
 namespace {
@@ -165,6 +169,14 @@ void run_shape(int64_t T, int64_t H, int64_t V, int threads) {
     }
     oracle_jsd_merge(terms.data(), k, T, keep.data(), rows.data());
     oracle_jsd_merge(terms.data(), k, T, nullptr, rows.data());
+    // the fused CE's shard backward, from the gathered partials' normalisers
+    std::vector<double> glse(T);
+    oracle_ce_partials_lse(m.data(), sm.data(), k, T, glse.data());
+    for (int64_t j = 0; j < k; ++j) {
+      const int64_t v0 = V * j / k, w1 = V * (j + 1) / k - v0;
+      oracle_flce_grad_shard_bf16(xb.data(), Wb.data() + v0 * H, t.data(), T, H, w1, v0, V, glse.data(), 1.5,
+                                  dx.data(), dW.data());
+    }
   }
   if (T % 2 == 0) {
     const int64_t B = 2, S = T / 2;

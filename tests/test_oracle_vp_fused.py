@@ -163,3 +163,41 @@ def test_jsd_merge_by_hand():
     assert mean == pytest.approx(4.75 / 2, rel=1e-15)
     mean, rows = oracle.jsd_merge(terms, np.zeros(3, np.uint8))
     assert mean == 0.0 and np.all(rows == 0.0)
+
+
+# ---------------------------------------------------------------- fused CE backward of a shard
+def test_partials_lse_is_scipy_logsumexp():
+    T, H, V = 7, 24, 59
+    x, W, t = flce_inputs(41, T, H, V)
+    m, s, _ = flce_partials(x, W, t, splits(V, 3, 8))
+    np.testing.assert_allclose(oracle.ce_partials_lse(m, s), sp.logsumexp(oracle.logits_bf16(x, W), axis=1),
+                               rtol=1e-14)
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_flce_shard_grads_sum_to_unsharded(k):
+    """The shards' dx shares add up to the unsharded dx and their dW rows stack
+    into the unsharded dW (targets on shard edges, scale 1.7)."""
+    T, H, V = 6, 16, 47
+    x, W, t = flce_inputs(43 + k, T, H, V)
+    shards = splits(V, k, 2 + k)
+    edge = [c for v0, w in shards for c in (v0, v0 + w - 1)]
+    t[:min(T, len(edge))] = edge[:T]
+    m, s, _ = flce_partials(x, W, t, shards)
+    lse = oracle.ce_partials_lse(m, s)
+    dx_full, dW_full = oracle.flce_grad_bf16(x, W, t, 1.7)
+    dx_sum = np.zeros_like(dx_full)
+    for v0, w in shards:
+        dx, dW = oracle.flce_grad_shard_bf16(x, np.ascontiguousarray(W[v0:v0 + w]), t, v0, V, lse, 1.7)
+        dx_sum += dx
+        np.testing.assert_allclose(dW, dW_full[v0:v0 + w], rtol=1e-11, atol=1e-15)
+    np.testing.assert_allclose(dx_sum, dx_full, rtol=1e-11, atol=1e-15)
+
+
+def test_flce_shard_grad_bad_target_is_nan_row():
+    T, H, V = 4, 16, 30
+    x, W, t = flce_inputs(47, T, H, V)
+    t[1] = V
+    m, s, _ = flce_partials(x, W, t, [(0, 12), (12, 18)])
+    dx, dW = oracle.flce_grad_shard_bf16(x, np.ascontiguousarray(W[:12]), t, 0, V, oracle.ce_partials_lse(m, s))
+    assert np.all(np.isnan(dx[1])) and np.all(np.isfinite(np.delete(dx, 1, axis=0))) and np.all(np.isnan(dW))
