@@ -364,6 +364,28 @@ int fljsd_fwd_bf16_ex(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt
 int flce_partials_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t* target, int64_t T,
                        int64_t H, int64_t V_local, int64_t vocab_start, float* partials, void* ws,
                        size_t ws_bytes, void* stream);
+
+/* flce_shard_bwd_bf16: the backward of one shard of the vocab-parallel fused
+ * CE, gradients of grad_scale * (mean loss over the T tokens):
+ *   dZ_shard = (grad_scale / T)(softmax(x W^T) - onehot(target)) restricted to
+ *     the shard's columns, the softmax with each token's GLOBAL normaliser,
+ *     taken from the gathered partials of the forward;
+ *   dx_partial [T, H] fp32 = dZ_shard W_local: this rank's share of dx; the
+ *     ranks' shares sum to dx (an all-reduce done by the caller);
+ *   dW_local [V_local, H] fp32 = dZ_shard^T x: this rank's rows of dW.
+ *   partials  [shards][3][T] fp32 device: every shard's flce_partials_bf16
+ *             output in shard order (the forward's all-gather);
+ *   V         the global vocabulary size: a target outside [0, V) makes that
+ *             token's dZ row, and so dx's row and every dW entry, NaN;
+ *   dx_partial, dW_local 16-byte aligned; ws_bytes >=
+ *   flce_bwd_workspace_bytes(T, H, V_local), zeroed before first use.
+ * dZ is rounded to bf16 for the two tensor-core products, as in
+ * flce_fwd_bwd_bf16.  Launches: the normaliser merge, the dZ pass, the two
+ * products (each with a K-slice sum when it splits K). */
+int flce_shard_bwd_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t* target,
+                        const float* partials, int64_t shards, int64_t T, int64_t H, int64_t V_local,
+                        int64_t vocab_start, int64_t V, float grad_scale, float* dx_partial,
+                        float* dW_local, void* ws, size_t ws_bytes, void* stream);
 int fljsd_lse_partials_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_t* xt,
                             const uint16_t* Wt_local, int64_t T, int64_t H, int64_t V_local,
                             float temperature, float* lse_local, void* ws, size_t ws_bytes,
@@ -444,7 +466,8 @@ int lmho_set_raster_group(int group_m);
  * flce_fwd_bf16 2 (tensor-core pass, finaliser), fljsd_fwd_bf16 4
  * (log-sum-exp pass, finaliser, divergence pass, finaliser),
  * flce_partials_bf16, fljsd_lse_partials_bf16 and fljsd_terms_bf16 2 each
- * (tensor-core pass, finaliser), lse_merge_partials 1, jsd_merge_terms 1
+ * (tensor-core pass, finaliser), flce_shard_bwd_bf16 3 (normaliser merge and
+ * dZ pass, dx share, dW rows), lse_merge_partials 1, jsd_merge_terms 1
  * (the merge and its dependent mean together), rows_mean_f32 1.  Calls made by
  * other threads are not affected.  Pass (NULL, 0) to turn it off. */
 void lmho_set_launch_events(void* const* events, int n);

@@ -38,7 +38,7 @@ EXPORTS = (
     "flce_workspace_bytes", "flce_fwd_bf16", "flce_bwd_workspace_bytes", "flce_fwd_bwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "fljsd_bwd_workspace_bytes", "fljsd_fwd_bwd_bf16",
     "flce_cpo_workspace_bytes", "flce_cpo_fwd_bf16", "flce_cpo_bwd_workspace_bytes", "flce_cpo_fwd_bwd_bf16",
-    "flce_partials_bf16", "fljsd_lse_partials_bf16", "lse_merge_partials", "fljsd_terms_bf16", "jsd_merge_terms",
+    "flce_partials_bf16", "flce_shard_bwd_bf16", "fljsd_lse_partials_bf16", "lse_merge_partials", "fljsd_terms_bf16", "jsd_merge_terms",
     "rows_mean_f32",
     "lmho_ws_status", "lmho_probe_read", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
@@ -114,6 +114,8 @@ def load():
         lib.flce_cpo_fwd_bwd_bf16.restype = ci
         lib.flce_partials_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, sz, vp]
         lib.flce_partials_bf16.restype = ci
+        lib.flce_shard_bwd_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp, vp, sz, vp]
+        lib.flce_shard_bwd_bf16.restype = ci
         lib.fljsd_lse_partials_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, sz, vp]
         lib.fljsd_lse_partials_bf16.restype = ci
         lib.lse_merge_partials.argtypes = [vp, i64, i64, vp, vp]
@@ -627,6 +629,38 @@ def flce_partials_bf16(x, W_local, target, vocab_start, partials=None, ws=None, 
         _check(lib.flce_partials_bf16(px, pw, pt, T, H, Vl, int(vocab_start), _dev(partials, "partials", torch.float32, 2),
                                       _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "flce_partials_bf16")
     return partials
+
+
+def flce_shard_bwd_bf16(x, W_local, target, partials, vocab_start, V, grad_scale=1.0, dx=None, dW=None, ws=None,
+                        stream=None):
+    """Backward of one shard of the vocab-parallel fused linear + CE:
+    gradients of grad_scale * mean loss.  partials: fp32 [shards, 3, T], every
+    shard's flce_partials_bf16 output in shard order; V the global vocabulary.
+    Returns (dx_partial fp32 [T, H], this rank's share of dx -- the ranks'
+    shares sum to dx --, dW_local fp32 [V_local, H], this rank's rows of dW)."""
+    lib = load()
+    px = _dev(x, "x", torch.bfloat16, 2)
+    pw = _dev(W_local, "W_local", torch.bfloat16, 2)
+    pt = _dev(target, "target", torch.int64, 1)
+    pp = _dev(partials, "partials", torch.float32, 3)
+    T, H = x.shape
+    Vl = W_local.shape[0]
+    k = partials.shape[0]
+    if W_local.shape[1] != H or target.shape[0] != T or tuple(partials.shape[1:]) != (3, T):
+        raise ValueError("shape mismatch: x [T,H], W_local [V_local,H], target [T], partials [shards,3,T]")
+    if dx is None:
+        dx = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    if dW is None:
+        dW = torch.empty((Vl, H), dtype=torch.float32, device=x.device)
+    if tuple(dx.shape) != (T, H) or tuple(dW.shape) != (Vl, H):
+        raise ValueError("dx must be [T, H] and dW [V_local, H]")
+    if ws is None:
+        ws = workspace(lib.flce_bwd_workspace_bytes(T, H, Vl), x.device)
+    with _on(x, W_local, target, partials, dx, dW, ws):
+        _check(lib.flce_shard_bwd_bf16(px, pw, pt, pp, k, T, H, Vl, int(vocab_start), int(V), float(grad_scale),
+                                       _dev(dx, "dx", torch.float32, 2), _dev(dW, "dW", torch.float32, 2),
+                                       _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "flce_shard_bwd_bf16")
+    return dx, dW
 
 
 def fljsd_lse_partials_bf16(xs, Ws_local, xt, Wt_local, temperature=1.0, out=None, ws=None, stream=None):

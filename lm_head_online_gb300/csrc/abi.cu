@@ -645,6 +645,41 @@ int flce_partials_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t
   return cuda_status(launch_flce_partials(tx, tw, target, vocab_start, g, partials, w, L));
 }
 
+int flce_shard_bwd_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t* target, const float* partials,
+                        int64_t shards, int64_t T, int64_t H, int64_t V_local, int64_t vocab_start, int64_t V,
+                        float grad_scale, float* dx_partial, float* dW_local, void* ws, size_t ws_bytes,
+                        void* stream) {
+  if (!x || !W_local || !target || !partials || !dx_partial || !dW_local || !ws) return LMHO_ERR_INVALID_ARG;
+  if (int c = check_fused_common(T, H, V_local)) return c;
+  if (shards <= 0 || shards > (int64_t(1) << 20) || V > (int64_t(1) << 31) || vocab_start < 0 || V < V_local ||
+      vocab_start > V - V_local)
+    return LMHO_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_scale)) return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_local) || !aligned16(dx_partial) || !aligned16(dW_local))
+    return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < flce_bwd_ws_bytes(T, H, V_local) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const Range in[4] = {rng(x, 2 * static_cast<size_t>(T) * H), rng(W_local, 2 * static_cast<size_t>(V_local) * H),
+                       rng(target, 8 * static_cast<size_t>(T)),
+                       rng(partials, 12 * static_cast<size_t>(T) * static_cast<size_t>(shards))};
+  const Range out[3] = {rng(dx_partial, 4 * static_cast<size_t>(T) * H),
+                        rng(dW_local, 4 * static_cast<size_t>(V_local) * H), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 4, out, 3)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  const FusedWs w = flce_ws_carve(ws, ws_bytes, T, V_local);
+  const FlceBwdWs bw = flce_bwd_ws_carve(ws, T, H, V_local);
+  FlceBwdMaps m;
+  if (tmap_bf16(&m.x, x, T, H, kBM) || tmap_bf16(&m.w, W_local, V_local, H, kBoxBFwd) ||
+      tmap_bf16_ld(&m.dz, bw.dz, T, V_local, bw.ld_dz, kBM) || tmap_bf16_mn(&m.w_mn, W_local, V_local, H, H, kBoxBGrad) ||
+      tmap_bf16_mn(&m.dz_mn, bw.dz, T, V_local, bw.ld_dz, kBM) || tmap_bf16_mn(&m.x_mn, x, T, H, H, kBoxBGrad))
+    return LMHO_ERR_CUDA;
+  const FusedGeometry g = geometry(T, H, V_local, kBN_CE);
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_flce_shard_bwd(m, target, partials, shards, vocab_start, V, g, grad_scale, dx_partial,
+                                           dW_local, w, bw, L));
+}
+
 namespace {
 // Arguments shared by the two shard passes of the vocab-parallel fused JSD.
 int check_jsd_shard(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt, const uint16_t* Wt, int64_t T,

@@ -142,7 +142,8 @@ struct Params {
   int32_t num_m, num_n, group_m, k_blocks;
   int64_t units;
   const int64_t* target;  // CE
-  int64_t v0;             // CE: first global vocab column of W (a vocabulary shard; 0 = the whole vocabulary)
+  int64_t v0;             // CE, DZ: first global vocab column of W (a vocabulary shard; 0 = the whole vocabulary)
+  int64_t v_total;        // DZ: global vocabulary size, targets outside [0, v_total) give NaN rows (0 = V)
   float* part0;
   float* part1;
   float* part2;
@@ -663,13 +664,15 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
           if (MODE == kModeDZ) {
             float v[32];
             tmem_ld32_sync(tbase + cc * 32, v);
-            const bool bad = tgt < 0 || tgt >= p.V;
+            // a vocabulary shard: the target is global, its column here is tgt - v0
+            const bool bad = tgt < 0 || tgt >= (p.v_total ? p.v_total : p.V);
+            const int64_t tl = bad ? -1 : tgt - p.v0;
             const float g = gdz, nl = -ls * kLog2e;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int64_t col = col0 + j;
               float d = col < p.V ? g * ex2_approx(fmaf(v[j], kLog2e, nl)) : 0.f;
-              if (col == tgt) d -= g;
+              if (col == tl) d -= g;
               v[j] = bad ? __int_as_float(0x7FC00000) : d;
             }
             // Each lane's 64-byte dZ row segment (32 bf16; ld_dz is a multiple of the
@@ -1321,6 +1324,38 @@ cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const int64_t* target, con
       cudaSuccess)
     return e;
   launch_mark(4, L.stream);
+  return cudaSuccess;
+}
+
+cudaError_t launch_flce_shard_bwd(const FlceBwdMaps& m, const int64_t* target, const float* partials,
+                                  int64_t shards, int64_t v0, int64_t v_total, const FusedGeometry& g,
+                                  float grad_scale, float* dx, float* dW, const FusedWs& ws, const FlceBwdWs& bw,
+                                  const FusedLaunch& L) {
+  cudaError_t e;
+  launch_mark(0, L.stream);
+  // each token's global log-sum-exp from every shard's partials
+  if ((e = launch_partials_lse(partials, shards, g.T, bw.lse, L.num_sms, L.stream)) != cudaSuccess) return e;
+  // recompute the shard's logit tiles, write its dZ columns
+  Params q = base_params<kModeDZ>(g, L, ws.ctrl);
+  q.units = static_cast<int64_t>(q.num_m) * q.num_n;
+  q.target = target;
+  q.v0 = v0;
+  q.v_total = v_total;
+  q.lse = bw.lse;
+  q.gscale = grad_scale / static_cast<float>(g.T);
+  q.dz = bw.dz;
+  q.ld_dz = bw.ld_dz;
+  if ((e = launch_gemm<kModeDZ>(m.x, m.w, m.x, m.w, q, L)) != cudaSuccess) return e;
+  launch_mark(1, L.stream);
+  // this shard's share of dx [T, H] = dZ_shard W_local, and its rows of dW = dZ_shard^T x
+  if ((e = launch_store_gemm<kModeStore>(m.dz, m.w_mn, g.T, g.H, g.V, dx, bw.split, g.group_store, ws.ctrl, L)) !=
+      cudaSuccess)
+    return e;
+  launch_mark(2, L.stream);
+  if ((e = launch_store_gemm<kModeStoreT>(m.dz_mn, m.x_mn, g.V, g.H, g.T, dW, bw.split, g.group_store, ws.ctrl, L)) !=
+      cudaSuccess)
+    return e;
+  launch_mark(3, L.stream);
   return cudaSuccess;
 }
 

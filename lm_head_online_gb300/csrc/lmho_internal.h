@@ -189,6 +189,9 @@ cudaError_t launch_lse_merge(const float* parts, int64_t shards, int64_t T, floa
 cudaError_t launch_jsd_merge(const float* terms, int64_t shards, int64_t T, const uint8_t* keep, float* rows,
                              float* loss, int num_sms, cudaStream_t st);
 cudaError_t launch_rows_mean(const float* rows, int64_t n, const uint8_t* keep, float* mean, cudaStream_t st);
+// Each token's global log-sum-exp [T] from gathered CE partials [k][3][T].
+cudaError_t launch_partials_lse(const float* partials, int64_t shards, int64_t T, float* lse, int num_sms,
+                                cudaStream_t st);
 
 // Records the caller's measurement event `i` on `st` if the hook is set
 // (lmho_set_launch_events); no-op otherwise.
@@ -224,6 +227,15 @@ struct FlceBwdMaps {
 };
 size_t flce_bwd_ws_bytes(int64_t T, int64_t H, int64_t V);
 FlceBwdWs flce_bwd_ws_carve(void* ws, int64_t T, int64_t H, int64_t V);
+// Fused linear + CE backward of one vocabulary shard (W = the global rows
+// [v0, v0 + g.V)): each token's global log-sum-exp from the gathered CE
+// partials [shards][3][T] (into bw.lse), the shard's dZ columns (targets global; v_total = the global vocabulary
+// size), this shard's share of dx (the ranks' shares sum to dx) and its own
+// rows of dW.
+cudaError_t launch_flce_shard_bwd(const FlceBwdMaps& m, const int64_t* target, const float* partials,
+                                  int64_t shards, int64_t v0, int64_t v_total, const FusedGeometry& g,
+                                  float grad_scale, float* dx, float* dW, const FusedWs& ws, const FlceBwdWs& bw,
+                                  const FusedLaunch& L);
 // CPO on the fused linear + CE: pairs of sequences (chosen b, rejected b + B/2)
 // of S tokens.  Workspace pieces beyond the fused CE's.
 struct CpoArgs {

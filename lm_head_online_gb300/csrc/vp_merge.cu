@@ -11,10 +11,12 @@
 //     shards' sums of its JSD terms (compensated fp32); tokens whose keep
 //     flag is 0 get 0; then the batchmean over the kept tokens;
 //   * row mean: fixed-order compensated fp32 mean of per-token values (over
-//     the kept ones when a mask is given), bitwise reproducible.
+//     the kept ones when a mask is given), bitwise reproducible;
+//   * the global log-sum-exp of each token from gathered cross-entropy
+//     partials, for the backward of the vocab-parallel fused CE.
 // The cross-entropy's shard merge is ce_merge_rows (ce_rows.cu).
 //
-// All three are tiny next to the passes that produce their inputs: they read
+// All of them are tiny next to the passes that produce their inputs: they read
 // 8 k or 4 k bytes per token for k shards.
 #include <cmath>
 #include <cstdint>
@@ -67,6 +69,22 @@ __global__ void __launch_bounds__(256) rows_mean_kernel(const float* __restrict_
   mean_sum(rows, T, mean, keep);
 }
 
+// lse [T] from gathered cross-entropy partials [k][3][T] (m, s, z per shard):
+// the (m, s) merged in shard order exactly as ce_merge_rows merges them, then
+// m + ln s -- each token's global log-sum-exp, for the sharded backward.
+__global__ void __launch_bounds__(256) partials_lse_rows(const float* __restrict__ part, int64_t shards, int64_t T,
+                                                          float* __restrict__ lse) {
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < T;
+       r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    MS tot = ms_empty();
+    for (int64_t j = 0; j < shards; ++j) {
+      const float* p = part + 3 * j * T;
+      tot = ms_merge(tot, MS{__ldg(p + r), __ldg(p + T + r)});
+    }
+    lse[r] = tot.m + logf(tot.s);
+  }
+}
+
 unsigned grid_for(int64_t n, int num_sms) {
   int64_t blocks = (n + 255) / 256;
   if (blocks > 8 * static_cast<int64_t>(num_sms)) blocks = 8 * static_cast<int64_t>(num_sms);
@@ -102,6 +120,12 @@ cudaError_t launch_jsd_merge(const float* terms, int64_t shards, int64_t T, cons
       e != cudaSuccess)
     return e;
   launch_mark(1, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_partials_lse(const float* partials, int64_t shards, int64_t T, float* lse, int num_sms,
+                                cudaStream_t st) {
+  partials_lse_rows<<<grid_for(T, num_sms), 256, 0, st>>>(partials, shards, T, lse);
   return cudaGetLastError();
 }
 

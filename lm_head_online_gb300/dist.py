@@ -109,6 +109,27 @@ def vocab_parallel_flce(x, W_local, target, vocab_start: int, V: int, group=None
     return rows_mean(rows), rows
 
 
+def vocab_parallel_flce_fwd_bwd(x, W_local, target, vocab_start: int, V: int, grad_scale=1.0, group=None,
+                                ws=None):
+    """vocab_parallel_flce and the gradients of grad_scale * mean loss: returns
+    (mean loss [1], per-token losses [T], dx [T, H] fp32 -- the ranks' shares
+    summed by one all-reduce, the same on every rank --, dW_local [V_local, H]
+    fp32, this rank's rows of dW).  The backward reuses the forward's gathered
+    partials for the global normalisers: no further exchange before dx."""
+    from lm_head_online_gb300 import (ce_merge_partials, flce_bwd_workspace_bytes, flce_partials_bf16,
+                                      flce_shard_bwd_bf16, rows_mean, workspace)
+
+    T, H = x.shape
+    if ws is None:
+        ws = workspace(flce_bwd_workspace_bytes(T, H, W_local.shape[0]), x.device)
+    part = flce_partials_bf16(x, W_local, target, vocab_start, ws=ws)     # [3, T]
+    allp = gather_partials(part, group)                                    # [world, 3, T]
+    rows = ce_merge_partials(allp.view(allp.shape[0], 3, T, 1), target.view(T, 1), V).view(T)
+    dx, dW = flce_shard_bwd_bf16(x, W_local, target, allp, vocab_start, V, grad_scale, ws=ws)
+    dist.all_reduce(dx, op=dist.ReduceOp.SUM, group=group)
+    return rows_mean(rows), rows, dx, dW
+
+
 def vocab_parallel_fljsd(xs, Ws_local, xt, Wt_local, beta=0.5, temperature=1.0, keep=None, group=None, ws=None):
     """Fused linear + generalized JSD with both heads' rows sharded over the
     ranks of `group` (Ws_local, Wt_local: this rank's rows [V_local, H] of the

@@ -2,6 +2,7 @@
 symbol include/lmho.h declares, and rejects bad arguments before touching a
 device."""
 import ctypes
+import math
 import os
 import re
 
@@ -215,6 +216,21 @@ def test_vocab_parallel_fused_argument_checks(lib):
     assert lib.flce_partials_bf16(A, B + 2, C, 4, 16, 10, 0, D, E, ws, None) == 1        # W_local unaligned
     assert lib.flce_partials_bf16(A, B, C, 4, 16, 10, 0, D, E, 256, None) == 3           # short workspace
     assert lib.flce_partials_bf16(A, B, C, 4, 16, 10, 0, C + 16, E, ws, None) == 2       # partials over target
+    # flce_shard_bwd_bf16(x, W_local, target, partials, shards, T, H, V_local, vocab_start, V, grad_scale,
+    #                     dx_partial, dW_local, ws, ws_bytes, stream)
+    g = f(1.0)
+    assert lib.flce_shard_bwd_bf16(A, B, C, None, 2, 4, 16, 10, 0, 20, g, D, D + 4096, E, ws, None) == 1
+    assert lib.flce_shard_bwd_bf16(A, B, C, 0x60000000, 0, 4, 16, 10, 0, 20, g, D, D + 4096, E, ws, None) == 1
+    assert lib.flce_shard_bwd_bf16(A, B, C, 0x60000000, 2, 4, 16, 10, 15, 20, g, D, D + 4096, E, ws,
+                                   None) == 1                                  # shard past the vocabulary
+    assert lib.flce_shard_bwd_bf16(A, B, C, 0x60000000, 2, 4, 16, 10, 0, 20, f(math.inf), D, D + 4096, E, ws,
+                                   None) == 1                                  # non-finite scale
+    assert lib.flce_shard_bwd_bf16(A, B, C, 0x60000000, 2, 4, 16, 10, 0, 20, g, D + 4, D + 4096, E, ws,
+                                   None) == 1                                  # dx not 16-byte aligned
+    assert lib.flce_shard_bwd_bf16(A, B, C, 0x60000000, 2, 4, 16, 10, 0, 20, g, D, D + 4096, E, 256,
+                                   None) == 3                                  # short workspace
+    assert lib.flce_shard_bwd_bf16(A, B, C, 0x60000000, 2, 4, 16, 10, 0, 20, g, 0x60000010, D + 4096, E, ws,
+                                   None) == 2                                  # dx over the partials
     # fljsd_lse_partials_bf16(xs, Ws, xt, Wt, T, H, V_local, temperature, lse_local, ws, ws_bytes, stream)
     assert lib.fljsd_lse_partials_bf16(A, B, C, D, 4, 16, 10, f(1.0), None, E, ws, None) == 1
     assert lib.fljsd_lse_partials_bf16(A, B, C, D, 4, 16, 10, f(0.0), E + (1 << 31), E, ws, None) == 1

@@ -252,9 +252,18 @@ def test_vocab_parallel_fused_guards(gpu_lib, T, H, V):
     gpu_lib.ce_merge_partials(parts.view(k, 3, T, 1), t.view(T, 1), V, loss=ce_rows)
     mean = g.view(4, torch.float32, (1,))
     gpu_lib.rows_mean(ce_rows.view(T), out=mean)
+    grads = []
+    for v0, w in shards:
+        dx = g.view(4 * T * H, torch.float32, (T, H))
+        dW = g.view(4 * w * H, torch.float32, (w, H))
+        ws = g.ws(gpu_lib.flce_bwd_workspace_bytes(T, H, w))
+        gpu_lib.flce_shard_bwd_bf16(x, W[v0:v0 + w], t, parts, v0, V, 1.5, dx=dx, dW=dW, ws=ws)
+        g.check()
+        assert gpu_lib.ws_status(ws) == 0
+        grads += [dx, dW]
     g.check()
     assert not bool(torch.isnan(parts).any()), "a partial was never written"   # -inf is a valid target logit
-    written(lparts, lse, terms, rows, loss, ce_rows, mean)
+    written(lparts, lse, terms, rows, loss, ce_rows, mean, *grads)
     unchanged(before, [x, xt, W, Wt, t, keep])
 
 

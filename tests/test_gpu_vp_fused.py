@@ -23,7 +23,7 @@ import torch
 
 import gen
 import oracle
-from tests.helpers import to_dev, to_dev_bf16
+from tests.helpers import assert_within_bounds, ce_error_scale, grad_bounds, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -168,6 +168,95 @@ def test_flce_vp_full_size_sampled(gpu_lib):
     np.testing.assert_allclose(np64(rows)[idx], want, rtol=RTOL_CE_TOKEN, atol=1e-5)
 
 
+# ---------------------------------------------------------------- fused linear + CE backward of a shard
+def run_flce_vp_bwd(lmho, xd, Wd, td, shards, V, scale):
+    """Forward partials of every shard, then each shard's backward with the
+    gathered partials: returns (partials [k, 3, T], [(dx share, dW rows)])."""
+    parts, _, _ = run_flce_vp(lmho, xd, Wd, td, shards, V)
+    outs = [lmho.flce_shard_bwd_bf16(xd, Wd[v0:v0 + w].clone(), td, parts, v0, V, scale) for v0, w in shards]
+    torch.cuda.synchronize()
+    return parts, outs
+
+
+@pytest.mark.parametrize("T,H,V,k", [(130, 128, 1000, 3), (257, 200, 4097, 2), (64, 256, 513, 4),
+                                     (96, 1024, 2000, 3)])
+def test_flce_vp_backward_matches_oracle(gpu_lib, T, H, V, k):
+    """Each shard's dx share and dW rows against the oracle's shard gradient,
+    every element within its own bound (bf16 dZ, fp32 accumulation over the
+    shard's K); the shares' sum against the unsharded oracle dx within the
+    sum of the shares' bounds."""
+    x, W, t = flce_inputs(70 + k, T, H, V)
+    shards = uneven_shards(V, k, 12 + k)
+    edge = [c for v0, w in shards for c in (v0, v0 + w - 1)]
+    t[:min(T, len(edge))] = edge[:T]
+    scale = 1.3
+    _, outs = run_flce_vp_bwd(gpu_lib, to_dev_bf16(x), to_dev_bf16(W), to_dev(t), shards, V, scale)
+    dz = oracle.ce_grad_f64(oracle.logits_bf16(x, W), t, None, scale / T)
+    S = ce_error_scale(dz, t, scale / T)
+    xd = gen.bf16_bits_to_f32(x).astype(np.float64)
+    Wd = gen.bf16_bits_to_f32(W).astype(np.float64)
+    om = [oracle.flce_partials_bf16(x, np.ascontiguousarray(W[v0:v0 + w]), t, v0) for v0, w in shards]
+    lse = oracle.ce_partials_lse(np.stack([p[0] for p in om]), np.stack([p[1] for p in om]))
+    dx_sum, b_sum = np.zeros((T, H)), np.zeros((T, H))
+    for j, (v0, w) in enumerate(shards):
+        bdx, bdW = grad_bounds(dz[:, v0:v0 + w], S[:, v0:v0 + w], xd, Wd[v0:v0 + w])
+        dx_ref, dW_ref = oracle.flce_grad_shard_bf16(x, np.ascontiguousarray(W[v0:v0 + w]), t, v0, V, lse, scale)
+        got_dx, got_dW = np64(outs[j][0]), np64(outs[j][1])
+        assert_within_bounds(got_dx, dx_ref, bdx, f"dx share of shard {j}")
+        assert_within_bounds(got_dW, dW_ref, bdW, f"dW rows of shard {j}")
+        dx_sum += got_dx
+        b_sum += bdx
+    dx_full, _ = oracle.flce_grad_bf16(x, W, t, scale)
+    assert_within_bounds(dx_sum, dx_full, b_sum, "sum of the dx shares")
+
+
+def test_flce_vp_backward_single_shard_bitwise_and_bad_target(gpu_lib):
+    """One shard holding all of W gives flce_fwd_bwd_bf16's dx and dW bit for
+    bit; a target outside [0, V) gives a NaN dx row and NaN dW, as unsharded."""
+    T, H, V = 200, 256, 3000
+    x, W, t = flce_inputs(75, T, H, V)
+    xd, Wd, td = to_dev_bf16(x), to_dev_bf16(W), to_dev(t)
+    ws = gpu_lib.workspace(gpu_lib.flce_bwd_workspace_bytes(T, H, V))
+    _, dx_ref, dW_ref = gpu_lib.flce_fwd_bwd_bf16(xd, Wd, td, 0.7, ws=ws)
+    _, outs = run_flce_vp_bwd(gpu_lib, xd, Wd, td, [(0, V)], V, 0.7)
+    assert torch.equal(outs[0][0], dx_ref) and torch.equal(outs[0][1], dW_ref)
+    t[5] = V
+    _, outs = run_flce_vp_bwd(gpu_lib, xd, Wd, to_dev(t), uneven_shards(V, 2, 3), V, 0.7)
+    for dx, dW in outs:
+        assert bool(torch.isnan(dx[5]).all()) and bool(torch.isfinite(torch.cat([dx[:5], dx[6:]])).all())
+        assert bool(torch.isnan(dW).all())
+
+
+def test_flce_vp_backward_full_size(gpu_lib):
+    """x [2048, 4096], W [128256, 4096] ~ N(0, 0.02^2) over 8 shards: the dx
+    shares' sum and the stacked dW rows against the unsharded backward
+    (normwise 1e-3: both round dZ to bf16 from normalisers merged in different
+    orders), and sampled dx rows against the oracle within their bounds."""
+    T, H, V, k = 2048, 4096, 128256, 8
+    x = gen.normal_bf16_bits(0, gen.STREAM_X, (T, H))
+    W = gen.normal_bf16_bits(0, gen.STREAM_W, (V, H), sigma=0.02)
+    t = gen.targets(0, gen.STREAM_TARGET, (T,), V)
+    xd, Wd, td = to_dev_bf16(x), to_dev_bf16(W), to_dev(t)
+    shards = [(j * V // k, (j + 1) * V // k - j * V // k) for j in range(k)]
+    _, outs = run_flce_vp_bwd(gpu_lib, xd, Wd, td, shards, V, 1.0)
+    dx = outs[0][0].clone()
+    for j in range(1, k):
+        dx += outs[j][0]
+    dW = torch.cat([o[1] for o in outs])
+    del outs
+    ws = gpu_lib.workspace(gpu_lib.flce_bwd_workspace_bytes(T, H, V))
+    _, dx_ref, dW_ref = gpu_lib.flce_fwd_bwd_bf16(xd, Wd, td, 1.0, ws=ws)
+    assert float(torch.linalg.norm(dx - dx_ref)) <= 1e-3 * float(torch.linalg.norm(dx_ref))
+    assert float(torch.linalg.norm(dW - dW_ref)) <= 1e-3 * float(torch.linalg.norm(dW_ref))
+    del dW, dW_ref, ws
+    idx = np.array([0, 777, 2047])
+    dz = oracle.ce_grad_f64(oracle.logits_bf16(x[idx], W), t[idx], None, 1.0 / T)
+    S = ce_error_scale(dz, t[idx], 1.0 / T)
+    Wd64 = gen.bf16_bits_to_f32(W).astype(np.float64)
+    bdx, _ = grad_bounds(dz, S, gen.bf16_bits_to_f32(x[idx]).astype(np.float64), Wd64)
+    assert_within_bounds(np64(dx)[idx], dz @ Wd64, bdx, "dx rows (sum of 8 shares)")
+
+
 # ---------------------------------------------------------------- fused linear + JSD
 FLJSD_VP_CASES = [(64, 64, 300, 2, 0.5, 1.0, False), (200, 128, 1500, 3, 0.3, 2.0, True),
                   (129, 256, 777, 4, 0.5, 0.7, False), (5, 64, 37, 5, 0.8, 1.0, True),
@@ -278,6 +367,10 @@ def _nccl_one_rank(port, q):
         ws = lmho.workspace(lmho.flce_workspace_bytes(T, H, V))
         ref = lmho.flce_fwd_bf16(xd, Wd, td, ws=ws)
         ok_ce = torch.equal(rows, lmho.row_losses(ws, T)) and torch.equal(mean, ref)
+        m2, rows2, dx, dW = lmdist.vocab_parallel_flce_fwd_bwd(xd, Wd, td, 0, V, 0.9)
+        wsb = lmho.workspace(lmho.flce_bwd_workspace_bytes(T, H, V))
+        ref_l, ref_dx, ref_dW = lmho.flce_fwd_bwd_bf16(xd, Wd, td, 0.9, ws=wsb)
+        ok_ce = ok_ce and torch.equal(m2, ref_l) and torch.equal(dx, ref_dx) and torch.equal(dW, ref_dW)
         xs, Ws, xt, Wt = jsd_inputs(62, T, H, V, sw=0.2)
         d = [to_dev_bf16(a) for a in (xs, Ws, xt, Wt)]
         keep = to_dev((np.arange(T) % 5 != 3).astype(np.uint8))
