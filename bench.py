@@ -687,7 +687,8 @@ def run_tp_fused(args, rank, world, local_rank):
     holds the rows shard_vocab(V, r, world) of W (of both heads for the JSD);
     the inputs x / xs, xt and the targets are on every rank.  One step:
       flce:  flce_partials_bf16, one NCCL all-gather of [3, T], ce_merge_partials,
-             rows_mean;
+             rows_mean; its backward flce_shard_bwd_bf16 (the rank's dx share and
+             dW rows) and one all-reduce of dx;
       fljsd: fljsd_lse_partials_bf16, all-gather of [2, T], lse_merge_partials,
              fljsd_terms_bf16, all-gather of [1, T], jsd_merge_terms.
     Total work is fixed as N grows ("strong").  A one-rank NCCL group is used at
@@ -725,7 +726,9 @@ def run_tp_fused(args, rank, world, local_rank):
     tgt = torch.from_numpy(gen.targets(args.seed, gen.STREAM_TARGET, (Tc,), V, threads=thr)).to(dev)
     xs, xt = host_bf16(gen.STREAM_X, Tj), host_bf16(gen.STREAM_XT, Tj)
     Ws, Wt = rows_of(gen.STREAM_W, 0.02), rows_of(gen.STREAM_WT, 0.02)
-    ws_c = lmho.workspace(lmho.flce_workspace_bytes(Tc, H, w), dev)
+    ws_c = lmho.workspace(lmho.flce_bwd_workspace_bytes(Tc, H, w), dev)
+    dx = torch.empty((Tc, H), device=dev)
+    dW = torch.empty((w, H), device=dev)
     ws_j = lmho.workspace(lmho.fljsd_workspace_bytes(Tj, H, w), dev)
     part = torch.empty((3, Tc), device=dev)
     g_part = torch.empty((world, 3, Tc), device=dev)
@@ -734,8 +737,8 @@ def run_tp_fused(args, rank, world, local_rank):
     terms = torch.empty((Tj,), device=dev)
     g_terms = torch.empty((world, Tj), device=dev)
     stream = torch.cuda.current_stream()
-    names = ("flce_pass", "flce_gather", "flce_merge", "lse_pass", "lse_gather", "lse_merge", "jsd_pass",
-             "jsd_gather", "jsd_merge")
+    names = ("flce_pass", "flce_gather", "flce_merge", "flce_bwd", "dx_allreduce", "lse_pass", "lse_gather",
+             "lse_merge", "jsd_pass", "jsd_gather", "jsd_merge")
 
     def step(ev=None):
         def mark(i):
@@ -749,25 +752,29 @@ def run_tp_fused(args, rank, world, local_rank):
         rows = lmho.ce_merge_partials(g_part.view(world, 3, Tc, 1), tgt.view(Tc, 1), V).view(Tc)
         ce_mean = lmho.rows_mean(rows)
         mark(3)
-        lmho.fljsd_lse_partials_bf16(xs, Ws, xt, Wt, 1.0, out=lse_l, ws=ws_j)
+        lmho.flce_shard_bwd_bf16(x, W, tgt, g_part, v0, V, 1.0, dx=dx, dW=dW, ws=ws_c)
         mark(4)
-        tdist.all_gather_into_tensor(g_lse.view(world * 2, Tj), lse_l)
+        tdist.all_reduce(dx, op=tdist.ReduceOp.SUM)
         mark(5)
-        lse = lmho.lse_merge_partials(g_lse)
+        lmho.fljsd_lse_partials_bf16(xs, Ws, xt, Wt, 1.0, out=lse_l, ws=ws_j)
         mark(6)
-        lmho.fljsd_terms_bf16(xs, Ws, xt, Wt, lse, 0.5, 1.0, out=terms, ws=ws_j)
+        tdist.all_gather_into_tensor(g_lse.view(world * 2, Tj), lse_l)
         mark(7)
-        tdist.all_gather_into_tensor(g_terms, terms)
+        lse = lmho.lse_merge_partials(g_lse)
         mark(8)
-        jsd, _ = lmho.jsd_merge_terms(g_terms)
+        lmho.fljsd_terms_bf16(xs, Ws, xt, Wt, lse, 0.5, 1.0, out=terms, ws=ws_j)
         mark(9)
+        tdist.all_gather_into_tensor(g_terms, terms)
+        mark(10)
+        jsd, _ = lmho.jsd_merge_terms(g_terms)
+        mark(11)
         return ce_mean, jsd
 
     for _ in range(max(1, args.warmup)):
         ce_mean, jsd = step()
     torch.cuda.synchronize()
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks:
         tdist.barrier()
@@ -785,7 +792,8 @@ def run_tp_fused(args, rank, world, local_rank):
     fl_flops = 2 * Tc * H * w
     js_flops = 4 * Tj * H * w
     tf = js_flops / (ph["jsd_pass"] * 1e-3) / 1e12
-    res = {"metric": "vocab-parallel fused linear + CE and + JSD, us/step", "impl": "ours",
+    bwd_flops = 2 * fl_flops + fl_flops   # dZ recompute pass, dx and dW products
+    res = {"metric": "vocab-parallel fused linear + CE (forward and backward) and + JSD, us/step", "impl": "ours",
            "mode": "vocab-parallel fused", "value": round(ms * 1e3, 1), "unit": "us/step", "n_gpus": world,
            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False,
            "scaling": "strong", "vs_baseline": None, "dtype": "bf16 in, f32 accumulate",
@@ -795,30 +803,34 @@ def run_tp_fused(args, rank, world, local_rank):
                       "l2": "inputs larger than L2 (no flush)"},
            "phases_us": {k: round(v * 1e3, 1) for k, v in ph.items()},
            "TFLOP/s": {"flce_pass": round(fl_flops / (ph["flce_pass"] * 1e-3) / 1e12, 1),
+                       "flce_bwd": round(bwd_flops / (ph["flce_bwd"] * 1e-3) / 1e12, 1),
                        "lse_pass": round(js_flops / (ph["lse_pass"] * 1e-3) / 1e12, 1),
                        "jsd_pass": round(tf, 1)},
            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_sus"],
                         "unit": "TFLOP/s", "frac": round(tf / pk["bf16_sus"], 4), "traffic": None,
                         "kernel": "fljsd_terms_bf16 tensor-core pass"},
-           "gpu_launches": 11 * K, "clocks": clocks.summary(),
+           "gpu_launches": 15 * K, "clocks": clocks.summary(),
            "flce_loss": float(ce_mean.item()), "fljsd_loss": float(jsd.item())}
     if world == 1:
         # the unsharded calls on the same inputs, timed the same way
-        ws1 = lmho.workspace(lmho.flce_workspace_bytes(Tc, H, V), dev)
+        ws1 = lmho.workspace(lmho.flce_bwd_workspace_bytes(Tc, H, V), dev)
         ws2 = lmho.workspace(lmho.fljsd_workspace_bytes(Tj, H, V), dev)
+        dx1 = torch.empty_like(dx)
+        dW1 = torch.empty_like(dW)
         for _ in range(2):
-            a = lmho.flce_fwd_bf16(x, W, tgt, ws=ws1)
+            a = lmho.flce_fwd_bwd_bf16(x, W, tgt, 1.0, dx=dx1, dW=dW1, ws=ws1)[0]
             b = lmho.fljsd_fwd_bf16(xs, Ws, xt, Wt, 0.5, ws=ws2)
         torch.cuda.synchronize()
         u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         u0.record(stream)
         for _ in range(K):
-            a = lmho.flce_fwd_bf16(x, W, tgt, ws=ws1)
+            a = lmho.flce_fwd_bwd_bf16(x, W, tgt, 1.0, dx=dx1, dW=dW1, ws=ws1)[0]
             b = lmho.fljsd_fwd_bf16(xs, Ws, xt, Wt, 0.5, ws=ws2)
         u1.record(stream)
         torch.cuda.synchronize()
         res["unsharded_us_per_step"] = round(u0.elapsed_time(u1) / K * 1e3, 1)
-        res["bitwise_equal_to_unsharded"] = bool(torch.equal(a, ce_mean) and torch.equal(b, jsd))
+        res["bitwise_equal_to_unsharded"] = bool(torch.equal(a, ce_mean) and torch.equal(b, jsd) and
+                                                 torch.equal(dx1, dx) and torch.equal(dW1, dW))
     tdist.destroy_process_group()
     return res
 

@@ -180,3 +180,35 @@ def test_vocab_parallel_fused_exchanges_over_gloo_ranks(world):
     for mean, rows in out.values():
         np.testing.assert_allclose(rows, want_rows, rtol=1e-11, atol=1e-15)
         assert mean == pytest.approx(want_mean, rel=1e-11)
+
+
+def _vp_flce_bwd(rank, world):
+    """Each rank: its shard's forward partials, their all-gather, the oracle's
+    shard gradient with the global normalisers from the gathered partials,
+    and the all-reduce of the dx shares that dist.vocab_parallel_flce_fwd_bwd
+    makes; returns (dx, this rank's dW rows, its vocab range)."""
+    T, H, V = 5, 16, 71
+    x = gen.normal_bf16_bits(8, 0, (T, H), sigma=1.0)
+    W = gen.normal_bf16_bits(8, 1, (V, H), sigma=0.3)
+    t = gen.targets(8, 2, (T,), V)
+    v0, w = lmdist.shard_vocab(V, rank, world)
+    Wl = np.ascontiguousarray(W[v0:v0 + w])
+    m, s, zt = oracle.flce_partials_bf16(x, Wl, t, v0)
+    g = lmdist.gather_partials(torch.from_numpy(np.stack([m, s, zt]))).numpy()
+    lse = oracle.ce_partials_lse(g[:, 0], g[:, 1])
+    dx, dW = oracle.flce_grad_shard_bf16(x, Wl, t, v0, V, lse, 0.8)
+    dxt = torch.from_numpy(dx)
+    dist.all_reduce(dxt, op=dist.ReduceOp.SUM)
+    return dxt.numpy(), dW, (v0, w)
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_vocab_parallel_flce_backward_exchange_over_gloo_ranks(world):
+    out = spawn(_vp_flce_bwd, world=world)
+    T, H, V = 5, 16, 71
+    dx_want, dW_want = oracle.flce_grad_bf16(gen.normal_bf16_bits(8, 0, (T, H), sigma=1.0),
+                                             gen.normal_bf16_bits(8, 1, (V, H), sigma=0.3),
+                                             gen.targets(8, 2, (T,), V), 0.8)
+    for dx, dW, (v0, w) in out.values():
+        np.testing.assert_allclose(dx, dx_want, rtol=1e-11, atol=1e-15)
+        np.testing.assert_allclose(dW, dW_want[v0:v0 + w], rtol=1e-11, atol=1e-15)
