@@ -104,6 +104,11 @@ def _load():
             lib.oracle_ce_partials_lse.restype = None
             lib.oracle_flce_grad_shard_bf16.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, vp, dbl, vp, vp]
             lib.oracle_flce_grad_shard_bf16.restype = None
+            lib.oracle_fljsd_kl_shard_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, vp, ci]
+            lib.oracle_fljsd_kl_shard_bf16.restype = None
+            lib.oracle_fljsd_grad_shard_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, vp, vp, dbl,
+                                                         vp, vp]
+            lib.oracle_fljsd_grad_shard_bf16.restype = None
             lib.oracle_jsd_merge.argtypes = [vp, i64, i64, vp, vp]
             lib.oracle_jsd_merge.restype = dbl
             _lib = lib
@@ -544,4 +549,37 @@ def flce_grad_shard_bf16(x_bits, Wl_bits, target, v0, V, lse, scale=1.0):
     dW = np.empty((Vl, H), np.float64)
     _load().oracle_flce_grad_shard_bf16(px, pw, pt, T, H, Vl, int(v0), int(V), pl, float(scale), dx.ctypes.data,
                                         dW.ctypes.data)
+    return dx, dW
+
+
+def fljsd_kl_shard_bf16(xs_bits, Wsl_bits, xt_bits, Wtl_bits, lse, beta=0.5, temperature=1.0, threads=None):
+    """Vocab-parallel fused linear + JSD backward, one shard: with the global
+    log-sum-exps lse [2, T], each token's share of KL(P || M) over the shard's
+    columns -> float64 [T] (the shares sum to KL)."""
+    keep_alive, ptrs, T, H, Vl = _two_heads(xs_bits, Wsl_bits, xt_bits, Wtl_bits)
+    lse, pl = _c(lse, np.float64)
+    assert lse.shape == (2, T)
+    out = np.empty(T, np.float64)
+    _load().oracle_fljsd_kl_shard_bf16(*ptrs, T, H, Vl, float(beta), float(temperature), pl, out.ctypes.data,
+                                       _threads(threads))
+    return out
+
+
+def fljsd_grad_shard_bf16(xs_bits, Wsl_bits, xt_bits, Wtl_bits, lse, kl, beta=0.5, temperature=1.0, keep=None,
+                          scale=1.0):
+    """Student backward of one shard of the vocab-parallel fused linear + JSD:
+    with the global log-sum-exps lse [2, T] and KL(P || M) kl [T], returns
+    float64 (dxs share [T, H], dWs rows [Vl, H]) of scale * loss."""
+    keep_alive, ptrs, T, H, Vl = _two_heads(xs_bits, Wsl_bits, xt_bits, Wtl_bits)
+    lse, pl = _c(lse, np.float64)
+    kl, pk = _c(kl, np.float64)
+    assert lse.shape == (2, T) and kl.shape == (T,)
+    pm = None
+    if keep is not None:
+        keep, pm = _c(keep, np.uint8)
+        assert keep.shape == (T,)
+    dx = np.empty((T, H), np.float64)
+    dW = np.empty((Vl, H), np.float64)
+    _load().oracle_fljsd_grad_shard_bf16(*ptrs, T, H, Vl, float(beta), float(temperature), pm, pl, pk, float(scale),
+                                         dx.ctypes.data, dW.ctypes.data)
     return dx, dW

@@ -77,6 +77,10 @@
 //     beta P (lp - ln M) + (1 - beta) Q (lq - ln M), lp = zs/tau - lse_0,
 //     lq = zt/tau - lse_1, and the token's JSD is the sum of its shards' sums
 //     in shard order (so the split changes only the order of one sum).
+//   fused JSD student backward: the shards' shares of each token's
+//     KL(P || M) combine by a sum (one more exchange); with the global
+//     log-sum-exps and KL, the shard's columns of the student's dz, its share
+//     of dxs and its rows of dWs.
 //   fused CE backward: with each token's global log-sum-exp (from the
 //     gathered partials), the shard's columns of dz = (scale/T)(softmax -
 //     onehot); its share dz Wl of dx (the shares sum to dx) and its rows
@@ -788,6 +792,70 @@ void oracle_flce_grad_shard_bf16(const uint16_t* x16, const uint16_t* Wl16, cons
       double acc = 0.0;
       for (int64_t i = 0; i < T; ++i) acc += dz[i * Vl + v] * x[i * H + k];
       dWl[v * H + k] = acc;
+    }
+}
+
+// Vocab-parallel fused linear + JSD, the student backward of one shard
+// (student rows Wsl, teacher rows Wtl [Vl, H]), with the global log-sum-exps
+// lse [2][T] of the logits / tau:
+//   lp = zs/tau - lse_0, lq = zt/tau - lse_1, P = e^lp, lm = ln(beta P + (1-beta) e^lq);
+//   kl_i = sum over the shard's columns of P (lp - lm): the shard's share of
+//   KL(P || M) (the shares sum to it).
+void oracle_fljsd_kl_shard_bf16(const uint16_t* xs, const uint16_t* Wsl, const uint16_t* xt, const uint16_t* Wtl,
+                                int64_t T, int64_t H, int64_t Vl, double beta, double tau, const double* lse,
+                                double* kl, int threads) {
+  over_tokens(T, threads, [&](int64_t i) {
+    std::vector<double> zs(Vl), zt(Vl);
+    logits_row_bf16(xs + i * H, Wsl, H, Vl, zs.data());
+    logits_row_bf16(xt + i * H, Wtl, H, Vl, zt.data());
+    double acc = 0.0;
+    for (int64_t v = 0; v < Vl; ++v) {
+      const double lp = zs[v] / tau - lse[i], lq = zt[v] / tau - lse[T + i];
+      const double lm = std::log(beta * std::exp(lp) + (1.0 - beta) * std::exp(lq));
+      acc += std::exp(lp) * (lp - lm);
+    }
+    kl[i] = acc;
+  });
+}
+
+// ... and with each token's global KL(P || M) kl [T]: the shard's columns of
+//   dz_iv = g beta P (lp - lm - kl_i),  g = scale / (n_kept tau),
+// rows of tokens whose keep flag is 0 are 0 (keep may be null = all kept, a
+// batch with no kept token has g = 0); dxs = dz Wsl [T, H] (the shards' shares
+// sum to the student's dx), dWsl = dz^T xs [Vl, H] (its rows of dW).
+void oracle_fljsd_grad_shard_bf16(const uint16_t* xs16, const uint16_t* Wsl16, const uint16_t* xt16,
+                                  const uint16_t* Wtl16, int64_t T, int64_t H, int64_t Vl, double beta, double tau,
+                                  const uint8_t* keep, const double* lse, const double* kl, double scale, double* dxs,
+                                  double* dWsl) {
+  std::vector<double> xs(static_cast<size_t>(T) * H), Ws(static_cast<size_t>(Vl) * H),
+      dz(static_cast<size_t>(T) * Vl, 0.0);
+  for (size_t i = 0; i < xs.size(); ++i) xs[i] = bf16_to_double(xs16[i]);
+  for (size_t i = 0; i < Ws.size(); ++i) Ws[i] = bf16_to_double(Wsl16[i]);
+  int64_t kept = 0;
+  for (int64_t i = 0; i < T; ++i) kept += (!keep || keep[i]) ? 1 : 0;
+  const double g = kept ? scale / (static_cast<double>(kept) * tau) : 0.0;
+  std::vector<double> zs(Vl), zt(Vl);
+  for (int64_t i = 0; i < T; ++i) {
+    if (keep && !keep[i]) continue;
+    logits_row_bf16(xs16 + i * H, Wsl16, H, Vl, zs.data());
+    logits_row_bf16(xt16 + i * H, Wtl16, H, Vl, zt.data());
+    for (int64_t v = 0; v < Vl; ++v) {
+      const double lp = zs[v] / tau - lse[i], lq = zt[v] / tau - lse[T + i];
+      const double lm = std::log(beta * std::exp(lp) + (1.0 - beta) * std::exp(lq));
+      dz[i * Vl + v] = g * beta * std::exp(lp) * (lp - lm - kl[i]);
+    }
+  }
+  for (int64_t i = 0; i < T; ++i)
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t v = 0; v < Vl; ++v) acc += dz[i * Vl + v] * Ws[v * H + k];
+      dxs[i * H + k] = acc;
+    }
+  for (int64_t v = 0; v < Vl; ++v)
+    for (int64_t k = 0; k < H; ++k) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < T; ++i) acc += dz[i * Vl + v] * xs[i * H + k];
+      dWsl[v * H + k] = acc;
     }
 }
 

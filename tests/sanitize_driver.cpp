@@ -80,6 +80,13 @@ void oracle_fljsd_terms_shard_bf16(const uint16_t* xs, const uint16_t* Wsl, cons
                                    double* terms, int threads);
 double oracle_jsd_merge(const double* terms, int64_t k, int64_t T, const uint8_t* keep, double* rows);
 void oracle_ce_partials_lse(const double* m, const double* s, int64_t k, int64_t rows, double* lse);
+void oracle_fljsd_kl_shard_bf16(const uint16_t* xs, const uint16_t* Wsl, const uint16_t* xt, const uint16_t* Wtl,
+                                int64_t T, int64_t H, int64_t Vl, double beta, double tau, const double* lse,
+                                double* kl, int threads);
+void oracle_fljsd_grad_shard_bf16(const uint16_t* xs16, const uint16_t* Wsl16, const uint16_t* xt16,
+                                  const uint16_t* Wtl16, int64_t T, int64_t H, int64_t Vl, double beta, double tau,
+                                  const uint8_t* keep, const double* lse, const double* kl, double scale, double* dxs,
+                                  double* dWsl);
 void oracle_flce_grad_shard_bf16(const uint16_t* x16, const uint16_t* Wl16, const int64_t* target, int64_t T,
                                  int64_t H, int64_t Vl, int64_t v0, int64_t V, const double* lse, double scale,
                                  double* dx, double* dWl);
@@ -169,6 +176,20 @@ void run_shape(int64_t T, int64_t H, int64_t V, int threads) {
     }
     oracle_jsd_merge(terms.data(), k, T, keep.data(), rows.data());
     oracle_jsd_merge(terms.data(), k, T, nullptr, rows.data());
+    // the fused JSD's shard backward: KL shares, then each shard's gradient
+    std::vector<double> klsum(T, 0.0), klj(T);
+    for (int64_t j = 0; j < k; ++j) {
+      const int64_t v0 = V * j / k, w1 = V * (j + 1) / k - v0;
+      oracle_fljsd_kl_shard_bf16(xb.data(), Wb.data() + v0 * H, xb2.data(), Wb2.data() + v0 * H, T, H, w1, 0.3, 1.5,
+                                 lse.data(), klj.data(), threads);
+      for (int64_t i = 0; i < T; ++i) klsum[i] += klj[i];
+    }
+    for (int64_t j = 0; j < k; ++j) {
+      const int64_t v0 = V * j / k, w1 = V * (j + 1) / k - v0;
+      oracle_fljsd_grad_shard_bf16(xb.data(), Wb.data() + v0 * H, xb2.data(), Wb2.data() + v0 * H, T, H, w1, 0.3,
+                                   1.5, j == 0 ? keep.data() : nullptr, lse.data(), klsum.data(), 2.0, dx.data(),
+                                   dW.data());
+    }
     // the fused CE's shard backward, from the gathered partials' normalisers
     std::vector<double> glse(T);
     oracle_ce_partials_lse(m.data(), sm.data(), k, T, glse.data());

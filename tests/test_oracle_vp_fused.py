@@ -201,3 +201,40 @@ def test_flce_shard_grad_bad_target_is_nan_row():
     m, s, _ = flce_partials(x, W, t, [(0, 12), (12, 18)])
     dx, dW = oracle.flce_grad_shard_bf16(x, np.ascontiguousarray(W[:12]), t, 0, V, oracle.ce_partials_lse(m, s))
     assert np.all(np.isnan(dx[1])) and np.all(np.isfinite(np.delete(dx, 1, axis=0))) and np.all(np.isnan(dW))
+
+
+# ---------------------------------------------------------------- fused JSD student backward of a shard
+def _jsd_shard_setup(seed, T, H, V, k, tau):
+    xs, Ws, xt, Wt = jsd_inputs(seed, T, H, V)
+    shards = splits(V, k, seed)
+    sl = [(np.ascontiguousarray(Ws[v0:v0 + w]), np.ascontiguousarray(Wt[v0:v0 + w])) for v0, w in shards]
+    lse = oracle.lse_merge(np.stack([oracle.fljsd_lse_shard_bf16(xs, a, xt, b, tau) for a, b in sl]))
+    return xs, Ws, xt, Wt, shards, sl, lse
+
+
+@pytest.mark.parametrize("beta,tau", [(0.5, 1.0), (0.3, 1.7)])
+def test_fljsd_kl_shares_sum_to_scipy_rel_entr(beta, tau):
+    T, H, V = 6, 16, 43
+    xs, Ws, xt, Wt, shards, sl, lse = _jsd_shard_setup(51, T, H, V, 3, tau)
+    kl = sum(oracle.fljsd_kl_shard_bf16(xs, a, xt, b, lse, beta, tau) for a, b in sl)
+    P = sp.softmax(oracle.logits_bf16(xs, Ws) / tau, axis=1)
+    Q = sp.softmax(oracle.logits_bf16(xt, Wt) / tau, axis=1)
+    np.testing.assert_allclose(kl, sp.rel_entr(P, beta * P + (1 - beta) * Q).sum(axis=1), rtol=1e-11, atol=1e-15)
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+@pytest.mark.parametrize("beta,tau,masked", [(0.5, 1.0, False), (0.3, 2.0, True)])
+def test_fljsd_shard_grads_sum_to_unsharded(k, beta, tau, masked):
+    T, H, V = 6, 16, 41
+    xs, Ws, xt, Wt, shards, sl, lse = _jsd_shard_setup(53 + k, T, H, V, k, tau)
+    keep = (np.arange(T) % 3 != 1).astype(np.uint8) if masked else None
+    kl = sum(oracle.fljsd_kl_shard_bf16(xs, a, xt, b, lse, beta, tau) for a, b in sl)
+    dx_full, dW_full = oracle.fljsd_grad_bf16(xs, Ws, xt, Wt, beta, tau, keep, 1.4)
+    dx_sum = np.zeros_like(dx_full)
+    for (v0, w), (a, b) in zip(shards, sl):
+        dx, dW = oracle.fljsd_grad_shard_bf16(xs, a, xt, b, lse, kl, beta, tau, keep, 1.4)
+        dx_sum += dx
+        np.testing.assert_allclose(dW, dW_full[v0:v0 + w], rtol=1e-10, atol=1e-15)
+        if masked:
+            assert np.all(dx[keep == 0] == 0.0)
+    np.testing.assert_allclose(dx_sum, dx_full, rtol=1e-10, atol=1e-15)
