@@ -351,8 +351,10 @@ int fljsd_fwd_bf16_ex(const uint16_t* xs, const uint16_t* Ws, const uint16_t* xt
  * fljsd_terms_bf16: shard pass 2.  lse [2][T] fp32 device = the global
  *   log-sum-exps; terms [T] fp32 device output: each token's sum over the
  *   shard's columns of beta P ln(P/M) + (1 - beta) Q ln(Q/M), with P, Q from
- *   the global normalisers.  ws as pass 1 (the same workspace may serve both,
- *   one after the other).  Two launches.
+ *   the global normalisers.  kl_local [T] fp32 device, or NULL: with it, also
+ *   each token's share of KL(P || M) over the shard's columns (needed by the
+ *   backward below; the terms are the same bits either way).  ws as pass 1
+ *   (the same workspace may serve both, one after the other).  Two launches.
  * jsd_merge_terms: [shards][T] fp32 device (the all-gather of the terms) ->
  *   rows [T] fp32 device (16-byte aligned): each token's JSD, the shards'
  *   sums added in shard order (0 where keep[i] == 0; keep [T] uint8 device or
@@ -393,10 +395,33 @@ int fljsd_lse_partials_bf16(const uint16_t* xs, const uint16_t* Ws_local, const 
 int lse_merge_partials(const float* parts, int64_t shards, int64_t T, float* lse, void* stream);
 int fljsd_terms_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_t* xt,
                      const uint16_t* Wt_local, const float* lse, int64_t T, int64_t H,
-                     int64_t V_local, float beta, float temperature, float* terms, void* ws,
-                     size_t ws_bytes, void* stream);
+                     int64_t V_local, float beta, float temperature, float* terms, float* kl_local,
+                     void* ws, size_t ws_bytes, void* stream);
 int jsd_merge_terms(const float* terms, int64_t shards, int64_t T, const uint8_t* keep,
                     float* rows, float* loss, void* stream);
+
+/* fljsd_shard_bwd_bf16: the student's backward of one shard of the
+ * vocab-parallel fused JSD, gradients of grad_scale * loss:
+ *   lse [2][T] fp32 device   the global log-sum-exps (lse_merge_partials);
+ *   kl  [T] fp32 device      each token's KL(P || M): the shards' kl_local
+ *                            (fljsd_terms_bf16) all-gathered and summed, e.g.
+ *                            by jsd_merge_terms without a mask (its rows);
+ *   keep, beta, temperature  as for the forward;
+ *   dxs_partial [T, H] fp32  this rank's share of the student's dx (the ranks'
+ *                            shares sum to it: an all-reduce by the caller);
+ *   dWs_local [V_local, H]   fp32, this rank's rows of the student's dW;
+ *   dZs = (grad_scale / (n_kept temperature)) beta P (ln P - ln M - KL(P || M))
+ *   over the shard's columns, rounded to bf16 for the two tensor-core products
+ *   as in fljsd_fwd_bwd_bf16; left-out tokens contribute nothing.
+ *   dxs_partial, dWs_local 16-byte aligned; ws_bytes >=
+ *   fljsd_bwd_workspace_bytes(T, H, V_local), zeroed before first use.
+ * Launches: the kept-token count and the dZ pass, the two products (each with
+ * a K-slice sum when it splits K). */
+int fljsd_shard_bwd_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_t* xt,
+                         const uint16_t* Wt_local, const float* lse, const float* kl,
+                         const uint8_t* keep, int64_t T, int64_t H, int64_t V_local, float beta,
+                         float temperature, float grad_scale, float* dxs_partial, float* dWs_local,
+                         void* ws, size_t ws_bytes, void* stream);
 
 /* Deterministic mean of n fp32 values (rows 16-byte aligned, device) over
  * those with keep[i] != 0 (keep [n] uint8 device, or NULL = all; 0 when none
@@ -467,7 +492,8 @@ int lmho_set_raster_group(int group_m);
  * (log-sum-exp pass, finaliser, divergence pass, finaliser),
  * flce_partials_bf16, fljsd_lse_partials_bf16 and fljsd_terms_bf16 2 each
  * (tensor-core pass, finaliser), flce_shard_bwd_bf16 3 (normaliser merge and
- * dZ pass, dx share, dW rows), lse_merge_partials 1, jsd_merge_terms 1
+ * dZ pass, dx share, dW rows), fljsd_shard_bwd_bf16 3 (count and dZ pass, dxs
+ * share, dWs rows), lse_merge_partials 1, jsd_merge_terms 1
  * (the merge and its dependent mean together), rows_mean_f32 1.  Calls made by
  * other threads are not affected.  Pass (NULL, 0) to turn it off. */
 void lmho_set_launch_events(void* const* events, int n);

@@ -38,7 +38,7 @@ EXPORTS = (
     "flce_workspace_bytes", "flce_fwd_bf16", "flce_bwd_workspace_bytes", "flce_fwd_bwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "fljsd_bwd_workspace_bytes", "fljsd_fwd_bwd_bf16",
     "flce_cpo_workspace_bytes", "flce_cpo_fwd_bf16", "flce_cpo_bwd_workspace_bytes", "flce_cpo_fwd_bwd_bf16",
-    "flce_partials_bf16", "flce_shard_bwd_bf16", "fljsd_lse_partials_bf16", "lse_merge_partials", "fljsd_terms_bf16", "jsd_merge_terms",
+    "flce_partials_bf16", "flce_shard_bwd_bf16", "fljsd_lse_partials_bf16", "lse_merge_partials", "fljsd_terms_bf16", "fljsd_shard_bwd_bf16", "jsd_merge_terms",
     "rows_mean_f32",
     "lmho_ws_status", "lmho_probe_read", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
@@ -120,8 +120,11 @@ def load():
         lib.fljsd_lse_partials_bf16.restype = ci
         lib.lse_merge_partials.argtypes = [vp, i64, i64, vp, vp]
         lib.lse_merge_partials.restype = ci
-        lib.fljsd_terms_bf16.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, f32, f32, vp, vp, sz, vp]
+        lib.fljsd_terms_bf16.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, f32, f32, vp, vp, vp, sz, vp]
         lib.fljsd_terms_bf16.restype = ci
+        lib.fljsd_shard_bwd_bf16.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, f32, f32, vp, vp, vp, sz,
+                                             vp]
+        lib.fljsd_shard_bwd_bf16.restype = ci
         lib.jsd_merge_terms.argtypes = [vp, i64, i64, vp, vp, vp, vp]
         lib.jsd_merge_terms.restype = ci
         lib.rows_mean_f32.argtypes = [vp, i64, vp, vp, vp]
@@ -699,10 +702,12 @@ def lse_merge_partials(parts, out=None, stream=None):
     return out
 
 
-def fljsd_terms_bf16(xs, Ws_local, xt, Wt_local, lse, beta=0.5, temperature=1.0, out=None, ws=None, stream=None):
+def fljsd_terms_bf16(xs, Ws_local, xt, Wt_local, lse, beta=0.5, temperature=1.0, out=None, ws=None, stream=None,
+                     kl_local=None):
     """Vocab-parallel fused linear + JSD, shard pass 2: with the global
     log-sum-exps lse fp32 [2, T], each token's sum of the JSD terms over the
-    shard's columns, fp32 [T]."""
+    shard's columns, fp32 [T].  kl_local (fp32 [T], optional) receives each
+    token's share of KL(P || M) over the shard, for the backward."""
     lib = load()
     ptrs, T, H, Vl = _shard_pair(xs, Ws_local, xt, Wt_local)
     pl = _dev(lse, "lse", torch.float32, 2)
@@ -712,13 +717,48 @@ def fljsd_terms_bf16(xs, Ws_local, xt, Wt_local, lse, beta=0.5, temperature=1.0,
         out = torch.empty(T, dtype=torch.float32, device=xs.device)
     if tuple(out.shape) != (T,):
         raise ValueError("out must be [T]")
+    pkl = None
+    if kl_local is not None:
+        pkl = _dev(kl_local, "kl_local", torch.float32, 1)
+        if kl_local.shape[0] != T:
+            raise ValueError("kl_local must be [T]")
     if ws is None:
         ws = workspace(lib.fljsd_workspace_bytes(T, H, Vl), xs.device)
-    with _on(xs, Ws_local, xt, Wt_local, lse, out, ws):
+    with _on(xs, Ws_local, xt, Wt_local, lse, out, ws, kl_local):
         _check(lib.fljsd_terms_bf16(*ptrs, pl, T, H, Vl, float(beta), float(temperature),
-                                    _dev(out, "out", torch.float32, 1), _dev(ws, "ws", torch.uint8), ws.numel(),
+                                    _dev(out, "out", torch.float32, 1), pkl, _dev(ws, "ws", torch.uint8), ws.numel(),
                                     _stream(stream)), "fljsd_terms_bf16")
     return out
+
+
+def fljsd_shard_bwd_bf16(xs, Ws_local, xt, Wt_local, lse, kl, beta=0.5, temperature=1.0, keep=None, grad_scale=1.0,
+                         dx=None, dW=None, ws=None, stream=None):
+    """Student backward of one shard of the vocab-parallel fused linear + JSD:
+    gradients of grad_scale * loss given the global log-sum-exps lse fp32
+    [2, T] and each token's KL(P || M) kl fp32 [T] (the shards' kl_local
+    summed).  Returns (dxs share fp32 [T, H] -- the ranks' shares sum to the
+    student's dx --, dWs rows fp32 [V_local, H])."""
+    lib = load()
+    ptrs, T, H, Vl = _shard_pair(xs, Ws_local, xt, Wt_local)
+    pl = _dev(lse, "lse", torch.float32, 2)
+    pk = _dev(kl, "kl", torch.float32, 1)
+    if tuple(lse.shape) != (2, T) or kl.shape[0] != T:
+        raise ValueError("lse must be [2, T] and kl [T]")
+    pm = _keep_ptr(keep, T)
+    if dx is None:
+        dx = torch.empty((T, H), dtype=torch.float32, device=xs.device)
+    if dW is None:
+        dW = torch.empty((Vl, H), dtype=torch.float32, device=xs.device)
+    if tuple(dx.shape) != (T, H) or tuple(dW.shape) != (Vl, H):
+        raise ValueError("dx must be [T, H] and dW [V_local, H]")
+    if ws is None:
+        ws = workspace(lib.fljsd_bwd_workspace_bytes(T, H, Vl), xs.device)
+    with _on(xs, Ws_local, xt, Wt_local, lse, kl, dx, dW, ws, keep):
+        _check(lib.fljsd_shard_bwd_bf16(*ptrs, pl, pk, pm, T, H, Vl, float(beta), float(temperature),
+                                        float(grad_scale), _dev(dx, "dx", torch.float32, 2),
+                                        _dev(dW, "dW", torch.float32, 2), _dev(ws, "ws", torch.uint8), ws.numel(),
+                                        _stream(stream)), "fljsd_shard_bwd_bf16")
+    return dx, dW
 
 
 def jsd_merge_terms(terms, keep=None, rows=None, loss=None, stream=None):

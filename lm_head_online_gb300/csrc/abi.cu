@@ -729,15 +729,16 @@ int lse_merge_partials(const float* parts, int64_t shards, int64_t T, float* lse
 
 int fljsd_terms_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_t* xt, const uint16_t* Wt_local,
                      const float* lse, int64_t T, int64_t H, int64_t V_local, float beta, float temperature,
-                     float* terms, void* ws, size_t ws_bytes, void* stream) {
+                     float* terms, float* kl_local, void* ws, size_t ws_bytes, void* stream) {
   if (!lse || !terms) return LMHO_ERR_INVALID_ARG;
   if (int c = check_jsd_shard(xs, Ws_local, xt, Wt_local, T, H, V_local, temperature, ws, ws_bytes)) return c;
   if (!(beta > 0.f && beta < 1.f)) return LMHO_ERR_INVALID_ARG;
   const size_t xb = 2 * static_cast<size_t>(T) * H, wb = 2 * static_cast<size_t>(V_local) * H;
   const Range in[5] = {rng(xs, xb), rng(Ws_local, wb), rng(xt, xb), rng(Wt_local, wb),
                        rng(lse, 8 * static_cast<size_t>(T))};
-  const Range out[2] = {rng(terms, 4 * static_cast<size_t>(T)), rng(ws, ws_bytes)};
-  if (int a = check_alias(in, 5, out, 2)) return a;
+  const Range out[3] = {rng(terms, 4 * static_cast<size_t>(T)), rng(ws, ws_bytes),
+                        rng(kl_local, kl_local ? 4 * static_cast<size_t>(T) : 0)};
+  if (int a = check_alias(in, 5, out, 3)) return a;
   int sms = 0;
   if (int d = current_device(&sms)) return d;
   if (int e = get_encode()) return e;
@@ -748,7 +749,47 @@ int fljsd_terms_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_
   const FusedGeometry g = geometry(T, H, V_local, kBN_JSD, kGroupTwoHead);
   const FusedWs w = fljsd_ws_carve(ws, ws_bytes, T, V_local);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
-  return cuda_status(launch_fljsd_terms_shard(txs, tws, txt, twt, g, lse, beta, 1.f / temperature, terms, w, L));
+  return cuda_status(
+      launch_fljsd_terms_shard(txs, tws, txt, twt, g, lse, beta, 1.f / temperature, terms, kl_local, w, L));
+}
+
+int fljsd_shard_bwd_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_t* xt, const uint16_t* Wt_local,
+                         const float* lse, const float* kl, const uint8_t* keep, int64_t T, int64_t H, int64_t V_local,
+                         float beta, float temperature, float grad_scale, float* dxs_partial, float* dWs_local,
+                         void* ws, size_t ws_bytes, void* stream) {
+  if (!xs || !Ws_local || !xt || !Wt_local || !lse || !kl || !dxs_partial || !dWs_local || !ws)
+    return LMHO_ERR_INVALID_ARG;
+  if (int c = check_fused_common(T, H, V_local)) return c;
+  if (!(beta > 0.f && beta < 1.f)) return LMHO_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !(1.f / temperature < INFINITY) || !std::isfinite(grad_scale)) return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(xs) || !aligned16(Ws_local) || !aligned16(xt) || !aligned16(Wt_local) || !aligned16(dxs_partial) ||
+      !aligned16(dWs_local))
+    return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < fljsd_bwd_ws_bytes(T, H, V_local) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const size_t xb = 2 * static_cast<size_t>(T) * H, wb = 2 * static_cast<size_t>(V_local) * H;
+  const Range in[7] = {rng(xs, xb), rng(Ws_local, wb), rng(xt, xb), rng(Wt_local, wb),
+                       rng(lse, 8 * static_cast<size_t>(T)), rng(kl, 4 * static_cast<size_t>(T)),
+                       rng(keep, keep ? static_cast<size_t>(T) : 0)};
+  const Range out[3] = {rng(dxs_partial, 4 * static_cast<size_t>(T) * H),
+                        rng(dWs_local, 4 * static_cast<size_t>(V_local) * H), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 7, out, 3)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  if (int e = get_encode()) return e;
+  const BwdLayout lay = bwd_layout(T, H, V_local, fljsd_ws_bytes(T, H, V_local));
+  const FusedWs w = fljsd_ws_carve(ws, ws_bytes, T, V_local);
+  const FlceBwdWs bw = bwd_carve(ws, lay);
+  float* inv_count = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.end - kAlign);
+  FljsdBwdMaps m;
+  if (tmap_bf16(&m.xs, xs, T, H, kBM) || tmap_bf16(&m.xt, xt, T, H, kBM) ||
+      tmap_bf16(&m.wsj, Ws_local, V_local, H, kBN_JSD) || tmap_bf16(&m.wtj, Wt_local, V_local, H, kBN_JSD) ||
+      tmap_bf16_ld(&m.dz, bw.dz, T, V_local, bw.ld_dz, kBM) || tmap_bf16_mn(&m.ws_mn, Ws_local, V_local, H, H, kBoxBGrad) ||
+      tmap_bf16_mn(&m.dz_mn, bw.dz, T, V_local, bw.ld_dz, kBM) || tmap_bf16_mn(&m.xs_mn, xs, T, H, H, kBoxBGrad))
+    return LMHO_ERR_CUDA;
+  const FusedGeometry g = geometry(T, H, V_local, kBN_JSD, kGroupTwoHead);
+  const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_fljsd_shard_bwd(m, g, beta, 1.f / temperature, keep, grad_scale, lse, kl, dxs_partial,
+                                            dWs_local, w, bw, inv_count, L));
 }
 
 int jsd_merge_terms(const float* terms, int64_t shards, int64_t T, const uint8_t* keep, float* rows, float* loss,

@@ -1173,22 +1173,34 @@ cudaError_t launch_fljsd_lse_shard(const CUtensorMap& tm_xs, const CUtensorMap& 
 
 cudaError_t launch_fljsd_terms_shard(const CUtensorMap& tm_xs, const CUtensorMap& tm_wsj, const CUtensorMap& tm_xt,
                                      const CUtensorMap& tm_wtj, const FusedGeometry& g_jsd, const float* lse,
-                                     float beta, float inv_tau, float* terms, const FusedWs& ws,
+                                     float beta, float inv_tau, float* terms, float* kl_local, const FusedWs& ws,
                                      const FusedLaunch& L) {
-  Params q = base_params<kModeJSD>(g_jsd, L, ws.ctrl);
-  q.units = static_cast<int64_t>(q.num_m) * q.num_n;
-  q.part0 = ws.part0;
-  q.lse = lse;
-  q.beta = beta;
-  q.inv_tau = inv_tau;
   launch_mark(0, L.stream);
-  cudaError_t e = launch_gemm<kModeJSD>(tm_xs, tm_wsj, tm_xt, tm_wtj, q, L);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if (kl_local) {  // the backward's variant: also each token's share of KL(P || M); the same divergence bits
+    Params q = base_params<kModeJSDK>(g_jsd, L, ws.ctrl);
+    q.units = static_cast<int64_t>(q.num_m) * q.num_n;
+    q.part0 = ws.part0;
+    q.part1 = ws.part1;
+    q.lse = lse;
+    q.beta = beta;
+    q.inv_tau = inv_tau;
+    if ((e = launch_gemm<kModeJSDK>(tm_xs, tm_wsj, tm_xt, tm_wtj, q, L)) != cudaSuccess) return e;
+  } else {
+    Params q = base_params<kModeJSD>(g_jsd, L, ws.ctrl);
+    q.units = static_cast<int64_t>(q.num_m) * q.num_n;
+    q.part0 = ws.part0;
+    q.lse = lse;
+    q.beta = beta;
+    q.inv_tau = inv_tau;
+    if ((e = launch_gemm<kModeJSD>(tm_xs, tm_wsj, tm_xt, tm_wtj, q, L)) != cudaSuccess) return e;
+  }
   launch_mark(1, L.stream);
   const unsigned blocks = static_cast<unsigned>((g_jsd.T + kFinRows - 1) / kFinRows);
+  static_assert(ModeCfg<kModeJSD>::kColSplit == ModeCfg<kModeJSDK>::kColSplit, "one partial layout");
   jsd_finalize<<<blocks, kFinRows * kFinSplit, 0, L.stream>>>(
       ws.part0, g_jsd.T, static_cast<int>(g_jsd.num_n * ModeCfg<kModeJSD>::kColSplit), nullptr, terms, nullptr,
-      ws.ctrl);
+      ws.ctrl, kl_local ? ws.part1 : nullptr, kl_local);
   launch_mark(2, L.stream);
   return cudaGetLastError();
 }
@@ -1414,6 +1426,40 @@ cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const FusedGeometry& g_l
       cudaSuccess)
     return e;
   launch_mark(4, L.stream);
+  return cudaSuccess;
+}
+
+cudaError_t launch_fljsd_shard_bwd(const FljsdBwdMaps& m, const FusedGeometry& g_jsd, float beta, float inv_tau,
+                                   const uint8_t* keep, float grad_scale, const float* lse, const float* kl,
+                                   float* dxs, float* dWs, const FusedWs& ws, const FlceBwdWs& bw, float* inv_count,
+                                   const FusedLaunch& L) {
+  cudaError_t e;
+  const int64_t T = g_jsd.T, H = g_jsd.H, V = g_jsd.V;
+  launch_mark(0, L.stream);
+  // 1 / (kept tokens), then both heads' tiles of this shard again: the student's dZ columns
+  if ((e = launch_kept_inv_count(keep, T, inv_count, L.stream)) != cudaSuccess) return e;
+  Params r = base_params<kModeDZJ>(g_jsd, L, ws.ctrl);
+  r.units = static_cast<int64_t>(r.num_m) * r.num_n;
+  r.lse = lse;
+  r.beta = beta;
+  r.inv_tau = inv_tau;
+  r.gscale = grad_scale * inv_tau;
+  r.kl = kl;
+  r.keep = keep;
+  r.inv_count = inv_count;
+  r.dz = bw.dz;
+  r.ld_dz = bw.ld_dz;
+  if ((e = launch_gemm<kModeDZJ>(m.xs, m.wsj, m.xt, m.wtj, r, L)) != cudaSuccess) return e;
+  launch_mark(1, L.stream);
+  // this shard's share of dxs = dZs Ws_local (K = V_local), its rows of dWs = dZs^T xs (K = T)
+  if ((e = launch_store_gemm<kModeStore>(m.dz, m.ws_mn, T, H, V, dxs, bw.split, g_jsd.group_store, ws.ctrl, L)) !=
+      cudaSuccess)
+    return e;
+  launch_mark(2, L.stream);
+  if ((e = launch_store_gemm<kModeStoreT>(m.dz_mn, m.xs_mn, V, H, T, dWs, bw.split, g_jsd.group_store, ws.ctrl, L)) !=
+      cudaSuccess)
+    return e;
+  launch_mark(3, L.stream);
   return cudaSuccess;
 }
 

@@ -176,9 +176,11 @@ cudaError_t launch_fljsd_lse_shard(const CUtensorMap& tm_xs, const CUtensorMap& 
                                    float* lse_local, const FusedWs& ws, const FusedLaunch& L);
 //  * fused linear + JSD, second pass: with the global log-sum-exps lse [2][T],
 //    each token's sum of the JSD terms over the shard's columns -> terms [T].
+//    With kl_local set, also each token's share of KL(P || M) over the shard
+//    -> kl_local [T] (the backward's variant; the same divergence bits).
 cudaError_t launch_fljsd_terms_shard(const CUtensorMap& tm_xs, const CUtensorMap& tm_wsj, const CUtensorMap& tm_xt,
                                      const CUtensorMap& tm_wtj, const FusedGeometry& g_jsd, const float* lse,
-                                     float beta, float inv_tau, float* terms, const FusedWs& ws,
+                                     float beta, float inv_tau, float* terms, float* kl_local, const FusedWs& ws,
                                      const FusedLaunch& L);
 // Their combinations (vp_merge.cu): global log-sum-exps [2][T] from k shards'
 // [k][2][T]; per-token JSD rows [T] and their batchmean from k shards' term
@@ -189,6 +191,8 @@ cudaError_t launch_lse_merge(const float* parts, int64_t shards, int64_t T, floa
 cudaError_t launch_jsd_merge(const float* terms, int64_t shards, int64_t T, const uint8_t* keep, float* rows,
                              float* loss, int num_sms, cudaStream_t st);
 cudaError_t launch_rows_mean(const float* rows, int64_t n, const uint8_t* keep, float* mean, cudaStream_t st);
+// 1 / (kept tokens) (keep may be null: 1 / T; 0 when none is kept) -> inv_count [1].
+cudaError_t launch_kept_inv_count(const uint8_t* keep, int64_t T, float* inv_count, cudaStream_t st);
 // Each token's global log-sum-exp [T] from gathered CE partials [k][3][T].
 cudaError_t launch_partials_lse(const float* partials, int64_t shards, int64_t T, float* lse, int num_sms,
                                 cudaStream_t st);
@@ -262,6 +266,13 @@ struct FljsdBwdMaps {
   CUtensorMap dz_mn, xs_mn;                     // dWs = dZs^T xs
 };
 size_t fljsd_bwd_ws_bytes(int64_t T, int64_t H, int64_t V);
+// Student backward of one vocabulary shard of the fused linear + JSD: with the
+// global log-sum-exps lse [2][T] and KL(P || M) kl [T] (the shards' shares
+// summed), the shard's dZs columns, its share of dxs and its rows of dWs.
+cudaError_t launch_fljsd_shard_bwd(const FljsdBwdMaps& m, const FusedGeometry& g_jsd, float beta, float inv_tau,
+                                   const uint8_t* keep, float grad_scale, const float* lse, const float* kl,
+                                   float* dxs, float* dWs, const FusedWs& ws, const FlceBwdWs& bw, float* inv_count,
+                                   const FusedLaunch& L);
 cudaError_t launch_fljsd_fwd_bwd(const FljsdBwdMaps& m, const FusedGeometry& g_lse, const FusedGeometry& g_jsd,
                                  float beta, float inv_tau, const uint8_t* keep, float grad_scale, float* loss,
                                  float* dxs, float* dWs, const FusedWs& ws, const FlceBwdWs& bw, float* kl,

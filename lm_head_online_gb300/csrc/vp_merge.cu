@@ -85,6 +85,26 @@ __global__ void __launch_bounds__(256) partials_lse_rows(const float* __restrict
   }
 }
 
+// 1 / (number of tokens with keep != 0), or 1 / T with no mask, 0 when none is
+// kept: one block, an exact integer count in a fixed order.
+__global__ void __launch_bounds__(256) kept_inv_count_kernel(const uint8_t* __restrict__ keep, int64_t T,
+                                                              float* __restrict__ inv_count) {
+  __shared__ int64_t s_cnt[256];
+  int64_t c = 0;
+  if (keep) {
+    for (int64_t i = threadIdx.x; i < T; i += 256) c += __ldg(keep + i) != 0;
+  } else {
+    for (int64_t i = threadIdx.x; i < T; i += 256) ++c;
+  }
+  s_cnt[threadIdx.x] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int64_t n = 0;
+    for (int k = 0; k < 256; ++k) n += s_cnt[k];
+    *inv_count = n > 0 ? 1.f / static_cast<float>(n) : 0.f;
+  }
+}
+
 unsigned grid_for(int64_t n, int num_sms) {
   int64_t blocks = (n + 255) / 256;
   if (blocks > 8 * static_cast<int64_t>(num_sms)) blocks = 8 * static_cast<int64_t>(num_sms);
@@ -126,6 +146,11 @@ cudaError_t launch_jsd_merge(const float* terms, int64_t shards, int64_t T, cons
 cudaError_t launch_partials_lse(const float* partials, int64_t shards, int64_t T, float* lse, int num_sms,
                                 cudaStream_t st) {
   partials_lse_rows<<<grid_for(T, num_sms), 256, 0, st>>>(partials, shards, T, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kept_inv_count(const uint8_t* keep, int64_t T, float* inv_count, cudaStream_t st) {
+  kept_inv_count_kernel<<<1, 256, 0, st>>>(keep, T, inv_count);
   return cudaGetLastError();
 }
 

@@ -143,3 +143,28 @@ def vocab_parallel_fljsd(xs, Ws_local, xt, Wt_local, beta=0.5, temperature=1.0, 
     terms = fljsd_terms_bf16(xs, Ws_local, xt, Wt_local, lse, beta, temperature, ws=ws)       # [T]
     all_terms = gather_partials(terms.view(1, T), group).view(-1, T)                         # [world, T]
     return jsd_merge_terms(all_terms, keep)
+
+
+def vocab_parallel_fljsd_fwd_bwd(xs, Ws_local, xt, Wt_local, beta=0.5, temperature=1.0, keep=None, grad_scale=1.0,
+                                 group=None, ws=None):
+    """vocab_parallel_fljsd and the student's gradients of grad_scale * loss:
+    returns (batchmean [1], per-token JSD [T], dxs [T, H] fp32 -- the ranks'
+    shares summed by one all-reduce --, dWs_local [V_local, H] fp32, this
+    rank's rows of the student's dW).  The second exchange carries each
+    token's KL(P || M) share beside its JSD terms ([2, T] per rank)."""
+    from lm_head_online_gb300 import (fljsd_bwd_workspace_bytes, fljsd_lse_partials_bf16, fljsd_shard_bwd_bf16,
+                                      fljsd_terms_bf16, jsd_merge_terms, lse_merge_partials, workspace)
+
+    T, H = xs.shape
+    if ws is None:
+        ws = workspace(fljsd_bwd_workspace_bytes(T, H, Ws_local.shape[0]), xs.device)
+    lse_local = fljsd_lse_partials_bf16(xs, Ws_local, xt, Wt_local, temperature, ws=ws)       # [2, T]
+    lse = lse_merge_partials(gather_partials(lse_local, group))                              # [2, T]
+    tk = torch.empty((2, T), dtype=torch.float32, device=xs.device)                        # terms, KL shares
+    fljsd_terms_bf16(xs, Ws_local, xt, Wt_local, lse, beta, temperature, out=tk[0], ws=ws, kl_local=tk[1])
+    allp = gather_partials(tk, group)                                                        # [world, 2, T]
+    loss, rows = jsd_merge_terms(allp[:, 0].contiguous(), keep)
+    _, kl = jsd_merge_terms(allp[:, 1].contiguous())
+    dx, dW = fljsd_shard_bwd_bf16(xs, Ws_local, xt, Wt_local, lse, kl, beta, temperature, keep, grad_scale, ws=ws)
+    dist.all_reduce(dx, op=dist.ReduceOp.SUM, group=group)
+    return loss, rows, dx, dW

@@ -241,12 +241,29 @@ def test_vocab_parallel_fused_argument_checks(lib):
     assert lib.lse_merge_partials(A, 0, 4, C, None) == 1
     assert lib.lse_merge_partials(A, 2, 0, C, None) == 1
     assert lib.lse_merge_partials(A, 2, 4, A + 32, None) == 2                  # lse inside parts [2][2][4]
-    # fljsd_terms_bf16(xs, Ws, xt, Wt, lse, T, H, V_local, beta, temperature, terms, ws, ws_bytes, stream)
-    assert lib.fljsd_terms_bf16(A, B, C, D, None, 4, 16, 10, f(0.5), f(1.0), E + (1 << 31), E, ws, None) == 1
-    assert lib.fljsd_terms_bf16(A, B, C, D, 0x60000000, 4, 16, 10, f(1.0), f(1.0), E + (1 << 31), E, ws,
+    # fljsd_terms_bf16(xs, Ws, xt, Wt, lse, T, H, V_local, beta, temperature, terms, kl_local, ws, ws_bytes,
+    #                  stream)
+    assert lib.fljsd_terms_bf16(A, B, C, D, None, 4, 16, 10, f(0.5), f(1.0), E + (1 << 31), None, E, ws,
+                                None) == 1
+    assert lib.fljsd_terms_bf16(A, B, C, D, 0x60000000, 4, 16, 10, f(1.0), f(1.0), E + (1 << 31), None, E, ws,
                                 None) == 1                                     # beta not in (0, 1)
-    assert lib.fljsd_terms_bf16(A, B, C, D, 0x60000000, 4, 16, 10, f(0.5), f(1.0), 0x60000010, E, ws,
+    assert lib.fljsd_terms_bf16(A, B, C, D, 0x60000000, 4, 16, 10, f(0.5), f(1.0), 0x60000010, None, E, ws,
                                 None) == 2                                     # terms over lse
+    assert lib.fljsd_terms_bf16(A, B, C, D, 0x60000000, 4, 16, 10, f(0.5), f(1.0), E + (1 << 31),
+                                E + (1 << 31) + 8, E, ws, None) == 2           # kl_local over terms
+    # fljsd_shard_bwd_bf16(xs, Ws, xt, Wt, lse, kl, keep, T, H, V_local, beta, temperature, grad_scale, dxs, dWs,
+    #                      ws, ws_bytes, stream)
+    L_, K_ = 0x60000000, 0x61000000
+    assert lib.fljsd_shard_bwd_bf16(A, B, C, D, L_, None, None, 4, 16, 10, f(0.5), f(1.0), f(1.0), E + (1 << 31),
+                                    E + (1 << 32), E, ws, None) == 1           # null kl
+    assert lib.fljsd_shard_bwd_bf16(A, B, C, D, L_, K_, None, 4, 16, 10, f(0.0), f(1.0), f(1.0), E + (1 << 31),
+                                    E + (1 << 32), E, ws, None) == 1           # beta
+    assert lib.fljsd_shard_bwd_bf16(A, B, C, D, L_, K_, None, 4, 16, 10, f(0.5), f(1.0), f(math.nan),
+                                    E + (1 << 31), E + (1 << 32), E, ws, None) == 1   # grad scale
+    assert lib.fljsd_shard_bwd_bf16(A, B, C, D, L_, K_, None, 4, 16, 10, f(0.5), f(1.0), f(1.0), E + (1 << 31),
+                                    E + (1 << 32), E, 256, None) == 3          # short workspace
+    assert lib.fljsd_shard_bwd_bf16(A, B, C, D, L_, K_, None, 4, 16, 10, f(0.5), f(1.0), f(1.0), K_,
+                                    E + (1 << 32), E, ws, None) == 2           # dx over kl
     # jsd_merge_terms(terms, shards, T, keep, rows, loss, stream)
     assert lib.jsd_merge_terms(A, 2, 4, None, None, C, None) == 1
     assert lib.jsd_merge_terms(A, 0, 4, None, B, C, None) == 1

@@ -212,3 +212,40 @@ def test_vocab_parallel_flce_backward_exchange_over_gloo_ranks(world):
     for dx, dW, (v0, w) in out.values():
         np.testing.assert_allclose(dx, dx_want, rtol=1e-11, atol=1e-15)
         np.testing.assert_allclose(dW, dW_want[v0:v0 + w], rtol=1e-11, atol=1e-15)
+
+
+def _vp_fljsd_bwd(rank, world):
+    """The student backward's exchanges (log-sum-exps, then JSD terms and KL
+    shares in one [2, T] block, then the all-reduce of the dx shares), each
+    rank's steps done by the oracle."""
+    T, H, V = 5, 16, 67
+    xs = gen.normal_bf16_bits(9, 0, (T, H), sigma=1.0)
+    Ws = gen.normal_bf16_bits(9, 1, (V, H), sigma=0.3)
+    xt = gen.normal_bf16_bits(9, 2, (T, H), sigma=1.0)
+    Wt = gen.normal_bf16_bits(9, 3, (V, H), sigma=0.3)
+    keep = (np.arange(T) != 3).astype(np.uint8)
+    v0, w = lmdist.shard_vocab(V, rank, world)
+    a, b = np.ascontiguousarray(Ws[v0:v0 + w]), np.ascontiguousarray(Wt[v0:v0 + w])
+    lse = oracle.lse_merge(lmdist.gather_partials(torch.from_numpy(oracle.fljsd_lse_shard_bf16(xs, a, xt, b, 1.2)))
+                           .numpy())
+    tk = np.stack([oracle.fljsd_terms_shard_bf16(xs, a, xt, b, lse, 0.4, 1.2),
+                   oracle.fljsd_kl_shard_bf16(xs, a, xt, b, lse, 0.4, 1.2)])
+    allp = lmdist.gather_partials(torch.from_numpy(tk)).numpy()
+    kl = allp[:, 1].sum(axis=0)
+    dx, dW = oracle.fljsd_grad_shard_bf16(xs, a, xt, b, lse, kl, 0.4, 1.2, keep, 1.1)
+    dxt = torch.from_numpy(dx)
+    dist.all_reduce(dxt, op=dist.ReduceOp.SUM)
+    return dxt.numpy(), dW, (v0, w)
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_vocab_parallel_fljsd_backward_exchanges_over_gloo_ranks(world):
+    out = spawn(_vp_fljsd_bwd, world=world)
+    T, H, V = 5, 16, 67
+    dx_want, dW_want = oracle.fljsd_grad_bf16(
+        gen.normal_bf16_bits(9, 0, (T, H), sigma=1.0), gen.normal_bf16_bits(9, 1, (V, H), sigma=0.3),
+        gen.normal_bf16_bits(9, 2, (T, H), sigma=1.0), gen.normal_bf16_bits(9, 3, (V, H), sigma=0.3), 0.4, 1.2,
+        (np.arange(T) != 3).astype(np.uint8), 1.1)
+    for dx, dW, (v0, w) in out.values():
+        np.testing.assert_allclose(dx, dx_want, rtol=1e-10, atol=1e-15)
+        np.testing.assert_allclose(dW, dW_want[v0:v0 + w], rtol=1e-10, atol=1e-15)

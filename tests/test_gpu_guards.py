@@ -240,11 +240,24 @@ def test_vocab_parallel_fused_guards(gpu_lib, T, H, V):
         assert gpu_lib.ws_status(ws) == 0
     lse = g.view(2 * T * 4, torch.float32, (2, T))
     gpu_lib.lse_merge_partials(lparts, out=lse)
+    kls = g.view(k * T * 4, torch.float32, (k, T))
     for j, (v0, w) in enumerate(shards):
         ws = g.ws(gpu_lib.fljsd_workspace_bytes(T, H, w))
-        gpu_lib.fljsd_terms_bf16(x, W[v0:v0 + w], xt, Wt[v0:v0 + w], lse, 0.3, 1.5, out=terms[j], ws=ws)
+        gpu_lib.fljsd_terms_bf16(x, W[v0:v0 + w], xt, Wt[v0:v0 + w], lse, 0.3, 1.5, out=terms[j], ws=ws,
+                                 kl_local=kls[j])
         g.check()
         assert gpu_lib.ws_status(ws) == 0
+    kl = g.view(T * 4, torch.float32, (T,))
+    gpu_lib.jsd_merge_terms(kls, rows=kl, loss=g.view(4, torch.float32, (1,)))
+    for v0, w in shards:
+        dxs = g.view(4 * T * H, torch.float32, (T, H))
+        dWs = g.view(4 * w * H, torch.float32, (w, H))
+        ws = g.ws(gpu_lib.fljsd_bwd_workspace_bytes(T, H, w))
+        gpu_lib.fljsd_shard_bwd_bf16(x, W[v0:v0 + w], xt, Wt[v0:v0 + w], lse, kl, 0.3, 1.5, keep, 2.0, dx=dxs, dW=dWs,
+                                     ws=ws)
+        g.check()
+        assert gpu_lib.ws_status(ws) == 0
+        written(dxs, dWs)
     rows = g.view(T * 4, torch.float32, (T,))
     loss = g.view(4, torch.float32, (1,))
     gpu_lib.jsd_merge_terms(terms, keep, rows=rows, loss=loss)
@@ -263,7 +276,7 @@ def test_vocab_parallel_fused_guards(gpu_lib, T, H, V):
         grads += [dx, dW]
     g.check()
     assert not bool(torch.isnan(parts).any()), "a partial was never written"   # -inf is a valid target logit
-    written(lparts, lse, terms, rows, loss, ce_rows, mean, *grads)
+    written(lparts, lse, terms, kls, kl, rows, loss, ce_rows, mean, *grads)
     unchanged(before, [x, xt, W, Wt, t, keep])
 
 

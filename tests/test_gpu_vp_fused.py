@@ -327,6 +327,83 @@ def test_fljsd_vp_full_size_sampled(gpu_lib):
     np.testing.assert_allclose(np64(rows)[idx], want, rtol=RTOL_JSD_TOKEN, atol=ATOL_JSD_TOKEN)
 
 
+def run_fljsd_vp_bwd(lmho, d, shards, beta, tau, keep, scale):
+    """The vocab-parallel fused JSD forward and student backward over emulated
+    shards: returns (lse [2, T], terms and KL shares [k, 2, T], KL [T], rows,
+    loss, [(dxs share, dWs rows)])."""
+    xsd, Wsd, xtd, Wtd = d
+    T = xsd.shape[0]
+    k = len(shards)
+    local = [(Wsd[v0:v0 + w].clone(), Wtd[v0:v0 + w].clone()) for v0, w in shards]
+    lparts = torch.full((k, 2, T), float("nan"), device="cuda")
+    for j, (a, b) in enumerate(local):
+        lmho.fljsd_lse_partials_bf16(xsd, a, xtd, b, tau, out=lparts[j])
+    lse = lmho.lse_merge_partials(lparts)
+    tk = torch.full((k, 2, T), float("nan"), device="cuda")
+    for j, (a, b) in enumerate(local):
+        lmho.fljsd_terms_bf16(xsd, a, xtd, b, lse, beta, tau, out=tk[j, 0], kl_local=tk[j, 1])
+    loss, rows = lmho.jsd_merge_terms(tk[:, 0].contiguous(), keep)
+    _, kl = lmho.jsd_merge_terms(tk[:, 1].contiguous())
+    outs = [lmho.fljsd_shard_bwd_bf16(xsd, a, xtd, b, lse, kl, beta, tau, keep, scale) for a, b in local]
+    torch.cuda.synchronize()
+    return lse, tk, kl, rows, loss, outs
+
+
+@pytest.mark.parametrize("T,H,V,k,beta,tau,masked", [(130, 128, 1000, 3, 0.5, 1.0, False),
+                                                     (64, 256, 513, 2, 0.3, 2.0, True),
+                                                     (96, 1024, 2000, 3, 0.5, 1.0, False),
+                                                     (5, 64, 37, 4, 0.7, 0.8, True)])
+def test_fljsd_vp_backward_matches_oracle(gpu_lib, T, H, V, k, beta, tau, masked):
+    """KL shares against the oracle's; every shard's dxs share and dWs rows
+    within their per-element bounds of the oracle's shard gradient; the
+    shares' sum within the summed bounds of the unsharded oracle dxs."""
+    xs, Ws, xt, Wt = jsd_inputs(80 + k, T, H, V, sw=2.0 / math.sqrt(H))
+    keep = (np.arange(T) % 4 != 1).astype(np.uint8) if masked else None
+    shards = uneven_shards(V, k, 20 + k)
+    d = [to_dev_bf16(a) for a in (xs, Ws, xt, Wt)]
+    _, tk, _, rows, loss, outs = run_fljsd_vp_bwd(gpu_lib, d, shards, beta, tau,
+                                                  None if keep is None else to_dev(keep), 2.5)
+    sl = [(np.ascontiguousarray(Ws[v0:v0 + w]), np.ascontiguousarray(Wt[v0:v0 + w])) for v0, w in shards]
+    lse = oracle.lse_merge(np.stack([oracle.fljsd_lse_shard_bf16(xs, a, xt, b, tau) for a, b in sl]))
+    kls = [oracle.fljsd_kl_shard_bf16(xs, a, xt, b, lse, beta, tau) for a, b in sl]
+    kl = sum(kls)
+    want_mean, want_rows = oracle.fljsd_ex_bf16(xs, Ws, xt, Wt, beta, tau, keep)
+    np.testing.assert_allclose(np64(rows), want_rows, rtol=RTOL_JSD_TOKEN, atol=ATOL_JSD_TOKEN)
+    assert float(loss.item()) == pytest.approx(want_mean, rel=RTOL_SCALAR)
+    dz, gbp = oracle.fljsd_dz_bf16(xs, Ws, xt, Wt, beta, tau, keep, 2.5)
+    xsd = gen.bf16_bits_to_f32(xs).astype(np.float64)
+    Wsd = gen.bf16_bits_to_f32(Ws).astype(np.float64)
+    dx_sum, b_sum = np.zeros((T, H)), np.zeros((T, H))
+    for j, ((v0, w), (a, b)) in enumerate(zip(shards, sl)):
+        np.testing.assert_allclose(np64(tk[j, 1]), kls[j], rtol=RTOL_JSD_TOKEN, atol=ATOL_JSD_TOKEN)
+        bdx, bdW = grad_bounds(dz[:, v0:v0 + w], gbp[:, v0:v0 + w], xsd, Wsd[v0:v0 + w])
+        dx_ref, dW_ref = oracle.fljsd_grad_shard_bf16(xs, a, xt, b, lse, kl, beta, tau, keep, 2.5)
+        got_dx, got_dW = np64(outs[j][0]), np64(outs[j][1])
+        assert_within_bounds(got_dx, dx_ref, bdx, f"dxs share of shard {j}")
+        assert_within_bounds(got_dW, dW_ref, bdW, f"dWs rows of shard {j}")
+        if masked:
+            assert np.all(got_dx[keep == 0] == 0.0)
+        dx_sum += got_dx
+        b_sum += bdx
+    dx_full, _ = oracle.fljsd_grad_bf16(xs, Ws, xt, Wt, beta, tau, keep, 2.5)
+    assert_within_bounds(dx_sum, dx_full, b_sum, "sum of the dxs shares")
+
+
+@pytest.mark.parametrize("masked", [False, True])
+def test_fljsd_vp_backward_single_shard_bitwise(gpu_lib, masked):
+    """One shard holding both whole heads: the loss and the student's dxs and
+    dWs equal fljsd_fwd_bwd_bf16's bit for bit."""
+    T, H, V = 200, 256, 3000
+    xs, Ws, xt, Wt = jsd_inputs(85, T, H, V, sw=0.2)
+    d = [to_dev_bf16(a) for a in (xs, Ws, xt, Wt)]
+    keep = to_dev((np.arange(T) % 3 != 2).astype(np.uint8)) if masked else None
+    ws = gpu_lib.workspace(gpu_lib.fljsd_bwd_workspace_bytes(T, H, V))
+    ref_loss, ref_dx, ref_dW = gpu_lib.fljsd_fwd_bwd_bf16(*d, 0.4, 1.3, keep, 0.6, ws=ws)
+    _, _, _, _, loss, outs = run_fljsd_vp_bwd(gpu_lib, d, [(0, V)], 0.4, 1.3, keep, 0.6)
+    assert torch.equal(loss, ref_loss)
+    assert torch.equal(outs[0][0], ref_dx) and torch.equal(outs[0][1], ref_dW)
+
+
 # ---------------------------------------------------------------- merges alone
 def test_lse_merge_and_rows_mean(gpu_lib):
     rng = np.random.default_rng(3)
@@ -378,6 +455,10 @@ def _nccl_one_rank(port, q):
         ws2 = lmho.workspace(lmho.fljsd_workspace_bytes(T, H, V))
         ref2 = lmho.fljsd_fwd_bf16_ex(*d, 0.4, 1.5, keep, ws=ws2)
         ok_jsd = torch.equal(jrows, lmho.row_losses(ws2, T)) and torch.equal(loss, ref2)
+        l3, r3, dxs, dWs = lmdist.vocab_parallel_fljsd_fwd_bwd(*d, 0.4, 1.5, keep, 0.8)
+        ws3 = lmho.workspace(lmho.fljsd_bwd_workspace_bytes(T, H, V))
+        ref3, ref_dxs, ref_dWs = lmho.fljsd_fwd_bwd_bf16(*d, 0.4, 1.5, keep, 0.8, ws=ws3)
+        ok_jsd = ok_jsd and torch.equal(l3, ref3) and torch.equal(dxs, ref_dxs) and torch.equal(dWs, ref_dWs)
         dist.destroy_process_group()
         q.put((ok_ce, ok_jsd, None))
     except Exception as e:  # report to the parent
