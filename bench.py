@@ -690,7 +690,9 @@ def run_tp_fused(args, rank, world, local_rank):
              rows_mean; its backward flce_shard_bwd_bf16 (the rank's dx share and
              dW rows) and one all-reduce of dx;
       fljsd: fljsd_lse_partials_bf16, all-gather of [2, T], lse_merge_partials,
-             fljsd_terms_bf16, all-gather of [1, T], jsd_merge_terms.
+             fljsd_terms_bf16 with the KL shares, all-gather of [2, T], jsd_merge_terms
+             (terms and KL); the student backward fljsd_shard_bwd_bf16 and one
+             all-reduce of dxs.
     Total work is fixed as N grows ("strong").  A one-rank NCCL group is used at
     N = 1 (the collectives run there too), where the unsharded calls are timed
     beside it and their results compared."""
@@ -729,16 +731,18 @@ def run_tp_fused(args, rank, world, local_rank):
     ws_c = lmho.workspace(lmho.flce_bwd_workspace_bytes(Tc, H, w), dev)
     dx = torch.empty((Tc, H), device=dev)
     dW = torch.empty((w, H), device=dev)
-    ws_j = lmho.workspace(lmho.fljsd_workspace_bytes(Tj, H, w), dev)
+    ws_j = lmho.workspace(lmho.fljsd_bwd_workspace_bytes(Tj, H, w), dev)
+    dxs = torch.empty((Tj, H), device=dev)
+    dWs = torch.empty((w, H), device=dev)
     part = torch.empty((3, Tc), device=dev)
     g_part = torch.empty((world, 3, Tc), device=dev)
     lse_l = torch.empty((2, Tj), device=dev)
     g_lse = torch.empty((world, 2, Tj), device=dev)
-    terms = torch.empty((Tj,), device=dev)
-    g_terms = torch.empty((world, Tj), device=dev)
+    tk = torch.empty((2, Tj), device=dev)
+    g_tk = torch.empty((world, 2, Tj), device=dev)
     stream = torch.cuda.current_stream()
     names = ("flce_pass", "flce_gather", "flce_merge", "flce_bwd", "dx_allreduce", "lse_pass", "lse_gather",
-             "lse_merge", "jsd_pass", "jsd_gather", "jsd_merge")
+             "lse_merge", "jsd_pass", "jsd_gather", "jsd_merge", "jsd_bwd", "dxs_allreduce")
 
     def step(ev=None):
         def mark(i):
@@ -762,19 +766,24 @@ def run_tp_fused(args, rank, world, local_rank):
         mark(7)
         lse = lmho.lse_merge_partials(g_lse)
         mark(8)
-        lmho.fljsd_terms_bf16(xs, Ws, xt, Wt, lse, 0.5, 1.0, out=terms, ws=ws_j)
+        lmho.fljsd_terms_bf16(xs, Ws, xt, Wt, lse, 0.5, 1.0, out=tk[0], ws=ws_j, kl_local=tk[1])
         mark(9)
-        tdist.all_gather_into_tensor(g_terms, terms)
+        tdist.all_gather_into_tensor(g_tk.view(world * 2, Tj), tk)
         mark(10)
-        jsd, _ = lmho.jsd_merge_terms(g_terms)
+        jsd, _ = lmho.jsd_merge_terms(g_tk[:, 0].contiguous())
+        _, kl = lmho.jsd_merge_terms(g_tk[:, 1].contiguous())
         mark(11)
+        lmho.fljsd_shard_bwd_bf16(xs, Ws, xt, Wt, lse, kl, 0.5, 1.0, None, 1.0, dx=dxs, dW=dWs, ws=ws_j)
+        mark(12)
+        tdist.all_reduce(dxs, op=tdist.ReduceOp.SUM)
+        mark(13)
         return ce_mean, jsd
 
     for _ in range(max(1, args.warmup)):
         ce_mean, jsd = step()
     torch.cuda.synchronize()
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(14)] for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks:
         tdist.barrier()
@@ -793,7 +802,8 @@ def run_tp_fused(args, rank, world, local_rank):
     js_flops = 4 * Tj * H * w
     tf = js_flops / (ph["jsd_pass"] * 1e-3) / 1e12
     bwd_flops = 2 * fl_flops + fl_flops   # dZ recompute pass, dx and dW products
-    res = {"metric": "vocab-parallel fused linear + CE (forward and backward) and + JSD, us/step", "impl": "ours",
+    jbwd_flops = 2 * js_flops   # both heads' dZ recompute (js_flops), then the dx and dW products (js_flops / 2 each)
+    res = {"metric": "vocab-parallel fused linear + CE and + JSD, forward and backward, us/step", "impl": "ours",
            "mode": "vocab-parallel fused", "value": round(ms * 1e3, 1), "unit": "us/step", "n_gpus": world,
            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False,
            "scaling": "strong", "vs_baseline": None, "dtype": "bf16 in, f32 accumulate",
@@ -805,32 +815,34 @@ def run_tp_fused(args, rank, world, local_rank):
            "TFLOP/s": {"flce_pass": round(fl_flops / (ph["flce_pass"] * 1e-3) / 1e12, 1),
                        "flce_bwd": round(bwd_flops / (ph["flce_bwd"] * 1e-3) / 1e12, 1),
                        "lse_pass": round(js_flops / (ph["lse_pass"] * 1e-3) / 1e12, 1),
-                       "jsd_pass": round(tf, 1)},
+                       "jsd_pass": round(tf, 1),
+                       "jsd_bwd": round(jbwd_flops / (ph["jsd_bwd"] * 1e-3) / 1e12, 1)},
            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": pk["bf16_sus"],
                         "unit": "TFLOP/s", "frac": round(tf / pk["bf16_sus"], 4), "traffic": None,
                         "kernel": "fljsd_terms_bf16 tensor-core pass"},
-           "gpu_launches": 15 * K, "clocks": clocks.summary(),
+           "gpu_launches": 21 * K, "clocks": clocks.summary(),
            "flce_loss": float(ce_mean.item()), "fljsd_loss": float(jsd.item())}
     if world == 1:
         # the unsharded calls on the same inputs, timed the same way
         ws1 = lmho.workspace(lmho.flce_bwd_workspace_bytes(Tc, H, V), dev)
-        ws2 = lmho.workspace(lmho.fljsd_workspace_bytes(Tj, H, V), dev)
-        dx1 = torch.empty_like(dx)
-        dW1 = torch.empty_like(dW)
+        ws2 = lmho.workspace(lmho.fljsd_bwd_workspace_bytes(Tj, H, V), dev)
+        dx1, dW1 = torch.empty_like(dx), torch.empty_like(dW)
+        dxs1, dWs1 = torch.empty_like(dxs), torch.empty_like(dWs)
         for _ in range(2):
             a = lmho.flce_fwd_bwd_bf16(x, W, tgt, 1.0, dx=dx1, dW=dW1, ws=ws1)[0]
-            b = lmho.fljsd_fwd_bf16(xs, Ws, xt, Wt, 0.5, ws=ws2)
+            b = lmho.fljsd_fwd_bwd_bf16(xs, Ws, xt, Wt, 0.5, 1.0, None, 1.0, dxs=dxs1, dWs=dWs1, ws=ws2)[0]
         torch.cuda.synchronize()
         u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         u0.record(stream)
         for _ in range(K):
             a = lmho.flce_fwd_bwd_bf16(x, W, tgt, 1.0, dx=dx1, dW=dW1, ws=ws1)[0]
-            b = lmho.fljsd_fwd_bf16(xs, Ws, xt, Wt, 0.5, ws=ws2)
+            b = lmho.fljsd_fwd_bwd_bf16(xs, Ws, xt, Wt, 0.5, 1.0, None, 1.0, dxs=dxs1, dWs=dWs1, ws=ws2)[0]
         u1.record(stream)
         torch.cuda.synchronize()
         res["unsharded_us_per_step"] = round(u0.elapsed_time(u1) / K * 1e3, 1)
         res["bitwise_equal_to_unsharded"] = bool(torch.equal(a, ce_mean) and torch.equal(b, jsd) and
-                                                 torch.equal(dx1, dx) and torch.equal(dW1, dW))
+                                                 torch.equal(dx1, dx) and torch.equal(dW1, dW) and
+                                                 torch.equal(dxs1, dxs) and torch.equal(dWs1, dWs))
     tdist.destroy_process_group()
     return res
 
