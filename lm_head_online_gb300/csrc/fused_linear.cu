@@ -275,6 +275,30 @@ __device__ __forceinline__ void jsd_term2_x2(float& acc, uint64_t zs2, uint64_t 
   acc += t1;
 }
 
+// jsd_term2 and, from the same three MUFU results, the student's pieces the
+// KL(P || M) sum needs, in base 2: with lm2 = log2(beta 2^lp2 + (1-beta) 2^lq2)
+// = hi + lg2(s),
+//   P = 2^lp2 = 2^hi (2^-d when q is the larger side),
+//   lp2 - lm2 = -lg2(s) (- d when q is the larger side).
+// `term` takes exactly jsd_term2's steps, so the divergence keeps its bits.
+__device__ __forceinline__ void jsd_term2_student(float lp2, float lq2, float beta, float omb, float& term, float& P,
+                                                  float& lp_lm2) {
+  const float diff = __fsub_rn(lp2, lq2);
+  const float hi = fmaxf(lp2, lq2);
+  const float d = fabsf(diff);
+  const bool p_is_hi = diff >= 0.f;
+  const float w_hi = p_is_hi ? beta : omb;
+  const float w_lo = p_is_hi ? omb : beta;
+  const float e = ex2_approx(-d);
+  const float u = __fmul_rn(w_lo, e);
+  const float sv = __fadd_rn(u, w_hi);
+  const float l = lg2_approx(sv);
+  const float ph = ex2_approx(hi);
+  term = __fmul_rn(ph, fmaf(sv, l, __fmul_rn(u, d)));
+  P = p_is_hi ? ph : __fmul_rn(ph, e);
+  lp_lm2 = p_is_hi ? -l : -__fadd_rn(l, d);
+}
+
 // The pieces of one generalized-JSD pair the backward needs: P = e^{lp} and
 // lp - lm (the larger-side evaluation of jsd_term2, in natural log).
 __device__ __forceinline__ void jsd_student(float lp, float lq, float beta, float omb, float* P, float* lp_lm) {
@@ -629,11 +653,11 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               if (col0 + j < p.V) {
-                const float zs = __uint_as_float(rs[j]), zq = __uint_as_float(rt[j]);
-                float P, lplm;
-                jsd_student(fmaf(zs, it, -ls), fmaf(zq, it, -lt), beta, omb, &P, &lplm);
-                jsd += jsd_term2(fmaf(zs, it2, -ls2), fmaf(zq, it2, -lt2), beta, omb);
-                kacc = fmaf(P, lplm, kacc);
+                float t, P, lplm2;
+                jsd_term2_student(fmaf(__uint_as_float(rs[j]), it2, -ls2), fmaf(__uint_as_float(rt[j]), it2, -lt2),
+                                  beta, omb, t, P, lplm2);
+                jsd += t;
+                kacc = fmaf(P, lplm2, kacc);   // KL(P || M) share in base 2, scaled by ln 2 when written
               }
             }
           } else {  // kModeDZJ: the student's dZ for this row and 16 columns
@@ -768,7 +792,7 @@ __global__ void __launch_bounds__(ModeCfg<MODE>::kThreads, 1)
         const int64_t slot = static_cast<int64_t>(c.nt) * C::kColSplit + half;
         if (MODE == kModeJSD || MODE == kModeJSDK) {
           p.part0[slot * p.T + row] = -kLn2 * jsd;
-          if (MODE == kModeJSDK) p.part1[slot * p.T + row] = kacc;
+          if (MODE == kModeJSDK) p.part1[slot * p.T + row] = kLn2 * kacc;
         } else {
           const int64_t idx = (static_cast<int64_t>(c.head) * p.num_n * C::kColSplit + slot) * p.T + row;
           p.part0[idx] = st.m;
