@@ -86,6 +86,8 @@ def _load():
             lib.oracle_cpo_grad_bf16.restype = None
             lib.oracle_ce_partials_bf16.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp]
             lib.oracle_ce_partials_bf16.restype = None
+            lib.oracle_ce_partials_f32.argtypes = [vp, vp, i64, i64, i64, vp, vp, vp]
+            lib.oracle_ce_partials_f32.restype = None
             lib.oracle_ce_merge.argtypes = [vp, vp, vp, i64, vp, i64, i64, vp]
             lib.oracle_ce_merge.restype = None
             lib.oracle_fljsd_dz_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, dbl, dbl, vp, dbl, vp, vp]
@@ -166,6 +168,18 @@ def ce_partials_bf16(z_bits, target, v0):
     rows = t.size
     m, s, zt = (np.empty(t.shape, np.float64) for _ in range(3))
     _load().oracle_ce_partials_bf16(pz, pt, rows, Vl, int(v0), m.ctypes.data, s.ctypes.data, zt.ctypes.data)
+    return m, s, zt
+
+
+def ce_partials_f32(z, target, v0):
+    """ce_partials_bf16 for the flat layout: fp32 logits [T, Vl] holding the
+    global columns [v0, v0 + Vl), global targets [T] -> float64 (m, s, zt)."""
+    z, pz = _c(z, np.float32)
+    Vl = z.shape[-1]
+    t, pt = _c(target, np.int64)
+    assert z.shape[:-1] == t.shape
+    m, s, zt = (np.empty(t.shape, np.float64) for _ in range(3))
+    _load().oracle_ce_partials_f32(pz, pt, t.size, Vl, int(v0), m.ctypes.data, s.ctypes.data, zt.ctypes.data)
     return m, s, zt
 
 

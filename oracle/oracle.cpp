@@ -235,6 +235,25 @@ void oracle_ce_partials_bf16(const uint16_t* z16, const int64_t* target, int64_t
   }
 }
 
+// The same for the flat layout: fp32 logits [rows, Vl] of the global vocab
+// columns [v0, v0 + Vl).
+void oracle_ce_partials_f32(const float* z32, const int64_t* target, int64_t rows, int64_t Vl, int64_t v0,
+                            double* m_out, double* s_out, double* zt_out) {
+  std::vector<double> row(Vl);
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t v = 0; v < Vl; ++v) row[v] = static_cast<double>(z32[r * Vl + v]);
+    double M = row[0];
+    for (int64_t v = 1; v < Vl; ++v)
+      if (row[v] > M || std::isnan(row[v])) M = row[v];
+    double sum = 0.0;
+    for (int64_t v = 0; v < Vl; ++v) sum += std::exp(row[v] - M);
+    const int64_t tl = target[r] - v0;
+    m_out[r] = M;
+    s_out[r] = sum;
+    zt_out[r] = (tl >= 0 && tl < Vl) ? row[tl] : -std::numeric_limits<double>::infinity();
+  }
+}
+
 // Vocab-parallel CE, the combination of k shards' partials (each [k][rows],
 // shard-major) into per-row losses; V = the global vocabulary size.
 void oracle_ce_merge(const double* m, const double* s, const double* zt, int64_t k, const int64_t* target,

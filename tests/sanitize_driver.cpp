@@ -65,6 +65,8 @@ void oracle_cpo_grad_bf16(const uint16_t* x16, const uint16_t* W16, const int64_
 void oracle_logits_bf16(const uint16_t* x, const uint16_t* W, int64_t T, int64_t H, int64_t V, double* z);
 void oracle_ce_partials_bf16(const uint16_t* z16, const int64_t* target, int64_t rows, int64_t Vl, int64_t v0,
                              double* m_out, double* s_out, double* zt_out);
+void oracle_ce_partials_f32(const float* z32, const int64_t* target, int64_t rows, int64_t Vl, int64_t v0,
+                            double* m_out, double* s_out, double* zt_out);
 void oracle_ce_merge(const double* m, const double* s, const double* zt, int64_t k, const int64_t* target,
                      int64_t rows, int64_t V, double* loss);
 void oracle_fljsd_dz_bf16(const uint16_t* xs16, const uint16_t* Ws16, const uint16_t* xt16, const uint16_t* Wt16,
@@ -156,6 +158,15 @@ void run_shape(int64_t T, int64_t H, int64_t V, int threads) {
         for (int64_t v = 0; v < w1; ++v) local[i * w1 + v] = zb[i * V + v0 + v];
       oracle_ce_partials_bf16(local.data(), t.data(), T, w1, v0, m.data() + j * T, sm.data() + j * T,
                               zt.data() + j * T);
+    }
+    oracle_ce_merge(m.data(), sm.data(), zt.data(), k, t.data(), T, V, rows.data());
+    for (int64_t j = 0; j < k; ++j) {   // the flat fp32 layout
+      const int64_t v0 = V * j / k, w1 = V * (j + 1) / k - v0;
+      std::vector<float> local(T * w1);
+      for (int64_t i = 0; i < T; ++i)
+        for (int64_t v = 0; v < w1; ++v) local[i * w1 + v] = zf[i * V + v0 + v];
+      oracle_ce_partials_f32(local.data(), t.data(), T, w1, v0, m.data() + j * T, sm.data() + j * T,
+                             zt.data() + j * T);
     }
     oracle_ce_merge(m.data(), sm.data(), zt.data(), k, t.data(), T, V, rows.data());
     // the fused forms: shards of W's rows, each its own [w, H] slice of the same buffer

@@ -124,3 +124,20 @@ def test_out_of_range_target_is_nan_and_single_shard_is_plain_ce():
     np.testing.assert_allclose(loss[ok], oracle.ce_sbv_bf16(z, t)[ok], rtol=1e-13)
     # one shard: m + ln s - zt is the plain cross-entropy of the row
     np.testing.assert_allclose((m + np.log(s) - zt)[ok], oracle.ce_sbv_bf16(z, t)[ok], rtol=1e-13)
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 5])
+def test_flat_f32_shards_merge_to_unsharded(k):
+    """The flat fp32 layout's shard partials (the cross-entropy page's
+    [tokens, vocab] logits with the vocab split the same way) merge into the
+    unsharded flat oracle's per-token losses, targets on shard edges."""
+    T, V = 9, 233
+    z = gen.normal_f32(12, 0, (T, V))
+    t = gen.targets(12, 1, (T,), V)
+    shards = splits(V, k, 30 + k)
+    edge = [c for v0, w in shards for c in (v0, v0 + w - 1)]
+    t[:min(T, len(edge))] = edge[:T]
+    parts = [oracle.ce_partials_f32(np.ascontiguousarray(z[:, v0:v0 + w]), t, v0) for v0, w in shards]
+    m, s, zt = (np.stack([p[i] for p in parts]) for i in range(3))
+    _, want = oracle.ce_f32(z, t)
+    np.testing.assert_allclose(oracle.ce_merge(m, s, zt, t, V), want, rtol=1e-12, atol=1e-12)
