@@ -159,6 +159,16 @@ int ce_partials_sbv_bf16(const uint16_t* logits_local, const int64_t* target, in
 int ce_merge_partials(const float* partials, int64_t shards, const int64_t* target, int64_t S,
                       int64_t B, int64_t V, float* loss, void* stream);
 
+/* ce_partials_f32: the same shard partials for the flat fp32 layout (page
+ * "Cross-entropy loss", logits [tokens, vocab]) with the vocabulary split the
+ * same way: logits_local [T, V_local] fp32 device, the global columns
+ * [vocab_start, vocab_start + V_local); target [T] global; partials [3][T]
+ * fp32 device output as above.  Merge with ce_merge_partials(S = T, B = 1);
+ * rows_mean_f32 of the merged losses is ce_fwd_f32's mean.  One launch (the
+ * flat CE row decompositions). */
+int ce_partials_f32(const float* logits_local, const int64_t* target, int64_t T, int64_t V_local,
+                    int64_t vocab_start, float* partials, void* stream);
+
 /* ------------------------------------------------------------------------
  * Cross-entropy forward + backward: the losses and their gradient with
  * respect to the logits in one pass over HBM (logits read once, gradient

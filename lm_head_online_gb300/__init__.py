@@ -33,7 +33,7 @@ LMHO_ERR_TIMEOUT = 6
 # Every symbol declared in include/lmho.h.
 EXPORTS = (
     "lmho_strerror", "lmho_version", "ce_workspace_bytes", "ce_fwd_f32", "ce_fwd_f32_noalloc", "ce_fwd_sbv_bf16",
-    "ce_partials_sbv_bf16", "ce_merge_partials",
+    "ce_partials_sbv_bf16", "ce_partials_f32", "ce_merge_partials",
     "ce_fwd_bwd_f32", "ce_fwd_bwd_sbv_bf16",
     "flce_workspace_bytes", "flce_fwd_bf16", "flce_bwd_workspace_bytes", "flce_fwd_bwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "fljsd_bwd_workspace_bytes", "fljsd_fwd_bwd_bf16",
@@ -79,6 +79,8 @@ def load():
         lib.ce_fwd_sbv_bf16.restype = ci
         lib.ce_partials_sbv_bf16.argtypes = [vp, vp, i64, i64, i64, i64, vp, vp]
         lib.ce_partials_sbv_bf16.restype = ci
+        lib.ce_partials_f32.argtypes = [vp, vp, i64, i64, i64, vp, vp]
+        lib.ce_partials_f32.restype = ci
         lib.ce_merge_partials.argtypes = [vp, i64, vp, i64, i64, i64, vp, vp]
         lib.ce_merge_partials.restype = ci
         lib.ce_fwd_bwd_f32.argtypes = [vp, vp, i64, i64, f32, vp, vp, vp, sz, vp]
@@ -284,6 +286,27 @@ def ce_partials_sbv_bf16(logits_local, target, vocab_start, partials=None, strea
     with _on(logits_local, target, partials):
         _check(lib.ce_partials_sbv_bf16(pl, pt, S, B, Vl, int(vocab_start), _dev(partials, "partials", torch.float32, 3),
                                         _stream(stream)), "ce_partials_sbv_bf16")
+    return partials
+
+
+def ce_partials_f32(logits_local, target, vocab_start, partials=None, stream=None):
+    """One vocabulary shard of the flat fp32 cross-entropy: logits_local fp32
+    [T, V_local] = the global columns [vocab_start, vocab_start + V_local),
+    target int64 [T] global.  Returns fp32 [3, T] (max, sum of exp, target
+    logit or -inf); merge with ce_merge_partials(p.view(k, 3, T, 1), ...)."""
+    lib = load()
+    pl = _dev(logits_local, "logits_local", torch.float32, 2)
+    T, Vl = logits_local.shape
+    pt = _dev(target, "target", torch.int64, 1)
+    if target.shape[0] != T:
+        raise ValueError("target must be [T]")
+    if partials is None:
+        partials = torch.empty((3, T), dtype=torch.float32, device=logits_local.device)
+    if tuple(partials.shape) != (3, T):
+        raise ValueError("partials must be [3, T]")
+    with _on(logits_local, target, partials):
+        _check(lib.ce_partials_f32(pl, pt, T, Vl, int(vocab_start), _dev(partials, "partials", torch.float32, 2),
+                                   _stream(stream)), "ce_partials_f32")
     return partials
 
 

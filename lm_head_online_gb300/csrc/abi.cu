@@ -467,6 +467,21 @@ int ce_partials_sbv_bf16(const uint16_t* logits_local, const int64_t* target, in
                                              static_cast<cudaStream_t>(stream)));
 }
 
+int ce_partials_f32(const float* logits_local, const int64_t* target, int64_t T, int64_t V_local,
+                    int64_t vocab_start, float* partials, void* stream) {
+  if (!logits_local || !target || !partials) return LMHO_ERR_INVALID_ARG;
+  if (T <= 0 || V_local <= 0 || vocab_start < 0) return LMHO_ERR_INVALID_ARG;
+  if (T > (int64_t(1) << 31) - 1 || vocab_start > (int64_t(1) << 62)) return LMHO_ERR_INVALID_ARG;
+  const Range in[2] = {rng(logits_local, 4 * static_cast<size_t>(T) * V_local), rng(target, 8 * static_cast<size_t>(T))};
+  const Range out[1] = {rng(partials, 12 * static_cast<size_t>(T))};
+  if (int a = check_alias(in, 2, out, 1)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  const CeConfig cfg = choose_ce(logits_local, T, V_local, 4, sms);
+  return cuda_status(launch_ce_partials_f32(logits_local, target, T, V_local, vocab_start, partials, cfg,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 int ce_merge_partials(const float* partials, int64_t shards, const int64_t* target, int64_t S, int64_t B, int64_t V,
                       float* loss, void* stream) {
   if (!partials || !target || !loss) return LMHO_ERR_INVALID_ARG;

@@ -486,6 +486,12 @@ cudaError_t launch_ce_partials_bf16(const uint16_t* logits, const int64_t* targe
   return launch_rows<uint16_t>(logits, target, rows, V_local, sink, nullptr, nullptr, nullptr, cfg, st);
 }
 
+cudaError_t launch_ce_partials_f32(const float* logits, const int64_t* target, int64_t rows, int64_t V_local,
+                                   int64_t v0, float* partials, const CeConfig& cfg, cudaStream_t st) {
+  const PartialSink sink{partials, partials + rows, partials + 2 * rows, v0};
+  return launch_rows<float>(logits, target, rows, V_local, sink, nullptr, nullptr, nullptr, cfg, st);
+}
+
 cudaError_t launch_probe_read(const void* data, int64_t nseg, int64_t seg_bytes, uint32_t* out, cudaStream_t st) {
   launch_mark(0, st);
   const unsigned nb = static_cast<unsigned>((nseg + 1) / 2);

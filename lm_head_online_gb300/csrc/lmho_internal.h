@@ -58,6 +58,9 @@ cudaError_t launch_ce_bf16_rows(const uint16_t* logits, const int64_t* target, i
 // `shards` such blocks ([shards][3][rows]) into per-row losses.
 cudaError_t launch_ce_partials_bf16(const uint16_t* logits, const int64_t* target, int64_t rows, int64_t V_local,
                                     int64_t v0, float* partials, const CeConfig& cfg, cudaStream_t st);
+// The same for fp32 logits [rows, V_local] (the flat layout).
+cudaError_t launch_ce_partials_f32(const float* logits, const int64_t* target, int64_t rows, int64_t V_local,
+                                   int64_t v0, float* partials, const CeConfig& cfg, cudaStream_t st);
 cudaError_t launch_ce_merge(const float* partials, int64_t shards, const int64_t* target, int64_t rows, int64_t V,
                             float* loss, int num_sms, cudaStream_t st);
 

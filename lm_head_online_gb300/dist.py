@@ -168,3 +168,17 @@ def vocab_parallel_fljsd_fwd_bwd(xs, Ws_local, xt, Wt_local, beta=0.5, temperatu
     dx, dW = fljsd_shard_bwd_bf16(xs, Ws_local, xt, Wt_local, lse, kl, beta, temperature, keep, grad_scale, ws=ws)
     dist.all_reduce(dx, op=dist.ReduceOp.SUM, group=group)
     return loss, rows, dx, dW
+
+
+def vocab_parallel_ce_f32(logits_local, target, vocab_start: int, V: int, group=None):
+    """Flat fp32 cross-entropy with the vocabulary sharded over the ranks of
+    `group`: this rank holds logits_local [T, V_local] = the global columns
+    [vocab_start, vocab_start + V_local); target [T] global on every rank.
+    Returns (mean loss [1], per-token losses [T]), the same on every rank."""
+    from lm_head_online_gb300 import ce_merge_partials, ce_partials_f32, rows_mean
+
+    T = target.shape[0]
+    part = ce_partials_f32(logits_local, target, vocab_start)             # [3, T]
+    allp = gather_partials(part, group)                                    # [world, 3, T]
+    rows = ce_merge_partials(allp.view(allp.shape[0], 3, T, 1), target.view(T, 1), V).view(T)
+    return rows_mean(rows), rows

@@ -196,6 +196,11 @@ def test_vocab_parallel_argument_checks(lib):
     assert lib.ce_partials_sbv_bf16(A, B, 2, 2, 8, -1, C, None) == 1            # negative vocab start
     assert lib.ce_partials_sbv_bf16(A, B, 2, 2, 8, 16, A + 8, None) == 2        # partials over logits
     assert lib.ce_partials_sbv_bf16(A, B, 2, 2, 8, 16, B + 24, None) == 2       # partials over target
+    # ce_partials_f32(logits_local, target, T, V_local, vocab_start, partials, stream)
+    assert lib.ce_partials_f32(None, B, 4, 8, 0, C, None) == 1
+    assert lib.ce_partials_f32(A, B, 0, 8, 0, C, None) == 1
+    assert lib.ce_partials_f32(A, B, 4, 8, -1, C, None) == 1
+    assert lib.ce_partials_f32(A, B, 4, 8, 0, A + 64, None) == 2                # partials over logits
     # ce_merge_partials(partials, shards, target, S, B, V, loss, stream)
     assert lib.ce_merge_partials(None, 2, B, 2, 2, 16, C, None) == 1
     assert lib.ce_merge_partials(A, 0, B, 2, 2, 16, C, None) == 1               # no shard

@@ -249,3 +249,21 @@ def test_vocab_parallel_fljsd_backward_exchanges_over_gloo_ranks(world):
     for dx, dW, (v0, w) in out.values():
         np.testing.assert_allclose(dx, dx_want, rtol=1e-10, atol=1e-15)
         np.testing.assert_allclose(dW, dW_want[v0:v0 + w], rtol=1e-10, atol=1e-15)
+
+
+def _vp_flat(rank, world):
+    T, V = 7, 301
+    z = gen.normal_f32(10, 0, (T, V))
+    t = gen.targets(10, 1, (T,), V)
+    v0, w = lmdist.shard_vocab(V, rank, world)
+    m, s, zt = oracle.ce_partials_f32(np.ascontiguousarray(z[:, v0:v0 + w]), t, v0)
+    g = lmdist.gather_partials(torch.from_numpy(np.stack([m, s, zt]))).numpy()
+    return oracle.ce_merge(g[:, 0], g[:, 1], g[:, 2], t, V)
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_vocab_parallel_flat_exchange_over_gloo_ranks(world):
+    out = spawn(_vp_flat, world=world)
+    _, want = oracle.ce_f32(gen.normal_f32(10, 0, (7, 301)), gen.targets(10, 1, (7,), 301))
+    for loss in out.values():
+        np.testing.assert_allclose(loss, want, rtol=1e-12, atol=1e-12)

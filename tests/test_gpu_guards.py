@@ -280,6 +280,21 @@ def test_vocab_parallel_fused_guards(gpu_lib, T, H, V):
     unchanged(before, [x, xt, W, Wt, t, keep])
 
 
+def test_flat_f32_vocab_parallel_guards(gpu_lib):
+    g = Guarded()
+    T, V = 37, 1001
+    z = to_dev(gen.normal_f32(27, 0, (T, V)))
+    t = to_dev(gen.targets(27, 1, (T,), V))
+    before = snapshot(z, t)
+    shards = [(0, 333), (333, V - 333)]
+    parts = g.view(2 * 3 * T * 4, torch.float32, (2, 3, T))
+    for j, (v0, w) in enumerate(shards):
+        gpu_lib.ce_partials_f32(z[:, v0:v0 + w].contiguous(), t, v0, partials=parts[j])
+    g.check()
+    unchanged(before, [z, t])
+    assert not bool(torch.isnan(parts).any()), "a partial was never written"
+
+
 def test_probe_read_guards(gpu_lib):
     g = Guarded()
     words = gen.targets(25, 0, (5 * 4096,), 2 ** 32).astype(np.uint32)

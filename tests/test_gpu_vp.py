@@ -162,3 +162,53 @@ def test_full_size_eight_shards_sampled(gpu_lib):
     rows = rows_bf16(0, 0, idx, V, sigma=2.0)
     ref = oracle.ce_sbv_bf16(rows.reshape(-1, 1, V), t.reshape(-1)[idx].reshape(-1, 1)).reshape(-1)
     np.testing.assert_allclose(loss.cpu().numpy().reshape(-1)[idx], ref, rtol=0, atol=ATOL_BF16)
+
+
+# ---------------------------------------------------------------- the flat fp32 layout
+def run_vp_f32(lmho, zd, td, shards, V):
+    """zd: device fp32 [T, V]; each shard copied to its own buffer; returns
+    (partials [k, 3, T], per-token losses [T], mean [1])."""
+    T = zd.shape[0]
+    parts = torch.full((len(shards), 3, T), float("nan"), device="cuda")
+    for j, (v0, w) in enumerate(shards):
+        lmho.ce_partials_f32(zd[:, v0:v0 + w].contiguous(), td, v0, partials=parts[j])
+    rows = lmho.ce_merge_partials(parts.view(len(shards), 3, T, 1), td.view(T, 1), V).view(T)
+    mean = lmho.rows_mean(rows)
+    torch.cuda.synchronize()
+    return parts, rows, mean
+
+
+@pytest.mark.parametrize("variant", ["auto", "warp", "cta", "cta512", "cluster2", "cluster8", "bulk"])
+@pytest.mark.parametrize("T,V,k", [(37, 1001, 3), (130, 4099, 2), (5, 40000, 4)])
+def test_flat_f32_vocab_parallel_matches_oracle(gpu_lib, variant, T, V, k):
+    """Flat fp32 logits (page "Cross-entropy loss") with the vocabulary split:
+    partial maxima and target logits exact (fp32 values), partial sums rel
+    1e-5, per-token losses and the mean rel 1e-5 of the oracle (the flat bar);
+    targets on the first and last column of every shard."""
+    gpu_lib.set_ce_variant(variant)
+    z = gen.normal_f32(16, 0, (T, V))
+    t = gen.targets(16, 1, (T,), V)
+    shards = uneven_shards(V, k, seed=T + k)
+    edges = [c for v0, w in shards for c in (v0, v0 + w - 1)]
+    t[:min(T, len(edges))] = edges[:T]
+    parts, rows, mean = run_vp_f32(gpu_lib, to_dev(z), to_dev(t), shards, V)
+    got = parts.cpu().numpy().astype(np.float64)
+    for j, (v0, w) in enumerate(shards):
+        m, s, zt = oracle.ce_partials_f32(np.ascontiguousarray(z[:, v0:v0 + w]), t, v0)
+        np.testing.assert_array_equal(got[j, 0], m)
+        np.testing.assert_allclose(got[j, 1], s, rtol=RTOL_SUM)
+        np.testing.assert_array_equal(got[j, 2], zt)
+    want_mean, want = oracle.ce_f32(z, t)
+    np.testing.assert_allclose(rows.cpu().numpy().astype(np.float64), want, rtol=1e-5, atol=1e-6)
+    assert float(mean.item()) == pytest.approx(want_mean, rel=1e-5)
+
+
+def test_flat_f32_one_shard_is_ce_fwd_f32_bitwise(gpu_lib):
+    T, V = 300, 4096
+    z = gen.normal_f32(17, 0, (T, V))
+    t = gen.targets(17, 1, (T,), V)
+    zd, td = to_dev(z), to_dev(t)
+    ws = gpu_lib.workspace(gpu_lib.ce_workspace_bytes(T, V))
+    ref = gpu_lib.ce_fwd_f32(zd, td, ws=ws)
+    _, rows, mean = run_vp_f32(gpu_lib, zd, td, [(0, V)], V)
+    assert torch.equal(rows, gpu_lib.row_losses(ws, T)) and torch.equal(mean, ref)
