@@ -270,6 +270,38 @@ def time_back_to_back(fns, torch, warmup, steps):
     return e0.elapsed_time(e1) * 1e3 / steps
 
 
+def time_graph(fns, torch, steps, replays=3):
+    """Per-call time of the same back-to-back sequence captured once into a
+    CUDA graph (after an eager warm-up of every call on the capture stream's
+    side) and replayed: median over `replays` replays of one event pair around
+    the replay, graph launch included.  Inside a graph the next kernel is
+    already staged when the previous one completes, so the gap between calls
+    shrinks; the calls and their results are the same."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for f in fns:
+            f()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(steps):
+            fns[i % len(fns)]()
+    g.replay()
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1) * 1e3 / steps)
+    del g
+    return float(np.median(per))
+
+
 def run_small_ce_only(args):
     import torch
     import lm_head_online_gb300 as lmho
@@ -282,11 +314,12 @@ def run_small_ce_only(args):
 
 
 def small_ce(lmho, torch, dev, seed, pk, steps=50):
-    """The smallest CE workloads, each timed alone two ways (see above).
-    The roofline uses the back-to-back time; the flushed per-call time, which
-    adds a fixed event and launch cost of about 3 us, is reported beside it,
-    and so is the back-to-back time of a bare read of the same bytes with the
-    same loads (lmho_probe_read): the floor at that size."""
+    """The smallest CE workloads, each timed alone (see above): back to back
+    on the stream (the roofline's time), the same calls replayed from one CUDA
+    graph (a second roofline entry, "<op>.graph"), and one flushed call at a
+    time, which adds a fixed event and launch cost of about 3 us; beside them
+    the back-to-back time of a bare read of the same bytes with the same loads
+    (lmho_probe_read): the stream floor at that size."""
     import gen
     thr = os.cpu_count() or 1
     flush = torch.ones(128 << 20, dtype=torch.float32, device=dev)
@@ -310,6 +343,7 @@ def small_ce(lmho, torch, dev, seed, pk, steps=50):
             fns = [lambda zz=zz: lmho.ce_fwd_sbv_bf16(zz, t, loss=loss) for zz in copies]
             nbytes, key, shape = rl.ce_sbv_bytes(T, 4, V), f"ce_fwd_sbv_bf16.S{T}_B4_V{V}", f"bf16[{T},4,{V}]"
         b2b = time_back_to_back(fns, torch, 5, steps)
+        gr = time_graph(fns, torch, steps)
         fl = time_flushed(fns, torch, 5, steps, flush)
         # the bare read of the same bytes with the same loads (nothing computed)
         seg = z.shape[-1] * z.element_size()
@@ -320,6 +354,7 @@ def small_ce(lmho, torch, dev, seed, pk, steps=50):
         gbs = nbytes / (b2b * 1e-6) / 1e9
         ops[key] = {"shape": shape, "bytes": nbytes, "copies": len(fns),
                     "us_back_to_back": round(b2b, 2), "GB/s_back_to_back": round(gbs, 1),
+                    "us_graph": round(gr, 2), "GB/s_graph": round(nbytes / (gr * 1e-6) / 1e9, 1),
                     "us_bare_read_back_to_back": round(floor, 2),
                     "frac_of_bare_read": round(floor / b2b, 4),
                     "us_flushed_median": round(med, 2), "us_flushed_p10": round(float(np.percentile(fl, 10)), 2),
@@ -328,9 +363,14 @@ def small_ce(lmho, torch, dev, seed, pk, steps=50):
         roofs[key] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                       "frac": round(gbs / pk["hbm"], 4), "traffic": None,
                       "timing": f"back to back over {len(fns)} copies (> 3x L2), mean per call"}
+        gg = nbytes / (gr * 1e-6) / 1e9
+        roofs[key + ".graph"] = {"bound": "hbm", "achieved": round(gg, 1), "peak": pk["hbm"], "unit": "GB/s",
+                                 "frac": round(gg / pk["hbm"], 4), "traffic": None,
+                                 "timing": f"the same {steps} calls captured in one CUDA graph, median of 3 replays "
+                                           f"(graph launch included), mean per call"}
         del fns, reads, copies, z
         torch.cuda.empty_cache()
-    return ops, roofs, 2 * steps * sum(2 if n == "ce_fwd_f32" else 1 for n, _, _ in SMALL_CE)
+    return ops, roofs, (2 + 3) * steps * sum(2 if n == "ce_fwd_f32" else 1 for n, _, _ in SMALL_CE)
 
 
 # ---------------------------------------------------------------- our arm
