@@ -390,7 +390,7 @@ const char* lmho_strerror(int status) {
   }
 }
 
-int lmho_version(void) { return 100; }
+int lmho_version(void) { return 200; }
 
 void lmho_set_launch_events(void* const* events, int n) {
   t_nevents = 0;

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_strerror_and_version(lib):
     import lm_head_online_gb300 as lmho
-    assert lib.lmho_version() >= 100
+    assert lib.lmho_version() >= 200
     for code in range(0, 8):
         assert isinstance(lmho.strerror(code), str) and lmho.strerror(code)
 
