@@ -387,7 +387,8 @@ int flce_partials_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t
  *   dW_local [V_local, H] fp32 = dZ_shard^T x: this rank's rows of dW.
  *   partials  [shards][3][T] fp32 device: every shard's flce_partials_bf16
  *             output in shard order (the forward's all-gather);
- *   V         the global vocabulary size: a target outside [0, V) makes that
+ *   V         the global vocabulary size (vocab_start + V_local <= V, else
+ *             LMHO_ERR_INVALID_ARG): a target outside [0, V) makes that
  *             token's dZ row, and so dx's row and every dW entry, NaN;
  *   dx_partial, dW_local 16-byte aligned; ws_bytes >=
  *   flce_bwd_workspace_bytes(T, H, V_local), zeroed before first use.
