@@ -399,6 +399,33 @@ int flce_shard_bwd_bf16(const uint16_t* x, const uint16_t* W_local, const int64_
                         const float* partials, int64_t shards, int64_t T, int64_t H, int64_t V_local,
                         int64_t vocab_start, int64_t V, float grad_scale, float* dx_partial,
                         float* dW_local, void* ws, size_t ws_bytes, void* stream);
+
+/* flce_shard_bwd_rows_bf16: flce_shard_bwd_bf16 with a weight per token in
+ * place of the mean's 1/T: dZ_shard row i = grad_scale * row_w[i] *
+ * (softmax - onehot) over the shard's columns.  row_w [T] fp32 device (not
+ * NULL), e.g. the CPO weights below.  Other arguments, workspace and launches
+ * as flce_shard_bwd_bf16.
+ *
+ * cpo_combine_rows: the CPO objective (page "Fused linear + CPO loss"; the
+ * published Contrastive Preference Optimization form, as flce_cpo_fwd_bf16)
+ * of given per-token CE losses, e.g. the merged losses of the vocab-parallel
+ * fused CE: rows [B * S] fp32 device, sequence b < B/2 chosen, b + B/2 its
+ * rejected answer (B even >= 2); beta > 0, alpha >= 0 finite.
+ *   loss  [1] fp32 device: alpha * (chosen NLL token mean) + mean softplus(-beta d_k);
+ *   logps [B] fp32 device or NULL: each sequence's log-likelihood -sum_s rows;
+ *   row_w [B * S] fp32 device or NULL: d loss / d rows_i, the weights of
+ *         flce_shard_bwd_rows_bf16 for the CPO backward;
+ *   ws    ws_bytes >= cpo_combine_workspace_bytes(B), 256-byte aligned, zeroed
+ *         before first use.  One launch (a block per sequence, the last to
+ *         finish combines the pairs in order). */
+int flce_shard_bwd_rows_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t* target,
+                             const float* partials, int64_t shards, int64_t T, int64_t H,
+                             int64_t V_local, int64_t vocab_start, int64_t V, const float* row_w,
+                             float grad_scale, float* dx_partial, float* dW_local, void* ws,
+                             size_t ws_bytes, void* stream);
+size_t cpo_combine_workspace_bytes(int64_t B);
+int cpo_combine_rows(const float* rows, int64_t B, int64_t S, float beta, float alpha, float* loss,
+                     float* logps, float* row_w, void* ws, size_t ws_bytes, void* stream);
 int fljsd_lse_partials_bf16(const uint16_t* xs, const uint16_t* Ws_local, const uint16_t* xt,
                             const uint16_t* Wt_local, int64_t T, int64_t H, int64_t V_local,
                             float temperature, float* lse_local, void* ws, size_t ws_bytes,
@@ -502,8 +529,9 @@ int lmho_set_raster_group(int group_m);
  * flce_fwd_bf16 2 (tensor-core pass, finaliser), fljsd_fwd_bf16 4
  * (log-sum-exp pass, finaliser, divergence pass, finaliser),
  * flce_partials_bf16, fljsd_lse_partials_bf16 and fljsd_terms_bf16 2 each
- * (tensor-core pass, finaliser), flce_shard_bwd_bf16 3 (normaliser merge and
- * dZ pass, dx share, dW rows), fljsd_shard_bwd_bf16 3 (count and dZ pass, dxs
+ * (tensor-core pass, finaliser), flce_shard_bwd_bf16 and
+ * flce_shard_bwd_rows_bf16 3 (normaliser merge and dZ pass, dx share, dW
+ * rows), cpo_combine_rows 1, fljsd_shard_bwd_bf16 3 (count and dZ pass, dxs
  * share, dWs rows), lse_merge_partials 1, jsd_merge_terms 1
  * (the merge and its dependent mean together), rows_mean_f32 1.  Calls made by
  * other threads are not affected.  Pass (NULL, 0) to turn it off. */

@@ -38,7 +38,8 @@ EXPORTS = (
     "flce_workspace_bytes", "flce_fwd_bf16", "flce_bwd_workspace_bytes", "flce_fwd_bwd_bf16", "fljsd_workspace_bytes", "fljsd_fwd_bf16", "fljsd_fwd_bf16_ex",
     "fljsd_bwd_workspace_bytes", "fljsd_fwd_bwd_bf16",
     "flce_cpo_workspace_bytes", "flce_cpo_fwd_bf16", "flce_cpo_bwd_workspace_bytes", "flce_cpo_fwd_bwd_bf16",
-    "flce_partials_bf16", "flce_shard_bwd_bf16", "fljsd_lse_partials_bf16", "lse_merge_partials", "fljsd_terms_bf16", "fljsd_shard_bwd_bf16", "jsd_merge_terms",
+    "flce_partials_bf16", "flce_shard_bwd_bf16", "flce_shard_bwd_rows_bf16", "cpo_combine_workspace_bytes",
+    "cpo_combine_rows", "fljsd_lse_partials_bf16", "lse_merge_partials", "fljsd_terms_bf16", "fljsd_shard_bwd_bf16", "jsd_merge_terms",
     "rows_mean_f32",
     "lmho_ws_status", "lmho_probe_read", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
@@ -118,6 +119,13 @@ def load():
         lib.flce_partials_bf16.restype = ci
         lib.flce_shard_bwd_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp, vp, vp, sz, vp]
         lib.flce_shard_bwd_bf16.restype = ci
+        lib.flce_shard_bwd_rows_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, vp, f32, vp, vp, vp,
+                                                 sz, vp]
+        lib.flce_shard_bwd_rows_bf16.restype = ci
+        lib.cpo_combine_workspace_bytes.argtypes = [i64]
+        lib.cpo_combine_workspace_bytes.restype = sz
+        lib.cpo_combine_rows.argtypes = [vp, i64, i64, f32, f32, vp, vp, vp, vp, sz, vp]
+        lib.cpo_combine_rows.restype = ci
         lib.fljsd_lse_partials_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, vp, vp, sz, vp]
         lib.fljsd_lse_partials_bf16.restype = ci
         lib.lse_merge_partials.argtypes = [vp, i64, i64, vp, vp]
@@ -658,12 +666,14 @@ def flce_partials_bf16(x, W_local, target, vocab_start, partials=None, ws=None, 
 
 
 def flce_shard_bwd_bf16(x, W_local, target, partials, vocab_start, V, grad_scale=1.0, dx=None, dW=None, ws=None,
-                        stream=None):
+                        stream=None, row_w=None):
     """Backward of one shard of the vocab-parallel fused linear + CE:
     gradients of grad_scale * mean loss.  partials: fp32 [shards, 3, T], every
     shard's flce_partials_bf16 output in shard order; V the global vocabulary.
     Returns (dx_partial fp32 [T, H], this rank's share of dx -- the ranks'
-    shares sum to dx --, dW_local fp32 [V_local, H], this rank's rows of dW)."""
+    shares sum to dx --, dW_local fp32 [V_local, H], this rank's rows of dW).
+    row_w (fp32 [T], optional): a weight per token in place of the mean's 1/T
+    (flce_shard_bwd_rows_bf16), e.g. cpo_combine_rows' weights."""
     lib = load()
     px = _dev(x, "x", torch.bfloat16, 2)
     pw = _dev(W_local, "W_local", torch.bfloat16, 2)
@@ -682,11 +692,52 @@ def flce_shard_bwd_bf16(x, W_local, target, partials, vocab_start, V, grad_scale
         raise ValueError("dx must be [T, H] and dW [V_local, H]")
     if ws is None:
         ws = workspace(lib.flce_bwd_workspace_bytes(T, H, Vl), x.device)
-    with _on(x, W_local, target, partials, dx, dW, ws):
-        _check(lib.flce_shard_bwd_bf16(px, pw, pt, pp, k, T, H, Vl, int(vocab_start), int(V), float(grad_scale),
-                                       _dev(dx, "dx", torch.float32, 2), _dev(dW, "dW", torch.float32, 2),
-                                       _dev(ws, "ws", torch.uint8), ws.numel(), _stream(stream)), "flce_shard_bwd_bf16")
+    with _on(x, W_local, target, partials, dx, dW, ws, row_w):
+        pdx, pdw, pws = _dev(dx, "dx", torch.float32, 2), _dev(dW, "dW", torch.float32, 2), _dev(ws, "ws", torch.uint8)
+        if row_w is None:
+            _check(lib.flce_shard_bwd_bf16(px, pw, pt, pp, k, T, H, Vl, int(vocab_start), int(V), float(grad_scale),
+                                           pdx, pdw, pws, ws.numel(), _stream(stream)), "flce_shard_bwd_bf16")
+        else:
+            pr = _dev(row_w, "row_w", torch.float32, 1)
+            if row_w.shape[0] != T:
+                raise ValueError("row_w must be [T]")
+            _check(lib.flce_shard_bwd_rows_bf16(px, pw, pt, pp, k, T, H, Vl, int(vocab_start), int(V), pr,
+                                                float(grad_scale), pdx, pdw, pws, ws.numel(), _stream(stream)),
+                   "flce_shard_bwd_rows_bf16")
     return dx, dW
+
+
+def cpo_combine_workspace_bytes(B: int) -> int:
+    return int(load().cpo_combine_workspace_bytes(B))
+
+
+def cpo_combine_rows(rows, B, beta=0.1, alpha=1.0, loss=None, logps=None, row_w=None, ws=None, stream=None):
+    """The CPO objective of per-token CE losses rows fp32 [B * S] (sequence
+    b < B/2 chosen, b + B/2 its rejected answer): returns (loss [1], logps
+    [B]); row_w (fp32 [B * S], optional) receives d loss / d rows, the weights
+    of the CPO backward (flce_shard_bwd_bf16(..., row_w=row_w))."""
+    lib = load()
+    pr = _dev(rows, "rows", torch.float32, 1)
+    n = rows.shape[0]
+    if B < 2 or n % B != 0:
+        raise ValueError("rows must hold B sequences of equal length")
+    S = n // B
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=rows.device)
+    if logps is None:
+        logps = torch.empty(B, dtype=torch.float32, device=rows.device)
+    pw = None
+    if row_w is not None:
+        pw = _dev(row_w, "row_w", torch.float32, 1)
+        if row_w.shape[0] != n:
+            raise ValueError("row_w must be [B * S]")
+    if ws is None:
+        ws = workspace(lib.cpo_combine_workspace_bytes(B), rows.device)
+    with _on(rows, loss, logps, ws, row_w):
+        _check(lib.cpo_combine_rows(pr, B, S, float(beta), float(alpha), _dev(loss, "loss", torch.float32),
+                                    _dev(logps, "logps", torch.float32, 1), pw, _dev(ws, "ws", torch.uint8),
+                                    ws.numel(), _stream(stream)), "cpo_combine_rows")
+    return loss, logps
 
 
 def fljsd_lse_partials_bf16(xs, Ws_local, xt, Wt_local, temperature=1.0, out=None, ws=None, stream=None):

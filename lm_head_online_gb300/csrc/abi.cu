@@ -660,10 +660,11 @@ int flce_partials_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t
   return cuda_status(launch_flce_partials(tx, tw, target, vocab_start, g, partials, w, L));
 }
 
-int flce_shard_bwd_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t* target, const float* partials,
+namespace {
+int flce_shard_bwd_impl(const uint16_t* x, const uint16_t* W_local, const int64_t* target, const float* partials,
                         int64_t shards, int64_t T, int64_t H, int64_t V_local, int64_t vocab_start, int64_t V,
-                        float grad_scale, float* dx_partial, float* dW_local, void* ws, size_t ws_bytes,
-                        void* stream) {
+                        const float* row_w, float grad_scale, float* dx_partial, float* dW_local, void* ws,
+                        size_t ws_bytes, void* stream) {
   if (!x || !W_local || !target || !partials || !dx_partial || !dW_local || !ws) return LMHO_ERR_INVALID_ARG;
   if (int c = check_fused_common(T, H, V_local)) return c;
   if (shards <= 0 || shards > (int64_t(1) << 20) || V > (int64_t(1) << 31) || vocab_start < 0 || V < V_local ||
@@ -673,12 +674,13 @@ int flce_shard_bwd_bf16(const uint16_t* x, const uint16_t* W_local, const int64_
   if (!aligned16(x) || !aligned16(W_local) || !aligned16(dx_partial) || !aligned16(dW_local))
     return LMHO_ERR_INVALID_ARG;
   if (ws_bytes < flce_bwd_ws_bytes(T, H, V_local) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
-  const Range in[4] = {rng(x, 2 * static_cast<size_t>(T) * H), rng(W_local, 2 * static_cast<size_t>(V_local) * H),
+  const Range in[5] = {rng(x, 2 * static_cast<size_t>(T) * H), rng(W_local, 2 * static_cast<size_t>(V_local) * H),
                        rng(target, 8 * static_cast<size_t>(T)),
-                       rng(partials, 12 * static_cast<size_t>(T) * static_cast<size_t>(shards))};
+                       rng(partials, 12 * static_cast<size_t>(T) * static_cast<size_t>(shards)),
+                       rng(row_w, row_w ? 4 * static_cast<size_t>(T) : 0)};
   const Range out[3] = {rng(dx_partial, 4 * static_cast<size_t>(T) * H),
                         rng(dW_local, 4 * static_cast<size_t>(V_local) * H), rng(ws, ws_bytes)};
-  if (int a = check_alias(in, 4, out, 3)) return a;
+  if (int a = check_alias(in, 5, out, 3)) return a;
   int sms = 0;
   if (int d = current_device(&sms)) return d;
   if (int e = get_encode()) return e;
@@ -691,8 +693,51 @@ int flce_shard_bwd_bf16(const uint16_t* x, const uint16_t* W_local, const int64_
     return LMHO_ERR_CUDA;
   const FusedGeometry g = geometry(T, H, V_local, kBN_CE);
   const FusedLaunch L{sms, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)};
-  return cuda_status(launch_flce_shard_bwd(m, target, partials, shards, vocab_start, V, g, grad_scale, dx_partial,
-                                           dW_local, w, bw, L));
+  return cuda_status(launch_flce_shard_bwd(m, target, partials, shards, vocab_start, V, g, grad_scale, row_w,
+                                           dx_partial, dW_local, w, bw, L));
+}
+}  // namespace
+
+int flce_shard_bwd_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t* target, const float* partials,
+                        int64_t shards, int64_t T, int64_t H, int64_t V_local, int64_t vocab_start, int64_t V,
+                        float grad_scale, float* dx_partial, float* dW_local, void* ws, size_t ws_bytes,
+                        void* stream) {
+  return flce_shard_bwd_impl(x, W_local, target, partials, shards, T, H, V_local, vocab_start, V, nullptr,
+                             grad_scale, dx_partial, dW_local, ws, ws_bytes, stream);
+}
+
+int flce_shard_bwd_rows_bf16(const uint16_t* x, const uint16_t* W_local, const int64_t* target, const float* partials,
+                             int64_t shards, int64_t T, int64_t H, int64_t V_local, int64_t vocab_start, int64_t V,
+                             const float* row_w, float grad_scale, float* dx_partial, float* dW_local, void* ws,
+                             size_t ws_bytes, void* stream) {
+  if (!row_w) return LMHO_ERR_INVALID_ARG;
+  return flce_shard_bwd_impl(x, W_local, target, partials, shards, T, H, V_local, vocab_start, V, row_w,
+                             grad_scale, dx_partial, dW_local, ws, ws_bytes, stream);
+}
+
+size_t cpo_combine_workspace_bytes(int64_t B) {
+  if (B <= 0) return kAlign;
+  return 2 * align_up(4 * static_cast<size_t>(B)) + kAlign;
+}
+
+int cpo_combine_rows(const float* rows, int64_t B, int64_t S, float beta, float alpha, float* loss, float* logps,
+                     float* row_w, void* ws, size_t ws_bytes, void* stream) {
+  if (!rows || !loss || !ws) return LMHO_ERR_INVALID_ARG;
+  if (B < 2 || B % 2 != 0 || S <= 0 || B > (int64_t(1) << 24) || B > ((int64_t(1) << 31) - 1) / S)
+    return LMHO_ERR_INVALID_ARG;
+  if (!(beta > 0.f) || !std::isfinite(beta) || !(alpha >= 0.f) || !std::isfinite(alpha)) return LMHO_ERR_INVALID_ARG;
+  if (ws_bytes < cpo_combine_workspace_bytes(B) || !aligned256(ws)) return LMHO_ERR_WORKSPACE;
+  const size_t T = static_cast<size_t>(B * S);
+  const Range in[1] = {rng(rows, 4 * T)};
+  const Range out[4] = {rng(loss, 4), rng(logps, logps ? 4 * static_cast<size_t>(B) : 0),
+                        rng(row_w, row_w ? 4 * T : 0), rng(ws, ws_bytes)};
+  if (int a = check_alias(in, 1, out, 4)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  float* lp = static_cast<float*>(ws);
+  float* sig = reinterpret_cast<float*>(static_cast<char*>(ws) + align_up(4 * static_cast<size_t>(B)));
+  return cuda_status(launch_cpo_combine(rows, B, S, beta, alpha, loss, logps, row_w, lp, sig, ctrl_of(ws, ws_bytes),
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 namespace {

@@ -1229,6 +1229,14 @@ cudaError_t launch_fljsd_terms_shard(const CUtensorMap& tm_xs, const CUtensorMap
   return cudaGetLastError();
 }
 
+cudaError_t launch_cpo_combine(const float* rows, int64_t B, int64_t S, float beta, float alpha, float* loss,
+                               float* logps, float* row_w, float* lp, float* sig, Ctrl* ctrl, cudaStream_t st) {
+  launch_mark(0, st);
+  cpo_finalize<<<static_cast<unsigned>(B), 256, 0, st>>>(rows, B, S, beta, alpha, lp, sig, loss, logps, row_w, ctrl);
+  launch_mark(1, st);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_flce_cpo(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const int64_t* target,
                             const FusedGeometry& g, float* loss, const FusedWs& ws, const CpoArgs& c,
                             const FusedLaunch& L) {
@@ -1365,8 +1373,8 @@ cudaError_t launch_flce_fwd_bwd(const FlceBwdMaps& m, const int64_t* target, con
 
 cudaError_t launch_flce_shard_bwd(const FlceBwdMaps& m, const int64_t* target, const float* partials,
                                   int64_t shards, int64_t v0, int64_t v_total, const FusedGeometry& g,
-                                  float grad_scale, float* dx, float* dW, const FusedWs& ws, const FlceBwdWs& bw,
-                                  const FusedLaunch& L) {
+                                  float grad_scale, const float* row_w, float* dx, float* dW, const FusedWs& ws,
+                                  const FlceBwdWs& bw, const FusedLaunch& L) {
   cudaError_t e;
   launch_mark(0, L.stream);
   // each token's global log-sum-exp from every shard's partials
@@ -1378,7 +1386,9 @@ cudaError_t launch_flce_shard_bwd(const FlceBwdMaps& m, const int64_t* target, c
   q.v0 = v0;
   q.v_total = v_total;
   q.lse = bw.lse;
-  q.gscale = grad_scale / static_cast<float>(g.T);
+  // the mean's weight 1/T on every row, or the caller's per-row weights (e.g. CPO's d loss / d l_i)
+  q.gscale = row_w ? grad_scale : grad_scale / static_cast<float>(g.T);
+  q.row_w = row_w;
   q.dz = bw.dz;
   q.ld_dz = bw.ld_dz;
   if ((e = launch_gemm<kModeDZ>(m.x, m.w, m.x, m.w, q, L)) != cudaSuccess) return e;

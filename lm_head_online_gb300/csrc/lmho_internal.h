@@ -239,10 +239,12 @@ FlceBwdWs flce_bwd_ws_carve(void* ws, int64_t T, int64_t H, int64_t V);
 // partials [shards][3][T] (into bw.lse), the shard's dZ columns (targets global; v_total = the global vocabulary
 // size), this shard's share of dx (the ranks' shares sum to dx) and its own
 // rows of dW.
+// Row weights: null = the mean's grad_scale / T on every row, else
+// grad_scale * row_w[i] (e.g. CPO's d loss / d l_i).
 cudaError_t launch_flce_shard_bwd(const FlceBwdMaps& m, const int64_t* target, const float* partials,
                                   int64_t shards, int64_t v0, int64_t v_total, const FusedGeometry& g,
-                                  float grad_scale, float* dx, float* dW, const FusedWs& ws, const FlceBwdWs& bw,
-                                  const FusedLaunch& L);
+                                  float grad_scale, const float* row_w, float* dx, float* dW, const FusedWs& ws,
+                                  const FlceBwdWs& bw, const FusedLaunch& L);
 // CPO on the fused linear + CE: pairs of sequences (chosen b, rejected b + B/2)
 // of S tokens.  Workspace pieces beyond the fused CE's.
 struct CpoArgs {
@@ -254,6 +256,11 @@ struct CpoArgs {
   float* logps;   // [B]   caller copy of lp, or null
   float* row_w;   // [T]   backward: d loss / d l_i, or null
 };
+// The CPO combination of given per-token CE losses rows [B * S]: loss, the
+// sequence log-likelihoods (logps, may be null) and, with row_w set, each
+// token's weight d loss / d l_i; lp [B], sig [B / 2] scratch, ctrl->ticket 0.
+cudaError_t launch_cpo_combine(const float* rows, int64_t B, int64_t S, float beta, float alpha, float* loss,
+                               float* logps, float* row_w, float* lp, float* sig, Ctrl* ctrl, cudaStream_t st);
 cudaError_t launch_flce_cpo(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const int64_t* target,
                             const FusedGeometry& g, float* loss, const FusedWs& ws, const CpoArgs& c,
                             const FusedLaunch& L);

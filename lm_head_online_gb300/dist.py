@@ -182,3 +182,29 @@ def vocab_parallel_ce_f32(logits_local, target, vocab_start: int, V: int, group=
     allp = gather_partials(part, group)                                    # [world, 3, T]
     rows = ce_merge_partials(allp.view(allp.shape[0], 3, T, 1), target.view(T, 1), V).view(T)
     return rows_mean(rows), rows
+
+
+def vocab_parallel_flce_cpo(x, W_local, target, vocab_start: int, V: int, B: int, beta=0.1, alpha=1.0, group=None,
+                            ws=None, backward=False, grad_scale=1.0):
+    """CPO on the fused linear + CE with W's rows sharded over the ranks of
+    `group`: x [B * S, H] bf16 (sequence b < B/2 chosen, b + B/2 its rejected
+    answer), target [B * S] global.  The per-token losses come from one
+    all-gather of the shards' partials, the CPO combination runs on every rank.
+    Returns (loss [1], logps [B]), and with backward=True also (dx [T, H],
+    summed over the ranks by one all-reduce, dW_local [V_local, H])."""
+    from lm_head_online_gb300 import (ce_merge_partials, cpo_combine_rows, flce_bwd_workspace_bytes,
+                                      flce_partials_bf16, flce_shard_bwd_bf16, workspace)
+
+    T, H = x.shape
+    if ws is None:
+        ws = workspace(flce_bwd_workspace_bytes(T, H, W_local.shape[0]), x.device)
+    part = flce_partials_bf16(x, W_local, target, vocab_start, ws=ws)     # [3, T]
+    allp = gather_partials(part, group)                                    # [world, 3, T]
+    rows = ce_merge_partials(allp.view(allp.shape[0], 3, T, 1), target.view(T, 1), V).view(T)
+    row_w = torch.empty_like(rows) if backward else None
+    loss, logps = cpo_combine_rows(rows, B, beta, alpha, row_w=row_w)
+    if not backward:
+        return loss, logps
+    dx, dW = flce_shard_bwd_bf16(x, W_local, target, allp, vocab_start, V, grad_scale, ws=ws, row_w=row_w)
+    dist.all_reduce(dx, op=dist.ReduceOp.SUM, group=group)
+    return loss, logps, dx, dW

@@ -236,6 +236,21 @@ def test_vocab_parallel_fused_argument_checks(lib):
                                    None) == 3                                  # short workspace
     assert lib.flce_shard_bwd_bf16(A, B, C, 0x60000000, 2, 4, 16, 10, 0, 20, g, 0x60000010, D + 4096, E, ws,
                                    None) == 2                                  # dx over the partials
+    # flce_shard_bwd_rows_bf16(..., vocab_start, V, row_w, grad_scale, dx, dW, ws, ws_bytes, stream)
+    assert lib.flce_shard_bwd_rows_bf16(A, B, C, 0x60000000, 2, 4, 16, 10, 0, 20, None, g, D, D + 4096, E, ws,
+                                        None) == 1                             # null weights
+    assert lib.flce_shard_bwd_rows_bf16(A, B, C, 0x60000000, 2, 4, 16, 10, 0, 20, D + 8, g, D, D + 4096, E, ws,
+                                        None) == 2                             # weights over dx
+    # cpo_combine_rows(rows, B, S, beta, alpha, loss, logps, row_w, ws, ws_bytes, stream)
+    cw = lib.cpo_combine_workspace_bytes(4)
+    assert cw >= 256 + 2 * 16 and lib.cpo_combine_workspace_bytes(0) == 256
+    assert lib.cpo_combine_rows(None, 4, 8, f(0.1), f(1.0), C, None, None, E, cw, None) == 1
+    assert lib.cpo_combine_rows(A, 3, 8, f(0.1), f(1.0), C, None, None, E, cw, None) == 1     # odd batch
+    assert lib.cpo_combine_rows(A, 4, 8, f(0.0), f(1.0), C, None, None, E, cw, None) == 1     # beta
+    assert lib.cpo_combine_rows(A, 4, 8, f(0.1), f(-1.0), C, None, None, E, cw, None) == 1    # alpha
+    assert lib.cpo_combine_rows(A, 4, 1 << 62, f(0.1), f(1.0), C, None, None, E, cw, None) == 1   # B * S too large
+    assert lib.cpo_combine_rows(A, 4, 8, f(0.1), f(1.0), C, None, None, E, 16, None) == 3     # short workspace
+    assert lib.cpo_combine_rows(A, 4, 8, f(0.1), f(1.0), C, None, A + 64, E, cw, None) == 2   # weights over rows
     # fljsd_lse_partials_bf16(xs, Ws, xt, Wt, T, H, V_local, temperature, lse_local, ws, ws_bytes, stream)
     assert lib.fljsd_lse_partials_bf16(A, B, C, D, 4, 16, 10, f(1.0), None, E, ws, None) == 1
     assert lib.fljsd_lse_partials_bf16(A, B, C, D, 4, 16, 10, f(0.0), E + (1 << 31), E, ws, None) == 1

@@ -280,6 +280,38 @@ def test_vocab_parallel_fused_guards(gpu_lib, T, H, V):
     unchanged(before, [x, xt, W, Wt, t, keep])
 
 
+def test_vocab_parallel_cpo_guards(gpu_lib):
+    """cpo_combine_rows and the weighted shard backward into guarded outputs."""
+    g = Guarded()
+    B, S, H, V = 4, 33, 200, 640
+    T = B * S
+    x = to_dev_bf16(gen.normal_bf16_bits(28, 0, (T, H)))
+    W = to_dev_bf16(gen.normal_bf16_bits(28, 2, (V, H), sigma=1.0 / math.sqrt(H)))
+    t = to_dev(gen.targets(28, 1, (T,), V))
+    rows = to_dev(np.abs(gen.normal_f32(28, 3, (T,))) + 1.0)
+    before = snapshot(x, W, t, rows)
+    loss = g.view(4, torch.float32, (1,))
+    logps = g.view(4 * B, torch.float32, (B,))
+    row_w = g.view(4 * T, torch.float32, (T,))
+    gpu_lib.cpo_combine_rows(rows, B, 0.2, 0.8, loss=loss, logps=logps, row_w=row_w,
+                             ws=g.ws(gpu_lib.cpo_combine_workspace_bytes(B)))
+    g.check()
+    written(loss, logps, row_w)
+    parts = torch.empty((2, 3, T), device="cuda")
+    shards = [(0, 300), (300, V - 300)]
+    for j, (v0, w) in enumerate(shards):
+        gpu_lib.flce_partials_bf16(x, W[v0:v0 + w], t, v0, partials=parts[j])
+    for v0, w in shards:
+        dx = g.view(4 * T * H, torch.float32, (T, H))
+        dW = g.view(4 * w * H, torch.float32, (w, H))
+        ws = g.ws(gpu_lib.flce_bwd_workspace_bytes(T, H, w))
+        gpu_lib.flce_shard_bwd_bf16(x, W[v0:v0 + w], t, parts, v0, V, 1.2, dx=dx, dW=dW, ws=ws, row_w=row_w)
+        g.check()
+        assert gpu_lib.ws_status(ws) == 0
+        written(dx, dW)
+    unchanged(before, [x, W, t, rows])
+
+
 def test_flat_f32_vocab_parallel_guards(gpu_lib):
     g = Guarded()
     T, V = 37, 1001

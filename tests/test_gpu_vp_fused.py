@@ -404,6 +404,70 @@ def test_fljsd_vp_backward_single_shard_bitwise(gpu_lib, masked):
     assert torch.equal(outs[0][0], ref_dx) and torch.equal(outs[0][1], ref_dW)
 
 
+# ---------------------------------------------------------------- CPO on the vocab-parallel fused CE
+def run_cpo_vp(lmho, xd, Wd, td, shards, V, B, beta, alpha, scale):
+    """Returns (loss, logps, row weights, [(dx share, dW rows)])."""
+    parts, rows, _ = run_flce_vp(lmho, xd, Wd, td, shards, V)
+    row_w = torch.full_like(rows, float("nan"))
+    loss, logps = lmho.cpo_combine_rows(rows, B, beta, alpha, row_w=row_w)
+    outs = [lmho.flce_shard_bwd_bf16(xd, Wd[v0:v0 + w].clone(), td, parts, v0, V, scale, row_w=row_w)
+            for v0, w in shards]
+    torch.cuda.synchronize()
+    return loss, logps, row_w, outs
+
+
+@pytest.mark.parametrize("B,S,H,V,k", [(4, 33, 128, 1000, 3), (2, 65, 256, 777, 2)])
+def test_cpo_vp_matches_oracle(gpu_lib, B, S, H, V, k):
+    """The CPO loss of the merged per-token losses against the oracle (2e-3),
+    its weights against the oracle's combination of the oracle's losses, and
+    every shard's weighted dx share and dW rows within their per-element
+    bounds; the shares' sum within the summed bounds of the oracle's dx."""
+    T = B * S
+    x, W, t = flce_inputs(90 + k, T, H, V)
+    shards = uneven_shards(V, k, 30 + k)
+    loss, logps, row_w, outs = run_cpo_vp(gpu_lib, to_dev_bf16(x), to_dev_bf16(W), to_dev(t), shards, V, B, 0.3,
+                                          0.7, 1.5)
+    want, rows_ref, want_lp = oracle.cpo_bf16(x.reshape(B, S, H), W, t.reshape(B, S), 0.3, 0.7)
+    assert float(loss.item()) == pytest.approx(want, rel=RTOL_SCALAR)
+    np.testing.assert_allclose(np64(logps), want_lp, rtol=1e-4)
+    _, _, w_ref = oracle.cpo_combine(rows_ref, 0.3, 0.7)
+    np.testing.assert_allclose(np64(row_w), w_ref.reshape(T), rtol=1e-3, atol=1e-7)
+    g = 1.5 * w_ref.reshape(T)
+    dz = oracle.ce_grad_f64(oracle.logits_bf16(x, W), t, g, 1.0)
+    S_err = ce_error_scale(dz, t, g)
+    xd = gen.bf16_bits_to_f32(x).astype(np.float64)
+    Wd = gen.bf16_bits_to_f32(W).astype(np.float64)
+    dx_sum, b_sum = np.zeros((T, H)), np.zeros((T, H))
+    for j, (v0, w) in enumerate(shards):
+        bdx, bdW = grad_bounds(dz[:, v0:v0 + w], S_err[:, v0:v0 + w], xd, Wd[v0:v0 + w])
+        # the weights themselves are fp32 values of the CPO combination: 1e-3 of each element's magnitude more
+        got_dx, got_dW = np64(outs[j][0]), np64(outs[j][1])
+        ref_dx, ref_dW = dz[:, v0:v0 + w] @ Wd[v0:v0 + w], dz[:, v0:v0 + w].T @ xd
+        assert_within_bounds(got_dx, ref_dx, bdx + 1e-3 * np.abs(dz[:, v0:v0 + w]) @ np.abs(Wd[v0:v0 + w]),
+                             f"dx share of shard {j}")
+        assert_within_bounds(got_dW, ref_dW, bdW + 1e-3 * np.abs(dz[:, v0:v0 + w]).T @ np.abs(xd),
+                             f"dW rows of shard {j}")
+        dx_sum += got_dx
+        b_sum += bdx + 1e-3 * np.abs(dz[:, v0:v0 + w]) @ np.abs(Wd[v0:v0 + w])
+    dx_full, _ = oracle.cpo_grad_bf16(x.reshape(B, S, H), W, t.reshape(B, S), 0.3, 0.7, 1.5)
+    assert_within_bounds(dx_sum, dx_full.reshape(T, H), b_sum, "sum of the dx shares")
+
+
+def test_cpo_vp_single_shard_is_bitwise_flce_cpo(gpu_lib):
+    """One shard holding all of W: the CPO loss, sequence log-likelihoods and
+    gradients equal flce_cpo_fwd_bwd_bf16's bit for bit."""
+    B, S, H, V = 4, 40, 256, 3000
+    T = B * S
+    x, W, t = flce_inputs(95, T, H, V)
+    xd, Wd, td = to_dev_bf16(x), to_dev_bf16(W), to_dev(t)
+    ws = gpu_lib.workspace(gpu_lib.flce_cpo_bwd_workspace_bytes(B, S, H, V))
+    ref_loss, ref_lp, ref_dx, ref_dW = gpu_lib.flce_cpo_fwd_bwd_bf16(xd.view(B, S, H), Wd, td.view(B, S), 0.2, 0.5,
+                                                                      1.3, ws=ws)
+    loss, logps, _, outs = run_cpo_vp(gpu_lib, xd, Wd, td, [(0, V)], V, B, 0.2, 0.5, 1.3)
+    assert torch.equal(loss, ref_loss) and torch.equal(logps, ref_lp)
+    assert torch.equal(outs[0][0], ref_dx.view(T, H)) and torch.equal(outs[0][1], ref_dW)
+
+
 # ---------------------------------------------------------------- merges alone
 def test_lse_merge_and_rows_mean(gpu_lib):
     rng = np.random.default_rng(3)
@@ -448,6 +512,13 @@ def _nccl_one_rank(port, q):
         wsb = lmho.workspace(lmho.flce_bwd_workspace_bytes(T, H, V))
         ref_l, ref_dx, ref_dW = lmho.flce_fwd_bwd_bf16(xd, Wd, td, 0.9, ws=wsb)
         ok_ce = ok_ce and torch.equal(m2, ref_l) and torch.equal(dx, ref_dx) and torch.equal(dW, ref_dW)
+        Bc, Sc = 4, T // 4
+        l4, lp4, dx4, dW4 = lmdist.vocab_parallel_flce_cpo(xd, Wd, td, 0, V, Bc, 0.2, 0.6, backward=True,
+                                                           grad_scale=1.1)
+        wsc = lmho.workspace(lmho.flce_cpo_bwd_workspace_bytes(Bc, Sc, H, V))
+        r4 = lmho.flce_cpo_fwd_bwd_bf16(xd.view(Bc, Sc, H), Wd, td.view(Bc, Sc), 0.2, 0.6, 1.1, ws=wsc)
+        ok_ce = ok_ce and torch.equal(l4, r4[0]) and torch.equal(lp4, r4[1]) and torch.equal(dx4, r4[2].view(T, H)) \
+            and torch.equal(dW4, r4[3])
         xs, Ws, xt, Wt = jsd_inputs(62, T, H, V, sw=0.2)
         d = [to_dev_bf16(a) for a in (xs, Ws, xt, Wt)]
         keep = to_dev((np.arange(T) % 5 != 3).astype(np.uint8))
