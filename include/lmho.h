@@ -14,7 +14,13 @@
  * Conventions shared by every entry point
  *   - Tensor pointers are DEVICE pointers, owned by the caller, contiguous and
  *     row-major.  bf16 tensors are passed as their 16-bit patterns
- *     (const uint16_t*), so this header needs no CUDA include.
+ *     (const uint16_t*), so this header needs no CUDA include.  Exception: the
+ *     CE row calls (ce_fwd_f32, ce_fwd_sbv_bf16, ce_partials_sbv_bf16,
+ *     ce_partials_f32) also take logits and targets in pinned (page-locked,
+ *     mapped) host memory: their kernels then read them over the host link
+ *     (one streaming read, at the link's rate; the results are the same bits
+ *     as from device memory).  Outputs and workspaces are always device
+ *     memory.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Calls only enqueue work on it: they never synchronise, never allocate and
  *     keep no state between calls.  They are thread-safe.  The exceptions are

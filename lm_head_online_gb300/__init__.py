@@ -187,13 +187,42 @@ def _dev(t: torch.Tensor, name: str, dtype, ndim=None):
     return t.data_ptr()
 
 
+def _host_or_dev(t: torch.Tensor, name: str, dtype, ndim=None):
+    """Pointer of a CUDA tensor or of a tensor in pinned host memory (which the
+    GPU reads directly over the host link: the CE row calls accept it for their
+    logits and targets)."""
+    if isinstance(t, torch.Tensor) and t.device.type == "cpu":
+        if not t.is_pinned():
+            raise TypeError(f"{name} must be a CUDA tensor or in pinned host memory")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        if ndim is not None and t.dim() != ndim:
+            raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        return t.data_ptr()
+    return _dev(t, name, dtype, ndim)
+
+
+def _cuda_device(*tensors):
+    """Where a call's outputs go: the device of its first CUDA tensor, else the
+    current CUDA device (all inputs in pinned host memory)."""
+    for t in tensors:
+        if t is not None and t.device.type == "cuda":
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
 def _on(*tensors):
-    """Context in which a call runs: the device of its tensors, which must all
-    be on one device (the kernels are launched on the current device, with the
-    current stream of that device)."""
-    dev = tensors[0].device
-    for t in tensors[1:]:
-        if t is not None and t.device != dev:
+    """Context in which a call runs: the device of its CUDA tensors, which must
+    all be on one device (the kernels are launched on the current device, with
+    the current stream of that device).  Pinned host tensors are skipped."""
+    cuda = [t for t in tensors if t is not None and t.device.type == "cuda"]
+    if not cuda:
+        raise ValueError("a call needs at least one CUDA tensor")
+    dev = cuda[0].device
+    for t in cuda[1:]:
+        if t.device != dev:
             raise ValueError(f"tensors on different devices: {dev} and {t.device}")
     return torch.cuda.device(dev)
 
@@ -221,18 +250,20 @@ def ce_fwd_f32(logits, target, loss=None, ws=None, stream=None):
     """Mean cross-entropy of fp32 logits [T, V] against int64 targets [T] -> fp32 [1].
 
     After the stream reaches this call's end, ``ws[:4*T]`` viewed as float32
-    holds the per-token losses.
+    holds the per-token losses.  logits and target may be CUDA tensors or in
+    pinned host memory (read directly over the host link).
     """
     lib = load()
-    pl = _dev(logits, "logits", torch.float32, 2)
+    pl = _host_or_dev(logits, "logits", torch.float32, 2)
     T, V = logits.shape
-    pt = _dev(target, "target", torch.int64, 1)
+    pt = _host_or_dev(target, "target", torch.int64, 1)
     if target.shape[0] != T:
         raise ValueError("target must have T entries")
+    dev = _cuda_device(loss, ws, logits, target)
     if loss is None:
-        loss = torch.empty(1, dtype=torch.float32, device=logits.device)
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
     if ws is None:
-        ws = workspace(lib.ce_workspace_bytes(T, V), logits.device)
+        ws = workspace(lib.ce_workspace_bytes(T, V), dev)
     with _on(logits, target, loss, ws):
         _check(lib.ce_fwd_f32(pl, pt, T, V, _dev(loss, "loss", torch.float32), _dev(ws, "ws", torch.uint8),
                               ws.numel(), _stream(stream)), "ce_fwd_f32")
@@ -259,15 +290,16 @@ def ce_fwd_f32_noalloc(logits, target, loss, stream=None):
 
 
 def ce_fwd_sbv_bf16(logits, target, loss=None, stream=None):
-    """Per-token cross-entropy of bf16 logits [S, B, V] -> fp32 [S, B]."""
+    """Per-token cross-entropy of bf16 logits [S, B, V] -> fp32 [S, B].
+    logits and target may be CUDA tensors or in pinned host memory."""
     lib = load()
-    pl = _dev(logits, "logits", torch.bfloat16, 3)
+    pl = _host_or_dev(logits, "logits", torch.bfloat16, 3)
     S, B, V = logits.shape
-    pt = _dev(target, "target", torch.int64, 2)
+    pt = _host_or_dev(target, "target", torch.int64, 2)
     if tuple(target.shape) != (S, B):
         raise ValueError("target must be [S, B]")
     if loss is None:
-        loss = torch.empty((S, B), dtype=torch.float32, device=logits.device)
+        loss = torch.empty((S, B), dtype=torch.float32, device=_cuda_device(logits, target))
     with _on(logits, target, loss):
         _check(lib.ce_fwd_sbv_bf16(pl, pt, S, B, V, _dev(loss, "loss", torch.float32), _stream(stream)),
                "ce_fwd_sbv_bf16")
@@ -280,15 +312,16 @@ def ce_partials_sbv_bf16(logits_local, target, vocab_start, partials=None, strea
     logits_local: bf16 [S, B, V_local], the global vocab columns
     [vocab_start, vocab_start + V_local); target: int64 [S, B] global indices.
     Returns fp32 [3, S, B]: the shard's max, sum of exp(z - max), and the
-    target logit (-inf where the target is not in this shard)."""
+    target logit (-inf where the target is not in this shard).  logits_local
+    and target may be CUDA tensors or in pinned host memory."""
     lib = load()
-    pl = _dev(logits_local, "logits_local", torch.bfloat16, 3)
+    pl = _host_or_dev(logits_local, "logits_local", torch.bfloat16, 3)
     S, B, Vl = logits_local.shape
-    pt = _dev(target, "target", torch.int64, 2)
+    pt = _host_or_dev(target, "target", torch.int64, 2)
     if tuple(target.shape) != (S, B):
         raise ValueError("target must be [S, B]")
     if partials is None:
-        partials = torch.empty((3, S, B), dtype=torch.float32, device=logits_local.device)
+        partials = torch.empty((3, S, B), dtype=torch.float32, device=_cuda_device(logits_local, target))
     if tuple(partials.shape) != (3, S, B):
         raise ValueError("partials must be [3, S, B]")
     with _on(logits_local, target, partials):
@@ -301,15 +334,16 @@ def ce_partials_f32(logits_local, target, vocab_start, partials=None, stream=Non
     """One vocabulary shard of the flat fp32 cross-entropy: logits_local fp32
     [T, V_local] = the global columns [vocab_start, vocab_start + V_local),
     target int64 [T] global.  Returns fp32 [3, T] (max, sum of exp, target
-    logit or -inf); merge with ce_merge_partials(p.view(k, 3, T, 1), ...)."""
+    logit or -inf); merge with ce_merge_partials(p.view(k, 3, T, 1), ...).
+    logits_local and target may be CUDA tensors or in pinned host memory."""
     lib = load()
-    pl = _dev(logits_local, "logits_local", torch.float32, 2)
+    pl = _host_or_dev(logits_local, "logits_local", torch.float32, 2)
     T, Vl = logits_local.shape
-    pt = _dev(target, "target", torch.int64, 1)
+    pt = _host_or_dev(target, "target", torch.int64, 1)
     if target.shape[0] != T:
         raise ValueError("target must be [T]")
     if partials is None:
-        partials = torch.empty((3, T), dtype=torch.float32, device=logits_local.device)
+        partials = torch.empty((3, T), dtype=torch.float32, device=_cuda_device(logits_local, target))
     if tuple(partials.shape) != (3, T):
         raise ValueError("partials must be [3, T]")
     with _on(logits_local, target, partials):

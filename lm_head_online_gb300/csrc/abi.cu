@@ -112,6 +112,19 @@ bool bulk_ok(const void* base, int64_t V, size_t elt) {
 
 }  // namespace
 
+namespace {
+// Memory the GPU owns (device or managed), as opposed to host memory mapped
+// into the address space (pinned, registered, or pageable through ATS).
+bool device_resident(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+}  // namespace
+
 CeConfig choose_ce(const void* base, int64_t rows, int64_t V, size_t elt, int num_sms) {
   CeConfig c{kCeCta, 256, 1};
   c.num_sms = num_sms;
@@ -126,8 +139,13 @@ CeConfig choose_ce(const void* base, int64_t rows, int64_t V, size_t elt, int nu
     case 5: c.variant = kCeCluster; c.cluster = 4; return c;
     case 6: c.variant = kCeCluster; c.cluster = 8; return c;
     case 7:
-      if (bulk_ok(base, V, elt)) c.variant = kCeBulk;   // else: CTA per row
-      return c;
+      // the ring copies rows with cp.async.bulk: device-resident logits only;
+      // otherwise (e.g. pinned host memory) the automatic choice below
+      if (bulk_ok(base, V, elt) && device_resident(base)) {
+        c.variant = kCeBulk;
+        return c;
+      }
+      break;
     default: break;
   }
   // Measured on GB300 (flat fp32 [16384, V], Megatron bf16 [2048, 4, V],
