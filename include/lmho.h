@@ -20,7 +20,8 @@
  *     mapped) host memory: their kernels then read them over the host link
  *     (one streaming read, at the link's rate; the results are the same bits
  *     as from device memory).  Outputs and workspaces are always device
- *     memory.
+ *     memory.  lmho_copy_h2d, the transfer utility, reads pinned host memory
+ *     too.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Calls only enqueue work on it: they never synchronise, never allocate and
  *     keep no state between calls.  They are thread-safe.  The exceptions are
@@ -553,6 +554,25 @@ void lmho_set_launch_events(void* const* events, int n);
  * over rows of that size can approach on this device.  One kernel launch. */
 int lmho_probe_read(const void* data, int64_t segments, int64_t segment_bytes, uint32_t* out,
                     void* stream);
+
+/* Host -> device copy by the SMs (a transfer utility of the library; no
+ * operation page defines it).  Copies `bytes` from src, pinned (page-locked)
+ * host memory with a device mapping (cudaHostAlloc, cudaMallocHost or
+ * cudaHostRegister memory, as PyTorch's pin_memory gives), to dst, device
+ * memory.  Both 16-byte aligned, bytes a multiple of 16, the two ranges
+ * disjoint; bytes == 0 does nothing.  One kernel on `stream`, half the SMs x
+ * 128 threads with 8 loads of 16 bytes in flight per thread; the copy engines
+ * are not used, and no launch event is recorded.
+ * Errors: LMHO_ERR_INVALID_ARG for a NULL pointer, a negative size or one not
+ * a multiple of 16, misalignment, a src that is not pinned host memory, or a
+ * dst that is not device (or managed) memory; LMHO_ERR_ALIAS if the ranges
+ * overlap.
+ * Why SM loads: on GB300 with a Grace host, copy-engine transfers from pinned
+ * memory were slowed, in bursts lasting a few hundred milliseconds, while the
+ * host served page faults caused by those transfers; SM loads fault only the
+ * first time a buffer is read and then held the host link's rate.  At this
+ * grid they run beside the library's tensor-core passes at ~205 GB/s. */
+int lmho_copy_h2d(void* dst, const void* src, int64_t bytes, void* stream);
 
 /* Upper bound, in nanoseconds, of every in-kernel wait of later calls
  * (default 2e9).  Process-wide. */

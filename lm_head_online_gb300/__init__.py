@@ -41,7 +41,7 @@ EXPORTS = (
     "flce_partials_bf16", "flce_shard_bwd_bf16", "flce_shard_bwd_rows_bf16", "cpo_combine_workspace_bytes",
     "cpo_combine_rows", "fljsd_lse_partials_bf16", "lse_merge_partials", "fljsd_terms_bf16", "fljsd_shard_bwd_bf16", "jsd_merge_terms",
     "rows_mean_f32",
-    "lmho_ws_status", "lmho_probe_read", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
+    "lmho_ws_status", "lmho_probe_read", "lmho_copy_h2d", "lmho_set_ce_variant", "lmho_set_raster_group", "lmho_set_launch_events", "lmho_set_wait_timeout_ns", "lmho_selftest_wait_timeout",
 )
 
 CE_VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "cta512": 3, "cluster2": 4, "cluster4": 5, "cluster8": 6, "bulk": 7}
@@ -141,6 +141,8 @@ def load():
         lib.rows_mean_f32.restype = ci
         lib.lmho_probe_read.argtypes = [vp, i64, i64, vp, vp]
         lib.lmho_probe_read.restype = ci
+        lib.lmho_copy_h2d.argtypes = [vp, vp, i64, vp]
+        lib.lmho_copy_h2d.restype = ci
         lib.lmho_ws_status.argtypes = [vp, sz, vp]
         lib.lmho_ws_status.restype = ci
         lib.lmho_set_ce_variant.argtypes = [ci]
@@ -922,6 +924,24 @@ def probe_read(data: torch.Tensor, segment_bytes: int, out=None, stream=None) ->
     _check(load().lmho_probe_read(data.data_ptr(), n, int(segment_bytes), _dev(out, "out", torch.int32, 1),
                                   _stream(stream)), "lmho_probe_read")
     return out
+
+
+def copy_h2d(dst: torch.Tensor, src: torch.Tensor, stream=None) -> torch.Tensor:
+    """Copy `src` (a contiguous tensor in pinned host memory) into `dst` (a
+    contiguous CUDA tensor of the same size in bytes) with the library's SM
+    copy kernel, on the current stream of dst's device; returns dst."""
+    if not isinstance(src, torch.Tensor) or src.device.type != "cpu" or not src.is_pinned():
+        raise TypeError("src must be a tensor in pinned host memory")
+    if not isinstance(dst, torch.Tensor) or dst.device.type != "cuda":
+        raise TypeError("dst must be a CUDA tensor")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("src and dst must be contiguous")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("src and dst must hold the same number of bytes")
+    with _on(dst):
+        _check(load().lmho_copy_h2d(dst.data_ptr(), src.data_ptr(), nbytes, _stream(stream)), "lmho_copy_h2d")
+    return dst
 
 
 def ws_status(ws, stream=None) -> int:

@@ -15,8 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "liblmho.so")
-SOURCES = ["abi.cu", "ce_rows.cu", "ce_grad.cu", "fused_linear.cu", "noalloc.cu", "vp_merge.cu"]
-HEADERS = ["ptx.cuh", "rowstats.cuh", "lmho_internal.h"]
+SOURCES = ["abi.cu", "ce_rows.cu", "ce_grad.cu", "fused_linear.cu", "noalloc.cu", "vp_merge.cu", "transfer.cu"]
+HEADERS = ["ptx.cuh", "rowstats.cuh", "lmho_internal.h", "transfer.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -15,6 +15,7 @@
 #include "../../include/lmho.h"
 #include "lmho_internal.h"
 #include "ptx.cuh"
+#include "transfer.h"
 
 namespace lmho {
 namespace {
@@ -1028,6 +1029,28 @@ int lmho_probe_read(const void* data, int64_t segments, int64_t segment_bytes, u
   int sms = 0;
   if (int d = current_device(&sms)) return d;
   return cuda_status(launch_probe_read(data, segments, segment_bytes, out, static_cast<cudaStream_t>(stream)));
+}
+
+int lmho_copy_h2d(void* dst, const void* src, int64_t bytes, void* stream) {
+  if (bytes < 0) return LMHO_ERR_INVALID_ARG;
+  if (bytes == 0) return LMHO_OK;
+  if (!dst || !src || bytes % 16 != 0 || !aligned16(dst) || !aligned16(src)) return LMHO_ERR_INVALID_ARG;
+  const Range in[1] = {rng(src, static_cast<size_t>(bytes))};
+  const Range out_r[1] = {rng(dst, static_cast<size_t>(bytes))};
+  if (int a = check_alias(in, 1, out_r, 1)) return a;
+  int sms = 0;
+  if (int d = current_device(&sms)) return d;
+  // src: pinned host memory with a device mapping; dst: memory the GPU owns
+  cudaPointerAttributes as{}, ad{};
+  if (cudaPointerGetAttributes(&as, src) != cudaSuccess || cudaPointerGetAttributes(&ad, dst) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return LMHO_ERR_INVALID_ARG;
+  }
+  if (as.type != cudaMemoryTypeHost || !as.devicePointer) return LMHO_ERR_INVALID_ARG;
+  if (ad.type != cudaMemoryTypeDevice && ad.type != cudaMemoryTypeManaged) return LMHO_ERR_INVALID_ARG;
+  if (!aligned16(as.devicePointer)) return LMHO_ERR_INVALID_ARG;
+  const int blocks = sms / 2 > 0 ? sms / 2 : 1;
+  return cuda_status(launch_copy_h2d(as.devicePointer, dst, bytes, blocks, static_cast<cudaStream_t>(stream)));
 }
 
 int lmho_ws_status(void* ws, size_t ws_bytes, void* stream) {

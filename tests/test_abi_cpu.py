@@ -304,3 +304,15 @@ def test_probe_read_argument_checks(lib):
     assert lib.lmho_probe_read(A, 4, 24, C, None) == 1            # segment not whole 16-byte vectors
     assert lib.lmho_probe_read(A + 8, 4, 64, C, None) == 1        # data not 16-byte aligned
     assert lib.lmho_probe_read(A, 4, 64, A + 16, None) == 2       # out inside data
+
+
+def test_copy_h2d_argument_checks(lib):
+    # lmho_copy_h2d(dst, src, bytes, stream)
+    assert lib.lmho_copy_h2d(A, B, 0, None) == 0                  # nothing to copy: no device touched
+    assert lib.lmho_copy_h2d(None, B, 64, None) == 1
+    assert lib.lmho_copy_h2d(A, None, 64, None) == 1
+    assert lib.lmho_copy_h2d(A, B, -16, None) == 1
+    assert lib.lmho_copy_h2d(A, B, 24, None) == 1                 # not whole 16-byte words
+    assert lib.lmho_copy_h2d(A + 8, B, 64, None) == 1             # dst not 16-byte aligned
+    assert lib.lmho_copy_h2d(A, B + 4, 64, None) == 1             # src not 16-byte aligned
+    assert lib.lmho_copy_h2d(A, A + 32, 64, None) == 2            # overlapping ranges
