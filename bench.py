@@ -555,14 +555,16 @@ def run_ours(args, rank, world, local_rank):
         del probe_h, probe_d
 
         # Each op's inputs are copied on a second stream, in the order below (most
-        # compute per copied byte first), and each op waits only for its own
-        # inputs, so copies of later inputs overlap earlier ops' kernels.  A step's
+        # compute per copied byte first; of the two CE calls, whose compute per
+        # byte is alike, the shorter last, since its kernel is the step's tail),
+        # and each op waits only for its own inputs, so copies of later inputs
+        # overlap earlier ops' kernels.  A step's
         # copies start after the previous step's kernels (buffers are reused).
         # The copies are lmho_copy_h2d (SM loads from the pinned buffers): on this
         # machine copy-engine transfers stalled in bursts on host page faults.
         copy_stream = torch.cuda.Stream(device=dev)
         order = (("js", ("js_xs", "js_ws", "js_xt", "js_wt")), ("fl", ("fl_x", "fl_w", "fl_t")),
-                 ("sbv", ("sbv_z", "sbv_t")), ("ce", ("ce_z", "ce_t")))
+                 ("ce", ("ce_z", "ce_t")), ("sbv", ("sbv_z", "sbv_t")))
         assert sorted(k for _, ks in order for k in ks) == sorted(h)
         landed = {op: torch.cuda.Event() for op, _ in order}
 
