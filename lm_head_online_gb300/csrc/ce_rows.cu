@@ -32,11 +32,16 @@
 // two-warp blocks: 53 us with the in-kernel ticket, 46 us this way).
 #include <cmath>
 #include <cstdint>
+#include <utility>
 
 #include "lmho_internal.h"
 #include "ptx.cuh"
 #include "rowstats.cuh"
 
+// Row kernels launched as programmatic dependents (1, the default) or plainly (0).
+#ifndef LMHO_CE_PDL
+#define LMHO_CE_PDL 1
+#endif
 #ifndef LMHO_CE_F32_FOLD
 #define LMHO_CE_F32_FOLD 4   // fp32 vectors per fold of the warp-per-row kernel
 #endif
@@ -153,6 +158,9 @@ __global__ void __launch_bounds__(64, MINB) ce_warp_rows(const T* __restrict__ l
                                                     const int64_t* __restrict__ target, int64_t rows,
                                                     int64_t V, Sink sink) {
   griddep_launch_dependents();
+#if LMHO_CE_PDL
+  griddep_wait();  // a programmatic launch: the preceding grid's writes are visible from here
+#endif
   const int lane = threadIdx.x & 31;
   const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r < rows) {
@@ -169,6 +177,9 @@ __global__ void __launch_bounds__(NT) ce_cta_rows(const T* __restrict__ logits,
                                                   const int64_t* __restrict__ target, int64_t rows,
                                                   int64_t V, Sink sink) {
   griddep_launch_dependents();
+#if LMHO_CE_PDL
+  griddep_wait();  // a programmatic launch: the preceding grid's writes are visible from here
+#endif
   __shared__ MS s_part[NT / 32];
   const int64_t r = blockIdx.x;
   const T* row = logits + r * V;
@@ -189,6 +200,9 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT)
     ce_cluster_rows(const T* __restrict__ logits, const int64_t* __restrict__ target, int64_t rows,
                     int64_t V, Sink sink) {
   griddep_launch_dependents();
+#if LMHO_CE_PDL
+  griddep_wait();  // a programmatic launch: the preceding grid's writes are visible from here
+#endif
   __shared__ MS s_part[NT / 32];
   __shared__ float s_ms[2];
   const uint32_t rank = cluster_ctarank();
@@ -230,6 +244,9 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
                  Sink sink, Ctrl* ctrl, int stages, int nwa,
                  uint32_t stage_bytes, uint64_t timeout_ns) {
   griddep_launch_dependents();
+#if LMHO_CE_PDL
+  griddep_wait();  // a programmatic launch: the preceding grid's writes are visible from here
+#endif
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(stages) * stage_bytes);
@@ -340,11 +357,36 @@ __global__ void __launch_bounds__(256) ce_merge_rows(const float* __restrict__ p
   }
 }
 
+// Row kernels may be launched as programmatic dependents of the kernel before
+// them in the stream: their blocks are scheduled while that grid drains and
+// wait (griddep_wait, their first statement after allowing their own
+// dependents) until it has completed.
+template <class... P, class... A>
+cudaError_t launch_row_kernel(void (*kernel)(P...), unsigned grid, unsigned block, cudaStream_t st, A&&... args) {
+#if LMHO_CE_PDL
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(block);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, std::forward<A>(args)...);
+#else
+  kernel<<<grid, block, 0, st>>>(std::forward<A>(args)...);
+  return cudaSuccess;
+#endif
+}
+
 template <typename T, class Sink>
 cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, int64_t V, Sink sink,
                         const float* rows_for_mean, float* mean_out, Ctrl* ctrl, const CeConfig& cfg,
                         cudaStream_t st) {
   launch_mark(0, st);
+  cudaError_t le = cudaSuccess;
   switch (cfg.variant) {
     case kCeWarp: {
       // 16 loads per lane in flight: a 16 KB row takes one or two memory round
@@ -365,22 +407,26 @@ cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, in
       const bool aligned = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && (V * sizeof(T)) % 16 == 0;
       if constexpr (sizeof(T) == 2) {
         if (aligned)
-          ce_warp_rows<T, 16, 16, 1, true><<<nb, 64, 0, st>>>(logits, target, rows, V, sink);
+          le = launch_row_kernel(ce_warp_rows<T, 16, 16, 1, true, Sink>, nb, 64, st, logits, target, rows, V, sink);
         else
-          ce_warp_rows<T, 16, 16, 1, false><<<nb, 64, 0, st>>>(logits, target, rows, V, sink);
+          le = launch_row_kernel(ce_warp_rows<T, 16, 16, 1, false, Sink>, nb, 64, st, logits, target, rows, V, sink);
       } else {
         if (aligned)
-          ce_warp_rows<T, 16, LMHO_CE_F32_FOLD, 16, true><<<nb, 64, 0, st>>>(logits, target, rows, V, sink);
+          le = launch_row_kernel(ce_warp_rows<T, 16, LMHO_CE_F32_FOLD, 16, true, Sink>, nb, 64, st, logits, target, rows,
+                            V, sink);
         else
-          ce_warp_rows<T, 16, LMHO_CE_F32_FOLD, 16, false><<<nb, 64, 0, st>>>(logits, target, rows, V, sink);
+          le = launch_row_kernel(ce_warp_rows<T, 16, LMHO_CE_F32_FOLD, 16, false, Sink>, nb, 64, st, logits, target, rows,
+                            V, sink);
       }
       break;
     }
     case kCeCta:
       if (cfg.threads == 512)
-        ce_cta_rows<T, 4, 512><<<static_cast<unsigned>(rows), 512, 0, st>>>(logits, target, rows, V, sink);
+        le = launch_row_kernel(ce_cta_rows<T, 4, 512, Sink>, static_cast<unsigned>(rows), 512, st, logits, target, rows, V,
+                          sink);
       else
-        ce_cta_rows<T, 4, 256><<<static_cast<unsigned>(rows), 256, 0, st>>>(logits, target, rows, V, sink);
+        le = launch_row_kernel(ce_cta_rows<T, 4, 256, Sink>, static_cast<unsigned>(rows), 256, st, logits, target, rows, V,
+                          sink);
       break;
     case kCeBulk: {
       const uint32_t row_bytes = static_cast<uint32_t>(V * sizeof(T));
@@ -418,6 +464,7 @@ cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, in
     default:
       return cudaErrorInvalidValue;
   }
+  if (le != cudaSuccess) return le;
   if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
   if (mean_out) {
     // The mean: one block behind the row kernel, allowed to launch before the
