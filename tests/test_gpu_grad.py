@@ -143,3 +143,42 @@ def test_fwd_bwd_argument_errors(gpu_lib):
     with pytest.raises(gpu_lib.LmhoError) as e:
         gpu_lib.ce_fwd_bwd_f32(z, t, grad_scale=float("inf"))
     assert e.value.status == gpu_lib.LMHO_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("T,V", [(301, 2048), (5, 512)])
+def test_flat_warp_rows_bad_targets_and_odd_rows(gpu_lib, T, V):
+    # aligned rows of at most 8 KB take the warp-per-row kernel: an odd row
+    # count leaves one warp of the last block idle; targets out of range on
+    # either side make their rows (loss and gradient) NaN and the mean NaN
+    z = gen.normal_f32(35, 0, (T, V))
+    t = gen.targets(35, 1, (T,), V)
+    t[0], t[T - 1] = -1, V
+    m, rows, dz = run_flat(gpu_lib, z, t, 0.75)
+    d = dz.cpu().numpy().astype(np.float64)
+    assert math.isnan(m) and np.isnan(rows[0]) and np.isnan(rows[T - 1])
+    assert np.all(np.isnan(d[0])) and np.all(np.isnan(d[T - 1]))
+    keep = np.arange(1, T - 1)
+    rows_ref = oracle.ce_f32(z[keep], t[keep])[1]
+    np.testing.assert_allclose(rows[keep], rows_ref, rtol=1e-5, atol=1e-6)
+    ref = oracle.ce_grad_f32(z[keep], t[keep], 0.75) * (len(keep) / T)
+    np.testing.assert_allclose(d[keep], ref, rtol=2e-5, atol=1e-7 * 0.75 / T)
+
+
+@pytest.mark.parametrize("S,B,V", [(3, 3, 4096), (5, 1, 8)])
+def test_sbv_warp_rows_bad_targets_and_odd_rows(gpu_lib, S, B, V):
+    zb = gen.normal_bf16_bits(36, 0, (S, B, V), sigma=2.0)
+    t = gen.targets(36, 1, (S, B), V)
+    dl = gen.normal_f32(36, 5, (S, B))
+    t[0, 0], t[S - 1, B - 1] = -7, V + 3
+    loss, dz = gpu_lib.ce_fwd_bwd_sbv_bf16(to_dev_bf16(zb), to_dev(t), to_dev(dl), 0.5)
+    torch.cuda.synchronize()
+    lo = loss.cpu().numpy().reshape(-1)
+    d = bf16_to_f64(dz).reshape(S * B, V)
+    assert np.isnan(lo[0]) and np.isnan(lo[-1]) and np.all(np.isnan(d[0])) and np.all(np.isnan(d[-1]))
+    keep = np.arange(1, S * B - 1)
+    zr = zb.reshape(S * B, 1, V)[keep]
+    tr = t.reshape(-1, 1)[keep]
+    np.testing.assert_allclose(lo[keep], oracle.ce_sbv_bf16(zr, tr).reshape(-1), rtol=0, atol=2e-3)
+    ref = oracle.ce_grad_sbv_bf16(zr, tr, dl.reshape(-1, 1)[keep].astype(np.float64), 0.5).reshape(len(keep), V)
+    gmax = 0.5 * float(np.abs(dl).max())
+    np.testing.assert_allclose(d[keep], ref, rtol=4.5e-3, atol=1e-7 * gmax)
