@@ -18,8 +18,9 @@
 //     log-sum-exp);
 //   * each CTA then writes its slice of the gradient, 16-byte stores where the
 //     gradient row has the logits' alignment, scalar stores otherwise.
-// Aligned rows of at most 8 KB take a warp per row instead (ce_fb_warp_rows):
-// the row stays in registers between the fold and the gradient write.
+// Aligned rows of at most 16 KB take one or two warps per row instead
+// (ce_fb_warp_rows): the row stays in registers between the fold and the
+// gradient write.
 // When the slice's start and length are multiples of 16 bytes, one thread
 // stages it with a single cp.async.bulk (1-D TMA) completing on an mbarrier,
 // so the whole slice is in flight at once; otherwise the threads load it
@@ -40,7 +41,7 @@ namespace {
 
 constexpr int64_t kSliceMaxBytes = 192 * 1024;   // largest slice a CTA can stage (shared memory)
 #ifndef LMHO_FB_WARP
-#define LMHO_FB_WARP 1   // warp per row for aligned rows up to 8 KB
+#define LMHO_FB_WARP 1   // one or two warps per row for aligned rows up to 16 KB
 #endif
 
 template <typename T> struct Out;
@@ -227,46 +228,65 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(NT)
   if (mean_out && rank == 0) mean_tail(out_rows, rows, mean_out, ctrl, gridDim.x / C);
 }
 
-// Rows of at most 32 U 16-byte vectors (8 KB for U = 16), 16-byte aligned and whole vectors
-// (logits and gradient): a warp per row holds the whole row in registers (U
-// vectors per lane, lane-interleaved like the forward warp kernel), folds
-// (max, sum exp), merges them across the warp, and writes the gradient from
-// the same registers; lane 0 then patches the target element (after a warp
+// Rows of at most W x 32 x U 16-byte vectors, 16-byte aligned and whole
+// vectors (logits and gradient): W warps per row (W = 1: two rows per 64-thread
+// block; W = 2: one) hold the row in registers, U vectors per lane
+// lane-interleaved as in the forward warp kernel, fold (max, sum exp), merge
+// across the warp and then, for W = 2, through shared memory in warp order, so
+// both warps hold the same log-sum-exp.  The gradient is written from the same
+// registers; thread 0 of the row then patches the target element (after a
 // barrier, so it lands after the vector store covering it) and writes the
 // row's loss.  One read of the logits and one write of the gradient, with no
-// shared-memory staging or block barrier per row.
-template <typename T, int U, int G>
+// shared-memory staging of the row.  The flat mean is a one-block kernel
+// launched behind this one as a programmatic dependent.
+template <typename T, int U, int G, int W>
 __global__ void __launch_bounds__(64) ce_fb_warp_rows(const T* __restrict__ logits, const int64_t* __restrict__ target,
                                                      int64_t rows, int64_t V, const float* __restrict__ dloss,
                                                      float gscale, float* __restrict__ out_rows,
-                                                     T* __restrict__ dlogits, float* mean_out, Ctrl* ctrl) {
+                                                     T* __restrict__ dlogits) {
+  static_assert(W == 1 || W == 2, "one or two warps per row");
   constexpr int E = Elt<T>::kPerVec;
-  const int lane = threadIdx.x & 31;
-  const int64_t r = static_cast<int64_t>(blockIdx.x) * 2 + (threadIdx.x >> 5);
-  if (r < rows) {
-    const T* row = logits + r * V;
-    const int64_t t = __ldg(target + r);
-    const int64_t nvec = V / E;
-    const uint4* vec = reinterpret_cast<const uint4*>(row);
-    uint4 rv[U];
+  __shared__ float s_ms[2][2];
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t r = W == 1 ? static_cast<int64_t>(blockIdx.x) * 2 + w : static_cast<int64_t>(blockIdx.x);
+  const int64_t q_lo = W == 1 ? 0 : static_cast<int64_t>(w) * 32 * U;   // this warp's first vector
+  const bool live = r < rows;
+  const T* row = logits + (live ? r : 0) * V;
+  const int64_t nvec = V / E;
+  const uint4* vec = reinterpret_cast<const uint4*>(row);
+  uint4 rv[U];
+  MS a = ms_empty();
+  int64_t t = 0;
+  if (live) {
+    t = __ldg(target + r);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t q = u * 32 + lane;
+      const int64_t q = q_lo + u * 32 + lane;
       rv[u] = q < nvec ? ldg_stream_v4(vec + q) : neg_inf_vec<T>();
     }
-    MS a = ms_empty();
 #pragma unroll
     for (int gi = 0; gi < U; gi += G) ms_fold_vecs<T, G>(a, rv + gi);
     a = ms_warp_allreduce(a);
-    const float lse = a.m + logf(a.s);
-    const bool bad = t < 0 || t >= V;
-    const float g = gscale * (dloss ? __ldg(dloss + r) : 1.f);
-    const float nl = -lse * kLog2e;
-    const float nan = __int_as_float(0x7FC00000);
+  }
+  if constexpr (W == 2) {
+    if (lane == 0) {
+      s_ms[w][0] = a.m;
+      s_ms[w][1] = a.s;
+    }
+    __syncthreads();
+    a = ms_merge(MS{s_ms[0][0], s_ms[0][1]}, MS{s_ms[1][0], s_ms[1][1]});
+  }
+  const float lse = a.m + logf(a.s);
+  const bool bad = t < 0 || t >= V;
+  const float g = live ? gscale * (dloss ? __ldg(dloss + r) : 1.f) : 0.f;
+  const float nl = -lse * kLog2e;
+  const float nan = __int_as_float(0x7FC00000);
+  if (live) {
     uint4* dv = reinterpret_cast<uint4*>(dlogits + r * V);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t q = u * 32 + lane;
+      const int64_t q = q_lo + u * 32 + lane;
       if (q < nvec) {
         float v[E];
         Elt<T>::unpack(rv[u], v);
@@ -275,23 +295,43 @@ __global__ void __launch_bounds__(64) ce_fb_warp_rows(const T* __restrict__ logi
         dv[q] = Out<T>::pack(v);
       }
     }
-    __syncwarp();
-    if (lane == 0) {
-      const float zt = bad ? nan : Elt<T>::load1(row + t);
-      if (!bad) Out<T>::store1(dlogits + r * V + t, g * (ex2_approx(fmaf(zt, kLog2e, nl)) - 1.f));
-      out_rows[r] = lse - zt;
-    }
   }
-  if (mean_out) mean_tail(out_rows, rows, mean_out, ctrl, gridDim.x);
+  if constexpr (W == 2)
+    __syncthreads();
+  else
+    __syncwarp();
+  if (live && lane == 0 && (W == 1 || w == 0)) {
+    const float zt = bad ? nan : Elt<T>::load1(row + t);
+    if (!bad) Out<T>::store1(dlogits + r * V + t, g * (ex2_approx(fmaf(zt, kLog2e, nl)) - 1.f));
+    out_rows[r] = lse - zt;
+  }
 }
 
-template <typename T, int U, int G>
+// Mean of the row losses behind ce_fb_warp_rows (a programmatic dependent:
+// griddep_wait returns once that grid has completed and its writes are visible).
+__global__ void __launch_bounds__(256) fb_mean_rows(const float* __restrict__ out_rows, int64_t rows, float* loss) {
+  griddep_wait();
+  mean_sum(out_rows, rows, loss);
+}
+
+template <typename T, int U, int G, int W>
 cudaError_t launch_fb_warp(const T* logits, const int64_t* target, int64_t rows, int64_t V, const float* dloss,
-                           float gscale, float* out_rows, T* dlogits, float* mean_out, Ctrl* ctrl, cudaStream_t st) {
-  ce_fb_warp_rows<T, U, G><<<static_cast<unsigned>((rows + 1) / 2), 64, 0, st>>>(logits, target, rows, V, dloss,
-                                                                                  gscale, out_rows, dlogits, mean_out,
-                                                                                  ctrl);
-  return cudaGetLastError();
+                           float gscale, float* out_rows, T* dlogits, float* mean_out, cudaStream_t st) {
+  const unsigned blocks = static_cast<unsigned>(W == 1 ? (rows + 1) / 2 : rows);
+  ce_fb_warp_rows<T, U, G, W><<<blocks, 64, 0, st>>>(logits, target, rows, V, dloss, gscale, out_rows, dlogits);
+  if (const cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+  if (!mean_out) return cudaSuccess;
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(1);
+  lc.blockDim = dim3(256);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, fb_mean_rows, static_cast<const float*>(out_rows), rows, mean_out);
 }
 
 template <typename T, int C, int NT, bool STAGED>
@@ -334,13 +374,15 @@ cudaError_t launch_fb_rows(const T* logits, const int64_t* target, int64_t rows,
   constexpr int G = sizeof(T) == 2 ? 16 : 4;   // vectors per fold, as in the forward warp kernel
   const bool rows_aligned = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 &&
                             (reinterpret_cast<uintptr_t>(dlogits) & 15u) == 0 && row_bytes % 16 == 0;
-  // Rows up to 8 KB only, 16 vectors per lane.  Measured on GB300 (flushed calls):
-  // bf16 [2048 x 4, V] 30.6 -> 20.5 us at V = 2048 and 34.8 -> 24.6 us at 4096,
-  // fp32 [16384, 2048] 77.4 -> 57.3 us; a 32-vector instance for fp32 16 KB rows
-  // (164 registers, 12 resident warps per SM) took 110.6-112.4 us against the
-  // staged CTA kernel's 102.4, and for bf16 it spills.
+  // Rows up to 8 KB: one warp per row; up to 16 KB: two.  Measured on GB300
+  // (flushed calls, against the staged CTA kernel): bf16 [2048 x 4, V] 35.1 ->
+  // 23.7-24.0 us at V = 4096 and 49.5 -> 43.0 us at 8192; fp32 [16384, V]
+  // 78.1-78.5 -> 45.8-46.2 us at V = 2048 and 104.2 -> 83.5 us at 4096.  One
+  // warp holding a whole 16 KB row (32 vectors per lane) spills or runs slower.
   if (LMHO_FB_WARP && rows_aligned && row_bytes <= 32 * 16 * 16)
-    e = launch_fb_warp<T, 16, G>(logits, target, rows, V, dloss, gscale, out_rows, dlogits, mean_out, ctrl, st);
+    e = launch_fb_warp<T, 16, G, 1>(logits, target, rows, V, dloss, gscale, out_rows, dlogits, mean_out, st);
+  else if (LMHO_FB_WARP && rows_aligned && row_bytes <= 2 * 32 * 16 * 16)
+    e = launch_fb_warp<T, 16, G, 2>(logits, target, rows, V, dloss, gscale, out_rows, dlogits, mean_out, st);
   else if (row_bytes <= 16 * 1024)
     e = launch_fb<T, 1, 128, true>(logits, target, rows, V, slice_for(1), dloss, gscale, out_rows, dlogits, mean_out,
                                    ctrl, tmo, st);

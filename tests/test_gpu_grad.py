@@ -145,10 +145,11 @@ def test_fwd_bwd_argument_errors(gpu_lib):
     assert e.value.status == gpu_lib.LMHO_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("T,V", [(301, 2048), (5, 512)])
+@pytest.mark.parametrize("T,V", [(301, 2048), (5, 512), (7, 4096), (3, 2052)])
 def test_flat_warp_rows_bad_targets_and_odd_rows(gpu_lib, T, V):
-    # aligned rows of at most 8 KB take the warp-per-row kernel: an odd row
-    # count leaves one warp of the last block idle; targets out of range on
+    # aligned rows of at most 16 KB take the warp-per-row kernel (two warps per
+    # row above 8 KB): an odd row count leaves one warp of the last block idle
+    # (one warp per row); targets out of range on
     # either side make their rows (loss and gradient) NaN and the mean NaN
     z = gen.normal_f32(35, 0, (T, V))
     t = gen.targets(35, 1, (T,), V)
@@ -164,7 +165,7 @@ def test_flat_warp_rows_bad_targets_and_odd_rows(gpu_lib, T, V):
     np.testing.assert_allclose(d[keep], ref, rtol=2e-5, atol=1e-7 * 0.75 / T)
 
 
-@pytest.mark.parametrize("S,B,V", [(3, 3, 4096), (5, 1, 8)])
+@pytest.mark.parametrize("S,B,V", [(3, 3, 4096), (5, 1, 8), (3, 3, 8192), (1, 3, 4104)])
 def test_sbv_warp_rows_bad_targets_and_odd_rows(gpu_lib, S, B, V):
     zb = gen.normal_bf16_bits(36, 0, (S, B, V), sigma=2.0)
     t = gen.targets(36, 1, (S, B), V)
