@@ -30,13 +30,13 @@
  *     a change made by one thread applies to later calls of every thread.
  *     They choose kernels and limits, never results beyond rounding.  The
  *     measurement hook lmho_set_launch_events is per host thread.
- *   - Programmatic dependent launch: the cross-entropy row kernels (and the
- *     forward + backward row kernels) are launched as programmatic dependents
- *     of the kernel before them on the stream and wait for that kernel's
- *     completion before touching memory, so they are correct after any
- *     producer.  They also let the next kernel on the stream launch early: a
- *     caller's kernel launched with programmatic stream serialization must
- *     wait (griddepcontrol.wait) before it reads a call's outputs, as that
+ *   - Programmatic dependent launch: the cross-entropy forward row kernels
+ *     are launched as programmatic dependents of the kernel before them on
+ *     the stream and wait for that kernel's completion before touching
+ *     memory, so they are correct after any producer.  They, and the short-row
+ *     forward + backward kernel, also let the next kernel on the stream launch
+ *     early: a caller's kernel launched with programmatic stream serialization
+ *     must wait (griddepcontrol.wait) before it reads a call's outputs, as that
  *     launch mode requires of any dependent.
  *   - "No mutation or aliasing" (every page, section Semantics): inputs are
  *     never written, and an output or workspace byte range that overlaps an
