@@ -494,6 +494,12 @@ cudaError_t launch_rows(const T* logits, const int64_t* target, int64_t rows, in
 // read-once floor a cross-entropy call over rows of that size can approach.
 __global__ void __launch_bounds__(64, 16) probe_read_rows(const uint4* __restrict__ data, int64_t nseg,
                                                           int64_t seg_vec, uint32_t* __restrict__ out) {
+  // launched like the CE row kernels (programmatic dependent), so back-to-back
+  // probes compare with back-to-back calls
+  griddep_launch_dependents();
+#if LMHO_CE_PDL
+  griddep_wait();
+#endif
   const int lane = threadIdx.x & 31;
   const int64_t r = static_cast<int64_t>(blockIdx.x) * 2 + (threadIdx.x >> 5);
   if (r >= nseg) return;
@@ -542,7 +548,9 @@ cudaError_t launch_ce_partials_f32(const float* logits, const int64_t* target, i
 cudaError_t launch_probe_read(const void* data, int64_t nseg, int64_t seg_bytes, uint32_t* out, cudaStream_t st) {
   launch_mark(0, st);
   const unsigned nb = static_cast<unsigned>((nseg + 1) / 2);
-  probe_read_rows<<<nb, 64, 0, st>>>(static_cast<const uint4*>(data), nseg, seg_bytes / 16, out);
+  const cudaError_t e = launch_row_kernel(probe_read_rows, nb, 64, st, static_cast<const uint4*>(data), nseg,
+                                          seg_bytes / 16, out);
+  if (e != cudaSuccess) return e;
   launch_mark(1, st);
   return cudaGetLastError();
 }
