@@ -173,7 +173,7 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons, watts = [], 0.0, set(), []
+        sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             c = [x.strip() for x in ln.split(",")]
@@ -184,17 +184,12 @@ class ClockSampler:
                 mx = max(mx, float(c[1]))
             except ValueError:
                 continue
-            try:
-                watts.append(float(c[2]))
-            except ValueError:
-                pass
             for n, v in zip(names, c[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"], "samples": 0}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
-                "power_w": float(np.median(watts)) if watts else None}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ---------------------------------------------------------------- inputs

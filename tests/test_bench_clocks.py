@@ -1,6 +1,6 @@
 """Host-side parsing of the bench's clock samples (nvidia-smi CSV lines): the
-median SM clock under load, the highest maximum clock, every throttle reason
-seen active, and the median board power; unparsable lines are skipped."""
+median SM clock under load, the highest maximum clock and every throttle
+reason seen active; unparsable lines are skipped."""
 import os
 import sys
 
@@ -28,7 +28,6 @@ def test_reasons_clock_and_power():
     assert s["samples"] == 3
     assert s["sm_mhz"] == 1650.0 and s["sm_max_mhz"] == 2070.0
     assert s["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
-    assert s["power_w"] == 1398.5
 
 
 def test_no_samples():
