@@ -74,3 +74,21 @@ def test_copy_beside_a_fused_pass(gpu_lib):
     torch.cuda.synchronize()
     assert torch.equal(dst.cpu(), src)
     assert torch.equal(loss, ref)
+
+
+def test_copy_from_registered_host_memory(gpu_lib):
+    # host memory made page-locked with cudaHostRegister (not allocated by CUDA):
+    # the library reads it through the registration's device mapping
+    cudart = torch.cuda.cudart()
+    arr = np.frombuffer(gen.normal_f32(74, 0, (1 << 18,)).tobytes(), dtype=np.uint8).copy()
+    host = torch.from_numpy(arr)
+    assert int(cudart.cudaHostRegister(host.data_ptr(), host.numel(), 0)) == 0
+    try:
+        assert host.is_pinned()
+        dst = torch.zeros(host.numel(), dtype=torch.uint8, device="cuda")
+        gpu_lib.copy_h2d(dst, host)
+        torch.cuda.synchronize()
+        assert torch.equal(dst.cpu(), host)
+    finally:
+        torch.cuda.synchronize()
+        cudart.cudaHostUnregister(host.data_ptr())
