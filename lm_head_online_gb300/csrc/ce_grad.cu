@@ -389,6 +389,13 @@ cudaError_t launch_fb_rows(const T* logits, const int64_t* target, int64_t rows,
   else if (row_bytes <= single)
     e = launch_fb<T, 1, 256, true>(logits, target, rows, V, slice_for(1), dloss, gscale, out_rows, dlogits, mean_out,
                                    ctrl, tmo, st);
+  // fp32 rows over 96 KB and up to 128 KB: four CTAs of 24-32 KB slices.  At 128
+  // KB (V = 32768) they took 673-674 us against two 64 KB slices' 721-723 us
+  // (T = 16384) and 176 vs 190-191 us (T = 4096); bf16 rows of that size, and
+  // 256 KB rows of either type, were slower with the smaller slices.
+  else if (sizeof(T) == 4 && row_bytes > 96 * 1024 && row_bytes <= 128 * 1024 && cap == 64 * 1024)
+    e = launch_fb<T, 4, 256, true>(logits, target, rows, V, slice_for(4), dloss, gscale, out_rows, dlogits, mean_out,
+                                   ctrl, tmo, st);
   else if (slice_for(2) * static_cast<int64_t>(sizeof(T)) <= cap)
     e = launch_fb<T, 2, 256, true>(logits, target, rows, V, slice_for(2), dloss, gscale, out_rows, dlogits, mean_out,
                                    ctrl, tmo, st);

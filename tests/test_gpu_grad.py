@@ -33,7 +33,7 @@ def run_flat(lmho, z, t, scale, dlogits=None):
 
 
 FLAT = [(1, 1), (3, 5), (4, 8), (7, 4095), (33, 4097), (64, 4096), (300, 1000), (5, 16385), (3, 65537),
-        (2, 131071), (2, 200001), (9000, 1024)]
+        (2, 131071), (2, 200001), (9000, 1024), (3, 30000), (2, 32768), (2, 24577)]
 
 
 @pytest.mark.parametrize("T,V", FLAT)
